@@ -1,0 +1,178 @@
+/*
+ * w4a16.h -- C ABI of the B300 (sm_103a) W4A16 weight-only linear library.
+ *
+ * The library computes the fused dequantise-and-multiply linear layer of
+ * W4A16 weight-only quantisation: weights are stored as 4-bit codes with one
+ * FP16 scale and one 4-bit zero point per group of G input channels of each
+ * output column; activations stay BF16, accumulation is FP32 and the output
+ * is BF16.  The weights stay packed in device memory and are only expanded
+ * inside the kernels (klaylearn.com glossary "Weight-Only Quantisation", main
+ * body; zhuai.tech "Quantization Is Not a Zip File", section 8 "Engineering
+ * pitfalls": packed data stays packed until the kernel).
+ *
+ * ---------------------------------------------------------------------------
+ * Data layout (all row-major, all buffers owned by the caller):
+ *
+ *   W        FP16 [N, K]     weight in linear-layer orientation: row n is the
+ *                            K input channels of output column n.
+ *   x        BF16 [M, K]     activations, row pitch K.
+ *   y        BF16 [M, N]     output, y = x * W_hat^T, row pitch N.
+ *   qweight  uint32 [N, K/8] code of (n, k) in bits 4*(k%8) .. 4*(k%8)+3 of
+ *                            word qweight[n][k/8] (low nibble first).
+ *   scales   FP16 [N, ldS]   scales[n][g] = scale of group g = k / G;
+ *                            ldS = w4a16_scales_ld(K, G) (K/G rounded up to
+ *                            8 halves so each row starts on 16 bytes).
+ *   zeros    uint32 [N, ldZ] zero point of group g in bits 4*(g%8).. of word
+ *                            zeros[n][g/8]; ldZ = w4a16_zeros_ld(K, G).
+ *
+ *   W_hat[n][k] = (q[n][k] - z[n][k/G]) * s[n][k/G]        (exact in FP32)
+ *
+ * Reconstruction (q - zero_point) * scale is the asymmetric rule of instagit
+ * "Comparison of Quantization Methods: INT8 vs GPTQ vs AWQ vs GGUF", section
+ * "Practical Code Examples"; per-group scales of 32/64/128/256 weights follow
+ * zhuai.tech section 3 "The core idea: local structure, not global rounding".
+ *
+ * ---------------------------------------------------------------------------
+ * Conventions for every entry point:
+ *   - Pointers are DEVICE pointers unless stated; the caller owns them.  All
+ *     must be 16-byte aligned.  The library keeps no pointer after a call.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is
+ *     enqueued asynchronously; results are valid once the stream reaches the
+ *     point of the call.  Calls on distinct streams may run concurrently.
+ *   - Errors in arguments are reported before anything is launched, as a
+ *     status code; no entry point aborts, throws, traps or asserts.  A CUDA
+ *     launch error is reported as W4A16_ERR_CUDA.
+ *   - Preconditions: G in {32, 64, 128, 256}; K > 0 and K % G == 0;
+ *     N % 8 == 0; weights and activations finite; |x| < 65504.
+ *     M == 0 or N == 0 is an empty problem: W4A16_OK, nothing is launched.
+ */
+#ifndef W4A16_H
+#define W4A16_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+struct CUstream_st;
+typedef struct CUstream_st* w4a16_stream_t;
+
+typedef enum {
+    W4A16_OK = 0,
+    W4A16_ERR_INVALID_ARG = 1,   /* null pointer, bad size or shape mismatch */
+    W4A16_ERR_UNSUPPORTED = 2,   /* group size or shape outside what is built */
+    W4A16_ERR_MISALIGNED = 3,    /* a pointer is not 16-byte aligned */
+    W4A16_ERR_CUDA = 4,          /* the CUDA runtime reported an error */
+    W4A16_ERR_TIMEOUT = 5,       /* a kernel's bounded wait expired (see
+                                    w4a16_device_status) */
+    W4A16_ERR_NO_DEVICE = 6      /* no usable sm_103 device is current */
+} w4a16_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* w4a16_status_string(w4a16_status status);
+
+/* ---- layout helpers (elements per row; pure host functions) ------------- */
+
+/* uint32 words per qweight row: K / 8. */
+int64_t w4a16_qweight_ld(int64_t K);
+/* FP16 halves per scales row: K/G rounded up to a multiple of 8. */
+int64_t w4a16_scales_ld(int64_t K, int G);
+/* uint32 words per zeros row: ceil(K/G / 8) rounded up to a multiple of 4. */
+int64_t w4a16_zeros_ld(int64_t K, int G);
+
+/* ---- packer ------------------------------------------------------------------
+ * w4a16_pack: quantise FP16 W [N,K] to (qweight, scales, zeros), asymmetric
+ * min-max per group of G consecutive input channels of one output column:
+ *   lo = min(0, min w), hi = max(0, max w)            (range holds 0)
+ *   s  = RNE_fp16( fp32(hi - lo) / 15 )               (IEEE binary32 ops)
+ *   if s == 0: s = 1, z = 0                          (all-zero group)
+ *   z  = clamp(rne(-lo / s), 0, 15)
+ *   q  = clamp(rne(w / s) + z, 0, 15)
+ * Codes are taken against the stored FP16 scale.  The groupwise min-max
+ * scheme is the one the klaylearn glossary's main body describes (small
+ * integers plus scale and zero-point per group); the zero point and its
+ * reconstruction follow instagit's asymmetric example.
+ * Every element of qweight, scales and zeros is written, row padding as 0.
+ * Errors: W4A16_ERR_INVALID_ARG / _UNSUPPORTED / _MISALIGNED as above.
+ */
+w4a16_status w4a16_pack(const void* w_f16, int64_t N, int64_t K, int G,
+                        uint32_t* qweight, void* scales_f16, uint32_t* zeros,
+                        w4a16_stream_t stream);
+
+/* ---- dequantise (checking aid) -----------------------------------------------
+ * w4a16_dequant: w_out FP32 [N,K] = (q - z) * s, through the same in-register
+ * unpack routine the linear kernels use.  Exact in FP32.  Intended for tests
+ * and debugging; the linear entry points never call it and never expand
+ * weights in device memory.
+ */
+w4a16_status w4a16_dequant(const uint32_t* qweight, const void* scales_f16, const uint32_t* zeros,
+                           int64_t N, int64_t K, int G, float* w_out, w4a16_stream_t stream);
+
+/* ---- the layer ---------------------------------------------------------------
+ * w4a16_linear: y[M,N] (BF16) = x[M,K] (BF16) * W_hat^T, FP32 accumulation,
+ * one round-to-nearest-even to BF16 per output.  Dispatch: M <= 16 runs the
+ * bandwidth-bound decode GEMV (when x of M rows fits the kernel's shared
+ * memory), anything else runs the tcgen05 tensor-core GEMM.  Decode is
+ * weight-bandwidth bound and prefill compute bound (klaylearn glossary, FAQ
+ * "Why is it especially useful for decode?"; multigrid.ai, section "Where it
+ * stops being the right answer").
+ * x and y must not overlap the weight buffers.
+ */
+w4a16_status w4a16_linear(const void* x_bf16, const uint32_t* qweight, const void* scales_f16,
+                          const uint32_t* zeros, int64_t M, int64_t N, int64_t K, int G,
+                          void* y_bf16, w4a16_stream_t stream);
+
+/*
+ * w4a16_linear_dual: two projections of the same x (e.g. the gate and up
+ * projections of a gated FFN) in one launch that stages x once:
+ *   y_gate = x * W_hat_gate^T,  y_up = x * W_hat_up^T.
+ * Both weights share K, N and G.  Paired gate/up traversal is the zhuai.tech
+ * page's section 2 ("Moving fewer bytes can make decode faster") workload.
+ * M <= 16 runs the dual GEMV; larger M runs the GEMM once per projection.
+ */
+w4a16_status w4a16_linear_dual(const void* x_bf16,
+                               const uint32_t* qweight_gate, const void* scales_gate,
+                               const uint32_t* zeros_gate,
+                               const uint32_t* qweight_up, const void* scales_up,
+                               const uint32_t* zeros_up,
+                               int64_t M, int64_t N, int64_t K, int G,
+                               void* y_gate_bf16, void* y_up_bf16, w4a16_stream_t stream);
+
+/*
+ * Explicit-path variants of w4a16_linear, same arguments and result, for
+ * measuring both kernels on the same shape (e.g. the batch at which the
+ * decode kernel stops being bandwidth bound).
+ *   w4a16_linear_gemv: the decode kernel; W4A16_ERR_UNSUPPORTED if M > 16 or
+ *                      x does not fit the kernel's shared memory.
+ *   w4a16_linear_gemm: the tensor-core kernel, any M >= 1.
+ */
+w4a16_status w4a16_linear_gemv(const void* x_bf16, const uint32_t* qweight, const void* scales_f16,
+                               const uint32_t* zeros, int64_t M, int64_t N, int64_t K, int G,
+                               void* y_bf16, w4a16_stream_t stream);
+w4a16_status w4a16_linear_gemm(const void* x_bf16, const uint32_t* qweight, const void* scales_f16,
+                               const uint32_t* zeros, int64_t M, int64_t N, int64_t K, int G,
+                               void* y_bf16, w4a16_stream_t stream);
+
+/*
+ * Which kernel w4a16_linear would run for this shape: 1 = GEMV, 2 = GEMM,
+ * 0 = the shape is rejected.  Host-only, no device access.
+ */
+int w4a16_linear_path(int64_t M, int64_t N, int64_t K, int G);
+
+/*
+ * Every bounded wait inside the kernels (a tensor-core pipeline barrier that
+ * never completes) gives up after a fixed spin budget, records a code in a
+ * per-device status word and lets the kernel return.  This call synchronises
+ * the current device, returns W4A16_ERR_TIMEOUT if any kernel recorded a
+ * give-up since the last call (and clears the word), else W4A16_OK.  *detail
+ * (optional) receives the raw word.
+ */
+w4a16_status w4a16_device_status(uint32_t* detail);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_H */

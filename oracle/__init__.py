@@ -1,0 +1,198 @@
+"""CPU oracle for the W4A16 weight-only linear layer -- TEST INFRASTRUCTURE.
+
+Only `tests/`, `__graft_entry__.smoke()` and the `cpu_baseline` / reference
+leg of `bench.py` may import this package.  The product path (the CUDA
+library and its Python binding) never imports it and shares no code with it.
+
+This module is a thin ctypes wrapper around `w4a16_oracle.c` (plain C99,
+FP64 accumulation); every function's arithmetic lives in that file and is
+documented there with the page and section it follows.  Arrays are numpy:
+FP16 and BF16 values travel as their uint16 bit patterns.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        i64, i32, f32, f64 = ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_double
+        u16 = ctypes.c_uint16
+        p = ctypes.c_void_p
+        lib.oracle_f16_to_f32.argtypes, lib.oracle_f16_to_f32.restype = [u16], f32
+        lib.oracle_bf16_to_f32.argtypes, lib.oracle_bf16_to_f32.restype = [u16], f32
+        lib.oracle_f32_to_f16.argtypes, lib.oracle_f32_to_f16.restype = [f32], u16
+        lib.oracle_f32_to_bf16.argtypes, lib.oracle_f32_to_bf16.restype = [f32], u16
+        lib.oracle_f64_to_bf16.argtypes, lib.oracle_f64_to_bf16.restype = [f64], u16
+        lib.oracle_qweight_ld.argtypes, lib.oracle_qweight_ld.restype = [i64], i64
+        lib.oracle_scales_ld.argtypes, lib.oracle_scales_ld.restype = [i64, i64], i64
+        lib.oracle_zeros_ld.argtypes, lib.oracle_zeros_ld.restype = [i64, i64], i64
+        lib.oracle_quantize_group.argtypes = [p, i64, p, p, p]
+        lib.oracle_quantize_group.restype = None
+        lib.oracle_pack.argtypes = [p, i64, i64, i64, p, p, p, i32]
+        lib.oracle_pack.restype = i32
+        lib.oracle_dequant.argtypes = [p, p, p, i64, i64, i64, p, i32]
+        lib.oracle_dequant.restype = None
+        lib.oracle_linear.argtypes = [p, p, p, p, i64, i64, i64, i64, p, i32]
+        lib.oracle_linear.restype = None
+        lib.oracle_linear_sampled.argtypes = [p, p, p, p, i64, i64, p, p, i64, p, i32]
+        lib.oracle_linear_sampled.restype = None
+        lib.oracle_max_threads.argtypes, lib.oracle_max_threads.restype = [], i32
+        _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _u16(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.float16:
+        a = a.view(np.uint16)
+    assert a.dtype == np.uint16, f"expected FP16/BF16 bit patterns as uint16, got {a.dtype}"
+    return a
+
+
+# ---- scalar conversions (IEEE definitions) ---------------------------------
+
+def f16_to_f32(h: int) -> float:
+    return _load().oracle_f16_to_f32(int(h))
+
+
+def bf16_to_f32(b: int) -> float:
+    return _load().oracle_bf16_to_f32(int(b))
+
+
+def f32_to_f16(f: float) -> int:
+    return _load().oracle_f32_to_f16(float(np.float32(f)))
+
+
+def f32_to_bf16(f: float) -> int:
+    return _load().oracle_f32_to_bf16(float(np.float32(f)))
+
+
+def f64_to_bf16(d: float) -> int:
+    return _load().oracle_f64_to_bf16(float(d))
+
+
+def bf16_bits_to_f32_array(b: np.ndarray) -> np.ndarray:
+    """Exact widening of BF16 bit patterns (the top half of a binary32)."""
+    b = _u16(b)
+    return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+# ---- layout -----------------------------------------------------------------
+
+def qweight_ld(K: int) -> int:
+    return _load().oracle_qweight_ld(K)
+
+
+def scales_ld(K: int, G: int) -> int:
+    return _load().oracle_scales_ld(K, G)
+
+
+def zeros_ld(K: int, G: int) -> int:
+    return _load().oracle_zeros_ld(K, G)
+
+
+# ---- quantiser / packer -----------------------------------------------------
+
+def quantize_group(w: np.ndarray):
+    """One group: returns (scale_bits: int, zero: int, codes: uint8[G])."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    G = w.shape[0]
+    sb = np.zeros(1, np.uint16)
+    z = np.zeros(1, np.int32)
+    codes = np.zeros(G, np.uint8)
+    _load().oracle_quantize_group(_ptr(w), G, _ptr(sb), _ptr(z), _ptr(codes))
+    return int(sb[0]), int(z[0]), codes
+
+
+def pack(w_f16: np.ndarray, G: int, nthreads: int = 0):
+    """FP16 W [N,K] -> (qweight u32 [N,K/8], scales u16 [N,ldS], zeros u32 [N,ldZ])."""
+    w = _u16(w_f16)
+    N, K = w.shape
+    q = np.zeros((N, qweight_ld(K)), np.uint32)
+    s = np.zeros((N, scales_ld(K, G)), np.uint16)
+    z = np.zeros((N, zeros_ld(K, G)), np.uint32)
+    rc = _load().oracle_pack(_ptr(w), N, K, G, _ptr(q), _ptr(s), _ptr(z), nthreads)
+    if rc != 0:
+        raise ValueError(f"oracle_pack rejected N={N} K={K} G={G}")
+    return q, s, z
+
+
+# ---- unpack / dequant ---------------------------------------------------------
+
+def unpack_codes(q: np.ndarray, K: int) -> np.ndarray:
+    """Codes [N,K] (uint8), nibble k%8 of word k/8, low nibble first."""
+    q = np.ascontiguousarray(q, dtype=np.uint32)
+    N = q.shape[0]
+    out = np.zeros((N, K), np.uint8)
+    for j in range(8):
+        out[:, j::8] = ((q[:, : K // 8] >> np.uint32(4 * j)) & np.uint32(0xF)).astype(np.uint8)
+    return out
+
+
+def unpack_zeros(z: np.ndarray, K: int, G: int) -> np.ndarray:
+    """Zero points [N, K/G] (uint8)."""
+    z = np.ascontiguousarray(z, dtype=np.uint32)
+    ng = K // G
+    N = z.shape[0]
+    out = np.zeros((N, ng), np.uint8)
+    for g in range(ng):
+        out[:, g] = ((z[:, g // 8] >> np.uint32(4 * (g % 8))) & np.uint32(0xF)).astype(np.uint8)
+    return out
+
+
+def dequant(q, s, z, N: int, K: int, G: int, nthreads: int = 0) -> np.ndarray:
+    """W_hat [N,K] FP32, (q - z) * s per element."""
+    q = np.ascontiguousarray(q, dtype=np.uint32)
+    s = _u16(s)
+    z = np.ascontiguousarray(z, dtype=np.uint32)
+    out = np.zeros((N, K), np.float32)
+    _load().oracle_dequant(_ptr(q), _ptr(s), _ptr(z), N, K, G, _ptr(out), nthreads)
+    return out
+
+
+# ---- the layer ------------------------------------------------------------------
+
+def linear(x_bf16: np.ndarray, q, s, z, N: int, K: int, G: int, nthreads: int = 0) -> np.ndarray:
+    """y_ref [M,N] FP64 = x * W_hat^T, unrounded."""
+    x = _u16(x_bf16)
+    M = x.shape[0]
+    assert x.shape[1] == K
+    q = np.ascontiguousarray(q, dtype=np.uint32)
+    s = _u16(s)
+    z = np.ascontiguousarray(z, dtype=np.uint32)
+    y = np.zeros((M, N), np.float64)
+    _load().oracle_linear(_ptr(x), _ptr(q), _ptr(s), _ptr(z), M, N, K, G, _ptr(y), nthreads)
+    return y
+
+
+def linear_sampled(x_bf16: np.ndarray, q, s, z, K: int, G: int, ms, ns, nthreads: int = 0) -> np.ndarray:
+    """y_ref at the listed (m, n) positions only, FP64."""
+    x = _u16(x_bf16)
+    q = np.ascontiguousarray(q, dtype=np.uint32)
+    s = _u16(s)
+    z = np.ascontiguousarray(z, dtype=np.uint32)
+    ms = np.ascontiguousarray(ms, dtype=np.int64)
+    ns = np.ascontiguousarray(ns, dtype=np.int64)
+    assert ms.shape == ns.shape
+    y = np.zeros(ms.shape[0], np.float64)
+    _load().oracle_linear_sampled(_ptr(x), _ptr(q), _ptr(s), _ptr(z), K, G, _ptr(ms), _ptr(ns),
+                                  ms.shape[0], _ptr(y), nthreads)
+    return y
+
+
+def max_threads() -> int:
+    return _load().oracle_max_threads()

@@ -1,0 +1,338 @@
+/*
+ * w4a16_oracle.c -- plain, slow, obviously correct CPU oracle for the W4A16
+ * weight-only linear layer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or
+ * call this file: only the tests, the smoke check and the CPU-baseline leg of
+ * the benchmark use it.  It shares no code, header, table or constant with the
+ * CUDA library; both are written independently from the format description.
+ *
+ * What it computes, and where the pages say so:
+ *
+ *  - Weight-only quantisation keeps activations and accumulators in 16/32-bit
+ *    and stores only the weights in low precision, as small integers per group
+ *    plus a scale and a zero-point (klaylearn.com glossary "Weight-Only
+ *    Quantisation", first FAQ answer and main body; multigrid.ai "Weight-Only
+ *    Quantization Explained", section "What W4A16 actually names").
+ *  - Groups of 32/64/128/256 weights each get their own scale (zhuai.tech
+ *    "Quantization Is Not a Zip File", section 3 "The core idea: local
+ *    structure, not global rounding", paragraph "Block locality").
+ *  - Reconstruction of an asymmetric code is (q - zero_point) * scale
+ *    (instagit.com "Comparison of Quantization Methods: INT8 vs GPTQ vs AWQ vs
+ *    GGUF", section "Practical Code Examples", asymmetric example).
+ *  - The layer output is dequantise-then-multiply (klaylearn.com glossary,
+ *    main body: the kernel reconstructs 16-bit values of a tile and feeds a
+ *    fused dequantise-and-multiply path).
+ *
+ * Readings where the pages are silent (each is listed with its reason in the
+ * repository's design notes):
+ *  - Layout: W is [N,K] (output column n, input channel k), y = x * W_hat^T.
+ *    qweight[n][k/8] holds the code of k in bits 4*(k%8)..4*(k%8)+3 (low
+ *    nibble first).  scales[n][g] is the FP16 scale of group g, row pitch
+ *    ldS halves.  zeros[n][g/8] holds the 4-bit zero of group g in bits
+ *    4*(g%8).., row pitch ldZ words.  Padding is written as zero.
+ *  - Min-max range is widened to contain 0: lo = min(0, min w), hi = max(0,
+ *    max w), so the zero point is a representable code.
+ *  - scale = RNE_fp16( fp32(hi - lo) / 15 ) with IEEE single-precision
+ *    subtraction and division; codes are computed against the stored FP16
+ *    scale.  A scale that rounds to 0 is replaced by 1.0 with zero point 0.
+ *  - zero = clamp(rne(-lo / s), 0, 15); q = clamp(rne(w / s) + zero, 0, 15),
+ *    round-to-nearest-even, IEEE single-precision division.
+ *  - W_hat = (float)(q - zero) * (float)s, which is exact in FP32.
+ *  - y_ref[m][n] = sum_k (double)x[m][k] * (double)W_hat[n][k], accumulated in
+ *    FP64 and left unrounded.
+ *
+ * Build: plain C99 with optional OpenMP (the parallel loops only split
+ * independent output rows; each row's arithmetic order is fixed).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------------ */
+/* IEEE 754 binary16 / bfloat16 <-> binary32, written from the definitions.  */
+/* ------------------------------------------------------------------------ */
+
+/* binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+float oracle_f16_to_f32(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1F;
+    int m = h & 0x3FF;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)m, -24);                 /* subnormal: m * 2^-24 */
+    } else if (e == 31) {
+        v = (m == 0) ? INFINITY : NAN;
+    } else {
+        v = ldexp((double)(1024 + m), e - 25);     /* (1.m) * 2^(e-15) */
+    }
+    return (float)(sign ? -v : v);
+}
+
+/* bfloat16: the top 16 bits of a binary32. */
+float oracle_bf16_to_f32(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/*
+ * Round a finite double to a binary format with `p` significand bits
+ * (including the implicit one), minimum normal exponent `emin` and maximum
+ * exponent `emax`, round-to-nearest, ties-to-even.  Returns the rounded value
+ * as a double (or +-inf on overflow).  Used for binary16 (p=11, emin=-14,
+ * emax=15) and bfloat16 (p=8, emin=-126, emax=127).
+ */
+static double round_to_format(double v, int p, int emin, int emax)
+{
+    if (v == 0.0 || isnan(v) || isinf(v)) return v;
+    double a = fabs(v);
+    int e;
+    frexp(a, &e);              /* a = f * 2^e, f in [0.5, 1): exponent is e-1 */
+    e -= 1;
+    if (e < emin) e = emin;    /* subnormal range: fixed quantum */
+    double quantum = ldexp(1.0, e - (p - 1));
+    double m = nearbyint(a / quantum);           /* exact scaling, RNE */
+    double r = m * quantum;
+    /* overflow: the largest finite value is (2 - 2^(1-p)) * 2^emax */
+    double maxfin = ldexp(2.0 - ldexp(1.0, 1 - p), emax);
+    if (r > maxfin) r = INFINITY;
+    return v < 0 ? -r : r;
+}
+
+uint16_t oracle_f32_to_f16(float f)
+{
+    if (isnan(f)) return 0x7E00;
+    double r = round_to_format((double)f, 11, -14, 15);
+    uint16_t sign = signbit(r) ? 0x8000 : 0;
+    double a = fabs(r);
+    if (isinf(a)) return sign | 0x7C00;
+    if (a == 0.0) return sign;
+    if (a < ldexp(1.0, -14))                       /* subnormal */
+        return sign | (uint16_t)(a / ldexp(1.0, -24));
+    int e;
+    frexp(a, &e);
+    e -= 1;
+    uint16_t mant = (uint16_t)(a / ldexp(1.0, e - 10) - 1024.0);
+    return sign | (uint16_t)((e + 15) << 10) | mant;
+}
+
+uint16_t oracle_f64_to_bf16(double d)
+{
+    if (isnan(d)) return 0x7FC0;
+    double r = round_to_format(d, 8, -126, 127);
+    float f = (float)r;                            /* exact: r is a bf16 value */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(u >> 16);
+}
+
+uint16_t oracle_f32_to_bf16(float f) { return oracle_f64_to_bf16((double)f); }
+
+/* ------------------------------------------------------------------------ */
+/* Layout of the packed format.                                              */
+/* ------------------------------------------------------------------------ */
+
+static int64_t round_up(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
+
+/* uint32 words per row of qweight: 8 codes per word. */
+int64_t oracle_qweight_ld(int64_t K) { return K / 8; }
+/* halves per row of scales: K/G rounded up to 8 halves (16-byte pitch). */
+int64_t oracle_scales_ld(int64_t K, int64_t G) { return round_up(K / G, 8); }
+/* uint32 words per row of zeros: ceil(K/G / 8) rounded up to 4 words. */
+int64_t oracle_zeros_ld(int64_t K, int64_t G) { return round_up((K / G + 7) / 8, 4); }
+
+static int64_t clamp_i64(int64_t v, int64_t lo, int64_t hi)
+{
+    return v < lo ? lo : (v > hi ? hi : v);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Quantiser (packer): asymmetric min-max per group of G input channels.     */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Quantise one group of G FP32 weights.  Writes the FP16 scale bits, the zero
+ * point and G codes.  Follows the textbook asymmetric scheme: range -> scale,
+ * zero point from the minimum, codes = round(w / scale) + zero, clamped to the
+ * 4-bit grid [0, 15].
+ */
+void oracle_quantize_group(const float* w, int64_t G, uint16_t* scale_bits, int* zero, uint8_t* codes)
+{
+    float lo = 0.0f, hi = 0.0f;                    /* range widened to hold 0 */
+    for (int64_t i = 0; i < G; ++i) {
+        if (w[i] < lo) lo = w[i];
+        if (w[i] > hi) hi = w[i];
+    }
+    volatile float range = hi - lo;                /* IEEE binary32 subtraction */
+    volatile float s32 = range / 15.0f;            /* IEEE binary32 division */
+    uint16_t sb = oracle_f32_to_f16(s32);
+    float s = oracle_f16_to_f32(sb);
+    int z;
+    if (s == 0.0f) {                               /* degenerate group */
+        sb = 0x3C00;                               /* 1.0 */
+        s = 1.0f;
+        z = 0;
+    } else {
+        volatile float t = -lo / s;
+        z = (int)clamp_i64((int64_t)nearbyintf(t), 0, 15);
+    }
+    for (int64_t i = 0; i < G; ++i) {
+        volatile float t = w[i] / s;
+        int64_t q = (int64_t)nearbyintf(t) + z;
+        codes[i] = (uint8_t)clamp_i64(q, 0, 15);
+    }
+    *scale_bits = sb;
+    *zero = z;
+}
+
+/*
+ * Pack an [N,K] FP16 weight (bits) into qweight [N, K/8], scales [N, ldS],
+ * zeros [N, ldZ].  Output buffers are fully written, padding included.
+ * Returns 0 on success, -1 on bad arguments.
+ */
+int oracle_pack(const uint16_t* w_f16, int64_t N, int64_t K, int64_t G,
+                uint32_t* qweight, uint16_t* scales, uint32_t* zeros, int nthreads)
+{
+    if (N <= 0 || K <= 0 || G <= 0 || G > 256 || K % G != 0 || G % 8 != 0) return -1;
+    const int64_t ldq = oracle_qweight_ld(K);
+    const int64_t lds = oracle_scales_ld(K, G);
+    const int64_t ldz = oracle_zeros_ld(K, G);
+    const int64_t ngroups = K / G;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(static)
+#endif
+    for (int64_t n = 0; n < N; ++n) {
+        float wf[256];
+        uint8_t codes[256];
+        uint32_t* qrow = qweight + n * ldq;
+        uint16_t* srow = scales + n * lds;
+        uint32_t* zrow = zeros + n * ldz;
+        for (int64_t i = 0; i < ldq; ++i) qrow[i] = 0;
+        for (int64_t i = 0; i < lds; ++i) srow[i] = 0;
+        for (int64_t i = 0; i < ldz; ++i) zrow[i] = 0;
+        for (int64_t g = 0; g < ngroups; ++g) {
+            for (int64_t i = 0; i < G; ++i) wf[i] = oracle_f16_to_f32(w_f16[n * K + g * G + i]);
+            uint16_t sb;
+            int z;
+            oracle_quantize_group(wf, G, &sb, &z, codes);
+            srow[g] = sb;
+            zrow[g / 8] |= (uint32_t)z << (4 * (g % 8));
+            for (int64_t i = 0; i < G; ++i) {
+                int64_t k = g * G + i;
+                qrow[k / 8] |= (uint32_t)codes[i] << (4 * (k % 8));
+            }
+        }
+    }
+    (void)nthreads;
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Unpack and dequantise.                                                    */
+/* ------------------------------------------------------------------------ */
+
+int oracle_code(const uint32_t* qweight, int64_t K, int64_t n, int64_t k)
+{
+    return (int)((qweight[n * oracle_qweight_ld(K) + k / 8] >> (4 * (k % 8))) & 0xF);
+}
+
+int oracle_zero(const uint32_t* zeros, int64_t K, int64_t G, int64_t n, int64_t g)
+{
+    return (int)((zeros[n * oracle_zeros_ld(K, G) + g / 8] >> (4 * (g % 8))) & 0xF);
+}
+
+float oracle_scale(const uint16_t* scales, int64_t K, int64_t G, int64_t n, int64_t g)
+{
+    return oracle_f16_to_f32(scales[n * oracle_scales_ld(K, G) + g]);
+}
+
+/* W_hat[n][k] = (q - z) * s in FP32 (exact: at most 15 significant bits). */
+float oracle_dequant_one(const uint32_t* qweight, const uint16_t* scales, const uint32_t* zeros,
+                         int64_t K, int64_t G, int64_t n, int64_t k)
+{
+    int64_t g = k / G;
+    int q = oracle_code(qweight, K, n, k);
+    int z = oracle_zero(zeros, K, G, n, g);
+    float s = oracle_scale(scales, K, G, n, g);
+    return (float)(q - z) * s;
+}
+
+/* Full dequantisation to an FP32 [N,K] matrix. */
+void oracle_dequant(const uint32_t* qweight, const uint16_t* scales, const uint32_t* zeros,
+                    int64_t N, int64_t K, int64_t G, float* w_out, int nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(static)
+#endif
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k)
+            w_out[n * K + k] = oracle_dequant_one(qweight, scales, zeros, K, G, n, k);
+    (void)nthreads;
+}
+
+/* ------------------------------------------------------------------------ */
+/* The layer: y_ref = x * W_hat^T in FP64.                                   */
+/* ------------------------------------------------------------------------ */
+
+/* One output element, the plain definition. */
+double oracle_linear_one(const uint16_t* x_bf16, const uint32_t* qweight, const uint16_t* scales,
+                         const uint32_t* zeros, int64_t K, int64_t G, int64_t m, int64_t n)
+{
+    double acc = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        double xv = (double)oracle_bf16_to_f32(x_bf16[m * K + k]);
+        double wv = (double)oracle_dequant_one(qweight, scales, zeros, K, G, n, k);
+        acc += xv * wv;
+    }
+    return acc;
+}
+
+/*
+ * y_ref [M,N] (FP64) for all outputs: every element is the plain definition
+ * of oracle_linear_one (products summed over k in increasing order).
+ */
+void oracle_linear(const uint16_t* x_bf16, const uint32_t* qweight, const uint16_t* scales,
+                   const uint32_t* zeros, int64_t M, int64_t N, int64_t K, int64_t G,
+                   double* y_out, int nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t m = 0; m < M; ++m)
+            y_out[m * N + n] = oracle_linear_one(x_bf16, qweight, scales, zeros, K, G, m, n);
+    (void)nthreads;
+}
+
+/* Selected outputs only: y_out[i] = y_ref[ms[i]][ns[i]]. */
+void oracle_linear_sampled(const uint16_t* x_bf16, const uint32_t* qweight, const uint16_t* scales,
+                           const uint32_t* zeros, int64_t K, int64_t G, const int64_t* ms,
+                           const int64_t* ns, int64_t count, double* y_out, int nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int64_t i = 0; i < count; ++i)
+        y_out[i] = oracle_linear_one(x_bf16, qweight, scales, zeros, K, G, ms[i], ns[i]);
+    (void)nthreads;
+}
+
+int oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

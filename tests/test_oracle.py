@@ -1,0 +1,325 @@
+"""Pins for the CPU oracle: what the pages and the mathematics fix, checked on
+the CPU without any GPU code.
+
+Each test ties the oracle to something other than itself:
+  * library routines for the IEEE conversions (numpy float16, torch bfloat16);
+  * hand-derived packing examples (tests/golden/pack_examples.json);
+  * numbers the pages print (tests/golden/closed_forms.json);
+  * closed forms (on-grid round trip, the rounding-error bound);
+  * exact rational brute force of dequantise-then-multiply on tiny shapes;
+  * special cases with exact answers (one-hot x, q == z, power-of-two x).
+"""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _h(s):
+    return int(s, 16)
+
+
+# --------------------------------------------------------------------------
+# IEEE conversions against library routines
+# --------------------------------------------------------------------------
+
+def test_f16_to_f32_all_bit_patterns():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float32)
+    got = np.array([oracle.f16_to_f32(int(b)) for b in bits], np.float32)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+
+
+def _f16_probe_values(rng):
+    v = []
+    # random magnitudes spanning subnormal .. overflow
+    e = rng.uniform(-27, 17, 20000)
+    v.append(np.sign(rng.standard_normal(20000)) * np.exp2(e))
+    # exact midpoints between neighbouring FP16 values (ties), normal and subnormal
+    b = rng.integers(0, 0x7BFF, 5000).astype(np.uint16)
+    lo = b.view(np.float16).astype(np.float64)
+    hi = (b + 1).astype(np.uint16).view(np.float16).astype(np.float64)
+    v.append((lo + hi) / 2)
+    v.append(np.array([65504.0, 65519.0, 65519.996, 65520.0, 65536.0, 1e6, 2.0 ** -24, 2.0 ** -25,
+                       2.0 ** -25 * 1.0001, 2.0 ** -14, 2.0 ** -14 * (1 - 2.0 ** -12), 0.0, -0.0]))
+    return np.concatenate(v).astype(np.float32)
+
+
+def test_f32_to_f16_rne_matches_numpy():
+    rng = np.random.default_rng(1)
+    vals = _f16_probe_values(rng)
+    ref = vals.astype(np.float16).view(np.uint16)
+    got = np.array([oracle.f32_to_f16(float(x)) for x in vals], np.uint16)
+    assert np.array_equal(got, ref)
+
+
+def test_bf16_conversions_match_torch():
+    rng = np.random.default_rng(2)
+    e = rng.uniform(-140, 127, 20000)
+    vals = (np.sign(rng.standard_normal(20000)) * np.exp2(e)).astype(np.float32)
+    # ties: FP32 values exactly halfway between neighbouring BF16 values
+    b = rng.integers(0, 0x7F7F, 5000).astype(np.uint32)
+    ties = ((b << 16) | 0x8000).astype(np.uint32).view(np.float32)
+    vals = np.concatenate([vals, ties, np.array([0.0, -0.0, 3.4e38, 1e-45], np.float32)])
+    ref = torch.from_numpy(vals).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = np.array([oracle.f32_to_bf16(float(x)) for x in vals], np.uint16)
+    assert np.array_equal(got, ref)
+    # widening is exact: every finite pattern round-trips
+    pats = np.arange(0, 65536, 7, dtype=np.uint32).astype(np.uint16)
+    wide = oracle.bf16_bits_to_f32_array(pats)
+    fin = np.isfinite(wide)
+    back = torch.from_numpy(wide[fin]).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(back, pats[fin])
+
+
+# --------------------------------------------------------------------------
+# Hand-derived packing examples
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("idx", range(4))
+def test_golden_group(idx):
+    g = _golden("pack_examples.json")["groups"][idx]
+    w = np.array(g["w"], np.float32)
+    sb, z, codes = oracle.quantize_group(w)
+    assert sb == _h(g["scale_bits"]), g["name"]
+    assert z == g["zero"], g["name"]
+    assert codes.tolist() == g["codes"], g["name"]
+    # the same group through the full packer (FP16 input, N = 1, K = G)
+    q, s, zz = oracle.pack(w.astype(np.float16).reshape(1, -1), g["G"])
+    assert [int(v) for v in q[0]] == [_h(v) for v in g["words"]]
+    assert int(s[0, 0]) == _h(g["scale_bits"])
+    assert int(zz[0, 0]) == g["zero"]
+    # sum of the dequantised row (exact)
+    what = oracle.dequant(q, s, zz, 1, w.shape[0], g["G"])
+    assert float(what.astype(np.float64).sum()) == g["sum_w_hat"]
+
+
+def test_golden_two_group_row():
+    d = _golden("pack_examples.json")
+    row = np.concatenate([np.array(d["groups"][0]["w"]), np.array(d["groups"][2]["w"])])
+    w = row.astype(np.float16).reshape(1, 64)
+    q, s, z = oracle.pack(w, 32)
+    ex = d["two_group_row"]
+    assert [int(v) for v in s[0]] == [_h(v) for v in ex["scales_row"]]
+    assert [int(v) for v in z[0]] == [_h(v) for v in ex["zeros_row"]]
+    x = np.full((1, 64), 0x3F80, np.uint16)          # BF16 1.0
+    y = oracle.linear(x, q, s, z, 1, 64, 32)
+    assert y[0, 0] == ex["y_all_ones"]
+
+
+# --------------------------------------------------------------------------
+# Numbers printed on the pages
+# --------------------------------------------------------------------------
+
+def _algorithmic_bytes(q, N, K, G):
+    """Packed bytes per matrix: codes + one FP16 scale + one 4-bit zero per group (padding excluded)."""
+    return q.nbytes + N * (K // G) * 2 + N * (K // G) // 2
+
+
+def test_closed_form_bits_per_weight_and_model_sizes():
+    cf = _golden("closed_forms.json")
+    N, K, G = 8, 4096, 128
+    rng = np.random.default_rng(3)
+    w = (rng.standard_normal((N, K)) * 0.02).astype(np.float16)
+    q, s, z = oracle.pack(w, G)
+    bpw = _algorithmic_bytes(q, N, K, G) * 8 / (N * K)
+    assert bpw == 4 + (16 + 4) / 128                        # 4.15625
+    assert round(bpw, cf["bits_per_weight_g128"]["decimals"]) == cf["bits_per_weight_g128"]["value"]
+    m = cf["model_13b_bytes"]
+    fp16_gb = m["params"] * 16 / 8 / 1e9
+    w4_gb = m["params"] * bpw / 8 / 1e9
+    assert round(fp16_gb, 1) == m["fp16_gb"]
+    assert round(w4_gb, 2) == m["w4_gb"]
+    assert round(fp16_gb - w4_gb, 1) == m["saved_gb"]
+    a = cf["activation_row_5120"]
+    x = np.zeros((1, a["hidden"]), np.uint16)                # one BF16 activation row
+    assert round(x.nbytes / 1000, 1) == a["bf16_kb"]
+    assert round(x.nbytes / 2 / 1000, 1) == a["int8_kb"]
+    b = cf["model_70b_bytes"]
+    assert b["params"] * 2 / 1e9 == b["bf16_gb"]
+    assert b["params"] * 4 / 8 / 1e9 == b["int4_gb"]
+
+
+# --------------------------------------------------------------------------
+# Closed forms: on-grid round trip and the error bound
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("G", [32, 64, 128, 256])
+def test_on_grid_round_trip(G):
+    """Weights already on a group's grid are recovered exactly: q, s and z."""
+    rng = np.random.default_rng(G)
+    N, K = 8, 2 * G
+    ng = K // G
+    mant = rng.integers(64, 128, (N, ng))                   # 7-bit significands
+    expo = rng.integers(-18, -8, (N, ng))
+    s = mant.astype(np.float64) * np.exp2(expo)
+    z = rng.integers(0, 16, (N, ng))
+    q = rng.integers(0, 16, (N, K))
+    for n in range(N):
+        for g in range(ng):
+            pos = rng.choice(G, 2, replace=False)
+            q[n, g * G + pos[0]] = 0
+            q[n, g * G + pos[1]] = 15
+    w = (q - np.repeat(z, G, axis=1)) * np.repeat(s, G, axis=1)
+    w16 = w.astype(np.float16)
+    assert np.array_equal(w16.astype(np.float64), w)          # on the FP16 grid
+    qq, ss, zz = oracle.pack(w16, G)
+    assert np.array_equal(oracle.unpack_codes(qq, K), q.astype(np.uint8))
+    assert np.array_equal(oracle.unpack_zeros(zz, K, G), z.astype(np.uint8))
+    assert np.array_equal(ss[:, :ng].view(np.float16).astype(np.float64), s)
+
+
+@pytest.mark.parametrize("G", [32, 64, 128, 256])
+def test_error_bound_and_extremes(G):
+    """|w - W_hat| <= (1/2 + 16*2^-11) s for every weight, the group minimum maps
+    to code 0 when it is negative, and codes are monotone in w within a group."""
+    rng = np.random.default_rng(100 + G)
+    N, K = 16, 4 * G
+    w = rng.standard_normal((N, K)) * 0.02
+    w[:, rng.choice(K, 3, replace=False)] *= 20.0             # outlier channels
+    w16 = w.astype(np.float16)
+    q, s, z = oracle.pack(w16, G)
+    what = oracle.dequant(q, s, z, N, K, G).astype(np.float64)
+    codes = oracle.unpack_codes(q, K)
+    sc = np.repeat(s[:, : K // G].view(np.float16).astype(np.float64), G, axis=1)
+    wf = w16.astype(np.float64)
+    assert np.all(np.abs(wf - what) <= (0.5 + 16 * 2.0 ** -11) * sc)
+    for n in range(N):
+        for g in range(K // G):
+            ww = wf[n, g * G:(g + 1) * G]
+            cc = codes[n, g * G:(g + 1) * G].astype(int)
+            if ww.min() < 0:
+                assert cc[np.argmin(ww)] == 0
+            order = np.argsort(ww, kind="stable")
+            assert np.all(np.diff(cc[order]) >= 0)
+
+
+def test_degenerate_groups():
+    w = np.zeros((8, 64), np.float16)
+    w[1, :32] = np.float16(1e-7)           # scale underflows FP16 -> degenerate
+    w[2, 32:] = np.float16(-3e-8)
+    q, s, z = oracle.pack(w, 32)
+    assert np.all(q == 0)
+    assert np.all(s[:, :2] == 0x3C00)
+    assert np.all(z == 0)
+    assert np.all(oracle.dequant(q, s, z, 8, 64, 32) == 0)
+
+
+def test_pack_rejects_bad_shapes():
+    with pytest.raises(ValueError):
+        oracle.pack(np.zeros((8, 48), np.float16), 32)       # K % G != 0
+    with pytest.raises(ValueError):
+        oracle.pack(np.zeros((8, 512), np.float16), 512)     # G beyond 256
+
+
+# --------------------------------------------------------------------------
+# Exact rational brute force of dequantise-then-multiply
+# --------------------------------------------------------------------------
+
+def _frac_f16(bits):
+    return Fraction(float(np.array([bits], np.uint16).view(np.float16)[0]))
+
+
+def _frac_bf16(bits):
+    return Fraction(float(oracle.bf16_bits_to_f32_array(np.array([bits], np.uint16))[0]))
+
+
+@pytest.mark.parametrize("M,N,Kg,G", [(1, 8, 1, 32), (3, 16, 2, 32), (1, 16, 2, 64), (3, 8, 1, 128)])
+def test_brute_force_rational(M, N, Kg, G):
+    K = Kg * G
+    rng = np.random.default_rng(M * 1000 + N * 10 + Kg)
+    w16 = (rng.standard_normal((N, K)) * 0.05).astype(np.float16)
+    xb = torch.from_numpy(rng.standard_normal((M, K)).astype(np.float32)).to(torch.bfloat16)
+    x = xb.view(torch.int16).numpy().view(np.uint16)
+    q, s, z = oracle.pack(w16, G)
+    y = oracle.linear(x, q, s, z, N, K, G)
+    for m in range(M):
+        for n in range(N):
+            acc = Fraction(0)
+            for k in range(K):
+                code = (int(q[n, k // 8]) >> (4 * (k % 8))) & 0xF
+                g = k // G
+                zero = (int(z[n, g // 8]) >> (4 * (g % 8))) & 0xF
+                acc += _frac_bf16(x[m, k]) * (code - zero) * _frac_f16(s[n, g])
+            ref = float(acc)
+            assert abs(y[m, n] - ref) <= 1e-12 * max(1.0, abs(ref)), (m, n, y[m, n], ref)
+
+
+# --------------------------------------------------------------------------
+# Special cases with exact answers
+# --------------------------------------------------------------------------
+
+def _random_packed(N, K, G, seed):
+    rng = np.random.default_rng(seed)
+    w16 = (rng.standard_normal((N, K)) * 0.02).astype(np.float16)
+    return oracle.pack(w16, G)
+
+
+def test_one_hot_selects_column_of_w_hat():
+    N, K, G = 16, 256, 64
+    q, s, z = _random_packed(N, K, G, 7)
+    what = oracle.dequant(q, s, z, N, K, G)
+    for k in (0, 5, 63, 64, 200, 255):
+        x = np.zeros((1, K), np.uint16)
+        x[0, k] = 0x3F80
+        y = oracle.linear(x, q, s, z, N, K, G)
+        assert np.array_equal(y[0], what[:, k].astype(np.float64))
+
+
+def test_codes_equal_zero_give_zero():
+    N, K, G = 8, 128, 32
+    q, s, z = _random_packed(N, K, G, 8)
+    zeros = oracle.unpack_zeros(z, K, G)
+    qz = np.zeros_like(q)
+    for k in range(K):
+        qz[:, k // 8] |= (zeros[:, k // G].astype(np.uint32) << np.uint32(4 * (k % 8)))
+    x = torch.randn(3, K, generator=torch.Generator().manual_seed(0)).to(torch.bfloat16)
+    y = oracle.linear(x.view(torch.int16).numpy().view(np.uint16), qz, s, z, N, K, G)
+    assert np.all(y == 0.0)
+
+
+def test_power_of_two_scaling_of_x():
+    N, K, G = 16, 256, 128
+    q, s, z = _random_packed(N, K, G, 9)
+    x = torch.randn(2, K, generator=torch.Generator().manual_seed(1)).to(torch.bfloat16)
+    y0 = oracle.linear(x.view(torch.int16).numpy().view(np.uint16), q, s, z, N, K, G)
+    for j in (-3, 4):
+        xs = (x.float() * 2.0 ** j).to(torch.bfloat16)
+        yj = oracle.linear(xs.view(torch.int16).numpy().view(np.uint16), q, s, z, N, K, G)
+        assert np.array_equal(yj, y0 * 2.0 ** j)
+
+
+def test_sampled_equals_full():
+    N, K, G = 24, 512, 128
+    q, s, z = _random_packed(N, K, G, 10)
+    x = torch.randn(4, K, generator=torch.Generator().manual_seed(2)).to(torch.bfloat16)
+    xb = x.view(torch.int16).numpy().view(np.uint16)
+    y = oracle.linear(xb, q, s, z, N, K, G)
+    ms = np.array([0, 3, 1, 2, 3])
+    ns = np.array([0, 23, 7, 11, 5])
+    ys = oracle.linear_sampled(xb, q, s, z, K, G, ms, ns)
+    assert np.array_equal(ys, y[ms, ns])
+
+
+def test_bf16_output_rounding_is_rne():
+    # the oracle's FP64 -> BF16 used by the one-hot exactness checks
+    vals = np.array([1.0, 1.00390625, 1.01171875, -2.5e-3, 7.0e4, 3.0e38], np.float64)
+    ref = torch.from_numpy(vals).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = np.array([oracle.f64_to_bf16(float(v)) for v in vals], np.uint16)
+    assert np.array_equal(got, ref)
+    assert math.isclose(oracle.bf16_to_f32(0x3F80), 1.0)

@@ -1,0 +1,95 @@
+"""Seeded synthetic inputs and the workload table for the W4A16 linear layer.
+
+This module holds no quantisation or GEMM arithmetic.  It only draws the
+random inputs (FP16 weights, BF16 activations) that both the CUDA path and the
+CPU oracle consume, so the two sides see bit-identical data.
+
+Input recipe (weights are never trained; no dataset is involved):
+  * torch CPU generator, ``torch.Generator().manual_seed(seed)``;
+  * W ~ N(0, sigma) drawn in FP32, optional outlier input channels multiplied
+    by 20 in FP32, then round-to-nearest-even to FP16;
+  * x ~ N(0, 1) drawn in FP32, then round-to-nearest-even to BF16;
+  * the j-th matrix of a workload uses seed + 100*j, its activations seed +
+    100*j + 50.
+
+The shapes follow the pages' examples: a 13B-class layer (hidden 5120, FFN
+13824: multigrid.ai "Weight-Only Quantization Explained", section "The memory
+arithmetic") and a 70B-class layer (hidden 8192, FFN 28672: zhuai.tech
+"Quantization Is Not a Zip File", section 2 "Capacity comes first" sizes a 70B
+model).  Group sizes are 32/64/128/256 (same page, section 3, "Block
+locality").  Decode uses M=1..16 rows, prefill M=2048.
+"""
+from dataclasses import dataclass
+from typing import Tuple
+
+import torch
+
+
+@dataclass(frozen=True)
+class Linear:
+    name: str
+    K: int
+    N: int
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    linears: Tuple[Linear, ...]
+    Ms: Tuple[int, ...]
+    Gs: Tuple[int, ...]
+    sigma: float
+    outlier_frac: float
+    seed: int
+    dual: bool = False
+
+
+WORKLOADS = {
+    # single 4096x4096 decode GEMV
+    "single_4096": Workload("single_4096", (Linear("linear", 4096, 4096),), (1,), (128,), 0.02, 0.0, 0),
+    # 13B-shaped decoder-layer linears at decode
+    "layer13b_decode": Workload(
+        "layer13b_decode",
+        (Linear("q", 5120, 5120), Linear("k", 5120, 5120), Linear("v", 5120, 5120), Linear("o", 5120, 5120),
+         Linear("gate", 5120, 13824), Linear("up", 5120, 13824), Linear("down", 13824, 5120)),
+        (1,), (128,), 0.02, 0.001, 1),
+    # batch x group-size sweep on the 5120->13824 up-projection
+    "up13b_sweep": Workload("up13b_sweep", (Linear("up", 5120, 13824),), (1, 2, 4, 8, 16, 32),
+                            (32, 64, 128, 256), 0.02, 0.001, 2),
+    # paired gate/up projections sharing one x
+    "gateup13b_dual": Workload("gateup13b_dual", (Linear("gate", 5120, 13824), Linear("up", 5120, 13824)),
+                               (1, 4), (128,), 0.02, 0.0, 3, dual=True),
+    # 70B-shaped FFN gate and down, decode (M=1) and prefill (M=2048)
+    "ffn70b": Workload("ffn70b", (Linear("gate", 8192, 28672), Linear("down", 28672, 8192)), (1, 2048),
+                       (128,), 0.015, 0.0, 4),
+}
+
+
+def weight_f16(N: int, K: int, sigma: float, seed: int, outlier_frac: float = 0.0) -> torch.Tensor:
+    """FP16 [N,K] weight: N(0, sigma) in FP32, outlier channels x20, RNE to FP16."""
+    g = torch.Generator().manual_seed(seed)
+    w = torch.randn(N, K, generator=g, dtype=torch.float32) * sigma
+    n_out = int(round(outlier_frac * K))
+    if n_out > 0:
+        cols = torch.randperm(K, generator=g)[:n_out]
+        w[:, cols] *= 20.0
+    return w.to(torch.float16)
+
+
+def activations_bf16(M: int, K: int, seed: int) -> torch.Tensor:
+    """BF16 [M,K] activations: N(0,1) in FP32, RNE to BF16."""
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(M, K, generator=g, dtype=torch.float32).to(torch.bfloat16)
+
+
+def matrix_seed(workload: Workload, j: int) -> int:
+    return workload.seed + 100 * j
+
+
+def act_seed(workload: Workload, j: int) -> int:
+    return workload.seed + 100 * j + 50
+
+
+def bits_u16(t: torch.Tensor):
+    """FP16/BF16 tensor -> numpy uint16 bit patterns (for the oracle)."""
+    return t.contiguous().view(torch.int16).numpy().view("uint16")
