@@ -1,0 +1,403 @@
+"""Benchmark of the W4A16 weight-only linear layer on one B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Workload: the 70B-shaped FFN gate (8192 -> 28672) and down (28672 -> 8192)
+projections, G = 128, weights ~ N(0, 0.015) quantised by the library's
+packer, activations ~ N(0, 1) in BF16.  One step = one pass of the whole hot
+path over one batch: decode (M = 1, the GEMV) on gate and down, then prefill
+(M = 2048, the tensor-core GEMM) on gate and down.
+
+`value` is the decode metric: effective weight GB/s of the GEMV at M = 1,
+counting packed codes + FP16 scales + 4-bit zeros + x + y bytes.  The
+prefill metric (TFLOP/s at M = 2048) is reported beside it under "gemm".
+Both are whole-job figures with inputs resident in HBM; "e2e" repeats the
+measurement through the same C entry points with pinned host buffers and the
+host<->device copies inside the timed region.
+
+Cold L2: each matrix has 2 device copies used alternately, so every launch
+reads weights that at least 3 other matrices' worth of traffic (> 360 MB,
+L2 = 126 MB) has passed since their last use.
+
+`--impl reference` times the CPU oracle (the plain C implementation the tests
+compare against) on the host cores: the decode GEMVs in full, the prefill
+GEMMs on a sampled set of output rows.  That arm exists for comparison only.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+WORKLOAD = "ffn70b"
+M_DECODE, M_PREFILL = 1, 2048
+G = 128
+METRIC = "W4A16 GEMV weight GB/s (% of HBM peak) at M=1; GEMM TFLOP/s at M=2048"
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+def gemv_bytes(M, N, K, G):
+    """Algorithmic bytes of one decode launch: packed codes (K/2 per row),
+    one FP16 scale and one 4-bit zero per (row, group), x and y in BF16."""
+    return N * K // 2 + N * (K // G) * 2 + N * (K // G) // 2 + M * K * 2 + M * N * 2
+
+
+def gemm_flops(M, N, K):
+    return 2.0 * M * N * K
+
+
+def kernel_hashes():
+    """Source hashes of the kernels whose ncu counters are stored in profiles/."""
+    out = {}
+    for name in ("gemv.cu", "gemm_tc.cu"):
+        p = os.path.join(ROOT, "w4a16_weight_only_linear_b300", "csrc", name)
+        if os.path.exists(p):
+            out[name] = hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+    return out
+
+
+def stored_traffic(kernel, key):
+    """DRAM bytes per launch from a committed ncu summary, or None when the
+    kernel source changed since the capture."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    d = json.load(open(path)).get(key)
+    if not d or d.get("source_hash") != kernel_hashes().get(kernel):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import w4a16_weight_only_linear_b300 as w4
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    wk = wl.WORKLOADS[WORKLOAD]
+    pk = peaks()
+    copies = 2
+
+    # weights: generated once per matrix (seeded), packed on the device; each rank
+    # is an independent replica (the layer has no exchange step on one GPU)
+    mats = []
+    for j, lin in enumerate(wk.linears):
+        w = wl.weight_f16(lin.N, lin.K, wk.sigma, wl.matrix_seed(wk, j), wk.outlier_frac).to(dev)
+        packed = [w4.w4a16_pack(w, G) for _ in range(copies)]
+        del w
+        mats.append((lin, packed))
+    torch.cuda.synchronize()
+    gemm_ok = all(w4.w4a16_linear_path(M_PREFILL, lin.N, lin.K, G) == 2 for lin, _ in mats)
+    try:
+        xt = torch.zeros(M_PREFILL, mats[0][0].K, dtype=torch.bfloat16, device=dev)
+        w4.w4a16_linear(xt, *mats[0][1][0], G)
+        torch.cuda.synchronize()
+        del xt
+    except w4.W4A16Error:
+        gemm_ok = False
+
+    xs_dec = [wl.activations_bf16(M_DECODE, lin.K, wl.act_seed(wk, j)).to(dev) for j, (lin, _) in enumerate(mats)]
+    xs_pre = [wl.activations_bf16(M_PREFILL, lin.K, wl.act_seed(wk, j) + 7).to(dev) for j, (lin, _) in enumerate(mats)]
+    ys_dec = [torch.empty(M_DECODE, lin.N, dtype=torch.bfloat16, device=dev) for lin, _ in mats]
+    ys_pre = [torch.empty(M_PREFILL, lin.N, dtype=torch.bfloat16, device=dev) for lin, _ in mats]
+    stream = torch.cuda.current_stream()
+
+    def step(i, events=None):
+        c = i % copies
+        for j, (lin, packed) in enumerate(mats):
+            if events is not None:
+                events["dec"][j].append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
+                events["dec"][j][-1][0].record(stream)
+            w4.w4a16_linear(xs_dec[j], *packed[c], G, out=ys_dec[j], stream=stream)
+            if events is not None:
+                events["dec"][j][-1][1].record(stream)
+        if gemm_ok:
+            for j, (lin, packed) in enumerate(mats):
+                if events is not None:
+                    events["pre"][j].append((torch.cuda.Event(enable_timing=True),
+                                             torch.cuda.Event(enable_timing=True)))
+                    events["pre"][j][-1][0].record(stream)
+                w4.w4a16_linear(xs_pre[j], *packed[c], G, out=ys_pre[j], stream=stream)
+                if events is not None:
+                    events["pre"][j][-1][1].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+
+    events = {"dec": [[] for _ in mats], "pre": [[] for _ in mats]}
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        t0.record(stream)
+        for i in range(args.steps):
+            step(i, events)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    total_ms = t0.elapsed_time(t1)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+        torch.distributed.barrier()
+
+    dec_ms = [sum(a.elapsed_time(b) for a, b in ev) for ev in events["dec"]]
+    pre_ms = [sum(a.elapsed_time(b) for a, b in ev) for ev in events["pre"]] if gemm_ok else None
+    dec_bytes = [gemv_bytes(M_DECODE, lin.N, lin.K, G) for lin, _ in mats]
+    dec_gbs = world * sum(dec_bytes) * args.steps / (sum(dec_ms) * 1e-3) / 1e9
+    out = {
+        "metric": METRIC, "value": round(dec_gbs, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "ffn70b: 70B-shaped FFN gate 8192->28672 and down 28672->8192, G=128, "
+                               "decode M=1 (GEMV) + prefill M=2048 (tcgen05 GEMM), weights N(0,0.015), x N(0,1)",
+                   "M_decode": M_DECODE, "M_prefill": M_PREFILL if gemm_ok else None, "G": G,
+                   "l2": "inputs larger than L2: 2 rotating device copies of each 122 MB packed matrix",
+                   "parallelism": f"replicas x{world}"},
+    }
+    # roofline, per kernel, from the CUDA-event durations inside the timed region
+    gemv_launch_ms = sum(dec_ms) / (len(mats) * args.steps)
+    gemv_bytes_per_launch = sum(dec_bytes) / len(mats)
+    gemv_ach = gemv_bytes_per_launch / (gemv_launch_ms * 1e-3) / 1e9
+    roof_gemv = {"kernel": "gemv (M=1, mean of gate and down launches)", "bound": "hbm",
+                 "achieved": round(gemv_ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                 "frac": round(gemv_ach / pk["hbm_gbs"], 4), "peak_source": pk["source"],
+                 "traffic": stored_traffic("gemv.cu", "gemv_ffn70b_M1"),
+                 "algorithmic_bytes_per_launch": gemv_bytes_per_launch,
+                 "launch_us": round(gemv_launch_ms * 1e3, 3),
+                 "per_matrix_gbs": {lin.name: round(b / (ms / args.steps * 1e-3) / 1e9, 1)
+                                    for (lin, _), b, ms in zip(mats, dec_bytes, dec_ms)}}
+    out["roofline"] = roof_gemv
+    launches = len(mats) * args.steps
+    if gemm_ok:
+        flops = [gemm_flops(M_PREFILL, lin.N, lin.K) for lin, _ in mats]
+        tflops = world * sum(flops) * args.steps / (sum(pre_ms) * 1e-3) / 1e12
+        gemm_launch_ms = sum(pre_ms) / (len(mats) * args.steps)
+        ach = (sum(flops) / len(mats)) / (gemm_launch_ms * 1e-3) / 1e12
+        roof_gemm = {"kernel": "gemm_tc (M=2048, mean of gate and down launches)", "bound": "tensor",
+                     "achieved": round(ach, 1), "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                     "frac": round(ach / pk["bf16_tflops_sustained"], 4),
+                     "frac_of_burst_peak": round(ach / pk["bf16_tflops"], 4), "peak_source": pk["source"],
+                     "peak_kind": "sustained (timed inside a seconds-long step loop)",
+                     "traffic": stored_traffic("gemm_tc.cu", "gemm_ffn70b_M2048"),
+                     "algorithmic_flops_per_launch": sum(flops) / len(mats),
+                     "launch_us": round(gemm_launch_ms * 1e3, 3),
+                     "per_matrix_tflops": {lin.name: round(f / (ms / args.steps * 1e-3) / 1e12, 1)
+                                           for (lin, _), f, ms in zip(mats, flops, pre_ms)}}
+        out["gemm"] = {"value": round(tflops, 1), "unit": "TFLOP/s", "roofline": roof_gemm}
+        launches += len(mats) * args.steps
+        # the dominant kernel by time is the prefill GEMM
+        out["roofline_gemv"] = roof_gemv
+        out["roofline"] = roof_gemm
+    else:
+        out["gemm"] = {"value": None, "unit": "TFLOP/s", "note": "tensor-core GEMM not available for this shape"}
+    out["gpu_launches"] = launches
+    out["clocks"] = clk.summary()
+    out["e2e"] = e2e_ours(w4, mats, dev, args, gemm_ok)
+    if rank == 0:
+        out["cpu_baseline"] = cpu_baseline(args)
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def e2e_ours(w4, mats, dev, args, gemm_ok):
+    """Same metric through the C entry points, host buffers: every step copies
+    x from pinned host memory, runs the layer and reads y back to the host."""
+    wk = wl.WORKLOADS[WORKLOAD]
+    hx = [wl.activations_bf16(M_DECODE, lin.K, wl.act_seed(wk, j)).pin_memory() for j, (lin, _) in enumerate(mats)]
+    hy = [torch.empty(M_DECODE, lin.N, dtype=torch.bfloat16).pin_memory() for lin, _ in mats]
+    dx = [torch.empty_like(h, device=dev) for h in hx]
+    dy = [torch.empty(M_DECODE, lin.N, dtype=torch.bfloat16, device=dev) for lin, _ in mats]
+    stream = torch.cuda.current_stream()
+    steps = max(args.steps, 20)
+
+    def run(n):
+        for i in range(n):
+            for j, (lin, packed) in enumerate(mats):
+                dx[j].copy_(hx[j], non_blocking=True)
+                w4.w4a16_linear(dx[j], *packed[i % 2], G, out=dy[j], stream=stream)
+                hy[j].copy_(dy[j], non_blocking=True)
+        torch.cuda.synchronize()
+
+    run(3)
+    t = time.perf_counter()
+    run(steps)
+    dt = time.perf_counter() - t
+    byts = sum(gemv_bytes(M_DECODE, lin.N, lin.K, G) for lin, _ in mats)
+    return {"value": round(byts * steps / dt / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": sum(h.numel() * 2 for h in hx),
+            "d2h_bytes_per_step": sum(h.numel() * 2 for h in hy),
+            "scope": "decode GEMVs (M=1) of the step, host wall clock, pinned buffers"}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (reported baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+def _oracle_setup():
+    import oracle
+    wk = wl.WORKLOADS[WORKLOAD]
+    mats = []
+    for j, lin in enumerate(wk.linears):
+        w = wl.weight_f16(lin.N, lin.K, wk.sigma, wl.matrix_seed(wk, j), wk.outlier_frac)
+        mats.append((lin, oracle.pack(wl.bits_u16(w), G)))
+    xs = [wl.bits_u16(wl.activations_bf16(M_DECODE, lin.K, wl.act_seed(wk, j))) for j, (lin, _) in enumerate(mats)]
+    return oracle, mats, xs
+
+
+def _oracle_decode_pass(oracle, mats, xs):
+    for (lin, (q, s, z)), x in zip(mats, xs):
+        oracle.linear(x, q, s, z, lin.N, lin.K, G)
+
+
+def cpu_baseline(args, budget_s=10.0):
+    oracle, mats, xs = _oracle_setup()
+    threads = oracle.max_threads()
+    byts = sum(gemv_bytes(M_DECODE, lin.N, lin.K, G) for lin, _ in mats)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        _oracle_decode_pass(oracle, mats, xs)
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(byts * n / dt / 1e9, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} full decode passes (M=1 gate and down GEMVs, FP64 oracle) in {dt:.1f} s"}
+
+
+REF_ROW_FRACTION = 32   # the reference arm's step: every 32nd output row of each matrix
+
+
+def _oracle_sampled_pass(oracle, mats, xs):
+    for (lin, (q, s, z)), x in zip(mats, xs):
+        ns = np.arange(0, lin.N, REF_ROW_FRACTION, dtype=np.int64)
+        oracle.linear_sampled(x, q, s, z, lin.K, G, np.zeros_like(ns), ns)
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    oracle, mats, xs = _oracle_setup()
+    threads = oracle.max_threads()
+    byts = sum(gemv_bytes(M_DECODE, lin.N // REF_ROW_FRACTION, lin.K, G) for lin, _ in mats)
+    for _ in range(args.warmup):
+        _oracle_sampled_pass(oracle, mats, xs)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_sampled_pass(oracle, mats, xs)
+    dt = time.perf_counter() - t0
+    v = byts * args.steps / dt / 1e9
+    out = {"metric": METRIC, "value": round(v, 3), "unit": "GB/s", "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "impl": "reference",
+           "config": {"workload": "ffn70b decode: gate 8192->28672 and down 28672->8192, G=128, M=1",
+                      "M_decode": M_DECODE, "G": G, "parallelism": "host cores"},
+           "cpu_baseline": {"value": round(v, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                            "sample": f"{args.steps} steps, each the M=1 gate and down GEMVs on every "
+                                      f"{REF_ROW_FRACTION}th output row (FP64 oracle)"},
+           "e2e": {"value": round(v, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

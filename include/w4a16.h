@@ -51,6 +51,12 @@
 
 #include <stdint.h>
 
+#if defined(__GNUC__)
+#define W4A16_API __attribute__((visibility("default")))
+#else
+#define W4A16_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -71,16 +77,16 @@ typedef enum {
 } w4a16_status;
 
 /* Human-readable name of a status code (static string, never NULL). */
-const char* w4a16_status_string(w4a16_status status);
+W4A16_API const char* w4a16_status_string(w4a16_status status);
 
 /* ---- layout helpers (elements per row; pure host functions) ------------- */
 
 /* uint32 words per qweight row: K / 8. */
-int64_t w4a16_qweight_ld(int64_t K);
+W4A16_API int64_t w4a16_qweight_ld(int64_t K);
 /* FP16 halves per scales row: K/G rounded up to a multiple of 8. */
-int64_t w4a16_scales_ld(int64_t K, int G);
+W4A16_API int64_t w4a16_scales_ld(int64_t K, int G);
 /* uint32 words per zeros row: ceil(K/G / 8) rounded up to a multiple of 4. */
-int64_t w4a16_zeros_ld(int64_t K, int G);
+W4A16_API int64_t w4a16_zeros_ld(int64_t K, int G);
 
 /* ---- packer ------------------------------------------------------------------
  * w4a16_pack: quantise FP16 W [N,K] to (qweight, scales, zeros), asymmetric
@@ -97,7 +103,7 @@ int64_t w4a16_zeros_ld(int64_t K, int G);
  * Every element of qweight, scales and zeros is written, row padding as 0.
  * Errors: W4A16_ERR_INVALID_ARG / _UNSUPPORTED / _MISALIGNED as above.
  */
-w4a16_status w4a16_pack(const void* w_f16, int64_t N, int64_t K, int G,
+W4A16_API w4a16_status w4a16_pack(const void* w_f16, int64_t N, int64_t K, int G,
                         uint32_t* qweight, void* scales_f16, uint32_t* zeros,
                         w4a16_stream_t stream);
 
@@ -107,7 +113,7 @@ w4a16_status w4a16_pack(const void* w_f16, int64_t N, int64_t K, int G,
  * and debugging; the linear entry points never call it and never expand
  * weights in device memory.
  */
-w4a16_status w4a16_dequant(const uint32_t* qweight, const void* scales_f16, const uint32_t* zeros,
+W4A16_API w4a16_status w4a16_dequant(const uint32_t* qweight, const void* scales_f16, const uint32_t* zeros,
                            int64_t N, int64_t K, int G, float* w_out, w4a16_stream_t stream);
 
 /* ---- the layer ---------------------------------------------------------------
@@ -120,7 +126,7 @@ w4a16_status w4a16_dequant(const uint32_t* qweight, const void* scales_f16, cons
  * stops being the right answer").
  * x and y must not overlap the weight buffers.
  */
-w4a16_status w4a16_linear(const void* x_bf16, const uint32_t* qweight, const void* scales_f16,
+W4A16_API w4a16_status w4a16_linear(const void* x_bf16, const uint32_t* qweight, const void* scales_f16,
                           const uint32_t* zeros, int64_t M, int64_t N, int64_t K, int G,
                           void* y_bf16, w4a16_stream_t stream);
 
@@ -132,7 +138,7 @@ w4a16_status w4a16_linear(const void* x_bf16, const uint32_t* qweight, const voi
  * page's section 2 ("Moving fewer bytes can make decode faster") workload.
  * M <= 16 runs the dual GEMV; larger M runs the GEMM once per projection.
  */
-w4a16_status w4a16_linear_dual(const void* x_bf16,
+W4A16_API w4a16_status w4a16_linear_dual(const void* x_bf16,
                                const uint32_t* qweight_gate, const void* scales_gate,
                                const uint32_t* zeros_gate,
                                const uint32_t* qweight_up, const void* scales_up,
@@ -148,10 +154,10 @@ w4a16_status w4a16_linear_dual(const void* x_bf16,
  *                      x does not fit the kernel's shared memory.
  *   w4a16_linear_gemm: the tensor-core kernel, any M >= 1.
  */
-w4a16_status w4a16_linear_gemv(const void* x_bf16, const uint32_t* qweight, const void* scales_f16,
+W4A16_API w4a16_status w4a16_linear_gemv(const void* x_bf16, const uint32_t* qweight, const void* scales_f16,
                                const uint32_t* zeros, int64_t M, int64_t N, int64_t K, int G,
                                void* y_bf16, w4a16_stream_t stream);
-w4a16_status w4a16_linear_gemm(const void* x_bf16, const uint32_t* qweight, const void* scales_f16,
+W4A16_API w4a16_status w4a16_linear_gemm(const void* x_bf16, const uint32_t* qweight, const void* scales_f16,
                                const uint32_t* zeros, int64_t M, int64_t N, int64_t K, int G,
                                void* y_bf16, w4a16_stream_t stream);
 
@@ -159,7 +165,7 @@ w4a16_status w4a16_linear_gemm(const void* x_bf16, const uint32_t* qweight, cons
  * Which kernel w4a16_linear would run for this shape: 1 = GEMV, 2 = GEMM,
  * 0 = the shape is rejected.  Host-only, no device access.
  */
-int w4a16_linear_path(int64_t M, int64_t N, int64_t K, int G);
+W4A16_API int w4a16_linear_path(int64_t M, int64_t N, int64_t K, int G);
 
 /*
  * Every bounded wait inside the kernels (a tensor-core pipeline barrier that
@@ -169,7 +175,7 @@ int w4a16_linear_path(int64_t M, int64_t N, int64_t K, int G);
  * give-up since the last call (and clears the word), else W4A16_OK.  *detail
  * (optional) receives the raw word.
  */
-w4a16_status w4a16_device_status(uint32_t* detail);
+W4A16_API w4a16_status w4a16_device_status(uint32_t* detail);
 
 #ifdef __cplusplus
 }

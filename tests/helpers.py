@@ -1,0 +1,60 @@
+"""Shared helpers for the GPU parity tests: move oracle-packed data to the
+device, and the output tolerance.
+
+Tolerance (the output is BF16, compared with the unrounded FP64 oracle):
+  * relative L2 error ||y - y_ref|| / ||y_ref|| <= 2e-3;
+  * per element |y - y_ref| <= 1e-2 * rms(y_ref) + ulp_bf16(y_ref) / 2.
+The half-ulp term is the output rounding itself: a correctly rounded BF16
+result can already differ from y_ref by half a BF16 ulp, which for the
+largest outputs exceeds 1e-2 * rms(y_ref), so the per-element bound is read
+as "1e-2 * rms beyond the unavoidable output rounding".
+"""
+import numpy as np
+import torch
+
+REL_L2 = 2e-3
+MAXABS_RMS = 1e-2
+
+
+def dev_packed(q, s, z):
+    """Oracle numpy arrays -> device tensors in the binding's dtypes."""
+    return (torch.from_numpy(q.view(np.int32)).cuda(), torch.from_numpy(s.view(np.float16)).cuda(),
+            torch.from_numpy(z.view(np.int32)).cuda())
+
+
+def host_u32(t):
+    return t.cpu().numpy().view(np.uint32)
+
+
+def host_u16(t):
+    return t.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16_ulp(v):
+    """ulp of BF16 at |v| (8 significant bits)."""
+    v = np.abs(np.asarray(v, np.float64))
+    _, e = np.frexp(np.where(v == 0, 1e-300, v))
+    return np.ldexp(1.0, e - 8)
+
+
+def y_to_f64(y):
+    return y.float().cpu().numpy().astype(np.float64)
+
+
+def error_stats(y, y_ref):
+    """(relL2, max |err| / rms, max over elements of |err| / bound); bound <= 1 passes."""
+    y = y_to_f64(y) if isinstance(y, torch.Tensor) else np.asarray(y, np.float64)
+    y_ref = np.asarray(y_ref, np.float64)
+    err = np.abs(y - y_ref)
+    nrm = np.linalg.norm(y_ref)
+    rel = np.linalg.norm(y - y_ref) / nrm if nrm > 0 else float(np.linalg.norm(y - y_ref))
+    rms = np.sqrt(np.mean(y_ref ** 2)) if y_ref.size else 0.0
+    bound = MAXABS_RMS * rms + 0.5 * bf16_ulp(y_ref)
+    return rel, (err.max() / rms if rms > 0 else 0.0), float((err / bound).max()) if y_ref.size else 0.0
+
+
+def assert_close(y, y_ref, what=""):
+    rel, maxrel, worst = error_stats(y, y_ref)
+    assert rel <= REL_L2, f"{what}: relL2 {rel:.3e} > {REL_L2}"
+    assert worst <= 1.0, f"{what}: max-abs bound exceeded by x{worst:.3f} (max|err|/rms = {maxrel:.3e})"
+    return rel, maxrel

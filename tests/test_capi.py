@@ -1,0 +1,108 @@
+"""The C-ABI library on a machine without a GPU: it loads, exports every
+symbol include/w4a16.h declares, and rejects bad arguments on the host before
+touching any device (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import w4a16_weight_only_linear_b300 as w4
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "w4a16.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"W4A16_API\s+[\w\s\*]+?\b(w4a16_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    for required in ("w4a16_pack", "w4a16_linear", "w4a16_linear_dual", "w4a16_dequant", "w4a16_status_string"):
+        assert required in names
+    assert set(names) == set(w4.EXPORTS), "binding and header disagree"
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(w4.LIB_PATH)
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_library_exports_nothing_else():
+    # the build hides everything but the declared C entry points
+    out = os.popen(f"nm -D --defined-only {w4.LIB_PATH}").read()
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    ours = {s for s in exported if s.startswith("w4a16")}
+    assert ours == set(declared_symbols())
+
+
+def test_status_strings():
+    assert w4.w4a16_status_string(0) == "W4A16_OK"
+    for code, name in w4.STATUS_NAMES.items():
+        assert w4.w4a16_status_string(code) == name
+    assert w4.w4a16_status_string(99) == "W4A16_ERR_UNKNOWN"
+
+
+@pytest.mark.parametrize("K,G", [(4096, 128), (5120, 128), (13824, 128), (5120, 32), (5120, 64), (5120, 256),
+                                 (64, 32), (96, 32)])
+def test_layout_helpers(K, G):
+    ng = K // G
+    assert w4.w4a16_qweight_ld(K) == K // 8
+    lds = w4.w4a16_scales_ld(K, G)
+    ldz = w4.w4a16_zeros_ld(K, G)
+    assert lds >= ng and lds % 8 == 0 and lds - ng < 8            # 16-byte rows of halves
+    assert ldz >= (ng + 7) // 8 and ldz % 4 == 0 and ldz - (ng + 7) // 8 < 4
+
+
+def _call_linear(fn, x=1 << 12, q=1 << 12, s=1 << 12, z=1 << 12, M=1, N=64, K=256, G=128, y=1 << 12):
+    # fake, never-dereferenced addresses: every call here must fail validation
+    v = ctypes.c_void_p
+    return getattr(w4._lib, fn)(v(x), v(q), v(s), v(z), M, N, K, G, v(y), v(0))
+
+
+@pytest.mark.parametrize("fn", ["w4a16_linear", "w4a16_linear_gemv", "w4a16_linear_gemm"])
+def test_linear_argument_errors(fn):
+    assert _call_linear(fn, G=48) == 2                  # unsupported group size
+    assert _call_linear(fn, G=512) == 2
+    assert _call_linear(fn, K=200) == 1                 # K % G
+    assert _call_linear(fn, N=60) == 1                  # N % 8
+    assert _call_linear(fn, K=0) == 1
+    assert _call_linear(fn, M=-1) == 1
+    assert _call_linear(fn, x=0) == 1                   # null pointers
+    assert _call_linear(fn, q=0) == 1
+    assert _call_linear(fn, y=0) == 1
+    assert _call_linear(fn, x=(1 << 12) + 8) == 3      # misaligned
+    assert _call_linear(fn, s=(1 << 12) + 2) == 3
+    assert _call_linear(fn, M=0) == 0                   # empty problem: nothing launched
+    assert _call_linear(fn, N=0) == 0
+
+
+def test_pack_and_dequant_argument_errors():
+    v = ctypes.c_void_p
+    a = v(1 << 12)
+    assert w4._lib.w4a16_pack(a, 64, 256, 100, a, a, a, v(0)) == 2
+    assert w4._lib.w4a16_pack(a, 60, 256, 128, a, a, a, v(0)) == 1
+    assert w4._lib.w4a16_pack(v(0), 64, 256, 128, a, a, a, v(0)) == 1
+    assert w4._lib.w4a16_pack(v((1 << 12) + 4), 64, 256, 128, a, a, a, v(0)) == 3
+    assert w4._lib.w4a16_pack(a, 0, 256, 128, a, a, a, v(0)) == 0
+    assert w4._lib.w4a16_dequant(a, a, a, 64, 250, 128, a, v(0)) == 1
+    assert w4._lib.w4a16_dequant(a, a, a, 64, 256, 128, v(0), v(0)) == 1
+
+
+def test_dual_argument_errors():
+    v = ctypes.c_void_p
+    a = v(1 << 12)
+    f = w4._lib.w4a16_linear_dual
+    assert f(a, a, a, a, a, a, a, 1, 64, 256, 96, a, a, v(0)) == 2
+    assert f(a, a, a, a, v(0), a, a, 1, 64, 256, 128, a, a, v(0)) == 1
+    assert f(a, a, a, a, a, a, a, 1, 64, 256, 128, a, v((1 << 12) + 2), v(0)) == 3
+    assert f(a, a, a, a, a, a, a, 0, 64, 256, 128, a, a, v(0)) == 0
+
+
+def test_path_query_rejects_bad_shapes():
+    assert w4.w4a16_linear_path(1, 60, 256, 128) == 0
+    assert w4.w4a16_linear_path(1, 64, 250, 128) == 0
+    assert w4.w4a16_linear_path(1, 64, 256, 100) == 0

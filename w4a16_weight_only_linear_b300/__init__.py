@@ -1,0 +1,194 @@
+"""B300 (sm_103a) W4A16 weight-only linear layer -- Python binding.
+
+A thin ctypes binding of ``libw4a16.so`` (declared in ``include/w4a16.h``).
+Every function here only marshals arguments: checks dtypes, devices and
+shapes of torch tensors, allocates outputs with torch when the caller does
+not pass them, and forwards raw device pointers plus the current CUDA stream
+to the C entry point of the same name.  All arithmetic runs in the library's
+CUDA kernels; there is no fallback path.  Importing this module fails loudly
+if the library has not been built (``python -m w4a16_weight_only_linear_b300.build``).
+
+Packed format (see the header): qweight uint32 [N, K/8], scales FP16
+[N, ldS], zeros uint32 [N, ldZ]; W_hat = (q - z) * s; y = x * W_hat^T.
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libw4a16.so")
+
+STATUS_NAMES = {
+    0: "W4A16_OK", 1: "W4A16_ERR_INVALID_ARG", 2: "W4A16_ERR_UNSUPPORTED", 3: "W4A16_ERR_MISALIGNED",
+    4: "W4A16_ERR_CUDA", 5: "W4A16_ERR_TIMEOUT", 6: "W4A16_ERR_NO_DEVICE",
+}
+
+# Entry points of the C ABI, with their ctypes signatures.
+_vp, _i64, _i32, _u32p = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+EXPORTS = {
+    "w4a16_status_string": ([_i32], ctypes.c_char_p),
+    "w4a16_qweight_ld": ([_i64], _i64),
+    "w4a16_scales_ld": ([_i64, _i32], _i64),
+    "w4a16_zeros_ld": ([_i64, _i32], _i64),
+    "w4a16_pack": ([_vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp], _i32),
+    "w4a16_dequant": ([_vp, _vp, _vp, _i64, _i64, _i32, _vp, _vp], _i32),
+    "w4a16_linear": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp], _i32),
+    "w4a16_linear_dual": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp, _vp], _i32),
+    "w4a16_linear_gemv": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp], _i32),
+    "w4a16_linear_gemm": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp], _i32),
+    "w4a16_linear_path": ([_i64, _i64, _i64, _i32], _i32),
+    "w4a16_device_status": ([_vp], _i32),
+}
+
+
+class W4A16Error(RuntimeError):
+    """A non-zero status returned by the library."""
+
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn}: {STATUS_NAMES.get(status, status)}")
+
+
+def _load_library():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with `python -m w4a16_weight_only_linear_b300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (args, res) in EXPORTS.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = res
+    return lib
+
+
+_lib = _load_library()
+
+
+def _check(fn, status):
+    if status != 0:
+        raise W4A16Error(fn, status)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dev(t, dtype, name):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+# ---- layout helpers ------------------------------------------------------------
+
+def w4a16_qweight_ld(K):
+    return _lib.w4a16_qweight_ld(K)
+
+
+def w4a16_scales_ld(K, G):
+    return _lib.w4a16_scales_ld(K, G)
+
+
+def w4a16_zeros_ld(K, G):
+    return _lib.w4a16_zeros_ld(K, G)
+
+
+def w4a16_status_string(status):
+    return _lib.w4a16_status_string(status).decode()
+
+
+def packed_shapes(N, K, G):
+    """Shapes of (qweight, scales, zeros) for an [N,K] weight."""
+    return (N, w4a16_qweight_ld(K)), (N, w4a16_scales_ld(K, G)), (N, w4a16_zeros_ld(K, G))
+
+
+def empty_packed(N, K, G, device="cuda"):
+    qs, ss, zs = packed_shapes(N, K, G)
+    return (torch.empty(qs, dtype=torch.int32, device=device), torch.empty(ss, dtype=torch.float16, device=device),
+            torch.empty(zs, dtype=torch.int32, device=device))
+
+
+# ---- entry points -----------------------------------------------------------------
+
+def w4a16_pack(w, G, out=None, stream=None):
+    """FP16 W [N,K] (CUDA) -> (qweight int32 [N,K/8], scales fp16 [N,ldS], zeros int32 [N,ldZ]).
+
+    The uint32 words travel as int32 tensors (torch has no uint32 arithmetic);
+    the bits are identical."""
+    N, K = w.shape
+    q, s, z = out if out is not None else empty_packed(N, K, G, w.device)
+    _check("w4a16_pack", _lib.w4a16_pack(_dev(w, torch.float16, "w"), N, K, G, _dev(q, torch.int32, "qweight"),
+                                         _dev(s, torch.float16, "scales"), _dev(z, torch.int32, "zeros"),
+                                         _stream(stream)))
+    return q, s, z
+
+
+def w4a16_dequant(q, s, z, N, K, G, out=None, stream=None):
+    """W_hat FP32 [N,K] = (q - z) * s, through the kernels' unpack routine (checking aid)."""
+    if out is None:
+        out = torch.empty((N, K), dtype=torch.float32, device=q.device)
+    _check("w4a16_dequant", _lib.w4a16_dequant(_dev(q, torch.int32, "qweight"), _dev(s, torch.float16, "scales"),
+                                               _dev(z, torch.int32, "zeros"), N, K, G,
+                                               _dev(out, torch.float32, "out"), _stream(stream)))
+    return out
+
+
+def _linear(fn, x, q, s, z, N, G, out, stream):
+    M, K = x.shape
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _check(fn, getattr(_lib, fn)(_dev(x, torch.bfloat16, "x"), _dev(q, torch.int32, "qweight"),
+                                 _dev(s, torch.float16, "scales"), _dev(z, torch.int32, "zeros"), M, N, K, G,
+                                 _dev(out, torch.bfloat16, "y"), _stream(stream)))
+    return out
+
+
+def w4a16_linear(x, q, s, z, G, out=None, stream=None):
+    """y BF16 [M,N] = x BF16 [M,K] * W_hat^T (N taken from qweight's rows)."""
+    return _linear("w4a16_linear", x, q, s, z, q.shape[0], G, out, stream)
+
+
+def w4a16_linear_gemv(x, q, s, z, G, out=None, stream=None):
+    """Decode kernel only (M <= 16)."""
+    return _linear("w4a16_linear_gemv", x, q, s, z, q.shape[0], G, out, stream)
+
+
+def w4a16_linear_gemm(x, q, s, z, G, out=None, stream=None):
+    """Tensor-core kernel only (any M)."""
+    return _linear("w4a16_linear_gemm", x, q, s, z, q.shape[0], G, out, stream)
+
+
+def w4a16_linear_dual(x, gate, up, G, out=None, stream=None):
+    """(y_gate, y_up) = (x * W_hat_gate^T, x * W_hat_up^T); gate/up = (qweight, scales, zeros)."""
+    M, K = x.shape
+    N = gate[0].shape[0]
+    if out is None:
+        out = (torch.empty((M, N), dtype=torch.bfloat16, device=x.device),
+               torch.empty((M, N), dtype=torch.bfloat16, device=x.device))
+    yg, yu = out
+    _check("w4a16_linear_dual", _lib.w4a16_linear_dual(
+        _dev(x, torch.bfloat16, "x"),
+        _dev(gate[0], torch.int32, "qweight_gate"), _dev(gate[1], torch.float16, "scales_gate"),
+        _dev(gate[2], torch.int32, "zeros_gate"),
+        _dev(up[0], torch.int32, "qweight_up"), _dev(up[1], torch.float16, "scales_up"),
+        _dev(up[2], torch.int32, "zeros_up"),
+        M, N, K, G, _dev(yg, torch.bfloat16, "y_gate"), _dev(yu, torch.bfloat16, "y_up"), _stream(stream)))
+    return yg, yu
+
+
+def w4a16_linear_path(M, N, K, G):
+    """1 = decode GEMV, 2 = tensor-core GEMM, 0 = rejected."""
+    return _lib.w4a16_linear_path(M, N, K, G)
+
+
+def w4a16_device_status():
+    """Synchronise; raise if a kernel's bounded wait gave up since the last call."""
+    word = ctypes.c_uint32(0)
+    _check("w4a16_device_status", _lib.w4a16_device_status(ctypes.byref(word)))
+    return word.value

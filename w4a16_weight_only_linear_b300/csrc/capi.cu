@@ -1,0 +1,174 @@
+// capi.cu -- the extern "C" boundary declared in include/w4a16.h.
+//
+// Every entry point validates its arguments on the host and returns a status
+// before anything is launched; kernels are enqueued on the caller's stream.
+// The runtime chooses a kernel by problem shape, the way a backend picks a
+// direct kernel for a packed format (zhuai.tech "Quantization Is Not a Zip
+// File", section 1: the backend selects a kernel by format and device).
+#include <cuda_runtime.h>
+
+#include "../../include/w4a16.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace {
+
+using w4a16::GemvMat;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool group_ok(int G) { return G == 32 || G == 64 || G == 128 || G == 256; }
+
+// Largest element count an index may reach (kernels use 64-bit row offsets,
+// 32-bit group and step counters).
+constexpr int64_t kMaxDim = int64_t(1) << 30;
+
+w4a16_status check_weight_shape(int64_t N, int64_t K, int G) {
+    if (!group_ok(G)) return W4A16_ERR_UNSUPPORTED;
+    if (N < 0 || K <= 0 || N > kMaxDim || K > kMaxDim) return W4A16_ERR_INVALID_ARG;
+    if (K % G != 0 || N % 8 != 0) return W4A16_ERR_INVALID_ARG;
+    return W4A16_OK;
+}
+
+w4a16_status check_weights(const uint32_t* q, const void* s, const uint32_t* z) {
+    if (!q || !s || !z) return W4A16_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(s) || !aligned16(z)) return W4A16_ERR_MISALIGNED;
+    return W4A16_OK;
+}
+
+w4a16_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return W4A16_OK;
+    if (e == cudaErrorNotSupported) return W4A16_ERR_UNSUPPORTED;
+    return W4A16_ERR_CUDA;
+}
+
+// Path for a shape whose arguments are valid: 1 = GEMV, 2 = GEMM.
+int choose_path(int64_t M, int64_t K, int G, int ntiles) {
+    if (M <= 16) {
+        const size_t need = w4a16::gemv_smem_bytes(M, K, G, ntiles);
+        const size_t have = w4a16::device_smem_optin();
+        if (need != 0 && (have == 0 || need <= have)) return 1;
+    }
+    return 2;
+}
+
+w4a16_status linear_common(const void* x, const uint32_t* q, const void* s, const uint32_t* z, int64_t M,
+                           int64_t N, int64_t K, int G, void* y, w4a16_stream_t stream, int force) {
+    w4a16_status st = check_weight_shape(N, K, G);
+    if (st != W4A16_OK) return st;
+    if (M < 0 || M > kMaxDim) return W4A16_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return W4A16_OK;
+    if ((st = check_weights(q, s, z)) != W4A16_OK) return st;
+    if (!x || !y) return W4A16_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(y)) return W4A16_ERR_MISALIGNED;
+    int path = force ? force : choose_path(M, K, G, 1);
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    GemvMat mat{q, s, z, y};
+    if (path == 1) {
+        if (M > 16) return W4A16_ERR_UNSUPPORTED;
+        const size_t need = w4a16::gemv_smem_bytes(M, K, G, 1);
+        const size_t have = w4a16::device_smem_optin();
+        if (have != 0 && need > have) return W4A16_ERR_UNSUPPORTED;
+        return from_cuda(w4a16::launch_gemv(x, &mat, 1, M, N, K, G, cs));
+    }
+    return from_cuda(w4a16::launch_gemm(x, mat, M, N, K, G, cs));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* w4a16_status_string(w4a16_status status) {
+    switch (status) {
+        case W4A16_OK: return "W4A16_OK";
+        case W4A16_ERR_INVALID_ARG: return "W4A16_ERR_INVALID_ARG";
+        case W4A16_ERR_UNSUPPORTED: return "W4A16_ERR_UNSUPPORTED";
+        case W4A16_ERR_MISALIGNED: return "W4A16_ERR_MISALIGNED";
+        case W4A16_ERR_CUDA: return "W4A16_ERR_CUDA";
+        case W4A16_ERR_TIMEOUT: return "W4A16_ERR_TIMEOUT";
+        case W4A16_ERR_NO_DEVICE: return "W4A16_ERR_NO_DEVICE";
+    }
+    return "W4A16_ERR_UNKNOWN";
+}
+
+int64_t w4a16_qweight_ld(int64_t K) { return w4a16::qweight_ld(K); }
+int64_t w4a16_scales_ld(int64_t K, int G) { return G > 0 ? w4a16::scales_ld(K, G) : 0; }
+int64_t w4a16_zeros_ld(int64_t K, int G) { return G > 0 ? w4a16::zeros_ld(K, G) : 0; }
+
+w4a16_status w4a16_pack(const void* w_f16, int64_t N, int64_t K, int G, uint32_t* qweight, void* scales_f16,
+                        uint32_t* zeros, w4a16_stream_t stream) {
+    w4a16_status st = check_weight_shape(N, K, G);
+    if (st != W4A16_OK) return st;
+    if (N == 0) return W4A16_OK;
+    if ((st = check_weights(qweight, scales_f16, zeros)) != W4A16_OK) return st;
+    if (!w_f16) return W4A16_ERR_INVALID_ARG;
+    if (!aligned16(w_f16)) return W4A16_ERR_MISALIGNED;
+    return from_cuda(w4a16::launch_pack(w_f16, N, K, G, qweight, scales_f16, zeros,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w4a16_dequant(const uint32_t* qweight, const void* scales_f16, const uint32_t* zeros, int64_t N,
+                           int64_t K, int G, float* w_out, w4a16_stream_t stream) {
+    w4a16_status st = check_weight_shape(N, K, G);
+    if (st != W4A16_OK) return st;
+    if (N == 0) return W4A16_OK;
+    if ((st = check_weights(qweight, scales_f16, zeros)) != W4A16_OK) return st;
+    if (!w_out) return W4A16_ERR_INVALID_ARG;
+    if (!aligned16(w_out)) return W4A16_ERR_MISALIGNED;
+    return from_cuda(w4a16::launch_dequant(qweight, scales_f16, zeros, N, K, G, w_out,
+                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w4a16_linear(const void* x_bf16, const uint32_t* qweight, const void* scales_f16,
+                          const uint32_t* zeros, int64_t M, int64_t N, int64_t K, int G, void* y_bf16,
+                          w4a16_stream_t stream) {
+    return linear_common(x_bf16, qweight, scales_f16, zeros, M, N, K, G, y_bf16, stream, 0);
+}
+
+w4a16_status w4a16_linear_gemv(const void* x_bf16, const uint32_t* qweight, const void* scales_f16,
+                               const uint32_t* zeros, int64_t M, int64_t N, int64_t K, int G, void* y_bf16,
+                               w4a16_stream_t stream) {
+    return linear_common(x_bf16, qweight, scales_f16, zeros, M, N, K, G, y_bf16, stream, 1);
+}
+
+w4a16_status w4a16_linear_gemm(const void* x_bf16, const uint32_t* qweight, const void* scales_f16,
+                               const uint32_t* zeros, int64_t M, int64_t N, int64_t K, int G, void* y_bf16,
+                               w4a16_stream_t stream) {
+    return linear_common(x_bf16, qweight, scales_f16, zeros, M, N, K, G, y_bf16, stream, 2);
+}
+
+w4a16_status w4a16_linear_dual(const void* x_bf16, const uint32_t* qweight_gate, const void* scales_gate,
+                               const uint32_t* zeros_gate, const uint32_t* qweight_up, const void* scales_up,
+                               const uint32_t* zeros_up, int64_t M, int64_t N, int64_t K, int G,
+                               void* y_gate_bf16, void* y_up_bf16, w4a16_stream_t stream) {
+    w4a16_status st = check_weight_shape(N, K, G);
+    if (st != W4A16_OK) return st;
+    if (M < 0 || M > kMaxDim) return W4A16_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return W4A16_OK;
+    if ((st = check_weights(qweight_gate, scales_gate, zeros_gate)) != W4A16_OK) return st;
+    if ((st = check_weights(qweight_up, scales_up, zeros_up)) != W4A16_OK) return st;
+    if (!x_bf16 || !y_gate_bf16 || !y_up_bf16) return W4A16_ERR_INVALID_ARG;
+    if (!aligned16(x_bf16) || !aligned16(y_gate_bf16) || !aligned16(y_up_bf16)) return W4A16_ERR_MISALIGNED;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const GemvMat mats[2] = {{qweight_gate, scales_gate, zeros_gate, y_gate_bf16},
+                             {qweight_up, scales_up, zeros_up, y_up_bf16}};
+    if (choose_path(M, K, G, 2) == 1) return from_cuda(w4a16::launch_gemv(x_bf16, mats, 2, M, N, K, G, cs));
+    st = from_cuda(w4a16::launch_gemm(x_bf16, mats[0], M, N, K, G, cs));
+    if (st != W4A16_OK) return st;
+    return from_cuda(w4a16::launch_gemm(x_bf16, mats[1], M, N, K, G, cs));
+}
+
+int w4a16_linear_path(int64_t M, int64_t N, int64_t K, int G) {
+    if (check_weight_shape(N, K, G) != W4A16_OK || M < 0) return 0;
+    return choose_path(M, K, G, 1);
+}
+
+w4a16_status w4a16_device_status(uint32_t* detail) {
+    uint32_t word = 0;
+    cudaError_t e = w4a16::read_and_clear_status(&word);
+    if (detail) *detail = word;
+    if (e != cudaSuccess) return W4A16_ERR_CUDA;
+    return word ? W4A16_ERR_TIMEOUT : W4A16_OK;
+}
+
+}  // extern "C"

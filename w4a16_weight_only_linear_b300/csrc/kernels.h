@@ -1,0 +1,38 @@
+// kernels.h -- internal launchers behind the C ABI (not part of the public header).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace w4a16 {
+
+cudaError_t launch_pack(const void* w, int64_t N, int64_t K, int G, uint32_t* qw, void* sc, uint32_t* zr,
+                        cudaStream_t stream);
+cudaError_t launch_dequant(const uint32_t* qw, const void* sc, const uint32_t* zr, int64_t N, int64_t K, int G,
+                           float* out, cudaStream_t stream);
+
+// One packed weight matrix and the output it feeds.
+struct GemvMat {
+    const uint32_t* q;
+    const void* s;
+    const uint32_t* z;
+    void* y;
+};
+
+// Shared memory the GEMV needs for this shape (bytes), or 0 when M is out of range.
+size_t gemv_smem_bytes(int64_t M, int64_t K, int G, int ntiles);
+// Largest dynamic shared memory a block may use on the current device.
+size_t device_smem_optin();
+
+// y_i = x * W_hat_i^T for one matrix (nmat = 1) or two matrices sharing x (nmat = 2).
+cudaError_t launch_gemv(const void* x, const GemvMat* mats, int nmat, int64_t M, int64_t N, int64_t K, int G,
+                        cudaStream_t stream);
+
+// Tensor-core path (any M); returns cudaErrorNotSupported until built for the shape.
+cudaError_t launch_gemm(const void* x, const GemvMat& mat, int64_t M, int64_t N, int64_t K, int G,
+                        cudaStream_t stream);
+
+// Per-device status word written by kernels whose bounded waits gave up.
+cudaError_t read_and_clear_status(uint32_t* word);
+
+}  // namespace w4a16

@@ -1,0 +1,158 @@
+// pack.cu -- FP16 weight -> packed 4-bit codes + FP16 scales + 4-bit zeros,
+// and the exact dequantisation used by the tests.
+//
+// Quantiser: group-wise asymmetric min-max over G consecutive input channels
+// of one output column (klaylearn.com glossary "Weight-Only Quantisation",
+// main body: small integers plus scale and zero-point per group; instagit
+// "Comparison of Quantization Methods", section "Practical Code Examples":
+// asymmetric codes reconstruct as (q - zero_point) * scale; zhuai.tech
+// "Quantization Is Not a Zip File", section 3: groups of 32..256).
+//   lo = min(0, min w), hi = max(0, max w)
+//   s  = RNE_fp16((hi - lo) / 15) in IEEE binary32; s == 0 -> s = 1, z = 0
+//   z  = clamp(rne(-lo / s), 0, 15),  q = clamp(rne(w / s) + z, 0, 15)
+// All divisions are correctly rounded binary32 (the library is built without
+// fast-math), so the codes are bit-identical to any IEEE implementation.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace w4a16 {
+
+// One warp per weight row; the row's groups are processed in order.  Lane l
+// holds the G/32 consecutive weights l*G/32 .. of the current group.
+template <int G>
+__global__ void __launch_bounds__(256) pack_kernel(const __half* __restrict__ w, int64_t N, int64_t K,
+                                                   uint32_t* __restrict__ qw, __half* __restrict__ sc,
+                                                   uint32_t* __restrict__ zr) {
+    constexpr int PER = G / 32;              // weights per lane: 1, 2, 4, 8
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    if (row >= N) return;                    // uniform per warp
+    const int64_t ngroups = K / G;
+    const int64_t ldq = qweight_ld(K), lds = scales_ld(K, G), ldz = zeros_ld(K, G);
+    const __half* wrow = w + row * K;
+    uint32_t* qrow = qw + row * ldq;
+    __half* srow = sc + row * lds;
+    uint32_t* zrow = zr + row * ldz;
+
+    uint32_t zword = 0;
+    for (int64_t g = 0; g < ngroups; ++g) {
+        const __half* src = wrow + g * G + lane * PER;
+        float v[PER];
+        if constexpr (PER == 8) {
+            uint4 u = *reinterpret_cast<const uint4*>(src);
+            const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                v[2 * i] = __half2float(__ushort_as_half((unsigned short)(uw[i] & 0xFFFF)));
+                v[2 * i + 1] = __half2float(__ushort_as_half((unsigned short)(uw[i] >> 16)));
+            }
+        } else if constexpr (PER == 4) {
+            uint2 u = *reinterpret_cast<const uint2*>(src);
+            v[0] = __half2float(__ushort_as_half((unsigned short)(u.x & 0xFFFF)));
+            v[1] = __half2float(__ushort_as_half((unsigned short)(u.x >> 16)));
+            v[2] = __half2float(__ushort_as_half((unsigned short)(u.y & 0xFFFF)));
+            v[3] = __half2float(__ushort_as_half((unsigned short)(u.y >> 16)));
+        } else if constexpr (PER == 2) {
+            uint32_t u = *reinterpret_cast<const uint32_t*>(src);
+            v[0] = __half2float(__ushort_as_half((unsigned short)(u & 0xFFFF)));
+            v[1] = __half2float(__ushort_as_half((unsigned short)(u >> 16)));
+        } else {
+            v[0] = __half2float(src[0]);
+        }
+        float lo = 0.0f, hi = 0.0f;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            lo = fminf(lo, v[i]);
+            hi = fmaxf(hi, v[i]);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            lo = fminf(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, off));
+            hi = fmaxf(hi, __shfl_xor_sync(0xFFFFFFFFu, hi, off));
+        }
+        const float range = __fsub_rn(hi, lo);
+        __half sh = __float2half_rn(__fdiv_rn(range, 15.0f));
+        float s = __half2float(sh);
+        int zp = 0;
+        if (s == 0.0f) {                     // all-zero (or underflowing) group
+            sh = __float2half_rn(1.0f);
+            s = 1.0f;
+        } else {
+            zp = min(max(__float2int_rn(__fdiv_rn(-lo, s)), 0), 15);
+        }
+        uint32_t bits = 0;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int c = min(max(__float2int_rn(__fdiv_rn(v[i], s)) + zp, 0), 15);
+            bits |= (uint32_t)c << (4 * ((lane * PER + i) & 7));
+        }
+        if constexpr (PER < 8) {             // lanes sharing one word OR their nibbles
+#pragma unroll
+            for (int off = 1; off < 8 / PER; off <<= 1) bits |= __shfl_xor_sync(0xFFFFFFFFu, bits, off);
+        }
+        if (((lane * PER) & 7) == 0) qrow[(g * G + lane * PER) / 8] = bits;
+        if (lane == 0) srow[g] = sh;
+        zword |= (uint32_t)zp << (4 * (g & 7));
+        if ((g & 7) == 7 || g == ngroups - 1) {
+            if (lane == 0) zrow[g / 8] = zword;
+            zword = 0;
+        }
+    }
+    for (int64_t i = ngroups + lane; i < lds; i += 32) srow[i] = __ushort_as_half((unsigned short)0);
+    for (int64_t i = (ngroups + 7) / 8 + lane; i < ldz; i += 32) zrow[i] = 0u;
+}
+
+// W_hat = (q - z) * s through the same in-register nibble expansion the
+// linear kernels use (BF16 128 + q), then exact FP32 arithmetic.
+// One thread per packed word (8 outputs).
+__global__ void __launch_bounds__(256) dequant_kernel(const uint32_t* __restrict__ qw, const __half* __restrict__ sc,
+                                                      const uint32_t* __restrict__ zr, int64_t N, int64_t K, int G,
+                                                      float* __restrict__ out) {
+    const int64_t words = K / 8;
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= N * words) return;
+    const int64_t n = idx / words, w8 = idx % words;
+    const int64_t g = (w8 * 8) / G;
+    const uint32_t word = qw[n * qweight_ld(K) + w8];
+    const float s = __half2float(sc[n * scales_ld(K, G) + g]);
+    const float off = 128.0f + (float)nibble(zr[n * zeros_ld(K, G) + g / 8], (int)(g & 7));
+    uint32_t p[4];
+    codes_to_bf16x2(word, p);
+    float o[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        o[j] = __fmul_rn(__fsub_rn(bf16lo_to_f32(p[j]), off), s);
+        o[j + 4] = __fmul_rn(__fsub_rn(bf16hi_to_f32(p[j]), off), s);
+    }
+    float4* dst = reinterpret_cast<float4*>(out + n * K + w8 * 8);
+    dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+}
+
+cudaError_t launch_pack(const void* w, int64_t N, int64_t K, int G, uint32_t* qw, void* sc, uint32_t* zr,
+                        cudaStream_t stream) {
+    const int warps = 8;
+    const dim3 block(32 * warps);
+    const dim3 grid((unsigned)((N + warps - 1) / warps));
+    const __half* wp = static_cast<const __half*>(w);
+    __half* sp = static_cast<__half*>(sc);
+    switch (G) {
+        case 32: pack_kernel<32><<<grid, block, 0, stream>>>(wp, N, K, qw, sp, zr); break;
+        case 64: pack_kernel<64><<<grid, block, 0, stream>>>(wp, N, K, qw, sp, zr); break;
+        case 128: pack_kernel<128><<<grid, block, 0, stream>>>(wp, N, K, qw, sp, zr); break;
+        case 256: pack_kernel<256><<<grid, block, 0, stream>>>(wp, N, K, qw, sp, zr); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dequant(const uint32_t* qw, const void* sc, const uint32_t* zr, int64_t N, int64_t K, int G,
+                           float* out, cudaStream_t stream) {
+    const int64_t total = N * (K / 8);
+    const dim3 block(256);
+    const dim3 grid((unsigned)((total + 255) / 256));
+    dequant_kernel<<<grid, block, 0, stream>>>(qw, static_cast<const __half*>(sc), zr, N, K, G, out);
+    return cudaGetLastError();
+}
+
+}  // namespace w4a16
