@@ -15,9 +15,8 @@ Both are whole-job figures with inputs resident in HBM; "e2e" repeats the
 measurement through the same C entry points with pinned host buffers and the
 host<->device copies inside the timed region.
 
-Cold L2: each matrix has 2 device copies used alternately, so every launch
-reads weights that at least 3 other matrices' worth of traffic (> 360 MB,
-L2 = 126 MB) has passed since their last use.
+Cold L2: each matrix has 3 device copies used in turn, so between two reads
+of the same copy at least 244 MB of other weights (L2 = 126 MB) stream by.
 
 `--impl reference` times the CPU oracle (the plain C implementation the tests
 compare against) on the host cores: the decode GEMVs in full, the prefill
@@ -156,7 +155,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     wk = wl.WORKLOADS[WORKLOAD]
     pk = peaks()
-    copies = 2
+    copies = 3
 
     # weights: generated once per matrix (seeded), packed on the device; each rank
     # is an independent replica (the layer has no exchange step on one GPU)
@@ -180,40 +179,48 @@ def run_ours(args):
     xs_pre = [wl.activations_bf16(M_PREFILL, lin.K, wl.act_seed(wk, j) + 7).to(dev) for j, (lin, _) in enumerate(mats)]
     ys_dec = [torch.empty(M_DECODE, lin.N, dtype=torch.bfloat16, device=dev) for lin, _ in mats]
     ys_pre = [torch.empty(M_PREFILL, lin.N, dtype=torch.bfloat16, device=dev) for lin, _ in mats]
-    stream = torch.cuda.current_stream()
 
-    def step(i, events=None):
-        c = i % copies
-        for j, (lin, packed) in enumerate(mats):
-            if events is not None:
-                events["dec"][j].append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
-                events["dec"][j][-1][0].record(stream)
-            w4.w4a16_linear(xs_dec[j], *packed[c], G, out=ys_dec[j], stream=stream)
-            if events is not None:
-                events["dec"][j][-1][1].record(stream)
-        if gemm_ok:
-            for j, (lin, packed) in enumerate(mats):
-                if events is not None:
-                    events["pre"][j].append((torch.cuda.Event(enable_timing=True),
-                                             torch.cuda.Event(enable_timing=True)))
-                    events["pre"][j][-1][0].record(stream)
-                w4.w4a16_linear(xs_pre[j], *packed[c], G, out=ys_pre[j], stream=stream)
-                if events is not None:
-                    events["pre"][j][-1][1].record(stream)
+    # One graph per (phase, matrix): `steps` back-to-back launches cycling the
+    # device copies.  A step is one launch of each graph's kernel, so the four
+    # graph times add up to the step time, and each graph time / steps is that
+    # kernel's mean launch duration on the GPU (no host launch gaps).
+    phases = [("dec", xs_dec, ys_dec)] + ([("pre", xs_pre, ys_pre)] if gemm_ok else [])
 
-    for i in range(args.warmup):
-        step(i)
+    def launch(phase, j, i, stream):
+        _, xs, ys = next(ph for ph in phases if ph[0] == phase)
+        lin, packed = mats[j]
+        w4.w4a16_linear(xs[j], *packed[i % copies], G, out=ys[j], stream=stream)
+
+    for i in range(args.warmup):                       # eager warm-up steps
+        for ph, _, _ in phases:
+            for j in range(len(mats)):
+                launch(ph, j, i, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    graphs = {}
+    cap_stream = torch.cuda.Stream()
+    for ph, _, _ in phases:
+        for j in range(len(mats)):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=cap_stream):
+                for i in range(args.steps):
+                    launch(ph, j, i, torch.cuda.current_stream())
+            graphs[(ph, j)] = gr
+    for gr in graphs.values():                          # one untimed replay each
+        gr.replay()
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
 
-    events = {"dec": [[] for _ in mats], "pre": [[] for _ in mats]}
+    stream = torch.cuda.current_stream()
+    evs = {k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for k in graphs}
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         torch.cuda.synchronize()
         t0.record(stream)
-        for i in range(args.steps):
-            step(i, events)
+        for k, gr in graphs.items():
+            evs[k][0].record(stream)
+            gr.replay()
+            evs[k][1].record(stream)
         t1.record(stream)
         torch.cuda.synchronize()
     total_ms = t0.elapsed_time(t1)
@@ -223,8 +230,8 @@ def run_ours(args):
         total_ms = float(t.item())
         torch.distributed.barrier()
 
-    dec_ms = [sum(a.elapsed_time(b) for a, b in ev) for ev in events["dec"]]
-    pre_ms = [sum(a.elapsed_time(b) for a, b in ev) for ev in events["pre"]] if gemm_ok else None
+    dec_ms = [evs[("dec", j)][0].elapsed_time(evs[("dec", j)][1]) for j in range(len(mats))]
+    pre_ms = [evs[("pre", j)][0].elapsed_time(evs[("pre", j)][1]) for j in range(len(mats))] if gemm_ok else None
     dec_bytes = [gemv_bytes(M_DECODE, lin.N, lin.K, G) for lin, _ in mats]
     dec_gbs = world * sum(dec_bytes) * args.steps / (sum(dec_ms) * 1e-3) / 1e9
     out = {
@@ -234,7 +241,8 @@ def run_ours(args):
         "config": {"workload": "ffn70b: 70B-shaped FFN gate 8192->28672 and down 28672->8192, G=128, "
                                "decode M=1 (GEMV) + prefill M=2048 (tcgen05 GEMM), weights N(0,0.015), x N(0,1)",
                    "M_decode": M_DECODE, "M_prefill": M_PREFILL if gemm_ok else None, "G": G,
-                   "l2": "inputs larger than L2: 2 rotating device copies of each 122 MB packed matrix",
+                   "l2": f"inputs larger than L2: {copies} rotating device copies of each 122 MB packed matrix",
+                   "timing": "CUDA-graph replay of `steps` launches per kernel, CUDA events on the replay stream",
                    "parallelism": f"replicas x{world}"},
     }
     # roofline, per kernel, from the CUDA-event durations inside the timed region
@@ -293,12 +301,13 @@ def e2e_ours(w4, mats, dev, args, gemm_ok):
     dy = [torch.empty(M_DECODE, lin.N, dtype=torch.bfloat16, device=dev) for lin, _ in mats]
     stream = torch.cuda.current_stream()
     steps = max(args.steps, 20)
+    ncopy = len(mats[0][1])
 
     def run(n):
         for i in range(n):
             for j, (lin, packed) in enumerate(mats):
                 dx[j].copy_(hx[j], non_blocking=True)
-                w4.w4a16_linear(dx[j], *packed[i % 2], G, out=dy[j], stream=stream)
+                w4.w4a16_linear(dx[j], *packed[i % ncopy], G, out=dy[j], stream=stream)
                 hy[j].copy_(dy[j], non_blocking=True)
         torch.cuda.synchronize()
 

@@ -8,6 +8,13 @@ The half-ulp term is the output rounding itself: a correctly rounded BF16
 result can already differ from y_ref by half a BF16 ulp, which for the
 largest outputs exceeds 1e-2 * rms(y_ref), so the per-element bound is read
 as "1e-2 * rms beyond the unavoidable output rounding".
+
+The relative-L2 bound is literal for problems with at least 4096 outputs
+(every workload size).  Output rounding alone has relative L2 error ~1.6e-3
+on average, and on a handful of outputs it fluctuates above 2e-3 (one 8-output
+case measures 2.13e-3 for the correctly rounded reference itself); for those
+small problems the bound is max(2e-3, r0 + 5e-4), r0 = relative L2 error of
+the correctly rounded reference.
 """
 import numpy as np
 import torch
@@ -53,8 +60,22 @@ def error_stats(y, y_ref):
     return rel, (err.max() / rms if rms > 0 else 0.0), float((err / bound).max()) if y_ref.size else 0.0
 
 
+def rounding_only_rel(y_ref):
+    y_ref = np.asarray(y_ref, np.float64)
+    yr = torch.from_numpy(y_ref).to(torch.bfloat16).double().numpy()
+    nrm = np.linalg.norm(y_ref)
+    return np.linalg.norm(yr - y_ref) / nrm if nrm > 0 else 0.0
+
+
+def rel_bound(y_ref):
+    if np.asarray(y_ref).size >= 4096:
+        return REL_L2
+    return max(REL_L2, rounding_only_rel(y_ref) + 5e-4)
+
+
 def assert_close(y, y_ref, what=""):
     rel, maxrel, worst = error_stats(y, y_ref)
-    assert rel <= REL_L2, f"{what}: relL2 {rel:.3e} > {REL_L2}"
+    bound = rel_bound(y_ref)
+    assert rel <= bound, f"{what}: relL2 {rel:.3e} > {bound:.3e}"
     assert worst <= 1.0, f"{what}: max-abs bound exceeded by x{worst:.3f} (max|err|/rms = {maxrel:.3e})"
     return rel, maxrel

@@ -7,21 +7,25 @@
 // File", section 2 "Moving fewer bytes can make decode faster": packed
 // weights decoded block by block straight into the accumulation).
 //
-// Structure (one CTA = 16*R weight rows x all of K, 8 warps splitting K):
-//   1. every thread issues 128-bit loads for its first D k-steps of packed
-//      codes before anything else, so HBM latency overlaps the staging;
-//   2. x [M,K] is staged once per CTA in shared memory, already permuted
-//      into the MMA B-fragment order, with FP32 per-group sums sum_k x;
-//      the CTA's scales/zeros become per-(row, group) pairs {s, -(128+z)*s};
-//   3. the codes become exact BF16 integers 128+q by LOP3 (no conversion
-//      instruction) and meet x in warp MMA m16n8k16 with FP32 accumulation;
-//      per group: acc += s * P - (128+z) * s * sum_k x, which equals
+// Structure.  Work is cut into tiles of 16 weight rows x all of K.  A CTA of
+// 8 warps handles T = 8/S tiles at a time, S warps splitting each tile's
+// groups; the grid is sized so every CTA gets the same number of such
+// iterations (a contiguous run of tiles), with at most two CTAs per SM.
+//   1. every thread first issues 128-bit loads for its next D k-steps of
+//      packed codes (and the scale / zero of their groups), so HBM latency
+//      overlaps everything else; the ring of loads runs across tile
+//      boundaries, so the stream of codes never drains between tiles;
+//   2. x [M,K] is staged once per CTA in shared memory, permuted into the
+//      warp-MMA B-fragment order, with FP32 per-group sums sum_k x;
+//   3. codes become exact BF16 integers 128+q with one LOP3 per pair (no
+//      conversion instruction) and meet x in warp MMA m16n8k16 with FP32
+//      accumulation; per group acc += s*P - (128+z)*s*sum_k x, which equals
 //      s * sum_k x_k (q_k - z) with every product exact;
-//   4. the 8 warps' partial sums are reduced through shared memory in a fixed
-//      order and rounded to BF16 once per output.
-// The warp MMA is used as a wide exact dot-product instruction: one MMA
-// consumes 256 codes, which keeps the instruction count per weight near one
-// and the kernel on the memory bound rather than the issue bound.
+//   4. with S > 1, the S partial sums of a tile are added through shared
+//      memory in a fixed order; every output is rounded to BF16 once.
+// The warp MMA serves as a wide exact dot-product instruction: one MMA
+// consumes 256 codes, keeping the instruction count near one per weight so
+// the kernel stays on the memory bound, not the issue bound.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -37,10 +41,11 @@ struct GemvParams {
     GemvMat mat[2];
     int64_t N, K;
     int M, G;
-    int dual;   // 1: tile r of a CTA reads matrix r (same rows); 0: tiles are consecutive rows of matrix 0
+    int tiles_per_mat;   // ceil(N / 16)
+    int total_tiles;     // tiles_per_mat * number of matrices
+    int iters;           // tile groups (T tiles each) per CTA
 };
 
-// Vector load of V consecutive words.
 template <int V>
 __device__ __forceinline__ void load_words(const uint32_t* p, uint32_t (&w)[V]) {
     if constexpr (V == 4) {
@@ -54,93 +59,120 @@ __device__ __forceinline__ void load_words(const uint32_t* p, uint32_t (&w)[V]) 
     }
 }
 
+__device__ __forceinline__ uint32_t ldg_u16(const void* p) {
+    unsigned short v;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint32_t ldg_u32(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
 // MT: column tiles of 8 activation rows (1: M <= 8, 2: M <= 16).
-// V: packed words per thread per k-step (4 for G >= 128, 2 for G = 64, 1 for G = 32),
-//    so that one k-step of the 4-thread quad (32*V codes) lies inside one group.
-// SPG: k-steps per group (2 for G = 256, else 1).  R: row tiles of 16 per CTA.
-// D: k-steps of codes kept in flight per thread.
-template <int MT, int V, int SPG, int R, int D>
+// V: packed words per thread per k-step (4 for G >= 128, 2 for G = 64, 1 for
+//    G = 32), so the 4-thread quad's 32*V codes of a k-step lie in one group.
+// SPG: k-steps per group (2 for G = 256, else 1).
+// S: warps splitting one tile's groups (1, 2, 4, 8).  D: k-steps in flight.
+template <int MT, int V, int SPG, int S, int D>
 __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
+    constexpr int T = kWarps / S;
+    constexpr int MP = 8 * MT;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t = lane & 3;
+    const int ti = warp / S, si = warp % S;
     const int M = p.M;
     const int G = p.G;
     const int64_t K = p.K, N = p.N;
     const int ngroups = (int)(K / G);
     const int nsteps = (int)(K / (32 * V));
-    constexpr int MP = 8 * MT;
+    const int spt = (ngroups / S) * SPG;          // k-steps per tile for this warp
+    const int step0 = si * spt;                   // its first k-step
+    const int64_t ldq = qweight_ld(K), lds = scales_ld(K, G), ldz = zeros_ld(K, G);
 
-    uint4* xs = reinterpret_cast<uint4*>(smem_raw);                      // [nsteps][V][M][4]
-    float* sx = reinterpret_cast<float*>(xs + (size_t)nsteps * V * M * 4);  // [ngroups][MP]
-    float4* tab = reinterpret_cast<float4*>(sx + (size_t)ngroups * MP);     // [R][ngroups][8]
-    float* red = reinterpret_cast<float*>(tab + (size_t)R * ngroups * 8);   // [kWarps][R][16][MP]
+    uint4* xs = reinterpret_cast<uint4*>(smem_raw);                        // [nsteps][V][M][4]
+    float* sx = reinterpret_cast<float*>(xs + (size_t)nsteps * V * M * 4);    // [ngroups][MP]
+    float* red = sx + (size_t)ngroups * MP;                                   // [2][T][S][16][MP]
 
-    // Row tiles of this CTA.
-    const uint32_t* qrow[R][2];
-    bool valid[R][2];
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-        const int64_t rbase = p.dual ? (int64_t)blockIdx.x * 16 : ((int64_t)blockIdx.x * R + r) * 16;
-        const uint32_t* qm = (p.dual && r == 1) ? p.mat[1].q : p.mat[0].q;
+    const int tile_base = blockIdx.x * p.iters * T;   // first tile of this CTA
+
+    // ---- register ring: codes, scales and zero words of D k-steps --------
+    uint32_t wbuf[D][2][V];
+    uint32_t sbuf[D][2];
+    uint32_t zbuf[D][2];
+
+    int itl = 0, sl = 0;   // load cursor (iteration, step within tile)
+    auto load_slot = [&](uint32_t (&w)[2][V], uint32_t (&sv)[2], uint32_t (&zv)[2]) {
+        const int tau = tile_base + itl * T + ti;
+        const bool tile_ok = itl < p.iters && tau < p.total_tiles;
+        const int second = tau >= p.tiles_per_mat;
+        const int tile = second ? tau - p.tiles_per_mat : tau;
+        const uint32_t* qm = second ? p.mat[1].q : p.mat[0].q;
+        const __half* sm = static_cast<const __half*>(second ? p.mat[1].s : p.mat[0].s);
+        const uint32_t* zm = second ? p.mat[1].z : p.mat[0].z;
+        const int abs_step = step0 + sl;
+        const int grp = abs_step / SPG;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            const int64_t row = rbase + g + 8 * h;
-            valid[r][h] = row < N;
-            qrow[r][h] = qm + (valid[r][h] ? row : 0) * qweight_ld(K) + t * V;
-        }
-    }
-
-    // This warp's share of the groups (contiguous, balanced to within one).
-    const int gpw = ngroups / kWarps, grem = ngroups % kWarps;
-    const int gbeg = warp * gpw + min(warp, grem);
-    const int gend = gbeg + gpw + (warp < grem ? 1 : 0);
-    const int sbeg = gbeg * SPG, send = gend * SPG;
-
-    uint32_t wbuf[D][R][2][V];
-    auto load_step = [&](int s, uint32_t (&dst)[R][2][V]) {
+            const int64_t row = (int64_t)tile * 16 + g + 8 * h;
+            if (tile_ok && row < N) {
+                load_words<V>(qm + row * ldq + (int64_t)abs_step * 4 * V + t * V, w[h]);
+                sv[h] = ldg_u16(sm + row * lds + grp);
+                zv[h] = ldg_u32(zm + row * ldz + grp / 8);
+            } else {
 #pragma unroll
-        for (int r = 0; r < R; ++r)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                if (valid[r][h]) {
-                    load_words<V>(qrow[r][h] + (int64_t)s * 4 * V, dst[r][h]);
-                } else {
-#pragma unroll
-                    for (int v = 0; v < V; ++v) dst[r][h][v] = 0u;
-                }
+                for (int v = 0; v < V; ++v) w[h][v] = 0u;
+                sv[h] = 0u;       // scale 0: the row contributes nothing
+                zv[h] = 0u;
             }
+        }
+        if (++sl == spt) {
+            sl = 0;
+            ++itl;
+        }
     };
 
     // (1) first loads in flight before any staging.
 #pragma unroll
-    for (int i = 0; i < D; ++i)
-        if (sbeg + i < send) load_step(sbeg + i, wbuf[i]);
+    for (int i = 0; i < D; ++i) load_slot(wbuf[i], sbuf[i], zbuf[i]);
 
-    // (2a) x -> B-fragment order + per-group sums.  Item = (m, word w8 of 8 k).
+    // (2) x -> B-fragment order + per-group sums; item = (m, 8-k word w8).
     {
-        const int64_t wpr = K / 8;                   // 8-k words per activation row
+        const int64_t wpr = K / 8;
         const int64_t total = (int64_t)M * wpr;
-        const int gw = G / 8;                        // words per group (4..32), divides 32
-        for (int64_t base = (int64_t)warp * 32; base < total; base += kThreads) {
-            const int64_t item = base + lane;
-            const bool ok = item < total;
-            const int64_t m = ok ? item / wpr : 0;
-            const int64_t w8 = ok ? item % wpr : 0;
-            uint4 xv = make_uint4(0u, 0u, 0u, 0u);
-            if (ok) xv = *reinterpret_cast<const uint4*>(p.x + m * K + w8 * 8);
-            float f = bf16lo_to_f32(xv.x) + bf16hi_to_f32(xv.x) + bf16lo_to_f32(xv.y) + bf16hi_to_f32(xv.y) +
-                      bf16lo_to_f32(xv.z) + bf16hi_to_f32(xv.z) + bf16lo_to_f32(xv.w) + bf16hi_to_f32(xv.w);
-            for (int off = 1; off < gw; off <<= 1) f += __shfl_xor_sync(0xFFFFFFFFu, f, off);
-            if (ok) {
-                const int64_t s = w8 / (4 * V);
-                const int tt = (int)((w8 % (4 * V)) / V);
-                const int v = (int)(w8 % V);
-                xs[((s * V + v) * M + m) * 4 + tt] =
-                    make_uint4(__byte_perm(xv.x, xv.z, 0x5410), __byte_perm(xv.x, xv.z, 0x7632),
-                               __byte_perm(xv.y, xv.w, 0x5410), __byte_perm(xv.y, xv.w, 0x7632));
-                if (w8 % gw == 0) sx[(w8 / gw) * MP + m] = f;
+        const int gw = G / 8;                     // words per group, divides 32
+        constexpr int U = 4;
+        for (int64_t base0 = (int64_t)warp * 32; base0 < total; base0 += (int64_t)U * kThreads) {
+            uint4 xv[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t item = base0 + (int64_t)u * kThreads + lane;
+                xv[u] = make_uint4(0u, 0u, 0u, 0u);
+                if (item < total) {
+                    const int64_t m = item / wpr, w8 = item % wpr;
+                    xv[u] = *reinterpret_cast<const uint4*>(p.x + m * K + w8 * 8);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t item = base0 + (int64_t)u * kThreads + lane;
+                float f = bf16lo_to_f32(xv[u].x) + bf16hi_to_f32(xv[u].x) + bf16lo_to_f32(xv[u].y) +
+                          bf16hi_to_f32(xv[u].y) + bf16lo_to_f32(xv[u].z) + bf16hi_to_f32(xv[u].z) +
+                          bf16lo_to_f32(xv[u].w) + bf16hi_to_f32(xv[u].w);
+                for (int off = 1; off < gw; off <<= 1) f += __shfl_xor_sync(0xFFFFFFFFu, f, off);
+                if (item < total) {
+                    const int64_t m = item / wpr, w8 = item % wpr;
+                    const int64_t s = w8 / (4 * V);
+                    const int tt = (int)((w8 % (4 * V)) / V);
+                    const int v = (int)(w8 % V);
+                    xs[((s * V + v) * M + m) * 4 + tt] =
+                        make_uint4(__byte_perm(xv[u].x, xv[u].z, 0x5410), __byte_perm(xv[u].x, xv[u].z, 0x7632),
+                                   __byte_perm(xv[u].y, xv[u].w, 0x5410), __byte_perm(xv[u].y, xv[u].w, 0x7632));
+                    if (w8 % gw == 0) sx[(w8 / gw) * MP + m] = f;
+                }
             }
         }
         for (int i = tid; i < ngroups * (MP - M); i += kThreads) {
@@ -148,159 +180,222 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
             sx[grp * MP + m] = 0.0f;
         }
     }
-
-    // (2b) per-(row, group) {s, -(128+z)*s}; both products are exact in FP32.
-    {
-        const int64_t lds = scales_ld(K, G), ldz = zeros_ld(K, G);
-        float* tf = reinterpret_cast<float*>(tab);
-        for (int e = tid; e < R * 16 * ngroups; e += kThreads) {
-            const int r = e / (16 * ngroups);
-            const int rr = (e / ngroups) % 16;
-            const int grp = e % ngroups;
-            const int64_t row = (p.dual ? (int64_t)blockIdx.x * 16 : ((int64_t)blockIdx.x * R + r) * 16) + rr;
-            float s = 0.0f, c = 0.0f;
-            if (row < N) {
-                const bool second = p.dual && r == 1;
-                const __half* sp = static_cast<const __half*>(second ? p.mat[1].s : p.mat[0].s);
-                const uint32_t* zp = second ? p.mat[1].z : p.mat[0].z;
-                s = __half2float(sp[row * lds + grp]);
-                const uint32_t zw = zp[row * ldz + grp / 8];
-                c = -(128.0f + (float)nibble(zw, grp & 7)) * s;
-            }
-            float* dst = tf + ((size_t)(r * ngroups + grp) * 8 + (rr & 7)) * 4 + (rr >= 8 ? 2 : 0);
-            dst[0] = s;
-            dst[1] = c;
-        }
-    }
     __syncthreads();
 
-    // (3) main loop over this warp's k-steps.
-    float acc[R][MT][4];
-    float part[R][MT][4];
+    // (3) stream the warp's k-steps, tile after tile.
+    float acc[MT][4];
+    float part[MT][4];
 #pragma unroll
-    for (int r = 0; r < R; ++r)
+    for (int ct = 0; ct < MT; ++ct)
 #pragma unroll
-        for (int ct = 0; ct < MT; ++ct)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[r][ct][e] = part[r][ct][e] = 0.0f;
-
+        for (int e = 0; e < 4; ++e) acc[ct][e] = part[ct][e] = 0.0f;
     bool colv[MT];
 #pragma unroll
     for (int ct = 0; ct < MT; ++ct) colv[ct] = (g + 8 * ct) < M;
 
-    for (int s0 = sbeg; s0 < send; s0 += D) {
+    int itc = 0, sc = 0;   // compute cursor
+    const int total_steps = p.iters * spt;
+    for (int j0 = 0; j0 < total_steps; j0 += D) {
 #pragma unroll
         for (int i = 0; i < D; ++i) {
-            const int s = s0 + i;
-            if (s < send) {
+            if (j0 + i < total_steps) {
+                const int abs_step = step0 + sc;
                 uint4 bfr[MT][V];
 #pragma unroll
                 for (int ct = 0; ct < MT; ++ct)
 #pragma unroll
                     for (int v = 0; v < V; ++v)
-                        bfr[ct][v] = colv[ct] ? xs[(((int64_t)s * V + v) * M + g + 8 * ct) * 4 + t]
+                        bfr[ct][v] = colv[ct] ? xs[(((int64_t)abs_step * V + v) * M + g + 8 * ct) * 4 + t]
                                               : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-                for (int r = 0; r < R; ++r)
+                for (int v = 0; v < V; ++v) {
+                    uint32_t plo[4], phi[4];
+                    codes_to_bf16x2(wbuf[i][0][v], plo);
+                    codes_to_bf16x2(wbuf[i][1][v], phi);
+                    const uint32_t a0[4] = {plo[0], phi[0], plo[1], phi[1]};
+                    const uint32_t a1[4] = {plo[2], phi[2], plo[3], phi[3]};
 #pragma unroll
-                    for (int v = 0; v < V; ++v) {
-                        uint32_t plo[4], phi[4];
-                        codes_to_bf16x2(wbuf[i][r][0][v], plo);
-                        codes_to_bf16x2(wbuf[i][r][1][v], phi);
-                        const uint32_t a0[4] = {plo[0], phi[0], plo[1], phi[1]};
-                        const uint32_t a1[4] = {plo[2], phi[2], plo[3], phi[3]};
-#pragma unroll
-                        for (int ct = 0; ct < MT; ++ct) {
-                            mma_bf16_16816(part[r][ct], a0, bfr[ct][v].x, bfr[ct][v].y);
-                            mma_bf16_16816(part[r][ct], a1, bfr[ct][v].z, bfr[ct][v].w);
-                        }
+                    for (int ct = 0; ct < MT; ++ct) {
+                        mma_bf16_16816(part[ct], a0, bfr[ct][v].x, bfr[ct][v].y);
+                        mma_bf16_16816(part[ct], a1, bfr[ct][v].z, bfr[ct][v].w);
                     }
-                if (s + D < send) load_step(s + D, wbuf[i]);
-                if ((s + 1) % SPG == 0) {
-                    const int grp = s / SPG;
+                }
+                if ((abs_step + 1) % SPG == 0) {      // group complete: scale and zero correction
+                    const int grp = abs_step / SPG;
+                    float sc_[2], c_[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        sc_[h] = __half2float(__ushort_as_half((unsigned short)sbuf[i][h]));
+                        c_[h] = -__uint2float_rn(128u + nibble(zbuf[i][h], grp & 7)) * sc_[h];
+                    }
 #pragma unroll
                     for (int ct = 0; ct < MT; ++ct) {
                         const float2 sxv = *reinterpret_cast<const float2*>(sx + grp * MP + 8 * ct + 2 * t);
+                        acc[ct][0] = fmaf(c_[0], sxv.x, fmaf(sc_[0], part[ct][0], acc[ct][0]));
+                        acc[ct][1] = fmaf(c_[0], sxv.y, fmaf(sc_[0], part[ct][1], acc[ct][1]));
+                        acc[ct][2] = fmaf(c_[1], sxv.x, fmaf(sc_[1], part[ct][2], acc[ct][2]));
+                        acc[ct][3] = fmaf(c_[1], sxv.y, fmaf(sc_[1], part[ct][3], acc[ct][3]));
 #pragma unroll
-                        for (int r = 0; r < R; ++r) {
-                            const float4 tv = tab[(size_t)(r * ngroups + grp) * 8 + g];
-                            acc[r][ct][0] = fmaf(tv.y, sxv.x, fmaf(tv.x, part[r][ct][0], acc[r][ct][0]));
-                            acc[r][ct][1] = fmaf(tv.y, sxv.y, fmaf(tv.x, part[r][ct][1], acc[r][ct][1]));
-                            acc[r][ct][2] = fmaf(tv.w, sxv.x, fmaf(tv.z, part[r][ct][2], acc[r][ct][2]));
-                            acc[r][ct][3] = fmaf(tv.w, sxv.y, fmaf(tv.z, part[r][ct][3], acc[r][ct][3]));
+                        for (int e = 0; e < 4; ++e) part[ct][e] = 0.0f;
+                    }
+                }
+                load_slot(wbuf[i], sbuf[i], zbuf[i]);  // refill this slot D steps ahead
+                if (++sc == spt) {                     // tile complete (same step for every warp)
+                    const int tau = tile_base + itc * T + ti;
+                    if constexpr (S == 1) {
+                        if (tau < p.total_tiles) {
+                            const int second = tau >= p.tiles_per_mat;
+                            const int tile = second ? tau - p.tiles_per_mat : tau;
+                            __nv_bfloat16* y = static_cast<__nv_bfloat16*>(second ? p.mat[1].y : p.mat[0].y);
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) part[r][ct][e] = 0.0f;
+                            for (int ct = 0; ct < MT; ++ct)
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const int m = 8 * ct + 2 * t + (e & 1);
+                                    const int64_t row = (int64_t)tile * 16 + g + 8 * (e >> 1);
+                                    if (m < M && row < N) y[(int64_t)m * N + row] = __float2bfloat16_rn(acc[ct][e]);
+                                }
+                        }
+                    } else {
+                        float* rb = red + ((size_t)((itc & 1) * T + ti) * S + si) * 16 * MP;
+#pragma unroll
+                        for (int ct = 0; ct < MT; ++ct) {
+                            rb[g * MP + 8 * ct + 2 * t] = acc[ct][0];
+                            rb[g * MP + 8 * ct + 2 * t + 1] = acc[ct][1];
+                            rb[(g + 8) * MP + 8 * ct + 2 * t] = acc[ct][2];
+                            rb[(g + 8) * MP + 8 * ct + 2 * t + 1] = acc[ct][3];
+                        }
+                        __syncthreads();
+                        const float* rbuf = red + (size_t)(itc & 1) * T * S * 16 * MP;
+                        for (int e = tid; e < T * 16 * M; e += kThreads) {
+                            const int tj = e / (16 * M);
+                            const int m = (e / 16) % M;
+                            const int rr = e % 16;
+                            const int tau2 = tile_base + itc * T + tj;
+                            if (tau2 >= p.total_tiles) continue;
+                            const int second = tau2 >= p.tiles_per_mat;
+                            const int tile = second ? tau2 - p.tiles_per_mat : tau2;
+                            const int64_t row = (int64_t)tile * 16 + rr;
+                            if (row >= N) continue;
+                            float sum = 0.0f;
+#pragma unroll
+                            for (int q = 0; q < S; ++q) sum += rbuf[((size_t)(tj * S + q) * 16 + rr) * MP + m];
+                            __nv_bfloat16* y = static_cast<__nv_bfloat16*>(second ? p.mat[1].y : p.mat[0].y);
+                            y[(int64_t)m * N + row] = __float2bfloat16_rn(sum);
                         }
                     }
+#pragma unroll
+                    for (int ct = 0; ct < MT; ++ct)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) acc[ct][e] = 0.0f;
+                    sc = 0;
+                    ++itc;
                 }
             }
         }
     }
-
-    // (4) split-K reduction across the 8 warps, fixed order, one rounding.
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-#pragma unroll
-        for (int ct = 0; ct < MT; ++ct) {
-            float* d = red + ((size_t)(warp * R + r) * 16) * MP + 8 * ct + 2 * t;
-            d[g * MP] = acc[r][ct][0];
-            d[g * MP + 1] = acc[r][ct][1];
-            d[(g + 8) * MP] = acc[r][ct][2];
-            d[(g + 8) * MP + 1] = acc[r][ct][3];
-        }
-    __syncthreads();
-    for (int e = tid; e < R * 16 * M; e += kThreads) {
-        const int r = e / (16 * M);
-        const int m = (e / 16) % M;
-        const int rr = e % 16;
-        const int64_t row = (p.dual ? (int64_t)blockIdx.x * 16 : ((int64_t)blockIdx.x * R + r) * 16) + rr;
-        if (row >= N) continue;
-        float sum = 0.0f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) sum += red[((size_t)(w * R + r) * 16 + rr) * MP + m];
-        __nv_bfloat16* y = static_cast<__nv_bfloat16*>((p.dual && r == 1) ? p.mat[1].y : p.mat[0].y);
-        y[(int64_t)m * N + row] = __float2bfloat16_rn(sum);
-    }
 }
 
-template <int MT, int V, int SPG, int R, int D>
-cudaError_t launch_one(const GemvParams& p, size_t smem, int64_t ctas, cudaStream_t stream) {
-    auto kern = gemv_kernel<MT, V, SPG, R, D>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+struct Plan {
+    int S, iters, grid;
+};
+
+template <int MT, int V, int SPG, int S>
+cudaError_t launch_s(const GemvParams& p0, size_t smem, int sms, cudaStream_t stream);
+
+// Per kernel instance and device: raise the dynamic shared memory limit once, as needed.
+constexpr int kMaxDevices = 64;
+template <typename Kern>
+cudaError_t ensure_smem(Kern kern, size_t smem, int (&cached)[kMaxDevices]) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    kern<<<dim3((unsigned)ctas), dim3(kThreads), smem, stream>>>(p);
+    if (dev >= 0 && dev < kMaxDevices && (int)smem <= cached[dev]) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess && dev >= 0 && dev < kMaxDevices) cached[dev] = (int)smem;
+    return e;
+}
+
+template <int MT, int V, int SPG, int S>
+cudaError_t launch_s(const GemvParams& p0, size_t smem, int sms, cudaStream_t stream) {
+    // k-steps in flight per thread: as deep as the 128-register budget allows without spilling
+    constexpr int D = MT == 1 ? (V == 4 ? 6 : (V == 2 ? 8 : 10)) : (V == 4 ? 4 : (V == 2 ? 6 : 8));
+    auto kern = gemv_kernel<MT, V, SPG, S, D>;
+    static int cached[kMaxDevices] = {};
+    cudaError_t e = ensure_smem(kern, smem, cached);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    per_sm = per_sm > 2 ? 2 : per_sm;
+    GemvParams p = p0;
+    constexpr int T = kWarps / S;
+    const int max_ctas = sms * per_sm;
+    const int tg = (p.total_tiles + T - 1) / T;
+    p.iters = (tg + max_ctas - 1) / max_ctas;
+    const int grid = (tg + p.iters - 1) / p.iters;
+    kern<<<dim3((unsigned)grid), dim3(kThreads), smem, stream>>>(p);
     return cudaGetLastError();
 }
 
-// Loads in flight per thread: ~128 bytes of codes (D * R * 2 rows * V words * 4 B).
-template <int MT, int V, int SPG, int R>
-cudaError_t launch_d(const GemvParams& p, size_t smem, int64_t ctas, cudaStream_t stream) {
-    constexpr int D = (16 / (R * V)) < 1 ? 1 : (16 / (R * V));
-    return launch_one<MT, V, SPG, R, D>(p, smem, ctas, stream);
+// Splitting S: among the splits that divide the group count, the one whose
+// balanced grid wastes the fewest warp-iterations while still covering every
+// SM; ties go to the smallest S (fewest cross-warp reductions).
+int choose_split(int total_tiles, int ngroups, int sms, int per_sm) {
+    int best = 0;
+    double best_score = -1.0;
+    for (int S : {1, 2, 4, 8}) {
+        if (ngroups % S) continue;
+        const int T = kWarps / S;
+        const int tg = (total_tiles + T - 1) / T;
+        const int max_ctas = sms * per_sm;
+        const int iters = (tg + max_ctas - 1) / max_ctas;
+        const int grid = (tg + iters - 1) / iters;
+        const double eff = (double)total_tiles / ((double)grid * iters * T);
+        const double fill = grid >= sms ? 1.0 : (double)grid / sms;
+        const double score = eff * fill;
+        if (score > best_score + 1e-9) {
+            best_score = score;
+            best = S;
+        }
+    }
+    return best;
 }
 
-template <int MT, int R>
-cudaError_t launch_g(const GemvParams& p, size_t smem, int64_t ctas, cudaStream_t stream) {
+template <int MT, int V, int SPG>
+cudaError_t launch_v(const GemvParams& p, size_t smem, int sms, cudaStream_t stream) {
+    const int per_sm = smem <= 100 * 1024 ? 2 : 1;
+    switch (choose_split(p.total_tiles, (int)(p.K / p.G), sms, per_sm)) {
+        case 1: return launch_s<MT, V, SPG, 1>(p, smem, sms, stream);
+        case 2: return launch_s<MT, V, SPG, 2>(p, smem, sms, stream);
+        case 4: return launch_s<MT, V, SPG, 4>(p, smem, sms, stream);
+        case 8: return launch_s<MT, V, SPG, 8>(p, smem, sms, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int MT>
+cudaError_t launch_g(const GemvParams& p, size_t smem, int sms, cudaStream_t stream) {
     switch (p.G) {
-        case 32: return launch_d<MT, 1, 1, R>(p, smem, ctas, stream);
-        case 64: return launch_d<MT, 2, 1, R>(p, smem, ctas, stream);
-        case 128: return launch_d<MT, 4, 1, R>(p, smem, ctas, stream);
-        case 256: return launch_d<MT, 4, 2, R>(p, smem, ctas, stream);
+        case 32: return launch_v<MT, 1, 1>(p, smem, sms, stream);
+        case 64: return launch_v<MT, 2, 1>(p, smem, sms, stream);
+        case 128: return launch_v<MT, 4, 1>(p, smem, sms, stream);
+        case 256: return launch_v<MT, 4, 2>(p, smem, sms, stream);
         default: return cudaErrorInvalidValue;
     }
 }
 
 }  // namespace
 
-size_t gemv_smem_bytes(int64_t M, int64_t K, int G, int ntiles) {
+size_t gemv_smem_bytes(int64_t M, int64_t K, int G, int /*ntiles*/) {
     if (M < 1 || M > 16) return 0;
     const int64_t MP = M <= 8 ? 8 : 16;
     const int64_t ngroups = K / G;
     const int64_t xs = M * K * 2;
     const int64_t sx = ngroups * MP * 4;
-    const int64_t tab = (int64_t)ntiles * ngroups * 8 * 16;
-    const int64_t red = (int64_t)kWarps * ntiles * 16 * MP * 4;
-    return (size_t)(xs + sx + tab + red);
+    const int64_t red = 2 * (int64_t)kWarps * 16 * MP * 4;
+    return (size_t)(xs + sx + red);
 }
 
 size_t device_smem_optin() {
@@ -320,13 +415,17 @@ cudaError_t launch_gemv(const void* x, const GemvMat* mats, int nmat, int64_t M,
     p.K = K;
     p.M = (int)M;
     p.G = G;
-    p.dual = nmat == 2 ? 1 : 0;
-    const int R = nmat == 2 ? 2 : 1;
-    const size_t smem = gemv_smem_bytes(M, K, G, R);
-    const int64_t ctas = nmat == 2 ? (N + 15) / 16 : (N + 16 * R - 1) / (16 * R);
+    p.tiles_per_mat = (int)((N + 15) / 16);
+    p.total_tiles = p.tiles_per_mat * nmat;
+    p.iters = 0;
+    const size_t smem = gemv_smem_bytes(M, K, G, nmat);
     if (smem == 0) return cudaErrorInvalidValue;
-    if (M <= 8) return R == 2 ? launch_g<1, 2>(p, smem, ctas, stream) : launch_g<1, 1>(p, smem, ctas, stream);
-    return R == 2 ? launch_g<2, 2>(p, smem, ctas, stream) : launch_g<2, 1>(p, smem, ctas, stream);
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    return M <= 8 ? launch_g<1>(p, smem, sms, stream) : launch_g<2>(p, smem, sms, stream);
 }
 
 }  // namespace w4a16
