@@ -180,7 +180,7 @@ def test_outputs_leave_guard_regions_untouched():
     # packer guard regions
     wd = w.cuda()
     qs, ss, zs = w4.packed_shapes(N, K, G)
-    big = torch.full((3 * pad,), 0x5A5A5A5A, dtype=torch.int32, device="cuda")
+    big = torch.full((2 * pad + qs[0] * qs[1],), 0x5A5A5A5A, dtype=torch.int32, device="cuda")
     qv = big[pad: pad + qs[0] * qs[1]].view(qs)
     zbig = torch.full((2 * pad + zs[0] * zs[1],), 0x5A5A5A5A, dtype=torch.int32, device="cuda")
     zv = zbig[pad: pad + zs[0] * zs[1]].view(zs)

@@ -6,7 +6,7 @@ shapes of torch tensors, allocates outputs with torch when the caller does
 not pass them, and forwards raw device pointers plus the current CUDA stream
 to the C entry point of the same name.  All arithmetic runs in the library's
 CUDA kernels; there is no fallback path.  Importing this module fails loudly
-if the library has not been built (``python -m w4a16_weight_only_linear_b300.build``).
+if the library has not been built (``python w4a16_weight_only_linear_b300/build.py``).
 
 Packed format (see the header): qweight uint32 [N, K/8], scales FP16
 [N, ldS], zeros uint32 [N, ldZ]; W_hat = (q - z) * s; y = x * W_hat^T.
@@ -52,7 +52,7 @@ class W4A16Error(RuntimeError):
 
 def _load_library():
     if not os.path.exists(LIB_PATH):
-        raise ImportError(f"{LIB_PATH} is missing: build it with `python -m w4a16_weight_only_linear_b300.build`")
+        raise ImportError(f"{LIB_PATH} is missing: build it with `python w4a16_weight_only_linear_b300/build.py`")
     lib = ctypes.CDLL(LIB_PATH)
     for name, (args, res) in EXPORTS.items():
         f = getattr(lib, name)

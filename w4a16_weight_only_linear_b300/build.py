@@ -1,6 +1,8 @@
 """Build libw4a16.so (the C-ABI library) in-tree with nvcc for sm_103a.
 
-    python -m w4a16_weight_only_linear_b300.build [--force]
+    python w4a16_weight_only_linear_b300/build.py [--force] [-v]
+
+(run as a script: importing the package itself needs the built library)
 
 The library is written to w4a16_weight_only_linear_b300/_lib/libw4a16.so.
 It links the CUDA runtime statically and resolves driver entry points at run

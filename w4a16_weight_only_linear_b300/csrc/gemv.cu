@@ -43,7 +43,7 @@ struct GemvParams {
     int M, G;
     int tiles_per_mat;   // ceil(N / 16)
     int total_tiles;     // tiles_per_mat * number of matrices
-    int iters;           // tile groups (T tiles each) per CTA
+    int tile_groups;     // ceil(total_tiles / T); CTA b takes groups [b*tg/grid, (b+1)*tg/grid)
 };
 
 template <int V>
@@ -59,9 +59,11 @@ __device__ __forceinline__ void load_words(const uint32_t* p, uint32_t (&w)[V]) 
     }
 }
 
-__device__ __forceinline__ uint32_t ldg_u16(const void* p) {
-    unsigned short v;
-    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+// 16-bit load straight into a 32-bit register (the load zero-extends), so no
+// instruction consumes the value before it is needed.
+__device__ __forceinline__ uint32_t ldg_u16(const unsigned short* p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=r"(v) : "l"(p));
     return v;
 }
 __device__ __forceinline__ uint32_t ldg_u32(const uint32_t* p) {
@@ -97,81 +99,118 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
     float* sx = reinterpret_cast<float*>(xs + (size_t)nsteps * V * M * 4);    // [ngroups][MP]
     float* red = sx + (size_t)ngroups * MP;                                   // [2][T][S][16][MP]
 
-    const int tile_base = blockIdx.x * p.iters * T;   // first tile of this CTA
+    // This CTA's contiguous, balanced run of tile groups (uniform in the CTA).
+    const int tg = p.tile_groups;
+    const int g0 = (int)(((int64_t)blockIdx.x * tg) / gridDim.x);
+    const int iters = (int)(((int64_t)(blockIdx.x + 1) * tg) / gridDim.x) - g0;
 
     // ---- register ring: codes, scales and zero words of D k-steps --------
     uint32_t wbuf[D][2][V];
     uint32_t sbuf[D][2];
     uint32_t zbuf[D][2];
 
-    int itl = 0, sl = 0;   // load cursor (iteration, step within tile)
-    auto load_slot = [&](uint32_t (&w)[2][V], uint32_t (&sv)[2], uint32_t (&zv)[2]) {
-        const int tau = tile_base + itl * T + ti;
-        const bool tile_ok = itl < p.iters && tau < p.total_tiles;
+    // Load cursor: pointers advance by a constant per k-step; 64-bit address
+    // arithmetic happens only when the cursor moves to the next tile.
+    int itl = 0, sl = 0, lgrp = 0;
+    bool lv0 = false, lv1 = false;
+    const uint32_t* lq0 = nullptr;
+    const uint32_t* lq1 = nullptr;
+    const unsigned short* ls0 = nullptr;
+    const unsigned short* ls1 = nullptr;
+    const uint32_t* lz0 = nullptr;
+    const uint32_t* lz1 = nullptr;
+    auto set_load_tile = [&]() {
+        const int tau = (g0 + itl) * T + ti;
+        const bool ok = itl < iters && tau < p.total_tiles;
         const int second = tau >= p.tiles_per_mat;
         const int tile = second ? tau - p.tiles_per_mat : tau;
+        const int64_t row = (int64_t)tile * 16 + g;
+        lv0 = ok && row < N;
+        lv1 = ok && row + 8 < N;
+        const int64_t r = lv0 ? row : 0;          // pointers of an absent row stay in the matrix
         const uint32_t* qm = second ? p.mat[1].q : p.mat[0].q;
-        const __half* sm = static_cast<const __half*>(second ? p.mat[1].s : p.mat[0].s);
+        const unsigned short* sm = static_cast<const unsigned short*>(second ? p.mat[1].s : p.mat[0].s);
         const uint32_t* zm = second ? p.mat[1].z : p.mat[0].z;
-        const int abs_step = step0 + sl;
-        const int grp = abs_step / SPG;
+        lgrp = step0 / SPG;
+        lq0 = qm + r * ldq + step0 * 4 * V + t * V;
+        lq1 = lq0 + (lv1 ? 8 * ldq : 0);
+        ls0 = sm + r * lds + lgrp;
+        ls1 = ls0 + (lv1 ? 8 * lds : 0);
+        lz0 = zm + r * ldz;
+        lz1 = lz0 + (lv1 ? 8 * ldz : 0);
+    };
+    auto load_slot = [&](uint32_t (&w)[2][V], uint32_t (&sv)[2], uint32_t (&zv)[2]) {
+        if (lv0) {
+            load_words<V>(lq0, w[0]);
+            sv[0] = ldg_u16(ls0);
+            zv[0] = ldg_u32(lz0 + (lgrp >> 3));
+        } else {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int64_t row = (int64_t)tile * 16 + g + 8 * h;
-            if (tile_ok && row < N) {
-                load_words<V>(qm + row * ldq + (int64_t)abs_step * 4 * V + t * V, w[h]);
-                sv[h] = ldg_u16(sm + row * lds + grp);
-                zv[h] = ldg_u32(zm + row * ldz + grp / 8);
-            } else {
+            for (int v = 0; v < V; ++v) w[0][v] = 0u;
+            sv[0] = 0u;          // scale 0: an absent row contributes nothing
+            zv[0] = 0u;
+        }
+        if (lv1) {
+            load_words<V>(lq1, w[1]);
+            sv[1] = ldg_u16(ls1);
+            zv[1] = ldg_u32(lz1 + (lgrp >> 3));
+        } else {
 #pragma unroll
-                for (int v = 0; v < V; ++v) w[h][v] = 0u;
-                sv[h] = 0u;       // scale 0: the row contributes nothing
-                zv[h] = 0u;
-            }
+            for (int v = 0; v < V; ++v) w[1][v] = 0u;
+            sv[1] = 0u;
+            zv[1] = 0u;
+        }
+        lq0 += 4 * V;
+        lq1 += 4 * V;
+        if (SPG == 1 || (sl & 1)) {
+            ++ls0;
+            ++ls1;
+            ++lgrp;
         }
         if (++sl == spt) {
             sl = 0;
             ++itl;
+            set_load_tile();
         }
     };
 
     // (1) first loads in flight before any staging.
+    set_load_tile();
 #pragma unroll
     for (int i = 0; i < D; ++i) load_slot(wbuf[i], sbuf[i], zbuf[i]);
 
     // (2) x -> B-fragment order + per-group sums; item = (m, 8-k word w8).
     {
-        const int64_t wpr = K / 8;
-        const int64_t total = (int64_t)M * wpr;
-        const int gw = G / 8;                     // words per group, divides 32
+        // x fits in shared memory, so every index here fits in 32 bits
+        const int wpr = (int)(K / 8);
+        const int total = M * wpr;
+        const int gw = G / 8;                     // words per group, a power of two dividing 32
+        const int gshift = __ffs(gw) - 1;
         constexpr int U = 4;
-        for (int64_t base0 = (int64_t)warp * 32; base0 < total; base0 += (int64_t)U * kThreads) {
+        for (int base0 = warp * 32; base0 < total; base0 += U * kThreads) {
             uint4 xv[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const int64_t item = base0 + (int64_t)u * kThreads + lane;
+                const int item = base0 + u * kThreads + lane;
                 xv[u] = make_uint4(0u, 0u, 0u, 0u);
-                if (item < total) {
-                    const int64_t m = item / wpr, w8 = item % wpr;
-                    xv[u] = *reinterpret_cast<const uint4*>(p.x + m * K + w8 * 8);
-                }
+                if (item < total) xv[u] = *reinterpret_cast<const uint4*>(p.x + (int64_t)item * 8);
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const int64_t item = base0 + (int64_t)u * kThreads + lane;
+                const int item = base0 + u * kThreads + lane;
                 float f = bf16lo_to_f32(xv[u].x) + bf16hi_to_f32(xv[u].x) + bf16lo_to_f32(xv[u].y) +
                           bf16hi_to_f32(xv[u].y) + bf16lo_to_f32(xv[u].z) + bf16hi_to_f32(xv[u].z) +
                           bf16lo_to_f32(xv[u].w) + bf16hi_to_f32(xv[u].w);
                 for (int off = 1; off < gw; off <<= 1) f += __shfl_xor_sync(0xFFFFFFFFu, f, off);
                 if (item < total) {
-                    const int64_t m = item / wpr, w8 = item % wpr;
-                    const int64_t s = w8 / (4 * V);
-                    const int tt = (int)((w8 % (4 * V)) / V);
-                    const int v = (int)(w8 % V);
+                    const int m = item / wpr, w8 = item - m * wpr;
+                    const int s = w8 / (4 * V);
+                    const int tt = (w8 % (4 * V)) / V;
+                    const int v = w8 % V;
                     xs[((s * V + v) * M + m) * 4 + tt] =
                         make_uint4(__byte_perm(xv[u].x, xv[u].z, 0x5410), __byte_perm(xv[u].x, xv[u].z, 0x7632),
                                    __byte_perm(xv[u].y, xv[u].w, 0x5410), __byte_perm(xv[u].y, xv[u].w, 0x7632));
-                    if (w8 % gw == 0) sx[(w8 / gw) * MP + m] = f;
+                    if ((w8 & (gw - 1)) == 0) sx[(w8 >> gshift) * MP + m] = f;
                 }
             }
         }
@@ -193,20 +232,22 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
 #pragma unroll
     for (int ct = 0; ct < MT; ++ct) colv[ct] = (g + 8 * ct) < M;
 
-    int itc = 0, sc = 0;   // compute cursor
-    const int total_steps = p.iters * spt;
+    const int xstep = V * M * 4;                  // uint4 per k-step of staged x
+    const int xlane = g * 4 + t;
+    int itc = 0, sc = 0;                          // compute cursor
+    int xoff = step0 * xstep;
+    int cgrp = step0 / SPG;
+    const int total_steps = iters * spt;
     for (int j0 = 0; j0 < total_steps; j0 += D) {
 #pragma unroll
         for (int i = 0; i < D; ++i) {
             if (j0 + i < total_steps) {
-                const int abs_step = step0 + sc;
                 uint4 bfr[MT][V];
 #pragma unroll
                 for (int ct = 0; ct < MT; ++ct)
 #pragma unroll
                     for (int v = 0; v < V; ++v)
-                        bfr[ct][v] = colv[ct] ? xs[(((int64_t)abs_step * V + v) * M + g + 8 * ct) * 4 + t]
-                                              : make_uint4(0u, 0u, 0u, 0u);
+                        bfr[ct][v] = colv[ct] ? xs[xoff + v * M * 4 + xlane + 32 * ct] : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
                 for (int v = 0; v < V; ++v) {
                     uint32_t plo[4], phi[4];
@@ -220,29 +261,31 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
                         mma_bf16_16816(part[ct], a1, bfr[ct][v].z, bfr[ct][v].w);
                     }
                 }
-                if ((abs_step + 1) % SPG == 0) {      // group complete: scale and zero correction
-                    const int grp = abs_step / SPG;
-                    float sc_[2], c_[2];
+                if (SPG == 1 || (sc & 1)) {           // group complete: scale and zero correction
+                    float s_[2], c_[2];
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        sc_[h] = __half2float(__ushort_as_half((unsigned short)sbuf[i][h]));
-                        c_[h] = -__uint2float_rn(128u + nibble(zbuf[i][h], grp & 7)) * sc_[h];
+                        s_[h] = __half2float(__ushort_as_half((unsigned short)sbuf[i][h]));
+                        // 128 + z exactly: 2^23 + 128 + z has ulp 1, minus 2^23
+                        c_[h] = __uint_as_float(0x4B000080u + nibble(zbuf[i][h], cgrp & 7)) - 8388608.0f;
                     }
 #pragma unroll
                     for (int ct = 0; ct < MT; ++ct) {
-                        const float2 sxv = *reinterpret_cast<const float2*>(sx + grp * MP + 8 * ct + 2 * t);
-                        acc[ct][0] = fmaf(c_[0], sxv.x, fmaf(sc_[0], part[ct][0], acc[ct][0]));
-                        acc[ct][1] = fmaf(c_[0], sxv.y, fmaf(sc_[0], part[ct][1], acc[ct][1]));
-                        acc[ct][2] = fmaf(c_[1], sxv.x, fmaf(sc_[1], part[ct][2], acc[ct][2]));
-                        acc[ct][3] = fmaf(c_[1], sxv.y, fmaf(sc_[1], part[ct][3], acc[ct][3]));
+                        const float2 sxv = *reinterpret_cast<const float2*>(sx + cgrp * MP + 8 * ct + 2 * t);
+                        acc[ct][0] = fmaf(s_[0], fmaf(-c_[0], sxv.x, part[ct][0]), acc[ct][0]);
+                        acc[ct][1] = fmaf(s_[0], fmaf(-c_[0], sxv.y, part[ct][1]), acc[ct][1]);
+                        acc[ct][2] = fmaf(s_[1], fmaf(-c_[1], sxv.x, part[ct][2]), acc[ct][2]);
+                        acc[ct][3] = fmaf(s_[1], fmaf(-c_[1], sxv.y, part[ct][3]), acc[ct][3]);
 #pragma unroll
                         for (int e = 0; e < 4; ++e) part[ct][e] = 0.0f;
                     }
+                    ++cgrp;
                 }
                 load_slot(wbuf[i], sbuf[i], zbuf[i]);  // refill this slot D steps ahead
+                xoff += xstep;
                 if (++sc == spt) {                     // tile complete (same step for every warp)
-                    const int tau = tile_base + itc * T + ti;
                     if constexpr (S == 1) {
+                        const int tau = (g0 + itc) * T + ti;
                         if (tau < p.total_tiles) {
                             const int second = tau >= p.tiles_per_mat;
                             const int tile = second ? tau - p.tiles_per_mat : tau;
@@ -271,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
                             const int tj = e / (16 * M);
                             const int m = (e / 16) % M;
                             const int rr = e % 16;
-                            const int tau2 = tile_base + itc * T + tj;
+                            const int tau2 = (g0 + itc) * T + tj;
                             if (tau2 >= p.total_tiles) continue;
                             const int second = tau2 >= p.tiles_per_mat;
                             const int tile = second ? tau2 - p.tiles_per_mat : tau2;
@@ -279,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
                             if (row >= N) continue;
                             float sum = 0.0f;
 #pragma unroll
-                            for (int q = 0; q < S; ++q) sum += rbuf[((size_t)(tj * S + q) * 16 + rr) * MP + m];
+                            for (int q = 0; q < S; ++q) sum += rbuf[((tj * S + q) * 16 + rr) * MP + m];
                             __nv_bfloat16* y = static_cast<__nv_bfloat16*>(second ? p.mat[1].y : p.mat[0].y);
                             y[(int64_t)m * N + row] = __float2bfloat16_rn(sum);
                         }
@@ -290,6 +333,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
                         for (int e = 0; e < 4; ++e) acc[ct][e] = 0.0f;
                     sc = 0;
                     ++itc;
+                    xoff = step0 * xstep;
+                    cgrp = step0 / SPG;
                 }
             }
         }
@@ -331,17 +376,17 @@ cudaError_t launch_s(const GemvParams& p0, size_t smem, int sms, cudaStream_t st
     per_sm = per_sm > 2 ? 2 : per_sm;
     GemvParams p = p0;
     constexpr int T = kWarps / S;
-    const int max_ctas = sms * per_sm;
-    const int tg = (p.total_tiles + T - 1) / T;
-    p.iters = (tg + max_ctas - 1) / max_ctas;
-    const int grid = (tg + p.iters - 1) / p.iters;
+    p.tile_groups = (p.total_tiles + T - 1) / T;
+    const int grid = p.tile_groups < sms * per_sm ? p.tile_groups : sms * per_sm;
     kern<<<dim3((unsigned)grid), dim3(kThreads), smem, stream>>>(p);
     return cudaGetLastError();
 }
 
 // Splitting S: among the splits that divide the group count, the one whose
-// balanced grid wastes the fewest warp-iterations while still covering every
-// SM; ties go to the smallest S (fewest cross-warp reductions).
+// balanced partition leaves the busiest SM with the least work.  CTA b is
+// assumed to land on SM b % sms; an SM's work is the warp k-steps of its
+// CTAs; the score is the mean useful work per SM over the busiest SM's work.
+// Ties go to the smallest S (fewest cross-warp reductions).
 int choose_split(int total_tiles, int ngroups, int sms, int per_sm) {
     int best = 0;
     double best_score = -1.0;
@@ -349,12 +394,19 @@ int choose_split(int total_tiles, int ngroups, int sms, int per_sm) {
         if (ngroups % S) continue;
         const int T = kWarps / S;
         const int tg = (total_tiles + T - 1) / T;
-        const int max_ctas = sms * per_sm;
-        const int iters = (tg + max_ctas - 1) / max_ctas;
-        const int grid = (tg + iters - 1) / iters;
-        const double eff = (double)total_tiles / ((double)grid * iters * T);
-        const double fill = grid >= sms ? 1.0 : (double)grid / sms;
-        const double score = eff * fill;
+        const int grid = tg < sms * per_sm ? tg : sms * per_sm;
+        const int64_t spt = ngroups / S;
+        int64_t busiest = 0;
+        for (int sm = 0; sm < sms && sm < grid; ++sm) {
+            int64_t w = 0;
+            for (int b = sm; b < grid; b += sms) {
+                const int64_t it = ((int64_t)(b + 1) * tg) / grid - ((int64_t)b * tg) / grid;
+                w += it * kWarps * spt;
+            }
+            if (w > busiest) busiest = w;
+        }
+        const double useful = (double)total_tiles * ngroups / sms;
+        const double score = busiest > 0 ? useful / (double)busiest : 0.0;
         if (score > best_score + 1e-9) {
             best_score = score;
             best = S;
@@ -417,7 +469,7 @@ cudaError_t launch_gemv(const void* x, const GemvMat* mats, int nmat, int64_t M,
     p.G = G;
     p.tiles_per_mat = (int)((N + 15) / 16);
     p.total_tiles = p.tiles_per_mat * nmat;
-    p.iters = 0;
+    p.tile_groups = 0;
     const size_t smem = gemv_smem_bytes(M, K, G, nmat);
     if (smem == 0) return cudaErrorInvalidValue;
     int dev = 0, sms = 0;
