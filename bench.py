@@ -180,10 +180,12 @@ def run_ours(args):
     ys_dec = [torch.empty(M_DECODE, lin.N, dtype=torch.bfloat16, device=dev) for lin, _ in mats]
     ys_pre = [torch.empty(M_PREFILL, lin.N, dtype=torch.bfloat16, device=dev) for lin, _ in mats]
 
-    # One graph per (phase, matrix): `steps` back-to-back launches cycling the
-    # device copies.  A step is one launch of each graph's kernel, so the four
-    # graph times add up to the step time, and each graph time / steps is that
-    # kernel's mean launch duration on the GPU (no host launch gaps).
+    # Decode: one CUDA graph per matrix holding `steps` back-to-back GEMV
+    # launches cycling the device copies (a launch is ~20-50 us, so host launch
+    # gaps would otherwise show).  Prefill: eager launches (each ~1 ms; the call
+    # also converts x to FP16 in stream-ordered scratch).  A step is one launch
+    # per (phase, matrix), so the per-(phase, matrix) times add up to the step
+    # time, and each time / steps is that call's mean duration on the GPU.
     phases = [("dec", xs_dec, ys_dec)] + ([("pre", xs_pre, ys_pre)] if gemm_ok else [])
 
     def launch(phase, j, i, stream):
@@ -198,13 +200,12 @@ def run_ours(args):
     torch.cuda.synchronize()
     graphs = {}
     cap_stream = torch.cuda.Stream()
-    for ph, _, _ in phases:
-        for j in range(len(mats)):
-            gr = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gr, stream=cap_stream):
-                for i in range(args.steps):
-                    launch(ph, j, i, torch.cuda.current_stream())
-            graphs[(ph, j)] = gr
+    for j in range(len(mats)):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=cap_stream):
+            for i in range(args.steps):
+                launch("dec", j, i, torch.cuda.current_stream())
+        graphs[("dec", j)] = gr
     for gr in graphs.values():                          # one untimed replay each
         gr.replay()
     torch.cuda.synchronize()
@@ -212,14 +213,19 @@ def run_ours(args):
         torch.distributed.barrier()
 
     stream = torch.cuda.current_stream()
-    evs = {k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for k in graphs}
+    keys = [("dec", j) for j in range(len(mats))] + ([("pre", j) for j in range(len(mats))] if gemm_ok else [])
+    evs = {k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for k in keys}
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         torch.cuda.synchronize()
         t0.record(stream)
-        for k, gr in graphs.items():
+        for k in keys:
             evs[k][0].record(stream)
-            gr.replay()
+            if k[0] == "dec":
+                graphs[k].replay()
+            else:
+                for i in range(args.steps):
+                    launch("pre", k[1], i, stream)
             evs[k][1].record(stream)
         t1.record(stream)
         torch.cuda.synchronize()
@@ -242,7 +248,7 @@ def run_ours(args):
                                "decode M=1 (GEMV) + prefill M=2048 (tcgen05 GEMM), weights N(0,0.015), x N(0,1)",
                    "M_decode": M_DECODE, "M_prefill": M_PREFILL if gemm_ok else None, "G": G,
                    "l2": f"inputs larger than L2: {copies} rotating device copies of each 122 MB packed matrix",
-                   "timing": "CUDA-graph replay of `steps` launches per kernel, CUDA events on the replay stream",
+                   "timing": "decode: CUDA-graph replay of `steps` launches per matrix; prefill: `steps` eager calls per matrix; CUDA events on the launch stream",
                    "parallelism": f"replicas x{world}"},
     }
     # roofline, per kernel, from the CUDA-event durations inside the timed region
@@ -264,7 +270,7 @@ def run_ours(args):
         tflops = world * sum(flops) * args.steps / (sum(pre_ms) * 1e-3) / 1e12
         gemm_launch_ms = sum(pre_ms) / (len(mats) * args.steps)
         ach = (sum(flops) / len(mats)) / (gemm_launch_ms * 1e-3) / 1e12
-        roof_gemm = {"kernel": "gemm_tc (M=2048, mean of gate and down launches)", "bound": "tensor",
+        roof_gemm = {"kernel": "prefill call = x->FP16 conversion + tcgen05 GEMM (M=2048, mean of gate and down)", "bound": "tensor",
                      "achieved": round(ach, 1), "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
                      "frac": round(ach / pk["bf16_tflops_sustained"], 4),
                      "frac_of_burst_peak": round(ach / pk["bf16_tflops"], 4), "peak_source": pk["source"],
@@ -275,7 +281,7 @@ def run_ours(args):
                      "per_matrix_tflops": {lin.name: round(f / (ms / args.steps * 1e-3) / 1e12, 1)
                                            for (lin, _), f, ms in zip(mats, flops, pre_ms)}}
         out["gemm"] = {"value": round(tflops, 1), "unit": "TFLOP/s", "roofline": roof_gemm}
-        launches += len(mats) * args.steps
+        launches += 2 * len(mats) * args.steps          # x -> FP16 conversion + GEMM per call
         # the dominant kernel by time is the prefill GEMM
         out["roofline_gemv"] = roof_gemv
         out["roofline"] = roof_gemm
@@ -393,8 +399,32 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+def run_profile(args):
+    """Small case for ncu captures: one packed 70B gate matrix (8192 -> 28672,
+    ~122 MB of packed weights, above L2), `warmup` + 2 calls of one phase, no
+    timing and no CPU leg."""
+    import w4a16_weight_only_linear_b300 as w4
+    wk = wl.WORKLOADS[WORKLOAD]
+    lin = wk.linears[int(args.matrix)]
+    w = wl.weight_f16(lin.N, lin.K, wk.sigma, wl.matrix_seed(wk, int(args.matrix)), wk.outlier_frac).cuda()
+    packed = w4.w4a16_pack(w, G)
+    del w
+    M = M_DECODE if args.profile == "decode" else M_PREFILL
+    x = wl.activations_bf16(M, lin.K, wl.act_seed(wk, int(args.matrix))).cuda()
+    y = torch.empty(M, lin.N, dtype=torch.bfloat16, device="cuda")
+    for _ in range(args.warmup + 2):
+        w4.w4a16_linear(x, *packed, G, out=y)
+    torch.cuda.synchronize()
+    assert w4.w4a16_device_status() == 0
+    print(json.dumps({"profile": args.profile, "matrix": lin.name, "M": M, "N": lin.N, "K": lin.K, "G": G,
+                      "calls": args.warmup + 2}))
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--profile", choices=["decode", "prefill"], default=None,
+                    help="small case for ncu: one matrix, warmup + 2 calls of one phase")
+    ap.add_argument("--matrix", choices=["0", "1"], default="0", help="with --profile: 0 = gate, 1 = down")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
@@ -402,7 +432,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.profile:
+        run_profile(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -76,3 +76,56 @@ def test_dual_workload(M):
     xb = wl.bits_u16(x)
     assert_close(yg, oracle.linear(xb, *pg, lg.N, lg.K, G), "dual gate")
     assert_close(yu, oracle.linear(xb, *pu, lu.N, lu.K, G), "dual up")
+
+
+def _prefill_cases():
+    cases = []
+    for name, wk in wl.WORKLOADS.items():
+        if wk.dual:
+            continue
+        for j, lin in enumerate(wk.linears):
+            for G in wk.Gs:
+                for M in wk.Ms:
+                    if M > 16:
+                        cases.append(pytest.param(name, j, G, M, id=f"{name}-{lin.name}-G{G}-M{M}"))
+    return cases
+
+
+def _sample_positions(M, N, count, seed):
+    """Seeded random (m, n) pairs plus every tile corner the kernel has."""
+    rng = np.random.default_rng(seed)
+    ms = list(rng.integers(0, M, count))
+    ns = list(rng.integers(0, N, count))
+    edge_m = sorted({0, 1, M - 1, M - 2} | {v for b in range(256, M, 256) for v in (b - 1, b)})
+    edge_n = sorted({0, 1, N - 1, N - 2} | {v for b in range(128, N, 128 * 7) for v in (b - 1, b)})
+    for m in edge_m:
+        for n in edge_n:
+            ms.append(m)
+            ns.append(n)
+    return np.array(ms, np.int64), np.array(ns, np.int64)
+
+
+@pytest.mark.parametrize("name,j,G,M", _prefill_cases())
+def test_prefill_workload(name, j, G, M):
+    """Full workload sizes through w4a16_linear (the tensor-core path for M > 16).
+    Small problems are compared in full; the M = 2048 ones on >= 4096 sampled
+    outputs, each computed one by one by the oracle (relative L2 over the
+    sample, per-element bound with rms(y_ref) over the sample)."""
+    wk = wl.WORKLOADS[name]
+    lin = wk.linears[j]
+    (q, s, z), dev = _packed(name, j, G)
+    seed = wl.act_seed(wk, j) + (7 if M == 2048 else 0)   # the benchmark's prefill activations
+    x = wl.activations_bf16(M, lin.K, seed)
+    assert w4.w4a16_linear_path(M, lin.N, lin.K, G) == 2
+    y = w4.w4a16_linear(x.cuda(), *dev, G)
+    torch.cuda.synchronize()
+    xb = wl.bits_u16(x)
+    if M * lin.N * lin.K <= 4e9:
+        y_ref = oracle.linear(xb, q, s, z, lin.N, lin.K, G)
+        assert_close(y, y_ref, f"{name}/{lin.name} G={G} M={M}")
+        return
+    ms, ns = _sample_positions(M, lin.N, 4096, seed=M + lin.N)
+    y_ref = oracle.linear_sampled(xb, q, s, z, lin.K, G, ms, ns)
+    got = y.float().cpu().numpy()[ms, ns].astype(np.float64)
+    assert_close(got, y_ref, f"{name}/{lin.name} G={G} M={M} (sampled)")
+    assert np.all(np.isfinite(y.float().cpu().numpy()))

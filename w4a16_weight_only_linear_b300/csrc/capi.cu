@@ -71,7 +71,7 @@ w4a16_status linear_common(const void* x, const uint32_t* q, const void* s, cons
         if (have != 0 && need > have) return W4A16_ERR_UNSUPPORTED;
         return from_cuda(w4a16::launch_gemv(x, &mat, 1, M, N, K, G, cs));
     }
-    return from_cuda(w4a16::launch_gemm(x, mat, M, N, K, G, cs));
+    return from_cuda(w4a16::launch_gemm(x, &mat, 1, M, N, K, G, cs));
 }
 
 }  // namespace
@@ -153,9 +153,7 @@ w4a16_status w4a16_linear_dual(const void* x_bf16, const uint32_t* qweight_gate,
     const GemvMat mats[2] = {{qweight_gate, scales_gate, zeros_gate, y_gate_bf16},
                              {qweight_up, scales_up, zeros_up, y_up_bf16}};
     if (choose_path(M, K, G, 2) == 1) return from_cuda(w4a16::launch_gemv(x_bf16, mats, 2, M, N, K, G, cs));
-    st = from_cuda(w4a16::launch_gemm(x_bf16, mats[0], M, N, K, G, cs));
-    if (st != W4A16_OK) return st;
-    return from_cuda(w4a16::launch_gemm(x_bf16, mats[1], M, N, K, G, cs));
+    return from_cuda(w4a16::launch_gemm(x_bf16, mats, 2, M, N, K, G, cs));
 }
 
 int w4a16_linear_path(int64_t M, int64_t N, int64_t K, int G) {

@@ -1,15 +1,587 @@
 // gemm_tc.cu -- prefill path of the W4A16 linear layer on the tcgen05 tensor
-// cores (placeholder until the kernel lands: reports "not supported").
+// cores (any M; the library routes M > 16 here).
+//
+// At prefill many activation rows share each weight, so the layer is a dense
+// contraction bound by tensor-core throughput; the dequantisation is extra
+// CUDA-core work on the critical path (klaylearn.com glossary "Weight-Only
+// Quantisation", FAQ on prefill; multigrid.ai "Weight-Only Quantization
+// Explained", section "Where it stops being the right answer").
+//
+// Formulation.  The kernel computes the transposed product
+//     D[n, m] = sum_k W_hat[n, k] * x[m, k]      (y[m, n] = D[n, m])
+// so that the dequantised weights are the MMA's A operand, which tcgen05 can
+// read straight from tensor memory: expanded weights are written by CUDA
+// cores into TMEM and never touch shared memory or HBM.  x is the B operand,
+// brought into shared memory by TMA.
+//
+// Precision.  Operands are FP16: A = RN_fp16((q - z) * s) (the code difference
+// is exact in FP16, one rounding for the product), B = x converted from BF16
+// to FP16 once per call (exact for normal-range values), FP32 accumulation in
+// TMEM, one BF16 rounding per output.  A BF16 A operand would round W_hat to
+// 8 significant bits, which alone costs more relative error than the output
+// tolerance leaves after the BF16 output rounding; FP16 keeps 11.
+//
+// Structure: a persistent kernel, one 320-thread CTA per SM, warp-specialised.
+//   warp 0      TMA producer: 64-k slices of x (BN rows, 128-byte swizzle) and
+//               256-k slices of packed codes (128 rows x 128 bytes, swizzled)
+//   warp 1      tensor-memory owner and MMA issuer (one thread): per 64-k
+//               slice, four 128 x BN x 16 MMAs, A from TMEM, B from smem
+//   warps 2..5  dequantisers: thread = weight row = TMEM lane; codes from
+//               smem -> FP16 pairs with PRMT/LOP3 (no conversion
+//               instruction), code difference and scale in packed FP16 ->
+//               tcgen05.st into a ring of 64-k A slices in TMEM
+//   warps 6..9  epilogue: tcgen05.ld of the FP32 accumulator, BF16 rounding,
+//               stores to y
+// Tiles are 128 weight rows x BN activation rows (BN <= 256), ordered with the
+// activation tile fastest so consecutive CTAs share a weight tile in L2.
+// Every wait is bounded: on expiry the kernel records a code in the status
+// word, waits (bounded) for its own copies and MMAs in flight, frees its
+// tensor memory and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
+#include "tc.cuh"
 
 namespace w4a16 {
 
 // Per-device word that kernels set when a bounded wait gives up.
 __device__ uint32_t g_status_word = 0;
 
-cudaError_t launch_gemm(const void*, const GemvMat&, int64_t, int64_t, int64_t, int, cudaStream_t) {
-    return cudaErrorNotSupported;
+namespace {
+
+constexpr int kThreads = 320;              // 10 warps
+constexpr int kBM = 128;                   // weight rows per tile (MMA M)
+constexpr int kXS = 5;                     // x ring: slices of 64 k
+constexpr int kCS = 3;                     // code ring: slices of 256 k
+constexpr int kAS = 8;                     // A ring in TMEM: slices of 64 k (32 columns)
+constexpr uint32_t kCodeStageBytes = 128u * 128u;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kACol0 = 256;           // D uses columns [0, BN), A slices [256, 512)
+constexpr long long kSpinCycles = 1ll << 31;
+constexpr int kNumBars = 2 * kXS + 2 * kCS + 2 * kAS + 2;
+
+// Status codes (bit fields) recorded when a wait gives up.
+constexpr uint32_t kStatusProducer = 1u << 0;
+constexpr uint32_t kStatusMma = 1u << 1;
+constexpr uint32_t kStatusDequant = 1u << 2;
+constexpr uint32_t kStatusEpilogue = 1u << 3;
+constexpr uint32_t kStatusDrain = 1u << 4;
+
+struct GemmParams {
+    const unsigned short* s;   // FP16 scales [N, lds]
+    const uint32_t* z;         // packed zeros [N, ldz]
+    __nv_bfloat16* y;          // [M, N]
+    int M, N, K, BN;
+    int lds, ldz, ngroups;
+    int mtiles, tiles;
+    int nk64, nk256;
+};
+
+// Dynamic shared memory per CTA.  Never less than 120 KB, so at most one CTA
+// is resident per SM and the 512 tensor-memory columns it allocates are free.
+size_t gemm_smem_bytes(int BN) {
+    const size_t need = 1024 + (size_t)kXS * BN * 128 + (size_t)kCS * kCodeStageBytes + kNumBars * 8 + 16;
+    return need < 120 * 1024 ? 120 * 1024 : need;
+}
+
+__device__ __forceinline__ uint32_t lop3_and_or_(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ uint32_t hsub2_rn(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t hmul2_rn(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ uint4 ldg128_nc(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint32_t ldg32_nc(const void* p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+// Eight codes (one packed word, k = 8j .. 8j+7) -> four FP16 pairs
+// (k = 8j+2i in the low half, 8j+2i+1 in the high half) of RN((q - z) * s).
+// Byte i of the word holds codes 2i (low nibble) and 2i+1 (high nibble);
+// PRMT copies it into both halves, one LOP3 keeps the low nibble in the low
+// half and the high nibble at bits 4..7 of the high half and ORs in the
+// FP16 exponents of 1024 (ulp 1) and 64 (ulp 1/16), giving 1024 + q and
+// 64 + q exactly.  zz holds 1024 + z and 64 + z, so the packed subtraction
+// is the exact code difference, and one packed multiply rounds it times s.
+__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t s2, uint32_t zz, uint32_t* out) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t r = __byte_perm(w, 0u, 0x4040u + 0x0101u * i);
+        const uint32_t t = lop3_and_or_(r, 0x00F0000Fu, 0x54006400u);
+        out[i] = hmul2_rn(hsub2_rn(t, zz), s2);
+    }
+}
+
+// Scale (both halves) and zero offsets of group h of an 8-group chunk.
+__device__ __forceinline__ void group_consts(const uint4& sv, uint32_t zw, int h, bool valid, uint32_t& s2,
+                                             uint32_t& zz) {
+    const uint32_t word = (h & 4) ? ((h & 2) ? sv.w : sv.z) : ((h & 2) ? sv.y : sv.x);
+    uint32_t sb = (h & 1) ? (word >> 16) : (word & 0xFFFFu);
+    sb = valid ? sb : 0u;
+    const uint32_t z = (zw >> (4 * h)) & 0xFu;
+    s2 = sb | (sb << 16);
+    zz = ((0x5400u | (z << 4)) << 16) | (0x6400u | z);
+}
+
+struct Smem {
+    uint8_t* x;       // kXS slices of BN * 128 bytes
+    uint8_t* c;       // kCS slices of 16 KB
+    uint64_t* bar;
+    uint32_t* tmem_slot;
+    volatile int* abort_flag;
+    __device__ uint32_t x_full(int i) const { return tc::smem_u32(bar + i); }
+    __device__ uint32_t x_empty(int i) const { return tc::smem_u32(bar + kXS + i); }
+    __device__ uint32_t c_full(int i) const { return tc::smem_u32(bar + 2 * kXS + i); }
+    __device__ uint32_t c_empty(int i) const { return tc::smem_u32(bar + 2 * kXS + kCS + i); }
+    __device__ uint32_t a_full(int i) const { return tc::smem_u32(bar + 2 * kXS + 2 * kCS + i); }
+    __device__ uint32_t a_empty(int i) const { return tc::smem_u32(bar + 2 * kXS + 2 * kCS + kAS + i); }
+    __device__ uint32_t d_full() const { return tc::smem_u32(bar + 2 * kXS + 2 * kCS + 2 * kAS); }
+    __device__ uint32_t d_empty() const { return tc::smem_u32(bar + 2 * kXS + 2 * kCS + 2 * kAS + 1); }
+};
+
+// Bounded wait for a barrier phase; gives up (recording `site`) after
+// kSpinCycles, or at once when another role has given up.
+__device__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint32_t site) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (tc::mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (clock64() - t0 > kSpinCycles) {
+            *abort_flag = 1;
+            atomicOr(&g_status_word, site);
+            return false;
+        }
+    }
+}
+
+// Bounded wait used while shutting down after a give-up: ignores the abort flag.
+__device__ void drain_phase(uint32_t bar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (!tc::mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > kSpinCycles) {
+            atomicOr(&g_status_word, kStatusDrain);
+            return;
+        }
+    }
+}
+
+template <int G>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_q,
+                const GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t xbytes = (uint32_t)p.BN * 128u;
+    Smem sm;
+    sm.x = base;
+    sm.c = base + kXS * xbytes;
+    sm.bar = reinterpret_cast<uint64_t*>(sm.c + kCS * kCodeStageBytes);
+    sm.tmem_slot = reinterpret_cast<uint32_t*>(sm.bar + kNumBars);
+    sm.abort_flag = reinterpret_cast<volatile int*>(sm.tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kXS; ++i) {
+            tc::mbar_init(sm.x_full(i), 1);
+            tc::mbar_init(sm.x_empty(i), 1);
+        }
+        for (int i = 0; i < kCS; ++i) {
+            tc::mbar_init(sm.c_full(i), 1);
+            tc::mbar_init(sm.c_empty(i), 4);
+        }
+        for (int i = 0; i < kAS; ++i) {
+            tc::mbar_init(sm.a_full(i), 4);
+            tc::mbar_init(sm.a_empty(i), 1);
+        }
+        tc::mbar_init(sm.d_full(), 1);
+        tc::mbar_init(sm.d_empty(), 4);
+        *sm.abort_flag = 0;
+        tc::fence_barrier_init();
+        tc::tma_prefetch_desc(&tm_x);
+        tc::tma_prefetch_desc(&tm_q);
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tc::smem_u32(sm.tmem_slot), kTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *sm.tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int xi = 0, ci = 0;
+            uint32_t xph = 0, cph = 0;
+            long long x_issued = 0, c_issued = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < p.tiles && ok; t += gridDim.x) {
+                const int n0 = (t / p.mtiles) * kBM, m0 = (t % p.mtiles) * p.BN;
+                for (int kb = 0; kb < p.nk64; ++kb) {
+                    if ((kb & 3) == 0) {
+                        if (!(ok = wait_phase(sm.c_empty(ci), cph ^ 1u, sm.abort_flag, kStatusProducer))) break;
+                        tc::mbar_arrive_expect_tx(sm.c_full(ci), kCodeStageBytes);
+                        tc::tma_load_2d(tc::smem_u32(sm.c + ci * kCodeStageBytes), &tm_q, (kb >> 2) * 32, n0,
+                                        sm.c_full(ci));
+                        ++c_issued;
+                        if (++ci == kCS) { ci = 0; cph ^= 1u; }
+                    }
+                    if (!(ok = wait_phase(sm.x_empty(xi), xph ^ 1u, sm.abort_flag, kStatusProducer))) break;
+                    tc::mbar_arrive_expect_tx(sm.x_full(xi), xbytes);
+                    tc::tma_load_2d(tc::smem_u32(sm.x + xi * xbytes), &tm_x, kb * 64, m0, sm.x_full(xi));
+                    ++x_issued;
+                    if (++xi == kXS) { xi = 0; xph ^= 1u; }
+                }
+            }
+            if (!ok) {   // wait for the copies this thread started
+                for (int s = 0; s < kXS; ++s)
+                    if (x_issued > s) drain_phase(sm.x_full(s), s < xi ? xph : (xph ^ 1u));
+                for (int s = 0; s < kCS; ++s)
+                    if (c_issued > s) drain_phase(sm.c_full(s), s < ci ? cph : (cph ^ 1u));
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = tc::idesc_f16_f32(kBM, p.BN);
+            int xi = 0, ai = 0;
+            uint32_t xph = 0, aph = 0, dph = 0, d_commits = 0;
+            bool ok = true;
+            bool issued = false;
+            for (int t = blockIdx.x; t < p.tiles && ok; t += gridDim.x) {
+                if (!(ok = wait_phase(sm.d_empty(), dph ^ 1u, sm.abort_flag, kStatusMma))) break;
+                dph ^= 1u;
+                tc::tc_fence_after();
+                for (int kb = 0; kb < p.nk64; ++kb) {
+                    if (!(ok = wait_phase(sm.x_full(xi), xph, sm.abort_flag, kStatusMma))) break;
+                    if (!(ok = wait_phase(sm.a_full(ai), aph, sm.abort_flag, kStatusMma))) break;
+                    tc::tc_fence_after();
+                    const uint64_t bdesc = tc::smem_desc_k_sw128(tc::smem_u32(sm.x + xi * xbytes));
+                    const uint32_t a_t = tmem + kACol0 + (uint32_t)ai * 32u;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc::mma_f16_ts(tmem, a_t + 8u * kk, bdesc + (uint64_t)(2 * kk), idesc,
+                                       (kb | kk) != 0 ? 1u : 0u);
+                    issued = true;
+                    tc::mma_commit(sm.x_empty(xi));
+                    tc::mma_commit(sm.a_empty(ai));
+                    if (++xi == kXS) { xi = 0; xph ^= 1u; }
+                    if (++ai == kAS) { ai = 0; aph ^= 1u; }
+                }
+                if (!ok) break;
+                tc::mma_commit(sm.d_full());
+                ++d_commits;
+            }
+            if (!ok && issued) {   // wait for the MMAs this thread issued
+                tc::mma_commit(sm.d_full());
+                drain_phase(sm.d_full(), d_commits & 1u);
+            }
+        }
+    } else if (warp < 6) {
+        // ------------------------------------------------------------ dequantisers
+        const int qd = warp & 3;
+        const int r = qd * 32 + lane;                       // weight row in the tile = TMEM lane
+        const uint32_t a_lane = tmem + ((uint32_t)(qd * 32) << 16) + kACol0;
+        int ci = 0, ai = 0;
+        uint32_t cph = 0, aph = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < p.tiles && ok; t += gridDim.x) {
+            const int n = (t / p.mtiles) * kBM + r;
+            const bool rv = n < p.N;
+            const unsigned short* srow = p.s + (int64_t)(rv ? n : 0) * p.lds;
+            const uint32_t* zrow = p.z + (int64_t)(rv ? n : 0) * p.ldz;
+            for (int ks = 0; ks < p.nk256 && ok; ++ks) {
+                const int chunk = (ks * (256 / G)) >> 3;           // 8-group chunk holding this slice's groups
+                uint4 sv = make_uint4(0u, 0u, 0u, 0u);
+                uint32_t zw = 0u;
+                if (rv) {
+                    sv = ldg128_nc(srow + chunk * 8);
+                    zw = ldg32_nc(zrow + chunk);
+                }
+                ok = wait_phase(sm.c_full(ci), cph, sm.abort_flag, kStatusDequant);
+                if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
+                const uint32_t rowp = tc::smem_u32(sm.c + ci * kCodeStageBytes) + (uint32_t)r * 128u;
+                const int nsub = min(4, p.nk64 - ks * 4);
+                for (int sub = 0; sub < nsub; ++sub) {
+                    ok = wait_phase(sm.a_empty(ai), aph ^ 1u, sm.abort_flag, kStatusDequant);
+                    if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
+                    tc::tc_fence_after();
+                    const uint4 w0 = lds128(rowp + ((uint32_t)((2 * sub) ^ (r & 7)) << 4));
+                    const uint4 w1 = lds128(rowp + ((uint32_t)((2 * sub + 1) ^ (r & 7)) << 4));
+                    const int ga = (ks * 256 + sub * 64) / G;        // group of the slice's first code
+                    uint32_t s2a, zza, s2b, zzb;
+                    group_consts(sv, zw, ga & 7, ga < p.ngroups, s2a, zza);
+                    if constexpr (G == 32) {
+                        group_consts(sv, zw, (ga + 1) & 7, ga + 1 < p.ngroups, s2b, zzb);
+                    } else {
+                        s2b = s2a;
+                        zzb = zza;
+                    }
+                    uint32_t a[32];
+                    dequant_word(w0.x, s2a, zza, a + 0);
+                    dequant_word(w0.y, s2a, zza, a + 4);
+                    dequant_word(w0.z, s2a, zza, a + 8);
+                    dequant_word(w0.w, s2a, zza, a + 12);
+                    dequant_word(w1.x, s2b, zzb, a + 16);
+                    dequant_word(w1.y, s2b, zzb, a + 20);
+                    dequant_word(w1.z, s2b, zzb, a + 24);
+                    dequant_word(w1.w, s2b, zzb, a + 28);
+                    tc::tmem_st32_wait(a_lane + (uint32_t)ai * 32u, a);
+                    tc::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(sm.a_full(ai));
+                    if (++ai == kAS) { ai = 0; aph ^= 1u; }
+                }
+                if (!ok) break;
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(sm.c_empty(ci));
+                if (++ci == kCS) { ci = 0; cph ^= 1u; }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int qd = warp & 3;
+        const int r = qd * 32 + lane;
+        const uint32_t d_lane = tmem + ((uint32_t)(qd * 32) << 16);
+        uint32_t dph = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < p.tiles && ok; t += gridDim.x) {
+            const int n = (t / p.mtiles) * kBM + r, m0 = (t % p.mtiles) * p.BN;
+            ok = wait_phase(sm.d_full(), dph, sm.abort_flag, kStatusEpilogue);
+            if (!__all_sync(0xFFFFFFFFu, ok)) break;
+            dph ^= 1u;
+            tc::tc_fence_after();
+            uint32_t packed[128];
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+                if (ch * 32 < p.BN) {
+                    uint32_t v[32];
+                    tc::tmem_ld32_wait(d_lane + (uint32_t)ch * 32u, v);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const __nv_bfloat162 b =
+                            __floats2bfloat162_rn(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+                        packed[ch * 16 + j] = *reinterpret_cast<const uint32_t*>(&b);
+                    }
+                }
+            }
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(sm.d_empty());
+            if (n < p.N) {
+                unsigned short* yc = reinterpret_cast<unsigned short*>(p.y) + n;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    if (ch * 32 < p.BN) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int m = m0 + ch * 32 + j;
+                            if (m < p.M) {
+                                const uint32_t pr = packed[ch * 16 + (j >> 1)];
+                                yc[(int64_t)m * p.N] = (unsigned short)((j & 1) ? (pr >> 16) : (pr & 0xFFFFu));
+                            }
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+// BF16 -> FP16, round to nearest even (exact for normal-range values).
+__global__ void __launch_bounds__(256) bf16_to_f16_kernel(const uint4* __restrict__ x, uint4* __restrict__ out,
+                                                          int64_t nvec) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
+        const uint4 v = x[i];
+        const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const __half2 h = __floats2half2_rn(bf16lo_to_f32(in[j]), bf16hi_to_f32(in[j]));
+            o[j] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        out[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+// ---- host side -----------------------------------------------------------------
+
+constexpr int kMaxDevices = 64;
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// 2-D row-major tensor [outer][inner], 128-byte swizzled boxes.
+bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                 uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t es[2] = {1, 1};
+    return enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Stream-ordered scratch from a library-private pool per device, which keeps
+// up to 1 GiB cached between calls.
+cudaError_t scratch_alloc(void** ptr, size_t bytes, cudaStream_t stream) {
+    static cudaMemPool_t pools[kMaxDevices] = {};
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    cudaMemPool_t pool;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!pools[dev]) {
+            cudaMemPoolProps props = {};
+            props.allocType = cudaMemAllocationTypePinned;
+            props.location.type = cudaMemLocationTypeDevice;
+            props.location.id = dev;
+            e = cudaMemPoolCreate(&pools[dev], &props);
+            if (e != cudaSuccess) {
+                pools[dev] = nullptr;
+                return e;
+            }
+            uint64_t keep = uint64_t(1) << 30;
+            cudaMemPoolSetAttribute(pools[dev], cudaMemPoolAttrReleaseThreshold, &keep);
+        }
+        pool = pools[dev];
+    }
+    return cudaMallocFromPoolAsync(ptr, bytes, pool, stream);
+}
+
+template <int G>
+cudaError_t launch_g(const CUtensorMap& tmx, const CUtensorMap& tmq, const GemmParams& p, int grid, size_t smem,
+                     cudaStream_t stream) {
+    static int cached[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if ((int)smem > cached[dev]) {
+        e = cudaFuncSetAttribute(gemm_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        cached[dev] = (int)smem;
+    }
+    gemm_kernel<G><<<grid, kThreads, smem, stream>>>(tmx, tmq, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int gemm_tile_n(int64_t M) { return M >= 256 ? 256 : (int)((M + 31) / 32 * 32); }
+
+cudaError_t launch_gemm(const void* x, const GemvMat* mats, int nmat, int64_t M, int64_t N, int64_t K, int G,
+                        cudaStream_t stream) {
+    if (M < 1 || N < 1 || K < 1) return cudaSuccess;
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX || K % 32 != 0) return cudaErrorInvalidValue;
+    if (!tensor_map_encoder()) return cudaErrorNotSupported;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+
+    // FP16 copy of x (the B operand), shared by every matrix of the call
+    void* x16 = nullptr;
+    const size_t xbytes = (size_t)M * (size_t)K * 2;
+    if ((e = scratch_alloc(&x16, xbytes, stream)) != cudaSuccess) return e;
+    {
+        const int64_t nvec = M * K / 8;
+        int64_t blocks = (nvec + 255) / 256;
+        if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
+        bf16_to_f16_kernel<<<(unsigned)blocks, 256, 0, stream>>>(static_cast<const uint4*>(x),
+                                                                 static_cast<uint4*>(x16), nvec);
+        e = cudaGetLastError();
+    }
+    GemmParams p;
+    p.M = (int)M;
+    p.N = (int)N;
+    p.K = (int)K;
+    p.BN = gemm_tile_n(M);
+    p.lds = (int)scales_ld(K, G);
+    p.ldz = (int)zeros_ld(K, G);
+    p.ngroups = (int)(K / G);
+    p.mtiles = (int)((M + p.BN - 1) / p.BN);
+    const int64_t tiles = ((N + kBM - 1) / kBM) * p.mtiles;
+    if (tiles > INT32_MAX) e = cudaErrorInvalidValue;
+    p.tiles = (int)tiles;
+    p.nk64 = (int)((K + 63) / 64);
+    p.nk256 = (int)((K + 255) / 256);
+    const int grid = (int)(tiles < sms ? tiles : sms);
+    const size_t smem = gemm_smem_bytes(p.BN);
+    CUtensorMap tmx;
+    if (e == cudaSuccess &&
+        !make_map_2d(&tmx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x16, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, 64,
+                     (uint32_t)p.BN))
+        e = cudaErrorInvalidValue;
+    for (int i = 0; i < nmat && e == cudaSuccess; ++i) {
+        CUtensorMap tmq;
+        if (!make_map_2d(&tmq, CU_TENSOR_MAP_DATA_TYPE_UINT32, mats[i].q, (uint64_t)(K / 8), (uint64_t)N,
+                         (uint64_t)(K / 8) * 4, 32, kBM)) {
+            e = cudaErrorInvalidValue;
+            break;
+        }
+        p.s = static_cast<const unsigned short*>(mats[i].s);
+        p.z = mats[i].z;
+        p.y = static_cast<__nv_bfloat16*>(mats[i].y);
+        switch (G) {
+            case 32: e = launch_g<32>(tmx, tmq, p, grid, smem, stream); break;
+            case 64: e = launch_g<64>(tmx, tmq, p, grid, smem, stream); break;
+            case 128: e = launch_g<128>(tmx, tmq, p, grid, smem, stream); break;
+            case 256: e = launch_g<256>(tmx, tmq, p, grid, smem, stream); break;
+            default: e = cudaErrorInvalidValue;
+        }
+    }
+    const cudaError_t ef = cudaFreeAsync(x16, stream);
+    return e != cudaSuccess ? e : ef;
 }
 
 cudaError_t read_and_clear_status(uint32_t* word) {

@@ -28,9 +28,12 @@ size_t device_smem_optin();
 cudaError_t launch_gemv(const void* x, const GemvMat* mats, int nmat, int64_t M, int64_t N, int64_t K, int G,
                         cudaStream_t stream);
 
-// Tensor-core path (any M); returns cudaErrorNotSupported until built for the shape.
-cudaError_t launch_gemm(const void* x, const GemvMat& mat, int64_t M, int64_t N, int64_t K, int G,
+// Tensor-core path (any M): y_i = x * W_hat_i^T for nmat matrices sharing x
+// (x is converted to FP16 once, into stream-ordered scratch).
+cudaError_t launch_gemm(const void* x, const GemvMat* mats, int nmat, int64_t M, int64_t N, int64_t K, int G,
                         cudaStream_t stream);
+// Activation rows per tensor-core tile for M rows.
+int gemm_tile_n(int64_t M);
 
 // Per-device status word written by kernels whose bounded waits gave up.
 cudaError_t read_and_clear_status(uint32_t* word);
