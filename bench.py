@@ -270,11 +270,12 @@ def run_ours(args):
         tflops = world * sum(flops) * args.steps / (sum(pre_ms) * 1e-3) / 1e12
         gemm_launch_ms = sum(pre_ms) / (len(mats) * args.steps)
         ach = (sum(flops) / len(mats)) / (gemm_launch_ms * 1e-3) / 1e12
-        roof_gemm = {"kernel": "prefill call = x->FP16 conversion + tcgen05 GEMM (M=2048, mean of gate and down)", "bound": "tensor",
-                     "achieved": round(ach, 1), "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                     "frac": round(ach / pk["bf16_tflops_sustained"], 4),
-                     "frac_of_burst_peak": round(ach / pk["bf16_tflops"], 4), "peak_source": pk["source"],
-                     "peak_kind": "sustained (timed inside a seconds-long step loop)",
+        roof_gemm = {"kernel": "prefill call = x->FP16 conversion + tcgen05 GEMM (M=2048, mean of gate and down)",
+                     "bound": "tensor", "achieved": round(ach, 1), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": round(ach / pk["bf16_tflops"], 4),
+                     "frac_of_sustained_peak": round(ach / pk["bf16_tflops_sustained"], 4),
+                     "peak_source": pk["source"],
+                     "peak_kind": "burst (dense BF16 GEMM timed alone); FP16 kind::f16 runs at the same rate",
                      "traffic": stored_traffic("gemm_tc.cu", "gemm_ffn70b_M2048"),
                      "algorithmic_flops_per_launch": sum(flops) / len(mats),
                      "launch_us": round(gemm_launch_ms * 1e3, 3),
