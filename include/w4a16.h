@@ -162,6 +162,33 @@ W4A16_API w4a16_status w4a16_linear_gemm(const void* x_bf16, const uint32_t* qwe
                                void* y_bf16, w4a16_stream_t stream);
 
 /*
+ * w4a16_linear_gemm_noalloc: the tensor-core path of w4a16_linear_gemm for
+ * callers that may not allocate device memory while they run the layer (an
+ * engine that fixes its memory budget at start-up and forbids later
+ * allocations, or code that records its launches into a CUDA graph that must
+ * hold no memory nodes).  The pages this library follows have no counterpart
+ * to this entry point; it is a deployment variant of the same computation.
+ *
+ * Same arguments and result as w4a16_linear_gemm.  The per-call FP16 copy of
+ * x, which the allocating entry points take from a stream-ordered pool, here
+ * lives in one file-scope device array of W4A16_NOALLOC_MAX_X_ELEMS FP16
+ * values (16 MiB), which every GPU that loads the library holds until the
+ * process exits.  The call itself allocates and frees nothing.
+ *   - M * K > W4A16_NOALLOC_MAX_X_ELEMS: W4A16_ERR_UNSUPPORTED, nothing runs.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current).  Make that first call before
+ *     any stream capture on the device.
+ *   - All calls share the array: two calls whose kernels may overlap on the
+ *     GPU (different streams with no ordering between them) race on it and
+ *     give undefined results.  Calls ordered on one stream are safe; each
+ *     call overwrites the part of the array it uses before reading it.
+ */
+#define W4A16_NOALLOC_MAX_X_ELEMS (8u * 1024u * 1024u)
+W4A16_API w4a16_status w4a16_linear_gemm_noalloc(const void* x_bf16, const uint32_t* qweight,
+                                       const void* scales_f16, const uint32_t* zeros, int64_t M, int64_t N,
+                                       int64_t K, int G, void* y_bf16, w4a16_stream_t stream);
+
+/*
  * Which kernel w4a16_linear would run for this shape: 1 = GEMV, 2 = GEMM,
  * 0 = the shape is rejected.  Host-only, no device access.
  */

@@ -37,6 +37,7 @@ EXPORTS = {
     "w4a16_linear_dual": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp, _vp], _i32),
     "w4a16_linear_gemv": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp], _i32),
     "w4a16_linear_gemm": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp], _i32),
+    "w4a16_linear_gemm_noalloc": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp], _i32),
     "w4a16_linear_path": ([_i64, _i64, _i64, _i32], _i32),
     "w4a16_device_status": ([_vp], _i32),
 }
@@ -162,6 +163,17 @@ def w4a16_linear_gemv(x, q, s, z, G, out=None, stream=None):
 def w4a16_linear_gemm(x, q, s, z, G, out=None, stream=None):
     """Tensor-core kernel only (any M)."""
     return _linear("w4a16_linear_gemm", x, q, s, z, q.shape[0], G, out, stream)
+
+
+def w4a16_linear_gemm_noalloc(x, q, s, z, G, out=None, stream=None):
+    """Tensor-core kernel only, with its FP16 copy of x in the library's fixed
+    device array instead of an allocation (M * K <= NOALLOC_MAX_X_ELEMS).  The
+    C call allocates nothing; pass `out` to keep this wrapper from allocating
+    y with torch."""
+    return _linear("w4a16_linear_gemm_noalloc", x, q, s, z, q.shape[0], G, out, stream)
+
+
+NOALLOC_MAX_X_ELEMS = 8 * 1024 * 1024
 
 
 def w4a16_linear_dual(x, gate, up, G, out=None, stream=None):

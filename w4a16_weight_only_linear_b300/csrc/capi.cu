@@ -156,6 +156,21 @@ w4a16_status w4a16_linear_dual(const void* x_bf16, const uint32_t* qweight_gate,
     return from_cuda(w4a16::launch_gemm(x_bf16, mats, 2, M, N, K, G, cs));
 }
 
+w4a16_status w4a16_linear_gemm_noalloc(const void* x_bf16, const uint32_t* qweight, const void* scales_f16,
+                                       const uint32_t* zeros, int64_t M, int64_t N, int64_t K, int G,
+                                       void* y_bf16, w4a16_stream_t stream) {
+    w4a16_status st = check_weight_shape(N, K, G);
+    if (st != W4A16_OK) return st;
+    if (M < 0 || M > kMaxDim) return W4A16_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return W4A16_OK;
+    if ((st = check_weights(qweight, scales_f16, zeros)) != W4A16_OK) return st;
+    if (!x_bf16 || !y_bf16) return W4A16_ERR_INVALID_ARG;
+    if (!aligned16(x_bf16) || !aligned16(y_bf16)) return W4A16_ERR_MISALIGNED;
+    if (M * K > (int64_t)W4A16_NOALLOC_MAX_X_ELEMS) return W4A16_ERR_UNSUPPORTED;
+    const GemvMat mat{qweight, scales_f16, zeros, y_bf16};
+    return from_cuda(w4a16::launch_gemm_noalloc(x_bf16, mat, M, N, K, G, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int w4a16_linear_path(int64_t M, int64_t N, int64_t K, int G) {
     if (check_weight_shape(N, K, G) != W4A16_OK || M < 0) return 0;
     return choose_path(M, K, G, 1);

@@ -42,6 +42,7 @@
 
 #include <mutex>
 
+#include "../../include/w4a16.h"
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
@@ -582,6 +583,95 @@ cudaError_t launch_gemm(const void* x, const GemvMat* mats, int nmat, int64_t M,
     }
     const cudaError_t ef = cudaFreeAsync(x16, stream);
     return e != cudaSuccess ? e : ef;
+}
+
+
+// ---- tensor-core path without any allocation ----------------------------------
+//
+// Some callers cannot allocate device memory while they run the layer: an
+// engine that owns a fixed memory budget and forbids allocations after
+// start-up, or code that records its launches into a CUDA graph and must not
+// add memory nodes to it.  For them the FP16 copy of x lives in one
+// file-scope device array of fixed size instead of a stream-ordered
+// allocation.  Every GPU that loads the library holds this array until the
+// process exits.  All calls share it, so two calls whose kernels overlap on
+// the GPU (different streams, no ordering between them) race on its contents.
+constexpr size_t kNoAllocScratchBytes = (size_t)W4A16_NOALLOC_MAX_X_ELEMS * 2;
+static __device__ __align__(256) uint8_t g_noalloc_x16[kNoAllocScratchBytes];
+
+// Device address of the array, looked up once per device with that device
+// current (in host code the symbol itself is only a host-side stand-in).
+cudaError_t noalloc_scratch(void** ptr) {
+    static void* addr[kMaxDevices] = {};
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_x16);
+        if (e != cudaSuccess) return e;
+        addr[dev] = p;
+    }
+    *ptr = addr[dev];
+    return cudaSuccess;
+}
+
+cudaError_t launch_gemm_noalloc(const void* x, const GemvMat& mat, int64_t M, int64_t N, int64_t K, int G,
+                                cudaStream_t stream) {
+    if (M < 1 || N < 1 || K < 1) return cudaSuccess;
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX || K % 32 != 0) return cudaErrorInvalidValue;
+    if (M * K > (int64_t)W4A16_NOALLOC_MAX_X_ELEMS) return cudaErrorNotSupported;
+    if (!tensor_map_encoder()) return cudaErrorNotSupported;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    void* x16 = nullptr;
+    if ((e = noalloc_scratch(&x16)) != cudaSuccess) return e;
+    {
+        const int64_t nvec = M * K / 8;
+        int64_t blocks = (nvec + 255) / 256;
+        if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
+        bf16_to_f16_kernel<<<(unsigned)blocks, 256, 0, stream>>>(static_cast<const uint4*>(x),
+                                                                 static_cast<uint4*>(x16), nvec);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    GemmParams p;
+    p.M = (int)M;
+    p.N = (int)N;
+    p.K = (int)K;
+    p.BN = gemm_tile_n(M);
+    p.lds = (int)scales_ld(K, G);
+    p.ldz = (int)zeros_ld(K, G);
+    p.ngroups = (int)(K / G);
+    p.mtiles = (int)((M + p.BN - 1) / p.BN);
+    const int64_t tiles = ((N + kBM - 1) / kBM) * p.mtiles;
+    if (tiles > INT32_MAX) return cudaErrorInvalidValue;
+    p.tiles = (int)tiles;
+    p.nk64 = (int)((K + 63) / 64);
+    p.nk256 = (int)((K + 255) / 256);
+    const int grid = (int)(tiles < sms ? tiles : sms);
+    const size_t smem = gemm_smem_bytes(p.BN);
+    CUtensorMap tmx, tmq;
+    if (!make_map_2d(&tmx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x16, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, 64,
+                     (uint32_t)p.BN))
+        return cudaErrorInvalidValue;
+    if (!make_map_2d(&tmq, CU_TENSOR_MAP_DATA_TYPE_UINT32, mat.q, (uint64_t)(K / 8), (uint64_t)N,
+                     (uint64_t)(K / 8) * 4, 32, kBM))
+        return cudaErrorInvalidValue;
+    p.s = static_cast<const unsigned short*>(mat.s);
+    p.z = mat.z;
+    p.y = static_cast<__nv_bfloat16*>(mat.y);
+    switch (G) {
+        case 32: return launch_g<32>(tmx, tmq, p, grid, smem, stream);
+        case 64: return launch_g<64>(tmx, tmq, p, grid, smem, stream);
+        case 128: return launch_g<128>(tmx, tmq, p, grid, smem, stream);
+        case 256: return launch_g<256>(tmx, tmq, p, grid, smem, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 cudaError_t read_and_clear_status(uint32_t* word) {

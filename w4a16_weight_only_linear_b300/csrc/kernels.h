@@ -32,6 +32,11 @@ cudaError_t launch_gemv(const void* x, const GemvMat* mats, int nmat, int64_t M,
 // (x is converted to FP16 once, into stream-ordered scratch).
 cudaError_t launch_gemm(const void* x, const GemvMat* mats, int nmat, int64_t M, int64_t N, int64_t K, int G,
                         cudaStream_t stream);
+// The same tensor-core path for one matrix with the FP16 copy of x in a
+// fixed-size file-scope device array (no allocation; M * K bounded by the
+// header's W4A16_NOALLOC_MAX_X_ELEMS, else cudaErrorNotSupported).
+cudaError_t launch_gemm_noalloc(const void* x, const GemvMat& mat, int64_t M, int64_t N, int64_t K, int G,
+                                cudaStream_t stream);
 // Activation rows per tensor-core tile for M rows.
 int gemm_tile_n(int64_t M);
 
