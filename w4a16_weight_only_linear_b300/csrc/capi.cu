@@ -43,12 +43,8 @@ w4a16_status from_cuda(cudaError_t e) {
 }
 
 // Path for a shape whose arguments are valid: 1 = GEMV, 2 = GEMM.
-int choose_path(int64_t M, int64_t K, int G, int ntiles) {
-    if (M <= 16) {
-        const size_t need = w4a16::gemv_smem_bytes(M, K, G, ntiles);
-        const size_t have = w4a16::device_smem_optin();
-        if (need != 0 && (have == 0 || need <= have)) return 1;
-    }
+int choose_path(int64_t M, int64_t N, int64_t K, int G, int nmat) {
+    if (M <= 16 && w4a16::gemv_fits(M, N, K, G, nmat)) return 1;
     return 2;
 }
 
@@ -61,14 +57,11 @@ w4a16_status linear_common(const void* x, const uint32_t* q, const void* s, cons
     if ((st = check_weights(q, s, z)) != W4A16_OK) return st;
     if (!x || !y) return W4A16_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(y)) return W4A16_ERR_MISALIGNED;
-    int path = force ? force : choose_path(M, K, G, 1);
+    int path = force ? force : choose_path(M, N, K, G, 1);
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     GemvMat mat{q, s, z, y};
     if (path == 1) {
-        if (M > 16) return W4A16_ERR_UNSUPPORTED;
-        const size_t need = w4a16::gemv_smem_bytes(M, K, G, 1);
-        const size_t have = w4a16::device_smem_optin();
-        if (have != 0 && need > have) return W4A16_ERR_UNSUPPORTED;
+        if (M > 16 || !w4a16::gemv_fits(M, N, K, G, 1)) return W4A16_ERR_UNSUPPORTED;
         return from_cuda(w4a16::launch_gemv(x, &mat, 1, M, N, K, G, cs));
     }
     return from_cuda(w4a16::launch_gemm(x, &mat, 1, M, N, K, G, cs));
@@ -152,7 +145,7 @@ w4a16_status w4a16_linear_dual(const void* x_bf16, const uint32_t* qweight_gate,
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     const GemvMat mats[2] = {{qweight_gate, scales_gate, zeros_gate, y_gate_bf16},
                              {qweight_up, scales_up, zeros_up, y_up_bf16}};
-    if (choose_path(M, K, G, 2) == 1) return from_cuda(w4a16::launch_gemv(x_bf16, mats, 2, M, N, K, G, cs));
+    if (choose_path(M, N, K, G, 2) == 1) return from_cuda(w4a16::launch_gemv(x_bf16, mats, 2, M, N, K, G, cs));
     return from_cuda(w4a16::launch_gemm(x_bf16, mats, 2, M, N, K, G, cs));
 }
 
@@ -173,7 +166,7 @@ w4a16_status w4a16_linear_gemm_noalloc(const void* x_bf16, const uint32_t* qweig
 
 int w4a16_linear_path(int64_t M, int64_t N, int64_t K, int G) {
     if (check_weight_shape(N, K, G) != W4A16_OK || M < 0) return 0;
-    return choose_path(M, K, G, 1);
+    return choose_path(M, N, K, G, 1);
 }
 
 w4a16_status w4a16_device_status(uint32_t* detail) {

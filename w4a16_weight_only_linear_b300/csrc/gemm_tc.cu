@@ -680,7 +680,11 @@ cudaError_t read_and_clear_status(uint32_t* word) {
     e = cudaMemcpyFromSymbol(word, g_status_word, sizeof(uint32_t));
     if (e != cudaSuccess) return e;
     const uint32_t zero = 0;
-    return cudaMemcpyToSymbol(g_status_word, &zero, sizeof(uint32_t));
+    if ((e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof(uint32_t))) != cudaSuccess) return e;
+    uint32_t gw = 0;
+    e = gemv_take_status(&gw);
+    *word |= gw;
+    return e;
 }
 
 }  // namespace w4a16

@@ -7,448 +7,737 @@
 // File", section 2 "Moving fewer bytes can make decode faster": packed
 // weights decoded block by block straight into the accumulation).
 //
-// Structure.  Work is cut into tiles of 16 weight rows x all of K.  A CTA of
-// 8 warps handles T = 8/S tiles at a time, S warps splitting each tile's
-// groups; the grid is sized so every CTA gets the same number of such
-// iterations (a contiguous run of tiles), with at most two CTAs per SM.
-//   1. every thread first issues 128-bit loads for its next D k-steps of
-//      packed codes (and the scale / zero of their groups), so HBM latency
-//      overlaps everything else; the ring of loads runs across tile
-//      boundaries, so the stream of codes never drains between tiles;
-//   2. x [M,K] is staged once per CTA in shared memory, permuted into the
-//      warp-MMA B-fragment order, with FP32 per-group sums sum_k x;
-//   3. codes become exact BF16 integers 128+q with one LOP3 per pair (no
-//      conversion instruction) and meet x in warp MMA m16n8k16 with FP32
-//      accumulation; per group acc += s*P - (128+z)*s*sum_k x, which equals
-//      s * sum_k x_k (q_k - z) with every product exact;
-//   4. with S > 1, the S partial sums of a tile are added through shared
-//      memory in a fixed order; every output is rounded to BF16 once.
-// The warp MMA serves as a wide exact dot-product instruction: one MMA
-// consumes 256 codes, keeping the instruction count near one per weight so
-// the kernel stays on the memory bound, not the issue bound.
+// Geometry.  Each weight row's K codes are cut into P equal segments, and a
+// virtual row is one (row, segment) pair: the packed matrix [N, K/8] words is
+// read as [N*P, K/(8P)].  A tile is 16 virtual rows = R = 16/P weight rows;
+// the 16 rows of a warp MMA m16n8k16 are the tile's virtual rows, and the MMA's
+// B columns hold the P segments of x (times M activation rows; P*M <= 8, or
+// two column blocks for M > 8).  So one MMA advances all segments of R rows at
+// once, and only the diagonal (segment of the row == segment of the column)
+// of D is kept.  At M = 1 a tile is 2 weight rows, which lets the grid split
+// the rows evenly over the SMs.
+//
+// Data path.  One CTA per SM takes a balanced contiguous range of tiles; its
+// work is (tile, 256-code chunk) units, split into contiguous runs over 12
+// warps.  Each warp streams its own units with TMA (16 virtual rows x 128
+// bytes per unit, 128-byte swizzle) into a private ring of shared-memory
+// stages, so no load instruction sits on the code path.  Per word of 8 codes
+// the lane makes four FP16 pairs with one shift and four LOP3s: the FP16
+// exponents of 1024 (ulp 1) and 64 (ulp 1/16) turn a nibble at bits 0..3 or
+// 4..7 of a half into the exact values 1024 + q and 64 + q.  These meet x
+// (converted to FP16 once per CTA and staged in shared memory in fragment
+// order) in the warp MMA with FP32 accumulation.  At the end of each group the
+// lane subtracts the staged sum of (1024 or 64) * x plus z * sum x, scales by
+// s and accumulates; at the end of a tile the diagonal is reduced over
+// segments.  Warps that share a tile (run boundaries) leave partial sums in
+// fixed slots, added in a fixed order at the end, so results are
+// deterministic.  Every output is rounded to BF16 once.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
+#include "tc.cuh"
 
 namespace w4a16 {
 
+// Per-device word the decode kernel sets when a bounded wait gives up (read
+// and cleared together with the tensor-core path's word).
+__device__ uint32_t g_gemv_status = 0;
+
 namespace {
 
-constexpr int kWarps = 8;
+constexpr int kWarps = 12;
 constexpr int kThreads = kWarps * 32;
+constexpr int kUnitBytes = 2048;          // 16 virtual rows x 128 bytes (256 codes)
+constexpr int kSlots = 4;                 // partial-sum slots per output (warps sharing a tile)
+constexpr int kMaxDevices = 64;
+constexpr long long kSpinCycles = 1ll << 31;
+constexpr uint32_t kStatusGemv = 1u << 8;
+constexpr uint32_t kStatusGemvDrain = 1u << 9;
+
+// MMA row i (< 8) of a warp reads virtual row sigma(i) = i/2 + 4*(i%2) of the
+// tile (and row i + 8 reads sigma(i) + 8): lanes that share a shared-memory
+// phase then hit swizzle patterns that differ in bit 2, so 128-bit code loads
+// are free of bank conflicts.
+__device__ __forceinline__ int sigma8(int i) { return (i >> 1) + ((i & 1) << 2); }
 
 struct GemvParams {
-    const __nv_bfloat16* x;
-    GemvMat mat[2];
-    int64_t N, K;
-    int M, G;
-    int tiles_per_mat;   // ceil(N / 16)
-    int total_tiles;     // tiles_per_mat * number of matrices
-    int tile_groups;     // ceil(total_tiles / T); CTA b takes groups [b*tg/grid, (b+1)*tg/grid)
+    const __nv_bfloat16* x;                // [M, K]
+    const unsigned short* s[2];            // FP16 scales [N, lds]
+    const uint32_t* z[2];                  // zeros [N, ldz]
+    __nv_bfloat16* y[2];                   // [M, N]
+    int M, N, K, G;
+    int P, R, cols, xcols;                 // segments, weight rows per tile, B columns used (P*H*M),
+                                           // staged x columns (P*M)
+    int Ks, C, ngs, ng;                    // codes per segment padded to whole chunks (C of 256), groups
+                                           // per padded segment, groups per row
+    int lds, ldz;
+    int tiles_per_mat, total_tiles;
+    int warps;                             // consumer warps that take units (<= kWarps)
+    int nst;                               // unit slots per warp ring (power of two)
+    int rows_cap;                          // weight rows per CTA the partial buffer holds
 };
 
+struct Layout {
+    uint32_t ring, xs, zero, exs, ms, mz, part, red, bars;
+    uint32_t total;
+};
+
+__host__ __device__ inline uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
+
+__host__ __device__ inline Layout make_layout(const GemvParams& p, int nb, int H) {
+    Layout L;
+    uint32_t off = 0;
+    L.ring = off;
+    off += (uint32_t)(kWarps * p.nst * kUnitBytes);
+    L.xs = off;
+    off += align_up((uint32_t)p.xcols * (uint32_t)p.Ks * 2u, 16);        // xcols x Ks FP16 (whole chunks)
+    L.zero = off;
+    off += 16;
+    L.exs = off;
+    off += align_up((uint32_t)(p.ngs / H) * 8u * (uint32_t)nb * 8u, 16);
+    L.ms = off;
+    off += align_up((uint32_t)p.rows_cap * (uint32_t)p.lds * 2u, 16);
+    L.mz = off;
+    off += align_up((uint32_t)p.rows_cap * (uint32_t)p.ldz * 4u, 16);
+    L.part = off;
+    off += align_up((uint32_t)p.rows_cap * (uint32_t)p.M * kSlots * 4u, 16);
+    L.red = off;
+    off += (uint32_t)kWarps * 16u * 8u * (uint32_t)nb * 4u;
+    L.bars = off;
+    off += (uint32_t)kWarps * (uint32_t)p.nst * 8u;
+    L.total = off;
+    return L;
+}
+
+// Warp MMA m16n8k16, FP16 inputs, FP32 accumulate (D = A*B + C).
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+    return v;
+}
+
+// V codes words of one virtual row at 16-byte chunk `ch` (plus word offset).
 template <int V>
-__device__ __forceinline__ void load_words(const uint32_t* p, uint32_t (&w)[V]) {
+__device__ __forceinline__ void load_codes(uint32_t row_addr, int ch, int v7, int word_in_chunk, uint32_t (&w)[V]) {
+    const uint32_t a = row_addr + ((uint32_t)(ch ^ v7) << 4) + (uint32_t)word_in_chunk * 4u;
     if constexpr (V == 4) {
-        uint4 u = ldg_stream_v4(p);
+        const uint4 u = lds128(a);
         w[0] = u.x; w[1] = u.y; w[2] = u.z; w[3] = u.w;
     } else if constexpr (V == 2) {
-        uint2 u = ldg_stream_v2(p);
+        const uint2 u = lds64(a);
         w[0] = u.x; w[1] = u.y;
     } else {
-        w[0] = ldg_stream_v1(p);
+        w[0] = lds32(a);
     }
 }
 
-// 16-bit load straight into a 32-bit register (the load zero-extends), so no
-// instruction consumes the value before it is needed.
-__device__ __forceinline__ uint32_t ldg_u16(const unsigned short* p) {
-    uint32_t v;
-    asm volatile("ld.global.nc.u16 %0, [%1];" : "=r"(v) : "l"(p));
-    return v;
-}
-__device__ __forceinline__ uint32_t ldg_u32(const uint32_t* p) {
-    uint32_t v;
-    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
-    return v;
+// Zero point in nibble j of a (shifted) zero word, as a float (2^23 + z has ulp 1).
+__device__ __forceinline__ float meta_zero(uint32_t zshifted, int j) {
+    return __uint_as_float(0x4B000000u | ((zshifted >> (4 * j)) & 0xFu)) - 8388608.0f;
 }
 
-// MT: column tiles of 8 activation rows (1: M <= 8, 2: M <= 16).
-// V: packed words per thread per k-step (4 for G >= 128, 2 for G = 64, 1 for
-//    G = 32), so the 4-thread quad's 32*V codes of a k-step lie in one group.
-// SPG: k-steps per group (2 for G = 256, else 1).
-// S: warps splitting one tile's groups (1, 2, 4, 8).  D: k-steps in flight.
-template <int MT, int V, int SPG, int S, int D>
-__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
-    constexpr int T = kWarps / S;
-    constexpr int MP = 8 * MT;
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    const int tid = threadIdx.x;
-    const int lane = tid & 31, warp = tid >> 5;
+// Bounded wait on a barrier phase; the thread sleeps between polls.
+__device__ __forceinline__ bool gemv_wait(uint32_t bar, uint32_t parity) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!tc::mbar_try_wait_sleep(bar, parity, 100000u)) {
+        if (clock64() - t0 > kSpinCycles) {
+            atomicOr(&g_gemv_status, kStatusGemv);
+            return false;
+        }
+    }
+    return true;
+}
+
+template <int NB, int G, int H>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemv_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
+                const GemvParams p) {
+    constexpr int V = G >= 128 ? 4 : G / 32;      // words per lane per code load
+    constexpr int GPC = 256 / G;                  // groups per chunk (H divides it)
+    constexpr int WSG = G / 32;                   // word steps per group
+    constexpr int DM = 4;                         // unroll of the unit loop
+    static_assert(GPC % H == 0, "a block of H groups lies inside one chunk");
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const Layout L = make_layout(p, NB, H);
+    const uint32_t sbase = tc::smem_u32(base);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t = lane & 3;
-    const int ti = warp / S, si = warp % S;
-    const int M = p.M;
-    const int G = p.G;
-    const int64_t K = p.K, N = p.N;
-    const int ngroups = (int)(K / G);
-    const int nsteps = (int)(K / (32 * V));
-    const int spt = (ngroups / S) * SPG;          // k-steps per tile for this warp
-    const int step0 = si * spt;                   // its first k-step
-    const int64_t ldq = qweight_ld(K), lds = scales_ld(K, G), ldz = zeros_ld(K, G);
 
-    uint4* xs = reinterpret_cast<uint4*>(smem_raw);                        // [nsteps][V][M][4]
-    float* sx = reinterpret_cast<float*>(xs + (size_t)nsteps * V * M * 4);    // [ngroups][MP]
-    float* red = sx + (size_t)ngroups * MP;                                   // [2][T][S][16][MP]
+    // ---- this CTA's tiles and this warp's run of (tile, chunk) units ----------
+    const int T = p.total_tiles;
+    const int tile0 = (int)(((long long)blockIdx.x * T) / gridDim.x);
+    const int tile1 = (int)(((long long)(blockIdx.x + 1) * T) / gridDim.x);
+    const int tc_ = tile1 - tile0;
+    const int units = tc_ * p.C;                  // < 2^26 (host check), so products below fit 32 bits
+    const bool active = warp < p.warps;
+    const int u0 = active ? (warp * units) / p.warps : 0;
+    const int u1 = active ? ((warp + 1) * units) / p.warps : 0;
+    const int nsl = p.nst;                        // unit slots in this warp's ring (power of two)
+    const uint32_t ring = sbase + L.ring + (uint32_t)(warp * nsl * kUnitBytes);
+    const uint32_t bar0 = sbase + L.bars + (uint32_t)(warp * nsl * 8);
 
-    // This CTA's contiguous, balanced run of tile groups (uniform in the CTA).
-    const int tg = p.tile_groups;
-    const int g0 = (int)(((int64_t)blockIdx.x * tg) / gridDim.x);
-    const int iters = (int)(((int64_t)(blockIdx.x + 1) * tg) / gridDim.x) - g0;
+    if (tid == 0) {
+        for (int i = 0; i < kWarps * nsl; ++i) tc::mbar_init(sbase + L.bars + 8u * i, 1);
+        tc::fence_barrier_init();
+    }
+    __syncthreads();
 
-    // ---- register ring: codes, scales and zero words of D k-steps --------
-    uint32_t wbuf[D][2][V];
-    uint32_t sbuf[D][2];
-    uint32_t zbuf[D][2];
-
-    // Load cursor: pointers advance by a constant per k-step; 64-bit address
-    // arithmetic happens only when the cursor moves to the next tile.
-    int itl = 0, sl = 0, lgrp = 0;
-    bool lv0 = false, lv1 = false;
-    const uint32_t* lq0 = nullptr;
-    const uint32_t* lq1 = nullptr;
-    const unsigned short* ls0 = nullptr;
-    const unsigned short* ls1 = nullptr;
-    const uint32_t* lz0 = nullptr;
-    const uint32_t* lz1 = nullptr;
-    auto set_load_tile = [&]() {
-        const int tau = (g0 + itl) * T + ti;
-        const bool ok = itl < iters && tau < p.total_tiles;
-        const int second = tau >= p.tiles_per_mat;
-        const int tile = second ? tau - p.tiles_per_mat : tau;
-        const int64_t row = (int64_t)tile * 16 + g;
-        lv0 = ok && row < N;
-        lv1 = ok && row + 8 < N;
-        const int64_t r = lv0 ? row : 0;          // pointers of an absent row stay in the matrix
-        const uint32_t* qm = second ? p.mat[1].q : p.mat[0].q;
-        const unsigned short* sm = static_cast<const unsigned short*>(second ? p.mat[1].s : p.mat[0].s);
-        const uint32_t* zm = second ? p.mat[1].z : p.mat[0].z;
-        lgrp = step0 / SPG;
-        lq0 = qm + r * ldq + step0 * 4 * V + t * V;
-        lq1 = lq0 + (lv1 ? 8 * ldq : 0);
-        ls0 = sm + r * lds + lgrp;
-        ls1 = ls0 + (lv1 ? 8 * lds : 0);
-        lz0 = zm + r * ldz;
-        lz1 = lz0 + (lv1 ? 8 * ldz : 0);
-    };
-    auto load_slot = [&](uint32_t (&w)[2][V], uint32_t (&sv)[2], uint32_t (&zv)[2]) {
-        if (lv0) {
-            load_words<V>(lq0, w[0]);
-            sv[0] = ldg_u16(ls0);
-            zv[0] = ldg_u32(lz0 + (lgrp >> 3));
-        } else {
-#pragma unroll
-            for (int v = 0; v < V; ++v) w[0][v] = 0u;
-            sv[0] = 0u;          // scale 0: an absent row contributes nothing
-            zv[0] = 0u;
-        }
-        if (lv1) {
-            load_words<V>(lq1, w[1]);
-            sv[1] = ldg_u16(ls1);
-            zv[1] = ldg_u32(lz1 + (lgrp >> 3));
-        } else {
-#pragma unroll
-            for (int v = 0; v < V; ++v) w[1][v] = 0u;
-            sv[1] = 0u;
-            zv[1] = 0u;
-        }
-        lq0 += 4 * V;
-        lq1 += 4 * V;
-        if (SPG == 1 || (sl & 1)) {
-            ++ls0;
-            ++ls1;
-            ++lgrp;
-        }
-        if (++sl == spt) {
-            sl = 0;
-            ++itl;
-            set_load_tile();
+    // ---- stream: lane 0 of each warp keeps its ring of units filled -----------
+    int it_u = u0, it_tl = 0, it_c = 0;
+    if (active) {
+        it_tl = u0 / p.C;
+        it_c = u0 - it_tl * p.C;
+    }
+    auto issue_next = [&]() {
+        const int tau = tile0 + it_tl;
+        const int mat = tau >= p.tiles_per_mat;
+        const int tile = mat ? tau - p.tiles_per_mat : tau;
+        const uint32_t slot = (uint32_t)((it_u - u0) & (nsl - 1));
+        const uint32_t bar = bar0 + 8u * slot;
+        tc::mbar_arrive_expect_tx(bar, (uint32_t)kUnitBytes);
+        tc::tma_load_2d(ring + slot * (uint32_t)kUnitBytes, mat ? (const void*)&tm1 : (const void*)&tm0, it_c * 32,
+                        tile * 16, bar);
+        ++it_u;
+        if (++it_c == p.C) {
+            it_c = 0;
+            ++it_tl;
         }
     };
+    if (active && lane == 0) {
+        for (int i = 0; i < nsl && it_u < u1; ++i) issue_next();
+    }
 
-    // (1) first loads in flight before any staging.
-    set_load_tile();
-#pragma unroll
-    for (int i = 0; i < D; ++i) load_slot(wbuf[i], sbuf[i], zbuf[i]);
-
-    // (2) x -> B-fragment order + per-group sums; item = (m, 8-k word w8).
+    // ---- stage x (FP16, fragment order), per-block sums; zero slots -----------
+    // Work item of a warp: 32 consecutive words (one per lane) of one staged
+    // column (segment p, activation row m); words of one group sit in
+    // consecutive lanes, so the group sums are warp shuffles.
     {
-        // x fits in shared memory, so every index here fits in 32 bits
-        const int wpr = (int)(K / 8);
-        const int total = M * wpr;
-        const int gw = G / 8;                     // words per group, a power of two dividing 32
-        const int gshift = __ffs(gw) - 1;
-        constexpr int U = 4;
-        for (int base0 = warp * 32; base0 < total; base0 += U * kThreads) {
-            uint4 xv[U];
+        const int xcols = p.xcols, M = p.M, C = p.C;
+        uint4* xs = reinterpret_cast<uint4*>(base + L.xs);
+        float2* exs = reinterpret_cast<float2*>(base + L.exs);
+        const int kseg = p.K / p.P;                        // real codes per segment
+        constexpr int GW = G / 8;                          // words per group
+        const int items = xcols * C;                       // (column, 32-word block)
+        for (int it = warp; it < items; it += kWarps) {
+            const int xc = it / C, c = it - xc * C;        // one division per 32 words
+            const int pseg = xc / M, m = xc - pseg * M;
+            const int wseg = c * 32 + lane;                // word in the padded segment
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (wseg * 8 < kseg)
+                v = *reinterpret_cast<const uint4*>(p.x + (int64_t)m * p.K + (int64_t)pseg * kseg + wseg * 8);
+            const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+            float f[8];
+            unsigned short h[8];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int item = base0 + u * kThreads + lane;
-                xv[u] = make_uint4(0u, 0u, 0u, 0u);
-                if (item < total) xv[u] = *reinterpret_cast<const uint4*>(p.x + (int64_t)item * 8);
+            for (int j = 0; j < 4; ++j) {
+                const __half lo = __float2half_rn(bf16lo_to_f32(in[j]));
+                const __half hi = __float2half_rn(bf16hi_to_f32(in[j]));
+                h[2 * j] = __half_as_ushort(lo);
+                h[2 * j + 1] = __half_as_ushort(hi);
+                f[2 * j] = __half2float(lo);
+                f[2 * j + 1] = __half2float(hi);
             }
+            // 1024 * (x0 + x2 + x4 + x6) + 64 * (x1 + x3 + x5 + x7), and sum x
+            float e = 1024.0f * (f[0] + f[2] + f[4] + f[6]) + 64.0f * (f[1] + f[3] + f[5] + f[7]);
+            float xsum = f[0] + f[1] + f[2] + f[3] + f[4] + f[5] + f[6] + f[7];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int item = base0 + u * kThreads + lane;
-                float f = bf16lo_to_f32(xv[u].x) + bf16hi_to_f32(xv[u].x) + bf16lo_to_f32(xv[u].y) +
-                          bf16hi_to_f32(xv[u].y) + bf16lo_to_f32(xv[u].z) + bf16hi_to_f32(xv[u].z) +
-                          bf16lo_to_f32(xv[u].w) + bf16hi_to_f32(xv[u].w);
-                for (int off = 1; off < gw; off <<= 1) f += __shfl_xor_sync(0xFFFFFFFFu, f, off);
-                if (item < total) {
-                    const int m = item / wpr, w8 = item - m * wpr;
-                    const int s = w8 / (4 * V);
-                    const int tt = (w8 % (4 * V)) / V;
-                    const int v = w8 % V;
-                    xs[((s * V + v) * M + m) * 4 + tt] =
-                        make_uint4(__byte_perm(xv[u].x, xv[u].z, 0x5410), __byte_perm(xv[u].x, xv[u].z, 0x7632),
-                                   __byte_perm(xv[u].y, xv[u].w, 0x5410), __byte_perm(xv[u].y, xv[u].w, 0x7632));
-                    if ((w8 & (gw - 1)) == 0) sx[(w8 >> gshift) * MP + m] = f;
+            for (int off = 1; off < GW; off <<= 1) {
+                e += __shfl_xor_sync(0xFFFFFFFFu, e, off);
+                xsum += __shfl_xor_sync(0xFFFFFFFFu, xsum, off);
+            }
+            const int bq = lane / (4 * V), rem = lane % (4 * V);
+            const int tt = rem / V, ii = rem % V;
+            const int stp = c * 8 + bq * V + ii;
+            xs[(stp * xcols + xc) * 4 + tt] =
+                make_uint4((uint32_t)h[0] | ((uint32_t)h[4] << 16), (uint32_t)h[1] | ((uint32_t)h[5] << 16),
+                           (uint32_t)h[2] | ((uint32_t)h[6] << 16), (uint32_t)h[3] | ((uint32_t)h[7] << 16));
+            if ((wseg & (GW - 1)) == 0) {
+                const int gam = wseg / GW;                 // group in the segment
+                const int col = ((pseg * H) + (gam % H)) * M + m;
+                exs[(gam / H) * (8 * NB) + col] = make_float2(e, xsum);
+            }
+        }
+        // E/X columns that no (segment, parity, row) uses stay zero; so does the zero block
+        const int nblk = p.ngs / H;
+        for (int i = tid; i < nblk * (8 * NB - p.cols); i += kThreads) {
+            const int b = i / (8 * NB - p.cols), col = p.cols + i % (8 * NB - p.cols);
+            exs[b * (8 * NB) + col] = make_float2(0.0f, 0.0f);
+        }
+        if (tid == 0) *reinterpret_cast<uint4*>(base + L.zero) = make_uint4(0u, 0u, 0u, 0u);
+        // the CTA's scale and zero rows: contiguous in each matrix, copied with 16-byte vectors
+        // (rows past N, and the gap before the second matrix's rows, stay zero)
+        {
+            const int r0 = tile0 < p.tiles_per_mat ? tile0 * p.R : 0;                  // first row, matrix 0 part
+            const int n0 = tile1 <= p.tiles_per_mat ? tc_ * p.R : (p.tiles_per_mat - tile0) * p.R;
+            const int l1 = tile0 < p.tiles_per_mat ? (p.tiles_per_mat - tile0) * p.R : 0;   // local row of matrix 1
+            const int t1a = tile0 < p.tiles_per_mat ? p.tiles_per_mat : tile0;
+            const int r1 = (t1a - p.tiles_per_mat) * p.R;                                // first row, matrix 1 part
+            const int n1 = tile1 > p.tiles_per_mat ? (tile1 - t1a) * p.R : 0;
+            const int sv = p.lds / 8, zv = p.ldz / 4;                                   // uint4 per row
+            uint4* ms = reinterpret_cast<uint4*>(base + L.ms);
+            uint4* mz = reinterpret_cast<uint4*>(base + L.mz);
+            for (int i = tid; i < p.rows_cap * (sv + zv); i += kThreads) {
+                const bool isz = i >= p.rows_cap * sv;
+                const int ii = isz ? i - p.rows_cap * sv : i;
+                const int per = isz ? zv : sv;
+                const int lr = ii / per, col = ii - lr * per;
+                int mat = -1, row = 0;
+                if (tile0 < p.tiles_per_mat && lr < n0) {
+                    mat = 0;
+                    row = r0 + lr;
+                } else if (lr >= l1 && lr - l1 < n1) {
+                    mat = 1;
+                    row = r1 + (lr - l1);
+                }
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                if (mat >= 0 && row < p.N) {
+                    if (isz) v = reinterpret_cast<const uint4*>((mat ? p.z[1] : p.z[0]) + (int64_t)row * p.ldz)[col];
+                    else v = reinterpret_cast<const uint4*>((mat ? p.s[1] : p.s[0]) + (int64_t)row * p.lds)[col];
+                }
+                (isz ? mz : ms)[ii] = v;
+            }
+        }
+        float* part = reinterpret_cast<float*>(base + L.part);
+        for (int i = tid; i < p.rows_cap * p.M * kSlots; i += kThreads) part[i] = 0.0f;
+    }
+    __syncthreads();
+
+    // ---- compute -------------------------------------------------------------------
+    bool ok = true;
+    if (active) {
+        const int va = sigma8(g), vb = va + 8, v7 = va & 7;
+        const int rho_a = va / p.P, pa = va - rho_a * p.P;
+        const int rho_b = vb / p.P, pb = vb - rho_b * p.P;
+        float* red = reinterpret_cast<float*>(base + L.red) + warp * 16 * 8 * NB;
+        float* part = reinterpret_cast<float*>(base + L.part);
+        uint32_t coff[8 / V];                              // byte offset of this lane's words in a 128-byte row
+#pragma unroll
+        for (int bq = 0; bq < 8 / V; ++bq) {
+            const int wf = bq * 4 * V + t * V;
+            coff[bq] = ((uint32_t)((wf >> 2) ^ v7) << 4) + (uint32_t)(wf & 3) * 4u;
+        }
+        // B column of this lane per column block: (segment, group parity, activation row)
+        const uint32_t xstep = (uint32_t)p.xcols * 64u;    // bytes of staged x per word step
+        const uint32_t zaddr = sbase + L.zero;
+        uint32_t xl[NB];                                    // lane's staged column (bytes, without the step)
+        int lh[NB];                                         // its group parity; -1 = idle column
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+            const int j = nb * 8 + g;
+            if (j < p.cols) {
+                const int m = j % p.M, ph = j / p.M;
+                const int hh = ph % H, ps = ph / H;
+                xl[nb] = sbase + L.xs + (uint32_t)(((ps * p.M + m) * 4 + t) * 16);
+                lh[nb] = hh;
+            } else {
+                xl[nb] = zaddr;
+                lh[nb] = -1;
+            }
+        }
+        // group parity of the lane's two D columns (2t, 2t+1) in each column block
+        int hc[NB][2];
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int j = nb * 8 + 2 * t + e;
+                hc[nb][e] = j < p.cols ? (j / p.M) % H : 0;
+            }
+        const uint32_t exlane = sbase + L.exs + (uint32_t)(2 * t * 8);
+
+        // slot of the first tile of the run: warps before this one that hold units of it
+        int first_slot = 0;
+        {
+            const int ftl = u0 / p.C;
+            const int fu = ftl * p.C;
+            if (fu < u0) {
+                int fw = warp;
+                while (fw > 0 && (fw * units) / p.warps > fu) --fw;
+                first_slot = warp - fw;
+            }
+        }
+
+        // this lane's rows (local to the CTA) for the scale/zero tables
+        const unsigned short* smtab = reinterpret_cast<const unsigned short*>(base + L.ms);
+        const uint32_t* zmtab = reinterpret_cast<const uint32_t*>(base + L.mz);
+
+        float acc[NB][4];
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[nb][e] = 0.0f;
+        int tl = u0 / p.C, c = u0 - (u0 / p.C) * p.C;
+        const int lg = 31 - __clz(nsl);
+        for (int ub = u0; ub < u1 && ok; ub += DM) {
+#pragma unroll
+            for (int jj = 0; jj < DM; ++jj) {
+                const int u = ub + jj;
+                if (u < u1 && ok) {
+                    const uint32_t slot = (uint32_t)((u - u0) & (nsl - 1));
+                    ok = gemv_wait(bar0 + 8u * slot, (uint32_t)(((u - u0) >> lg) & 1));
+                    ok = __all_sync(0xFFFFFFFFu, ok);
+                    if (ok) {
+                        const int rla = tl * p.R + rho_a, rlb = tl * p.R + rho_b;   // local rows
+                        const unsigned short* sra = smtab + rla * p.lds + pa * p.ngs + c * GPC;
+                        const unsigned short* srb = smtab + rlb * p.lds + pb * p.ngs + c * GPC;
+                        const uint32_t* zra = zmtab + rla * p.ldz;
+                        const uint32_t* zrb = zmtab + rlb * p.ldz;
+                        const int gia = pa * p.ngs + c * GPC, gib = pb * p.ngs + c * GPC;   // first group of the chunk
+                        const uint32_t unit = ring + slot * (uint32_t)kUnitBytes;
+                        const uint32_t row_a = unit + (uint32_t)va * 128u, row_b = row_a + 8u * 128u;
+                        const uint32_t xu = (uint32_t)(c * 8) * xstep;
+                        // per group parity: x base and step of this lane (idle lanes read zeros)
+                        uint32_t xb[NB][H], xsp[NB][H];
+#pragma unroll
+                        for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+                            for (int hh = 0; hh < H; ++hh) {
+                                const bool on = lh[nb] == hh;
+                                xb[nb][hh] = on ? xl[nb] + xu : zaddr;
+                                xsp[nb][hh] = on ? xstep : 0u;
+                            }
+                        float da[NB][4], db[NB][4];
+#pragma unroll
+                        for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) da[nb][e] = db[nb][e] = 0.0f;
+#pragma unroll
+                        for (int bq = 0; bq < 8 / V; ++bq) {
+                            uint32_t wa[V], wb[V];
+                            if constexpr (V == 4) {
+                                const uint4 x0 = lds128(row_a + coff[bq]);
+                                const uint4 x1 = lds128(row_b + coff[bq]);
+                                wa[0] = x0.x; wa[1] = x0.y; wa[2] = x0.z; wa[3] = x0.w;
+                                wb[0] = x1.x; wb[1] = x1.y; wb[2] = x1.z; wb[3] = x1.w;
+                            } else if constexpr (V == 2) {
+                                const uint2 x0 = lds64(row_a + coff[bq]);
+                                const uint2 x1 = lds64(row_b + coff[bq]);
+                                wa[0] = x0.x; wa[1] = x0.y;
+                                wb[0] = x1.x; wb[1] = x1.y;
+                            } else {
+                                wa[0] = lds32(row_a + coff[bq]);
+                                wb[0] = lds32(row_b + coff[bq]);
+                            }
+#pragma unroll
+                            for (int i = 0; i < V; ++i) {
+                                const int ws = bq * V + i;                   // word step in the chunk
+                                const int jg = ws / WSG;                     // group in the chunk
+                                const int hcur = jg % H;                     // its parity (c * GPC is a multiple of H)
+                                const uint32_t a8 = wa[i] >> 8, b8 = wb[i] >> 8;
+                                const uint32_t a0 = lop3_and_or(wa[i], 0x000F000Fu, 0x64006400u);
+                                const uint32_t a1 = lop3_and_or(wa[i], 0x00F000F0u, 0x54005400u);
+                                const uint32_t a2 = lop3_and_or(a8, 0x000F000Fu, 0x64006400u);
+                                const uint32_t a3 = lop3_and_or(a8, 0x00F000F0u, 0x54005400u);
+                                const uint32_t b0 = lop3_and_or(wb[i], 0x000F000Fu, 0x64006400u);
+                                const uint32_t b1 = lop3_and_or(wb[i], 0x00F000F0u, 0x54005400u);
+                                const uint32_t b2 = lop3_and_or(b8, 0x000F000Fu, 0x64006400u);
+                                const uint32_t b3 = lop3_and_or(b8, 0x00F000F0u, 0x54005400u);
+#pragma unroll
+                                for (int nb = 0; nb < NB; ++nb) {
+                                    const uint4 xv = lds128(xb[nb][hcur] + (uint32_t)ws * xsp[nb][hcur]);
+                                    mma_f16(da[nb], a0, b0, a1, b1, xv.x, xv.y);
+                                    mma_f16(db[nb], a2, b2, a3, b3, xv.z, xv.w);
+                                }
+                                if ((ws + 1) % (WSG * H) == 0) {            // block of H groups complete
+                                    const int jg0 = jg - (H - 1);           // first group of the block in the chunk
+                                    const int blk = (c * GPC + jg0) / H;    // block in the segment
+                                    // scales of the block's H groups (consecutive halves) and their zero points;
+                                    // groups past the row end (last, partial chunk of one segment) get scale 0
+                                    float sa[H], sb[H], za[H], zb[H];
+                                    {
+                                        const uint32_t zwa = zra[(gia + jg0) >> 3] >> (4 * ((gia + jg0) & 7));
+                                        const uint32_t zwb = zrb[(gib + jg0) >> 3] >> (4 * ((gib + jg0) & 7));
+#pragma unroll
+                                        for (int hh = 0; hh < H; ++hh) {
+                                            const bool va_ = gia + jg0 + hh < p.ng, vb_ = gib + jg0 + hh < p.ng;
+                                            sa[hh] = va_ ? __half2float(__ushort_as_half(sra[jg0 + hh])) : 0.0f;
+                                            sb[hh] = vb_ ? __half2float(__ushort_as_half(srb[jg0 + hh])) : 0.0f;
+                                            za[hh] = meta_zero(zwa, hh);
+                                            zb[hh] = meta_zero(zwb, hh);
+                                        }
+                                    }
+#pragma unroll
+                                    for (int nb = 0; nb < NB; ++nb) {
+                                        const float4 ex = lds_f4(exlane + (uint32_t)((blk * 8 * NB + nb * 8) * 8));
+#pragma unroll
+                                        for (int e = 0; e < 2; ++e) {
+                                            float s_a = sa[0], s_b = sb[0], z_a = za[0], z_b = zb[0];
+#pragma unroll
+                                            for (int hh = 1; hh < H; ++hh)
+                                                if (hc[nb][e] == hh) {
+                                                    s_a = sa[hh]; s_b = sb[hh]; z_a = za[hh]; z_b = zb[hh];
+                                                }
+                                            const float E = e ? ex.z : ex.x, X = e ? ex.w : ex.y;
+                                            acc[nb][e] = fmaf(s_a, (da[nb][e] + db[nb][e]) - fmaf(z_a, X, E), acc[nb][e]);
+                                            acc[nb][2 + e] =
+                                                fmaf(s_b, (da[nb][2 + e] + db[nb][2 + e]) - fmaf(z_b, X, E), acc[nb][2 + e]);
+                                        }
+#pragma unroll
+                                        for (int e = 0; e < 4; ++e) da[nb][e] = db[nb][e] = 0.0f;
+                                    }
+                                }
+                            }
+                        }
+                        // tile finished in this warp's run: reduce the diagonal over segments and parities
+                        if (c == p.C - 1 || u == u1 - 1) {
+#pragma unroll
+                            for (int nb = 0; nb < NB; ++nb) {
+                                red[va * 8 * NB + nb * 8 + 2 * t] = acc[nb][0];
+                                red[va * 8 * NB + nb * 8 + 2 * t + 1] = acc[nb][1];
+                                red[vb * 8 * NB + nb * 8 + 2 * t] = acc[nb][2];
+                                red[vb * 8 * NB + nb * 8 + 2 * t + 1] = acc[nb][3];
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) acc[nb][e] = 0.0f;
+                            }
+                            __syncwarp();
+                            const int slotp = (tl * p.C < u0) ? first_slot : 0;
+                            for (int o = lane; o < p.R * p.M; o += 32) {   // R*M reaches 256
+                                const int rho = o / p.M, m = o - rho * p.M;
+                                float sum = 0.0f;
+                                for (int q = 0; q < p.P; ++q)
+#pragma unroll
+                                    for (int hh = 0; hh < H; ++hh)
+                                        sum += red[(rho * p.P + q) * 8 * NB + (q * H + hh) * p.M + m];
+                                part[((tl * p.R + rho) * p.M + m) * kSlots + slotp] = sum;
+                            }
+                            __syncwarp();
+                        }
+                        // this slot is read: refill it with the unit nsl ahead
+                        __syncwarp();
+                        if (lane == 0 && it_u < u1) {
+                            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                            issue_next();
+                        }
+                        if (++c == p.C) {
+                            c = 0;
+                            ++tl;
+                        }
+                    }
                 }
             }
         }
-        for (int i = tid; i < ngroups * (MP - M); i += kThreads) {
-            const int grp = i / (MP - M), m = M + i % (MP - M);
-            sx[grp * MP + m] = 0.0f;
+        if (!ok && lane == 0) {   // wait for this warp's copies still in flight
+            for (int uu = it_u - nsl; uu < it_u; ++uu) {
+                if (uu < u0) continue;
+                const uint32_t bar = bar0 + 8u * (uint32_t)((uu - u0) & (nsl - 1));
+                const long long t0 = clock64();
+                while (!tc::mbar_try_wait(bar, (uint32_t)(((uu - u0) >> lg) & 1))) {
+                    if (clock64() - t0 > kSpinCycles) {
+                        atomicOr(&g_gemv_status, kStatusGemvDrain);
+                        break;
+                    }
+                }
+            }
         }
     }
     __syncthreads();
 
-    // (3) stream the warp's k-steps, tile after tile.
-    float acc[MT][4];
-    float part[MT][4];
+    // ---- combine the slots in a fixed order and store ------------------------------
+    {
+        const float* part = reinterpret_cast<const float*>(base + L.part);
+        const int nout = tc_ * p.R * p.M;
+        for (int i = tid; i < nout; i += kThreads) {
+            const int rl = i / p.M, m = i - rl * p.M;
+            const int tl2 = rl / p.R, rho = rl - tl2 * p.R;
+            const int tau = tile0 + tl2;
+            const int mat = tau >= p.tiles_per_mat;
+            const int row = (mat ? tau - p.tiles_per_mat : tau) * p.R + rho;
+            if (row >= p.N) continue;
+            float sum = 0.0f;
 #pragma unroll
-    for (int ct = 0; ct < MT; ++ct)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[ct][e] = part[ct][e] = 0.0f;
-    bool colv[MT];
-#pragma unroll
-    for (int ct = 0; ct < MT; ++ct) colv[ct] = (g + 8 * ct) < M;
-
-    const int xstep = V * M * 4;                  // uint4 per k-step of staged x
-    const int xlane = g * 4 + t;
-    int itc = 0, sc = 0;                          // compute cursor
-    int xoff = step0 * xstep;
-    int cgrp = step0 / SPG;
-    const int total_steps = iters * spt;
-    for (int j0 = 0; j0 < total_steps; j0 += D) {
-#pragma unroll
-        for (int i = 0; i < D; ++i) {
-            if (j0 + i < total_steps) {
-                uint4 bfr[MT][V];
-#pragma unroll
-                for (int ct = 0; ct < MT; ++ct)
-#pragma unroll
-                    for (int v = 0; v < V; ++v)
-                        bfr[ct][v] = colv[ct] ? xs[xoff + v * M * 4 + xlane + 32 * ct] : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-                for (int v = 0; v < V; ++v) {
-                    uint32_t plo[4], phi[4];
-                    codes_to_bf16x2(wbuf[i][0][v], plo);
-                    codes_to_bf16x2(wbuf[i][1][v], phi);
-                    const uint32_t a0[4] = {plo[0], phi[0], plo[1], phi[1]};
-                    const uint32_t a1[4] = {plo[2], phi[2], plo[3], phi[3]};
-#pragma unroll
-                    for (int ct = 0; ct < MT; ++ct) {
-                        mma_bf16_16816(part[ct], a0, bfr[ct][v].x, bfr[ct][v].y);
-                        mma_bf16_16816(part[ct], a1, bfr[ct][v].z, bfr[ct][v].w);
-                    }
-                }
-                if (SPG == 1 || (sc & 1)) {           // group complete: scale and zero correction
-                    float s_[2], c_[2];
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        s_[h] = __half2float(__ushort_as_half((unsigned short)sbuf[i][h]));
-                        // 128 + z exactly: 2^23 + 128 + z has ulp 1, minus 2^23
-                        c_[h] = __uint_as_float(0x4B000080u + nibble(zbuf[i][h], cgrp & 7)) - 8388608.0f;
-                    }
-#pragma unroll
-                    for (int ct = 0; ct < MT; ++ct) {
-                        const float2 sxv = *reinterpret_cast<const float2*>(sx + cgrp * MP + 8 * ct + 2 * t);
-                        acc[ct][0] = fmaf(s_[0], fmaf(-c_[0], sxv.x, part[ct][0]), acc[ct][0]);
-                        acc[ct][1] = fmaf(s_[0], fmaf(-c_[0], sxv.y, part[ct][1]), acc[ct][1]);
-                        acc[ct][2] = fmaf(s_[1], fmaf(-c_[1], sxv.x, part[ct][2]), acc[ct][2]);
-                        acc[ct][3] = fmaf(s_[1], fmaf(-c_[1], sxv.y, part[ct][3]), acc[ct][3]);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) part[ct][e] = 0.0f;
-                    }
-                    ++cgrp;
-                }
-                load_slot(wbuf[i], sbuf[i], zbuf[i]);  // refill this slot D steps ahead
-                xoff += xstep;
-                if (++sc == spt) {                     // tile complete (same step for every warp)
-                    if constexpr (S == 1) {
-                        const int tau = (g0 + itc) * T + ti;
-                        if (tau < p.total_tiles) {
-                            const int second = tau >= p.tiles_per_mat;
-                            const int tile = second ? tau - p.tiles_per_mat : tau;
-                            __nv_bfloat16* y = static_cast<__nv_bfloat16*>(second ? p.mat[1].y : p.mat[0].y);
-#pragma unroll
-                            for (int ct = 0; ct < MT; ++ct)
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const int m = 8 * ct + 2 * t + (e & 1);
-                                    const int64_t row = (int64_t)tile * 16 + g + 8 * (e >> 1);
-                                    if (m < M && row < N) y[(int64_t)m * N + row] = __float2bfloat16_rn(acc[ct][e]);
-                                }
-                        }
-                    } else {
-                        float* rb = red + ((size_t)((itc & 1) * T + ti) * S + si) * 16 * MP;
-#pragma unroll
-                        for (int ct = 0; ct < MT; ++ct) {
-                            rb[g * MP + 8 * ct + 2 * t] = acc[ct][0];
-                            rb[g * MP + 8 * ct + 2 * t + 1] = acc[ct][1];
-                            rb[(g + 8) * MP + 8 * ct + 2 * t] = acc[ct][2];
-                            rb[(g + 8) * MP + 8 * ct + 2 * t + 1] = acc[ct][3];
-                        }
-                        __syncthreads();
-                        const float* rbuf = red + (size_t)(itc & 1) * T * S * 16 * MP;
-                        for (int e = tid; e < T * 16 * M; e += kThreads) {
-                            const int tj = e / (16 * M);
-                            const int m = (e / 16) % M;
-                            const int rr = e % 16;
-                            const int tau2 = (g0 + itc) * T + tj;
-                            if (tau2 >= p.total_tiles) continue;
-                            const int second = tau2 >= p.tiles_per_mat;
-                            const int tile = second ? tau2 - p.tiles_per_mat : tau2;
-                            const int64_t row = (int64_t)tile * 16 + rr;
-                            if (row >= N) continue;
-                            float sum = 0.0f;
-#pragma unroll
-                            for (int q = 0; q < S; ++q) sum += rbuf[((tj * S + q) * 16 + rr) * MP + m];
-                            __nv_bfloat16* y = static_cast<__nv_bfloat16*>(second ? p.mat[1].y : p.mat[0].y);
-                            y[(int64_t)m * N + row] = __float2bfloat16_rn(sum);
-                        }
-                    }
-#pragma unroll
-                    for (int ct = 0; ct < MT; ++ct)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) acc[ct][e] = 0.0f;
-                    sc = 0;
-                    ++itc;
-                    xoff = step0 * xstep;
-                    cgrp = step0 / SPG;
-                }
-            }
+            for (int q = 0; q < kSlots; ++q) sum += part[i * kSlots + q];
+            (mat ? p.y[1] : p.y[0])[(int64_t)m * p.N + row] = __float2bfloat16_rn(sum);
         }
+    }
+}
+
+// ---- host side -------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// Packed codes viewed as [N*P virtual rows][K/(8P) words], boxes of 32 words x 16 rows.
+bool make_code_map(CUtensorMap* map, const uint32_t* q, int64_t N, int64_t K, int P) {
+    auto enc = encoder();
+    if (!enc) return false;
+    const uint64_t words = (uint64_t)(K / 8 / P);
+    cuuint64_t dims[2] = {words, (uint64_t)(N * P)};
+    cuuint64_t strides[1] = {words * 4};
+    cuuint32_t box[2] = {32, 16};
+    cuuint32_t es[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(q), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Segments P and group parities H per row for M activation rows: the B
+// operand's columns are (segment, parity, row) triples, P*H*M <= 8 (one
+// column block; M > 8 uses two blocks with P = H = 1).  Preferred: few weight
+// rows per tile (P large, for an even split over the SMs) and H > 1 (the
+// scale/zero correction runs once per H groups).  P > 1 needs each segment to
+// be whole 256-code chunks; H must divide the groups of a chunk.
+void choose_segments(int64_t M, int64_t K, int G, int& P, int& H) {
+    P = 1;
+    H = 1;
+    if (M > 8) return;
+    const int gpc = 256 / G;
+    static const int pref[][2] = {{4, 2}, {2, 4}, {8, 1}, {4, 1}, {2, 2}, {1, 4}, {2, 1}, {1, 2}, {1, 1}};
+    for (const auto& c : pref) {
+        const int p = c[0], h = c[1];
+        if (p * h * M > 8 || h > gpc || gpc % h) continue;
+        if (p > 1 && K % (256 * p)) continue;
+        P = p;
+        H = h;
+        return;
     }
 }
 
 struct Plan {
-    int S, iters, grid;
+    GemvParams p;
+    int nb, grid, H;
+    size_t smem;
 };
 
-template <int MT, int V, int SPG, int S>
-cudaError_t launch_s(const GemvParams& p0, size_t smem, int sms, cudaStream_t stream);
+bool make_plan(int64_t M, int64_t N, int64_t K, int G, int nmat, int sms, size_t smem_cap, Plan& pl) {
+    if (M < 1 || M > 16 || N < 1 || K < 32 || K % 32 || K % G) return false;
+    if (N > (int64_t)1 << 24 || K > (int64_t)1 << 20) return false;   // keeps tile/unit indices small
+    GemvParams& p = pl.p;
+    p.M = (int)M;
+    p.N = (int)N;
+    p.K = (int)K;
+    p.G = G;
+    choose_segments(M, K, G, p.P, pl.H);
+    p.R = 16 / p.P;
+    p.cols = p.P * pl.H * p.M;
+    p.xcols = p.P * p.M;
+    pl.nb = M > 8 ? 2 : 1;
+    p.C = (int)((K / p.P + 255) / 256);
+    p.Ks = p.C * 256;                           // equals K / P whenever P > 1
+    p.ng = (int)(K / G);
+    p.ngs = p.Ks / G;
+    p.lds = (int)scales_ld(K, G);
+    p.ldz = (int)zeros_ld(K, G);
+    p.tiles_per_mat = (int)((N + p.R - 1) / p.R);
+    p.total_tiles = p.tiles_per_mat * nmat;
+    pl.grid = p.total_tiles < sms ? p.total_tiles : sms;
+    const int tmin = p.total_tiles / pl.grid, tmax = (p.total_tiles + pl.grid - 1) / pl.grid;
+    if ((long long)tmax * p.C >= (1ll << 26)) return false;
+    // warps taking units: as many as keep every tile within kSlots consecutive warps
+    p.warps = 1;
+    for (int w = kWarps; w >= 1; --w) {
+        const long long units = (long long)tmin * p.C;
+        const long long per = units / w;
+        if (per < 1) continue;
+        const long long span = (p.C + per - 1) / per + 1;
+        if (span <= kSlots) {
+            p.warps = w;
+            break;
+        }
+    }
+    p.rows_cap = tmax * p.R;
+    // the deepest per-warp ring of units that fits
+    for (int nst = 4; nst >= 1; nst >>= 1) {
+        p.nst = nst;
+        pl.smem = make_layout(p, pl.nb, pl.H).total + 1024;
+        if (pl.smem <= smem_cap) return true;
+    }
+    return false;
+}
 
-// Per kernel instance and device: raise the dynamic shared memory limit once, as needed.
-constexpr int kMaxDevices = 64;
-template <typename Kern>
-cudaError_t ensure_smem(Kern kern, size_t smem, int (&cached)[kMaxDevices]) {
+template <int NB, int G, int H>
+cudaError_t launch_t(const CUtensorMap& tm0, const CUtensorMap& tm1, const Plan& pl, cudaStream_t stream) {
+    static int cached[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < kMaxDevices && (int)smem <= cached[dev]) return cudaSuccess;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess && dev >= 0 && dev < kMaxDevices) cached[dev] = (int)smem;
-    return e;
-}
-
-template <int MT, int V, int SPG, int S>
-cudaError_t launch_s(const GemvParams& p0, size_t smem, int sms, cudaStream_t stream) {
-    // k-steps in flight per thread: as deep as the 128-register budget allows without spilling
-    constexpr int D = MT == 1 ? (V == 4 ? 6 : (V == 2 ? 8 : 10)) : (V == 4 ? 4 : (V == 2 ? 6 : 8));
-    auto kern = gemv_kernel<MT, V, SPG, S, D>;
-    static int cached[kMaxDevices] = {};
-    cudaError_t e = ensure_smem(kern, smem, cached);
-    if (e != cudaSuccess) return e;
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) return cudaErrorInvalidConfiguration;
-    per_sm = per_sm > 2 ? 2 : per_sm;
-    GemvParams p = p0;
-    constexpr int T = kWarps / S;
-    p.tile_groups = (p.total_tiles + T - 1) / T;
-    const int grid = p.tile_groups < sms * per_sm ? p.tile_groups : sms * per_sm;
-    kern<<<dim3((unsigned)grid), dim3(kThreads), smem, stream>>>(p);
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if ((int)pl.smem > cached[dev]) {
+        e = cudaFuncSetAttribute(gemv_kernel<NB, G, H>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+        if (e != cudaSuccess) return e;
+        cached[dev] = (int)pl.smem;
+    }
+    gemv_kernel<NB, G, H><<<pl.grid, kThreads, pl.smem, stream>>>(tm0, tm1, pl.p);
     return cudaGetLastError();
 }
 
-// Splitting S: among the splits that divide the group count, the one whose
-// balanced partition leaves the busiest SM with the least work.  CTA b is
-// assumed to land on SM b % sms; an SM's work is the warp k-steps of its
-// CTAs; the score is the mean useful work per SM over the busiest SM's work.
-// Ties go to the smallest S (fewest cross-warp reductions).
-int choose_split(int total_tiles, int ngroups, int sms, int per_sm) {
-    int best = 0;
-    double best_score = -1.0;
-    for (int S : {1, 2, 4, 8}) {
-        if (ngroups % S) continue;
-        const int T = kWarps / S;
-        const int tg = (total_tiles + T - 1) / T;
-        const int grid = tg < sms * per_sm ? tg : sms * per_sm;
-        const int64_t spt = ngroups / S;
-        int64_t busiest = 0;
-        for (int sm = 0; sm < sms && sm < grid; ++sm) {
-            int64_t w = 0;
-            for (int b = sm; b < grid; b += sms) {
-                const int64_t it = ((int64_t)(b + 1) * tg) / grid - ((int64_t)b * tg) / grid;
-                w += it * kWarps * spt;
-            }
-            if (w > busiest) busiest = w;
+template <int NB, int G>
+cudaError_t launch_h(const CUtensorMap& tm0, const CUtensorMap& tm1, const Plan& pl, cudaStream_t stream) {
+    if constexpr (NB == 2) {
+        return launch_t<NB, G, 1>(tm0, tm1, pl, stream);
+    } else {
+        switch (pl.H) {
+            case 1: return launch_t<NB, G, 1>(tm0, tm1, pl, stream);
+            case 2:
+                if constexpr (256 / G >= 2) return launch_t<NB, G, 2>(tm0, tm1, pl, stream);
+                break;
+            case 4:
+                if constexpr (256 / G >= 4) return launch_t<NB, G, 4>(tm0, tm1, pl, stream);
+                break;
         }
-        const double useful = (double)total_tiles * ngroups / sms;
-        const double score = busiest > 0 ? useful / (double)busiest : 0.0;
-        if (score > best_score + 1e-9) {
-            best_score = score;
-            best = S;
-        }
+        return cudaErrorInvalidValue;
     }
-    return best;
 }
 
-template <int MT, int V, int SPG>
-cudaError_t launch_v(const GemvParams& p, size_t smem, int sms, cudaStream_t stream) {
-    const int per_sm = smem <= 100 * 1024 ? 2 : 1;
-    switch (choose_split(p.total_tiles, (int)(p.K / p.G), sms, per_sm)) {
-        case 1: return launch_s<MT, V, SPG, 1>(p, smem, sms, stream);
-        case 2: return launch_s<MT, V, SPG, 2>(p, smem, sms, stream);
-        case 4: return launch_s<MT, V, SPG, 4>(p, smem, sms, stream);
-        case 8: return launch_s<MT, V, SPG, 8>(p, smem, sms, stream);
+template <int NB>
+cudaError_t launch_nb(const CUtensorMap& tm0, const CUtensorMap& tm1, const Plan& pl, cudaStream_t stream) {
+    switch (pl.p.G) {
+        case 32: return launch_h<NB, 32>(tm0, tm1, pl, stream);
+        case 64: return launch_h<NB, 64>(tm0, tm1, pl, stream);
+        case 128: return launch_h<NB, 128>(tm0, tm1, pl, stream);
+        case 256: return launch_h<NB, 256>(tm0, tm1, pl, stream);
         default: return cudaErrorInvalidValue;
     }
 }
 
-template <int MT>
-cudaError_t launch_g(const GemvParams& p, size_t smem, int sms, cudaStream_t stream) {
-    switch (p.G) {
-        case 32: return launch_v<MT, 1, 1>(p, smem, sms, stream);
-        case 64: return launch_v<MT, 2, 1>(p, smem, sms, stream);
-        case 128: return launch_v<MT, 4, 1>(p, smem, sms, stream);
-        case 256: return launch_v<MT, 4, 2>(p, smem, sms, stream);
-        default: return cudaErrorInvalidValue;
-    }
+int device_sms() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return sms;
 }
 
 }  // namespace
-
-size_t gemv_smem_bytes(int64_t M, int64_t K, int G, int /*ntiles*/) {
-    if (M < 1 || M > 16) return 0;
-    const int64_t MP = M <= 8 ? 8 : 16;
-    const int64_t ngroups = K / G;
-    const int64_t xs = M * K * 2;
-    const int64_t sx = ngroups * MP * 4;
-    const int64_t red = 2 * (int64_t)kWarps * 16 * MP * 4;
-    return (size_t)(xs + sx + red);
-}
 
 size_t device_smem_optin() {
     int dev = 0, v = 0;
@@ -457,27 +746,40 @@ size_t device_smem_optin() {
     return (size_t)v;
 }
 
+cudaError_t gemv_take_status(uint32_t* word) {
+    cudaError_t e = cudaMemcpyFromSymbol(word, g_gemv_status, sizeof(uint32_t));
+    if (e != cudaSuccess) return e;
+    const uint32_t zero = 0;
+    return cudaMemcpyToSymbol(g_gemv_status, &zero, sizeof(uint32_t));
+}
+
+bool gemv_fits(int64_t M, int64_t N, int64_t K, int G, int nmat) {
+    Plan pl;
+    int sms = device_sms();
+    if (sms <= 0) sms = 148;
+    size_t cap = device_smem_optin();
+    if (cap == 0) cap = 227 * 1024;
+    return make_plan(M, N, K, G, nmat, sms, cap, pl);
+}
+
 cudaError_t launch_gemv(const void* x, const GemvMat* mats, int nmat, int64_t M, int64_t N, int64_t K, int G,
                         cudaStream_t stream) {
-    GemvParams p;
+    const int sms = device_sms();
+    if (sms <= 0) return cudaErrorNoDevice;
+    const size_t cap = device_smem_optin();
+    Plan pl;
+    if (!make_plan(M, N, K, G, nmat, sms, cap, pl)) return cudaErrorNotSupported;
+    GemvParams& p = pl.p;
     p.x = static_cast<const __nv_bfloat16*>(x);
-    p.mat[0] = mats[0];
-    p.mat[1] = nmat == 2 ? mats[1] : mats[0];
-    p.N = N;
-    p.K = K;
-    p.M = (int)M;
-    p.G = G;
-    p.tiles_per_mat = (int)((N + 15) / 16);
-    p.total_tiles = p.tiles_per_mat * nmat;
-    p.tile_groups = 0;
-    const size_t smem = gemv_smem_bytes(M, K, G, nmat);
-    if (smem == 0) return cudaErrorInvalidValue;
-    int dev = 0, sms = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    return M <= 8 ? launch_g<1>(p, smem, sms, stream) : launch_g<2>(p, smem, sms, stream);
+    CUtensorMap tm[2];
+    for (int i = 0; i < 2; ++i) {
+        const GemvMat& mt = mats[i < nmat ? i : 0];
+        p.s[i] = static_cast<const unsigned short*>(mt.s);
+        p.z[i] = mt.z;
+        p.y[i] = static_cast<__nv_bfloat16*>(mt.y);
+        if (!make_code_map(&tm[i], mt.q, N, K, p.P)) return cudaErrorInvalidValue;
+    }
+    return pl.nb == 1 ? launch_nb<1>(tm[0], tm[1], pl, stream) : launch_nb<2>(tm[0], tm[1], pl, stream);
 }
 
 }  // namespace w4a16

@@ -19,8 +19,9 @@ struct GemvMat {
     void* y;
 };
 
-// Shared memory the GEMV needs for this shape (bytes), or 0 when M is out of range.
-size_t gemv_smem_bytes(int64_t M, int64_t K, int G, int ntiles);
+// Whether the decode GEMV takes this shape (M <= 16 and its x staging plus
+// stream rings fit the device's shared memory).  Host only.
+bool gemv_fits(int64_t M, int64_t N, int64_t K, int G, int nmat);
 // Largest dynamic shared memory a block may use on the current device.
 size_t device_smem_optin();
 
@@ -40,7 +41,10 @@ cudaError_t launch_gemm_noalloc(const void* x, const GemvMat& mat, int64_t M, in
 // Activation rows per tensor-core tile for M rows.
 int gemm_tile_n(int64_t M);
 
-// Per-device status word written by kernels whose bounded waits gave up.
+// Per-device status words written by kernels whose bounded waits gave up:
+// synchronise, return the OR of both paths' words and clear them.
 cudaError_t read_and_clear_status(uint32_t* word);
+// The decode kernel's word (read and cleared; no synchronisation).
+cudaError_t gemv_take_status(uint32_t* word);
 
 }  // namespace w4a16
