@@ -49,8 +49,9 @@ __device__ uint32_t g_gemv_status = 0;
 
 namespace {
 
-constexpr int kWarps = 12;
-constexpr int kThreads = kWarps * 32;
+// Warps per CTA: 16 where the kernel instance fits 128 registers per thread
+// (one activation-row block, G >= 64), else 12.
+__host__ __device__ constexpr int cta_warps(int NB, int G) { return NB == 1 && G >= 64 ? 16 : 12; }
 constexpr int kUnitBytes = 2048;          // 16 virtual rows x 128 bytes (256 codes)
 constexpr int kSlots = 4;                 // partial-sum slots per output (warps sharing a tile)
 constexpr int kMaxDevices = 64;
@@ -76,7 +77,8 @@ struct GemvParams {
                                            // per padded segment, groups per row
     int lds, ldz;
     int tiles_per_mat, total_tiles;
-    int warps;                             // consumer warps that take units (<= kWarps)
+    int nw;                                // warps in the CTA
+    int warps;                             // warps that take units (<= nw)
     int nst;                               // unit slots per warp ring (power of two)
     int rows_cap;                          // weight rows per CTA the partial buffer holds
 };
@@ -92,7 +94,7 @@ __host__ __device__ inline Layout make_layout(const GemvParams& p, int nb, int H
     Layout L;
     uint32_t off = 0;
     L.ring = off;
-    off += (uint32_t)(kWarps * p.nst * kUnitBytes);
+    off += (uint32_t)(p.nw * p.nst * kUnitBytes);
     L.xs = off;
     off += align_up((uint32_t)p.xcols * (uint32_t)p.Ks * 2u, 16);        // xcols x Ks FP16 (whole chunks)
     L.zero = off;
@@ -106,9 +108,9 @@ __host__ __device__ inline Layout make_layout(const GemvParams& p, int nb, int H
     L.part = off;
     off += align_up((uint32_t)p.rows_cap * (uint32_t)p.M * kSlots * 4u, 16);
     L.red = off;
-    off += (uint32_t)kWarps * 16u * 8u * (uint32_t)nb * 4u;
+    off += (uint32_t)p.nw * 16u * 8u * (uint32_t)nb * 4u;
     L.bars = off;
-    off += (uint32_t)kWarps * (uint32_t)p.nst * 8u;
+    off += (uint32_t)p.nw * (uint32_t)p.nst * 8u;
     L.total = off;
     return L;
 }
@@ -116,11 +118,21 @@ __host__ __device__ inline Layout make_layout(const GemvParams& p, int nb, int H
 // Warp MMA m16n8k16, FP16 inputs, FP32 accumulate (D = A*B + C).
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                         uint32_t b0, uint32_t b1) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
         "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Same with C = 0 (starts a fresh accumulation).
+__device__ __forceinline__ void mma_f16_c0(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                           uint32_t b0, uint32_t b1) {
+    asm(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};\n"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -177,17 +189,24 @@ __device__ __forceinline__ bool gemv_wait(uint32_t bar, uint32_t parity) {
     return true;
 }
 
-template <int NB, int G, int H>
-__global__ void __launch_bounds__(kThreads, 1)
+// M1: one activation row with P >= 2 segments.  The B columns are then
+// (parity, segment) pairs and each lane holds at most one useful D value per
+// row, so the block-end correction is done once per row on that value only.
+template <int NB, int G, int H, bool M1>
+__global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
     gemv_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
                 const GemvParams p) {
     constexpr int V = G >= 128 ? 4 : G / 32;      // words per lane per code load
     constexpr int GPC = 256 / G;                  // groups per chunk (H divides it)
     constexpr int WSG = G / 32;                   // word steps per group
     constexpr int DM = 4;                         // unroll of the unit loop
+    constexpr int kWarps = cta_warps(NB, G);
+    constexpr int kThreads = kWarps * 32;
     static_assert(GPC % H == 0, "a block of H groups lies inside one chunk");
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned base; derived by pointer arithmetic on the shared array so
+    // the compiler keeps every access below in the shared address space
+    uint8_t* base = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
     const Layout L = make_layout(p, NB, H);
     const uint32_t sbase = tc::smem_u32(base);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -283,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                            (uint32_t)h[2] | ((uint32_t)h[6] << 16), (uint32_t)h[3] | ((uint32_t)h[7] << 16));
             if ((wseg & (GW - 1)) == 0) {
                 const int gam = wseg / GW;                 // group in the segment
-                const int col = ((pseg * H) + (gam % H)) * M + m;
+                const int col = M1 ? (gam % H) * p.P + pseg : ((pseg * H) + (gam % H)) * M + m;
                 exs[(gam / H) * (8 * NB) + col] = make_float2(e, xsum);
             }
         }
@@ -355,8 +374,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int nb = 0; nb < NB; ++nb) {
             const int j = nb * 8 + g;
             if (j < p.cols) {
-                const int m = j % p.M, ph = j / p.M;
-                const int hh = ph % H, ps = ph / H;
+                int m, hh, ps;
+                if constexpr (M1) {
+                    m = 0;
+                    hh = j / p.P;
+                    ps = j - hh * p.P;
+                } else {
+                    m = j % p.M;
+                    const int ph = j / p.M;
+                    hh = ph % H;
+                    ps = ph / H;
+                }
                 xl[nb] = sbase + L.xs + (uint32_t)(((ps * p.M + m) * 4 + t) * 16);
                 lh[nb] = hh;
             } else {
@@ -374,6 +402,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 hc[nb][e] = j < p.cols ? (j / p.M) % H : 0;
             }
         const uint32_t exlane = sbase + L.exs + (uint32_t)(2 * t * 8);
+        // M1: this lane's D columns 2t, 2t+1 are segments p0, p0+1 of parity h_use; it holds the
+        // useful value of its rows (segment pa) when pa is one of them, in column e_use
+        const int p0 = (2 * t) % p.P, h_use = (2 * t) / p.P;
+        const int e_use = pa - p0;
+        const bool useful = M1 && (unsigned)e_use < 2u && 2 * t < p.cols;   // columns past P*H are idle
+        const uint32_t ex_m1 = sbase + L.exs + (uint32_t)((h_use * p.P + pa) * 8);
 
         // slot of the first tile of the run: warps before this one that hold units of it
         int first_slot = 0;
@@ -396,6 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[nb][e] = 0.0f;
+        float acc_a = 0.0f, acc_b = 0.0f;                  // M1: this lane's useful sums
         int tl = u0 / p.C, c = u0 - (u0 / p.C) * p.C;
         const int lg = 31 - __clz(nsl);
         for (int ub = u0; ub < u1 && ok; ub += DM) {
@@ -413,6 +448,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t* zra = zmtab + rla * p.ldz;
                         const uint32_t* zrb = zmtab + rlb * p.ldz;
                         const int gia = pa * p.ngs + c * GPC, gib = pb * p.ngs + c * GPC;   // first group of the chunk
+                        // M1: scales of the lane's parity; zero words shifted to the lane's first group
+                        const unsigned short* sra1 = sra + h_use;
+                        const unsigned short* srb1 = srb + h_use;
+                        uint32_t zwa1 = 0u, zwb1 = 0u;
+                        if constexpr (M1) {
+                            zwa1 = zra[gia >> 3] >> (4 * ((gia & 7) + h_use));
+                            zwb1 = zrb[gib >> 3] >> (4 * ((gib & 7) + h_use));
+                        }
                         const uint32_t unit = ring + slot * (uint32_t)kUnitBytes;
                         const uint32_t row_a = unit + (uint32_t)va * 128u, row_b = row_a + 8u * 128u;
                         const uint32_t xu = (uint32_t)(c * 8) * xstep;
@@ -427,10 +470,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 xsp[nb][hh] = on ? xstep : 0u;
                             }
                         float da[NB][4], db[NB][4];
-#pragma unroll
-                        for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) da[nb][e] = db[nb][e] = 0.0f;
 #pragma unroll
                         for (int bq = 0; bq < 8 / V; ++bq) {
                             uint32_t wa[V], wb[V];
@@ -465,16 +504,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                                 for (int nb = 0; nb < NB; ++nb) {
                                     const uint4 xv = lds128(xb[nb][hcur] + (uint32_t)ws * xsp[nb][hcur]);
-                                    mma_f16(da[nb], a0, b0, a1, b1, xv.x, xv.y);
-                                    mma_f16(db[nb], a2, b2, a3, b3, xv.z, xv.w);
+                                    if (ws % (WSG * H) == 0) {              // first step of a block
+                                        mma_f16_c0(da[nb], a0, b0, a1, b1, xv.x, xv.y);
+                                        mma_f16_c0(db[nb], a2, b2, a3, b3, xv.z, xv.w);
+                                    } else {
+                                        mma_f16(da[nb], a0, b0, a1, b1, xv.x, xv.y);
+                                        mma_f16(db[nb], a2, b2, a3, b3, xv.z, xv.w);
+                                    }
                                 }
                                 if ((ws + 1) % (WSG * H) == 0) {            // block of H groups complete
                                     const int jg0 = jg - (H - 1);           // first group of the block in the chunk
                                     const int blk = (c * GPC + jg0) / H;    // block in the segment
-                                    // scales of the block's H groups (consecutive halves) and their zero points;
-                                    // groups past the row end (last, partial chunk of one segment) get scale 0
-                                    float sa[H], sb[H], za[H], zb[H];
-                                    {
+                                    if constexpr (M1) {
+                                        // one useful value per row: segment pa, parity h_use, column e_use
+                                        const float va_ = e_use ? da[0][1] + db[0][1] : da[0][0] + db[0][0];
+                                        const float vb_ = e_use ? da[0][3] + db[0][3] : da[0][2] + db[0][2];
+                                        const float s_a = __half2float(__ushort_as_half(sra1[jg0]));
+                                        const float s_b = __half2float(__ushort_as_half(srb1[jg0]));
+                                        const float z_a = meta_zero(zwa1, jg0), z_b = meta_zero(zwb1, jg0);
+                                        const float2 ex = *reinterpret_cast<const float2*>(
+                                            base + (ex_m1 - sbase) + (uint32_t)(blk * 8 * 8));
+                                        acc_a = fmaf(s_a, va_ - fmaf(z_a, ex.y, ex.x), acc_a);
+                                        acc_b = fmaf(s_b, vb_ - fmaf(z_b, ex.y, ex.x), acc_b);
+                                    } else {
+                                        // scales of the block's H groups (consecutive halves) and their zero
+                                        // points; groups past the row end (last, partial chunk of one
+                                        // segment) get scale 0
+                                        float sa[H], sb[H], za[H], zb[H];
                                         const uint32_t zwa = zra[(gia + jg0) >> 3] >> (4 * ((gia + jg0) & 7));
                                         const uint32_t zwb = zrb[(gib + jg0) >> 3] >> (4 * ((gib + jg0) & 7));
 #pragma unroll
@@ -485,52 +541,70 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             za[hh] = meta_zero(zwa, hh);
                                             zb[hh] = meta_zero(zwb, hh);
                                         }
-                                    }
 #pragma unroll
-                                    for (int nb = 0; nb < NB; ++nb) {
-                                        const float4 ex = lds_f4(exlane + (uint32_t)((blk * 8 * NB + nb * 8) * 8));
+                                        for (int nb = 0; nb < NB; ++nb) {
+                                            const float4 ex = lds_f4(exlane + (uint32_t)((blk * 8 * NB + nb * 8) * 8));
 #pragma unroll
-                                        for (int e = 0; e < 2; ++e) {
-                                            float s_a = sa[0], s_b = sb[0], z_a = za[0], z_b = zb[0];
+                                            for (int e = 0; e < 2; ++e) {
+                                                float s_a = sa[0], s_b = sb[0], z_a = za[0], z_b = zb[0];
 #pragma unroll
-                                            for (int hh = 1; hh < H; ++hh)
-                                                if (hc[nb][e] == hh) {
-                                                    s_a = sa[hh]; s_b = sb[hh]; z_a = za[hh]; z_b = zb[hh];
-                                                }
-                                            const float E = e ? ex.z : ex.x, X = e ? ex.w : ex.y;
-                                            acc[nb][e] = fmaf(s_a, (da[nb][e] + db[nb][e]) - fmaf(z_a, X, E), acc[nb][e]);
-                                            acc[nb][2 + e] =
-                                                fmaf(s_b, (da[nb][2 + e] + db[nb][2 + e]) - fmaf(z_b, X, E), acc[nb][2 + e]);
+                                                for (int hh = 1; hh < H; ++hh)
+                                                    if (hc[nb][e] == hh) {
+                                                        s_a = sa[hh]; s_b = sb[hh]; z_a = za[hh]; z_b = zb[hh];
+                                                    }
+                                                const float E = e ? ex.z : ex.x, X = e ? ex.w : ex.y;
+                                                acc[nb][e] =
+                                                    fmaf(s_a, (da[nb][e] + db[nb][e]) - fmaf(z_a, X, E), acc[nb][e]);
+                                                acc[nb][2 + e] = fmaf(s_b, (da[nb][2 + e] + db[nb][2 + e]) -
+                                                                               fmaf(z_b, X, E), acc[nb][2 + e]);
+                                            }
                                         }
-#pragma unroll
-                                        for (int e = 0; e < 4; ++e) da[nb][e] = db[nb][e] = 0.0f;
                                     }
                                 }
                             }
                         }
                         // tile finished in this warp's run: reduce the diagonal over segments and parities
                         if (c == p.C - 1 || u == u1 - 1) {
+                            if constexpr (M1) {
+                                // red[vrow][parity]: written by the one lane holding each useful sum
+                                if (useful) {
+                                    red[va * H + h_use] = acc_a;
+                                    red[vb * H + h_use] = acc_b;
+                                }
+                                acc_a = acc_b = 0.0f;
+                                __syncwarp();
+                                const int slotp = (tl * p.C < u0) ? first_slot : 0;
+                                if (lane < p.R) {
+                                    float sum = 0.0f;
+                                    for (int q = 0; q < p.P; ++q)
 #pragma unroll
-                            for (int nb = 0; nb < NB; ++nb) {
-                                red[va * 8 * NB + nb * 8 + 2 * t] = acc[nb][0];
-                                red[va * 8 * NB + nb * 8 + 2 * t + 1] = acc[nb][1];
-                                red[vb * 8 * NB + nb * 8 + 2 * t] = acc[nb][2];
-                                red[vb * 8 * NB + nb * 8 + 2 * t + 1] = acc[nb][3];
+                                        for (int hh = 0; hh < H; ++hh) sum += red[(lane * p.P + q) * H + hh];
+                                    part[(tl * p.R + lane) * kSlots + slotp] = sum;
+                                }
+                                __syncwarp();
+                            } else {
 #pragma unroll
-                                for (int e = 0; e < 4; ++e) acc[nb][e] = 0.0f;
+                                for (int nb = 0; nb < NB; ++nb) {
+                                    red[va * 8 * NB + nb * 8 + 2 * t] = acc[nb][0];
+                                    red[va * 8 * NB + nb * 8 + 2 * t + 1] = acc[nb][1];
+                                    red[vb * 8 * NB + nb * 8 + 2 * t] = acc[nb][2];
+                                    red[vb * 8 * NB + nb * 8 + 2 * t + 1] = acc[nb][3];
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) acc[nb][e] = 0.0f;
+                                }
+                                __syncwarp();
+                                const int slotp = (tl * p.C < u0) ? first_slot : 0;
+                                for (int o = lane; o < p.R * p.M; o += 32) {   // R*M reaches 256
+                                    const int rho = o / p.M, m = o - rho * p.M;
+                                    float sum = 0.0f;
+                                    for (int q = 0; q < p.P; ++q)
+#pragma unroll
+                                        for (int hh = 0; hh < H; ++hh)
+                                            sum += red[(rho * p.P + q) * 8 * NB + (q * H + hh) * p.M + m];
+                                    part[((tl * p.R + rho) * p.M + m) * kSlots + slotp] = sum;
+                                }
+                                __syncwarp();
                             }
-                            __syncwarp();
-                            const int slotp = (tl * p.C < u0) ? first_slot : 0;
-                            for (int o = lane; o < p.R * p.M; o += 32) {   // R*M reaches 256
-                                const int rho = o / p.M, m = o - rho * p.M;
-                                float sum = 0.0f;
-                                for (int q = 0; q < p.P; ++q)
-#pragma unroll
-                                    for (int hh = 0; hh < H; ++hh)
-                                        sum += red[(rho * p.P + q) * 8 * NB + (q * H + hh) * p.M + m];
-                                part[((tl * p.R + rho) * p.M + m) * kSlots + slotp] = sum;
-                            }
-                            __syncwarp();
                         }
                         // this slot is read: refill it with the unit nsl ahead
                         __syncwarp();
@@ -665,7 +739,8 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int G, int nmat, int sms, size_t
     if ((long long)tmax * p.C >= (1ll << 26)) return false;
     // warps taking units: as many as keep every tile within kSlots consecutive warps
     p.warps = 1;
-    for (int w = kWarps; w >= 1; --w) {
+    p.nw = cta_warps(pl.nb, G);
+    for (int w = p.nw; w >= 1; --w) {
         const long long units = (long long)tmin * p.C;
         const long long per = units / w;
         if (per < 1) continue;
@@ -685,20 +760,29 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int G, int nmat, int sms, size_t
     return false;
 }
 
-template <int NB, int G, int H>
-cudaError_t launch_t(const CUtensorMap& tm0, const CUtensorMap& tm1, const Plan& pl, cudaStream_t stream) {
+template <int NB, int G, int H, bool M1>
+cudaError_t launch_m(const CUtensorMap& tm0, const CUtensorMap& tm1, const Plan& pl, cudaStream_t stream) {
     static int cached[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     if ((int)pl.smem > cached[dev]) {
-        e = cudaFuncSetAttribute(gemv_kernel<NB, G, H>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+        e = cudaFuncSetAttribute(gemv_kernel<NB, G, H, M1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)pl.smem);
         if (e != cudaSuccess) return e;
         cached[dev] = (int)pl.smem;
     }
-    gemv_kernel<NB, G, H><<<pl.grid, kThreads, pl.smem, stream>>>(tm0, tm1, pl.p);
+    gemv_kernel<NB, G, H, M1><<<pl.grid, cta_warps(NB, G) * 32, pl.smem, stream>>>(tm0, tm1, pl.p);
     return cudaGetLastError();
+}
+
+template <int NB, int G, int H>
+cudaError_t launch_t(const CUtensorMap& tm0, const CUtensorMap& tm1, const Plan& pl, cudaStream_t stream) {
+    if constexpr (NB == 1) {
+        if (pl.p.M == 1 && pl.p.P >= 2) return launch_m<NB, G, H, true>(tm0, tm1, pl, stream);
+    }
+    return launch_m<NB, G, H, false>(tm0, tm1, pl, stream);
 }
 
 template <int NB, int G>
