@@ -256,54 +256,107 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
         for (int i = 0; i < nsl && it_u < u1; ++i) issue_next();
     }
 
-    // ---- stage x (FP16, fragment order), per-block sums; zero slots -----------
-    // Work item of a warp: 32 consecutive words (one per lane) of one staged
-    // column (segment p, activation row m); words of one group sit in
-    // consecutive lanes, so the group sums are warp shuffles.
+    // ---- stage x (FP16, fragment order), per-block sums; scale/zero rows ------
     {
+        // the CTA's scale and zero rows (contiguous in each matrix) as asynchronous 16-byte copies
+        // that overlap the x staging; rows past N and the gap before the second matrix's rows are
+        // zero-filled
+        {
+            const int r0 = tile0 < p.tiles_per_mat ? tile0 * p.R : 0;                  // first row, matrix 0 part
+            const int n0 = tile1 <= p.tiles_per_mat ? tc_ * p.R : (p.tiles_per_mat - tile0) * p.R;
+            const int l1 = tile0 < p.tiles_per_mat ? (p.tiles_per_mat - tile0) * p.R : 0;   // local row of matrix 1
+            const int t1a = tile0 < p.tiles_per_mat ? p.tiles_per_mat : tile0;
+            const int r1 = (t1a - p.tiles_per_mat) * p.R;                                // first row, matrix 1 part
+            const int n1 = tile1 > p.tiles_per_mat ? (tile1 - t1a) * p.R : 0;
+            const int sv = p.lds / 8, zv = p.ldz / 4;                                   // uint4 per row
+            const uint32_t ms = sbase + L.ms, mz = sbase + L.mz;
+            for (int i = tid; i < p.rows_cap * (sv + zv); i += kThreads) {
+                const bool isz = i >= p.rows_cap * sv;
+                const int ii = isz ? i - p.rows_cap * sv : i;
+                const int per = isz ? zv : sv;
+                const int lr = ii / per, col = ii - lr * per;
+                int mat = 0, row = -1;
+                if (tile0 < p.tiles_per_mat && lr < n0) {
+                    row = r0 + lr;
+                } else if (lr >= l1 && lr - l1 < n1) {
+                    mat = 1;
+                    row = r1 + (lr - l1);
+                }
+                const bool have = row >= 0 && row < p.N;
+                const uint4* src = isz ? reinterpret_cast<const uint4*>((mat ? p.z[1] : p.z[0]) +
+                                                                        (int64_t)(have ? row : 0) * p.ldz)
+                                       : reinterpret_cast<const uint4*>((mat ? p.s[1] : p.s[0]) +
+                                                                        (int64_t)(have ? row : 0) * p.lds);
+                const uint32_t dst = (isz ? mz : ms) + (uint32_t)ii * 16u;
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src + col),
+                             "r"(have ? 16 : 0)
+                             : "memory");
+            }
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        }
+        // x: work item of a warp = 32 consecutive words (one per lane) of one staged column
+        // (segment p, activation row m); words of one group sit in consecutive lanes, so the
+        // group sums are warp shuffles.  Up to 8 items' loads are in flight before any is used.
         const int xcols = p.xcols, M = p.M, C = p.C;
         uint4* xs = reinterpret_cast<uint4*>(base + L.xs);
         float2* exs = reinterpret_cast<float2*>(base + L.exs);
         const int kseg = p.K / p.P;                        // real codes per segment
         constexpr int GW = G / 8;                          // words per group
+        constexpr int XB = 8;                              // items per batch
         const int items = xcols * C;                       // (column, 32-word block)
-        for (int it = warp; it < items; it += kWarps) {
-            const int xc = it / C, c = it - xc * C;        // one division per 32 words
-            const int pseg = xc / M, m = xc - pseg * M;
-            const int wseg = c * 32 + lane;                // word in the padded segment
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (wseg * 8 < kseg)
-                v = *reinterpret_cast<const uint4*>(p.x + (int64_t)m * p.K + (int64_t)pseg * kseg + wseg * 8);
-            const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-            float f[8];
-            unsigned short h[8];
+        for (int it0 = warp; it0 < items; it0 += XB * kWarps) {
+            uint4 vv[XB];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const __half lo = __float2half_rn(bf16lo_to_f32(in[j]));
-                const __half hi = __float2half_rn(bf16hi_to_f32(in[j]));
-                h[2 * j] = __half_as_ushort(lo);
-                h[2 * j + 1] = __half_as_ushort(hi);
-                f[2 * j] = __half2float(lo);
-                f[2 * j + 1] = __half2float(hi);
+            for (int j = 0; j < XB; ++j) {
+                const int it = it0 + j * kWarps;
+                vv[j] = make_uint4(0u, 0u, 0u, 0u);
+                if (it < items) {
+                    const int xc = it / C, c = it - xc * C;
+                    const int pseg = xc / M, m = xc - pseg * M;
+                    const int wseg = c * 32 + lane;
+                    if (wseg * 8 < kseg)
+                        vv[j] = *reinterpret_cast<const uint4*>(p.x + (int64_t)m * p.K + (int64_t)pseg * kseg +
+                                                                wseg * 8);
+                }
             }
-            // 1024 * (x0 + x2 + x4 + x6) + 64 * (x1 + x3 + x5 + x7), and sum x
-            float e = 1024.0f * (f[0] + f[2] + f[4] + f[6]) + 64.0f * (f[1] + f[3] + f[5] + f[7]);
-            float xsum = f[0] + f[1] + f[2] + f[3] + f[4] + f[5] + f[6] + f[7];
 #pragma unroll
-            for (int off = 1; off < GW; off <<= 1) {
-                e += __shfl_xor_sync(0xFFFFFFFFu, e, off);
-                xsum += __shfl_xor_sync(0xFFFFFFFFu, xsum, off);
-            }
-            const int bq = lane / (4 * V), rem = lane % (4 * V);
-            const int tt = rem / V, ii = rem % V;
-            const int stp = c * 8 + bq * V + ii;
-            xs[(stp * xcols + xc) * 4 + tt] =
-                make_uint4((uint32_t)h[0] | ((uint32_t)h[4] << 16), (uint32_t)h[1] | ((uint32_t)h[5] << 16),
-                           (uint32_t)h[2] | ((uint32_t)h[6] << 16), (uint32_t)h[3] | ((uint32_t)h[7] << 16));
-            if ((wseg & (GW - 1)) == 0) {
-                const int gam = wseg / GW;                 // group in the segment
-                const int col = M1 ? (gam % H) * p.P + pseg : ((pseg * H) + (gam % H)) * M + m;
-                exs[(gam / H) * (8 * NB) + col] = make_float2(e, xsum);
+            for (int j = 0; j < XB; ++j) {
+                const int it = it0 + j * kWarps;
+                if (it >= items) break;                    // warp-uniform
+                const int xc = it / C, c = it - xc * C;
+                const int pseg = xc / M, m = xc - pseg * M;
+                const int wseg = c * 32 + lane;            // word in the padded segment
+                const uint32_t in[4] = {vv[j].x, vv[j].y, vv[j].z, vv[j].w};
+                float f[8];
+                unsigned short h[8];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const __half lo = __float2half_rn(bf16lo_to_f32(in[q]));
+                    const __half hi = __float2half_rn(bf16hi_to_f32(in[q]));
+                    h[2 * q] = __half_as_ushort(lo);
+                    h[2 * q + 1] = __half_as_ushort(hi);
+                    f[2 * q] = __half2float(lo);
+                    f[2 * q + 1] = __half2float(hi);
+                }
+                // 1024 * (x0 + x2 + x4 + x6) + 64 * (x1 + x3 + x5 + x7), and sum x
+                float e = 1024.0f * (f[0] + f[2] + f[4] + f[6]) + 64.0f * (f[1] + f[3] + f[5] + f[7]);
+                float xsum = f[0] + f[1] + f[2] + f[3] + f[4] + f[5] + f[6] + f[7];
+#pragma unroll
+                for (int off = 1; off < GW; off <<= 1) {
+                    e += __shfl_xor_sync(0xFFFFFFFFu, e, off);
+                    xsum += __shfl_xor_sync(0xFFFFFFFFu, xsum, off);
+                }
+                const int bq = lane / (4 * V), rem = lane % (4 * V);
+                const int tt = rem / V, ii = rem % V;
+                const int stp = c * 8 + bq * V + ii;
+                xs[(stp * xcols + xc) * 4 + tt] =
+                    make_uint4((uint32_t)h[0] | ((uint32_t)h[4] << 16), (uint32_t)h[1] | ((uint32_t)h[5] << 16),
+                               (uint32_t)h[2] | ((uint32_t)h[6] << 16), (uint32_t)h[3] | ((uint32_t)h[7] << 16));
+                if ((wseg & (GW - 1)) == 0) {
+                    const int gam = wseg / GW;                 // group in the segment
+                    const int col = M1 ? (gam % H) * p.P + pseg : ((pseg * H) + (gam % H)) * M + m;
+                    exs[(gam / H) * (8 * NB) + col] = make_float2(e, xsum);
+                }
             }
         }
         // E/X columns that no (segment, parity, row) uses stay zero; so does the zero block
@@ -313,41 +366,9 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
             exs[b * (8 * NB) + col] = make_float2(0.0f, 0.0f);
         }
         if (tid == 0) *reinterpret_cast<uint4*>(base + L.zero) = make_uint4(0u, 0u, 0u, 0u);
-        // the CTA's scale and zero rows: contiguous in each matrix, copied with 16-byte vectors
-        // (rows past N, and the gap before the second matrix's rows, stay zero)
-        {
-            const int r0 = tile0 < p.tiles_per_mat ? tile0 * p.R : 0;                  // first row, matrix 0 part
-            const int n0 = tile1 <= p.tiles_per_mat ? tc_ * p.R : (p.tiles_per_mat - tile0) * p.R;
-            const int l1 = tile0 < p.tiles_per_mat ? (p.tiles_per_mat - tile0) * p.R : 0;   // local row of matrix 1
-            const int t1a = tile0 < p.tiles_per_mat ? p.tiles_per_mat : tile0;
-            const int r1 = (t1a - p.tiles_per_mat) * p.R;                                // first row, matrix 1 part
-            const int n1 = tile1 > p.tiles_per_mat ? (tile1 - t1a) * p.R : 0;
-            const int sv = p.lds / 8, zv = p.ldz / 4;                                   // uint4 per row
-            uint4* ms = reinterpret_cast<uint4*>(base + L.ms);
-            uint4* mz = reinterpret_cast<uint4*>(base + L.mz);
-            for (int i = tid; i < p.rows_cap * (sv + zv); i += kThreads) {
-                const bool isz = i >= p.rows_cap * sv;
-                const int ii = isz ? i - p.rows_cap * sv : i;
-                const int per = isz ? zv : sv;
-                const int lr = ii / per, col = ii - lr * per;
-                int mat = -1, row = 0;
-                if (tile0 < p.tiles_per_mat && lr < n0) {
-                    mat = 0;
-                    row = r0 + lr;
-                } else if (lr >= l1 && lr - l1 < n1) {
-                    mat = 1;
-                    row = r1 + (lr - l1);
-                }
-                uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                if (mat >= 0 && row < p.N) {
-                    if (isz) v = reinterpret_cast<const uint4*>((mat ? p.z[1] : p.z[0]) + (int64_t)row * p.ldz)[col];
-                    else v = reinterpret_cast<const uint4*>((mat ? p.s[1] : p.s[0]) + (int64_t)row * p.lds)[col];
-                }
-                (isz ? mz : ms)[ii] = v;
-            }
-        }
         float* part = reinterpret_cast<float*>(base + L.part);
         for (int i = tid; i < p.rows_cap * p.M * kSlots; i += kThreads) part[i] = 0.0f;
+        asm volatile("cp.async.wait_all;" ::: "memory");
     }
     __syncthreads();
 
