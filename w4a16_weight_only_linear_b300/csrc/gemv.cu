@@ -112,7 +112,7 @@ __host__ __device__ inline Layout make_layout(const GemvParams& p, int nb, int H
     L.red = off;
     off += (uint32_t)p.nw * 16u * 8u * (uint32_t)nb * 4u;
     L.bars = off;
-    off += (uint32_t)p.nw * (uint32_t)p.nst * 8u;
+    off += (uint32_t)p.nw * (uint32_t)p.nst * 8u + 8u;    // ring barriers, then the prologue copies' barrier
     L.total = off;
     return L;
 }
@@ -216,8 +216,8 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
 
     // ---- this CTA's tiles and this warp's run of (tile, chunk) units ----------
     const int T = p.total_tiles;
-    const int tile0 = (int)(((long long)blockIdx.x * T) / gridDim.x);
-    const int tile1 = (int)(((long long)(blockIdx.x + 1) * T) / gridDim.x);
+    const int tile0 = (int)((blockIdx.x * (uint32_t)T) / gridDim.x);        // T * grid < 2^32 (host check)
+    const int tile1 = (int)(((blockIdx.x + 1) * (uint32_t)T) / gridDim.x);
     const int tc_ = tile1 - tile0;
     const int units = tc_ * p.C2;                 // < 2^26 (host check), so products below fit 32 bits
     const bool active = warp < p.warps;
@@ -226,12 +226,6 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
     const int nsl = p.nst;                        // unit slots in this warp's ring (power of two)
     const uint32_t ring = sbase + L.ring + (uint32_t)(warp * nsl * kUnitBytes);
     const uint32_t bar0 = sbase + L.bars + (uint32_t)(warp * nsl * 8);
-
-    if (tid == 0) {
-        for (int i = 0; i < kWarps * nsl; ++i) tc::mbar_init(sbase + L.bars + 8u * i, 1);
-        tc::fence_barrier_init();
-    }
-    __syncthreads();
 
     // ---- stream: lane 0 of each warp keeps its ring of units filled -----------
     int it_u = u0, it_tl = 0, it_c = 0;
@@ -256,114 +250,146 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
             ++it_tl;
         }
     };
-    if (active && lane == 0) {
-        for (int i = 0; i < nsl && it_u < u1; ++i) issue_next();
-    }
 
-    // ---- stage x (FP16, fragment order), per-block sums; scale/zero rows ------
+    // ---- prologue ---------------------------------------------------------------------
+    // One thread bulk-copies this CTA's scale and zero rows (contiguous in each matrix);
+    // meanwhile every warp requests its first x items.  Once the rows have landed the
+    // weight ring starts, and x is staged while its first units are in flight (copies
+    // issued together complete in no particular order, so starting the ring earlier would
+    // hold the small inputs behind its bytes).
+    const uint32_t pbar = sbase + L.bars + 8u * (uint32_t)(kWarps * nsl);
+    bool pro_ok = true;                           // the prologue's copies landed (warp-uniform)
+    if (tid == 0) {
+        for (int i = 0; i < kWarps * nsl; ++i) tc::mbar_init(sbase + L.bars + 8u * i, 1);
+        tc::mbar_init(pbar, 1);
+        tc::fence_barrier_init();
+    }
+    __syncthreads();
     {
-        // the CTA's scale and zero rows (contiguous in each matrix) as asynchronous 16-byte copies
-        // that overlap the x staging; rows past N and the gap before the second matrix's rows are
-        // zero-filled
-        {
-            const int r0 = tile0 < p.tiles_per_mat ? tile0 * p.R : 0;                  // first row, matrix 0 part
-            const int n0 = tile1 <= p.tiles_per_mat ? tc_ * p.R : (p.tiles_per_mat - tile0) * p.R;
-            const int l1 = tile0 < p.tiles_per_mat ? (p.tiles_per_mat - tile0) * p.R : 0;   // local row of matrix 1
-            const int t1a = tile0 < p.tiles_per_mat ? p.tiles_per_mat : tile0;
-            const int r1 = (t1a - p.tiles_per_mat) * p.R;                                // first row, matrix 1 part
-            const int n1 = tile1 > p.tiles_per_mat ? (tile1 - t1a) * p.R : 0;
-            const int sv = p.lds / 8, zv = p.ldz / 4;                                   // uint4 per row
-            const uint32_t ms = sbase + L.ms, mz = sbase + L.mz;
-            for (int i = tid; i < p.rows_cap * (sv + zv); i += kThreads) {
-                const bool isz = i >= p.rows_cap * sv;
-                const int ii = isz ? i - p.rows_cap * sv : i;
-                const int per = isz ? zv : sv;
-                const int lr = ii / per, col = ii - lr * per;
-                int mat = 0, row = -1;
-                if (tile0 < p.tiles_per_mat && lr < n0) {
-                    row = r0 + lr;
-                } else if (lr >= l1 && lr - l1 < n1) {
-                    mat = 1;
-                    row = r1 + (lr - l1);
-                }
-                const bool have = row >= 0 && row < p.N;
-                const uint4* src = isz ? reinterpret_cast<const uint4*>((mat ? p.z[1] : p.z[0]) +
-                                                                        (int64_t)(have ? row : 0) * p.ldz)
-                                       : reinterpret_cast<const uint4*>((mat ? p.s[1] : p.s[0]) +
-                                                                        (int64_t)(have ? row : 0) * p.lds);
-                const uint32_t dst = (isz ? mz : ms) + (uint32_t)ii * 16u;
-                asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src + col),
-                             "r"(have ? 16 : 0)
-                             : "memory");
+        // local rows: matrix 0 part at [0, n0), matrix 1 part at [l1, l1 + n1); rows at or past N
+        // and the gap between the parts are not copied but zero-filled
+        const int tpm = p.tiles_per_mat;
+        const bool has0 = tile0 < tpm;
+        const int r0 = has0 ? tile0 * p.R : 0;                                  // first row, matrix 0 part
+        const int n0 = !has0 ? 0 : tile1 <= tpm ? tc_ * p.R : (tpm - tile0) * p.R;
+        const int l1 = has0 ? (tpm - tile0) * p.R : 0;                        // local row of matrix 1
+        const int t1a = has0 ? tpm : tile0;
+        const int r1 = (t1a - tpm) * p.R;                                      // first row, matrix 1 part
+        const int n1 = tile1 > tpm ? (tile1 - t1a) * p.R : 0;
+        const int c0 = max(0, min(n0, p.N - r0)), c1 = max(0, min(n1, p.N - r1));   // rows copied
+        const uint32_t sbytes = (uint32_t)p.lds * 2u, zbytes = (uint32_t)p.ldz * 4u;   // per row
+        const uint32_t ms = sbase + L.ms, mz = sbase + L.mz;
+        if (tid == 0) {
+            tc::mbar_arrive_expect_tx(pbar, (uint32_t)(c0 + c1) * (sbytes + zbytes));
+            if (c0 > 0) {
+                tc::bulk_load(ms, p.s[0] + (int64_t)r0 * p.lds, (uint32_t)c0 * sbytes, pbar);
+                tc::bulk_load(mz, p.z[0] + (int64_t)r0 * p.ldz, (uint32_t)c0 * zbytes, pbar);
             }
-            asm volatile("cp.async.commit_group;" ::: "memory");
+            if (c1 > 0) {
+                tc::bulk_load(ms + (uint32_t)l1 * sbytes, p.s[1] + (int64_t)r1 * p.lds, (uint32_t)c1 * sbytes, pbar);
+                tc::bulk_load(mz + (uint32_t)l1 * zbytes, p.z[1] + (int64_t)r1 * p.ldz, (uint32_t)c1 * zbytes, pbar);
+            }
         }
+
         // x: work item of a warp = 32 consecutive words (one per lane) of one staged column
-        // (segment p, activation row m); words of one group sit in consecutive lanes, so the
-        // group sums are warp shuffles.  Up to 8 items' loads are in flight before any is used.
+        // xc = (segment pseg, activation row m) and 32-word block c; the warp's items are
+        // it = warp + k * kWarps, k = 0, 1, ..., stepped through without division.  Words of one
+        // group sit in consecutive lanes, so the group sums are warp shuffles.  A batch of XB
+        // items' loads is in flight before any is used.
         const int xcols = p.xcols, M = p.M, C = p.C;
         uint4* xs = reinterpret_cast<uint4*>(base + L.xs);
         float2* exs = reinterpret_cast<float2*>(base + L.exs);
         const int kseg = p.K / p.P;                        // real codes per segment
         constexpr int GW = G / 8;                          // words per group
         constexpr int XB = 8;                              // items per batch
-        const int items = xcols * C;                       // (column, 32-word block)
-        for (int it0 = warp; it0 < items; it0 += XB * kWarps) {
-            uint4 vv[XB];
+        const int dxc = kWarps / C, dc = kWarps - dxc * C;                 // item step as (column, block)
+        const uint32_t minv = (65536u + (uint32_t)M - 1u) / (uint32_t)M;  // xc / M = (xc * minv) >> 16 (xc < 2^12)
+        int xc_n = warp / C, c_n = warp - (warp / C) * C;  // next item of this warp
+        int bxc[XB], bc[XB];                               // the batch's items
+        uint4 vv[XB];
+        auto x_load = [&]() {                              // next batch: positions, then loads
 #pragma unroll
             for (int j = 0; j < XB; ++j) {
-                const int it = it0 + j * kWarps;
-                vv[j] = make_uint4(0u, 0u, 0u, 0u);
-                if (it < items) {
-                    const int xc = it / C, c = it - xc * C;
-                    const int pseg = xc / M, m = xc - pseg * M;
-                    const int wseg = c * 32 + lane;
-                    if (wseg * 8 < kseg)
-                        vv[j] = *reinterpret_cast<const uint4*>(p.x + (int64_t)m * p.K + (int64_t)pseg * kseg +
-                                                                wseg * 8);
+                bxc[j] = xc_n;
+                bc[j] = c_n;
+                c_n += dc;
+                xc_n += dxc;
+                if (c_n >= C) {
+                    c_n -= C;
+                    ++xc_n;
                 }
             }
 #pragma unroll
             for (int j = 0; j < XB; ++j) {
-                const int it = it0 + j * kWarps;
-                if (it >= items) break;                    // warp-uniform
-                const int xc = it / C, c = it - xc * C;
-                const int pseg = xc / M, m = xc - pseg * M;
+                vv[j] = make_uint4(0u, 0u, 0u, 0u);
+                const int pseg = (int)(((uint32_t)bxc[j] * minv) >> 16), m = bxc[j] - pseg * M;
+                const int wseg = bc[j] * 32 + lane;
+                if (bxc[j] < xcols && wseg * 8 < kseg)
+                    vv[j] = *reinterpret_cast<const uint4*>(p.x + (int64_t)m * p.K + (int64_t)pseg * kseg + wseg * 8);
+            }
+        };
+        auto x_stage = [&]() {
+            const int bq = lane / (4 * V), rem = lane % (4 * V);
+            const int tt = rem / V, ii = rem % V;
+#pragma unroll
+            for (int j = 0; j < XB; ++j) {
+                if (bxc[j] >= xcols) break;                // warp-uniform
+                const int xc = bxc[j], c = bc[j];
+                const int pseg = (int)(((uint32_t)xc * minv) >> 16), m = xc - pseg * M;
                 const int wseg = c * 32 + lane;            // word in the padded segment
+                // FP16 pairs (x0,x4), (x1,x5), (x2,x6), (x3,x7) of the word's 8 values, and the
+                // FP16-rounded values as floats for the sums
                 const uint32_t in[4] = {vv[j].x, vv[j].y, vv[j].z, vv[j].w};
                 float f[8];
-                unsigned short h[8];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    const __half lo = __float2half_rn(bf16lo_to_f32(in[q]));
-                    const __half hi = __float2half_rn(bf16hi_to_f32(in[q]));
-                    h[2 * q] = __half_as_ushort(lo);
-                    h[2 * q + 1] = __half_as_ushort(hi);
-                    f[2 * q] = __half2float(lo);
-                    f[2 * q + 1] = __half2float(hi);
+                    f[2 * q] = bf16lo_to_f32(in[q]);
+                    f[2 * q + 1] = bf16hi_to_f32(in[q]);
+                }
+                __half2 hp[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    hp[q] = __floats2half2_rn(f[q], f[q + 4]);
+                    f[q] = __low2float(hp[q]);
+                    f[q + 4] = __high2float(hp[q]);
                 }
                 // 1024 * (x0 + x2 + x4 + x6) + 64 * (x1 + x3 + x5 + x7), and sum x
-                float e = 1024.0f * (f[0] + f[2] + f[4] + f[6]) + 64.0f * (f[1] + f[3] + f[5] + f[7]);
-                float xsum = f[0] + f[1] + f[2] + f[3] + f[4] + f[5] + f[6] + f[7];
+                const float se = (f[0] + f[2]) + (f[4] + f[6]), so = (f[1] + f[3]) + (f[5] + f[7]);
+                float e = fmaf(1024.0f, se, 64.0f * so);
+                float xsum = se + so;
 #pragma unroll
                 for (int off = 1; off < GW; off <<= 1) {
                     e += __shfl_xor_sync(0xFFFFFFFFu, e, off);
                     xsum += __shfl_xor_sync(0xFFFFFFFFu, xsum, off);
                 }
-                const int bq = lane / (4 * V), rem = lane % (4 * V);
-                const int tt = rem / V, ii = rem % V;
                 const int stp = c * 8 + bq * V + ii;
                 xs[(stp * xcols + xc) * 4 + tt] =
-                    make_uint4((uint32_t)h[0] | ((uint32_t)h[4] << 16), (uint32_t)h[1] | ((uint32_t)h[5] << 16),
-                               (uint32_t)h[2] | ((uint32_t)h[6] << 16), (uint32_t)h[3] | ((uint32_t)h[7] << 16));
-                if ((wseg & (GW - 1)) == 0) {
+                    make_uint4(*reinterpret_cast<const uint32_t*>(&hp[0]), *reinterpret_cast<const uint32_t*>(&hp[1]),
+                               *reinterpret_cast<const uint32_t*>(&hp[2]), *reinterpret_cast<const uint32_t*>(&hp[3]));
+                if ((lane & (GW - 1)) == 0) {
                     const int gam = wseg / GW;                 // group in the segment
                     const int col = M1 ? (gam % H) * p.P + pseg : ((pseg * H) + (gam % H)) * M + m;
                     exs[(gam / H) * (8 * NB) + col] = make_float2(e, xsum);
                 }
             }
+        };
+        x_load();
+
+        // zero fills: table rows not copied, E/X columns no (segment, parity, row) uses, the
+        // zero block, the partial sums
+        {
+            const int zr0 = c0, zr1 = min(has0 ? l1 : 0, p.rows_cap), zr2 = (has0 ? l1 : 0) + c1;
+            const int sv = p.lds / 8, per = sv + p.ldz / 4;                       // uint4 per row
+            const int nz = (zr1 > zr0 ? zr1 - zr0 : 0) + (p.rows_cap > zr2 ? p.rows_cap - zr2 : 0);
+            for (int i = tid; i < nz * per; i += kThreads) {
+                const int k = i / per, col = i - k * per;
+                const int lr = zr0 + k < zr1 ? zr0 + k : zr2 + (k - (zr1 > zr0 ? zr1 - zr0 : 0));
+                const uint32_t dst = col < sv ? ms + (uint32_t)lr * sbytes + (uint32_t)col * 16u
+                                              : mz + (uint32_t)lr * zbytes + (uint32_t)(col - sv) * 16u;
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(0u), "r"(0u), "r"(0u), "r"(0u)
+                             : "memory");
+            }
         }
-        // E/X columns that no (segment, parity, row) uses stay zero; so does the zero block
         const int nblk = p.ngs / H;
         for (int i = tid; i < nblk * (8 * NB - p.cols); i += kThreads) {
             const int b = i / (8 * NB - p.cols), col = p.cols + i % (8 * NB - p.cols);
@@ -372,12 +398,23 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
         if (tid == 0) *reinterpret_cast<uint4*>(base + L.zero) = make_uint4(0u, 0u, 0u, 0u);
         float* part = reinterpret_cast<float*>(base + L.part);
         for (int i = tid; i < p.rows_cap * p.M * kSlots; i += kThreads) part[i] = 0.0f;
-        asm volatile("cp.async.wait_all;" ::: "memory");
+
+        // the scale/zero rows have landed: lane 0 of each warp starts its ring of units and keeps
+        // it filled from here on
+        pro_ok = __all_sync(0xFFFFFFFFu, gemv_wait(pbar, 0));
+        if (pro_ok && active && lane == 0) {
+            for (int i = 0; i < nsl && it_u < u1; ++i) issue_next();
+        }
+        for (;;) {
+            x_stage();
+            if (xc_n >= xcols) break;                      // warp-uniform
+            x_load();
+        }
     }
     __syncthreads();
 
     // ---- compute -------------------------------------------------------------------
-    bool ok = true;
+    bool ok = pro_ok;
     if (active) {
         const int va = sigma8(g), vb = va + 8, v7 = va & 7;
         const int rho_a = va / p.P, pa = va - rho_a * p.P;
@@ -650,7 +687,7 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
                 }
             }
         }
-        if (!ok && lane == 0) {   // wait for this warp's copies still in flight
+        if (!ok && lane == 0) {   // wait for this warp's ring copies still in flight
             for (int uu = it_u - nsl; uu < it_u; ++uu) {
                 if (uu < u0) continue;
                 const uint32_t bar = bar0 + 8u * (uint32_t)((uu - u0) & (nsl - 1));
@@ -661,6 +698,15 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
                         break;
                     }
                 }
+            }
+        }
+    }
+    if (!pro_ok && tid == 0) {    // the prologue's copies timed out: wait for them once more
+        const long long t0 = clock64();
+        while (!tc::mbar_try_wait(pbar, 0)) {
+            if (clock64() - t0 > kSpinCycles) {
+                atomicOr(&g_gemv_status, kStatusGemvDrain);
+                break;
             }
         }
     }
@@ -768,6 +814,7 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int G, int nmat, int sms, size_t
     pl.grid = p.total_tiles < sms ? p.total_tiles : sms;
     const int tmin = p.total_tiles / pl.grid, tmax = (p.total_tiles + pl.grid - 1) / pl.grid;
     if ((long long)tmax * p.C2 >= (1ll << 26)) return false;
+    if ((long long)p.total_tiles * pl.grid >= (1ll << 32)) return false;
     p.rows_cap = tmax * p.R;
     // CTA warps (the instance's launch bound, or fewer when shared memory is short), then the
     // deepest per-warp ring of units that fits
