@@ -257,6 +257,10 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
     // weight ring starts, and x is staged while its first units are in flight (copies
     // issued together complete in no particular order, so starting the ring earlier would
     // hold the small inputs behind its bytes).
+    // Launched with programmatic stream serialisation: the next launch on the stream may be
+    // scheduled at once (its CTAs take SMs as this grid's CTAs exit), and this grid reads no
+    // global memory before the previous grid on the stream has completed.
+    tc::griddep_launch_dependents();
     const uint32_t pbar = sbase + L.bars + 8u * (uint32_t)(kWarps * nsl);
     bool pro_ok = true;                           // the prologue's copies landed (warp-uniform)
     if (tid == 0) {
@@ -264,6 +268,7 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
         tc::mbar_init(pbar, 1);
         tc::fence_barrier_init();
     }
+    tc::griddep_wait();
     __syncthreads();
     {
         // local rows: matrix 0 part at [0, n0), matrix 1 part at [l1, l1 + n1); rows at or past N
@@ -854,8 +859,18 @@ cudaError_t launch_m(const CUtensorMap& tm0, const CUtensorMap& tm1, const Plan&
         if (e != cudaSuccess) return e;
         cached[dev] = (int)pl.smem;
     }
-    gemv_kernel<NB, G, H, M1><<<pl.grid, pl.p.nw * 32, pl.smem, stream>>>(tm0, tm1, pl.p);
-    return cudaGetLastError();
+    // programmatic stream serialisation: set-up overlaps the tail of the previous launch
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)pl.grid);
+    cfg.blockDim = dim3((unsigned)(pl.p.nw * 32));
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<NB, G, H, M1>, tm0, tm1, pl.p);
 }
 
 template <int NB, int G, int H>

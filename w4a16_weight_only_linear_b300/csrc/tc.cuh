@@ -85,6 +85,18 @@ __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
+// ---- programmatic dependent launch --------------------------------------------
+
+// Lets the next grid on the stream (launched with programmatic stream
+// serialisation) be scheduled before this one finishes; it still waits in
+// griddep_wait for this grid's completion before it reads what this grid wrote.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Blocks until the grids this one depends on have completed and their memory
+// operations are visible; returns at once when the launch had no such dependency.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---- tcgen05 ------------------------------------------------------------------
 
 // Warp-wide: allocate `ncols` tensor-memory columns, base address to smem.
