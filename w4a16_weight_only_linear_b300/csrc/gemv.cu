@@ -74,7 +74,6 @@ struct GemvParams {
     int M, N, K, G;
     int P, R, cols, xcols;                 // segments, weight rows per tile, B columns used (P*H*M),
                                            // staged x columns (P*M)
-    int C2;                                // units per tile: chunk pairs, ceil(C / 2)
     int Ks, C, ngs, ng;                    // codes per segment padded to whole chunks (C of 256), groups
                                            // per padded segment, groups per row
     int lds, ldz;
@@ -201,7 +200,6 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
     constexpr int V = G >= 128 ? 4 : G / 32;      // words per lane per code load
     constexpr int GPC = 256 / G;                  // groups per chunk (H divides it)
     constexpr int WSG = G / 32;                   // word steps per group
-    constexpr int DM = 1;                         // unroll of the unit loop (larger unrolls only grow the code)
     const int kWarps = p.nw;                      // warps launched (at most the launch bound)
     const int kThreads = kWarps * 32;
     static_assert(GPC % H == 0, "a block of H groups lies inside one chunk");
@@ -214,38 +212,43 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t = lane & 3;
 
-    // ---- this CTA's tiles and this warp's run of (tile, chunk) units ----------
+    // ---- this CTA's tiles and this warp's run of chunks -------------------------
     const int T = p.total_tiles;
     const int tile0 = (int)((blockIdx.x * (uint32_t)T) / gridDim.x);        // T * grid < 2^32 (host check)
     const int tile1 = (int)(((blockIdx.x + 1) * (uint32_t)T) / gridDim.x);
     const int tc_ = tile1 - tile0;
-    const int units = tc_ * p.C2;                 // < 2^26 (host check), so products below fit 32 bits
+    const int chunks = tc_ * p.C;                 // < 2^26 (host check), so products below fit 32 bits
     const bool active = warp < p.warps;
-    const int u0 = active ? (warp * units) / p.warps : 0;
-    const int u1 = active ? ((warp + 1) * units) / p.warps : 0;
+    const int ch0 = active ? (warp * chunks) / p.warps : 0;        // this warp's chunks [ch0, ch1)
+    const int ch1 = active ? ((warp + 1) * chunks) / p.warps : 0;
     const int nsl = p.nst;                        // unit slots in this warp's ring (power of two)
     const uint32_t ring = sbase + L.ring + (uint32_t)(warp * nsl * kUnitBytes);
     const uint32_t bar0 = sbase + L.bars + (uint32_t)(warp * nsl * 8);
 
     // ---- stream: lane 0 of each warp keeps its ring of units filled -----------
-    int it_u = u0, it_tl = 0, it_c = 0;
+    // A unit is two consecutive chunks of one tile under one barrier, or one chunk where the
+    // tile or the run ends; producer and consumer walk the same sequence.
+    int it_n = 0, it_ch = ch0, it_tl = 0, it_c = 0;   // units issued; next chunk, its tile and chunk in it
     if (active) {
-        it_tl = u0 / p.C2;
-        it_c = u0 - it_tl * p.C2;
+        it_tl = ch0 / p.C;
+        it_c = ch0 - it_tl * p.C;
     }
     auto issue_next = [&]() {
         const int tau = tile0 + it_tl;
         const int mat = tau >= p.tiles_per_mat;
         const int tile = mat ? tau - p.tiles_per_mat : tau;
-        const uint32_t slot = (uint32_t)((it_u - u0) & (nsl - 1));
+        const uint32_t slot = (uint32_t)(it_n & (nsl - 1));
         const uint32_t bar = bar0 + 8u * slot;
-        const bool two = 2 * it_c + 1 < p.C;             // an odd chunk count leaves a one-chunk unit
+        const bool two = it_c + 1 < p.C && it_ch + 1 < ch1;
         tc::mbar_arrive_expect_tx(bar, (uint32_t)(two ? 2 * kBoxBytes : kBoxBytes));
         const void* tm = mat ? (const void*)&tm1 : (const void*)&tm0;
-        tc::tma_load_2d(ring + slot * (uint32_t)kUnitBytes, tm, 2 * it_c * 32, tile * 16, bar);
-        if (two) tc::tma_load_2d(ring + slot * (uint32_t)kUnitBytes + kBoxBytes, tm, (2 * it_c + 1) * 32, tile * 16, bar);
-        ++it_u;
-        if (++it_c == p.C2) {
+        tc::tma_load_2d(ring + slot * (uint32_t)kUnitBytes, tm, it_c * 32, tile * 16, bar);
+        if (two) tc::tma_load_2d(ring + slot * (uint32_t)kUnitBytes + kBoxBytes, tm, (it_c + 1) * 32, tile * 16, bar);
+        const int n = two ? 2 : 1;
+        ++it_n;
+        it_ch += n;
+        it_c += n;
+        if (it_c == p.C) {
             it_c = 0;
             ++it_tl;
         }
@@ -408,7 +411,7 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
         // it filled from here on
         pro_ok = __all_sync(0xFFFFFFFFu, gemv_wait(pbar, 0));
         if (pro_ok && active && lane == 0) {
-            for (int i = 0; i < nsl && it_u < u1; ++i) issue_next();
+            for (int i = 0; i < nsl && it_ch < ch1; ++i) issue_next();
         }
         for (;;) {
             x_stage();
@@ -476,14 +479,13 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
         const bool useful = M1 && (unsigned)e_use < 2u && 2 * t < p.cols;   // columns past P*H are idle
         const uint32_t ex_m1 = sbase + L.exs + (uint32_t)((h_use * p.P + pa) * 8);
 
-        // slot of the first tile of the run: warps before this one that hold units of it
+        // slot of the first tile of the run: warps before this one that hold chunks of it
         int first_slot = 0;
         {
-            const int ftl = u0 / p.C2;
-            const int fu = ftl * p.C2;
-            if (fu < u0) {
+            const int fch = (ch0 / p.C) * p.C;              // the tile's first chunk
+            if (fch < ch0) {
                 int fw = warp;
-                while (fw > 0 && (fw * units) / p.warps > fu) --fw;
+                while (fw > 0 && (fw * chunks) / p.warps > fch) --fw;
                 first_slot = warp - fw;
             }
         }
@@ -498,206 +500,204 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[nb][e] = 0.0f;
         float acc_a = 0.0f, acc_b = 0.0f;                  // M1: this lane's useful sums
-        int tl = u0 / p.C2, c2 = u0 - (u0 / p.C2) * p.C2;
+        int tl = ch0 / p.C, cu = ch0 - (ch0 / p.C) * p.C, ch = ch0;   // unit's tile, chunk in it, chunk in run
         const int lg = 31 - __clz(nsl);
-        for (int ub = u0; ub < u1 && ok; ub += DM) {
+        for (int k = 0; ch < ch1 && ok; ++k) {
+            const uint32_t slot = (uint32_t)(k & (nsl - 1));
+            ok = gemv_wait(bar0 + 8u * slot, (uint32_t)((k >> lg) & 1));
+            ok = __all_sync(0xFFFFFFFFu, ok);
+            if (ok) {
+                const bool two = cu + 1 < p.C && ch + 1 < ch1;   // as in issue_next
 #pragma unroll
-            for (int jj = 0; jj < DM; ++jj) {
-                const int u = ub + jj;
-                if (u < u1 && ok) {
-                    const uint32_t slot = (uint32_t)((u - u0) & (nsl - 1));
-                    ok = gemv_wait(bar0 + 8u * slot, (uint32_t)(((u - u0) >> lg) & 1));
-                    ok = __all_sync(0xFFFFFFFFu, ok);
-                    if (ok) {
+                for (int cc = 0; cc < 2; ++cc) {
+                  if (cc == 1 && !two) break;                 // one-chunk unit (uniform)
+                  const int c = cu + cc;                      // chunk in the tile
+                  const int rla = tl * p.R + rho_a, rlb = tl * p.R + rho_b;   // local rows
+                  const unsigned short* sra = smtab + rla * p.lds + pa * p.ngs + c * GPC;
+                  const unsigned short* srb = smtab + rlb * p.lds + pb * p.ngs + c * GPC;
+                  const uint32_t* zra = zmtab + rla * p.ldz;
+                  const uint32_t* zrb = zmtab + rlb * p.ldz;
+                  const int gia = pa * p.ngs + c * GPC, gib = pb * p.ngs + c * GPC;   // first group of the chunk
+                  // M1: scales of the lane's parity; zero words shifted to the lane's first group
+                  const unsigned short* sra1 = sra + h_use;
+                  const unsigned short* srb1 = srb + h_use;
+                  uint32_t zwa1 = 0u, zwb1 = 0u;
+                  if constexpr (M1) {
+                      zwa1 = zra[gia >> 3] >> (4 * ((gia & 7) + h_use));
+                      zwb1 = zrb[gib >> 3] >> (4 * ((gib & 7) + h_use));
+                  }
+                  const uint32_t unit = ring + slot * (uint32_t)kUnitBytes + (uint32_t)cc * kBoxBytes;
+                  const uint32_t row_a = unit + (uint32_t)va * 128u, row_b = row_a + 8u * 128u;
+                  const uint32_t xu = (uint32_t)(c * 8) * xstep;
+                  // per group parity: x base and step of this lane (idle lanes read zeros)
+                  uint32_t xb[NB][H], xsp[NB][H];
 #pragma unroll
-                        for (int cc = 0; cc < 2; ++cc) {
-                          const int c = 2 * c2 + cc;                  // chunk in the tile
-                          if (c >= p.C) break;                        // one-chunk unit (uniform)
-                          const int rla = tl * p.R + rho_a, rlb = tl * p.R + rho_b;   // local rows
-                          const unsigned short* sra = smtab + rla * p.lds + pa * p.ngs + c * GPC;
-                          const unsigned short* srb = smtab + rlb * p.lds + pb * p.ngs + c * GPC;
-                          const uint32_t* zra = zmtab + rla * p.ldz;
-                          const uint32_t* zrb = zmtab + rlb * p.ldz;
-                          const int gia = pa * p.ngs + c * GPC, gib = pb * p.ngs + c * GPC;   // first group of the chunk
-                          // M1: scales of the lane's parity; zero words shifted to the lane's first group
-                          const unsigned short* sra1 = sra + h_use;
-                          const unsigned short* srb1 = srb + h_use;
-                          uint32_t zwa1 = 0u, zwb1 = 0u;
-                          if constexpr (M1) {
-                              zwa1 = zra[gia >> 3] >> (4 * ((gia & 7) + h_use));
-                              zwb1 = zrb[gib >> 3] >> (4 * ((gib & 7) + h_use));
-                          }
-                          const uint32_t unit = ring + slot * (uint32_t)kUnitBytes + (uint32_t)cc * kBoxBytes;
-                          const uint32_t row_a = unit + (uint32_t)va * 128u, row_b = row_a + 8u * 128u;
-                          const uint32_t xu = (uint32_t)(c * 8) * xstep;
-                          // per group parity: x base and step of this lane (idle lanes read zeros)
-                          uint32_t xb[NB][H], xsp[NB][H];
+                  for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-                          for (int nb = 0; nb < NB; ++nb)
+                      for (int hh = 0; hh < H; ++hh) {
+                          const bool on = lh[nb] == hh;
+                          xb[nb][hh] = on ? xl[nb] + xu : zaddr;
+                          xsp[nb][hh] = on ? xstep : 0u;
+                      }
+                  float da[NB][4], db[NB][4];
 #pragma unroll
-                              for (int hh = 0; hh < H; ++hh) {
-                                  const bool on = lh[nb] == hh;
-                                  xb[nb][hh] = on ? xl[nb] + xu : zaddr;
-                                  xsp[nb][hh] = on ? xstep : 0u;
-                              }
-                          float da[NB][4], db[NB][4];
+                  for (int bq = 0; bq < 8 / V; ++bq) {
+                      uint32_t wa[V], wb[V];
+                      if constexpr (V == 4) {
+                          const uint4 x0 = lds128(row_a + coff[bq]);
+                          const uint4 x1 = lds128(row_b + coff[bq]);
+                          wa[0] = x0.x; wa[1] = x0.y; wa[2] = x0.z; wa[3] = x0.w;
+                          wb[0] = x1.x; wb[1] = x1.y; wb[2] = x1.z; wb[3] = x1.w;
+                      } else if constexpr (V == 2) {
+                          const uint2 x0 = lds64(row_a + coff[bq]);
+                          const uint2 x1 = lds64(row_b + coff[bq]);
+                          wa[0] = x0.x; wa[1] = x0.y;
+                          wb[0] = x1.x; wb[1] = x1.y;
+                      } else {
+                          wa[0] = lds32(row_a + coff[bq]);
+                          wb[0] = lds32(row_b + coff[bq]);
+                      }
 #pragma unroll
-                          for (int bq = 0; bq < 8 / V; ++bq) {
-                              uint32_t wa[V], wb[V];
-                              if constexpr (V == 4) {
-                                  const uint4 x0 = lds128(row_a + coff[bq]);
-                                  const uint4 x1 = lds128(row_b + coff[bq]);
-                                  wa[0] = x0.x; wa[1] = x0.y; wa[2] = x0.z; wa[3] = x0.w;
-                                  wb[0] = x1.x; wb[1] = x1.y; wb[2] = x1.z; wb[3] = x1.w;
-                              } else if constexpr (V == 2) {
-                                  const uint2 x0 = lds64(row_a + coff[bq]);
-                                  const uint2 x1 = lds64(row_b + coff[bq]);
-                                  wa[0] = x0.x; wa[1] = x0.y;
-                                  wb[0] = x1.x; wb[1] = x1.y;
+                      for (int i = 0; i < V; ++i) {
+                          const int ws = bq * V + i;                   // word step in the chunk
+                          const int jg = ws / WSG;                     // group in the chunk
+                          const int hcur = jg % H;                     // its parity (c * GPC is a multiple of H)
+                          const uint32_t a8 = wa[i] >> 8, b8 = wb[i] >> 8;
+                          const uint32_t a0 = lop3_and_or(wa[i], 0x000F000Fu, 0x64006400u);
+                          const uint32_t a1 = lop3_and_or(wa[i], 0x00F000F0u, 0x54005400u);
+                          const uint32_t a2 = lop3_and_or(a8, 0x000F000Fu, 0x64006400u);
+                          const uint32_t a3 = lop3_and_or(a8, 0x00F000F0u, 0x54005400u);
+                          const uint32_t b0 = lop3_and_or(wb[i], 0x000F000Fu, 0x64006400u);
+                          const uint32_t b1 = lop3_and_or(wb[i], 0x00F000F0u, 0x54005400u);
+                          const uint32_t b2 = lop3_and_or(b8, 0x000F000Fu, 0x64006400u);
+                          const uint32_t b3 = lop3_and_or(b8, 0x00F000F0u, 0x54005400u);
+#pragma unroll
+                          for (int nb = 0; nb < NB; ++nb) {
+                              const uint4 xv = lds128(xb[nb][hcur] + (uint32_t)ws * xsp[nb][hcur]);
+                              if (ws % (WSG * H) == 0) {              // first step of a block
+                                  mma_f16_c0(da[nb], a0, b0, a1, b1, xv.x, xv.y);
+                                  mma_f16_c0(db[nb], a2, b2, a3, b3, xv.z, xv.w);
                               } else {
-                                  wa[0] = lds32(row_a + coff[bq]);
-                                  wb[0] = lds32(row_b + coff[bq]);
+                                  mma_f16(da[nb], a0, b0, a1, b1, xv.x, xv.y);
+                                  mma_f16(db[nb], a2, b2, a3, b3, xv.z, xv.w);
                               }
+                          }
+                          if ((ws + 1) % (WSG * H) == 0) {            // block of H groups complete
+                              const int jg0 = jg - (H - 1);           // first group of the block in the chunk
+                              const int blk = (c * GPC + jg0) / H;    // block in the segment
+                              if constexpr (M1) {
+                                  // one useful value per row: segment pa, parity h_use, column e_use
+                                  const float va_ = e_use ? da[0][1] + db[0][1] : da[0][0] + db[0][0];
+                                  const float vb_ = e_use ? da[0][3] + db[0][3] : da[0][2] + db[0][2];
+                                  const float s_a = __half2float(__ushort_as_half(sra1[jg0]));
+                                  const float s_b = __half2float(__ushort_as_half(srb1[jg0]));
+                                  const float z_a = meta_zero(zwa1, jg0), z_b = meta_zero(zwb1, jg0);
+                                  const float2 ex = *reinterpret_cast<const float2*>(
+                                      base + (ex_m1 - sbase) + (uint32_t)(blk * 8 * 8));
+                                  acc_a = fmaf(s_a, va_ - fmaf(z_a, ex.y, ex.x), acc_a);
+                                  acc_b = fmaf(s_b, vb_ - fmaf(z_b, ex.y, ex.x), acc_b);
+                              } else {
+                                  // scales of the block's H groups (consecutive halves) and their zero
+                                  // points; groups past the row end (last, partial chunk of one
+                                  // segment) get scale 0
+                                  float sa[H], sb[H], za[H], zb[H];
+                                  const uint32_t zwa = zra[(gia + jg0) >> 3] >> (4 * ((gia + jg0) & 7));
+                                  const uint32_t zwb = zrb[(gib + jg0) >> 3] >> (4 * ((gib + jg0) & 7));
 #pragma unroll
-                              for (int i = 0; i < V; ++i) {
-                                  const int ws = bq * V + i;                   // word step in the chunk
-                                  const int jg = ws / WSG;                     // group in the chunk
-                                  const int hcur = jg % H;                     // its parity (c * GPC is a multiple of H)
-                                  const uint32_t a8 = wa[i] >> 8, b8 = wb[i] >> 8;
-                                  const uint32_t a0 = lop3_and_or(wa[i], 0x000F000Fu, 0x64006400u);
-                                  const uint32_t a1 = lop3_and_or(wa[i], 0x00F000F0u, 0x54005400u);
-                                  const uint32_t a2 = lop3_and_or(a8, 0x000F000Fu, 0x64006400u);
-                                  const uint32_t a3 = lop3_and_or(a8, 0x00F000F0u, 0x54005400u);
-                                  const uint32_t b0 = lop3_and_or(wb[i], 0x000F000Fu, 0x64006400u);
-                                  const uint32_t b1 = lop3_and_or(wb[i], 0x00F000F0u, 0x54005400u);
-                                  const uint32_t b2 = lop3_and_or(b8, 0x000F000Fu, 0x64006400u);
-                                  const uint32_t b3 = lop3_and_or(b8, 0x00F000F0u, 0x54005400u);
+                                  for (int hh = 0; hh < H; ++hh) {
+                                      const bool va_ = gia + jg0 + hh < p.ng, vb_ = gib + jg0 + hh < p.ng;
+                                      sa[hh] = va_ ? __half2float(__ushort_as_half(sra[jg0 + hh])) : 0.0f;
+                                      sb[hh] = vb_ ? __half2float(__ushort_as_half(srb[jg0 + hh])) : 0.0f;
+                                      za[hh] = meta_zero(zwa, hh);
+                                      zb[hh] = meta_zero(zwb, hh);
+                                  }
 #pragma unroll
                                   for (int nb = 0; nb < NB; ++nb) {
-                                      const uint4 xv = lds128(xb[nb][hcur] + (uint32_t)ws * xsp[nb][hcur]);
-                                      if (ws % (WSG * H) == 0) {              // first step of a block
-                                          mma_f16_c0(da[nb], a0, b0, a1, b1, xv.x, xv.y);
-                                          mma_f16_c0(db[nb], a2, b2, a3, b3, xv.z, xv.w);
-                                      } else {
-                                          mma_f16(da[nb], a0, b0, a1, b1, xv.x, xv.y);
-                                          mma_f16(db[nb], a2, b2, a3, b3, xv.z, xv.w);
-                                      }
-                                  }
-                                  if ((ws + 1) % (WSG * H) == 0) {            // block of H groups complete
-                                      const int jg0 = jg - (H - 1);           // first group of the block in the chunk
-                                      const int blk = (c * GPC + jg0) / H;    // block in the segment
-                                      if constexpr (M1) {
-                                          // one useful value per row: segment pa, parity h_use, column e_use
-                                          const float va_ = e_use ? da[0][1] + db[0][1] : da[0][0] + db[0][0];
-                                          const float vb_ = e_use ? da[0][3] + db[0][3] : da[0][2] + db[0][2];
-                                          const float s_a = __half2float(__ushort_as_half(sra1[jg0]));
-                                          const float s_b = __half2float(__ushort_as_half(srb1[jg0]));
-                                          const float z_a = meta_zero(zwa1, jg0), z_b = meta_zero(zwb1, jg0);
-                                          const float2 ex = *reinterpret_cast<const float2*>(
-                                              base + (ex_m1 - sbase) + (uint32_t)(blk * 8 * 8));
-                                          acc_a = fmaf(s_a, va_ - fmaf(z_a, ex.y, ex.x), acc_a);
-                                          acc_b = fmaf(s_b, vb_ - fmaf(z_b, ex.y, ex.x), acc_b);
-                                      } else {
-                                          // scales of the block's H groups (consecutive halves) and their zero
-                                          // points; groups past the row end (last, partial chunk of one
-                                          // segment) get scale 0
-                                          float sa[H], sb[H], za[H], zb[H];
-                                          const uint32_t zwa = zra[(gia + jg0) >> 3] >> (4 * ((gia + jg0) & 7));
-                                          const uint32_t zwb = zrb[(gib + jg0) >> 3] >> (4 * ((gib + jg0) & 7));
+                                      const float4 ex = lds_f4(exlane + (uint32_t)((blk * 8 * NB + nb * 8) * 8));
 #pragma unroll
-                                          for (int hh = 0; hh < H; ++hh) {
-                                              const bool va_ = gia + jg0 + hh < p.ng, vb_ = gib + jg0 + hh < p.ng;
-                                              sa[hh] = va_ ? __half2float(__ushort_as_half(sra[jg0 + hh])) : 0.0f;
-                                              sb[hh] = vb_ ? __half2float(__ushort_as_half(srb[jg0 + hh])) : 0.0f;
-                                              za[hh] = meta_zero(zwa, hh);
-                                              zb[hh] = meta_zero(zwb, hh);
-                                          }
+                                      for (int e = 0; e < 2; ++e) {
+                                          float s_a = sa[0], s_b = sb[0], z_a = za[0], z_b = zb[0];
 #pragma unroll
-                                          for (int nb = 0; nb < NB; ++nb) {
-                                              const float4 ex = lds_f4(exlane + (uint32_t)((blk * 8 * NB + nb * 8) * 8));
-#pragma unroll
-                                              for (int e = 0; e < 2; ++e) {
-                                                  float s_a = sa[0], s_b = sb[0], z_a = za[0], z_b = zb[0];
-#pragma unroll
-                                                  for (int hh = 1; hh < H; ++hh)
-                                                      if (hc[nb][e] == hh) {
-                                                          s_a = sa[hh]; s_b = sb[hh]; z_a = za[hh]; z_b = zb[hh];
-                                                      }
-                                                  const float E = e ? ex.z : ex.x, X = e ? ex.w : ex.y;
-                                                  acc[nb][e] =
-                                                      fmaf(s_a, (da[nb][e] + db[nb][e]) - fmaf(z_a, X, E), acc[nb][e]);
-                                                  acc[nb][2 + e] = fmaf(s_b, (da[nb][2 + e] + db[nb][2 + e]) -
-                                                                                 fmaf(z_b, X, E), acc[nb][2 + e]);
+                                          for (int hh = 1; hh < H; ++hh)
+                                              if (hc[nb][e] == hh) {
+                                                  s_a = sa[hh]; s_b = sb[hh]; z_a = za[hh]; z_b = zb[hh];
                                               }
-                                          }
+                                          const float E = e ? ex.z : ex.x, X = e ? ex.w : ex.y;
+                                          acc[nb][e] =
+                                              fmaf(s_a, (da[nb][e] + db[nb][e]) - fmaf(z_a, X, E), acc[nb][e]);
+                                          acc[nb][2 + e] = fmaf(s_b, (da[nb][2 + e] + db[nb][2 + e]) -
+                                                                         fmaf(z_b, X, E), acc[nb][2 + e]);
                                       }
                                   }
                               }
                           }
+                      }
+                  }
+                }
+                // tile finished in this warp's run: reduce the diagonal over segments and parities
+                const int n = two ? 2 : 1;
+                if (cu + n == p.C || ch + n == ch1) {
+                    if constexpr (M1) {
+                        // red[vrow][parity]: written by the one lane holding each useful sum
+                        if (useful) {
+                            red[va * H + h_use] = acc_a;
+                            red[vb * H + h_use] = acc_b;
                         }
-                        // tile finished in this warp's run: reduce the diagonal over segments and parities
-                        if (c2 == p.C2 - 1 || u == u1 - 1) {
-                            if constexpr (M1) {
-                                // red[vrow][parity]: written by the one lane holding each useful sum
-                                if (useful) {
-                                    red[va * H + h_use] = acc_a;
-                                    red[vb * H + h_use] = acc_b;
-                                }
-                                acc_a = acc_b = 0.0f;
-                                __syncwarp();
-                                const int slotp = (tl * p.C2 < u0) ? first_slot : 0;
-                                if (lane < p.R) {
-                                    float sum = 0.0f;
-                                    for (int q = 0; q < p.P; ++q)
-#pragma unroll
-                                        for (int hh = 0; hh < H; ++hh) sum += red[(lane * p.P + q) * H + hh];
-                                    part[(tl * p.R + lane) * kSlots + slotp] = sum;
-                                }
-                                __syncwarp();
-                            } else {
-#pragma unroll
-                                for (int nb = 0; nb < NB; ++nb) {
-                                    red[va * 8 * NB + nb * 8 + 2 * t] = acc[nb][0];
-                                    red[va * 8 * NB + nb * 8 + 2 * t + 1] = acc[nb][1];
-                                    red[vb * 8 * NB + nb * 8 + 2 * t] = acc[nb][2];
-                                    red[vb * 8 * NB + nb * 8 + 2 * t + 1] = acc[nb][3];
-#pragma unroll
-                                    for (int e = 0; e < 4; ++e) acc[nb][e] = 0.0f;
-                                }
-                                __syncwarp();
-                                const int slotp = (tl * p.C2 < u0) ? first_slot : 0;
-                                for (int o = lane; o < p.R * p.M; o += 32) {   // R*M reaches 256
-                                    const int rho = o / p.M, m = o - rho * p.M;
-                                    float sum = 0.0f;
-                                    for (int q = 0; q < p.P; ++q)
-#pragma unroll
-                                        for (int hh = 0; hh < H; ++hh)
-                                            sum += red[(rho * p.P + q) * 8 * NB + (q * H + hh) * p.M + m];
-                                    part[((tl * p.R + rho) * p.M + m) * kSlots + slotp] = sum;
-                                }
-                                __syncwarp();
-                            }
-                        }
-                        // this slot is read: refill it with the unit nsl ahead
+                        acc_a = acc_b = 0.0f;
                         __syncwarp();
-                        if (lane == 0 && it_u < u1) {
-                            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                            issue_next();
+                        const int slotp = (tl * p.C < ch0) ? first_slot : 0;
+                        if (lane < p.R) {
+                            float sum = 0.0f;
+                            for (int q = 0; q < p.P; ++q)
+#pragma unroll
+                                for (int hh = 0; hh < H; ++hh) sum += red[(lane * p.P + q) * H + hh];
+                            part[(tl * p.R + lane) * kSlots + slotp] = sum;
                         }
-                        if (++c2 == p.C2) {
-                            c2 = 0;
-                            ++tl;
+                        __syncwarp();
+                    } else {
+#pragma unroll
+                        for (int nb = 0; nb < NB; ++nb) {
+                            red[va * 8 * NB + nb * 8 + 2 * t] = acc[nb][0];
+                            red[va * 8 * NB + nb * 8 + 2 * t + 1] = acc[nb][1];
+                            red[vb * 8 * NB + nb * 8 + 2 * t] = acc[nb][2];
+                            red[vb * 8 * NB + nb * 8 + 2 * t + 1] = acc[nb][3];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) acc[nb][e] = 0.0f;
                         }
+                        __syncwarp();
+                        const int slotp = (tl * p.C < ch0) ? first_slot : 0;
+                        for (int o = lane; o < p.R * p.M; o += 32) {   // R*M reaches 256
+                            const int rho = o / p.M, m = o - rho * p.M;
+                            float sum = 0.0f;
+                            for (int q = 0; q < p.P; ++q)
+#pragma unroll
+                                for (int hh = 0; hh < H; ++hh)
+                                    sum += red[(rho * p.P + q) * 8 * NB + (q * H + hh) * p.M + m];
+                            part[((tl * p.R + rho) * p.M + m) * kSlots + slotp] = sum;
+                        }
+                        __syncwarp();
                     }
+                }
+                // this slot is read: refill it with the unit nsl ahead
+                __syncwarp();
+                if (lane == 0 && it_ch < ch1) {
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    issue_next();
+                }
+                ch += n;
+                cu += n;
+                if (cu == p.C) {
+                    cu = 0;
+                    ++tl;
                 }
             }
         }
         if (!ok && lane == 0) {   // wait for this warp's ring copies still in flight
-            for (int uu = it_u - nsl; uu < it_u; ++uu) {
-                if (uu < u0) continue;
-                const uint32_t bar = bar0 + 8u * (uint32_t)((uu - u0) & (nsl - 1));
+            for (int kk = it_n - nsl; kk < it_n; ++kk) {
+                if (kk < 0) continue;
+                const uint32_t bar = bar0 + 8u * (uint32_t)(kk & (nsl - 1));
                 const long long t0 = clock64();
-                while (!tc::mbar_try_wait(bar, (uint32_t)(((uu - u0) >> lg) & 1))) {
+                while (!tc::mbar_try_wait(bar, (uint32_t)((kk >> lg) & 1))) {
                     if (clock64() - t0 > kSpinCycles) {
                         atomicOr(&g_gemv_status, kStatusGemvDrain);
                         break;
@@ -809,7 +809,6 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int G, int nmat, int sms, size_t
     pl.nb = M > 8 ? 2 : 1;
     p.C = (int)((K / p.P + 255) / 256);
     p.Ks = p.C * 256;                           // equals K / P whenever P > 1
-    p.C2 = (p.C + 1) / 2;
     p.ng = (int)(K / G);
     p.ngs = p.Ks / G;
     p.lds = (int)scales_ld(K, G);
@@ -818,7 +817,7 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int G, int nmat, int sms, size_t
     p.total_tiles = p.tiles_per_mat * nmat;
     pl.grid = p.total_tiles < sms ? p.total_tiles : sms;
     const int tmin = p.total_tiles / pl.grid, tmax = (p.total_tiles + pl.grid - 1) / pl.grid;
-    if ((long long)tmax * p.C2 >= (1ll << 26)) return false;
+    if ((long long)tmax * p.C >= (1ll << 26)) return false;
     if ((long long)p.total_tiles * pl.grid >= (1ll << 32)) return false;
     p.rows_cap = tmax * p.R;
     // CTA warps (the instance's launch bound, or fewer when shared memory is short), then the
@@ -828,10 +827,10 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int G, int nmat, int sms, size_t
         // warps taking units: as many as keep every tile within kSlots consecutive warps
         p.warps = 1;
         for (int w = nw; w >= 1; --w) {
-            const long long units = (long long)tmin * p.C2;
-            const long long per = units / w;
+            const long long chunks = (long long)tmin * p.C;
+            const long long per = chunks / w;
             if (per < 1) continue;
-            const long long span = (p.C2 + per - 1) / per + 1;
+            const long long span = (p.C + per - 1) / per + 1;
             if (span <= kSlots) {
                 p.warps = w;
                 break;
