@@ -91,15 +91,20 @@ struct Layout {
 
 __host__ __device__ inline uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
+// M = 1 with P >= 2 segments: the specialised kernel (its B columns are (parity, segment)
+// pairs and it keeps one useful value per row; see gemv_kernel).
+__host__ __device__ inline bool m1_kernel(const GemvParams& p) { return p.M == 1 && p.P >= 2; }
+
 __host__ __device__ inline Layout make_layout(const GemvParams& p, int nb, int H) {
+    const bool m1 = m1_kernel(p);
     Layout L;
     uint32_t off = 0;
     L.ring = off;
     off += (uint32_t)(p.nw * p.nst * kUnitBytes);
     L.xs = off;
     off += align_up((uint32_t)p.xcols * (uint32_t)p.Ks * 2u, 16);        // xcols x Ks FP16 (whole chunks)
-    L.zero = off;
-    off += 16;
+    L.zero = off;                                         // zeros read by idle B columns: one 16-byte
+    off += m1 ? 8u * (uint32_t)p.xcols * 64u : 16u;        // block, or (M = 1) a chunk's 8 word steps of x
     L.exs = off;
     off += align_up((uint32_t)(p.ngs / H) * 8u * (uint32_t)nb * 8u, 16);
     L.ms = off;
@@ -109,7 +114,7 @@ __host__ __device__ inline Layout make_layout(const GemvParams& p, int nb, int H
     L.part = off;
     off += align_up((uint32_t)p.rows_cap * (uint32_t)p.M * kSlots * 4u, 16);
     L.red = off;
-    off += (uint32_t)p.nw * 16u * 8u * (uint32_t)nb * 4u;
+    off += (uint32_t)p.nw * 16u * (m1 ? (uint32_t)H : 8u * (uint32_t)nb) * 4u;
     L.bars = off;
     off += (uint32_t)p.nw * (uint32_t)p.nst * 8u + 8u;    // ring barriers, then the prologue copies' barrier
     L.total = off;
@@ -193,7 +198,7 @@ __device__ __forceinline__ bool gemv_wait(uint32_t bar, uint32_t parity) {
 // M1: one activation row with P >= 2 segments.  The B columns are then
 // (parity, segment) pairs and each lane holds at most one useful D value per
 // row, so the block-end correction is done once per row on that value only.
-template <int NB, int G, int H, bool M1>
+template <int NB, int G, int H, bool M1, int PT>
 __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
     gemv_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
                 const GemvParams p) {
@@ -201,6 +206,8 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
     constexpr int GPC = 256 / G;                  // groups per chunk (H divides it)
     constexpr int WSG = G / 32;                   // word steps per group
     const int kWarps = p.nw;                      // warps launched (at most the launch bound)
+    const int P = PT > 0 ? PT : p.P;            // segments per row (a template constant at M = 1)
+    const int R = 16 / P;                         // weight rows per tile
     const int kThreads = kWarps * 32;
     static_assert(GPC % H == 0, "a block of H groups lies inside one chunk");
     extern __shared__ uint8_t smem_raw[];
@@ -278,12 +285,12 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
         // and the gap between the parts are not copied but zero-filled
         const int tpm = p.tiles_per_mat;
         const bool has0 = tile0 < tpm;
-        const int r0 = has0 ? tile0 * p.R : 0;                                  // first row, matrix 0 part
-        const int n0 = !has0 ? 0 : tile1 <= tpm ? tc_ * p.R : (tpm - tile0) * p.R;
-        const int l1 = has0 ? (tpm - tile0) * p.R : 0;                        // local row of matrix 1
+        const int r0 = has0 ? tile0 * R : 0;                                  // first row, matrix 0 part
+        const int n0 = !has0 ? 0 : tile1 <= tpm ? tc_ * R : (tpm - tile0) * R;
+        const int l1 = has0 ? (tpm - tile0) * R : 0;                        // local row of matrix 1
         const int t1a = has0 ? tpm : tile0;
-        const int r1 = (t1a - tpm) * p.R;                                      // first row, matrix 1 part
-        const int n1 = tile1 > tpm ? (tile1 - t1a) * p.R : 0;
+        const int r1 = (t1a - tpm) * R;                                      // first row, matrix 1 part
+        const int n1 = tile1 > tpm ? (tile1 - t1a) * R : 0;
         const int c0 = max(0, min(n0, p.N - r0)), c1 = max(0, min(n1, p.N - r1));   // rows copied
         const uint32_t sbytes = (uint32_t)p.lds * 2u, zbytes = (uint32_t)p.ldz * 4u;   // per row
         const uint32_t ms = sbase + L.ms, mz = sbase + L.mz;
@@ -307,7 +314,7 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
         const int xcols = p.xcols, M = p.M, C = p.C;
         uint4* xs = reinterpret_cast<uint4*>(base + L.xs);
         float2* exs = reinterpret_cast<float2*>(base + L.exs);
-        const int kseg = p.K / p.P;                        // real codes per segment
+        const int kseg = p.K / P;                        // real codes per segment
         constexpr int GW = G / 8;                          // words per group
         constexpr int XB = 8;                              // items per batch
         const int dxc = kWarps / C, dc = kWarps - dxc * C;                 // item step as (column, block)
@@ -376,7 +383,7 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
                                *reinterpret_cast<const uint32_t*>(&hp[2]), *reinterpret_cast<const uint32_t*>(&hp[3]));
                 if ((lane & (GW - 1)) == 0) {
                     const int gam = wseg / GW;                 // group in the segment
-                    const int col = M1 ? (gam % H) * p.P + pseg : ((pseg * H) + (gam % H)) * M + m;
+                    const int col = M1 ? (gam % H) * P + pseg : ((pseg * H) + (gam % H)) * M + m;
                     exs[(gam / H) * (8 * NB) + col] = make_float2(e, xsum);
                 }
             }
@@ -403,7 +410,8 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
             const int b = i / (8 * NB - p.cols), col = p.cols + i % (8 * NB - p.cols);
             exs[b * (8 * NB) + col] = make_float2(0.0f, 0.0f);
         }
-        if (tid == 0) *reinterpret_cast<uint4*>(base + L.zero) = make_uint4(0u, 0u, 0u, 0u);
+        for (uint32_t i = tid; i < (M1 ? 8u * (uint32_t)P * 64u : 16u) / 16u; i += kThreads)
+            reinterpret_cast<uint4*>(base + L.zero)[i] = make_uint4(0u, 0u, 0u, 0u);
         float* part = reinterpret_cast<float*>(base + L.part);
         for (int i = tid; i < p.rows_cap * p.M * kSlots; i += kThreads) part[i] = 0.0f;
 
@@ -425,9 +433,9 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
     bool ok = pro_ok;
     if (active) {
         const int va = sigma8(g), vb = va + 8, v7 = va & 7;
-        const int rho_a = va / p.P, pa = va - rho_a * p.P;
-        const int rho_b = vb / p.P, pb = vb - rho_b * p.P;
-        float* red = reinterpret_cast<float*>(base + L.red) + warp * 16 * 8 * NB;
+        const int rho_a = va / P, pa = va - rho_a * P;
+        const int rho_b = vb / P, pb = vb - rho_b * P;
+        float* red = reinterpret_cast<float*>(base + L.red) + warp * 16 * (M1 ? H : 8 * NB);
         float* part = reinterpret_cast<float*>(base + L.part);
         uint32_t coff[8 / V];                              // byte offset of this lane's words in a 128-byte row
 #pragma unroll
@@ -436,7 +444,7 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
             coff[bq] = ((uint32_t)((wf >> 2) ^ v7) << 4) + (uint32_t)(wf & 3) * 4u;
         }
         // B column of this lane per column block: (segment, group parity, activation row)
-        const uint32_t xstep = (uint32_t)p.xcols * 64u;    // bytes of staged x per word step
+        const uint32_t xstep = (uint32_t)(M1 ? P : p.xcols) * 64u;   // bytes of staged x per word step
         const uint32_t zaddr = sbase + L.zero;
         uint32_t xl[NB];                                    // lane's staged column (bytes, without the step)
         int lh[NB];                                         // its group parity; -1 = idle column
@@ -447,8 +455,8 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
                 int m, hh, ps;
                 if constexpr (M1) {
                     m = 0;
-                    hh = j / p.P;
-                    ps = j - hh * p.P;
+                    hh = j / P;
+                    ps = j - hh * P;
                 } else {
                     m = j % p.M;
                     const int ph = j / p.M;
@@ -474,10 +482,10 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
         const uint32_t exlane = sbase + L.exs + (uint32_t)(2 * t * 8);
         // M1: this lane's D columns 2t, 2t+1 are segments p0, p0+1 of parity h_use; it holds the
         // useful value of its rows (segment pa) when pa is one of them, in column e_use
-        const int p0 = (2 * t) % p.P, h_use = (2 * t) / p.P;
+        const int p0 = (2 * t) % P, h_use = (2 * t) / P;
         const int e_use = pa - p0;
         const bool useful = M1 && (unsigned)e_use < 2u && 2 * t < p.cols;   // columns past P*H are idle
-        const uint32_t ex_m1 = sbase + L.exs + (uint32_t)((h_use * p.P + pa) * 8);
+        const uint32_t ex_m1 = sbase + L.exs + (uint32_t)((h_use * P + pa) * 8);
 
         // slot of the first tile of the run: warps before this one that hold chunks of it
         int first_slot = 0;
@@ -512,7 +520,7 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
                 for (int cc = 0; cc < 2; ++cc) {
                   if (cc == 1 && !two) break;                 // one-chunk unit (uniform)
                   const int c = cu + cc;                      // chunk in the tile
-                  const int rla = tl * p.R + rho_a, rlb = tl * p.R + rho_b;   // local rows
+                  const int rla = tl * R + rho_a, rlb = tl * R + rho_b;   // local rows
                   const unsigned short* sra = smtab + rla * p.lds + pa * p.ngs + c * GPC;
                   const unsigned short* srb = smtab + rlb * p.lds + pb * p.ngs + c * GPC;
                   const uint32_t* zra = zmtab + rla * p.ldz;
@@ -529,7 +537,9 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
                   const uint32_t unit = ring + slot * (uint32_t)kUnitBytes + (uint32_t)cc * kBoxBytes;
                   const uint32_t row_a = unit + (uint32_t)va * 128u, row_b = row_a + 8u * 128u;
                   const uint32_t xu = (uint32_t)(c * 8) * xstep;
-                  // per group parity: x base and step of this lane (idle lanes read zeros)
+                  // per group parity: x base and step of this lane (idle lanes read zeros; at M = 1
+                  // from a zero area as long as a chunk's x, so every lane steps by the same
+                  // compile-time stride and the loads below take immediate offsets)
                   uint32_t xb[NB][H], xsp[NB][H];
 #pragma unroll
                   for (int nb = 0; nb < NB; ++nb)
@@ -537,7 +547,7 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
                       for (int hh = 0; hh < H; ++hh) {
                           const bool on = lh[nb] == hh;
                           xb[nb][hh] = on ? xl[nb] + xu : zaddr;
-                          xsp[nb][hh] = on ? xstep : 0u;
+                          xsp[nb][hh] = (M1 || on) ? xstep : 0u;
                       }
                   float da[NB][4], db[NB][4];
 #pragma unroll
@@ -646,12 +656,12 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
                         acc_a = acc_b = 0.0f;
                         __syncwarp();
                         const int slotp = (tl * p.C < ch0) ? first_slot : 0;
-                        if (lane < p.R) {
+                        if (lane < R) {
                             float sum = 0.0f;
-                            for (int q = 0; q < p.P; ++q)
+                            for (int q = 0; q < P; ++q)
 #pragma unroll
-                                for (int hh = 0; hh < H; ++hh) sum += red[(lane * p.P + q) * H + hh];
-                            part[(tl * p.R + lane) * kSlots + slotp] = sum;
+                                for (int hh = 0; hh < H; ++hh) sum += red[(lane * P + q) * H + hh];
+                            part[(tl * R + lane) * kSlots + slotp] = sum;
                         }
                         __syncwarp();
                     } else {
@@ -666,14 +676,14 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
                         }
                         __syncwarp();
                         const int slotp = (tl * p.C < ch0) ? first_slot : 0;
-                        for (int o = lane; o < p.R * p.M; o += 32) {   // R*M reaches 256
+                        for (int o = lane; o < R * p.M; o += 32) {   // R*M reaches 256
                             const int rho = o / p.M, m = o - rho * p.M;
                             float sum = 0.0f;
-                            for (int q = 0; q < p.P; ++q)
+                            for (int q = 0; q < P; ++q)
 #pragma unroll
                                 for (int hh = 0; hh < H; ++hh)
-                                    sum += red[(rho * p.P + q) * 8 * NB + (q * H + hh) * p.M + m];
-                            part[((tl * p.R + rho) * p.M + m) * kSlots + slotp] = sum;
+                                    sum += red[(rho * P + q) * 8 * NB + (q * H + hh) * p.M + m];
+                            part[((tl * R + rho) * p.M + m) * kSlots + slotp] = sum;
                         }
                         __syncwarp();
                     }
@@ -720,13 +730,13 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
     // ---- combine the slots in a fixed order and store ------------------------------
     {
         const float* part = reinterpret_cast<const float*>(base + L.part);
-        const int nout = tc_ * p.R * p.M;
+        const int nout = tc_ * R * p.M;
         for (int i = tid; i < nout; i += kThreads) {
             const int rl = i / p.M, m = i - rl * p.M;
-            const int tl2 = rl / p.R, rho = rl - tl2 * p.R;
+            const int tl2 = rl / R, rho = rl - tl2 * R;
             const int tau = tile0 + tl2;
             const int mat = tau >= p.tiles_per_mat;
-            const int row = (mat ? tau - p.tiles_per_mat : tau) * p.R + rho;
+            const int row = (mat ? tau - p.tiles_per_mat : tau) * R + rho;
             if (row >= p.N) continue;
             float sum = 0.0f;
 #pragma unroll
@@ -845,7 +855,7 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int G, int nmat, int sms, size_t
     return false;
 }
 
-template <int NB, int G, int H, bool M1>
+template <int NB, int G, int H, bool M1, int PT>
 cudaError_t launch_m(const CUtensorMap& tm0, const CUtensorMap& tm1, const Plan& pl, cudaStream_t stream) {
     static int cached[kMaxDevices] = {};
     int dev = 0;
@@ -853,7 +863,7 @@ cudaError_t launch_m(const CUtensorMap& tm0, const CUtensorMap& tm1, const Plan&
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     if ((int)pl.smem > cached[dev]) {
-        e = cudaFuncSetAttribute(gemv_kernel<NB, G, H, M1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(gemv_kernel<NB, G, H, M1, PT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)pl.smem);
         if (e != cudaSuccess) return e;
         cached[dev] = (int)pl.smem;
@@ -869,15 +879,22 @@ cudaError_t launch_m(const CUtensorMap& tm0, const CUtensorMap& tm1, const Plan&
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<NB, G, H, M1>, tm0, tm1, pl.p);
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<NB, G, H, M1, PT>, tm0, tm1, pl.p);
 }
 
 template <int NB, int G, int H>
 cudaError_t launch_t(const CUtensorMap& tm0, const CUtensorMap& tm1, const Plan& pl, cudaStream_t stream) {
     if constexpr (NB == 1) {
-        if (pl.p.M == 1 && pl.p.P >= 2) return launch_m<NB, G, H, true>(tm0, tm1, pl, stream);
+        if (m1_kernel(pl.p)) {                       // M = 1: the segment count is a template constant
+            switch (pl.p.P) {
+                case 2: return launch_m<NB, G, H, true, 2>(tm0, tm1, pl, stream);
+                case 4: return launch_m<NB, G, H, true, 4>(tm0, tm1, pl, stream);
+                case 8: return launch_m<NB, G, H, true, 8>(tm0, tm1, pl, stream);
+            }
+            return cudaErrorInvalidValue;
+        }
     }
-    return launch_m<NB, G, H, false>(tm0, tm1, pl, stream);
+    return launch_m<NB, G, H, false, 0>(tm0, tm1, pl, stream);
 }
 
 template <int NB, int G>
