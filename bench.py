@@ -421,6 +421,140 @@ def run_profile(args):
                       "calls": args.warmup + 2}))
 
 
+# ---------------------------------------------------------------------------
+# per-config sweep (the other workloads; not the bench line)
+# ---------------------------------------------------------------------------
+
+def _graph_us(launch, n, replays=5):
+    """Median over `replays` of the per-launch time of a CUDA graph holding `n`
+    launches (launch(i, stream) issues launch i); one untimed replay first."""
+    torch.cuda.synchronize()
+    for i in range(3):                                  # eager warm-up
+        launch(i, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    with torch.cuda.graph(gr, stream=cap):
+        for i in range(n):
+            launch(i, torch.cuda.current_stream())
+    gr.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ts = []
+    for _ in range(replays):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        gr.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e3 / n)
+    del gr
+    return statistics.median(ts)
+
+
+def run_sweep(args):
+    """Decode and small-batch timings of every workload in workloads.py other
+    than the bench's own: one JSON line per (workload, matrix, M, G, path) and
+    a crossover summary per G for the batch sweep.  Each figure is the median
+    of 5 replays of a CUDA graph of `steps` back-to-back launches over enough
+    rotating weight copies that more than 2x L2 streams between two reads of a
+    copy.  The tensor-core path runs through its allocation-free entry point so
+    that it can be captured in a graph like the GEMV."""
+    import w4a16_weight_only_linear_b300 as w4
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    pk = peaks()
+    n = args.steps
+    l2_bytes = 126 * 2 ** 20
+
+    def packed_copies(wk, j, lin, Gv):
+        w = wl.weight_f16(lin.N, lin.K, wk.sigma, wl.matrix_seed(wk, j), wk.outlier_frac).to(dev)
+        one = gemv_bytes(1, lin.N, lin.K, Gv)
+        copies = max(2, -(-2 * l2_bytes // one) + 1)
+        out = [w4.w4a16_pack(w, Gv) for _ in range(copies)]
+        del w
+        return out
+
+    def emit(rec):
+        print(json.dumps(rec), flush=True)
+        return rec
+
+    def record(wk, lin, M, Gv, path, us, nmat=1):
+        byts = nmat * gemv_bytes(M, lin.N, lin.K, Gv) - (nmat - 1) * M * lin.K * 2   # x read once
+        fl = nmat * gemm_flops(M, lin.N, lin.K)
+        return emit({"sweep": wk.name, "matrix": lin.name if nmat == 1 else "gate+up", "M": M, "N": lin.N,
+                     "K": lin.K, "G": Gv, "path": path, "us": round(us, 2),
+                     "gbs": round(byts / (us * 1e-6) / 1e9, 1), "frac_hbm": round(byts / (us * 1e-6) / 1e9 / pk["hbm_gbs"], 4),
+                     "tflops": round(fl / (us * 1e-6) / 1e12, 2),
+                     "frac_tensor": round(fl / (us * 1e-6) / 1e12 / pk["bf16_tflops"], 4)})
+
+    results = []
+    for name in ("single_4096", "layer13b_decode", "up13b_sweep", "gateup13b_dual"):
+        wk = wl.WORKLOADS[name]
+        if wk.dual:
+            for Gv in wk.Gs:
+                gate = packed_copies(wk, 0, wk.linears[0], Gv)
+                up = packed_copies(wk, 1, wk.linears[1], Gv)
+                nc = min(len(gate), len(up))
+                for M in wk.Ms:
+                    lin = wk.linears[0]
+                    x = wl.activations_bf16(M, lin.K, wl.act_seed(wk, 0)).to(dev)
+                    yg = torch.empty(M, lin.N, dtype=torch.bfloat16, device=dev)
+                    yu = torch.empty(M, lin.N, dtype=torch.bfloat16, device=dev)
+                    us = _graph_us(lambda i, s: w4.w4a16_linear_dual(x, gate[i % nc], up[i % nc], Gv, out=(yg, yu),
+                                                                      stream=s), n)
+                    results.append(record(wk, lin, M, Gv, "dual", us, nmat=2))
+                del gate, up
+            continue
+        for j, lin in enumerate(wk.linears):
+            for Gv in wk.Gs:
+                cps = packed_copies(wk, j, lin, Gv)
+                for M in wk.Ms:
+                    x = wl.activations_bf16(M, lin.K, wl.act_seed(wk, j)).to(dev)
+                    y = torch.empty(M, lin.N, dtype=torch.bfloat16, device=dev)
+                    paths = []
+                    if w4.w4a16_linear_path(M, lin.N, lin.K, Gv) == 1 or M <= 16:
+                        paths.append(("gemv", w4.w4a16_linear_gemv))
+                    if name == "up13b_sweep" and M * lin.K <= w4.NOALLOC_MAX_X_ELEMS:
+                        paths.append(("gemm", w4.w4a16_linear_gemm_noalloc))
+                    for pname, fn in paths:
+                        try:
+                            us = _graph_us(lambda i, s: fn(x, *cps[i % len(cps)], Gv, out=y, stream=s), n)
+                        except w4.W4A16Error:
+                            continue
+                        results.append(record(wk, lin, M, Gv, pname, us))
+                del cps
+    assert w4.w4a16_device_status() == 0
+
+    # crossover on the batch sweep, per G: the smallest M at which the tensor-core path is
+    # faster than the GEMV, and M* = the smallest M whose best achieved FLOP/s reaches 50 % of
+    # the tensor peak, or where the GEMV's weight GB/s drops below 90 % of its M = 1 value,
+    # whichever comes first
+    cross = {}
+    sw = [r for r in results if r["sweep"] == "up13b_sweep"]
+    for Gv in sorted({r["G"] for r in sw}):
+        rs = [r for r in sw if r["G"] == Gv]
+        Ms = sorted({r["M"] for r in rs})
+        t = {(r["M"], r["path"]): r for r in rs}
+        faster = next((M for M in Ms if (M, "gemm") in t and ((M, "gemv") not in t or
+                                                               t[(M, "gemm")]["us"] < t[(M, "gemv")]["us"])), None)
+        gv1 = t.get((1, "gemv"), {}).get("gbs")
+        drop = next((M for M in Ms if (M, "gemv") in t and gv1 and t[(M, "gemv")]["gbs"] < 0.9 * gv1), None)
+        # "50 % of the tensor roofline" read as half the dense tensor peak (the HBM-bound roofline
+        # of a small M is met by the GEMV at M = 1 already)
+        reach = None
+        for M in Ms:
+            best = min((t[(M, pth)] for pth in ("gemv", "gemm") if (M, pth) in t), key=lambda r: r["us"])
+            if best["tflops"] >= 0.5 * pk["bf16_tflops"]:
+                reach = M
+                break
+        rule = min([m for m in (reach, drop) if m is not None], default=None)
+        cross[str(Gv)] = {"gemm_faster_from_M": faster, "gemv_below_90pct_from_M": drop, "M_star": rule,
+                          "dispatch_gemv_up_to_M": max([M for M in Ms if w4.w4a16_linear_path(M, 13824, 5120, Gv) == 1],
+                                                       default=None)}
+    emit({"crossover": cross, "note": "pages: 16 to 32"})
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--profile", choices=["decode", "prefill"], default=None,
@@ -430,11 +564,15 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--sweep", action="store_true",
+                    help="time the other workloads (decode layers, batch x group sweep, dual) instead")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.profile:
         run_profile(args)
+    elif args.sweep:
+        run_sweep(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

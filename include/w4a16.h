@@ -118,9 +118,10 @@ W4A16_API w4a16_status w4a16_dequant(const uint32_t* qweight, const void* scales
 
 /* ---- the layer ---------------------------------------------------------------
  * w4a16_linear: y[M,N] (BF16) = x[M,K] (BF16) * W_hat^T, FP32 accumulation,
- * one round-to-nearest-even to BF16 per output.  Dispatch: M <= 16 runs the
+ * one round-to-nearest-even to BF16 per output.  Dispatch: M <= 8 runs the
  * bandwidth-bound decode GEMV (when x of M rows fits the kernel's shared
- * memory), anything else runs the tcgen05 tensor-core GEMM.  Decode is
+ * memory), anything else runs the tcgen05 tensor-core GEMM (measured: on a
+ * 5120 -> 13824 layer the GEMM is already the faster kernel at M = 16).  Decode is
  * weight-bandwidth bound and prefill compute bound (klaylearn glossary, FAQ
  * "Why is it especially useful for decode?"; multigrid.ai, section "Where it
  * stops being the right answer").
@@ -136,7 +137,7 @@ W4A16_API w4a16_status w4a16_linear(const void* x_bf16, const uint32_t* qweight,
  *   y_gate = x * W_hat_gate^T,  y_up = x * W_hat_up^T.
  * Both weights share K, N and G.  Paired gate/up traversal is the zhuai.tech
  * page's section 2 ("Moving fewer bytes can make decode faster") workload.
- * M <= 16 runs the dual GEMV; larger M runs the GEMM once per projection.
+ * M <= 8 runs the dual GEMV; larger M runs the GEMM once per projection.
  */
 W4A16_API w4a16_status w4a16_linear_dual(const void* x_bf16,
                                const uint32_t* qweight_gate, const void* scales_gate,

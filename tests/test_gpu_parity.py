@@ -88,7 +88,7 @@ def test_gemv_parity(M, N, K, G):
     assert_close(y, y_ref, f"gemv M={M} N={N} K={K} G={G}")
 
 
-@pytest.mark.parametrize("M", [1, 4, 16])
+@pytest.mark.parametrize("M", [1, 4, 8])
 def test_linear_dispatches_to_gemv(M):
     N, K, G = 264, 1024, 128
     assert w4.w4a16_linear_path(M, N, K, G) == 1
@@ -160,10 +160,13 @@ def test_dual_parity(M, N, K, G):
     torch.cuda.synchronize()
     assert_close(yg, yg_ref, "dual gate")
     assert_close(yu, yu_ref, "dual up")
-    # The dual call splits the concatenated tiles of both matrices over the
-    # SMs, so a tile's partial sums may be added in a different order than in
-    # a single-matrix call: the two agree to within one BF16 ulp.
-    for y2, y1 in ((yg, w4.w4a16_linear_gemv(xd, *dg, G)), (yu, w4.w4a16_linear_gemv(xd, *du, G))):
+    # Against the single-matrix call that dispatches the same way (the decode
+    # GEMV up to M = 8, the tensor-core GEMM above): the dual GEMV splits the
+    # concatenated tiles of both matrices over the SMs, so a tile's partial
+    # sums may be added in a different order than in a single-matrix call, and
+    # the two agree to within one BF16 ulp.
+    assert w4.w4a16_linear_path(M, N, K, G) == (1 if M <= 8 else 2)
+    for y2, y1 in ((yg, w4.w4a16_linear(xd, *dg, G)), (yu, w4.w4a16_linear(xd, *du, G))):
         a, b = y2.double().cpu().numpy(), y1.double().cpu().numpy()
         ulp = bf16_ulp(np.maximum(np.abs(a), np.abs(b)))
         assert np.all(np.abs(a - b) <= ulp)

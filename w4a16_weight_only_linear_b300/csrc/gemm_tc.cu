@@ -1,5 +1,5 @@
 // gemm_tc.cu -- prefill path of the W4A16 linear layer on the tcgen05 tensor
-// cores (any M; the library routes M > 16 here).
+// cores (any M; the library routes M > 8 here).
 //
 // At prefill many activation rows share each weight, so the layer is a dense
 // contraction bound by tensor-core throughput; the dequantisation is extra
