@@ -45,6 +45,8 @@ def _load():
         lib.oracle_linear.restype = None
         lib.oracle_linear_sampled.argtypes = [p, p, p, p, i64, i64, p, p, i64, p, i32]
         lib.oracle_linear_sampled.restype = None
+        lib.oracle_linear_xs.argtypes = [p, p, p, p, p, i64, i64, i64, i64, p, i32]
+        lib.oracle_linear_xs.restype = None
         lib.oracle_max_threads.argtypes, lib.oracle_max_threads.restype = [], i32
         _lib = lib
     return _lib
@@ -191,6 +193,23 @@ def linear_sampled(x_bf16: np.ndarray, q, s, z, K: int, G: int, ms, ns, nthreads
     y = np.zeros(ms.shape[0], np.float64)
     _load().oracle_linear_sampled(_ptr(x), _ptr(q), _ptr(s), _ptr(z), K, G, _ptr(ms), _ptr(ns),
                                   ms.shape[0], _ptr(y), nthreads)
+    return y
+
+
+def linear_xs(x_bf16: np.ndarray, x_scale: np.ndarray, q, s, z, N: int, K: int, G: int,
+              nthreads: int = 0) -> np.ndarray:
+    """y_ref [M,N] FP64 = (x * x_scale) * W_hat^T, unrounded; x_scale FP32 [K]
+    multiplies input channel k (the activation-scaled layer)."""
+    x = _u16(x_bf16)
+    M = x.shape[0]
+    assert x.shape[1] == K
+    xs = np.ascontiguousarray(x_scale, dtype=np.float32)
+    assert xs.shape == (K,)
+    q = np.ascontiguousarray(q, dtype=np.uint32)
+    s = _u16(s)
+    z = np.ascontiguousarray(z, dtype=np.uint32)
+    y = np.zeros((M, N), np.float64)
+    _load().oracle_linear_xs(_ptr(x), _ptr(xs), _ptr(q), _ptr(s), _ptr(z), M, N, K, G, _ptr(y), nthreads)
     return y
 
 

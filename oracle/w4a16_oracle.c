@@ -328,6 +328,45 @@ void oracle_linear_sampled(const uint16_t* x_bf16, const uint32_t* qweight, cons
     (void)nthreads;
 }
 
+/*
+ * The layer with a per-input-channel activation scale, the deployed form of
+ * activation-aware weight quantisation: salient input channels have their
+ * weights scaled up before quantisation and the activations scaled down by
+ * the same factor, so the layer itself stays an ordinary groupwise INT4
+ * dequantise-then-multiply (instagit.com "Comparison of Quantization Methods:
+ * INT8 vs GPTQ vs AWQ vs GGUF", section "AWQ: Activation-Aware Weight
+ * Quantization"; klaylearn.com glossary, FAQ "What is the difference between
+ * AWQ and GPTQ?").  x_scale[k] is the factor applied to input channel k:
+ *   y_ref[m][n] = sum_k (double)x[m][k] * (double)x_scale[k] * (double)W_hat[n][k],
+ * accumulated in FP64 in increasing k and left unrounded.
+ */
+double oracle_linear_xs_one(const uint16_t* x_bf16, const float* x_scale, const uint32_t* qweight,
+                            const uint16_t* scales, const uint32_t* zeros, int64_t K, int64_t G, int64_t m,
+                            int64_t n)
+{
+    double acc = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        double xv = (double)oracle_bf16_to_f32(x_bf16[m * K + k]) * (double)x_scale[k];
+        double wv = (double)oracle_dequant_one(qweight, scales, zeros, K, G, n, k);
+        acc += xv * wv;
+    }
+    return acc;
+}
+
+void oracle_linear_xs(const uint16_t* x_bf16, const float* x_scale, const uint32_t* qweight,
+                      const uint16_t* scales, const uint32_t* zeros, int64_t M, int64_t N, int64_t K, int64_t G,
+                      double* y_out, int nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t m = 0; m < M; ++m)
+            y_out[m * N + n] = oracle_linear_xs_one(x_bf16, x_scale, qweight, scales, zeros, K, G, m, n);
+    (void)nthreads;
+}
+
 int oracle_max_threads(void)
 {
 #ifdef _OPENMP

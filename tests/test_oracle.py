@@ -304,6 +304,60 @@ def test_power_of_two_scaling_of_x():
         assert np.array_equal(yj, y0 * 2.0 ** j)
 
 
+# --------------------------------------------------------------------------
+# Activation-scaled layer (x_scale per input channel)
+# --------------------------------------------------------------------------
+
+def _bits(t):
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def test_act_scale_of_ones_is_the_plain_layer():
+    N, K, G = 16, 512, 128
+    q, s, z = _random_packed(N, K, G, 11)
+    xb = _bits(torch.randn(3, K, generator=torch.Generator().manual_seed(3)).to(torch.bfloat16))
+    y = oracle.linear_xs(xb, np.ones(K, np.float32), q, s, z, N, K, G)
+    assert np.array_equal(y, oracle.linear(xb, q, s, z, N, K, G))
+
+
+def test_act_scale_by_powers_of_two_equals_prescaled_x():
+    # x_k * 2^j_k is exact in BF16 for these values, so scaling inside the layer and
+    # scaling the input beforehand must give the same FP64 sums bit for bit
+    N, K, G = 16, 256, 64
+    q, s, z = _random_packed(N, K, G, 12)
+    x = torch.randn(2, K, generator=torch.Generator().manual_seed(4)).to(torch.bfloat16)
+    j = torch.randint(-4, 5, (K,), generator=torch.Generator().manual_seed(5)).float()
+    xs = (2.0 ** j).numpy().astype(np.float32)
+    pre = (x.float() * 2.0 ** j).to(torch.bfloat16)
+    assert torch.equal(pre.float(), x.float() * 2.0 ** j)
+    y = oracle.linear_xs(_bits(x), xs, q, s, z, N, K, G)
+    assert np.array_equal(y, oracle.linear(_bits(pre), q, s, z, N, K, G))
+
+
+@pytest.mark.parametrize("M,N,Kg,G", [(1, 8, 1, 32), (2, 16, 2, 32), (3, 8, 1, 64)])
+def test_act_scale_brute_force_rational(M, N, Kg, G):
+    # arbitrary FP32 channel factors (not powers of two, some negative, one zero):
+    # an index mix-up between channel k and column n or group g fails here
+    K = Kg * G
+    rng = np.random.default_rng(M * 7 + N + Kg)
+    w16 = (rng.standard_normal((N, K)) * 0.05).astype(np.float16)
+    x = _bits(torch.from_numpy(rng.standard_normal((M, K)).astype(np.float32)).to(torch.bfloat16))
+    xs = (rng.uniform(0.2, 3.0, K) * rng.choice([-1.0, 1.0], K)).astype(np.float32)
+    xs[K // 3] = 0.0
+    q, s, z = oracle.pack(w16, G)
+    y = oracle.linear_xs(x, xs, q, s, z, N, K, G)
+    for m in range(M):
+        for n in range(N):
+            acc = Fraction(0)
+            for k in range(K):
+                code = (int(q[n, k // 8]) >> (4 * (k % 8))) & 0xF
+                g = k // G
+                zero = (int(z[n, g // 8]) >> (4 * (g % 8))) & 0xF
+                acc += _frac_bf16(x[m, k]) * Fraction(float(xs[k])) * (code - zero) * _frac_f16(s[n, g])
+            ref = float(acc)
+            assert abs(y[m, n] - ref) <= 1e-12 * max(1.0, abs(ref)), (m, n, y[m, n], ref)
+
+
 def test_sampled_equals_full():
     N, K, G = 24, 512, 128
     q, s, z = _random_packed(N, K, G, 10)

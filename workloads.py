@@ -10,7 +10,10 @@ Input recipe (weights are never trained; no dataset is involved):
     by 20 in FP32, then round-to-nearest-even to FP16;
   * x ~ N(0, 1) drawn in FP32, then round-to-nearest-even to BF16;
   * the j-th matrix of a workload uses seed + 100*j, its activations seed +
-    100*j + 50.
+    100*j + 50;
+  * activation-scaled workloads draw x_scale = 1/alpha with alpha = 1 except on a
+    seeded 1 % of input channels, where alpha ~ U[2, 4) (seed + 100*j + 70), and
+    pack W * alpha rounded to FP16.
 
 The shapes follow the pages' examples: a 13B-class layer (hidden 5120, FFN
 13824: multigrid.ai "Weight-Only Quantization Explained", section "The memory
@@ -42,6 +45,7 @@ class Workload:
     outlier_frac: float
     seed: int
     dual: bool = False
+    act_scaled: bool = False     # layer with a per-input-channel activation scale
 
 
 WORKLOADS = {
@@ -59,6 +63,9 @@ WORKLOADS = {
     # paired gate/up projections sharing one x
     "gateup13b_dual": Workload("gateup13b_dual", (Linear("gate", 5120, 13824), Linear("up", 5120, 13824)),
                                (1, 4), (128,), 0.02, 0.0, 3, dual=True),
+    # 13B FFN with an activation scale fused into x staging (salient channels 1 %)
+    "ffn13b_awq": Workload("ffn13b_awq", (Linear("gate", 5120, 13824), Linear("down", 13824, 5120)),
+                           (1, 4, 32), (128,), 0.02, 0.0, 5, act_scaled=True),
     # 70B-shaped FFN gate and down, decode (M=1) and prefill (M=2048)
     "ffn70b": Workload("ffn70b", (Linear("gate", 8192, 28672), Linear("down", 28672, 8192)), (1, 2048),
                        (128,), 0.015, 0.0, 4),
@@ -80,6 +87,25 @@ def activations_bf16(M: int, K: int, seed: int) -> torch.Tensor:
     """BF16 [M,K] activations: N(0,1) in FP32, RNE to BF16."""
     g = torch.Generator().manual_seed(seed)
     return torch.randn(M, K, generator=g, dtype=torch.float32).to(torch.bfloat16)
+
+
+def act_scale_f32(K: int, seed: int, salient_frac: float = 0.01) -> torch.Tensor:
+    """FP32 [K] activation scale of the activation-scaled layer, x_scale = 1 / alpha:
+    alpha = 1 on most input channels and alpha ~ U[2, 4) in FP32 on a seeded
+    `salient_frac` of them (the channels whose weights activation-aware
+    quantisation scales up before packing and whose activations it scales down)."""
+    g = torch.Generator().manual_seed(seed)
+    alpha = torch.ones(K, dtype=torch.float32)
+    n_sal = max(1, int(round(salient_frac * K)))
+    cols = torch.randperm(K, generator=g)[:n_sal]
+    alpha[cols] = 2.0 + 2.0 * torch.rand(n_sal, generator=g, dtype=torch.float32)
+    return 1.0 / alpha
+
+
+def awq_weight_f16(w: torch.Tensor, x_scale: torch.Tensor) -> torch.Tensor:
+    """FP16 [N,K] weight to pack for the activation-scaled layer: W * alpha per input
+    channel (alpha = 1 / x_scale), formed in FP32 and rounded to FP16."""
+    return (w.float() / x_scale.float()).to(torch.float16)
 
 
 def matrix_seed(workload: Workload, j: int) -> int:
