@@ -452,6 +452,24 @@ def _graph_us(launch, n, replays=5):
     return statistics.median(ts)
 
 
+def _eager_us(launch, n, replays=5):
+    """Median over `replays` of the per-launch time of `n` back-to-back eager launches."""
+    stream = torch.cuda.current_stream()
+    for i in range(3):
+        launch(i, stream)
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(replays):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(n):
+            launch(i, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e3 / n)
+    return statistics.median(ts)
+
+
 def run_sweep(args):
     """Decode and small-batch timings of every workload in workloads.py other
     than the bench's own: one JSON line per (workload, matrix, M, G, path) and
@@ -479,8 +497,8 @@ def run_sweep(args):
         print(json.dumps(rec), flush=True)
         return rec
 
-    def record(wk, lin, M, Gv, path, us, nmat=1):
-        byts = nmat * gemv_bytes(M, lin.N, lin.K, Gv) - (nmat - 1) * M * lin.K * 2   # x read once
+    def record(wk, lin, M, Gv, path, us, nmat=1, extra_bytes=0):
+        byts = nmat * gemv_bytes(M, lin.N, lin.K, Gv) - (nmat - 1) * M * lin.K * 2 + extra_bytes   # x read once
         fl = nmat * gemm_flops(M, lin.N, lin.K)
         return emit({"sweep": wk.name, "matrix": lin.name if nmat == 1 else "gate+up", "M": M, "N": lin.N,
                      "K": lin.K, "G": Gv, "path": path, "us": round(us, 2),
@@ -489,8 +507,30 @@ def run_sweep(args):
                      "frac_tensor": round(fl / (us * 1e-6) / 1e12 / pk["bf16_tflops"], 4)})
 
     results = []
-    for name in ("single_4096", "layer13b_decode", "up13b_sweep", "gateup13b_dual"):
+    for name in ("single_4096", "layer13b_decode", "up13b_sweep", "gateup13b_dual", "ffn13b_awq"):
         wk = wl.WORKLOADS[name]
+        if wk.act_scaled:
+            # activation scale fused into x staging (the x_scale vector counts as bytes read);
+            # the tensor-core path allocates stream-ordered scratch, so M > 8 is timed eagerly
+            for j, lin in enumerate(wk.linears):
+                for Gv in wk.Gs:
+                    xsc = wl.act_scale_f32(lin.K, wl.matrix_seed(wk, j) + 70).to(dev)
+                    w = wl.awq_weight_f16(wl.weight_f16(lin.N, lin.K, wk.sigma, wl.matrix_seed(wk, j),
+                                                        wk.outlier_frac), xsc.cpu()).to(dev)
+                    one = gemv_bytes(1, lin.N, lin.K, Gv)
+                    cps = [w4.w4a16_pack(w, Gv) for _ in range(max(2, -(-2 * l2_bytes // one) + 1))]
+                    del w
+                    for M in wk.Ms:
+                        x = wl.activations_bf16(M, lin.K, wl.act_seed(wk, j)).to(dev)
+                        y = torch.empty(M, lin.N, dtype=torch.bfloat16, device=dev)
+                        fn = lambda i, s: w4.w4a16_linear_act_scaled(x, xsc, *cps[i % len(cps)], Gv, out=y,
+                                                                     stream=s)
+                        graph = w4.w4a16_linear_path(M, lin.N, lin.K, Gv) == 1
+                        us = _graph_us(fn, n) if graph else _eager_us(fn, n)
+                        results.append(record(wk, lin, M, Gv, "gemv+scale" if graph else "gemm+scale (eager)", us,
+                                              extra_bytes=lin.K * 4))
+                    del cps
+            continue
         if wk.dual:
             for Gv in wk.Gs:
                 gate = packed_copies(wk, 0, wk.linears[0], Gv)

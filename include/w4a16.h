@@ -190,6 +190,41 @@ W4A16_API w4a16_status w4a16_linear_gemm_noalloc(const void* x_bf16, const uint3
                                        int64_t K, int G, void* y_bf16, w4a16_stream_t stream);
 
 /*
+ * w4a16_linear_act_scaled: the layer with a per-input-channel activation
+ * scale fused into the staging of x:
+ *   y[m,n] = bf16_rn( sum_k fp16_rn(fp32(x[m,k] * x_scale[k])) * W_hat[n,k] ).
+ * This is the deployed form of activation-aware weight quantisation: the
+ * weights of salient input channels (those that meet large activations) are
+ * scaled up by alpha_k before packing and the activations scaled down by the
+ * same factor, so the kernel stays an ordinary groupwise INT4 layer
+ * (instagit.com "Comparison of Quantization Methods: INT8 vs GPTQ vs AWQ vs
+ * GGUF", section "AWQ: Activation-Aware Weight Quantization"; klaylearn.com
+ * glossary "Weight-Only Quantisation", FAQ "What is the difference between AWQ
+ * and GPTQ?").  The caller packs W * diag(alpha) with w4a16_pack and passes
+ * x_scale[k] = 1 / alpha_k.
+ *   x_scale  FP32 [K], device, 16-byte aligned, owned by the caller; any
+ *            finite values (|x * x_scale| must stay in the FP16 range).
+ * Dispatch, layouts and the other arguments as for w4a16_linear.  The
+ * product is formed in FP32 and rounded to FP16 once, on both kernels.
+ * Errors: as w4a16_linear, plus W4A16_ERR_INVALID_ARG for a null x_scale and
+ * W4A16_ERR_MISALIGNED for a misaligned one.
+ */
+W4A16_API w4a16_status w4a16_linear_act_scaled(const void* x_bf16, const float* x_scale, const uint32_t* qweight,
+                                     const void* scales_f16, const uint32_t* zeros, int64_t M, int64_t N,
+                                     int64_t K, int G, void* y_bf16, w4a16_stream_t stream);
+
+/*
+ * w4a16_linear_dual_act_scaled: w4a16_linear_dual with the same activation
+ * scale applied to the shared x (both projections see x[m,k] * x_scale[k]).
+ */
+W4A16_API w4a16_status w4a16_linear_dual_act_scaled(const void* x_bf16, const float* x_scale,
+                                          const uint32_t* qweight_gate, const void* scales_gate,
+                                          const uint32_t* zeros_gate, const uint32_t* qweight_up,
+                                          const void* scales_up, const uint32_t* zeros_up, int64_t M, int64_t N,
+                                          int64_t K, int G, void* y_gate_bf16, void* y_up_bf16,
+                                          w4a16_stream_t stream);
+
+/*
  * Which kernel w4a16_linear would run for this shape: 1 = GEMV, 2 = GEMM,
  * 0 = the shape is rejected.  Host-only, no device access.
  */

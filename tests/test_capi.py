@@ -102,6 +102,23 @@ def test_dual_argument_errors():
     assert f(a, a, a, a, a, a, a, 0, 64, 256, 128, a, a, v(0)) == 0
 
 
+def test_act_scaled_argument_errors():
+    v = ctypes.c_void_p
+    a = v(1 << 12)
+    f = w4._lib.w4a16_linear_act_scaled
+    assert f(a, a, a, a, a, 1, 64, 256, 96, a, v(0)) == 2                  # unsupported group size
+    assert f(a, v(0), a, a, a, 1, 64, 256, 128, a, v(0)) == 1              # null x_scale
+    assert f(a, v((1 << 12) + 4), a, a, a, 1, 64, 256, 128, a, v(0)) == 3  # misaligned x_scale
+    assert f(a, a, a, a, a, 1, 60, 256, 128, a, v(0)) == 1                 # N % 8
+    assert f(v(0), a, a, a, a, 1, 64, 256, 128, a, v(0)) == 1              # null x
+    assert f(a, a, a, a, a, 0, 64, 256, 128, a, v(0)) == 0                 # empty problem
+    d = w4._lib.w4a16_linear_dual_act_scaled
+    assert d(a, v(0), a, a, a, a, a, a, 1, 64, 256, 128, a, a, v(0)) == 1
+    assert d(a, v((1 << 12) + 8), a, a, a, a, a, a, 1, 64, 256, 128, a, a, v(0)) == 3
+    assert d(a, a, a, a, a, a, a, a, 1, 64, 256, 96, a, a, v(0)) == 2
+    assert d(a, a, a, a, a, a, a, a, 0, 64, 256, 128, a, a, v(0)) == 0
+
+
 def test_path_query_rejects_bad_shapes():
     assert w4.w4a16_linear_path(1, 60, 256, 128) == 0
     assert w4.w4a16_linear_path(1, 64, 250, 128) == 0

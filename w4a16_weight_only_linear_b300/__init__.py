@@ -38,6 +38,9 @@ EXPORTS = {
     "w4a16_linear_gemv": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp], _i32),
     "w4a16_linear_gemm": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp], _i32),
     "w4a16_linear_gemm_noalloc": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp], _i32),
+    "w4a16_linear_act_scaled": ([_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp], _i32),
+    "w4a16_linear_dual_act_scaled": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp,
+                                      _vp], _i32),
     "w4a16_linear_path": ([_i64, _i64, _i64, _i32], _i32),
     "w4a16_device_status": ([_vp], _i32),
 }
@@ -186,6 +189,43 @@ def w4a16_linear_dual(x, gate, up, G, out=None, stream=None):
     yg, yu = out
     _check("w4a16_linear_dual", _lib.w4a16_linear_dual(
         _dev(x, torch.bfloat16, "x"),
+        _dev(gate[0], torch.int32, "qweight_gate"), _dev(gate[1], torch.float16, "scales_gate"),
+        _dev(gate[2], torch.int32, "zeros_gate"),
+        _dev(up[0], torch.int32, "qweight_up"), _dev(up[1], torch.float16, "scales_up"),
+        _dev(up[2], torch.int32, "zeros_up"),
+        M, N, K, G, _dev(yg, torch.bfloat16, "y_gate"), _dev(yu, torch.bfloat16, "y_up"), _stream(stream)))
+    return yg, yu
+
+
+def w4a16_linear_act_scaled(x, x_scale, q, s, z, G, out=None, stream=None):
+    """y BF16 [M,N] = (x * x_scale) * W_hat^T: x_scale FP32 [K] multiplies each
+    input channel of x before it is rounded to FP16 (the deployed form of
+    activation-aware quantisation, with W packed from W * diag(1 / x_scale))."""
+    M, K = x.shape
+    N = q.shape[0]
+    if x_scale.shape != (K,):
+        raise ValueError(f"x_scale must have shape ({K},), got {tuple(x_scale.shape)}")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _check("w4a16_linear_act_scaled", _lib.w4a16_linear_act_scaled(
+        _dev(x, torch.bfloat16, "x"), _dev(x_scale, torch.float32, "x_scale"), _dev(q, torch.int32, "qweight"),
+        _dev(s, torch.float16, "scales"), _dev(z, torch.int32, "zeros"), M, N, K, G,
+        _dev(out, torch.bfloat16, "y"), _stream(stream)))
+    return out
+
+
+def w4a16_linear_dual_act_scaled(x, x_scale, gate, up, G, out=None, stream=None):
+    """w4a16_linear_dual with the activation scale x_scale FP32 [K] applied to the shared x."""
+    M, K = x.shape
+    N = gate[0].shape[0]
+    if x_scale.shape != (K,):
+        raise ValueError(f"x_scale must have shape ({K},), got {tuple(x_scale.shape)}")
+    if out is None:
+        out = (torch.empty((M, N), dtype=torch.bfloat16, device=x.device),
+               torch.empty((M, N), dtype=torch.bfloat16, device=x.device))
+    yg, yu = out
+    _check("w4a16_linear_dual_act_scaled", _lib.w4a16_linear_dual_act_scaled(
+        _dev(x, torch.bfloat16, "x"), _dev(x_scale, torch.float32, "x_scale"),
         _dev(gate[0], torch.int32, "qweight_gate"), _dev(gate[1], torch.float16, "scales_gate"),
         _dev(gate[2], torch.int32, "zeros_gate"),
         _dev(up[0], torch.int32, "qweight_up"), _dev(up[1], torch.float16, "scales_up"),

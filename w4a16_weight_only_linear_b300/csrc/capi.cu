@@ -54,7 +54,8 @@ int choose_path(int64_t M, int64_t N, int64_t K, int G, int nmat) {
 }
 
 w4a16_status linear_common(const void* x, const uint32_t* q, const void* s, const uint32_t* z, int64_t M,
-                           int64_t N, int64_t K, int G, void* y, w4a16_stream_t stream, int force) {
+                           int64_t N, int64_t K, int G, void* y, w4a16_stream_t stream, int force,
+                           const float* xsc = nullptr) {
     w4a16_status st = check_weight_shape(N, K, G);
     if (st != W4A16_OK) return st;
     if (M < 0 || M > kMaxDim) return W4A16_ERR_INVALID_ARG;
@@ -67,9 +68,36 @@ w4a16_status linear_common(const void* x, const uint32_t* q, const void* s, cons
     GemvMat mat{q, s, z, y};
     if (path == 1) {
         if (M > 16 || !w4a16::gemv_fits(M, N, K, G, 1)) return W4A16_ERR_UNSUPPORTED;
-        return from_cuda(w4a16::launch_gemv(x, &mat, 1, M, N, K, G, cs));
+        return from_cuda(w4a16::launch_gemv(x, &mat, 1, M, N, K, G, cs, xsc));
     }
-    return from_cuda(w4a16::launch_gemm(x, &mat, 1, M, N, K, G, cs));
+    return from_cuda(w4a16::launch_gemm(x, &mat, 1, M, N, K, G, cs, xsc));
+}
+
+w4a16_status dual_common(const void* x_bf16, const uint32_t* qweight_gate, const void* scales_gate,
+                         const uint32_t* zeros_gate, const uint32_t* qweight_up, const void* scales_up,
+                         const uint32_t* zeros_up, int64_t M, int64_t N, int64_t K, int G, void* y_gate_bf16,
+                         void* y_up_bf16, w4a16_stream_t stream, const float* xsc) {
+    w4a16_status st = check_weight_shape(N, K, G);
+    if (st != W4A16_OK) return st;
+    if (M < 0 || M > kMaxDim) return W4A16_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return W4A16_OK;
+    if ((st = check_weights(qweight_gate, scales_gate, zeros_gate)) != W4A16_OK) return st;
+    if ((st = check_weights(qweight_up, scales_up, zeros_up)) != W4A16_OK) return st;
+    if (!x_bf16 || !y_gate_bf16 || !y_up_bf16) return W4A16_ERR_INVALID_ARG;
+    if (!aligned16(x_bf16) || !aligned16(y_gate_bf16) || !aligned16(y_up_bf16)) return W4A16_ERR_MISALIGNED;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const GemvMat mats[2] = {{qweight_gate, scales_gate, zeros_gate, y_gate_bf16},
+                             {qweight_up, scales_up, zeros_up, y_up_bf16}};
+    if (choose_path(M, N, K, G, 2) == 1)
+        return from_cuda(w4a16::launch_gemv(x_bf16, mats, 2, M, N, K, G, cs, xsc));
+    return from_cuda(w4a16::launch_gemm(x_bf16, mats, 2, M, N, K, G, cs, xsc));
+}
+
+// The activation-scale vector of the *_act_scaled entry points: present and 16-byte aligned.
+w4a16_status check_act_scale(const float* x_scale) {
+    if (!x_scale) return W4A16_ERR_INVALID_ARG;
+    if (!aligned16(x_scale)) return W4A16_ERR_MISALIGNED;
+    return W4A16_OK;
 }
 
 }  // namespace
@@ -139,19 +167,29 @@ w4a16_status w4a16_linear_dual(const void* x_bf16, const uint32_t* qweight_gate,
                                const uint32_t* zeros_gate, const uint32_t* qweight_up, const void* scales_up,
                                const uint32_t* zeros_up, int64_t M, int64_t N, int64_t K, int G,
                                void* y_gate_bf16, void* y_up_bf16, w4a16_stream_t stream) {
+    return dual_common(x_bf16, qweight_gate, scales_gate, zeros_gate, qweight_up, scales_up, zeros_up, M, N, K, G,
+                       y_gate_bf16, y_up_bf16, stream, nullptr);
+}
+
+w4a16_status w4a16_linear_act_scaled(const void* x_bf16, const float* x_scale, const uint32_t* qweight,
+                                     const void* scales_f16, const uint32_t* zeros, int64_t M, int64_t N, int64_t K,
+                                     int G, void* y_bf16, w4a16_stream_t stream) {
     w4a16_status st = check_weight_shape(N, K, G);
     if (st != W4A16_OK) return st;
-    if (M < 0 || M > kMaxDim) return W4A16_ERR_INVALID_ARG;
-    if (M == 0 || N == 0) return W4A16_OK;
-    if ((st = check_weights(qweight_gate, scales_gate, zeros_gate)) != W4A16_OK) return st;
-    if ((st = check_weights(qweight_up, scales_up, zeros_up)) != W4A16_OK) return st;
-    if (!x_bf16 || !y_gate_bf16 || !y_up_bf16) return W4A16_ERR_INVALID_ARG;
-    if (!aligned16(x_bf16) || !aligned16(y_gate_bf16) || !aligned16(y_up_bf16)) return W4A16_ERR_MISALIGNED;
-    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    const GemvMat mats[2] = {{qweight_gate, scales_gate, zeros_gate, y_gate_bf16},
-                             {qweight_up, scales_up, zeros_up, y_up_bf16}};
-    if (choose_path(M, N, K, G, 2) == 1) return from_cuda(w4a16::launch_gemv(x_bf16, mats, 2, M, N, K, G, cs));
-    return from_cuda(w4a16::launch_gemm(x_bf16, mats, 2, M, N, K, G, cs));
+    if ((st = check_act_scale(x_scale)) != W4A16_OK) return st;
+    return linear_common(x_bf16, qweight, scales_f16, zeros, M, N, K, G, y_bf16, stream, 0, x_scale);
+}
+
+w4a16_status w4a16_linear_dual_act_scaled(const void* x_bf16, const float* x_scale, const uint32_t* qweight_gate,
+                                          const void* scales_gate, const uint32_t* zeros_gate,
+                                          const uint32_t* qweight_up, const void* scales_up,
+                                          const uint32_t* zeros_up, int64_t M, int64_t N, int64_t K, int G,
+                                          void* y_gate_bf16, void* y_up_bf16, w4a16_stream_t stream) {
+    w4a16_status st = check_weight_shape(N, K, G);
+    if (st != W4A16_OK) return st;
+    if ((st = check_act_scale(x_scale)) != W4A16_OK) return st;
+    return dual_common(x_bf16, qweight_gate, scales_gate, zeros_gate, qweight_up, scales_up, zeros_up, M, N, K, G,
+                       y_gate_bf16, y_up_bf16, stream, x_scale);
 }
 
 w4a16_status w4a16_linear_gemm_noalloc(const void* x_bf16, const uint32_t* qweight, const void* scales_f16,

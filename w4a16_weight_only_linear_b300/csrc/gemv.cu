@@ -68,6 +68,7 @@ __device__ __forceinline__ int sigma8(int i) { return (i >> 1) + ((i & 1) << 2);
 
 struct GemvParams {
     const __nv_bfloat16* x;                // [M, K]
+    const float* xsc;                      // per-input-channel multiplier of x [K], or null
     const unsigned short* s[2];            // FP16 scales [N, lds]
     const uint32_t* z[2];                  // zeros [N, ldz]
     __nv_bfloat16* y[2];                   // [M, N]
@@ -360,6 +361,12 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
                 for (int q = 0; q < 4; ++q) {
                     f[2 * q] = bf16lo_to_f32(in[q]);
                     f[2 * q + 1] = bf16hi_to_f32(in[q]);
+                }
+                if (p.xsc != nullptr && wseg * 8 < kseg) {  // activation scale: x_k * xsc_k in FP32
+                    const float4* sp = reinterpret_cast<const float4*>(p.xsc + (int64_t)pseg * kseg + wseg * 8);
+                    const float4 s0 = sp[0], s1 = sp[1];
+                    f[0] *= s0.x; f[1] *= s0.y; f[2] *= s0.z; f[3] *= s0.w;
+                    f[4] *= s1.x; f[5] *= s1.y; f[6] *= s1.z; f[7] *= s1.w;
                 }
                 __half2 hp[4];
 #pragma unroll
@@ -959,7 +966,7 @@ bool gemv_fits(int64_t M, int64_t N, int64_t K, int G, int nmat) {
 }
 
 cudaError_t launch_gemv(const void* x, const GemvMat* mats, int nmat, int64_t M, int64_t N, int64_t K, int G,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, const float* xsc) {
     const int sms = device_sms();
     if (sms <= 0) return cudaErrorNoDevice;
     const size_t cap = device_smem_optin();
@@ -967,6 +974,7 @@ cudaError_t launch_gemv(const void* x, const GemvMat* mats, int nmat, int64_t M,
     if (!make_plan(M, N, K, G, nmat, sms, cap, pl)) return cudaErrorNotSupported;
     GemvParams& p = pl.p;
     p.x = static_cast<const __nv_bfloat16*>(x);
+    p.xsc = xsc;
     CUtensorMap tm[2];
     for (int i = 0; i < 2; ++i) {
         const GemvMat& mt = mats[i < nmat ? i : 0];

@@ -26,13 +26,14 @@ bool gemv_fits(int64_t M, int64_t N, int64_t K, int G, int nmat);
 size_t device_smem_optin();
 
 // y_i = x * W_hat_i^T for one matrix (nmat = 1) or two matrices sharing x (nmat = 2).
+// xsc (optional, FP32 [K], 16-byte aligned): x_k is taken as x_k * xsc_k.
 cudaError_t launch_gemv(const void* x, const GemvMat* mats, int nmat, int64_t M, int64_t N, int64_t K, int G,
-                        cudaStream_t stream);
+                        cudaStream_t stream, const float* xsc = nullptr);
 
 // Tensor-core path (any M): y_i = x * W_hat_i^T for nmat matrices sharing x
 // (x is converted to FP16 once, into stream-ordered scratch).
 cudaError_t launch_gemm(const void* x, const GemvMat* mats, int nmat, int64_t M, int64_t N, int64_t K, int G,
-                        cudaStream_t stream);
+                        cudaStream_t stream, const float* xsc = nullptr);
 // The same tensor-core path for one matrix with the FP16 copy of x in a
 // fixed-size file-scope device array (no allocation; M * K bounded by the
 // header's W4A16_NOALLOC_MAX_X_ELEMS, else cudaErrorNotSupported).
