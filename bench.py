@@ -65,13 +65,23 @@ def gemm_flops(M, N, K):
     return 2.0 * M * N * K
 
 
+def _code_only(text):
+    """C++ source without comments and whitespace, so that edits to comments do
+    not mark stored counters as stale (string literals hold no comment markers here)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return re.sub(r"\s+", "", text)
+
+
 def kernel_hashes():
-    """Source hashes of the kernels whose ncu counters are stored in profiles/."""
+    """Hashes of the code (comments and whitespace removed) of the kernels whose
+    ncu counters are stored in profiles/."""
     out = {}
     for name in ("gemv.cu", "gemm_tc.cu"):
         p = os.path.join(ROOT, "w4a16_weight_only_linear_b300", "csrc", name)
         if os.path.exists(p):
-            out[name] = hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+            out[name] = hashlib.sha256(_code_only(open(p).read()).encode()).hexdigest()[:16]
     return out
 
 

@@ -1,4 +1,5 @@
-// gemv.cu -- decode path of the W4A16 linear layer (M <= 16 activation rows).
+// gemv.cu -- decode path of the W4A16 linear layer (up to 16 activation rows;
+// the library dispatches M <= 8 here).
 //
 // Decode rereads every weight for each generated token with little work per
 // weight, so this kernel is bound by HBM bandwidth on the packed weights
@@ -11,27 +12,37 @@
 // virtual row is one (row, segment) pair: the packed matrix [N, K/8] words is
 // read as [N*P, K/(8P)].  A tile is 16 virtual rows = R = 16/P weight rows;
 // the 16 rows of a warp MMA m16n8k16 are the tile's virtual rows, and the MMA's
-// B columns hold the P segments of x (times M activation rows; P*M <= 8, or
-// two column blocks for M > 8).  So one MMA advances all segments of R rows at
-// once, and only the diagonal (segment of the row == segment of the column)
-// of D is kept.  At M = 1 a tile is 2 weight rows, which lets the grid split
-// the rows evenly over the SMs.
+// B columns hold (segment, group parity, activation row) triples of x (at most
+// 8 per column block; two blocks for M > 8).  So one MMA advances all segments
+// of R rows at once, and only the diagonal (segment of the row == segment of
+// the column) of D is kept.  H group parities let one column collect every
+// H-th group, so the scale/zero correction runs once per block of H groups.
+// At M = 1 the columns are (parity, segment) pairs, P is a template constant,
+// and each lane corrects only the one value per row it holds.
 //
-// Data path.  One CTA per SM takes a balanced contiguous range of tiles; its
-// work is (tile, 256-code chunk) units, split into contiguous runs over 12
-// warps.  Each warp streams its own units with TMA (16 virtual rows x 128
-// bytes per unit, 128-byte swizzle) into a private ring of shared-memory
-// stages, so no load instruction sits on the code path.  Per word of 8 codes
-// the lane makes four FP16 pairs with one shift and four LOP3s: the FP16
-// exponents of 1024 (ulp 1) and 64 (ulp 1/16) turn a nibble at bits 0..3 or
-// 4..7 of a half into the exact values 1024 + q and 64 + q.  These meet x
-// (converted to FP16 once per CTA and staged in shared memory in fragment
-// order) in the warp MMA with FP32 accumulation.  At the end of each group the
-// lane subtracts the staged sum of (1024 or 64) * x plus z * sum x, scales by
-// s and accumulates; at the end of a tile the diagonal is reduced over
-// segments.  Warps that share a tile (run boundaries) leave partial sums in
-// fixed slots, added in a fixed order at the end, so results are
+// Data path.  One CTA per SM (16 warps, or 12 when registers or shared memory
+// are short) takes a balanced contiguous range of tiles; its warps take
+// contiguous runs of 256-code chunks, balanced to the chunk.  Each warp
+// streams its run with TMA (16 virtual rows x 128 bytes per chunk, 128-byte
+// swizzle) into a private ring of shared-memory slots; a slot holds a unit of
+// two chunks of one tile under one barrier (one chunk where a tile or a run
+// ends).  Per word of 8 codes the lane makes four FP16 pairs with one shift
+// and four LOP3s: the FP16 exponents of 1024 (ulp 1) and 64 (ulp 1/16) turn a
+// nibble at bits 0..3 or 4..7 of a half into the exact values 1024 + q and
+// 64 + q.  These meet x (converted to FP16 once per CTA and staged in shared
+// memory in fragment order) in the warp MMA with FP32 accumulation.  At the end
+// of each block the lane subtracts the staged sum of (1024 or 64) * x plus
+// z * sum x, scales by s and accumulates; at the end of a tile the diagonal is
+// reduced over segments and parities.  Warps that share a tile leave partial
+// sums in fixed slots, added in a fixed order at the end, so results are
 // deterministic.  Every output is rounded to BF16 once.
+//
+// Prologue.  The launch uses programmatic stream serialisation: a CTA lets the
+// next launch be scheduled on entry and waits for the previous grid before it
+// reads global memory.  One thread then bulk-copies the CTA's scale and zero
+// rows while every warp loads its first x items; the weight ring starts once
+// the rows have landed (copies issued together complete in no particular
+// order), and x is staged while the first units are in flight.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -53,7 +64,7 @@ namespace {
 // (one activation-row block, G >= 64), else 12.
 __host__ __device__ constexpr int cta_warps(int NB, int G) { return NB == 1 && G >= 64 ? 16 : 12; }
 constexpr int kBoxBytes = 2048;           // one TMA box: 16 virtual rows x 128 bytes (256 codes)
-constexpr int kUnitBytes = 2 * kBoxBytes;  // a unit is two consecutive 256-code chunks of a tile
+constexpr int kUnitBytes = 2 * kBoxBytes;  // a ring slot: a unit of up to two consecutive chunks of a tile
 constexpr int kSlots = 4;                 // partial-sum slots per output (warps sharing a tile)
 constexpr int kMaxDevices = 64;
 constexpr long long kSpinCycles = 1ll << 31;
