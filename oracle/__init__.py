@@ -45,6 +45,12 @@ def _load():
         lib.oracle_linear.restype = None
         lib.oracle_linear_sampled.argtypes = [p, p, p, p, i64, i64, p, p, i64, p, i32]
         lib.oracle_linear_sampled.restype = None
+        lib.oracle_pack8.argtypes = [p, i64, i64, i64, p, p, p, i32]
+        lib.oracle_pack8.restype = i32
+        lib.oracle_dequant8.argtypes = [p, p, p, i64, i64, i64, p, i32]
+        lib.oracle_dequant8.restype = None
+        lib.oracle_linear8.argtypes = [p, p, p, p, i64, i64, i64, i64, p, i32]
+        lib.oracle_linear8.restype = None
         lib.oracle_linear_xs.argtypes = [p, p, p, p, p, i64, i64, i64, i64, p, i32]
         lib.oracle_linear_xs.restype = None
         lib.oracle_max_threads.argtypes, lib.oracle_max_threads.restype = [], i32
@@ -210,6 +216,47 @@ def linear_xs(x_bf16: np.ndarray, x_scale: np.ndarray, q, s, z, N: int, K: int, 
     z = np.ascontiguousarray(z, dtype=np.uint32)
     y = np.zeros((M, N), np.float64)
     _load().oracle_linear_xs(_ptr(x), _ptr(xs), _ptr(q), _ptr(s), _ptr(z), M, N, K, G, _ptr(y), nthreads)
+    return y
+
+
+# ---- the 8-bit variant ---------------------------------------------------------
+
+def pack8(w_f16: np.ndarray, G: int, nthreads: int = 0):
+    """FP16 [N,K] -> (qweight u32 [N, K/4], scales u16 [N, scales_ld(2K, G)],
+    zeros u32 [N, zeros_ld(2K, G)]): 8-bit codes kept as two 4-bit planes of a
+    2K-channel 4-bit layer (hi nibbles, then lo nibbles; scales 16*s8 then s8;
+    zeros z8 >> 4 then z8 & 15)."""
+    w = _u16(w_f16)
+    N, K = w.shape
+    q = np.zeros((N, qweight_ld(2 * K)), np.uint32)
+    s = np.zeros((N, scales_ld(2 * K, G)), np.uint16)
+    z = np.zeros((N, zeros_ld(2 * K, G)), np.uint32)
+    rc = _load().oracle_pack8(_ptr(w), N, K, G, _ptr(q), _ptr(s), _ptr(z), nthreads)
+    if rc != 0:
+        raise ValueError("oracle_pack8: bad shape")
+    return q, s, z
+
+
+def dequant8(q, s, z, N: int, K: int, G: int, nthreads: int = 0) -> np.ndarray:
+    """W_hat8 [N,K] FP32 = (q8 - z8) * s8 read back from the planes."""
+    q = np.ascontiguousarray(q, dtype=np.uint32)
+    s = _u16(s)
+    z = np.ascontiguousarray(z, dtype=np.uint32)
+    out = np.zeros((N, K), np.float32)
+    _load().oracle_dequant8(_ptr(q), _ptr(s), _ptr(z), N, K, G, _ptr(out), nthreads)
+    return out
+
+
+def linear8(x_bf16: np.ndarray, q, s, z, N: int, K: int, G: int, nthreads: int = 0) -> np.ndarray:
+    """y_ref [M,N] FP64 = x * W_hat8^T, unrounded."""
+    x = _u16(x_bf16)
+    M = x.shape[0]
+    assert x.shape[1] == K
+    q = np.ascontiguousarray(q, dtype=np.uint32)
+    s = _u16(s)
+    z = np.ascontiguousarray(z, dtype=np.uint32)
+    y = np.zeros((M, N), np.float64)
+    _load().oracle_linear8(_ptr(x), _ptr(q), _ptr(s), _ptr(z), M, N, K, G, _ptr(y), nthreads)
     return y
 
 

@@ -367,6 +367,152 @@ void oracle_linear_xs(const uint16_t* x_bf16, const float* x_scale, const uint32
     (void)nthreads;
 }
 
+/* ------------------------------------------------------------------------ */
+/* The 8-bit variant (W8A16).                                                 */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Weight-only quantisation stores the weights as INT8 or INT4 and leaves the
+ * activations in 16-bit (klaylearn.com glossary "Weight-Only Quantisation",
+ * first FAQ answer and main body).  The 8-bit quantiser here is the 4-bit one
+ * with 255 steps:
+ *   lo = min(0, min w), hi = max(0, max w)
+ *   s8 = RNE_fp16( fp32(hi - lo) / 255 ); s8 == 0 -> s8 = 1, z8 = 0
+ *   z8 = clamp(rne(-lo / s8), 0, 255),  q8 = clamp(rne(w / s8) + z8, 0, 255)
+ * Storage (a reading; the pages give none): an 8-bit code is kept as two 4-bit
+ * planes of a 4-bit layer with 2K input channels.  Row n holds the K high
+ * nibbles q8 >> 4 (channels 0..K-1) followed by the K low nibbles q8 & 15
+ * (channels K..2K-1) in the 4-bit layout; its scales are the K/G hi-plane
+ * scales 16*s8 followed by the K/G lo-plane scales s8, its zeros z8 >> 4 then
+ * z8 & 15.  8 bits per weight; row pitches those of the 2K-channel 4-bit layer.
+ */
+void oracle_quantize_group8(const float* w, int64_t G, uint16_t* scale_bits, int* zero, int* codes)
+{
+    float lo = 0.0f, hi = 0.0f;
+    for (int64_t i = 0; i < G; ++i) {
+        if (w[i] < lo) lo = w[i];
+        if (w[i] > hi) hi = w[i];
+    }
+    volatile float range = hi - lo;
+    volatile float s32 = range / 255.0f;
+    uint16_t sb = oracle_f32_to_f16(s32);
+    float s = oracle_f16_to_f32(sb);
+    int z;
+    if (s == 0.0f) {
+        sb = 0x3C00;
+        s = 1.0f;
+        z = 0;
+    } else {
+        volatile float t = -lo / s;
+        z = (int)clamp_i64((int64_t)nearbyintf(t), 0, 255);
+    }
+    for (int64_t i = 0; i < G; ++i) {
+        volatile float t = w[i] / s;
+        int64_t q = (int64_t)nearbyintf(t) + z;
+        codes[i] = (int)clamp_i64(q, 0, 255);
+    }
+    *scale_bits = sb;
+    *zero = z;
+}
+
+int oracle_pack8(const uint16_t* w_f16, int64_t N, int64_t K, int64_t G,
+                 uint32_t* qweight, uint16_t* scales, uint32_t* zeros, int nthreads)
+{
+    if (N <= 0 || K <= 0 || G <= 0 || G > 256 || K % G != 0 || G % 8 != 0) return -1;
+    const int64_t K2 = 2 * K;
+    const int64_t ldq = oracle_qweight_ld(K2);
+    const int64_t lds = oracle_scales_ld(K2, G);
+    const int64_t ldz = oracle_zeros_ld(K2, G);
+    const int64_t ngroups = K / G;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(static)
+#endif
+    for (int64_t n = 0; n < N; ++n) {
+        float wf[256];
+        int codes[256];
+        uint32_t* qrow = qweight + n * ldq;
+        uint16_t* srow = scales + n * lds;
+        uint32_t* zrow = zeros + n * ldz;
+        for (int64_t i = 0; i < ldq; ++i) qrow[i] = 0;
+        for (int64_t i = 0; i < lds; ++i) srow[i] = 0;
+        for (int64_t i = 0; i < ldz; ++i) zrow[i] = 0;
+        for (int64_t g = 0; g < ngroups; ++g) {
+            for (int64_t i = 0; i < G; ++i) wf[i] = oracle_f16_to_f32(w_f16[n * K + g * G + i]);
+            uint16_t sb;
+            int z;
+            oracle_quantize_group8(wf, G, &sb, &z, codes);
+            srow[g] = oracle_f32_to_f16(16.0f * oracle_f16_to_f32(sb));   /* exact: a power-of-two scaling */
+            srow[ngroups + g] = sb;
+            zrow[g / 8] |= (uint32_t)(z >> 4) << (4 * (g % 8));
+            zrow[(ngroups + g) / 8] |= (uint32_t)(z & 15) << (4 * ((ngroups + g) % 8));
+            for (int64_t i = 0; i < G; ++i) {
+                int64_t k = g * G + i;
+                qrow[k / 8] |= (uint32_t)(codes[i] >> 4) << (4 * (k % 8));
+                qrow[(K + k) / 8] |= (uint32_t)(codes[i] & 15) << (4 * ((K + k) % 8));
+            }
+        }
+    }
+    (void)nthreads;
+    return 0;
+}
+
+/* The 8-bit code, zero point and scale of weight (n, k) read back from the planes. */
+static int oracle_code8(const uint32_t* qweight, int64_t K, int64_t n, int64_t k)
+{
+    return 16 * oracle_code(qweight, 2 * K, n, k) + oracle_code(qweight, 2 * K, n, K + k);
+}
+static int oracle_zero8(const uint32_t* zeros, int64_t K, int64_t G, int64_t n, int64_t g)
+{
+    return 16 * oracle_zero(zeros, 2 * K, G, n, g) + oracle_zero(zeros, 2 * K, G, n, K / G + g);
+}
+
+/* W_hat8 = (q8 - z8) * s8, exact in FP32 (at most 9 + 11 significant bits). */
+float oracle_dequant8_one(const uint32_t* qweight, const uint16_t* scales, const uint32_t* zeros,
+                          int64_t K, int64_t G, int64_t n, int64_t k)
+{
+    int64_t g = k / G;
+    int q = oracle_code8(qweight, K, n, k);
+    int z = oracle_zero8(zeros, K, G, n, g);
+    float s = oracle_scale(scales, 2 * K, G, n, K / G + g);
+    return (float)(q - z) * s;
+}
+
+void oracle_dequant8(const uint32_t* qweight, const uint16_t* scales, const uint32_t* zeros,
+                     int64_t N, int64_t K, int64_t G, float* w_out, int nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(static)
+#endif
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k)
+            w_out[n * K + k] = oracle_dequant8_one(qweight, scales, zeros, K, G, n, k);
+    (void)nthreads;
+}
+
+/* y_ref[m][n] = sum_k (double)x[m][k] * (double)W_hat8[n][k], FP64 in increasing k, unrounded. */
+void oracle_linear8(const uint16_t* x_bf16, const uint32_t* qweight, const uint16_t* scales,
+                    const uint32_t* zeros, int64_t M, int64_t N, int64_t K, int64_t G, double* y_out,
+                    int nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t m = 0; m < M; ++m) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double xv = (double)oracle_bf16_to_f32(x_bf16[m * K + k]);
+                double wv = (double)oracle_dequant8_one(qweight, scales, zeros, K, G, n, k);
+                acc += xv * wv;
+            }
+            y_out[m * N + n] = acc;
+        }
+    (void)nthreads;
+}
+
 int oracle_max_threads(void)
 {
 #ifdef _OPENMP

@@ -358,6 +358,111 @@ def test_act_scale_brute_force_rational(M, N, Kg, G):
             assert abs(y[m, n] - ref) <= 1e-12 * max(1.0, abs(ref)), (m, n, y[m, n], ref)
 
 
+# --------------------------------------------------------------------------
+# The 8-bit variant: codes kept as two 4-bit planes of a 2K-channel layer
+# --------------------------------------------------------------------------
+
+def _planes(q, s, z, K, G):
+    """(q8 [N,K], z8 [N,K/G], s8 [N,K/G] as float, s_hi [N,K/G] as float) decoded here
+    from the stored planes with the layout rules written out directly."""
+    N, ng = q.shape[0], K // G
+    codes = oracle.unpack_codes(q, 2 * K)
+    zeros = oracle.unpack_zeros(z, 2 * K, G)
+    sf = s[:, : 2 * ng].view(np.float16).astype(np.float64)
+    q8 = 16 * codes[:, :K].astype(np.int64) + codes[:, K:]
+    z8 = 16 * zeros[:, :ng].astype(np.int64) + zeros[:, ng:2 * ng]
+    return q8, z8, sf[:, ng:], sf[:, :ng]
+
+
+@pytest.mark.parametrize("G", [32, 128, 256])
+def test_pack8_on_grid_round_trip(G):
+    # w = (q8 - z8) * s8 with s8 of <= 3 significant bits is exact in FP16; with codes 0 and
+    # 255 in every group, lo = -z8 s8 and hi = (255 - z8) s8, so (hi - lo) / 255 = s8 exactly
+    # and the packer must return these codes, zeros and scales
+    rng = np.random.default_rng(G)
+    N, K = 6, 2 * G
+    q8 = rng.integers(0, 256, (N, K))
+    z8 = rng.integers(0, 256, (N, K // G))
+    s8 = (rng.integers(4, 8, (N, K // G)) * 2.0 ** rng.integers(-14, -6, (N, K // G))).astype(np.float64)
+    for n in range(N):
+        for g in range(K // G):
+            q8[n, g * G] = 0
+            q8[n, g * G + 1] = 255
+    w = ((q8 - np.repeat(z8, G, axis=1)) * np.repeat(s8, G, axis=1))
+    w16 = w.astype(np.float16)
+    assert np.array_equal(w16.astype(np.float64), w)
+    q, s, z = oracle.pack8(w16, G)
+    gq8, gz8, gs8, gshi = _planes(q, s, z, K, G)
+    assert np.array_equal(gq8, q8) and np.array_equal(gz8, z8) and np.array_equal(gs8, s8)
+    assert np.array_equal(gshi, 16.0 * s8)
+
+
+@pytest.mark.parametrize("G", [32, 64, 128, 256])
+def test_pack8_error_bound_and_planes(G):
+    rng = np.random.default_rng(100 + G)
+    N, K = 8, 4 * G
+    w16 = (rng.standard_normal((N, K)) * 0.03).astype(np.float16)
+    w16[:, 3] = 0.0
+    q, s, z = oracle.pack8(w16, G)
+    q8, z8, s8, shi = _planes(q, s, z, K, G)
+    assert q8.min() >= 0 and q8.max() <= 255 and z8.min() >= 0 and z8.max() <= 255
+    assert np.array_equal(shi, 16.0 * s8)                       # hi-plane scale is 16 * s8, exactly
+    what = (q8 - np.repeat(z8, G, axis=1)) * np.repeat(s8, G, axis=1)
+    err = np.abs(w16.astype(np.float64) - what)
+    assert np.all(err <= (0.5 + 255 * 2.0 ** -11) * np.repeat(s8, G, axis=1))
+    assert np.all(what[:, 3] == 0.0)                            # exact zeros stay exact
+    assert np.array_equal(oracle.dequant8(q, s, z, N, K, G).astype(np.float64), what)
+    # each stored plane is itself a valid 4-bit layer row (codes and zeros in 0..15)
+    assert np.array_equal(oracle.dequant(q, s, z, N, 2 * K, G)[:, K:].astype(np.float64),
+                          (q8 % 16 - np.repeat(z8 % 16, G, axis=1)) * np.repeat(s8, G, axis=1))
+
+
+def test_pack8_degenerate_groups():
+    G, K = 64, 128
+    w16 = np.zeros((2, K), np.float16)
+    w16[1, G:] = np.float16(2.0 ** -24)                          # range / 255 underflows FP16
+    q, s, z = oracle.pack8(w16, G)
+    q8, z8, s8, _ = _planes(q, s, z, K, G)
+    assert np.all(q8 == 0) and np.all(z8 == 0) and np.all(s8 == 1.0)
+    assert np.all(oracle.dequant8(q, s, z, 2, K, G) == 0.0)
+
+
+@pytest.mark.parametrize("M,N,K,G", [(1, 16, 256, 128), (3, 8, 512, 64), (2, 24, 256, 32)])
+def test_linear8_is_the_4bit_layer_over_both_planes(M, N, K, G):
+    # the same result along the other route: the planes as a 4-bit layer with 2K input
+    # channels, applied to x repeated twice (hi plane meets x, lo plane meets x again)
+    rng = np.random.default_rng(M + N + K)
+    w16 = (rng.standard_normal((N, K)) * 0.05).astype(np.float16)
+    x = _bits(torch.from_numpy(rng.standard_normal((M, K)).astype(np.float32)).to(torch.bfloat16))
+    q, s, z = oracle.pack8(w16, G)
+    y8 = oracle.linear8(x, q, s, z, N, K, G)
+    y4 = oracle.linear(np.concatenate([x, x], axis=1), q, s, z, N, 2 * K, G)
+    assert np.all(np.abs(y8 - y4) <= 1e-12 * np.maximum(1.0, np.abs(y8)))
+
+
+@pytest.mark.parametrize("M,N,Kg,G", [(1, 8, 1, 32), (2, 8, 2, 32), (1, 8, 1, 64)])
+def test_linear8_brute_force_rational(M, N, Kg, G):
+    K = Kg * G
+    rng = np.random.default_rng(M * 11 + N + Kg)
+    w16 = (rng.standard_normal((N, K)) * 0.05).astype(np.float16)
+    x = _bits(torch.from_numpy(rng.standard_normal((M, K)).astype(np.float32)).to(torch.bfloat16))
+    q, s, z = oracle.pack8(w16, G)
+    y = oracle.linear8(x, q, s, z, N, K, G)
+    ng = K // G
+    for m in range(M):
+        for n in range(N):
+            acc = Fraction(0)
+            for k in range(K):
+                g = k // G
+                hi = (int(q[n, k // 8]) >> (4 * (k % 8))) & 0xF
+                lo = (int(q[n, (K + k) // 8]) >> (4 * ((K + k) % 8))) & 0xF
+                zhi = (int(z[n, g // 8]) >> (4 * (g % 8))) & 0xF
+                zlo = (int(z[n, (ng + g) // 8]) >> (4 * ((ng + g) % 8))) & 0xF
+                acc += _frac_bf16(x[m, k]) * ((16 * hi + lo) - (16 * zhi + zlo)) * _frac_f16(s[n, ng + g])
+            ref = float(acc)
+            assert abs(y[m, n] - ref) <= 1e-12 * max(1.0, abs(ref)), (m, n, y[m, n], ref)
+
+
 def test_sampled_equals_full():
     N, K, G = 24, 512, 128
     q, s, z = _random_packed(N, K, G, 10)
