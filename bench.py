@@ -517,8 +517,33 @@ def run_sweep(args):
                      "frac_tensor": round(fl / (us * 1e-6) / 1e12 / pk["bf16_tflops"], 4)})
 
     results = []
-    for name in ("single_4096", "layer13b_decode", "up13b_sweep", "gateup13b_dual", "ffn13b_awq"):
+    for name in ("single_4096", "layer13b_decode", "up13b_sweep", "gateup13b_dual", "ffn13b_awq", "up13b_w8"):
         wk = wl.WORKLOADS[name]
+        if wk.bits == 8:
+            # the 8-bit variant: codes as two 4-bit planes of a 2K-channel layer; the bytes read
+            # are those of that layer (both planes' scales and zeros) with x counted once
+            for j, lin in enumerate(wk.linears):
+                for Gv in wk.Gs:
+                    w = wl.weight_f16(lin.N, lin.K, wk.sigma, wl.matrix_seed(wk, j), wk.outlier_frac).to(dev)
+                    one = gemv_bytes(1, lin.N, 2 * lin.K, Gv)
+                    cps = [w4.w8a16_pack(w, Gv) for _ in range(max(2, -(-2 * l2_bytes // one) + 1))]
+                    del w
+                    for M in wk.Ms:
+                        x = wl.activations_bf16(M, lin.K, wl.act_seed(wk, j)).to(dev)
+                        y = torch.empty(M, lin.N, dtype=torch.bfloat16, device=dev)
+                        fn = lambda i, s: w4.w8a16_linear(x, *cps[i % len(cps)], Gv, out=y, stream=s)
+                        graph = w4.w4a16_linear_path(M, lin.N, 2 * lin.K, Gv) == 1
+                        us = _graph_us(fn, n) if graph else _eager_us(fn, n)
+                        byts = gemv_bytes(M, lin.N, 2 * lin.K, Gv) - M * lin.K * 2
+                        results.append(emit({"sweep": wk.name, "matrix": lin.name, "M": M, "N": lin.N, "K": lin.K,
+                                             "G": Gv, "path": "w8 gemv" if graph else "w8 gemm (eager)",
+                                             "us": round(us, 2), "gbs": round(byts / (us * 1e-6) / 1e9, 1),
+                                             "frac_hbm": round(byts / (us * 1e-6) / 1e9 / pk["hbm_gbs"], 4),
+                                             "tflops": round(gemm_flops(M, lin.N, lin.K) / (us * 1e-6) / 1e12, 2),
+                                             "frac_tensor": round(gemm_flops(M, lin.N, lin.K) / (us * 1e-6) / 1e12
+                                                                  / pk["bf16_tflops"], 4)}))
+                    del cps
+            continue
         if wk.act_scaled:
             # activation scale fused into x staging (the x_scale vector counts as bytes read);
             # the tensor-core path allocates stream-ordered scratch, so M > 8 is timed eagerly

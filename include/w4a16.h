@@ -224,6 +224,35 @@ W4A16_API w4a16_status w4a16_linear_dual_act_scaled(const void* x_bf16, const fl
                                           int64_t K, int G, void* y_gate_bf16, void* y_up_bf16,
                                           w4a16_stream_t stream);
 
+/* ---- the 8-bit variant (W8A16) ---------------------------------------------
+ * The same group-wise asymmetric min-max quantiser with 255 steps:
+ *   s8 = RNE_fp16( fp32(hi - lo) / 255 ); s8 == 0 -> s8 = 1, z8 = 0
+ *   z8 = clamp(rne(-lo / s8), 0, 255),  q8 = clamp(rne(w / s8) + z8, 0, 255)
+ * (weights stored as INT8 or INT4 with 16-bit activations: klaylearn.com
+ * glossary "Weight-Only Quantisation", first FAQ answer).  Storage: each 8-bit
+ * code is kept as two 4-bit planes of a 4-bit layer with 2K input channels,
+ * so the 4-bit kernels compute the 8-bit layer exactly
+ * (16 s8 (q8>>4 - z8>>4) + s8 (q8&15 - z8&15) = s8 (q8 - z8)):
+ *   qweight  uint32 [N, K/4]   row n: the K codes' high nibbles (channels
+ *                              0..K-1) then their low nibbles (K..2K-1), in the
+ *                              4-bit layout (8 bits per weight)
+ *   scales   FP16 [N, ldS8]    the K/G hi-plane scales 16*s8, then the K/G
+ *                              lo-plane scales s8 (ldS8 = w4a16_scales_ld(2K, G))
+ *   zeros    uint32 [N, ldZ8]  z8 >> 4 per group, then z8 & 15 per group, packed
+ *                              as 4-bit zeros of 2K/G groups (ldZ8 = w4a16_zeros_ld(2K, G))
+ * The layout helpers below return K/4, ldS8 and ldZ8.  Preconditions and
+ * errors as for the 4-bit calls; the dispatch is w4a16_linear_path(M, N, 2K, G).
+ */
+W4A16_API int64_t w8a16_qweight_ld(int64_t K);
+W4A16_API int64_t w8a16_scales_ld(int64_t K, int G);
+W4A16_API int64_t w8a16_zeros_ld(int64_t K, int G);
+W4A16_API w4a16_status w8a16_pack(const void* w_f16, int64_t N, int64_t K, int G, uint32_t* qweight,
+                                  void* scales_f16, uint32_t* zeros, w4a16_stream_t stream);
+/* y[M,N] (BF16) = x[M,K] (BF16) * W_hat8^T, FP32 accumulation, one BF16 rounding per output. */
+W4A16_API w4a16_status w8a16_linear(const void* x_bf16, const uint32_t* qweight, const void* scales_f16,
+                                    const uint32_t* zeros, int64_t M, int64_t N, int64_t K, int G,
+                                    void* y_bf16, w4a16_stream_t stream);
+
 /*
  * Which kernel w4a16_linear would run for this shape: 1 = GEMV, 2 = GEMM,
  * 0 = the shape is rejected.  Host-only, no device access.

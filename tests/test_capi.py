@@ -15,7 +15,7 @@ HEADER = os.path.join(ROOT, "include", "w4a16.h")
 
 def declared_symbols():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"W4A16_API\s+[\w\s\*]+?\b(w4a16_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"W4A16_API\s+[\w\s\*]+?\b(w[48]a16_\w+)\s*\(", text)))
 
 
 def test_header_declares_the_boundary():
@@ -35,7 +35,7 @@ def test_library_exports_nothing_else():
     # the build hides everything but the declared C entry points
     out = os.popen(f"nm -D --defined-only {w4.LIB_PATH}").read()
     exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
-    ours = {s for s in exported if s.startswith("w4a16")}
+    ours = {s for s in exported if s.startswith(("w4a16", "w8a16"))}
     assert ours == set(declared_symbols())
 
 
@@ -100,6 +100,24 @@ def test_dual_argument_errors():
     assert f(a, a, a, a, v(0), a, a, 1, 64, 256, 128, a, a, v(0)) == 1
     assert f(a, a, a, a, a, a, a, 1, 64, 256, 128, a, v((1 << 12) + 2), v(0)) == 3
     assert f(a, a, a, a, a, a, a, 0, 64, 256, 128, a, a, v(0)) == 0
+
+
+def test_w8a16_layout_and_argument_errors():
+    for K, G in ((4096, 128), (5120, 32), (13824, 128), (64, 32)):
+        assert w4._lib.w8a16_qweight_ld(K) == K // 4
+        assert w4._lib.w8a16_scales_ld(K, G) == w4.w4a16_scales_ld(2 * K, G)
+        assert w4._lib.w8a16_zeros_ld(K, G) == w4.w4a16_zeros_ld(2 * K, G)
+    v = ctypes.c_void_p
+    a = v(1 << 12)
+    assert w4._lib.w8a16_pack(a, 64, 256, 100, a, a, a, v(0)) == 2
+    assert w4._lib.w8a16_pack(a, 60, 256, 128, a, a, a, v(0)) == 1
+    assert w4._lib.w8a16_pack(v((1 << 12) + 4), 64, 256, 128, a, a, a, v(0)) == 3
+    assert w4._lib.w8a16_pack(a, 0, 256, 128, a, a, a, v(0)) == 0
+    assert _call_linear("w8a16_linear", G=48) == 2
+    assert _call_linear("w8a16_linear", K=200) == 1
+    assert _call_linear("w8a16_linear", x=0) == 1
+    assert _call_linear("w8a16_linear", s=(1 << 12) + 2) == 3
+    assert _call_linear("w8a16_linear", M=0) == 0
 
 
 def test_act_scaled_argument_errors():

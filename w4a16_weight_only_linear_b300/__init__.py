@@ -39,6 +39,11 @@ EXPORTS = {
     "w4a16_linear_gemm": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp], _i32),
     "w4a16_linear_gemm_noalloc": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp], _i32),
     "w4a16_linear_act_scaled": ([_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp], _i32),
+    "w8a16_qweight_ld": ([_i64], _i64),
+    "w8a16_scales_ld": ([_i64, _i32], _i64),
+    "w8a16_zeros_ld": ([_i64, _i32], _i64),
+    "w8a16_pack": ([_vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp], _i32),
+    "w8a16_linear": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp], _i32),
     "w4a16_linear_dual_act_scaled": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp,
                                       _vp], _i32),
     "w4a16_linear_path": ([_i64, _i64, _i64, _i32], _i32),
@@ -232,6 +237,33 @@ def w4a16_linear_dual_act_scaled(x, x_scale, gate, up, G, out=None, stream=None)
         _dev(up[2], torch.int32, "zeros_up"),
         M, N, K, G, _dev(yg, torch.bfloat16, "y_gate"), _dev(yu, torch.bfloat16, "y_up"), _stream(stream)))
     return yg, yu
+
+
+# ---- the 8-bit variant ---------------------------------------------------------
+
+def w8a16_packed_shapes(N, K, G):
+    """Shapes of (qweight int32, scales FP16, zeros int32) of an 8-bit layer."""
+    return (N, _lib.w8a16_qweight_ld(K)), (N, _lib.w8a16_scales_ld(K, G)), (N, _lib.w8a16_zeros_ld(K, G))
+
+
+def w8a16_pack(w, G, out=None, stream=None):
+    """FP16 W [N,K] -> (qweight, scales, zeros) of the 8-bit layer (codes as two
+    4-bit planes; see the header)."""
+    N, K = w.shape
+    if out is None:
+        sq, ss, sz = w8a16_packed_shapes(N, K, G)
+        out = (torch.empty(sq, dtype=torch.int32, device=w.device), torch.empty(ss, dtype=torch.float16, device=w.device),
+               torch.empty(sz, dtype=torch.int32, device=w.device))
+    q, s, z = out
+    _check("w8a16_pack", _lib.w8a16_pack(_dev(w, torch.float16, "w"), N, K, G, _dev(q, torch.int32, "qweight"),
+                                         _dev(s, torch.float16, "scales"), _dev(z, torch.int32, "zeros"),
+                                         _stream(stream)))
+    return q, s, z
+
+
+def w8a16_linear(x, q, s, z, G, out=None, stream=None):
+    """y BF16 [M,N] = x BF16 [M,K] * W_hat8^T."""
+    return _linear("w8a16_linear", x, q, s, z, q.shape[0], G, out, stream)
 
 
 def w4a16_linear_path(M, N, K, G):

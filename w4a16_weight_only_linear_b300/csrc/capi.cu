@@ -55,7 +55,7 @@ int choose_path(int64_t M, int64_t N, int64_t K, int G, int nmat) {
 
 w4a16_status linear_common(const void* x, const uint32_t* q, const void* s, const uint32_t* z, int64_t M,
                            int64_t N, int64_t K, int G, void* y, w4a16_stream_t stream, int force,
-                           const float* xsc = nullptr) {
+                           const float* xsc = nullptr, int64_t kx = 0) {
     w4a16_status st = check_weight_shape(N, K, G);
     if (st != W4A16_OK) return st;
     if (M < 0 || M > kMaxDim) return W4A16_ERR_INVALID_ARG;
@@ -68,9 +68,9 @@ w4a16_status linear_common(const void* x, const uint32_t* q, const void* s, cons
     GemvMat mat{q, s, z, y};
     if (path == 1) {
         if (M > 16 || !w4a16::gemv_fits(M, N, K, G, 1)) return W4A16_ERR_UNSUPPORTED;
-        return from_cuda(w4a16::launch_gemv(x, &mat, 1, M, N, K, G, cs, xsc));
+        return from_cuda(w4a16::launch_gemv(x, &mat, 1, M, N, K, G, cs, xsc, kx));
     }
-    return from_cuda(w4a16::launch_gemm(x, &mat, 1, M, N, K, G, cs, xsc));
+    return from_cuda(w4a16::launch_gemm(x, &mat, 1, M, N, K, G, cs, xsc, kx));
 }
 
 w4a16_status dual_common(const void* x_bf16, const uint32_t* qweight_gate, const void* scales_gate,
@@ -120,6 +120,33 @@ const char* w4a16_status_string(w4a16_status status) {
 int64_t w4a16_qweight_ld(int64_t K) { return w4a16::qweight_ld(K); }
 int64_t w4a16_scales_ld(int64_t K, int G) { return G > 0 ? w4a16::scales_ld(K, G) : 0; }
 int64_t w4a16_zeros_ld(int64_t K, int G) { return G > 0 ? w4a16::zeros_ld(K, G) : 0; }
+
+int64_t w8a16_qweight_ld(int64_t K) { return w4a16::qweight_ld(2 * K); }
+int64_t w8a16_scales_ld(int64_t K, int G) { return G > 0 ? w4a16::scales_ld(2 * K, G) : 0; }
+int64_t w8a16_zeros_ld(int64_t K, int G) { return G > 0 ? w4a16::zeros_ld(2 * K, G) : 0; }
+
+w4a16_status w8a16_pack(const void* w_f16, int64_t N, int64_t K, int G, uint32_t* qweight, void* scales_f16,
+                        uint32_t* zeros, w4a16_stream_t stream) {
+    w4a16_status st = check_weight_shape(N, K, G);
+    if (st != W4A16_OK) return st;
+    if (2 * K > kMaxDim) return W4A16_ERR_INVALID_ARG;
+    if (N == 0) return W4A16_OK;
+    if ((st = check_weights(qweight, scales_f16, zeros)) != W4A16_OK) return st;
+    if (!w_f16) return W4A16_ERR_INVALID_ARG;
+    if (!aligned16(w_f16)) return W4A16_ERR_MISALIGNED;
+    return from_cuda(w4a16::launch_pack8(w_f16, N, K, G, qweight, scales_f16, zeros,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w8a16_linear(const void* x_bf16, const uint32_t* qweight, const void* scales_f16,
+                          const uint32_t* zeros, int64_t M, int64_t N, int64_t K, int G, void* y_bf16,
+                          w4a16_stream_t stream) {
+    w4a16_status st = check_weight_shape(N, K, G);
+    if (st != W4A16_OK) return st;
+    if (2 * K > kMaxDim) return W4A16_ERR_INVALID_ARG;
+    // the two planes are a 4-bit layer of 2K input channels over x repeated twice
+    return linear_common(x_bf16, qweight, scales_f16, zeros, M, N, 2 * K, G, y_bf16, stream, 0, nullptr, K);
+}
 
 w4a16_status w4a16_pack(const void* w_f16, int64_t N, int64_t K, int G, uint32_t* qweight, void* scales_f16,
                         uint32_t* zeros, w4a16_stream_t stream) {

@@ -422,13 +422,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // BF16 -> FP16, round to nearest even (exact for normal-range values).  With a
 // per-input-channel multiplier xsc [K] (null: none), x_k * xsc_k is formed in
-// FP32 and rounded to FP16 once.  kvec = K / 8 vectors per row of x.
+// FP32 and rounded to FP16 once.  The output has kvec = K / 8 vectors per row;
+// the input rows have kxvec = kx / 8, and output channel k reads input channel
+// k mod kx (kx = K, or K / 2 for a layer over x repeated twice).
 __global__ void __launch_bounds__(256) bf16_to_f16_kernel(const uint4* __restrict__ x, uint4* __restrict__ out,
                                                           int64_t nvec, const float4* __restrict__ xsc,
-                                                          int64_t kvec) {
+                                                          int64_t kvec, int64_t kxvec) {
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
-        const uint4 v = x[i];
+        int64_t src = i, kv = 0;                 // input vector; its channel vector (when needed)
+        if (kxvec != kvec || xsc != nullptr) {
+            const int64_t m = i / kvec;
+            kv = i - m * kvec;
+            kv -= kv >= kxvec ? kxvec : 0;
+            src = m * kxvec + kv;
+        }
+        const uint4 v = x[src];
         const uint32_t in[4] = {v.x, v.y, v.z, v.w};
         float f[8];
 #pragma unroll
@@ -437,7 +446,6 @@ __global__ void __launch_bounds__(256) bf16_to_f16_kernel(const uint4* __restric
             f[2 * j + 1] = bf16hi_to_f32(in[j]);
         }
         if (xsc != nullptr) {
-            const int64_t kv = i % kvec;
             const float4 s0 = xsc[2 * kv], s1 = xsc[2 * kv + 1];
             f[0] *= s0.x; f[1] *= s0.y; f[2] *= s0.z; f[3] *= s0.w;
             f[4] *= s1.x; f[5] *= s1.y; f[6] *= s1.z; f[7] *= s1.w;
@@ -536,7 +544,9 @@ cudaError_t launch_g(const CUtensorMap& tmx, const CUtensorMap& tmq, const GemmP
 int gemm_tile_n(int64_t M) { return M >= 256 ? 256 : (int)((M + 31) / 32 * 32); }
 
 cudaError_t launch_gemm(const void* x, const GemvMat* mats, int nmat, int64_t M, int64_t N, int64_t K, int G,
-                        cudaStream_t stream, const float* xsc) {
+                        cudaStream_t stream, const float* xsc, int64_t kx) {
+    if (kx == 0) kx = K;
+    if (kx != K && (kx * 2 != K || kx % 8 != 0)) return cudaErrorInvalidValue;
     if (M < 1 || N < 1 || K < 1) return cudaSuccess;
     if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX || K % 32 != 0) return cudaErrorInvalidValue;
     if (!tensor_map_encoder()) return cudaErrorNotSupported;
@@ -555,7 +565,7 @@ cudaError_t launch_gemm(const void* x, const GemvMat* mats, int nmat, int64_t M,
         if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
         bf16_to_f16_kernel<<<(unsigned)blocks, 256, 0, stream>>>(static_cast<const uint4*>(x),
                                                                  static_cast<uint4*>(x16), nvec,
-                                                                 reinterpret_cast<const float4*>(xsc), K / 8);
+                                                                 reinterpret_cast<const float4*>(xsc), K / 8, kx / 8);
         e = cudaGetLastError();
     }
     GemmParams p;
@@ -652,7 +662,7 @@ cudaError_t launch_gemm_noalloc(const void* x, const GemvMat& mat, int64_t M, in
         int64_t blocks = (nvec + 255) / 256;
         if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
         bf16_to_f16_kernel<<<(unsigned)blocks, 256, 0, stream>>>(static_cast<const uint4*>(x),
-                                                                 static_cast<uint4*>(x16), nvec, nullptr, K / 8);
+                                                                 static_cast<uint4*>(x16), nvec, nullptr, K / 8, K / 8);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     GemmParams p;

@@ -80,6 +80,7 @@ __device__ __forceinline__ int sigma8(int i) { return (i >> 1) + ((i & 1) << 2);
 struct GemvParams {
     const __nv_bfloat16* x;                // [M, K]
     const float* xsc;                      // per-input-channel multiplier of x [K], or null
+    int kx;                                // row length of x: channel k reads x[k mod kx] (kx = K or K/2)
     const unsigned short* s[2];            // FP16 scales [N, lds]
     const uint32_t* z[2];                  // zeros [N, ldz]
     __nv_bfloat16* y[2];                   // [M, N]
@@ -351,8 +352,11 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
                 vv[j] = make_uint4(0u, 0u, 0u, 0u);
                 const int pseg = (int)(((uint32_t)bxc[j] * minv) >> 16), m = bxc[j] - pseg * M;
                 const int wseg = bc[j] * 32 + lane;
-                if (bxc[j] < xcols && wseg * 8 < kseg)
-                    vv[j] = *reinterpret_cast<const uint4*>(p.x + (int64_t)m * p.K + (int64_t)pseg * kseg + wseg * 8);
+                if (bxc[j] < xcols && wseg * 8 < kseg) {
+                    int kk = pseg * kseg + wseg * 8;       // channel of the layer (< 2 kx)
+                    kk -= kk >= p.kx ? p.kx : 0;
+                    vv[j] = *reinterpret_cast<const uint4*>(p.x + (int64_t)m * p.kx + kk);
+                }
             }
         };
         auto x_stage = [&]() {
@@ -374,7 +378,9 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
                     f[2 * q + 1] = bf16hi_to_f32(in[q]);
                 }
                 if (p.xsc != nullptr && wseg * 8 < kseg) {  // activation scale: x_k * xsc_k in FP32
-                    const float4* sp = reinterpret_cast<const float4*>(p.xsc + (int64_t)pseg * kseg + wseg * 8);
+                    int kk = pseg * kseg + wseg * 8;
+                    kk -= kk >= p.kx ? p.kx : 0;
+                    const float4* sp = reinterpret_cast<const float4*>(p.xsc + kk);
                     const float4 s0 = sp[0], s1 = sp[1];
                     f[0] *= s0.x; f[1] *= s0.y; f[2] *= s0.z; f[3] *= s0.w;
                     f[4] *= s1.x; f[5] *= s1.y; f[6] *= s1.z; f[7] *= s1.w;
@@ -977,7 +983,9 @@ bool gemv_fits(int64_t M, int64_t N, int64_t K, int G, int nmat) {
 }
 
 cudaError_t launch_gemv(const void* x, const GemvMat* mats, int nmat, int64_t M, int64_t N, int64_t K, int G,
-                        cudaStream_t stream, const float* xsc) {
+                        cudaStream_t stream, const float* xsc, int64_t kx) {
+    if (kx == 0) kx = K;
+    if (kx != K && (kx * 2 != K || kx % 8 != 0)) return cudaErrorInvalidValue;
     const int sms = device_sms();
     if (sms <= 0) return cudaErrorNoDevice;
     const size_t cap = device_smem_optin();
@@ -986,6 +994,7 @@ cudaError_t launch_gemv(const void* x, const GemvMat* mats, int nmat, int64_t M,
     GemvParams& p = pl.p;
     p.x = static_cast<const __nv_bfloat16*>(x);
     p.xsc = xsc;
+    p.kx = (int)kx;
     CUtensorMap tm[2];
     for (int i = 0; i < 2; ++i) {
         const GemvMat& mt = mats[i < nmat ? i : 0];

@@ -8,6 +8,9 @@ namespace w4a16 {
 
 cudaError_t launch_pack(const void* w, int64_t N, int64_t K, int G, uint32_t* qw, void* sc, uint32_t* zr,
                         cudaStream_t stream);
+// The 8-bit packer: codes as two 4-bit planes of a 2K-channel 4-bit layer (see pack.cu).
+cudaError_t launch_pack8(const void* w, int64_t N, int64_t K, int G, uint32_t* qw, void* sc, uint32_t* zr,
+                         cudaStream_t stream);
 cudaError_t launch_dequant(const uint32_t* qw, const void* sc, const uint32_t* zr, int64_t N, int64_t K, int G,
                            float* out, cudaStream_t stream);
 
@@ -27,13 +30,15 @@ size_t device_smem_optin();
 
 // y_i = x * W_hat_i^T for one matrix (nmat = 1) or two matrices sharing x (nmat = 2).
 // xsc (optional, FP32 [K], 16-byte aligned): x_k is taken as x_k * xsc_k.
+// kx (optional, 0 = K): row length of x; input channel k of the layer reads x[k mod kx]
+// (the two-plane 8-bit layer is a 4-bit layer of K = 2 kx channels over x repeated).
 cudaError_t launch_gemv(const void* x, const GemvMat* mats, int nmat, int64_t M, int64_t N, int64_t K, int G,
-                        cudaStream_t stream, const float* xsc = nullptr);
+                        cudaStream_t stream, const float* xsc = nullptr, int64_t kx = 0);
 
 // Tensor-core path (any M): y_i = x * W_hat_i^T for nmat matrices sharing x
 // (x is converted to FP16 once, into stream-ordered scratch).
 cudaError_t launch_gemm(const void* x, const GemvMat* mats, int nmat, int64_t M, int64_t N, int64_t K, int G,
-                        cudaStream_t stream, const float* xsc = nullptr);
+                        cudaStream_t stream, const float* xsc = nullptr, int64_t kx = 0);
 // The same tensor-core path for one matrix with the FP16 copy of x in a
 // fixed-size file-scope device array (no allocation; M * K bounded by the
 // header's W4A16_NOALLOC_MAX_X_ELEMS, else cudaErrorNotSupported).

@@ -17,6 +17,50 @@
 
 namespace w4a16 {
 
+// The PER consecutive FP16 weights at src (PER = 1, 2, 4 or 8; src aligned to
+// PER halves) as floats.
+template <int PER>
+__device__ __forceinline__ void load_weights(const __half* src, float (&v)[PER]) {
+    if constexpr (PER == 8) {
+        uint4 u = *reinterpret_cast<const uint4*>(src);
+        const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[2 * i] = __half2float(__ushort_as_half((unsigned short)(uw[i] & 0xFFFF)));
+            v[2 * i + 1] = __half2float(__ushort_as_half((unsigned short)(uw[i] >> 16)));
+        }
+    } else if constexpr (PER == 4) {
+        uint2 u = *reinterpret_cast<const uint2*>(src);
+        v[0] = __half2float(__ushort_as_half((unsigned short)(u.x & 0xFFFF)));
+        v[1] = __half2float(__ushort_as_half((unsigned short)(u.x >> 16)));
+        v[2] = __half2float(__ushort_as_half((unsigned short)(u.y & 0xFFFF)));
+        v[3] = __half2float(__ushort_as_half((unsigned short)(u.y >> 16)));
+    } else if constexpr (PER == 2) {
+        uint32_t u = *reinterpret_cast<const uint32_t*>(src);
+        v[0] = __half2float(__ushort_as_half((unsigned short)(u & 0xFFFF)));
+        v[1] = __half2float(__ushort_as_half((unsigned short)(u >> 16)));
+    } else {
+        v[0] = __half2float(src[0]);
+    }
+}
+
+// Range of a group over the warp: lo = min(0, min w), hi = max(0, max w).
+template <int PER>
+__device__ __forceinline__ void group_range(const float (&v)[PER], float& lo, float& hi) {
+    lo = 0.0f;
+    hi = 0.0f;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        lo = fminf(lo, v[i]);
+        hi = fmaxf(hi, v[i]);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        lo = fminf(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, off));
+        hi = fmaxf(hi, __shfl_xor_sync(0xFFFFFFFFu, hi, off));
+    }
+}
+
 // One warp per weight row; the row's groups are processed in order.  Lane l
 // holds the G/32 consecutive weights l*G/32 .. of the current group.
 template <int G>
@@ -36,40 +80,10 @@ __global__ void __launch_bounds__(256) pack_kernel(const __half* __restrict__ w,
 
     uint32_t zword = 0;
     for (int64_t g = 0; g < ngroups; ++g) {
-        const __half* src = wrow + g * G + lane * PER;
         float v[PER];
-        if constexpr (PER == 8) {
-            uint4 u = *reinterpret_cast<const uint4*>(src);
-            const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                v[2 * i] = __half2float(__ushort_as_half((unsigned short)(uw[i] & 0xFFFF)));
-                v[2 * i + 1] = __half2float(__ushort_as_half((unsigned short)(uw[i] >> 16)));
-            }
-        } else if constexpr (PER == 4) {
-            uint2 u = *reinterpret_cast<const uint2*>(src);
-            v[0] = __half2float(__ushort_as_half((unsigned short)(u.x & 0xFFFF)));
-            v[1] = __half2float(__ushort_as_half((unsigned short)(u.x >> 16)));
-            v[2] = __half2float(__ushort_as_half((unsigned short)(u.y & 0xFFFF)));
-            v[3] = __half2float(__ushort_as_half((unsigned short)(u.y >> 16)));
-        } else if constexpr (PER == 2) {
-            uint32_t u = *reinterpret_cast<const uint32_t*>(src);
-            v[0] = __half2float(__ushort_as_half((unsigned short)(u & 0xFFFF)));
-            v[1] = __half2float(__ushort_as_half((unsigned short)(u >> 16)));
-        } else {
-            v[0] = __half2float(src[0]);
-        }
-        float lo = 0.0f, hi = 0.0f;
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            lo = fminf(lo, v[i]);
-            hi = fmaxf(hi, v[i]);
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            lo = fminf(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, off));
-            hi = fmaxf(hi, __shfl_xor_sync(0xFFFFFFFFu, hi, off));
-        }
+        load_weights<PER>(wrow + g * G + lane * PER, v);
+        float lo, hi;
+        group_range<PER>(v, lo, hi);
         const float range = __fsub_rn(hi, lo);
         __half sh = __float2half_rn(__fdiv_rn(range, 15.0f));
         float s = __half2float(sh);
@@ -100,6 +114,75 @@ __global__ void __launch_bounds__(256) pack_kernel(const __half* __restrict__ w,
     }
     for (int64_t i = ngroups + lane; i < lds; i += 32) srow[i] = __ushort_as_half((unsigned short)0);
     for (int64_t i = (ngroups + 7) / 8 + lane; i < ldz; i += 32) zrow[i] = 0u;
+}
+
+// The 8-bit variant: 255 steps, s8 = RNE_fp16((hi - lo) / 255), z8 and codes in
+// 0..255.  Each 8-bit code is stored as two 4-bit planes of a 4-bit layer with
+// 2K input channels: the row's K high nibbles (channels 0..K-1), then its K low
+// nibbles (channels K..2K-1); scales 16*s8 (hi plane groups) then s8 (lo plane
+// groups); zeros z8 >> 4 then z8 & 15.  The 4-bit kernels then compute the
+// 8-bit layer exactly: 16 s8 (q_hi - z_hi) + s8 (q_lo - z_lo) = s8 (q8 - z8).
+template <int G>
+__global__ void __launch_bounds__(256) pack8_kernel(const __half* __restrict__ w, int64_t N, int64_t K,
+                                                    uint32_t* __restrict__ qw, __half* __restrict__ sc,
+                                                    uint32_t* __restrict__ zr) {
+    constexpr int PER = G / 32;
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    if (row >= N) return;                    // uniform per warp
+    const int64_t ngroups = K / G, K2 = 2 * K;
+    const int64_t ldq = qweight_ld(K2), lds = scales_ld(K2, G), ldz = zeros_ld(K2, G);
+    const __half* wrow = w + row * K;
+    uint32_t* qrow = qw + row * ldq;
+    __half* srow = sc + row * lds;
+    uint32_t* zrow = zr + row * ldz;
+    // zero words may hold nibbles of both planes (when K/G is not a multiple of 8): lane 0
+    // clears the row's words, then ORs each group's two nibbles in
+    if (lane == 0)
+        for (int64_t i = 0; i < ldz; ++i) zrow[i] = 0u;
+    for (int64_t g = 0; g < ngroups; ++g) {
+        float v[PER];
+        load_weights<PER>(wrow + g * G + lane * PER, v);
+        float lo, hi;
+        group_range<PER>(v, lo, hi);
+        const float range = __fsub_rn(hi, lo);
+        __half sh = __float2half_rn(__fdiv_rn(range, 255.0f));
+        float s = __half2float(sh);
+        int zp = 0;
+        if (s == 0.0f) {
+            sh = __float2half_rn(1.0f);
+            s = 1.0f;
+        } else {
+            zp = min(max(__float2int_rn(__fdiv_rn(-lo, s)), 0), 255);
+        }
+        uint32_t bh = 0, bl = 0;               // this lane's hi and lo nibbles, at their word positions
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int c = min(max(__float2int_rn(__fdiv_rn(v[i], s)) + zp, 0), 255);
+            const int sh4 = 4 * ((lane * PER + i) & 7);
+            bh |= (uint32_t)(c >> 4) << sh4;
+            bl |= (uint32_t)(c & 15) << sh4;
+        }
+        if constexpr (PER < 8) {
+#pragma unroll
+            for (int off = 1; off < 8 / PER; off <<= 1) {
+                bh |= __shfl_xor_sync(0xFFFFFFFFu, bh, off);
+                bl |= __shfl_xor_sync(0xFFFFFFFFu, bl, off);
+            }
+        }
+        if (((lane * PER) & 7) == 0) {
+            const int64_t k = g * G + lane * PER;                 // K and G are multiples of 8
+            qrow[k / 8] = bh;
+            qrow[(K + k) / 8] = bl;
+        }
+        if (lane == 0) {
+            srow[g] = __float2half_rn(16.0f * s);                 // exact: a power-of-two scaling
+            srow[ngroups + g] = sh;
+            atomicOr(zrow + g / 8, (uint32_t)(zp >> 4) << (4 * (g & 7)));
+            atomicOr(zrow + (ngroups + g) / 8, (uint32_t)(zp & 15) << (4 * ((ngroups + g) & 7)));
+        }
+    }
+    for (int64_t i = 2 * ngroups + lane; i < lds; i += 32) srow[i] = __ushort_as_half((unsigned short)0);
 }
 
 // W_hat = (q - z) * s through the same in-register nibble expansion the
@@ -141,6 +224,23 @@ cudaError_t launch_pack(const void* w, int64_t N, int64_t K, int G, uint32_t* qw
         case 64: pack_kernel<64><<<grid, block, 0, stream>>>(wp, N, K, qw, sp, zr); break;
         case 128: pack_kernel<128><<<grid, block, 0, stream>>>(wp, N, K, qw, sp, zr); break;
         case 256: pack_kernel<256><<<grid, block, 0, stream>>>(wp, N, K, qw, sp, zr); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pack8(const void* w, int64_t N, int64_t K, int G, uint32_t* qw, void* sc, uint32_t* zr,
+                         cudaStream_t stream) {
+    const int warps = 8;
+    const dim3 block(32 * warps);
+    const dim3 grid((unsigned)((N + warps - 1) / warps));
+    const __half* wp = static_cast<const __half*>(w);
+    __half* sp = static_cast<__half*>(sc);
+    switch (G) {
+        case 32: pack8_kernel<32><<<grid, block, 0, stream>>>(wp, N, K, qw, sp, zr); break;
+        case 64: pack8_kernel<64><<<grid, block, 0, stream>>>(wp, N, K, qw, sp, zr); break;
+        case 128: pack8_kernel<128><<<grid, block, 0, stream>>>(wp, N, K, qw, sp, zr); break;
+        case 256: pack8_kernel<256><<<grid, block, 0, stream>>>(wp, N, K, qw, sp, zr); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

@@ -46,6 +46,7 @@ class Workload:
     seed: int
     dual: bool = False
     act_scaled: bool = False     # layer with a per-input-channel activation scale
+    bits: int = 4                # weight code width: 4, or 8 (the W8A16 variant)
 
 
 WORKLOADS = {
@@ -66,6 +67,8 @@ WORKLOADS = {
     # 13B FFN with an activation scale fused into x staging (salient channels 1 %)
     "ffn13b_awq": Workload("ffn13b_awq", (Linear("gate", 5120, 13824), Linear("down", 13824, 5120)),
                            (1, 4, 32), (128,), 0.02, 0.0, 5, act_scaled=True),
+    # the 8-bit variant on the 13B up-projection, decode and a small batch
+    "up13b_w8": Workload("up13b_w8", (Linear("up", 5120, 13824),), (1, 4, 32), (128,), 0.02, 0.0, 6, bits=8),
     # 70B-shaped FFN gate and down, decode (M=1) and prefill (M=2048)
     "ffn70b": Workload("ffn70b", (Linear("gate", 8192, 28672), Linear("down", 28672, 8192)), (1, 2048),
                        (128,), 0.015, 0.0, 4),
