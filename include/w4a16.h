@@ -39,6 +39,10 @@
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is
  *     enqueued asynchronously; results are valid once the stream reaches the
  *     point of the call.  Calls on distinct streams may run concurrently.
+ *   - The decode kernel is launched with programmatic stream serialisation:
+ *     it may begin (initialise its barriers) while the previous kernel on the
+ *     stream finishes, but it reads and writes no global memory before that
+ *     kernel has completed, so stream order keeps its usual meaning.
  *   - Errors in arguments are reported before anything is launched, as a
  *     status code; no entry point aborts, throws, traps or asserts.  A CUDA
  *     launch error is reported as W4A16_ERR_CUDA.
