@@ -97,6 +97,24 @@ def stored_traffic(kernel, key):
     return d.get("dram_bytes_per_launch")
 
 
+def max_over_ranks(values, device):
+    """Elementwise maximum of a list of floats over all ranks of the process
+    group (the list itself when there is no group or a single rank): every
+    per-phase time of the job is the slowest rank's."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_gbs(bytes_per_rank_step, steps, ms, world):
+    """Whole-job GB/s: the bytes all `world` ranks moved in `steps` steps over
+    the slowest rank's time `ms` (milliseconds)."""
+    return world * bytes_per_rank_step * steps / (ms * 1e-3) / 1e9
+
+
 class ClockSampler:
     """nvidia-smi clock/throttle samples during the timed region."""
 
@@ -239,17 +257,15 @@ def run_ours(args):
             evs[k][1].record(stream)
         t1.record(stream)
         torch.cuda.synchronize()
-    total_ms = t0.elapsed_time(t1)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-        torch.distributed.barrier()
-
+    # every time below is the slowest rank's
     dec_ms = [evs[("dec", j)][0].elapsed_time(evs[("dec", j)][1]) for j in range(len(mats))]
-    pre_ms = [evs[("pre", j)][0].elapsed_time(evs[("pre", j)][1]) for j in range(len(mats))] if gemm_ok else None
+    pre_ms = [evs[("pre", j)][0].elapsed_time(evs[("pre", j)][1]) for j in range(len(mats))] if gemm_ok else []
+    times = max_over_ranks([t0.elapsed_time(t1)] + dec_ms + pre_ms, dev)
+    total_ms, dec_ms, pre_ms = times[0], times[1:1 + len(mats)], (times[1 + len(mats):] if gemm_ok else None)
+    if world > 1:
+        torch.distributed.barrier()
     dec_bytes = [gemv_bytes(M_DECODE, lin.N, lin.K, G) for lin, _ in mats]
-    dec_gbs = world * sum(dec_bytes) * args.steps / (sum(dec_ms) * 1e-3) / 1e9
+    dec_gbs = job_gbs(sum(dec_bytes), args.steps, sum(dec_ms), world)
     out = {
         "metric": METRIC, "value": round(dec_gbs, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
@@ -331,9 +347,10 @@ def e2e_ours(w4, mats, dev, args, gemm_ok):
     run(3)
     t = time.perf_counter()
     run(steps)
-    dt = time.perf_counter() - t
+    dt_ms = max_over_ranks([(time.perf_counter() - t) * 1e3], dev)[0]      # the slowest rank's
+    world = int(os.environ.get("WORLD_SIZE", "1"))
     byts = sum(gemv_bytes(M_DECODE, lin.N, lin.K, G) for lin, _ in mats)
-    return {"value": round(byts * steps / dt / 1e9, 1), "unit": "GB/s",
+    return {"value": round(job_gbs(byts, steps, dt_ms, world), 1), "unit": "GB/s",
             "h2d_bytes_per_step": sum(h.numel() * 2 for h in hx),
             "d2h_bytes_per_step": sum(h.numel() * 2 for h in hy),
             "scope": "decode GEMVs (M=1) of the step, host wall clock, pinned buffers"}
