@@ -53,6 +53,19 @@ def _load():
         lib.oracle_linear8.restype = None
         lib.oracle_linear_xs.argtypes = [p, p, p, p, p, i64, i64, i64, i64, p, i32]
         lib.oracle_linear_xs.restype = None
+        lib.oracle_q4k_meta_ld.argtypes, lib.oracle_q4k_meta_ld.restype = [i64], i64
+        lib.oracle_q4k_quantize_superblock.argtypes = [p, p, p, p, p, p]
+        lib.oracle_q4k_quantize_superblock.restype = None
+        lib.oracle_q4k_pack.argtypes = [p, i64, i64, p, p, i32]
+        lib.oracle_q4k_pack.restype = i32
+        lib.oracle_q4k_record.argtypes = [p, i64, i64, i64, p, p, p, p]
+        lib.oracle_q4k_record.restype = None
+        lib.oracle_q4k_dequant.argtypes = [p, p, i64, i64, p, i32]
+        lib.oracle_q4k_dequant.restype = None
+        lib.oracle_q4k_linear.argtypes = [p, p, p, i64, i64, i64, p, i32]
+        lib.oracle_q4k_linear.restype = None
+        lib.oracle_q4k_linear_sampled.argtypes = [p, p, p, i64, p, p, i64, p, i32]
+        lib.oracle_q4k_linear_sampled.restype = None
         lib.oracle_max_threads.argtypes, lib.oracle_max_threads.restype = [], i32
         _lib = lib
     return _lib
@@ -257,6 +270,79 @@ def linear8(x_bf16: np.ndarray, q, s, z, N: int, K: int, G: int, nthreads: int =
     z = np.ascontiguousarray(z, dtype=np.uint32)
     y = np.zeros((M, N), np.float64)
     _load().oracle_linear8(_ptr(x), _ptr(q), _ptr(s), _ptr(z), M, N, K, G, _ptr(y), nthreads)
+    return y
+
+
+# ---- the super-block (Q4_K-style) variant ----------------------------------------
+
+def q4k_meta_ld(K: int) -> int:
+    """uint32 words per row of the super-block records (4 per 256 channels)."""
+    return _load().oracle_q4k_meta_ld(K)
+
+
+def q4k_quantize_superblock(w: np.ndarray):
+    """256 FP32 weights -> (d bits, dmin bits, sc[8], m[8], q[256])."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    assert w.shape == (256,)
+    db, dmb = np.zeros(1, np.uint16), np.zeros(1, np.uint16)
+    sc, m = np.zeros(8, np.int32), np.zeros(8, np.int32)
+    q = np.zeros(256, np.uint8)
+    _load().oracle_q4k_quantize_superblock(_ptr(w), _ptr(db), _ptr(dmb), _ptr(sc), _ptr(m), _ptr(q))
+    return int(db[0]), int(dmb[0]), sc, m, q
+
+
+def q4k_pack(w_f16: np.ndarray, nthreads: int = 0):
+    """FP16 [N,K] -> (qweight u32 [N, K/8], meta u32 [N, K/256*4])."""
+    w = _u16(w_f16)
+    N, K = w.shape
+    q = np.zeros((N, qweight_ld(K)), np.uint32)
+    meta = np.zeros((N, max(q4k_meta_ld(K), 1)), np.uint32)
+    rc = _load().oracle_q4k_pack(_ptr(w), N, K, _ptr(q), _ptr(meta), nthreads)
+    if rc != 0:
+        raise ValueError("oracle_q4k_pack: K must be a positive multiple of 256")
+    return q, meta
+
+
+def q4k_record(meta, K: int, n: int, sb: int):
+    """(d, dmin, sc[8], m[8]) of super-block sb of row n, read back from its record."""
+    meta = np.ascontiguousarray(meta, dtype=np.uint32)
+    d, dmin = ctypes.c_float(), ctypes.c_float()
+    sc, m = np.zeros(8, np.int32), np.zeros(8, np.int32)
+    _load().oracle_q4k_record(_ptr(meta), K, n, sb, ctypes.byref(d), ctypes.byref(dmin), _ptr(sc), _ptr(m))
+    return d.value, dmin.value, sc, m
+
+
+def q4k_dequant(q, meta, N: int, K: int, nthreads: int = 0) -> np.ndarray:
+    """W_hat [N,K] FP32 = d*sc_j*q - dmin*m_j."""
+    q = np.ascontiguousarray(q, dtype=np.uint32)
+    meta = np.ascontiguousarray(meta, dtype=np.uint32)
+    out = np.zeros((N, K), np.float32)
+    _load().oracle_q4k_dequant(_ptr(q), _ptr(meta), N, K, _ptr(out), nthreads)
+    return out
+
+
+def q4k_linear(x_bf16: np.ndarray, q, meta, N: int, K: int, nthreads: int = 0) -> np.ndarray:
+    """y_ref [M,N] FP64 = x * W_hat^T, unrounded."""
+    x = _u16(x_bf16)
+    M = x.shape[0]
+    assert x.shape[1] == K
+    q = np.ascontiguousarray(q, dtype=np.uint32)
+    meta = np.ascontiguousarray(meta, dtype=np.uint32)
+    y = np.zeros((M, N), np.float64)
+    _load().oracle_q4k_linear(_ptr(x), _ptr(q), _ptr(meta), M, N, K, _ptr(y), nthreads)
+    return y
+
+
+def q4k_linear_sampled(x_bf16: np.ndarray, q, meta, K: int, ms, ns, nthreads: int = 0) -> np.ndarray:
+    """y_ref[ms[i], ns[i]] (FP64) for a list of outputs."""
+    x = _u16(x_bf16)
+    q = np.ascontiguousarray(q, dtype=np.uint32)
+    meta = np.ascontiguousarray(meta, dtype=np.uint32)
+    ms = np.ascontiguousarray(ms, dtype=np.int64)
+    ns = np.ascontiguousarray(ns, dtype=np.int64)
+    y = np.zeros(len(ms), np.float64)
+    _load().oracle_q4k_linear_sampled(_ptr(x), _ptr(q), _ptr(meta), K, _ptr(ms), _ptr(ns), len(ms), _ptr(y),
+                                      nthreads)
     return y
 
 

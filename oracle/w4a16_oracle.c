@@ -513,6 +513,210 @@ void oracle_linear8(const uint16_t* x_bf16, const uint32_t* qweight, const uint1
     (void)nthreads;
 }
 
+/* ------------------------------------------------------------------------ */
+/* The super-block variant (Q4_K-style K-quant).                              */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * K-quants keep 4-bit codes in 256-weight super-blocks whose sub-blocks carry
+ * their own scale and minimum, and those scales are themselves quantised
+ * against per-super-block factors (zhuai.tech "Quantization Is Not a Zip
+ * File", section 3 "The core idea: local structure, not global rounding",
+ * table "How to read common GGUF quantization names", K-quants row and the
+ * note on hierarchical K-quant scales; section 2 "Moving fewer bytes can make
+ * decode faster" on packed Q4_K decode dot products).
+ *
+ * Readings where the pages are silent:
+ *  - A super-block is 256 consecutive input channels of one output row, cut
+ *    into 8 sub-blocks of 32.  Sub-block j reconstructs as
+ *        W_hat = a'_j * q - b'_j,   a'_j = d * sc_j,   b'_j = dmin * m_j,
+ *    with q in [0, 15], 6-bit codes sc_j, m_j in [0, 63], and FP16 factors
+ *    d, dmin per super-block.  a'_j and b'_j are exact in FP32 (11 + 6
+ *    significant bits), so is a'_j * q (17 + 4); W_hat rounds once, at the
+ *    FP32 subtraction.
+ *  - Quantiser (min-max, no search), all decisions in IEEE binary32:
+ *        lo_j = min(0, min w), hi_j = max(0, max w)   (range holds 0)
+ *        a_j = (hi_j - lo_j) / 15,  b_j = -lo_j
+ *        d = RNE_fp16(max_j a_j / 63),  dmin = RNE_fp16(max_j b_j / 63)
+ *        d == 0 -> d = 1.0;  sc_j = clamp(rne(a_j / d), 0, 63)
+ *        dmin == 0 -> m_j = 0, else m_j = clamp(rne(b_j / dmin), 0, 63)
+ *        q = a'_j > 0 ? clamp(rne((w + b'_j) / a'_j), 0, 15) : 0
+ *  - Storage: qweight as the 4-bit layer ([N, K/8] words, low nibble first);
+ *    meta [N, K/256 * 4] words, one 16-byte record per super-block:
+ *        word 0: d bits (low half), dmin bits (high half)
+ *        word 1: sc_j & 15 at bits 4j..4j+3
+ *        word 2: m_j & 15 at bits 4j..4j+3
+ *        word 3: sc_j >> 4 at bits 2j..2j+1, m_j >> 4 at bits 16+2j..17+2j
+ *    4.5 bits per weight.  K must be a multiple of 256.
+ */
+int64_t oracle_q4k_meta_ld(int64_t K) { return K / 256 * 4; }
+
+/* Quantise one super-block of 256 FP32 weights: FP16 bits of d and dmin, the
+ * 8 sub-block codes sc[] and m[], and 256 codes q[]. */
+void oracle_q4k_quantize_superblock(const float* w, uint16_t* d_bits, uint16_t* dmin_bits, int* sc, int* m,
+                                    uint8_t* q)
+{
+    float a[8], b[8], amax = 0.0f, bmax = 0.0f;
+    for (int j = 0; j < 8; ++j) {
+        float lo = 0.0f, hi = 0.0f;
+        for (int i = 0; i < 32; ++i) {
+            float v = w[32 * j + i];
+            if (v < lo) lo = v;
+            if (v > hi) hi = v;
+        }
+        volatile float range = hi - lo;
+        volatile float aj = range / 15.0f;
+        a[j] = aj;
+        b[j] = -lo;
+        if (a[j] > amax) amax = a[j];
+        if (b[j] > bmax) bmax = b[j];
+    }
+    volatile float dq = amax / 63.0f, dmq = bmax / 63.0f;
+    uint16_t db = oracle_f32_to_f16(dq), dmb = oracle_f32_to_f16(dmq);
+    float d = oracle_f16_to_f32(db), dmin = oracle_f16_to_f32(dmb);
+    if (d == 0.0f) {
+        db = 0x3C00;
+        d = 1.0f;
+    }
+    for (int j = 0; j < 8; ++j) {
+        volatile float ts = a[j] / d;
+        sc[j] = (int)clamp_i64((int64_t)nearbyintf(ts), 0, 63);
+        if (dmin == 0.0f) {
+            m[j] = 0;
+        } else {
+            volatile float tm = b[j] / dmin;
+            m[j] = (int)clamp_i64((int64_t)nearbyintf(tm), 0, 63);
+        }
+        float ap = d * (float)sc[j], bp = dmin * (float)m[j];      /* exact products */
+        for (int i = 0; i < 32; ++i) {
+            if (ap > 0.0f) {
+                volatile float sum = w[32 * j + i] + bp;
+                volatile float t = sum / ap;
+                q[32 * j + i] = (uint8_t)clamp_i64((int64_t)nearbyintf(t), 0, 15);
+            } else {
+                q[32 * j + i] = 0;
+            }
+        }
+    }
+    *d_bits = db;
+    *dmin_bits = dmb;
+}
+
+/* Pack an [N,K] FP16 weight into qweight [N, K/8] and meta [N, K/256*4]. */
+int oracle_q4k_pack(const uint16_t* w_f16, int64_t N, int64_t K, uint32_t* qweight, uint32_t* meta, int nthreads)
+{
+    if (N <= 0 || K <= 0 || K % 256 != 0) return -1;
+    const int64_t ldq = oracle_qweight_ld(K);
+    const int64_t ldm = oracle_q4k_meta_ld(K);
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(static)
+#endif
+    for (int64_t n = 0; n < N; ++n) {
+        float wf[256];
+        uint8_t codes[256];
+        int sc[8], m[8];
+        uint32_t* qrow = qweight + n * ldq;
+        uint32_t* mrow = meta + n * ldm;
+        for (int64_t i = 0; i < ldq; ++i) qrow[i] = 0;
+        for (int64_t i = 0; i < ldm; ++i) mrow[i] = 0;
+        for (int64_t sb = 0; sb < K / 256; ++sb) {
+            for (int i = 0; i < 256; ++i) wf[i] = oracle_f16_to_f32(w_f16[n * K + sb * 256 + i]);
+            uint16_t db, dmb;
+            oracle_q4k_quantize_superblock(wf, &db, &dmb, sc, m, codes);
+            uint32_t* rec = mrow + sb * 4;
+            rec[0] = (uint32_t)db | ((uint32_t)dmb << 16);
+            for (int j = 0; j < 8; ++j) {
+                rec[1] |= (uint32_t)(sc[j] & 15) << (4 * j);
+                rec[2] |= (uint32_t)(m[j] & 15) << (4 * j);
+                rec[3] |= (uint32_t)(sc[j] >> 4) << (2 * j);
+                rec[3] |= (uint32_t)(m[j] >> 4) << (16 + 2 * j);
+            }
+            for (int i = 0; i < 256; ++i) {
+                int64_t k = sb * 256 + i;
+                qrow[k / 8] |= (uint32_t)codes[i] << (4 * (k % 8));
+            }
+        }
+    }
+    (void)nthreads;
+    return 0;
+}
+
+/* The 6-bit codes of sub-block j and the factors of super-block sb, read back from the record. */
+void oracle_q4k_record(const uint32_t* meta, int64_t K, int64_t n, int64_t sb, float* d, float* dmin, int* sc,
+                       int* m)
+{
+    const uint32_t* rec = meta + n * oracle_q4k_meta_ld(K) + sb * 4;
+    *d = oracle_f16_to_f32((uint16_t)(rec[0] & 0xFFFF));
+    *dmin = oracle_f16_to_f32((uint16_t)(rec[0] >> 16));
+    for (int j = 0; j < 8; ++j) {
+        sc[j] = (int)(((rec[1] >> (4 * j)) & 15) | (((rec[3] >> (2 * j)) & 3) << 4));
+        m[j] = (int)(((rec[2] >> (4 * j)) & 15) | (((rec[3] >> (16 + 2 * j)) & 3) << 4));
+    }
+}
+
+/* W_hat[n][k] = (d * sc_j) * q - dmin * m_j in FP32 (the two products exact, one rounding). */
+float oracle_q4k_dequant_one(const uint32_t* qweight, const uint32_t* meta, int64_t K, int64_t n, int64_t k)
+{
+    float d, dmin;
+    int sc[8], m[8];
+    oracle_q4k_record(meta, K, n, k / 256, &d, &dmin, sc, m);
+    const int j = (int)((k % 256) / 32);
+    const int q = oracle_code(qweight, K, n, k);
+    volatile float ap = d * (float)sc[j];
+    volatile float bp = dmin * (float)m[j];
+    volatile float t = ap * (float)q;                  /* exact: at most 17 + 4 significant bits */
+    return t - bp;
+}
+
+void oracle_q4k_dequant(const uint32_t* qweight, const uint32_t* meta, int64_t N, int64_t K, float* w_out,
+                        int nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(static)
+#endif
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k) w_out[n * K + k] = oracle_q4k_dequant_one(qweight, meta, K, n, k);
+    (void)nthreads;
+}
+
+/* y_ref[m][n] = sum_k (double)x[m][k] * (double)W_hat[n][k], FP64 in increasing k, unrounded. */
+double oracle_q4k_linear_one(const uint16_t* x_bf16, const uint32_t* qweight, const uint32_t* meta, int64_t K,
+                             int64_t m, int64_t n)
+{
+    double acc = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        double xv = (double)oracle_bf16_to_f32(x_bf16[m * K + k]);
+        double wv = (double)oracle_q4k_dequant_one(qweight, meta, K, n, k);
+        acc += xv * wv;
+    }
+    return acc;
+}
+
+void oracle_q4k_linear(const uint16_t* x_bf16, const uint32_t* qweight, const uint32_t* meta, int64_t M,
+                       int64_t N, int64_t K, double* y_out, int nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t m = 0; m < M; ++m) y_out[m * N + n] = oracle_q4k_linear_one(x_bf16, qweight, meta, K, m, n);
+    (void)nthreads;
+}
+
+void oracle_q4k_linear_sampled(const uint16_t* x_bf16, const uint32_t* qweight, const uint32_t* meta, int64_t K,
+                               const int64_t* ms, const int64_t* ns, int64_t count, double* y_out, int nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int64_t i = 0; i < count; ++i) y_out[i] = oracle_q4k_linear_one(x_bf16, qweight, meta, K, ms[i], ns[i]);
+    (void)nthreads;
+}
+
 int oracle_max_threads(void)
 {
 #ifdef _OPENMP

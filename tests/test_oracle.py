@@ -482,3 +482,165 @@ def test_bf16_output_rounding_is_rne():
     got = np.array([oracle.f64_to_bf16(float(v)) for v in vals], np.uint16)
     assert np.array_equal(got, ref)
     assert math.isclose(oracle.bf16_to_f32(0x3F80), 1.0)
+
+
+# --------------------------------------------------------------------------
+# The super-block (Q4_K-style) variant
+# --------------------------------------------------------------------------
+
+def _q4k_superblock_weights(d, dmin, sc, m, rng):
+    """256 weights on the grid of (d, dmin, sc, m): sub-block j holds d*sc_j*q - dmin*m_j for q = 0..15
+    (each code twice, in a random order), computed exactly in FP64."""
+    w = np.zeros(256, np.float64)
+    codes = np.zeros(256, np.int64)
+    for j in range(8):
+        q = rng.permutation(np.tile(np.arange(16), 2))
+        codes[32 * j:32 * j + 32] = q
+        w[32 * j:32 * j + 32] = d * sc[j] * q - dmin * m[j]
+    return w, codes
+
+
+def test_q4k_golden_record():
+    """The packer writes the hand-derived record, and the record reads back to the same factors and codes."""
+    gd = _golden("q4k_record.json")
+    d, dmin = oracle.f16_to_f32(_h(gd["d_bits"])), oracle.f16_to_f32(_h(gd["dmin_bits"]))
+    w, codes = _q4k_superblock_weights(d, dmin, gd["sc"], gd["m"], np.random.default_rng(5))
+    w16 = w.astype(np.float16)
+    assert np.array_equal(w16.astype(np.float64), w)          # the example is exact in FP16
+    q, meta = oracle.q4k_pack(w16.reshape(1, 256))
+    assert [int(v) for v in meta[0]] == [_h(s) for s in gd["words"]]
+    assert np.array_equal(oracle.unpack_codes(q, 256)[0], codes)
+    dd, dm, sc, m = oracle.q4k_record(meta, 256, 0, 0)
+    assert (dd, dm) == (d, dmin)
+    assert list(sc) == gd["sc"] and list(m) == gd["m"]
+    assert np.array_equal(oracle.q4k_dequant(q, meta, 1, 256)[0].astype(np.float64), w)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_q4k_on_grid_round_trip(seed):
+    """Weights on a super-block's grid (any FP16 d, dmin; sc and m spanning 0..63 with 63 present, and
+    15 d sc_j >= dmin m_j so each sub-block's range is [-dmin m_j, 15 d sc_j - dmin m_j]) come back exactly:
+    factors, 6-bit codes and 4-bit codes."""
+    rng = np.random.default_rng(100 + seed)
+    d = float(np.float16(rng.uniform(1e-4, 1e-2)))
+    dmin = float(np.float16(rng.uniform(1e-4, 1e-2)))
+    sc = rng.integers(1, 64, 8)
+    sc[rng.integers(8)] = 63
+    m = np.array([min(63, int(rng.integers(0, 64))) for _ in range(8)])
+    m[rng.integers(8)] = 63
+    for j in range(8):                                          # keep 0 inside the sub-block's range
+        while 15 * d * sc[j] < dmin * m[j]:
+            sc[j] += 1
+    sc = np.minimum(sc, 63)
+    assert all(15 * d * sc[j] >= dmin * m[j] for j in range(8))
+    w, codes = _q4k_superblock_weights(d, dmin, sc, m, rng)
+    w32 = w.astype(np.float32)            # d*sc*q is exact in FP32; the subtraction may round
+    db, dmb, sc_o, m_o, q_o = oracle.q4k_quantize_superblock(w32)
+    assert oracle.f16_to_f32(db) == d and oracle.f16_to_f32(dmb) == dmin
+    assert np.array_equal(sc_o, sc) and np.array_equal(m_o, m)
+    assert np.array_equal(q_o.astype(np.int64), codes)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_q4k_error_bounds(seed):
+    """Hierarchical step: the stored sub-block scale and minimum are within d/2 and dmin/2 of the sub-block's
+    own min-max values (6-bit codes of FP16 factors that are the maxima over 63).  Reconstruction: a weight
+    inside the stored range [-b'_j, 15 a'_j - b'_j] is within a'_j / 2 of its reconstruction; one outside is
+    clamped to the nearer end."""
+    rng = np.random.default_rng(200 + seed)
+    scale = [0.02, 1.0, 3e-3, 40.0][seed]
+    w = (rng.standard_normal(256) * scale).astype(np.float16).astype(np.float32)
+    w[rng.integers(256)] *= 6.0                                  # an outlier in one sub-block
+    db, dmb, sc, m, q = oracle.q4k_quantize_superblock(w)
+    d, dmin = oracle.f16_to_f32(db), oracle.f16_to_f32(dmb)
+    for j in range(8):
+        blk = w[32 * j:32 * j + 32].astype(np.float64)
+        lo, hi = min(0.0, blk.min()), max(0.0, blk.max())
+        a, b = (hi - lo) / 15, -lo
+        ap, bp = d * sc[j], dmin * m[j]
+        assert abs(ap - a) <= d / 2 * (1 + 1e-3) + 1e-7 * a, (j, ap, a, d)
+        assert abs(bp - b) <= dmin / 2 * (1 + 1e-3) + 1e-7 * b, (j, bp, b, dmin)
+        rec = ap * q[32 * j:32 * j + 32] - bp
+        for v, r in zip(blk, rec):
+            if -bp <= v <= 15 * ap - bp:
+                assert abs(v - r) <= ap / 2 * (1 + 1e-5) + 1e-7 * abs(v), (j, v, r, ap)
+            else:
+                assert r == (-bp if v < -bp else 15 * ap - bp)
+
+
+def test_q4k_degenerate_superblocks():
+    """All-zero super-block: d = 1, dmin = 0, every code 0, W_hat = 0.  A zero sub-block amid others
+    reconstructs as exact zeros.  A super-block without negative weights stores dmin = 0 and m = 0."""
+    z = np.zeros(256, np.float32)
+    db, dmb, sc, m, q = oracle.q4k_quantize_superblock(z)
+    assert (db, dmb) == (0x3C00, 0) and not sc.any() and not m.any() and not q.any()
+    rng = np.random.default_rng(7)
+    w = (rng.standard_normal(256) * 0.02).astype(np.float16)
+    w[64:96] = 0
+    q, meta = oracle.q4k_pack(w.reshape(1, 256))
+    wh = oracle.q4k_dequant(q, meta, 1, 256)[0]
+    assert not wh[64:96].any()
+    pos = np.abs(w).reshape(1, 256)
+    q, meta = oracle.q4k_pack(pos)
+    dd, dm, sc, m = oracle.q4k_record(meta, 256, 0, 0)
+    assert dm == 0.0 and not m.any()
+    with pytest.raises(ValueError):
+        oracle.q4k_pack(np.zeros((2, 384), np.float16))
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 4, 256), (2, 3, 512)])
+def test_q4k_brute_force_rational(M, N, K):
+    """y = sum_k x * (d sc_j q - dmin m_j), the fields decoded here from the record definition and summed
+    in exact rationals; the oracle's FP32 W_hat rounds once (relative 2^-24 per weight)."""
+    rng = np.random.default_rng(M * 100 + N + K)
+    w16 = (rng.standard_normal((N, K)) * 0.05).astype(np.float16)
+    xb = torch.from_numpy(rng.standard_normal((M, K)).astype(np.float32)).to(torch.bfloat16)
+    x = xb.view(torch.int16).numpy().view(np.uint16)
+    q, meta = oracle.q4k_pack(w16)
+    y = oracle.q4k_linear(x, q, meta, N, K)
+    for n in range(N):
+        for mm in range(M):
+            acc, mag = Fraction(0), 0.0
+            for k in range(K):
+                rec = [int(v) for v in meta[n, (k // 256) * 4:(k // 256) * 4 + 4]]
+                j = (k % 256) // 32
+                sc = ((rec[1] >> (4 * j)) & 15) | (((rec[3] >> (2 * j)) & 3) << 4)
+                mj = ((rec[2] >> (4 * j)) & 15) | (((rec[3] >> (16 + 2 * j)) & 3) << 4)
+                code = (int(q[n, k // 8]) >> (4 * (k % 8))) & 0xF
+                wv = _frac_f16(rec[0] & 0xFFFF) * sc * code - _frac_f16(rec[0] >> 16) * mj
+                acc += _frac_bf16(x[mm, k]) * wv
+                mag += abs(float(_frac_bf16(x[mm, k]) * wv))
+            ref = float(acc)
+            assert abs(y[mm, n] - ref) <= 2 ** -23 * mag + 1e-12, (mm, n, y[mm, n], ref)
+
+
+def test_q4k_linear_matches_dequant_then_matmul_and_sampling():
+    rng = np.random.default_rng(11)
+    N, K, M = 37, 768, 3
+    w16 = (rng.standard_normal((N, K)) * 0.02).astype(np.float16)
+    xb = torch.from_numpy(rng.standard_normal((M, K)).astype(np.float32)).to(torch.bfloat16)
+    x = xb.view(torch.int16).numpy().view(np.uint16)
+    q, meta = oracle.q4k_pack(w16)
+    y = oracle.q4k_linear(x, q, meta, N, K)
+    wh = oracle.q4k_dequant(q, meta, N, K).astype(np.float64)
+    ref = xb.float().numpy().astype(np.float64) @ wh.T
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-12)
+    # one-hot x picks a column of W_hat
+    e = np.zeros((1, K), np.uint16)
+    e[0, 300] = 0x3F80                                           # BF16 1.0
+    assert np.array_equal(oracle.q4k_linear(e, q, meta, N, K)[0], wh[:, 300])
+    ms, ns = np.array([0, 2, 1, 2]), np.array([0, 36, 17, 5])
+    assert np.array_equal(oracle.q4k_linear_sampled(x, q, meta, K, ms, ns), y[ms, ns])
+
+
+def test_q4k_bits_per_weight_and_70b_size():
+    """4 bits per code plus one 16-byte record per 256 weights: 4.5 bits per weight.  The pages put a 70B
+    model at about 35 GB in an ideal 4-bit encoding and note that real Q4_K files are larger because block
+    scales and minima take space (zhuai.tech, section 2 'Capacity comes first')."""
+    cf = _golden("closed_forms.json")["model_70b_bytes"]
+    N, K = 4, 1024
+    q, meta = oracle.q4k_pack(np.zeros((N, K), np.float16))
+    bpw = (q.nbytes + meta.nbytes) * 8 / (N * K)
+    assert bpw == 4.5
+    gb = cf["params"] * bpw / 8 / 1e9
+    assert gb > cf["int4_gb"] and round(gb, 2) == 39.38
