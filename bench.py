@@ -61,6 +61,12 @@ def gemv_bytes(M, N, K, G):
     return N * K // 2 + N * (K // G) * 2 + N * (K // G) // 2 + M * K * 2 + M * N * 2
 
 
+def q4k_bytes(M, N, K):
+    """Algorithmic bytes of one decode launch on the super-block layout: codes
+    (K/2 per row), one 16-byte record per 256 channels, x and y in BF16."""
+    return N * K // 2 + N * (K // 256) * 16 + M * K * 2 + M * N * 2
+
+
 def gemm_flops(M, N, K):
     return 2.0 * M * N * K
 
@@ -442,20 +448,26 @@ def run_profile(args):
     ~122 MB of packed weights, above L2), `warmup` + 2 calls of one phase, no
     timing and no CPU leg."""
     import w4a16_weight_only_linear_b300 as w4
-    wk = wl.WORKLOADS[WORKLOAD]
+    q4k = args.format == "q4k"
+    if q4k and args.profile != "decode":
+        raise SystemExit("--format q4k profiles the decode kernel only")
+    wk = wl.WORKLOADS["ffn70b_q4k" if q4k else WORKLOAD]
     lin = wk.linears[int(args.matrix)]
     w = wl.weight_f16(lin.N, lin.K, wk.sigma, wl.matrix_seed(wk, int(args.matrix)), wk.outlier_frac).cuda()
-    packed = w4.w4a16_pack(w, G)
+    packed = w4.q4k_pack(w) if q4k else w4.w4a16_pack(w, G)
     del w
     M = M_DECODE if args.profile == "decode" else M_PREFILL
     x = wl.activations_bf16(M, lin.K, wl.act_seed(wk, int(args.matrix))).cuda()
     y = torch.empty(M, lin.N, dtype=torch.bfloat16, device="cuda")
     for _ in range(args.warmup + 2):
-        w4.w4a16_linear(x, *packed, G, out=y)
+        if q4k:
+            w4.q4k_linear(x, *packed, out=y)
+        else:
+            w4.w4a16_linear(x, *packed, G, out=y)
     torch.cuda.synchronize()
     assert w4.w4a16_device_status() == 0
-    print(json.dumps({"profile": args.profile, "matrix": lin.name, "M": M, "N": lin.N, "K": lin.K, "G": G,
-                      "calls": args.warmup + 2}))
+    print(json.dumps({"profile": args.profile, "format": args.format, "matrix": lin.name, "M": M, "N": lin.N,
+                      "K": lin.K, "G": 32 if q4k else G, "calls": args.warmup + 2}))
 
 
 # ---------------------------------------------------------------------------
@@ -544,8 +556,52 @@ def run_sweep(args):
                      "frac_tensor": round(fl / (us * 1e-6) / 1e12 / pk["bf16_tflops"], 4)})
 
     results = []
-    for name in ("single_4096", "layer13b_decode", "up13b_sweep", "gateup13b_dual", "ffn13b_awq", "up13b_w8"):
+    names = ("single_4096", "layer13b_decode", "up13b_sweep", "gateup13b_dual", "ffn13b_awq", "up13b_w8",
+             "ffn70b_q4k")
+    if args.only:
+        names = tuple(nm for nm in names if nm in args.only.split(","))
+    for name in names:
         wk = wl.WORKLOADS[name]
+        if wk.q4k:
+            # the super-block layout (decode kernel only), beside the 4-bit G = 32 layer of the
+            # same weights, and the gate projection paired with a second matrix of its shape
+            def q4k_rec(lin, M, path, us, nmat=1):
+                byts = nmat * q4k_bytes(M, lin.N, lin.K) - (nmat - 1) * M * lin.K * 2
+                return emit({"sweep": wk.name, "matrix": lin.name if nmat == 1 else "gate+up", "M": M, "N": lin.N,
+                             "K": lin.K, "G": 32, "path": path, "us": round(us, 2),
+                             "gbs": round(byts / (us * 1e-6) / 1e9, 1),
+                             "frac_hbm": round(byts / (us * 1e-6) / 1e9 / pk["hbm_gbs"], 4)})
+            dual = []
+            for j, lin in enumerate(wk.linears):
+                w = wl.weight_f16(lin.N, lin.K, wk.sigma, wl.matrix_seed(wk, j), wk.outlier_frac).to(dev)
+                copies = max(2, -(-2 * l2_bytes // q4k_bytes(1, lin.N, lin.K)) + 1)
+                cps = [w4.q4k_pack(w) for _ in range(copies)]
+                g32 = [w4.w4a16_pack(w, 32) for _ in range(copies)]
+                del w
+                for M in wk.Ms:
+                    x = wl.activations_bf16(M, lin.K, wl.act_seed(wk, j)).to(dev)
+                    y = torch.empty(M, lin.N, dtype=torch.bfloat16, device=dev)
+                    us = _graph_us(lambda i, s: w4.q4k_linear(x, *cps[i % copies], out=y, stream=s), n)
+                    results.append(q4k_rec(lin, M, "q4k gemv", us))
+                    if w4.w4a16_linear_path(M, lin.N, lin.K, 32) == 1:      # where the 4-bit GEMV takes it
+                        us = _graph_us(lambda i, s: w4.w4a16_linear_gemv(x, *g32[i % copies], 32, out=y, stream=s), n)
+                        results.append(record(wk, lin, M, 32, "w4 g32 gemv", us))
+                del g32
+                if j == 0:
+                    dual.append(cps)
+                    w2 = wl.weight_f16(lin.N, lin.K, wk.sigma, wl.matrix_seed(wk, 2), wk.outlier_frac).to(dev)
+                    dual.append([w4.q4k_pack(w2) for _ in range(copies)])
+                    del w2
+                    for M in wk.Ms:
+                        x = wl.activations_bf16(M, lin.K, wl.act_seed(wk, j)).to(dev)
+                        yg = torch.empty(M, lin.N, dtype=torch.bfloat16, device=dev)
+                        yu = torch.empty(M, lin.N, dtype=torch.bfloat16, device=dev)
+                        us = _graph_us(lambda i, s: w4.q4k_linear_dual(x, dual[0][i % copies], dual[1][i % copies],
+                                                                       out=(yg, yu), stream=s), n)
+                        results.append(q4k_rec(lin, M, "q4k dual", us, nmat=2))
+                    dual = []
+                del cps
+            continue
         if wk.bits == 8:
             # the 8-bit variant: codes as two 4-bit planes of a 2K-channel layer; the bytes read
             # are those of that layer (both planes' scales and zeros) with x counted once
@@ -662,12 +718,15 @@ def main():
     ap.add_argument("--profile", choices=["decode", "prefill"], default=None,
                     help="small case for ncu: one matrix, warmup + 2 calls of one phase")
     ap.add_argument("--matrix", choices=["0", "1"], default="0", help="with --profile: 0 = gate, 1 = down")
+    ap.add_argument("--format", choices=["w4", "q4k"], default="w4",
+                    help="with --profile decode: the 4-bit group layout or the super-block layout")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--sweep", action="store_true",
                     help="time the other workloads (decode layers, batch x group sweep, dual) instead")
+    ap.add_argument("--only", default="", help="with --sweep: comma-separated workload names to time")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

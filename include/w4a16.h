@@ -257,6 +257,47 @@ W4A16_API w4a16_status w8a16_linear(const void* x_bf16, const uint32_t* qweight,
                                     const uint32_t* zeros, int64_t M, int64_t N, int64_t K, int G,
                                     void* y_bf16, w4a16_stream_t stream);
 
+/* ---- the super-block variant (Q4_K-style) ------------------------------------
+ * K-quants keep 4-bit codes in 256-weight super-blocks whose sub-blocks carry
+ * their own scale and minimum, quantised in turn against per-super-block
+ * factors (zhuai.tech "Quantization Is Not a Zip File", section 3, table "How
+ * to read common GGUF quantization names", K-quants row; section 2 "Moving
+ * fewer bytes can make decode faster" on packed Q4_K decode dot products and
+ * the paired gate/up traversal).  A super-block is 256 consecutive input
+ * channels of one row, cut into 8 sub-blocks of 32; sub-block j reconstructs
+ * as  W_hat = d*sc_j*q - dmin*m_j  with q in [0,15], 6-bit sc_j, m_j and FP16
+ * d, dmin.  Quantiser (min-max per sub-block, range widened to hold 0, all
+ * decisions in IEEE binary32):
+ *   a_j = (hi - lo) / 15, b_j = -lo;  d = RNE_fp16(max a_j / 63) (0 -> 1),
+ *   dmin = RNE_fp16(max b_j / 63);  sc_j = clamp(rne(a_j / d), 0, 63),
+ *   m_j = dmin == 0 ? 0 : clamp(rne(b_j / dmin), 0, 63),
+ *   q = d*sc_j > 0 ? clamp(rne((w + dmin*m_j) / (d*sc_j)), 0, 15) : 0
+ * Storage (4.5 bits per weight):
+ *   qweight  uint32 [N, K/8]         the codes in the 4-bit layout
+ *   meta     uint32 [N, K/256 * 4]   one 16-byte record per super-block:
+ *            word 0 = d bits | dmin bits << 16;  word 1 = sc_j & 15 at bit 4j;
+ *            word 2 = m_j & 15 at bit 4j;  word 3 = sc_j >> 4 at bit 2j and
+ *            m_j >> 4 at bit 16 + 2j
+ * Preconditions: K a positive multiple of 256, N a multiple of 8, every
+ * pointer 16-byte aligned (W4A16_ERR_INVALID_ARG / W4A16_ERR_MISALIGNED).
+ * The layer runs the decode kernel: up to 8 activation rows per launch, as
+ * many as its shared memory holds for this K (x staged as M*K FP16); larger M
+ * is split into row blocks, each of which reads the weights again.
+ * W4A16_ERR_UNSUPPORTED if not even one row fits (K beyond about 90k).
+ */
+W4A16_API int64_t q4k_meta_ld(int64_t K);   /* uint32 words per meta row: K/256*4 (0 if K % 256) */
+W4A16_API w4a16_status q4k_pack(const void* w_f16, int64_t N, int64_t K, uint32_t* qweight, uint32_t* meta,
+                                w4a16_stream_t stream);
+/* y[M,N] (BF16) = x[M,K] (BF16) * W_hat^T, FP32 accumulation, one BF16 rounding per output. */
+W4A16_API w4a16_status q4k_linear(const void* x_bf16, const uint32_t* qweight, const uint32_t* meta, int64_t M,
+                                  int64_t N, int64_t K, void* y_bf16, w4a16_stream_t stream);
+/* Two matrices of the same shape sharing x (gate and up projections) in one launch per row block, or
+ * one launch per matrix where the pair's super-block records do not fit a CTA's shared memory (at
+ * N = 28672, K = 8192 for instance). */
+W4A16_API w4a16_status q4k_linear_dual(const void* x_bf16, const uint32_t* qweight_gate, const uint32_t* meta_gate,
+                                       const uint32_t* qweight_up, const uint32_t* meta_up, int64_t M, int64_t N,
+                                       int64_t K, void* y_gate_bf16, void* y_up_bf16, w4a16_stream_t stream);
+
 /*
  * Which kernel w4a16_linear would run for this shape: 1 = GEMV, 2 = GEMM,
  * 0 = the shape is rejected.  Host-only, no device access.

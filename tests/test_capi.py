@@ -15,7 +15,7 @@ HEADER = os.path.join(ROOT, "include", "w4a16.h")
 
 def declared_symbols():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"W4A16_API\s+[\w\s\*]+?\b(w[48]a16_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"W4A16_API\s+[\w\s\*]+?\b((?:w[48]a16|q4k)_\w+)\s*\(", text)))
 
 
 def test_header_declares_the_boundary():
@@ -35,7 +35,7 @@ def test_library_exports_nothing_else():
     # the build hides everything but the declared C entry points
     out = os.popen(f"nm -D --defined-only {w4.LIB_PATH}").read()
     exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
-    ours = {s for s in exported if s.startswith(("w4a16", "w8a16"))}
+    ours = {s for s in exported if s.startswith(("w4a16", "w8a16", "q4k"))}
     assert ours == set(declared_symbols())
 
 
@@ -118,6 +118,35 @@ def test_w8a16_layout_and_argument_errors():
     assert _call_linear("w8a16_linear", x=0) == 1
     assert _call_linear("w8a16_linear", s=(1 << 12) + 2) == 3
     assert _call_linear("w8a16_linear", M=0) == 0
+
+
+def test_q4k_layout_and_argument_errors():
+    for K in (256, 4096, 8192, 28672):
+        assert w4._lib.q4k_meta_ld(K) == K // 256 * 4
+    assert w4._lib.q4k_meta_ld(384) == 0 and w4._lib.q4k_meta_ld(0) == 0
+    assert w4.q4k_packed_shapes(64, 512) == ((64, 64), (64, 8))
+    v = ctypes.c_void_p
+    a = v(1 << 12)
+    p = w4._lib.q4k_pack
+    assert p(a, 64, 384, a, a, v(0)) == 1                      # K % 256
+    assert p(a, 60, 256, a, a, v(0)) == 1                      # N % 8
+    assert p(a, 64, 256, a, v(0), v(0)) == 1                   # null meta
+    assert p(v((1 << 12) + 2), 64, 256, a, a, v(0)) == 3       # misaligned w
+    assert p(a, 64, 256, a, v((1 << 12) + 4), v(0)) == 3       # misaligned meta
+    assert p(a, 0, 256, a, a, v(0)) == 0                       # empty
+    f = w4._lib.q4k_linear
+    assert f(a, a, a, 1, 64, 384, a, v(0)) == 1
+    assert f(a, a, a, 1, 60, 256, a, v(0)) == 1
+    assert f(a, a, a, -1, 64, 256, a, v(0)) == 1
+    assert f(v(0), a, a, 1, 64, 256, a, v(0)) == 1
+    assert f(a, v((1 << 12) + 8), a, 1, 64, 256, a, v(0)) == 3
+    assert f(a, a, a, 1, 64, 256, v((1 << 12) + 2), v(0)) == 3
+    assert f(a, a, a, 0, 64, 256, a, v(0)) == 0
+    d = w4._lib.q4k_linear_dual
+    assert d(a, a, a, a, v(0), 1, 64, 256, a, a, v(0)) == 1
+    assert d(a, a, a, a, a, 1, 64, 512 + 128, a, a, v(0)) == 1
+    assert d(a, a, a, a, a, 1, 64, 256, a, v((1 << 12) + 2), v(0)) == 3
+    assert d(a, a, a, a, a, 0, 64, 256, a, a, v(0)) == 0
 
 
 def test_act_scaled_argument_errors():

@@ -46,6 +46,10 @@ EXPORTS = {
     "w8a16_linear": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp], _i32),
     "w4a16_linear_dual_act_scaled": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp,
                                       _vp], _i32),
+    "q4k_meta_ld": ([_i64], _i64),
+    "q4k_pack": ([_vp, _i64, _i64, _vp, _vp, _vp], _i32),
+    "q4k_linear": ([_vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp], _i32),
+    "q4k_linear_dual": ([_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp, _vp], _i32),
     "w4a16_linear_path": ([_i64, _i64, _i64, _i32], _i32),
     "w4a16_device_status": ([_vp], _i32),
 }
@@ -264,6 +268,50 @@ def w8a16_pack(w, G, out=None, stream=None):
 def w8a16_linear(x, q, s, z, G, out=None, stream=None):
     """y BF16 [M,N] = x BF16 [M,K] * W_hat8^T."""
     return _linear("w8a16_linear", x, q, s, z, q.shape[0], G, out, stream)
+
+
+def q4k_packed_shapes(N, K):
+    """Shapes of (qweight int32, meta int32) of a super-block (Q4_K-style) layer."""
+    return (N, _lib.w4a16_qweight_ld(K)), (N, _lib.q4k_meta_ld(K))
+
+
+def q4k_pack(w, out=None, stream=None):
+    """FP16 W [N,K] (K a multiple of 256) -> (qweight, meta) of the super-block layout."""
+    N, K = w.shape
+    if out is None:
+        sq, sm = q4k_packed_shapes(N, K)
+        out = (torch.empty(sq, dtype=torch.int32, device=w.device), torch.empty(sm, dtype=torch.int32, device=w.device))
+    q, meta = out
+    _check("q4k_pack", _lib.q4k_pack(_dev(w, torch.float16, "w"), N, K, _dev(q, torch.int32, "qweight"),
+                                     _dev(meta, torch.int32, "meta"), _stream(stream)))
+    return q, meta
+
+
+def q4k_linear(x, q, meta, out=None, stream=None):
+    """y BF16 [M,N] = x BF16 [M,K] * W_hat^T for the super-block layout (N from qweight's rows)."""
+    M, K = x.shape
+    N = q.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _check("q4k_linear", _lib.q4k_linear(_dev(x, torch.bfloat16, "x"), _dev(q, torch.int32, "qweight"),
+                                         _dev(meta, torch.int32, "meta"), M, N, K, _dev(out, torch.bfloat16, "y"),
+                                         _stream(stream)))
+    return out
+
+
+def q4k_linear_dual(x, gate, up, out=None, stream=None):
+    """(y_gate, y_up) for two super-block matrices sharing x; gate/up = (qweight, meta)."""
+    M, K = x.shape
+    N = gate[0].shape[0]
+    if out is None:
+        out = (torch.empty((M, N), dtype=torch.bfloat16, device=x.device),
+               torch.empty((M, N), dtype=torch.bfloat16, device=x.device))
+    yg, yu = out
+    _check("q4k_linear_dual", _lib.q4k_linear_dual(
+        _dev(x, torch.bfloat16, "x"), _dev(gate[0], torch.int32, "qweight_gate"), _dev(gate[1], torch.int32, "meta_gate"),
+        _dev(up[0], torch.int32, "qweight_up"), _dev(up[1], torch.int32, "meta_up"), M, N, K,
+        _dev(yg, torch.bfloat16, "y_gate"), _dev(yu, torch.bfloat16, "y_up"), _stream(stream)))
+    return yg, yu
 
 
 def w4a16_linear_path(M, N, K, G):

@@ -100,6 +100,55 @@ w4a16_status check_act_scale(const float* x_scale) {
     return W4A16_OK;
 }
 
+// The super-block layout: K a positive multiple of 256, N a multiple of 8.
+w4a16_status check_q4k_shape(int64_t N, int64_t K) {
+    if (N < 0 || K <= 0 || N > kMaxDim || K > kMaxDim) return W4A16_ERR_INVALID_ARG;
+    if (K % 256 != 0 || N % 8 != 0) return W4A16_ERR_INVALID_ARG;
+    return W4A16_OK;
+}
+
+w4a16_status check_q4k_weights(const uint32_t* q, const uint32_t* meta) {
+    if (!q || !meta) return W4A16_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(meta)) return W4A16_ERR_MISALIGNED;
+    return W4A16_OK;
+}
+
+// The super-block layer for nmat matrices sharing x: the decode kernel over row blocks of
+// up to 8 activation rows (as many as its shared memory holds at this K).
+w4a16_status q4k_common(const void* x, const uint32_t* const* q, const uint32_t* const* meta, void* const* y,
+                        int nmat, int64_t M, int64_t N, int64_t K, w4a16_stream_t stream) {
+    w4a16_status st = check_q4k_shape(N, K);
+    if (st != W4A16_OK) return st;
+    if (M < 0 || M > kMaxDim) return W4A16_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return W4A16_OK;
+    for (int i = 0; i < nmat; ++i) {
+        if ((st = check_q4k_weights(q[i], meta[i])) != W4A16_OK) return st;
+        if (!y[i]) return W4A16_ERR_INVALID_ARG;
+        if (!aligned16(y[i])) return W4A16_ERR_MISALIGNED;
+    }
+    if (!x) return W4A16_ERR_INVALID_ARG;
+    if (!aligned16(x)) return W4A16_ERR_MISALIGNED;
+    int64_t mb = M < 8 ? M : 8;
+    while (mb >= 1 && !w4a16::gemv_fits(mb, N, K, 32, nmat, true)) --mb;
+    if (mb < 1 && nmat == 2) {
+        // a pair holds twice the rows per CTA; where their records do not fit, one launch per matrix
+        for (int i = 0; i < 2; ++i)
+            if ((st = q4k_common(x, q + i, meta + i, y + i, 1, M, N, K, stream)) != W4A16_OK) return st;
+        return W4A16_OK;
+    }
+    if (mb < 1) return W4A16_ERR_UNSUPPORTED;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const auto* xb = static_cast<const uint16_t*>(x);
+    for (int64_t m0 = 0; m0 < M; m0 += mb) {
+        const int64_t mr = M - m0 < mb ? M - m0 : mb;
+        GemvMat mats[2];
+        for (int i = 0; i < nmat; ++i) mats[i] = {q[i], meta[i], nullptr, static_cast<uint16_t*>(y[i]) + m0 * N};
+        const cudaError_t e = w4a16::launch_gemv(xb + m0 * K, mats, nmat, mr, N, K, 32, cs, nullptr, 0, true);
+        if (e != cudaSuccess) return from_cuda(e);
+    }
+    return W4A16_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -232,6 +281,33 @@ w4a16_status w4a16_linear_gemm_noalloc(const void* x_bf16, const uint32_t* qweig
     if (M * K > (int64_t)W4A16_NOALLOC_MAX_X_ELEMS) return W4A16_ERR_UNSUPPORTED;
     const GemvMat mat{qweight, scales_f16, zeros, y_bf16};
     return from_cuda(w4a16::launch_gemm_noalloc(x_bf16, mat, M, N, K, G, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int64_t q4k_meta_ld(int64_t K) { return K > 0 && K % 256 == 0 ? K / 256 * 4 : 0; }
+
+w4a16_status q4k_pack(const void* w_f16, int64_t N, int64_t K, uint32_t* qweight, uint32_t* meta,
+                      w4a16_stream_t stream) {
+    w4a16_status st = check_q4k_shape(N, K);
+    if (st != W4A16_OK) return st;
+    if (N == 0) return W4A16_OK;
+    if ((st = check_q4k_weights(qweight, meta)) != W4A16_OK) return st;
+    if (!w_f16) return W4A16_ERR_INVALID_ARG;
+    if (!aligned16(w_f16)) return W4A16_ERR_MISALIGNED;
+    return from_cuda(w4a16::launch_pack_q4k(w_f16, N, K, qweight, meta, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status q4k_linear(const void* x_bf16, const uint32_t* qweight, const uint32_t* meta, int64_t M, int64_t N,
+                        int64_t K, void* y_bf16, w4a16_stream_t stream) {
+    return q4k_common(x_bf16, &qweight, &meta, &y_bf16, 1, M, N, K, stream);
+}
+
+w4a16_status q4k_linear_dual(const void* x_bf16, const uint32_t* qweight_gate, const uint32_t* meta_gate,
+                             const uint32_t* qweight_up, const uint32_t* meta_up, int64_t M, int64_t N, int64_t K,
+                             void* y_gate_bf16, void* y_up_bf16, w4a16_stream_t stream) {
+    const uint32_t* q[2] = {qweight_gate, qweight_up};
+    const uint32_t* meta[2] = {meta_gate, meta_up};
+    void* y[2] = {y_gate_bf16, y_up_bf16};
+    return q4k_common(x_bf16, q, meta, y, 2, M, N, K, stream);
 }
 
 int w4a16_linear_path(int64_t M, int64_t N, int64_t K, int G) {

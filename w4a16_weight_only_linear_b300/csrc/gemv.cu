@@ -37,6 +37,15 @@
 // sums in fixed slots, added in a fixed order at the end, so results are
 // deterministic.  Every output is rounded to BF16 once.
 //
+// Super-block mode (KQ).  Weights in the Q4_K-style layout (256-channel
+// super-blocks of 8 sub-blocks of 32; sub-block j reconstructs as
+// d*sc_j*q - dmin*m_j with 6-bit sc_j, m_j and FP16 d, dmin: zhuai.tech
+// "Quantization Is Not a Zip File", section 3, K-quants row of the GGUF names
+// table) run through the same path with G = 32: a 256-code chunk of a virtual
+// row is exactly one super-block, whose 16-byte record takes the place of the
+// scale and zero rows.  The block-end correction becomes
+// acc += s*(D - E) - mn*X with s = d*sc_j and mn = dmin*m_j, both exact in FP32.
+//
 // Prologue.  The launch uses programmatic stream serialisation: a CTA lets the
 // next launch be scheduled on entry and waits for the previous grid before it
 // reads global memory.  One thread then bulk-copies the CTA's scale and zero
@@ -81,8 +90,8 @@ struct GemvParams {
     const __nv_bfloat16* x;                // [M, K]
     const float* xsc;                      // per-input-channel multiplier of x [K], or null
     int kx;                                // row length of x: channel k reads x[k mod kx] (kx = K or K/2)
-    const unsigned short* s[2];            // FP16 scales [N, lds]
-    const uint32_t* z[2];                  // zeros [N, ldz]
+    const unsigned short* s[2];            // FP16 scales [N, lds] (KQ: super-block records, 8 halves each)
+    const uint32_t* z[2];                  // zeros [N, ldz] (KQ: unused, ldz = 0)
     __nv_bfloat16* y[2];                   // [M, N]
     int M, N, K, G;
     int P, R, cols, xcols;                 // segments, weight rows per tile, B columns used (P*H*M),
@@ -195,6 +204,15 @@ __device__ __forceinline__ float meta_zero(uint32_t zshifted, int j) {
     return __uint_as_float(0x4B000000u | ((zshifted >> (4 * j)) & 0xFu)) - 8388608.0f;
 }
 
+// 6-bit code j of a super-block record as a float: low 4 bits at bit 4j of
+// `lo`, high 2 bits at bit 2j + hs of `hi` (hs = 0 for sc, 16 for m).
+__device__ __forceinline__ float kq_code(uint32_t lo, uint32_t hi, int j, int hs) {
+    const uint32_t v = ((lo >> (4 * j)) & 0xFu) | (((hi >> (2 * j + hs)) & 3u) << 4);
+    return __uint_as_float(0x4B000000u | v) - 8388608.0f;
+}
+__device__ __forceinline__ float half_lo(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu))); }
+__device__ __forceinline__ float half_hi(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w >> 16))); }
+
 // Bounded wait on a barrier phase; the thread sleeps between polls.
 __device__ __forceinline__ bool gemv_wait(uint32_t bar, uint32_t parity) {
     if (tc::mbar_try_wait(bar, parity)) return true;
@@ -211,7 +229,7 @@ __device__ __forceinline__ bool gemv_wait(uint32_t bar, uint32_t parity) {
 // M1: one activation row with P >= 2 segments.  The B columns are then
 // (parity, segment) pairs and each lane holds at most one useful D value per
 // row, so the block-end correction is done once per row on that value only.
-template <int NB, int G, int H, bool M1, int PT>
+template <int NB, int G, int H, bool M1, int PT, bool KQ>
 __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
     gemv_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
                 const GemvParams p) {
@@ -223,6 +241,7 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
     const int R = 16 / P;                         // weight rows per tile
     const int kThreads = kWarps * 32;
     static_assert(GPC % H == 0, "a block of H groups lies inside one chunk");
+    static_assert(!KQ || G == 32, "a super-block is one chunk of 8 sub-blocks of 32");
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base; derived by pointer arithmetic on the shared array so
     // the compiler keeps every access below in the shared address space
@@ -311,11 +330,11 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
             tc::mbar_arrive_expect_tx(pbar, (uint32_t)(c0 + c1) * (sbytes + zbytes));
             if (c0 > 0) {
                 tc::bulk_load(ms, p.s[0] + (int64_t)r0 * p.lds, (uint32_t)c0 * sbytes, pbar);
-                tc::bulk_load(mz, p.z[0] + (int64_t)r0 * p.ldz, (uint32_t)c0 * zbytes, pbar);
+                if (!KQ) tc::bulk_load(mz, p.z[0] + (int64_t)r0 * p.ldz, (uint32_t)c0 * zbytes, pbar);
             }
             if (c1 > 0) {
                 tc::bulk_load(ms + (uint32_t)l1 * sbytes, p.s[1] + (int64_t)r1 * p.lds, (uint32_t)c1 * sbytes, pbar);
-                tc::bulk_load(mz + (uint32_t)l1 * zbytes, p.z[1] + (int64_t)r1 * p.ldz, (uint32_t)c1 * zbytes, pbar);
+                if (!KQ) tc::bulk_load(mz + (uint32_t)l1 * zbytes, p.z[1] + (int64_t)r1 * p.ldz, (uint32_t)c1 * zbytes, pbar);
             }
         }
 
@@ -554,9 +573,25 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
                   const unsigned short* sra1 = sra + h_use;
                   const unsigned short* srb1 = srb + h_use;
                   uint32_t zwa1 = 0u, zwb1 = 0u;
-                  if constexpr (M1) {
+                  if constexpr (M1 && !KQ) {
                       zwa1 = zra[gia >> 3] >> (4 * ((gia & 7) + h_use));
                       zwb1 = zrb[gib >> 3] >> (4 * ((gib & 7) + h_use));
+                  }
+                  // KQ: the super-block records of the lane's rows (segment pa/pb, chunk c); at M = 1 the
+                  // code words are shifted to the lane's group parity
+                  uint4 kra = make_uint4(0u, 0u, 0u, 0u), krb = kra;
+                  float kda = 0.0f, kma = 0.0f, kdb = 0.0f, kmb = 0.0f;
+                  if constexpr (KQ) {
+                      kra = *reinterpret_cast<const uint4*>(smtab + rla * p.lds + (pa * p.C + c) * 8);
+                      krb = *reinterpret_cast<const uint4*>(smtab + rlb * p.lds + (pb * p.C + c) * 8);
+                      kda = half_lo(kra.x);
+                      kma = half_hi(kra.x);
+                      kdb = half_lo(krb.x);
+                      kmb = half_hi(krb.x);
+                      if constexpr (M1) {
+                          kra.y >>= 4 * h_use; kra.z >>= 4 * h_use; kra.w >>= 2 * h_use;
+                          krb.y >>= 4 * h_use; krb.z >>= 4 * h_use; krb.w >>= 2 * h_use;
+                      }
                   }
                   const uint32_t unit = ring + slot * (uint32_t)kUnitBytes + (uint32_t)cc * kBoxBytes;
                   const uint32_t row_a = unit + (uint32_t)va * 128u, row_b = row_a + 8u * 128u;
@@ -623,27 +658,49 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
                                   // one useful value per row: segment pa, parity h_use, column e_use
                                   const float va_ = e_use ? da[0][1] + db[0][1] : da[0][0] + db[0][0];
                                   const float vb_ = e_use ? da[0][3] + db[0][3] : da[0][2] + db[0][2];
-                                  const float s_a = __half2float(__ushort_as_half(sra1[jg0]));
-                                  const float s_b = __half2float(__ushort_as_half(srb1[jg0]));
-                                  const float z_a = meta_zero(zwa1, jg0), z_b = meta_zero(zwb1, jg0);
                                   const float2 ex = *reinterpret_cast<const float2*>(
                                       base + (ex_m1 - sbase) + (uint32_t)(blk * 8 * 8));
-                                  acc_a = fmaf(s_a, va_ - fmaf(z_a, ex.y, ex.x), acc_a);
-                                  acc_b = fmaf(s_b, vb_ - fmaf(z_b, ex.y, ex.x), acc_b);
+                                  if constexpr (KQ) {
+                                      // sub-block jg0 + h_use: s = d*sc, mn = dmin*m
+                                      const float s_a = kda * kq_code(kra.y, kra.w, jg0, 0);
+                                      const float s_b = kdb * kq_code(krb.y, krb.w, jg0, 0);
+                                      const float n_a = kma * kq_code(kra.z, kra.w, jg0, 16);
+                                      const float n_b = kmb * kq_code(krb.z, krb.w, jg0, 16);
+                                      acc_a = fmaf(s_a, va_ - ex.x, fmaf(-n_a, ex.y, acc_a));
+                                      acc_b = fmaf(s_b, vb_ - ex.x, fmaf(-n_b, ex.y, acc_b));
+                                  } else {
+                                      const float s_a = __half2float(__ushort_as_half(sra1[jg0]));
+                                      const float s_b = __half2float(__ushort_as_half(srb1[jg0]));
+                                      const float z_a = meta_zero(zwa1, jg0), z_b = meta_zero(zwb1, jg0);
+                                      acc_a = fmaf(s_a, va_ - fmaf(z_a, ex.y, ex.x), acc_a);
+                                      acc_b = fmaf(s_b, vb_ - fmaf(z_b, ex.y, ex.x), acc_b);
+                                  }
                               } else {
                                   // scales of the block's H groups (consecutive halves) and their zero
                                   // points; groups past the row end (last, partial chunk of one
                                   // segment) get scale 0
+                                  // KQ: za/zb hold the sub-blocks' minima dmin*m (a super-block is a
+                                  // whole chunk, so no group lies past the row end)
                                   float sa[H], sb[H], za[H], zb[H];
-                                  const uint32_t zwa = zra[(gia + jg0) >> 3] >> (4 * ((gia + jg0) & 7));
-                                  const uint32_t zwb = zrb[(gib + jg0) >> 3] >> (4 * ((gib + jg0) & 7));
+                                  if constexpr (KQ) {
 #pragma unroll
-                                  for (int hh = 0; hh < H; ++hh) {
-                                      const bool va_ = gia + jg0 + hh < p.ng, vb_ = gib + jg0 + hh < p.ng;
-                                      sa[hh] = va_ ? __half2float(__ushort_as_half(sra[jg0 + hh])) : 0.0f;
-                                      sb[hh] = vb_ ? __half2float(__ushort_as_half(srb[jg0 + hh])) : 0.0f;
-                                      za[hh] = meta_zero(zwa, hh);
-                                      zb[hh] = meta_zero(zwb, hh);
+                                      for (int hh = 0; hh < H; ++hh) {
+                                          sa[hh] = kda * kq_code(kra.y, kra.w, jg0 + hh, 0);
+                                          sb[hh] = kdb * kq_code(krb.y, krb.w, jg0 + hh, 0);
+                                          za[hh] = kma * kq_code(kra.z, kra.w, jg0 + hh, 16);
+                                          zb[hh] = kmb * kq_code(krb.z, krb.w, jg0 + hh, 16);
+                                      }
+                                  } else {
+                                      const uint32_t zwa = zra[(gia + jg0) >> 3] >> (4 * ((gia + jg0) & 7));
+                                      const uint32_t zwb = zrb[(gib + jg0) >> 3] >> (4 * ((gib + jg0) & 7));
+#pragma unroll
+                                      for (int hh = 0; hh < H; ++hh) {
+                                          const bool va_ = gia + jg0 + hh < p.ng, vb_ = gib + jg0 + hh < p.ng;
+                                          sa[hh] = va_ ? __half2float(__ushort_as_half(sra[jg0 + hh])) : 0.0f;
+                                          sb[hh] = vb_ ? __half2float(__ushort_as_half(srb[jg0 + hh])) : 0.0f;
+                                          za[hh] = meta_zero(zwa, hh);
+                                          zb[hh] = meta_zero(zwb, hh);
+                                      }
                                   }
 #pragma unroll
                                   for (int nb = 0; nb < NB; ++nb) {
@@ -657,10 +714,17 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
                                                   s_a = sa[hh]; s_b = sb[hh]; z_a = za[hh]; z_b = zb[hh];
                                               }
                                           const float E = e ? ex.z : ex.x, X = e ? ex.w : ex.y;
-                                          acc[nb][e] =
-                                              fmaf(s_a, (da[nb][e] + db[nb][e]) - fmaf(z_a, X, E), acc[nb][e]);
-                                          acc[nb][2 + e] = fmaf(s_b, (da[nb][2 + e] + db[nb][2 + e]) -
-                                                                         fmaf(z_b, X, E), acc[nb][2 + e]);
+                                          if constexpr (KQ) {
+                                              acc[nb][e] = fmaf(s_a, (da[nb][e] + db[nb][e]) - E,
+                                                                fmaf(-z_a, X, acc[nb][e]));
+                                              acc[nb][2 + e] = fmaf(s_b, (da[nb][2 + e] + db[nb][2 + e]) - E,
+                                                                    fmaf(-z_b, X, acc[nb][2 + e]));
+                                          } else {
+                                              acc[nb][e] = fmaf(s_a, (da[nb][e] + db[nb][e]) - fmaf(z_a, X, E),
+                                                                acc[nb][e]);
+                                              acc[nb][2 + e] = fmaf(s_b, (da[nb][2 + e] + db[nb][2 + e]) -
+                                                                             fmaf(z_b, X, E), acc[nb][2 + e]);
+                                          }
                                       }
                                   }
                               }
@@ -828,8 +892,12 @@ struct Plan {
     size_t smem;
 };
 
-bool make_plan(int64_t M, int64_t N, int64_t K, int G, int nmat, int sms, size_t smem_cap, Plan& pl) {
+// kq: the super-block layout (G = 32, K a multiple of 256, M <= 8): one 16-byte
+// record per 256 codes in place of the scale row, no zero row.
+bool make_plan(int64_t M, int64_t N, int64_t K, int G, int nmat, int sms, size_t smem_cap, Plan& pl,
+               bool kq = false) {
     if (M < 1 || M > 16 || N < 1 || K < 32 || K % 32 || K % G) return false;
+    if (kq && (G != 32 || K % 256 || M > 8)) return false;
     if (N > (int64_t)1 << 24 || K > (int64_t)1 << 20) return false;   // keeps tile/unit indices small
     GemvParams& p = pl.p;
     p.M = (int)M;
@@ -845,8 +913,8 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int G, int nmat, int sms, size_t
     p.Ks = p.C * 256;                           // equals K / P whenever P > 1
     p.ng = (int)(K / G);
     p.ngs = p.Ks / G;
-    p.lds = (int)scales_ld(K, G);
-    p.ldz = (int)zeros_ld(K, G);
+    p.lds = kq ? (int)(K / 256 * 8) : (int)scales_ld(K, G);
+    p.ldz = kq ? 0 : (int)zeros_ld(K, G);
     p.tiles_per_mat = (int)((N + p.R - 1) / p.R);
     p.total_tiles = p.tiles_per_mat * nmat;
     pl.grid = p.total_tiles < sms ? p.total_tiles : sms;
@@ -879,7 +947,7 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int G, int nmat, int sms, size_t
     return false;
 }
 
-template <int NB, int G, int H, bool M1, int PT>
+template <int NB, int G, int H, bool M1, int PT, bool KQ>
 cudaError_t launch_m(const CUtensorMap& tm0, const CUtensorMap& tm1, const Plan& pl, cudaStream_t stream) {
     static int cached[kMaxDevices] = {};
     int dev = 0;
@@ -887,7 +955,7 @@ cudaError_t launch_m(const CUtensorMap& tm0, const CUtensorMap& tm1, const Plan&
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     if ((int)pl.smem > cached[dev]) {
-        e = cudaFuncSetAttribute(gemv_kernel<NB, G, H, M1, PT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(gemv_kernel<NB, G, H, M1, PT, KQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)pl.smem);
         if (e != cudaSuccess) return e;
         cached[dev] = (int)pl.smem;
@@ -903,36 +971,36 @@ cudaError_t launch_m(const CUtensorMap& tm0, const CUtensorMap& tm1, const Plan&
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<NB, G, H, M1, PT>, tm0, tm1, pl.p);
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<NB, G, H, M1, PT, KQ>, tm0, tm1, pl.p);
 }
 
-template <int NB, int G, int H>
+template <int NB, int G, int H, bool KQ>
 cudaError_t launch_t(const CUtensorMap& tm0, const CUtensorMap& tm1, const Plan& pl, cudaStream_t stream) {
     if constexpr (NB == 1) {
         if (m1_kernel(pl.p)) {                       // M = 1: the segment count is a template constant
             switch (pl.p.P) {
-                case 2: return launch_m<NB, G, H, true, 2>(tm0, tm1, pl, stream);
-                case 4: return launch_m<NB, G, H, true, 4>(tm0, tm1, pl, stream);
-                case 8: return launch_m<NB, G, H, true, 8>(tm0, tm1, pl, stream);
+                case 2: return launch_m<NB, G, H, true, 2, KQ>(tm0, tm1, pl, stream);
+                case 4: return launch_m<NB, G, H, true, 4, KQ>(tm0, tm1, pl, stream);
+                case 8: return launch_m<NB, G, H, true, 8, KQ>(tm0, tm1, pl, stream);
             }
             return cudaErrorInvalidValue;
         }
     }
-    return launch_m<NB, G, H, false, 0>(tm0, tm1, pl, stream);
+    return launch_m<NB, G, H, false, 0, KQ>(tm0, tm1, pl, stream);
 }
 
-template <int NB, int G>
+template <int NB, int G, bool KQ = false>
 cudaError_t launch_h(const CUtensorMap& tm0, const CUtensorMap& tm1, const Plan& pl, cudaStream_t stream) {
     if constexpr (NB == 2) {
-        return launch_t<NB, G, 1>(tm0, tm1, pl, stream);
+        return launch_t<NB, G, 1, KQ>(tm0, tm1, pl, stream);
     } else {
         switch (pl.H) {
-            case 1: return launch_t<NB, G, 1>(tm0, tm1, pl, stream);
+            case 1: return launch_t<NB, G, 1, KQ>(tm0, tm1, pl, stream);
             case 2:
-                if constexpr (256 / G >= 2) return launch_t<NB, G, 2>(tm0, tm1, pl, stream);
+                if constexpr (256 / G >= 2) return launch_t<NB, G, 2, KQ>(tm0, tm1, pl, stream);
                 break;
             case 4:
-                if constexpr (256 / G >= 4) return launch_t<NB, G, 4>(tm0, tm1, pl, stream);
+                if constexpr (256 / G >= 4) return launch_t<NB, G, 4, KQ>(tm0, tm1, pl, stream);
                 break;
         }
         return cudaErrorInvalidValue;
@@ -973,24 +1041,25 @@ cudaError_t gemv_take_status(uint32_t* word) {
     return cudaMemcpyToSymbol(g_gemv_status, &zero, sizeof(uint32_t));
 }
 
-bool gemv_fits(int64_t M, int64_t N, int64_t K, int G, int nmat) {
+bool gemv_fits(int64_t M, int64_t N, int64_t K, int G, int nmat, bool kq) {
     Plan pl;
     int sms = device_sms();
     if (sms <= 0) sms = 148;
     size_t cap = device_smem_optin();
     if (cap == 0) cap = 227 * 1024;
-    return make_plan(M, N, K, G, nmat, sms, cap, pl);
+    return make_plan(M, N, K, G, nmat, sms, cap, pl, kq);
 }
 
 cudaError_t launch_gemv(const void* x, const GemvMat* mats, int nmat, int64_t M, int64_t N, int64_t K, int G,
-                        cudaStream_t stream, const float* xsc, int64_t kx) {
+                        cudaStream_t stream, const float* xsc, int64_t kx, bool kq) {
     if (kx == 0) kx = K;
     if (kx != K && (kx * 2 != K || kx % 8 != 0)) return cudaErrorInvalidValue;
+    if (kq && (G != 32 || xsc != nullptr || kx != K)) return cudaErrorInvalidValue;
     const int sms = device_sms();
     if (sms <= 0) return cudaErrorNoDevice;
     const size_t cap = device_smem_optin();
     Plan pl;
-    if (!make_plan(M, N, K, G, nmat, sms, cap, pl)) return cudaErrorNotSupported;
+    if (!make_plan(M, N, K, G, nmat, sms, cap, pl, kq)) return cudaErrorNotSupported;
     GemvParams& p = pl.p;
     p.x = static_cast<const __nv_bfloat16*>(x);
     p.xsc = xsc;
@@ -1003,6 +1072,7 @@ cudaError_t launch_gemv(const void* x, const GemvMat* mats, int nmat, int64_t M,
         p.y[i] = static_cast<__nv_bfloat16*>(mt.y);
         if (!make_code_map(&tm[i], mt.q, N, K, p.P)) return cudaErrorInvalidValue;
     }
+    if (kq) return launch_h<1, 32, true>(tm[0], tm[1], pl, stream);      // make_plan: M <= 8, so one column block
     return pl.nb == 1 ? launch_nb<1>(tm[0], tm[1], pl, stream) : launch_nb<2>(tm[0], tm[1], pl, stream);
 }
 

@@ -13,6 +13,9 @@ cudaError_t launch_pack8(const void* w, int64_t N, int64_t K, int G, uint32_t* q
                          cudaStream_t stream);
 cudaError_t launch_dequant(const uint32_t* qw, const void* sc, const uint32_t* zr, int64_t N, int64_t K, int G,
                            float* out, cudaStream_t stream);
+// The super-block (Q4_K-style) packer: codes in the 4-bit layout, one 16-byte record per 256 channels
+// (see pack.cu).  K a multiple of 256.
+cudaError_t launch_pack_q4k(const void* w, int64_t N, int64_t K, uint32_t* qw, uint32_t* meta, cudaStream_t stream);
 
 // One packed weight matrix and the output it feeds.
 struct GemvMat {
@@ -24,7 +27,8 @@ struct GemvMat {
 
 // Whether the decode GEMV takes this shape (M <= 16 and its x staging plus
 // stream rings fit the device's shared memory).  Host only.
-bool gemv_fits(int64_t M, int64_t N, int64_t K, int G, int nmat);
+// kq: the super-block layout (G = 32, M <= 8).
+bool gemv_fits(int64_t M, int64_t N, int64_t K, int G, int nmat, bool kq = false);
 // Largest dynamic shared memory a block may use on the current device.
 size_t device_smem_optin();
 
@@ -32,8 +36,10 @@ size_t device_smem_optin();
 // xsc (optional, FP32 [K], 16-byte aligned): x_k is taken as x_k * xsc_k.
 // kx (optional, 0 = K): row length of x; input channel k of the layer reads x[k mod kx]
 // (the two-plane 8-bit layer is a 4-bit layer of K = 2 kx channels over x repeated).
+// kq: the matrices are in the super-block layout (GemvMat.s = records, .z unused; G = 32,
+// M <= 8, no xsc or kx).
 cudaError_t launch_gemv(const void* x, const GemvMat* mats, int nmat, int64_t M, int64_t N, int64_t K, int G,
-                        cudaStream_t stream, const float* xsc = nullptr, int64_t kx = 0);
+                        cudaStream_t stream, const float* xsc = nullptr, int64_t kx = 0, bool kq = false);
 
 // Tensor-core path (any M): y_i = x * W_hat_i^T for nmat matrices sharing x
 // (x is converted to FP16 once, into stream-ordered scratch).

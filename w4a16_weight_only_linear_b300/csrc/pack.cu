@@ -212,6 +212,92 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint32_t* __restrict
     dst[1] = make_float4(o[4], o[5], o[6], o[7]);
 }
 
+// Super-block (Q4_K-style) quantiser: 256 consecutive input channels of one
+// output row form a super-block of 8 sub-blocks of 32, each with its own scale
+// and minimum, and those are quantised against two FP16 factors per
+// super-block (zhuai.tech "Quantization Is Not a Zip File", section 3, table
+// "How to read common GGUF quantization names": K-quants keep sub-block
+// scales and minima inside 256-weight super-blocks, hierarchically).
+//   sub-block j:  lo = min(0, min w), hi = max(0, max w), a_j = (hi - lo) / 15, b_j = -lo
+//   d = RNE_fp16(max a_j / 63) (0 -> 1),  dmin = RNE_fp16(max b_j / 63)
+//   sc_j = clamp(rne(a_j / d), 0, 63),  m_j = dmin == 0 ? 0 : clamp(rne(b_j / dmin), 0, 63)
+//   q = d*sc_j > 0 ? clamp(rne((w + dmin*m_j) / (d*sc_j)), 0, 15) : 0
+// W_hat = d*sc_j*q - dmin*m_j.  Codes go to the 4-bit layout; each
+// super-block gets a 16-byte record: d | dmin << 16; sc_j & 15 at bits 4j;
+// m_j & 15 at bits 4j; sc_j >> 4 at bits 2j and m_j >> 4 at bits 16 + 2j.
+// One warp per super-block: lane l holds channels 8l..8l+7 (one code word),
+// so lanes 4j..4j+3 hold sub-block j.
+__global__ void __launch_bounds__(256) pack_q4k_kernel(const __half* __restrict__ w, int64_t N, int64_t K,
+                                                       uint32_t* __restrict__ qw, uint32_t* __restrict__ meta) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nsb = K / 256;
+    const int64_t sbg = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;   // super-block, row-major
+    if (sbg >= N * nsb) return;                                                     // warp-uniform
+    const int64_t n = sbg / nsb, sb = sbg - n * nsb;
+    float v[8];
+    load_weights<8>(w + n * K + sb * 256 + lane * 8, v);
+    float lo = 0.0f, hi = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        lo = fminf(lo, v[i]);
+        hi = fmaxf(hi, v[i]);
+    }
+#pragma unroll
+    for (int off = 1; off < 4; off <<= 1) {
+        lo = fminf(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, off));
+        hi = fmaxf(hi, __shfl_xor_sync(0xFFFFFFFFu, hi, off));
+    }
+    // b = 0 - lo rather than -lo: a sub-block without negative weights has minimum +0, so
+    // dmin of a super-block of them is stored as +0
+    const float a = __fdiv_rn(__fsub_rn(hi, lo), 15.0f), b = __fsub_rn(0.0f, lo);
+    float amax = a, bmax = b;
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+        bmax = fmaxf(bmax, __shfl_xor_sync(0xFFFFFFFFu, bmax, off));
+    }
+    __half dh = __float2half_rn(__fdiv_rn(amax, 63.0f));
+    const __half mh = __float2half_rn(__fdiv_rn(bmax, 63.0f));
+    float d = __half2float(dh);
+    const float dmin = __half2float(mh);
+    if (d == 0.0f) {
+        dh = __ushort_as_half((unsigned short)0x3C00);
+        d = 1.0f;
+    }
+    const int sc = min(max(__float2int_rn(__fdiv_rn(a, d)), 0), 63);
+    const int m = dmin == 0.0f ? 0 : min(max(__float2int_rn(__fdiv_rn(b, dmin)), 0), 63);
+    const float ap = __fmul_rn(d, (float)sc), bp = __fmul_rn(dmin, (float)m);    // exact products
+    uint32_t word = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int q = ap > 0.0f ? min(max(__float2int_rn(__fdiv_rn(__fadd_rn(v[i], bp), ap)), 0), 15) : 0;
+        word |= (uint32_t)q << (4 * i);
+    }
+    qw[n * qweight_ld(K) + sb * 32 + lane] = word;
+    // the record: every lane gathers the 8 sub-blocks' codes, lane 0 stores it
+    uint32_t w1 = 0, w2 = 0, w3 = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int scj = __shfl_sync(0xFFFFFFFFu, sc, 4 * j), mj = __shfl_sync(0xFFFFFFFFu, m, 4 * j);
+        w1 |= (uint32_t)(scj & 15) << (4 * j);
+        w2 |= (uint32_t)(mj & 15) << (4 * j);
+        w3 |= ((uint32_t)(scj >> 4) << (2 * j)) | ((uint32_t)(mj >> 4) << (16 + 2 * j));
+    }
+    if (lane == 0) {
+        const uint32_t w0 = (uint32_t)__half_as_ushort(dh) | ((uint32_t)__half_as_ushort(mh) << 16);
+        *reinterpret_cast<uint4*>(meta + n * (nsb * 4) + sb * 4) = make_uint4(w0, w1, w2, w3);
+    }
+}
+
+cudaError_t launch_pack_q4k(const void* w, int64_t N, int64_t K, uint32_t* qw, uint32_t* meta, cudaStream_t stream) {
+    const int warps = 8;
+    const int64_t total = N * (K / 256);
+    if ((total + warps - 1) / warps > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    const dim3 grid((unsigned)((total + warps - 1) / warps));
+    pack_q4k_kernel<<<grid, dim3(32 * warps), 0, stream>>>(static_cast<const __half*>(w), N, K, qw, meta);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_pack(const void* w, int64_t N, int64_t K, int G, uint32_t* qw, void* sc, uint32_t* zr,
                         cudaStream_t stream) {
     const int warps = 8;

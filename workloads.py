@@ -11,6 +11,8 @@ Input recipe (weights are never trained; no dataset is involved):
   * x ~ N(0, 1) drawn in FP32, then round-to-nearest-even to BF16;
   * the j-th matrix of a workload uses seed + 100*j, its activations seed +
     100*j + 50;
+  * super-block (Q4_K-style) workloads draw W the same way and pack it into
+    256-channel super-blocks (G is then the 32-channel sub-block);
   * activation-scaled workloads draw x_scale = 1/alpha with alpha = 1 except on a
     seeded 1 % of input channels, where alpha ~ U[2, 4) (seed + 100*j + 70), and
     pack W * alpha rounded to FP16.
@@ -47,6 +49,7 @@ class Workload:
     dual: bool = False
     act_scaled: bool = False     # layer with a per-input-channel activation scale
     bits: int = 4                # weight code width: 4, or 8 (the W8A16 variant)
+    q4k: bool = False            # super-block (Q4_K-style) layout instead of groups of G
 
 
 WORKLOADS = {
@@ -69,6 +72,9 @@ WORKLOADS = {
                            (1, 4, 32), (128,), 0.02, 0.0, 5, act_scaled=True),
     # the 8-bit variant on the 13B up-projection, decode and a small batch
     "up13b_w8": Workload("up13b_w8", (Linear("up", 5120, 13824),), (1, 4, 32), (128,), 0.02, 0.0, 6, bits=8),
+    # the 70B FFN gate and down in the super-block (Q4_K-style) layout, decode
+    "ffn70b_q4k": Workload("ffn70b_q4k", (Linear("gate", 8192, 28672), Linear("down", 28672, 8192)), (1, 3),
+                           (32,), 0.015, 0.0, 7, q4k=True),
     # 70B-shaped FFN gate and down, decode (M=1) and prefill (M=2048)
     "ffn70b": Workload("ffn70b", (Linear("gate", 8192, 28672), Linear("down", 28672, 8192)), (1, 2048),
                        (128,), 0.015, 0.0, 4),
