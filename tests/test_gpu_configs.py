@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 def _decode_cases():
     cases = []
     for name, wk in wl.WORKLOADS.items():
-        if wk.dual or wk.act_scaled or wk.bits != 4:        # those have their own tests
+        if wk.dual or wk.act_scaled or wk.bits != 4 or wk.q4k:        # those have their own tests
             continue
         for j, lin in enumerate(wk.linears):
             for G in wk.Gs:
@@ -81,7 +81,7 @@ def test_dual_workload(M):
 def _prefill_cases():
     cases = []
     for name, wk in wl.WORKLOADS.items():
-        if wk.dual or wk.act_scaled or wk.bits != 4:        # those have their own tests
+        if wk.dual or wk.act_scaled or wk.bits != 4 or wk.q4k:        # those have their own tests
             continue
         for j, lin in enumerate(wk.linears):
             for G in wk.Gs:
