@@ -584,6 +584,14 @@ def test_q4k_degenerate_superblocks():
     q, meta = oracle.q4k_pack(pos)
     dd, dm, sc, m = oracle.q4k_record(meta, 256, 0, 0)
     assert dm == 0.0 and not m.any()
+    # weights far from 0 on one side: the range widened to hold 0 keeps every weight within half a step
+    # plus the 6-bit rounding of the sub-block scale (|d sc_j - a_j| <= d/2, over 15 steps)
+    far = rng.uniform(0.5, 1.0, (1, 256)).astype(np.float16)
+    q, meta = oracle.q4k_pack(far)
+    dd, dm, sc, m = oracle.q4k_record(meta, 256, 0, 0)
+    wh = oracle.q4k_dequant(q, meta, 1, 256)[0].astype(np.float64)
+    err = np.abs(wh - far[0].astype(np.float64)).reshape(8, 32).max(axis=1)
+    assert (err <= dd * sc / 2 + 15 * dd / 2 + 1e-6).all(), (err, dd, sc)
     with pytest.raises(ValueError):
         oracle.q4k_pack(np.zeros((2, 384), np.float16))
 
