@@ -184,21 +184,6 @@ __device__ __forceinline__ float4 lds_f4(uint32_t addr) {
     return v;
 }
 
-// V codes words of one virtual row at 16-byte chunk `ch` (plus word offset).
-template <int V>
-__device__ __forceinline__ void load_codes(uint32_t row_addr, int ch, int v7, int word_in_chunk, uint32_t (&w)[V]) {
-    const uint32_t a = row_addr + ((uint32_t)(ch ^ v7) << 4) + (uint32_t)word_in_chunk * 4u;
-    if constexpr (V == 4) {
-        const uint4 u = lds128(a);
-        w[0] = u.x; w[1] = u.y; w[2] = u.z; w[3] = u.w;
-    } else if constexpr (V == 2) {
-        const uint2 u = lds64(a);
-        w[0] = u.x; w[1] = u.y;
-    } else {
-        w[0] = lds32(a);
-    }
-}
-
 // Zero point in nibble j of a (shifted) zero word, as a float (2^23 + z has ulp 1).
 __device__ __forceinline__ float meta_zero(uint32_t zshifted, int j) {
     return __uint_as_float(0x4B000000u | ((zshifted >> (4 * j)) & 0xFu)) - 8388608.0f;
