@@ -282,8 +282,12 @@ W4A16_API w4a16_status w8a16_linear(const void* x_bf16, const uint32_t* qweight,
  * pointer 16-byte aligned (W4A16_ERR_INVALID_ARG / W4A16_ERR_MISALIGNED).
  * The layer runs the decode kernel: up to 8 activation rows per launch, as
  * many as its shared memory holds for this K (x staged as M*K FP16); larger M
- * is split into row blocks, each of which reads the weights again.
- * W4A16_ERR_UNSUPPORTED if not even one row fits (K beyond about 90k).
+ * is split into row blocks, each of which reads the weights again.  Each CTA
+ * also holds the records of all its weight rows; where even one activation
+ * row does not fit that way (N*K above about 3e8 at M = 1, e.g. N = 28672
+ * with K > 13824), the weight rows are cut into slices that fit and the call
+ * runs one activation row per launch.  W4A16_ERR_UNSUPPORTED if K exceeds
+ * 77312 (not even 8 weight rows and one activation row fit).
  */
 W4A16_API int64_t q4k_meta_ld(int64_t K);   /* uint32 words per meta row: K/256*4 (0 if K % 256) */
 W4A16_API w4a16_status q4k_pack(const void* w_f16, int64_t N, int64_t K, uint32_t* qweight, uint32_t* meta,

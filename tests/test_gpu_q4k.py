@@ -123,3 +123,23 @@ def test_q4k_dual_workload_shape():
     for y, (q, meta), name in ((yg, packs[0], "gate"), (yu, packs[1], "up")):
         ref = oracle.q4k_linear_sampled(wl.bits_u16(x), q, meta, lin.K, ms, ns)
         assert_close(y.float().cpu().numpy()[ms, ns], ref, f"q4k dual {name} at 8192 -> 28672 (sampled)")
+
+
+@pytest.mark.parametrize("M", [1, 2])
+def test_q4k_row_slices(M):
+    """N = 4752, K = 49152: the records of the rows a CTA would hold do not fit its shared memory even for
+    one activation row, so the call cuts the weight rows into slices and runs one activation row per launch.
+    Sampled outputs (every slice edge among them) against the oracle."""
+    N, K = 4752, 49152
+    w = wl.weight_f16(N, K, 0.01, 77)
+    q, meta = oracle.q4k_pack(wl.bits_u16(w))
+    x = wl.activations_bf16(M, K, 78 + M)
+    y = w4.q4k_linear(x.cuda(), *_dev(q, meta))
+    torch.cuda.synchronize()
+    assert w4.w4a16_device_status() == 0
+    rng = np.random.default_rng(79)
+    edges = [0, 7, 8, 2375, 2376, 2383, N - 8, N - 1]
+    ns = np.concatenate([np.tile(edges, M), rng.integers(0, N, 256 * M)])
+    ms = np.concatenate([np.repeat(np.arange(M), len(edges)), rng.integers(0, M, 256 * M)])
+    ref = oracle.q4k_linear_sampled(wl.bits_u16(x), q, meta, K, ms, ns)
+    assert_close(y.float().cpu().numpy()[ms, ns], ref, f"q4k row slices M={M} (sampled)")

@@ -136,9 +136,25 @@ w4a16_status q4k_common(const void* x, const uint32_t* const* q, const uint32_t*
             if ((st = q4k_common(x, q + i, meta + i, y + i, 1, M, N, K, stream)) != W4A16_OK) return st;
         return W4A16_OK;
     }
-    if (mb < 1) return W4A16_ERR_UNSUPPORTED;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     const auto* xb = static_cast<const uint16_t*>(x);
+    if (mb < 1) {
+        // too many weight rows per CTA for their records: cut the rows into the largest slices
+        // (multiples of 8) that fit and run one activation row per launch, since a slice of
+        // y's row m is contiguous
+        int64_t nc = N;
+        while (nc > 8 && !w4a16::gemv_fits(1, nc, K, 32, 1, true)) nc = (nc / 2 + 7) / 8 * 8;
+        if (!w4a16::gemv_fits(1, nc, K, 32, 1, true)) return W4A16_ERR_UNSUPPORTED;
+        for (int64_t m = 0; m < M; ++m)
+            for (int64_t n0 = 0; n0 < N; n0 += nc) {
+                const int64_t nr = N - n0 < nc ? N - n0 : nc;
+                const GemvMat mat{q[0] + n0 * (K / 8), meta[0] + n0 * (K / 256 * 4), nullptr,
+                                  static_cast<uint16_t*>(y[0]) + m * N + n0};
+                const cudaError_t e = w4a16::launch_gemv(xb + m * K, &mat, 1, 1, nr, K, 32, cs, nullptr, 0, true);
+                if (e != cudaSuccess) return from_cuda(e);
+            }
+        return W4A16_OK;
+    }
     for (int64_t m0 = 0; m0 < M; m0 += mb) {
         const int64_t mr = M - m0 < mb ? M - m0 : mb;
         GemvMat mats[2];
