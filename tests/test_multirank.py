@@ -38,7 +38,7 @@ def _worker(rank, world, port, out):
 
 def test_times_are_the_slowest_ranks():
     world = 2
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()      # no fork of this (multi-threaded) process
     mp.spawn(_worker, args=(world, _free_port(), out), nprocs=world, join=True)
     expect = [2.0, 10.0, 10.0]
     assert out[0] == expect and out[1] == expect
