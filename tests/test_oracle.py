@@ -63,7 +63,8 @@ def _f16_probe_values(rng):
 def test_f32_to_f16_rne_matches_numpy():
     rng = np.random.default_rng(1)
     vals = _f16_probe_values(rng)
-    ref = vals.astype(np.float16).view(np.uint16)
+    with np.errstate(over="ignore"):                   # the probes include values that round to +-inf
+        ref = vals.astype(np.float16).view(np.uint16)
     got = np.array([oracle.f32_to_f16(float(x)) for x in vals], np.uint16)
     assert np.array_equal(got, ref)
 
