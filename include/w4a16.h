@@ -119,6 +119,9 @@ W4A16_API w4a16_status w4a16_pack(const void* w_f16, int64_t N, int64_t K, int G
  */
 W4A16_API w4a16_status w4a16_dequant(const uint32_t* qweight, const void* scales_f16, const uint32_t* zeros,
                            int64_t N, int64_t K, int G, float* w_out, w4a16_stream_t stream);
+/* The same call under its checking-aid name: identical arguments, behaviour and errors. */
+W4A16_API w4a16_status w4a16_dequant_debug(const uint32_t* qweight, const void* scales_f16, const uint32_t* zeros,
+                                           int64_t N, int64_t K, int G, float* w_out, w4a16_stream_t stream);
 
 /* ---- the layer ---------------------------------------------------------------
  * w4a16_linear: y[M,N] (BF16) = x[M,K] (BF16) * W_hat^T, FP32 accumulation,

@@ -80,6 +80,18 @@ def test_linear_argument_errors(fn):
     assert _call_linear(fn, N=0) == 0
 
 
+def test_dequant_debug_is_the_dequant_call():
+    # same validation as w4a16_dequant (no compute call here): bad group, N % 8, misaligned output, empty
+    v = ctypes.c_void_p
+    a = v(1 << 12)
+    for name in ("w4a16_dequant", "w4a16_dequant_debug"):
+        f = getattr(w4._lib, name)
+        assert f(a, a, a, 64, 256, 100, a, v(0)) == 2
+        assert f(a, a, a, 60, 256, 128, a, v(0)) == 1
+        assert f(a, a, a, 64, 256, 128, v((1 << 12) + 4), v(0)) == 3
+        assert f(a, a, a, 0, 256, 128, a, v(0)) == 0
+
+
 def test_pack_and_dequant_argument_errors():
     v = ctypes.c_void_p
     a = v(1 << 12)

@@ -33,6 +33,7 @@ EXPORTS = {
     "w4a16_zeros_ld": ([_i64, _i32], _i64),
     "w4a16_pack": ([_vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp], _i32),
     "w4a16_dequant": ([_vp, _vp, _vp, _i64, _i64, _i32, _vp, _vp], _i32),
+    "w4a16_dequant_debug": ([_vp, _vp, _vp, _i64, _i64, _i32, _vp, _vp], _i32),
     "w4a16_linear": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp], _i32),
     "w4a16_linear_dual": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp, _vp], _i32),
     "w4a16_linear_gemv": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp], _i32),

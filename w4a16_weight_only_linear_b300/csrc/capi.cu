@@ -237,6 +237,11 @@ w4a16_status w4a16_dequant(const uint32_t* qweight, const void* scales_f16, cons
                                            reinterpret_cast<cudaStream_t>(stream)));
 }
 
+w4a16_status w4a16_dequant_debug(const uint32_t* qweight, const void* scales_f16, const uint32_t* zeros,
+                                 int64_t N, int64_t K, int G, float* w_out, w4a16_stream_t stream) {
+    return w4a16_dequant(qweight, scales_f16, zeros, N, K, G, w_out, stream);
+}
+
 w4a16_status w4a16_linear(const void* x_bf16, const uint32_t* qweight, const void* scales_f16,
                           const uint32_t* zeros, int64_t M, int64_t N, int64_t K, int G, void* y_bf16,
                           w4a16_stream_t stream) {
