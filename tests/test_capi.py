@@ -182,3 +182,25 @@ def test_path_query_rejects_bad_shapes():
     assert w4.w4a16_linear_path(1, 60, 256, 128) == 0
     assert w4.w4a16_linear_path(1, 64, 250, 128) == 0
     assert w4.w4a16_linear_path(1, 64, 256, 100) == 0
+
+
+@pytest.mark.parametrize("N,K", [(4096, 4096), (5120, 5120), (13824, 5120), (5120, 13824), (28672, 8192),
+                                 (8192, 28672)])
+@pytest.mark.parametrize("G", [32, 64, 128, 256])
+def test_dispatch_rule(N, K, G):
+    """Host-only dispatch: the decode GEMV up to M = 8 where its x staging and tables fit, the tensor-core
+    GEMM above; M = 1 fits at every workload shape, and once a batch size leaves the GEMV every larger
+    one does too."""
+    paths = [w4.w4a16_linear_path(M, N, K, G) for M in range(1, 20)]
+    assert set(paths) <= {1, 2}
+    assert paths[0] == 1
+    assert all(p == 2 for p in paths[8:])                      # M >= 9
+    first_gemm = paths.index(2)
+    assert all(p == 2 for p in paths[first_gemm:])
+    assert w4.w4a16_linear_path(2048, N, K, G) == 2
+
+
+def test_dispatch_falls_back_when_the_gemv_does_not_fit():
+    # x staged as M*K FP16 plus G = 32 tables: at K = 65536 not even one row fits the decode kernel
+    assert w4.w4a16_linear_path(1, 8192, 65536, 32) == 2
+    assert w4.w4a16_linear_path(1, 8192, 65536, 128) == 1
