@@ -653,3 +653,38 @@ def test_q4k_bits_per_weight_and_70b_size():
     assert bpw == 4.5
     gb = cf["params"] * bpw / 8 / 1e9
     assert gb > cf["int4_gb"] and round(gb, 2) == 39.38
+
+
+# property-based: any super-block on the grid of (d, dmin, sc, m) comes back exactly
+from hypothesis import HealthCheck, given, settings, strategies as st  # noqa: E402
+
+
+@st.composite
+def _q4k_grid(draw):
+    # FP16 factors across a wide exponent range; the d*sc*q - dmin*m grid kept inside FP16's normal range
+    d = float(np.float16(draw(st.floats(2.0 ** -14, 2.0 ** -2, allow_nan=False, allow_infinity=False))))
+    dmin = float(np.float16(draw(st.floats(2.0 ** -14, 2.0 ** -2, allow_nan=False, allow_infinity=False))))
+    sc = draw(st.lists(st.integers(0, 63), min_size=8, max_size=8))
+    m = draw(st.lists(st.integers(0, 63), min_size=8, max_size=8))
+    sc[draw(st.integers(0, 7))] = 63
+    m[draw(st.integers(0, 7))] = 63
+    for j in range(8):                       # zero inside each sub-block's range, and a'_j > 0
+        if sc[j] == 0 or 15 * d * sc[j] < dmin * m[j]:
+            sc[j] = 63
+            if 15 * d * 63 < dmin * m[j]:
+                m[j] = int(15 * d * 63 // dmin)
+    seed = draw(st.integers(0, 2 ** 31 - 1))
+    return d, dmin, np.array(sc), np.array(m), seed
+
+
+@settings(max_examples=60, deadline=None, suppress_health_check=[HealthCheck.too_slow])
+@given(_q4k_grid())
+def test_q4k_on_grid_round_trip_property(grid):
+    d, dmin, sc, m, seed = grid
+    if m.max() < 63 or 15 * d * 63 < dmin * 63:
+        return                                # the clamp above removed the 63 that fixes dmin
+    w, codes = _q4k_superblock_weights(d, dmin, sc, m, np.random.default_rng(seed))
+    db, dmb, sc_o, m_o, q_o = oracle.q4k_quantize_superblock(w.astype(np.float32))
+    assert oracle.f16_to_f32(db) == d and oracle.f16_to_f32(dmb) == dmin
+    assert np.array_equal(sc_o, sc) and np.array_equal(m_o, m)
+    assert np.array_equal(q_o.astype(np.int64), codes)
