@@ -688,3 +688,32 @@ def test_q4k_on_grid_round_trip_property(grid):
     assert oracle.f16_to_f32(db) == d and oracle.f16_to_f32(dmb) == dmin
     assert np.array_equal(sc_o, sc) and np.array_equal(m_o, m)
     assert np.array_equal(q_o.astype(np.int64), codes)
+
+
+@st.composite
+def _w4_grid(draw):
+    G = draw(st.sampled_from([32, 64, 128, 256]))
+    mant = draw(st.integers(64, 127))                     # 7-bit significand: (q - z) * s is exact in FP16
+    expo = draw(st.integers(-18, -8))
+    z = draw(st.integers(0, 15))
+    seed = draw(st.integers(0, 2 ** 31 - 1))
+    return G, mant * 2.0 ** expo, z, seed
+
+
+@settings(max_examples=60, deadline=None)
+@given(_w4_grid())
+def test_on_grid_round_trip_property(grid):
+    """One group on the grid of any (s, z), codes 0 and 15 both present: the packer gives back s, z and every
+    code, including z = 0 (no negative weight) and z = 15 (no positive weight)."""
+    G, s, z, seed = grid
+    rng = np.random.default_rng(seed)
+    q = rng.integers(0, 16, G)
+    pos = rng.choice(G, 2, replace=False)
+    q[pos[0]], q[pos[1]] = 0, 15
+    w = (q - z) * s
+    w16 = w.astype(np.float16).reshape(1, G)
+    assert np.array_equal(w16.astype(np.float64)[0], w)
+    qq, ss, zz = oracle.pack(w16, G)
+    assert np.array_equal(oracle.unpack_codes(qq, G)[0], q.astype(np.uint8))
+    assert oracle.unpack_zeros(zz, G, G)[0, 0] == z
+    assert ss[0, 0].view(np.float16).astype(np.float64) == s
