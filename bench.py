@@ -67,6 +67,12 @@ def q4k_bytes(M, N, K):
     return N * K // 2 + N * (K // 256) * 16 + M * K * 2 + M * N * 2
 
 
+def _ordinal(n):
+    """1st, 2nd, 3rd, 4th, ..., 11th, 12th, 13th, 21st, 32nd ..."""
+    suffix = "th" if 10 <= n % 100 <= 20 else {1: "st", 2: "nd", 3: "rd"}.get(n % 10, "th")
+    return f"{n}{suffix}"
+
+
 def gemm_flops(M, N, K):
     return 2.0 * M * N * K
 
@@ -438,7 +444,7 @@ def run_reference(args):
                       "M_decode": M_DECODE, "G": G, "parallelism": "host cores"},
            "cpu_baseline": {"value": round(v, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
                             "sample": f"{args.steps} steps, each the M=1 gate and down GEMVs on every "
-                                      f"{REF_ROW_FRACTION}th output row (FP64 oracle)"},
+                                      f"{_ordinal(REF_ROW_FRACTION)} output row (FP64 oracle)"},
            "e2e": {"value": round(v, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
 
