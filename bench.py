@@ -258,6 +258,11 @@ def run_ours(args):
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         torch.cuda.synchronize()
+        # The sampler's start leaves the GPU idle for a few hundred ms.  One untimed replay of
+        # the first decode graph, enqueued right before the start event, puts the first timed
+        # launch behind running work, as every later one is (in a decode step the layer
+        # always follows another kernel); the timed region itself holds exactly `steps` steps.
+        graphs[keys[0]].replay()
         t0.record(stream)
         for k in keys:
             evs[k][0].record(stream)
@@ -354,7 +359,7 @@ def e2e_ours(w4, mats, dev, args, gemm_ok):
         ox += M_DECODE * lin.K
         oy += M_DECODE * lin.N
     stream = torch.cuda.current_stream()
-    steps = max(args.steps, 20)
+    steps = max(args.steps, 200)            # ~15 ms of steps: a few host hiccups do not dominate
     ncopy = len(mats[0][1])
 
     def run(n):
@@ -365,7 +370,7 @@ def e2e_ours(w4, mats, dev, args, gemm_ok):
             hy_all.copy_(dy_all, non_blocking=True)
         torch.cuda.synchronize()
 
-    run(3)
+    run(50)                                 # the host path (binding, caches, launch) warmed up
     t = time.perf_counter()
     run(steps)
     dt_ms = max_over_ranks([(time.perf_counter() - t) * 1e3], dev)[0]      # the slowest rank's

@@ -111,17 +111,31 @@ W4A16_API w4a16_status w4a16_pack(const void* w_f16, int64_t N, int64_t K, int G
                         uint32_t* qweight, void* scales_f16, uint32_t* zeros,
                         w4a16_stream_t stream);
 
-/* ---- dequantise (checking aid) -----------------------------------------------
- * w4a16_dequant: w_out FP32 [N,K] = (q - z) * s, through the same in-register
- * unpack routine the linear kernels use.  Exact in FP32.  Intended for tests
- * and debugging; the linear entry points never call it and never expand
- * weights in device memory.
+/* ---- dequantise (checking aids) ----------------------------------------------
+ * Each aid expands every packed word with one layer kernel's own inline
+ * routine (the same functions the kernel calls, not a separate
+ * implementation), so a bit-exact comparison of its output with the
+ * definition W_hat = (q - z) * s checks the instructions the layer runs: the
+ * nibble-to-FP16 expansion, the zero-point and scale extraction, and the
+ * order in which codes land in registers.  The linear entry points never call
+ * them and never expand weights in device memory.
+ *
+ * w4a16_dequant: w_out FP32 [N,K] = (q - z) * s through the decode kernel's
+ *   expansion (codes as the exact FP16 values 1024 + q and 64 + q, zero point
+ *   and scale as that kernel extracts them).  Exact in FP32.
+ * w4a16_dequant_debug: the same call under its checking-aid name (identical
+ *   arguments, behaviour and errors).
+ * w4a16_dequant_f16: w_out FP16 [N,K] = RN_fp16((q - z) * s) through the
+ *   tensor-core kernel's expansion: the FP16 operand it writes into tensor
+ *   memory (one rounding of the exact product).
+ * Errors: as w4a16_pack (shape, group size, null or misaligned pointers).
  */
 W4A16_API w4a16_status w4a16_dequant(const uint32_t* qweight, const void* scales_f16, const uint32_t* zeros,
                            int64_t N, int64_t K, int G, float* w_out, w4a16_stream_t stream);
-/* The same call under its checking-aid name: identical arguments, behaviour and errors. */
 W4A16_API w4a16_status w4a16_dequant_debug(const uint32_t* qweight, const void* scales_f16, const uint32_t* zeros,
                                            int64_t N, int64_t K, int G, float* w_out, w4a16_stream_t stream);
+W4A16_API w4a16_status w4a16_dequant_f16(const uint32_t* qweight, const void* scales_f16, const uint32_t* zeros,
+                                         int64_t N, int64_t K, int G, void* w_out_f16, w4a16_stream_t stream);
 
 /* ---- the layer ---------------------------------------------------------------
  * w4a16_linear: y[M,N] (BF16) = x[M,K] (BF16) * W_hat^T, FP32 accumulation,
@@ -170,12 +184,26 @@ W4A16_API w4a16_status w4a16_linear_gemm(const void* x_bf16, const uint32_t* qwe
                                void* y_bf16, w4a16_stream_t stream);
 
 /*
+ * w4a16_linear_f32: the layer with an FP32 output y_f32 [M,N]: the kernels'
+ * FP32 sums without the final BF16 rounding (for a caller that accumulates a
+ * residual in FP32, and to check the kernels' arithmetic against a bound
+ * tighter than the BF16 output allows).  path: 0 = the kernel w4a16_linear
+ * would choose, 1 = the decode kernel (as w4a16_linear_gemv), 2 = the
+ * tensor-core kernel.  Other arguments and errors as w4a16_linear; a path
+ * outside 0..2 is W4A16_ERR_INVALID_ARG.
+ */
+W4A16_API w4a16_status w4a16_linear_f32(const void* x_bf16, const uint32_t* qweight, const void* scales_f16,
+                                        const uint32_t* zeros, int64_t M, int64_t N, int64_t K, int G, int path,
+                                        float* y_f32, w4a16_stream_t stream);
+
+/*
  * w4a16_linear_gemm_noalloc: the tensor-core path of w4a16_linear_gemm for
- * callers that may not allocate device memory while they run the layer (an
- * engine that fixes its memory budget at start-up and forbids later
- * allocations, or code that records its launches into a CUDA graph that must
- * hold no memory nodes).  The pages this library follows have no counterpart
- * to this entry point; it is a deployment variant of the same computation.
+ * callers that may not allocate device memory while they run the layer: an
+ * engine that reserves its whole memory budget at start-up and forbids any
+ * later allocation, so that a running model never fails half-way on an
+ * out-of-memory error or fragments a pool it manages itself.  The pages this
+ * library follows have no counterpart to this entry point; it is a
+ * deployment variant of the same computation.
  *
  * Same arguments and result as w4a16_linear_gemm.  The per-call FP16 copy of
  * x, which the allocating entry points take from a stream-ordered pool, here
@@ -293,6 +321,11 @@ W4A16_API w4a16_status w8a16_linear(const void* x_bf16, const uint32_t* qweight,
  * 77312 (not even 8 weight rows and one activation row fit).
  */
 W4A16_API int64_t q4k_meta_ld(int64_t K);   /* uint32 words per meta row: K/256*4 (0 if K % 256) */
+/* Checking aid: w_out FP32 [N,K] = d*sc_j*q - dmin*m_j through the decode kernel's super-block
+ * decoding (its code expansion and record fields), s = d*sc_j and mn = dmin*m_j exact, then s*q
+ * (exact) minus mn rounded once.  Errors as q4k_pack. */
+W4A16_API w4a16_status q4k_dequant(const uint32_t* qweight, const uint32_t* meta, int64_t N, int64_t K,
+                                   float* w_out, w4a16_stream_t stream);
 W4A16_API w4a16_status q4k_pack(const void* w_f16, int64_t N, int64_t K, uint32_t* qweight, uint32_t* meta,
                                 w4a16_stream_t stream);
 /* y[M,N] (BF16) = x[M,K] (BF16) * W_hat^T, FP32 accumulation, one BF16 rounding per output. */
@@ -312,14 +345,38 @@ W4A16_API w4a16_status q4k_linear_dual(const void* x_bf16, const uint32_t* qweig
 W4A16_API int w4a16_linear_path(int64_t M, int64_t N, int64_t K, int G);
 
 /*
- * Every bounded wait inside the kernels (a tensor-core pipeline barrier that
- * never completes) gives up after a fixed spin budget, records a code in a
- * per-device status word and lets the kernel return.  This call synchronises
+ * Every wait inside the kernels on an asynchronous copy or a pipeline barrier
+ * is bounded: after a spin budget (default 2^31 SM cycles, about 1 s) the
+ * waiting warp records a code in a per-device status word, the kernel stops
+ * issuing work, waits (again bounded) for the copies and MMAs it did issue,
+ * frees its tensor memory and returns; nothing traps.  This call synchronises
  * the current device, returns W4A16_ERR_TIMEOUT if any kernel recorded a
  * give-up since the last call (and clears the word), else W4A16_OK.  *detail
- * (optional) receives the raw word.
+ * (optional) receives the raw word: bit 0 tensor-core producer, 1 its MMA
+ * issuer, 2 its dequantisers, 3 its epilogue, 4 a tensor-core drain that also
+ * ran out, 8 the decode kernel, 9 a decode drain that also ran out.
  */
 W4A16_API w4a16_status w4a16_device_status(uint32_t* detail);
+
+/*
+ * Testing hooks for the give-up path above (not needed in normal use).  The
+ * pages this library follows have no counterpart; they exist so that a test
+ * can make a wait run out without faulting, trapping or hanging the GPU.
+ * w4a16_debug_set_wait_limit: the spin budget, in SM cycles, of every bounded
+ *   wait in launches made after the call (any device, any thread); cycles <= 0
+ *   restores the default.
+ * w4a16_debug_withhold_copy: arms the NEXT launch of one kernel (1 = decode
+ *   kernel, 2 = tensor-core kernel; 0 disarms) to withhold one copy by
+ *   construction: the decode kernel's first warp of its first block never
+ *   issues its first unit of weights, the tensor-core kernel's first block
+ *   never issues its first slice of codes.  No copy or MMA is ever in flight
+ *   against the withheld barrier, so the waiting warps give up after the spin
+ *   budget, the kernel drains what it did issue and returns; that launch's
+ *   outputs are undefined and w4a16_device_status reports the timeout.
+ *   W4A16_ERR_INVALID_ARG for a kernel outside 0..2.
+ */
+W4A16_API void w4a16_debug_set_wait_limit(int64_t cycles);
+W4A16_API w4a16_status w4a16_debug_withhold_copy(int kernel);
 
 #ifdef __cplusplus
 }

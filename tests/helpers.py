@@ -73,8 +73,18 @@ def rel_bound(y_ref):
     return max(REL_L2, rounding_only_rel(y_ref) + 5e-4)
 
 
+# Every comparison's relative L2 error and literal max |err| / rms(y_ref), kept for the
+# end-of-session summary (conftest.py): (what, relL2, literal max-abs ratio, FP32 output?).
+LITERAL_LOG = []
+
+
+def record_literal(what, rel, lit, fp32=False):
+    LITERAL_LOG.append((what, float(rel), float(lit), bool(fp32)))
+
+
 def assert_close(y, y_ref, what=""):
     rel, maxrel, worst = error_stats(y, y_ref)
+    record_literal(what, rel, maxrel)
     bound = rel_bound(y_ref)
     assert rel <= bound, f"{what}: relL2 {rel:.3e} > {bound:.3e}"
     assert worst <= 1.0, f"{what}: max-abs bound exceeded by x{worst:.3f} (max|err|/rms = {maxrel:.3e})"

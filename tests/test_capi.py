@@ -104,6 +104,37 @@ def test_pack_and_dequant_argument_errors():
     assert w4._lib.w4a16_dequant(a, a, a, 64, 256, 128, v(0), v(0)) == 1
 
 
+def test_dequant_f16_and_q4k_dequant_argument_errors():
+    v = ctypes.c_void_p
+    a = v(1 << 12)
+    f = w4._lib.w4a16_dequant_f16
+    assert f(a, a, a, 64, 256, 100, a, v(0)) == 2
+    assert f(a, a, a, 60, 256, 128, a, v(0)) == 1
+    assert f(a, a, a, 64, 256, 128, v(0), v(0)) == 1
+    assert f(a, a, a, 64, 256, 128, v((1 << 12) + 4), v(0)) == 3
+    assert f(a, a, a, 0, 256, 128, a, v(0)) == 0
+    g = w4._lib.q4k_dequant
+    assert g(a, a, 64, 300, a, v(0)) == 1                # K % 256
+    assert g(a, a, 60, 256, a, v(0)) == 1                # N % 8
+    assert g(a, v(0), 64, 256, a, v(0)) == 1
+    assert g(a, a, 64, 256, v((1 << 12) + 8), v(0)) == 3
+    assert g(a, a, 0, 256, a, v(0)) == 0
+
+
+def test_linear_f32_argument_errors():
+    v = ctypes.c_void_p
+    a = v(1 << 12)
+    f = w4._lib.w4a16_linear_f32
+    for path in (0, 1, 2):
+        assert f(a, a, a, a, 1, 64, 256, 48, path, a, v(0)) == 2
+        assert f(a, a, a, a, 1, 60, 256, 128, path, a, v(0)) == 1
+        assert f(a, a, a, a, 1, 64, 256, 128, path, v(0), v(0)) == 1
+        assert f(a, a, a, a, 1, 64, 256, 128, path, v((1 << 12) + 4), v(0)) == 3
+        assert f(a, a, a, a, 0, 64, 256, 128, path, a, v(0)) == 0
+    assert f(a, a, a, a, 1, 64, 256, 128, 3, a, v(0)) == 1          # no such path
+    assert f(a, a, a, a, 1, 64, 256, 128, -1, a, v(0)) == 1
+
+
 def test_dual_argument_errors():
     v = ctypes.c_void_p
     a = v(1 << 12)
@@ -204,3 +235,45 @@ def test_dispatch_falls_back_when_the_gemv_does_not_fit():
     # x staged as M*K FP16 plus G = 32 tables: at K = 65536 not even one row fits the decode kernel
     assert w4.w4a16_linear_path(1, 8192, 65536, 32) == 2
     assert w4.w4a16_linear_path(1, 8192, 65536, 128) == 1
+
+
+def test_withhold_hook_rejects_unknown_kernels():
+    assert w4._lib.w4a16_debug_withhold_copy(3) == 1
+    assert w4._lib.w4a16_debug_withhold_copy(-1) == 1
+    assert w4._lib.w4a16_debug_withhold_copy(0) == 0          # disarmed
+    w4._lib.w4a16_debug_set_wait_limit(0)                      # default budget
+
+
+def test_entry_points_from_several_threads():
+    """The host-side state (device attributes, tensor-map cache, per-kernel
+    attribute caches, the test hooks) is shared by every thread; calls from
+    several threads at once must give each caller its own, correct answer.
+    Without a GPU only the host paths run: dispatch queries, layout helpers and
+    argument validation."""
+    import threading
+    v = ctypes.c_void_p
+    a = v(1 << 12)
+    expect = {(M, N, K, G): w4.w4a16_linear_path(M, N, K, G)
+              for M in (1, 4, 8, 16, 300) for N in (264, 4096, 13824) for K in (1024, 5120) for G in (32, 128)}
+    errors = []
+
+    def worker(seed):
+        try:
+            for i in range(300):
+                for key, path in expect.items():
+                    if w4.w4a16_linear_path(*key) != path:
+                        errors.append(("path", key))
+                K = 256 * (1 + (i + seed) % 8)
+                if w4.w4a16_scales_ld(K, 128) != ((K // 128 + 7) // 8) * 8:
+                    errors.append(("lds", K))
+                if w4._lib.w4a16_linear(a, a, a, a, 1, 60, K, 128, a, v(0)) != 1:
+                    errors.append(("validate", K))
+        except Exception as e:          # pragma: no cover - reported below
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=worker, args=(t,)) for t in range(4)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors[:5]

@@ -75,7 +75,7 @@ def test_gemm_and_gemv_agree_on_small_batches():
     assert_close(yb, y_ref, "gemv")
 
 
-@pytest.mark.parametrize("G", [32, 128])
+@pytest.mark.parametrize("G", [32, 64, 128, 256])
 def test_gemm_one_hot_rows(G):
     """x rows = e_k: y[i, n] = bf16_rn(fp16_rn(W_hat[n, k_i])).  The kernel's
     weight operand is W_hat rounded once to FP16, and a single product by 1.0

@@ -1,9 +1,10 @@
 """The allocation-free tensor-core entry point, called through the C ABI.
 
 w4a16_linear_gemm_noalloc serves callers that may not allocate device memory
-while they run the layer (a fixed memory budget, or launches recorded into a
-CUDA graph that must hold no memory nodes): its FP16 copy of x sits in one
-fixed device array shared by every call.  These tests check that two calls in
+while they run the layer (an engine that reserves its whole memory budget at
+start-up and forbids later allocations, so a running model never fails
+half-way on an out-of-memory error): its FP16 copy of x sits in one fixed
+device array shared by every call.  These tests check that two calls in
 a row (different shapes, so the second overwrites what the first left in the
 array) each match the allocating entry point w4a16_linear_gemm within the
 output tolerance of helpers.py, and that a problem too large for the array is

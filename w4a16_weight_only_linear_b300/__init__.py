@@ -34,6 +34,9 @@ EXPORTS = {
     "w4a16_pack": ([_vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp], _i32),
     "w4a16_dequant": ([_vp, _vp, _vp, _i64, _i64, _i32, _vp, _vp], _i32),
     "w4a16_dequant_debug": ([_vp, _vp, _vp, _i64, _i64, _i32, _vp, _vp], _i32),
+    "w4a16_dequant_f16": ([_vp, _vp, _vp, _i64, _i64, _i32, _vp, _vp], _i32),
+    "w4a16_linear_f32": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _vp, _vp], _i32),
+    "q4k_dequant": ([_vp, _vp, _i64, _i64, _vp, _vp], _i32),
     "w4a16_linear": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp], _i32),
     "w4a16_linear_dual": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp, _vp], _i32),
     "w4a16_linear_gemv": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp], _i32),
@@ -53,6 +56,8 @@ EXPORTS = {
     "q4k_linear_dual": ([_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp, _vp], _i32),
     "w4a16_linear_path": ([_i64, _i64, _i64, _i32], _i32),
     "w4a16_device_status": ([_vp], _i32),
+    "w4a16_debug_set_wait_limit": ([_i64], None),
+    "w4a16_debug_withhold_copy": ([_i32], _i32),
 }
 
 
@@ -144,12 +149,37 @@ def w4a16_pack(w, G, out=None, stream=None):
 
 
 def w4a16_dequant(q, s, z, N, K, G, out=None, stream=None):
-    """W_hat FP32 [N,K] = (q - z) * s, through the kernels' unpack routine (checking aid)."""
+    """W_hat FP32 [N,K] = (q - z) * s, through the decode kernel's own expansion
+    routine (checking aid)."""
     if out is None:
         out = torch.empty((N, K), dtype=torch.float32, device=q.device)
     _check("w4a16_dequant", _lib.w4a16_dequant(_dev(q, torch.int32, "qweight"), _dev(s, torch.float16, "scales"),
                                                _dev(z, torch.int32, "zeros"), N, K, G,
                                                _dev(out, torch.float32, "out"), _stream(stream)))
+    return out
+
+
+def w4a16_dequant_f16(q, s, z, N, K, G, out=None, stream=None):
+    """RN_fp16(W_hat) FP16 [N,K], through the tensor-core kernel's own expansion
+    routine (the operand it writes into tensor memory; checking aid)."""
+    if out is None:
+        out = torch.empty((N, K), dtype=torch.float16, device=q.device)
+    _check("w4a16_dequant_f16", _lib.w4a16_dequant_f16(
+        _dev(q, torch.int32, "qweight"), _dev(s, torch.float16, "scales"), _dev(z, torch.int32, "zeros"), N, K, G,
+        _dev(out, torch.float16, "out"), _stream(stream)))
+    return out
+
+
+def w4a16_linear_f32(x, q, s, z, G, path=0, out=None, stream=None):
+    """y FP32 [M,N] = x * W_hat^T without the BF16 output rounding.  path: 0 =
+    the kernel w4a16_linear would choose, 1 = decode kernel, 2 = tensor-core kernel."""
+    M, K = x.shape
+    N = q.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    _check("w4a16_linear_f32", _lib.w4a16_linear_f32(
+        _dev(x, torch.bfloat16, "x"), _dev(q, torch.int32, "qweight"), _dev(s, torch.float16, "scales"),
+        _dev(z, torch.int32, "zeros"), M, N, K, G, path, _dev(out, torch.float32, "y"), _stream(stream)))
     return out
 
 
@@ -288,6 +318,16 @@ def q4k_pack(w, out=None, stream=None):
     return q, meta
 
 
+def q4k_dequant(q, meta, N, K, out=None, stream=None):
+    """W_hat FP32 [N,K] of the super-block layout, through the decode kernel's own
+    code expansion and record decoding (checking aid)."""
+    if out is None:
+        out = torch.empty((N, K), dtype=torch.float32, device=q.device)
+    _check("q4k_dequant", _lib.q4k_dequant(_dev(q, torch.int32, "qweight"), _dev(meta, torch.int32, "meta"), N, K,
+                                           _dev(out, torch.float32, "out"), _stream(stream)))
+    return out
+
+
 def q4k_linear(x, q, meta, out=None, stream=None):
     """y BF16 [M,N] = x BF16 [M,K] * W_hat^T for the super-block layout (N from qweight's rows)."""
     M, K = x.shape
@@ -325,3 +365,11 @@ def w4a16_device_status():
     word = ctypes.c_uint32(0)
     _check("w4a16_device_status", _lib.w4a16_device_status(ctypes.byref(word)))
     return word.value
+
+
+def device_status_word():
+    """Synchronise; (status, raw word) of w4a16_device_status without raising:
+    W4A16_ERR_TIMEOUT (5) with the give-up bits, or 0."""
+    word = ctypes.c_uint32(0)
+    st = _lib.w4a16_device_status(ctypes.byref(word))
+    return st, word.value

@@ -242,6 +242,39 @@ w4a16_status w4a16_dequant_debug(const uint32_t* qweight, const void* scales_f16
     return w4a16_dequant(qweight, scales_f16, zeros, N, K, G, w_out, stream);
 }
 
+w4a16_status w4a16_dequant_f16(const uint32_t* qweight, const void* scales_f16, const uint32_t* zeros, int64_t N,
+                               int64_t K, int G, void* w_out_f16, w4a16_stream_t stream) {
+    w4a16_status st = check_weight_shape(N, K, G);
+    if (st != W4A16_OK) return st;
+    if (N == 0) return W4A16_OK;
+    if ((st = check_weights(qweight, scales_f16, zeros)) != W4A16_OK) return st;
+    if (!w_out_f16) return W4A16_ERR_INVALID_ARG;
+    if (!aligned16(w_out_f16)) return W4A16_ERR_MISALIGNED;
+    return from_cuda(w4a16::launch_dequant_f16(qweight, scales_f16, zeros, N, K, G, w_out_f16,
+                                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w4a16_linear_f32(const void* x_bf16, const uint32_t* qweight, const void* scales_f16,
+                              const uint32_t* zeros, int64_t M, int64_t N, int64_t K, int G, int path, float* y_f32,
+                              w4a16_stream_t stream) {
+    if (path < 0 || path > 2) return W4A16_ERR_INVALID_ARG;
+    w4a16_status st = check_weight_shape(N, K, G);
+    if (st != W4A16_OK) return st;
+    if (M < 0 || M > kMaxDim) return W4A16_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return W4A16_OK;
+    if ((st = check_weights(qweight, scales_f16, zeros)) != W4A16_OK) return st;
+    if (!x_bf16 || !y_f32) return W4A16_ERR_INVALID_ARG;
+    if (!aligned16(x_bf16) || !aligned16(y_f32)) return W4A16_ERR_MISALIGNED;
+    if (path == 0) path = choose_path(M, N, K, G, 1);
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    GemvMat mat{qweight, scales_f16, zeros, y_f32};
+    if (path == 1) {
+        if (M > 16 || !w4a16::gemv_fits(M, N, K, G, 1)) return W4A16_ERR_UNSUPPORTED;
+        return from_cuda(w4a16::launch_gemv(x_bf16, &mat, 1, M, N, K, G, cs, nullptr, 0, false, true));
+    }
+    return from_cuda(w4a16::launch_gemm(x_bf16, &mat, 1, M, N, K, G, cs, nullptr, 0, true));
+}
+
 w4a16_status w4a16_linear(const void* x_bf16, const uint32_t* qweight, const void* scales_f16,
                           const uint32_t* zeros, int64_t M, int64_t N, int64_t K, int G, void* y_bf16,
                           w4a16_stream_t stream) {
@@ -306,6 +339,17 @@ w4a16_status w4a16_linear_gemm_noalloc(const void* x_bf16, const uint32_t* qweig
 
 int64_t q4k_meta_ld(int64_t K) { return K > 0 && K % 256 == 0 ? K / 256 * 4 : 0; }
 
+w4a16_status q4k_dequant(const uint32_t* qweight, const uint32_t* meta, int64_t N, int64_t K, float* w_out,
+                         w4a16_stream_t stream) {
+    w4a16_status st = check_q4k_shape(N, K);
+    if (st != W4A16_OK) return st;
+    if (N == 0) return W4A16_OK;
+    if ((st = check_q4k_weights(qweight, meta)) != W4A16_OK) return st;
+    if (!w_out) return W4A16_ERR_INVALID_ARG;
+    if (!aligned16(w_out)) return W4A16_ERR_MISALIGNED;
+    return from_cuda(w4a16::launch_dequant_q4k(qweight, meta, N, K, w_out, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 w4a16_status q4k_pack(const void* w_f16, int64_t N, int64_t K, uint32_t* qweight, uint32_t* meta,
                       w4a16_stream_t stream) {
     w4a16_status st = check_q4k_shape(N, K);
@@ -334,6 +378,14 @@ w4a16_status q4k_linear_dual(const void* x_bf16, const uint32_t* qweight_gate, c
 int w4a16_linear_path(int64_t M, int64_t N, int64_t K, int G) {
     if (check_weight_shape(N, K, G) != W4A16_OK || M < 0) return 0;
     return choose_path(M, N, K, G, 1);
+}
+
+void w4a16_debug_set_wait_limit(int64_t cycles) { w4a16::set_wait_limit(cycles); }
+
+w4a16_status w4a16_debug_withhold_copy(int kernel) {
+    if (kernel < 0 || kernel > 2) return W4A16_ERR_INVALID_ARG;
+    w4a16::arm_withhold(kernel);
+    return W4A16_OK;
 }
 
 w4a16_status w4a16_device_status(uint32_t* detail) {

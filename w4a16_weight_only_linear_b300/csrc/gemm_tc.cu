@@ -40,12 +40,14 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "../../include/w4a16.h"
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
+#include "unpack.cuh"
 
 namespace w4a16 {
 
@@ -62,7 +64,6 @@ constexpr int kAS = 8;                     // A ring in TMEM: slices of 64 k (32
 constexpr uint32_t kCodeStageBytes = 128u * 128u;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kACol0 = 256;           // D uses columns [0, BN), A slices [256, 512)
-constexpr long long kSpinCycles = 1ll << 31;
 constexpr int kNumBars = 2 * kXS + 2 * kCS + 2 * kAS + 2;
 
 // Status codes (bit fields) recorded when a wait gives up.
@@ -75,11 +76,14 @@ constexpr uint32_t kStatusDrain = 1u << 4;
 struct GemmParams {
     const unsigned short* s;   // FP16 scales [N, lds]
     const uint32_t* z;         // packed zeros [N, ldz]
-    __nv_bfloat16* y;          // [M, N]
+    void* y;                   // [M, N], BF16 (or FP32 when yf32)
+    int yf32;                  // 1: FP32 outputs (no BF16 rounding)
     int M, N, K, BN;
     int lds, ldz, ngroups;
     int mtiles, tiles;
     int nk64, nk256;
+    long long spin_limit;      // cycles a bounded wait spins before it gives up
+    int withhold;              // test hook: CTA 0 never issues its first code copy
 };
 
 // Dynamic shared memory per CTA.  Never less than 120 KB, so at most one CTA
@@ -89,21 +93,6 @@ size_t gemm_smem_bytes(int BN) {
     return need < 120 * 1024 ? 120 * 1024 : need;
 }
 
-__device__ __forceinline__ uint32_t lop3_and_or_(uint32_t a, uint32_t b, uint32_t c) {
-    uint32_t d;
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-__device__ __forceinline__ uint32_t hsub2_rn(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-__device__ __forceinline__ uint32_t hmul2_rn(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
@@ -118,34 +107,6 @@ __device__ __forceinline__ uint32_t ldg32_nc(const void* p) {
     uint32_t v;
     asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
     return v;
-}
-
-// Eight codes (one packed word, k = 8j .. 8j+7) -> four FP16 pairs
-// (k = 8j+2i in the low half, 8j+2i+1 in the high half) of RN((q - z) * s).
-// Byte i of the word holds codes 2i (low nibble) and 2i+1 (high nibble);
-// PRMT copies it into both halves, one LOP3 keeps the low nibble in the low
-// half and the high nibble at bits 4..7 of the high half and ORs in the
-// FP16 exponents of 1024 (ulp 1) and 64 (ulp 1/16), giving 1024 + q and
-// 64 + q exactly.  zz holds 1024 + z and 64 + z, so the packed subtraction
-// is the exact code difference, and one packed multiply rounds it times s.
-__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t s2, uint32_t zz, uint32_t* out) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t r = __byte_perm(w, 0u, 0x4040u + 0x0101u * i);
-        const uint32_t t = lop3_and_or_(r, 0x00F0000Fu, 0x54006400u);
-        out[i] = hmul2_rn(hsub2_rn(t, zz), s2);
-    }
-}
-
-// Scale (both halves) and zero offsets of group h of an 8-group chunk.
-__device__ __forceinline__ void group_consts(const uint4& sv, uint32_t zw, int h, bool valid, uint32_t& s2,
-                                             uint32_t& zz) {
-    const uint32_t word = (h & 4) ? ((h & 2) ? sv.w : sv.z) : ((h & 2) ? sv.y : sv.x);
-    uint32_t sb = (h & 1) ? (word >> 16) : (word & 0xFFFFu);
-    sb = valid ? sb : 0u;
-    const uint32_t z = (zw >> (4 * h)) & 0xFu;
-    s2 = sb | (sb << 16);
-    zz = ((0x5400u | (z << 4)) << 16) | (0x6400u | z);
 }
 
 struct Smem {
@@ -164,15 +125,15 @@ struct Smem {
     __device__ uint32_t d_empty() const { return tc::smem_u32(bar + 2 * kXS + 2 * kCS + 2 * kAS + 1); }
 };
 
-// Bounded wait for a barrier phase; gives up (recording `site`) after
-// kSpinCycles, or at once when another role has given up.
-__device__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint32_t site) {
+// Bounded wait for a barrier phase; gives up (recording `site`) after `limit`
+// cycles, or at once when another role has given up.
+__device__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint32_t site, long long limit) {
     if (tc::mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
         if (tc::mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (clock64() - t0 > kSpinCycles) {
+        if (clock64() - t0 > limit) {
             *abort_flag = 1;
             atomicOr(&g_status_word, site);
             return false;
@@ -181,10 +142,10 @@ __device__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_fl
 }
 
 // Bounded wait used while shutting down after a give-up: ignores the abort flag.
-__device__ void drain_phase(uint32_t bar, uint32_t parity) {
+__device__ void drain_phase(uint32_t bar, uint32_t parity, long long limit) {
     const long long t0 = clock64();
     while (!tc::mbar_try_wait(bar, parity)) {
-        if (clock64() - t0 > kSpinCycles) {
+        if (clock64() - t0 > limit) {
             atomicOr(&g_status_word, kStatusDrain);
             return;
         }
@@ -242,18 +203,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t xph = 0, cph = 0;
             long long x_issued = 0, c_issued = 0;
             bool ok = true;
+            // test hook: CTA 0 skips its first code copy (slot 0, never refilled since its
+            // consumers never release it), so the dequantisers' wait on it runs out
+            const bool withhold = p.withhold && blockIdx.x == 0;
             for (int t = blockIdx.x; t < p.tiles && ok; t += gridDim.x) {
                 const int n0 = (t / p.mtiles) * kBM, m0 = (t % p.mtiles) * p.BN;
                 for (int kb = 0; kb < p.nk64; ++kb) {
                     if ((kb & 3) == 0) {
-                        if (!(ok = wait_phase(sm.c_empty(ci), cph ^ 1u, sm.abort_flag, kStatusProducer))) break;
-                        tc::mbar_arrive_expect_tx(sm.c_full(ci), kCodeStageBytes);
-                        tc::tma_load_2d(tc::smem_u32(sm.c + ci * kCodeStageBytes), &tm_q, (kb >> 2) * 32, n0,
-                                        sm.c_full(ci));
+                        if (!(ok = wait_phase(sm.c_empty(ci), cph ^ 1u, sm.abort_flag, kStatusProducer, p.spin_limit))) break;
+                        if (!(withhold && c_issued == 0)) {
+                            tc::mbar_arrive_expect_tx(sm.c_full(ci), kCodeStageBytes);
+                            tc::tma_load_2d(tc::smem_u32(sm.c + ci * kCodeStageBytes), &tm_q, (kb >> 2) * 32, n0,
+                                            sm.c_full(ci));
+                        }
                         ++c_issued;
                         if (++ci == kCS) { ci = 0; cph ^= 1u; }
                     }
-                    if (!(ok = wait_phase(sm.x_empty(xi), xph ^ 1u, sm.abort_flag, kStatusProducer))) break;
+                    if (!(ok = wait_phase(sm.x_empty(xi), xph ^ 1u, sm.abort_flag, kStatusProducer, p.spin_limit))) break;
                     tc::mbar_arrive_expect_tx(sm.x_full(xi), xbytes);
                     tc::tma_load_2d(tc::smem_u32(sm.x + xi * xbytes), &tm_x, kb * 64, m0, sm.x_full(xi));
                     ++x_issued;
@@ -262,9 +228,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) {   // wait for the copies this thread started
                 for (int s = 0; s < kXS; ++s)
-                    if (x_issued > s) drain_phase(sm.x_full(s), s < xi ? xph : (xph ^ 1u));
+                    if (x_issued > s) drain_phase(sm.x_full(s), s < xi ? xph : (xph ^ 1u), p.spin_limit);
                 for (int s = 0; s < kCS; ++s)
-                    if (c_issued > s) drain_phase(sm.c_full(s), s < ci ? cph : (cph ^ 1u));
+                    if (c_issued > s && !(withhold && s == 0 && c_issued <= kCS)) drain_phase(sm.c_full(s), s < ci ? cph : (cph ^ 1u), p.spin_limit);
             }
         }
     } else if (warp == 1) {
@@ -276,12 +242,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             bool issued = false;
             for (int t = blockIdx.x; t < p.tiles && ok; t += gridDim.x) {
-                if (!(ok = wait_phase(sm.d_empty(), dph ^ 1u, sm.abort_flag, kStatusMma))) break;
+                if (!(ok = wait_phase(sm.d_empty(), dph ^ 1u, sm.abort_flag, kStatusMma, p.spin_limit))) break;
                 dph ^= 1u;
                 tc::tc_fence_after();
                 for (int kb = 0; kb < p.nk64; ++kb) {
-                    if (!(ok = wait_phase(sm.x_full(xi), xph, sm.abort_flag, kStatusMma))) break;
-                    if (!(ok = wait_phase(sm.a_full(ai), aph, sm.abort_flag, kStatusMma))) break;
+                    if (!(ok = wait_phase(sm.x_full(xi), xph, sm.abort_flag, kStatusMma, p.spin_limit))) break;
+                    if (!(ok = wait_phase(sm.a_full(ai), aph, sm.abort_flag, kStatusMma, p.spin_limit))) break;
                     tc::tc_fence_after();
                     const uint64_t bdesc = tc::smem_desc_k_sw128(tc::smem_u32(sm.x + xi * xbytes));
                     const uint32_t a_t = tmem + kACol0 + (uint32_t)ai * 32u;
@@ -301,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok && issued) {   // wait for the MMAs this thread issued
                 tc::mma_commit(sm.d_full());
-                drain_phase(sm.d_full(), d_commits & 1u);
+                drain_phase(sm.d_full(), d_commits & 1u, p.spin_limit);
             }
         }
     } else if (warp < 6) {
@@ -325,12 +291,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     sv = ldg128_nc(srow + chunk * 8);
                     zw = ldg32_nc(zrow + chunk);
                 }
-                ok = wait_phase(sm.c_full(ci), cph, sm.abort_flag, kStatusDequant);
+                ok = wait_phase(sm.c_full(ci), cph, sm.abort_flag, kStatusDequant, p.spin_limit);
                 if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
                 const uint32_t rowp = tc::smem_u32(sm.c + ci * kCodeStageBytes) + (uint32_t)r * 128u;
                 const int nsub = min(4, p.nk64 - ks * 4);
                 for (int sub = 0; sub < nsub; ++sub) {
-                    ok = wait_phase(sm.a_empty(ai), aph ^ 1u, sm.abort_flag, kStatusDequant);
+                    ok = wait_phase(sm.a_empty(ai), aph ^ 1u, sm.abort_flag, kStatusDequant, p.spin_limit);
                     if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
                     tc::tc_fence_after();
                     const uint4 w0 = lds128(rowp + ((uint32_t)((2 * sub) ^ (r & 7)) << 4));
@@ -374,10 +340,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int t = blockIdx.x; t < p.tiles && ok; t += gridDim.x) {
             const int n = (t / p.mtiles) * kBM + r, m0 = (t % p.mtiles) * p.BN;
-            ok = wait_phase(sm.d_full(), dph, sm.abort_flag, kStatusEpilogue);
+            ok = wait_phase(sm.d_full(), dph, sm.abort_flag, kStatusEpilogue, p.spin_limit);
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
             dph ^= 1u;
             tc::tc_fence_after();
+            if (p.yf32) {
+                // FP32 output (no BF16 rounding): each 32-column chunk is stored as loaded, and the
+                // accumulator is released after the last one
+#pragma unroll 1
+                for (int ch = 0; ch < 8; ++ch) {
+                    if (ch * 32 < p.BN) {
+                        uint32_t v[32];
+                        tc::tmem_ld32_wait(d_lane + (uint32_t)ch * 32u, v);
+                        if (n < p.N) {
+                            float* yc = static_cast<float*>(p.y) + n;
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {
+                                const int m = m0 + ch * 32 + j;
+                                if (m < p.M) yc[(int64_t)m * p.N] = __uint_as_float(v[j]);
+                            }
+                        }
+                    }
+                }
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(sm.d_empty());
+                continue;
+            }
             uint32_t packed[128];
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch) {
@@ -462,113 +451,38 @@ __global__ void __launch_bounds__(256) bf16_to_f16_kernel(const uint4* __restric
 
 // ---- host side -----------------------------------------------------------------
 
-constexpr int kMaxDevices = 64;
-
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    });
-    return fn;
-}
-
-// 2-D row-major tensor [outer][inner], 128-byte swizzled boxes.
-bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
-                 uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
-    auto enc = tensor_map_encoder();
-    if (!enc) return false;
-    cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {row_bytes};
-    cuuint32_t box[2] = {box_inner, box_outer};
-    cuuint32_t es[2] = {1, 1};
-    return enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// Stream-ordered scratch from a library-private pool per device, which keeps
-// up to 1 GiB cached between calls.
-cudaError_t scratch_alloc(void** ptr, size_t bytes, cudaStream_t stream) {
-    static cudaMemPool_t pools[kMaxDevices] = {};
-    static std::mutex mu;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    cudaMemPool_t pool;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (!pools[dev]) {
-            cudaMemPoolProps props = {};
-            props.allocType = cudaMemAllocationTypePinned;
-            props.location.type = cudaMemLocationTypeDevice;
-            props.location.id = dev;
-            e = cudaMemPoolCreate(&pools[dev], &props);
-            if (e != cudaSuccess) {
-                pools[dev] = nullptr;
-                return e;
-            }
-            uint64_t keep = uint64_t(1) << 30;
-            cudaMemPoolSetAttribute(pools[dev], cudaMemPoolAttrReleaseThreshold, &keep);
-        }
-        pool = pools[dev];
-    }
-    return cudaMallocFromPoolAsync(ptr, bytes, pool, stream);
-}
-
 template <int G>
 cudaError_t launch_g(const CUtensorMap& tmx, const CUtensorMap& tmq, const GemmParams& p, int grid, size_t smem,
-                     cudaStream_t stream) {
-    static int cached[kMaxDevices] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    if ((int)smem > cached[dev]) {
-        e = cudaFuncSetAttribute(gemm_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                     int dev, cudaStream_t stream) {
+    // largest dynamic shared memory this instance is already allowed per device (a raise may
+    // race with another thread's: both set the attribute, the larger value stays)
+    static std::atomic<int> cached[kMaxDevices];
+    int have = cached[dev].load(std::memory_order_relaxed);
+    if ((int)smem > have) {
+        const cudaError_t e = cudaFuncSetAttribute(gemm_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        cached[dev] = (int)smem;
+        while (have < (int)smem && !cached[dev].compare_exchange_weak(have, (int)smem)) {
+        }
     }
     gemm_kernel<G><<<grid, kThreads, smem, stream>>>(tmx, tmq, p);
     return cudaGetLastError();
 }
 
-}  // namespace
+// Converts x (BF16 [M, kx]) into the FP16 B operand x16 [M, K] (see bf16_to_f16_kernel).
+cudaError_t convert_x(const void* x, void* x16, int64_t M, int64_t K, int64_t kx, const float* xsc, int sms,
+                      cudaStream_t stream) {
+    const int64_t nvec = M * K / 8;
+    int64_t blocks = (nvec + 255) / 256;
+    if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
+    bf16_to_f16_kernel<<<(unsigned)blocks, 256, 0, stream>>>(static_cast<const uint4*>(x), static_cast<uint4*>(x16),
+                                                             nvec, reinterpret_cast<const float4*>(xsc), K / 8,
+                                                             kx / 8);
+    return cudaGetLastError();
+}
 
-int gemm_tile_n(int64_t M) { return M >= 256 ? 256 : (int)((M + 31) / 32 * 32); }
-
-cudaError_t launch_gemm(const void* x, const GemvMat* mats, int nmat, int64_t M, int64_t N, int64_t K, int G,
-                        cudaStream_t stream, const float* xsc, int64_t kx) {
-    if (kx == 0) kx = K;
-    if (kx != K && (kx * 2 != K || kx % 8 != 0)) return cudaErrorInvalidValue;
-    if (M < 1 || N < 1 || K < 1) return cudaSuccess;
-    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX || K % 32 != 0) return cudaErrorInvalidValue;
-    if (!tensor_map_encoder()) return cudaErrorNotSupported;
-    int dev = 0, sms = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-
-    // FP16 copy of x (the B operand), shared by every matrix of the call
-    void* x16 = nullptr;
-    const size_t xbytes = (size_t)M * (size_t)K * 2;
-    if ((e = scratch_alloc(&x16, xbytes, stream)) != cudaSuccess) return e;
-    {
-        const int64_t nvec = M * K / 8;
-        int64_t blocks = (nvec + 255) / 256;
-        if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
-        bf16_to_f16_kernel<<<(unsigned)blocks, 256, 0, stream>>>(static_cast<const uint4*>(x),
-                                                                 static_cast<uint4*>(x16), nvec,
-                                                                 reinterpret_cast<const float4*>(xsc), K / 8, kx / 8);
-        e = cudaGetLastError();
-    }
-    GemmParams p;
+// Tiles, grid and the map of x16 for one call; false if a size is out of range.
+bool plan_gemm(int64_t M, int64_t N, int64_t K, int G, const void* x16, const DeviceInfo& di, GemmParams& p,
+               int& grid, size_t& smem, CUtensorMap& tmx) {
     p.M = (int)M;
     p.N = (int)N;
     p.K = (int)K;
@@ -578,35 +492,66 @@ cudaError_t launch_gemm(const void* x, const GemvMat* mats, int nmat, int64_t M,
     p.ngroups = (int)(K / G);
     p.mtiles = (int)((M + p.BN - 1) / p.BN);
     const int64_t tiles = ((N + kBM - 1) / kBM) * p.mtiles;
-    if (tiles > INT32_MAX) e = cudaErrorInvalidValue;
+    if (tiles > INT32_MAX) return false;
     p.tiles = (int)tiles;
     p.nk64 = (int)((K + 63) / 64);
     p.nk256 = (int)((K + 255) / 256);
-    const int grid = (int)(tiles < sms ? tiles : sms);
-    const size_t smem = gemm_smem_bytes(p.BN);
-    CUtensorMap tmx;
-    if (e == cudaSuccess &&
-        !make_map_2d(&tmx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x16, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, 64,
-                     (uint32_t)p.BN))
-        e = cudaErrorInvalidValue;
-    for (int i = 0; i < nmat && e == cudaSuccess; ++i) {
-        CUtensorMap tmq;
-        if (!make_map_2d(&tmq, CU_TENSOR_MAP_DATA_TYPE_UINT32, mats[i].q, (uint64_t)(K / 8), (uint64_t)N,
-                         (uint64_t)(K / 8) * 4, 32, kBM)) {
-            e = cudaErrorInvalidValue;
-            break;
-        }
-        p.s = static_cast<const unsigned short*>(mats[i].s);
-        p.z = mats[i].z;
-        p.y = static_cast<__nv_bfloat16*>(mats[i].y);
-        switch (G) {
-            case 32: e = launch_g<32>(tmx, tmq, p, grid, smem, stream); break;
-            case 64: e = launch_g<64>(tmx, tmq, p, grid, smem, stream); break;
-            case 128: e = launch_g<128>(tmx, tmq, p, grid, smem, stream); break;
-            case 256: e = launch_g<256>(tmx, tmq, p, grid, smem, stream); break;
-            default: e = cudaErrorInvalidValue;
-        }
+    grid = (int)(tiles < di.sms ? tiles : di.sms);
+    smem = gemm_smem_bytes(p.BN);
+    return encode_tmap_2d(&tmx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x16, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, 64,
+                          (uint32_t)p.BN, di.dev);
+}
+
+cudaError_t launch_one(const void* x16, const GemvMat& mat, const GemmParams& p0, int G, int grid, size_t smem,
+                       const CUtensorMap& tmx, int dev, cudaStream_t stream) {
+    CUtensorMap tmq;
+    if (!encode_tmap_2d(&tmq, CU_TENSOR_MAP_DATA_TYPE_UINT32, mat.q, (uint64_t)(p0.K / 8), (uint64_t)p0.N,
+                        (uint64_t)(p0.K / 8) * 4, 32, kBM, dev))
+        return cudaErrorInvalidValue;
+    GemmParams p = p0;
+    p.spin_limit = wait_limit();
+    p.withhold = take_withhold(2) ? 1 : 0;
+    p.s = static_cast<const unsigned short*>(mat.s);
+    p.z = mat.z;
+    p.y = mat.y;
+    switch (G) {
+        case 32: return launch_g<32>(tmx, tmq, p, grid, smem, dev, stream);
+        case 64: return launch_g<64>(tmx, tmq, p, grid, smem, dev, stream);
+        case 128: return launch_g<128>(tmx, tmq, p, grid, smem, dev, stream);
+        case 256: return launch_g<256>(tmx, tmq, p, grid, smem, dev, stream);
+        default: return cudaErrorInvalidValue;
     }
+}
+
+}  // namespace
+
+int gemm_tile_n(int64_t M) { return M >= 256 ? 256 : (int)((M + 31) / 32 * 32); }
+
+// The FP16 copy of x is taken from the device's current memory pool with a
+// stream-ordered allocation and freed on the stream after the call's kernels.
+// The library keeps no pool or cache of its own: what stays reserved between
+// calls is that pool's policy (its release threshold), which belongs to the
+// application.
+cudaError_t launch_gemm(const void* x, const GemvMat* mats, int nmat, int64_t M, int64_t N, int64_t K, int G,
+                        cudaStream_t stream, const float* xsc, int64_t kx, bool yf32) {
+    if (kx == 0) kx = K;
+    if (kx != K && (kx * 2 != K || kx % 8 != 0)) return cudaErrorInvalidValue;
+    if (M < 1 || N < 1 || K < 1) return cudaSuccess;
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX || K % 32 != 0) return cudaErrorInvalidValue;
+    if (!tmap_encoder_available()) return cudaErrorNotSupported;
+    DeviceInfo di;
+    cudaError_t e = current_device(di);
+    if (e != cudaSuccess) return e;
+    void* x16 = nullptr;
+    if ((e = cudaMallocAsync(&x16, (size_t)M * (size_t)K * 2, stream)) != cudaSuccess) return e;
+    e = convert_x(x, x16, M, K, kx, xsc, di.sms, stream);
+    GemmParams p;
+    p.yf32 = yf32 ? 1 : 0;
+    int grid = 0;
+    size_t smem = 0;
+    CUtensorMap tmx;
+    if (e == cudaSuccess && !plan_gemm(M, N, K, G, x16, di, p, grid, smem, tmx)) e = cudaErrorInvalidValue;
+    for (int i = 0; i < nmat && e == cudaSuccess; ++i) e = launch_one(x16, mats[i], p, G, grid, smem, tmx, di.dev, stream);
     const cudaError_t ef = cudaFreeAsync(x16, stream);
     return e != cudaSuccess ? e : ef;
 }
@@ -615,29 +560,25 @@ cudaError_t launch_gemm(const void* x, const GemvMat* mats, int nmat, int64_t M,
 // ---- tensor-core path without any allocation ----------------------------------
 //
 // Some callers cannot allocate device memory while they run the layer: an
-// engine that owns a fixed memory budget and forbids allocations after
-// start-up, or code that records its launches into a CUDA graph and must not
-// add memory nodes to it.  For them the FP16 copy of x lives in one
-// file-scope device array of fixed size instead of a stream-ordered
-// allocation.  Every GPU that loads the library holds this array until the
-// process exits.  All calls share it, so two calls whose kernels overlap on
-// the GPU (different streams, no ordering between them) race on its contents.
+// engine that reserves its whole memory budget at start-up and forbids any
+// later allocation, so that a running model never fails half-way on an
+// out-of-memory error.  For them the FP16 copy of x lives in one file-scope
+// device array of fixed size instead of a stream-ordered allocation.  Every
+// GPU that loads the library holds this array until the process exits.  All
+// calls share it, so two calls whose kernels overlap on the GPU (different
+// streams, no ordering between them) race on its contents.
 constexpr size_t kNoAllocScratchBytes = (size_t)W4A16_NOALLOC_MAX_X_ELEMS * 2;
 static __device__ __align__(256) uint8_t g_noalloc_x16[kNoAllocScratchBytes];
 
 // Device address of the array, looked up once per device with that device
 // current (in host code the symbol itself is only a host-side stand-in).
-cudaError_t noalloc_scratch(void** ptr) {
+cudaError_t noalloc_scratch(int dev, void** ptr) {
     static void* addr[kMaxDevices] = {};
     static std::mutex mu;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(mu);
     if (!addr[dev]) {
         void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_x16);
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_x16);
         if (e != cudaSuccess) return e;
         addr[dev] = p;
     }
@@ -650,54 +591,21 @@ cudaError_t launch_gemm_noalloc(const void* x, const GemvMat& mat, int64_t M, in
     if (M < 1 || N < 1 || K < 1) return cudaSuccess;
     if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX || K % 32 != 0) return cudaErrorInvalidValue;
     if (M * K > (int64_t)W4A16_NOALLOC_MAX_X_ELEMS) return cudaErrorNotSupported;
-    if (!tensor_map_encoder()) return cudaErrorNotSupported;
-    int dev = 0, sms = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    if (!tmap_encoder_available()) return cudaErrorNotSupported;
+    DeviceInfo di;
+    cudaError_t e = current_device(di);
     if (e != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     void* x16 = nullptr;
-    if ((e = noalloc_scratch(&x16)) != cudaSuccess) return e;
-    {
-        const int64_t nvec = M * K / 8;
-        int64_t blocks = (nvec + 255) / 256;
-        if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
-        bf16_to_f16_kernel<<<(unsigned)blocks, 256, 0, stream>>>(static_cast<const uint4*>(x),
-                                                                 static_cast<uint4*>(x16), nvec, nullptr, K / 8, K / 8);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
+    if ((e = noalloc_scratch(di.dev, &x16)) != cudaSuccess) return e;
+    // every element of the array this call reads is written first by the conversion
+    if ((e = convert_x(x, x16, M, K, K, nullptr, di.sms, stream)) != cudaSuccess) return e;
     GemmParams p;
-    p.M = (int)M;
-    p.N = (int)N;
-    p.K = (int)K;
-    p.BN = gemm_tile_n(M);
-    p.lds = (int)scales_ld(K, G);
-    p.ldz = (int)zeros_ld(K, G);
-    p.ngroups = (int)(K / G);
-    p.mtiles = (int)((M + p.BN - 1) / p.BN);
-    const int64_t tiles = ((N + kBM - 1) / kBM) * p.mtiles;
-    if (tiles > INT32_MAX) return cudaErrorInvalidValue;
-    p.tiles = (int)tiles;
-    p.nk64 = (int)((K + 63) / 64);
-    p.nk256 = (int)((K + 255) / 256);
-    const int grid = (int)(tiles < sms ? tiles : sms);
-    const size_t smem = gemm_smem_bytes(p.BN);
-    CUtensorMap tmx, tmq;
-    if (!make_map_2d(&tmx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x16, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, 64,
-                     (uint32_t)p.BN))
-        return cudaErrorInvalidValue;
-    if (!make_map_2d(&tmq, CU_TENSOR_MAP_DATA_TYPE_UINT32, mat.q, (uint64_t)(K / 8), (uint64_t)N,
-                     (uint64_t)(K / 8) * 4, 32, kBM))
-        return cudaErrorInvalidValue;
-    p.s = static_cast<const unsigned short*>(mat.s);
-    p.z = mat.z;
-    p.y = static_cast<__nv_bfloat16*>(mat.y);
-    switch (G) {
-        case 32: return launch_g<32>(tmx, tmq, p, grid, smem, stream);
-        case 64: return launch_g<64>(tmx, tmq, p, grid, smem, stream);
-        case 128: return launch_g<128>(tmx, tmq, p, grid, smem, stream);
-        case 256: return launch_g<256>(tmx, tmq, p, grid, smem, stream);
-        default: return cudaErrorInvalidValue;
-    }
+    p.yf32 = 0;
+    int grid = 0;
+    size_t smem = 0;
+    CUtensorMap tmx;
+    if (!plan_gemm(M, N, K, G, x16, di, p, grid, smem, tmx)) return cudaErrorInvalidValue;
+    return launch_one(x16, mat, p, G, grid, smem, tmx, di.dev, stream);
 }
 
 cudaError_t read_and_clear_status(uint32_t* word) {

@@ -55,11 +55,12 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
-#include <mutex>
+#include <atomic>
 
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
+#include "unpack.cuh"
 
 namespace w4a16 {
 
@@ -75,8 +76,6 @@ __host__ __device__ constexpr int cta_warps(int NB, int G) { return NB == 1 && G
 constexpr int kBoxBytes = 2048;           // one TMA box: 16 virtual rows x 128 bytes (256 codes)
 constexpr int kUnitBytes = 2 * kBoxBytes;  // a ring slot: a unit of up to two consecutive chunks of a tile
 constexpr int kSlots = 4;                 // partial-sum slots per output (warps sharing a tile)
-constexpr int kMaxDevices = 64;
-constexpr long long kSpinCycles = 1ll << 31;
 constexpr uint32_t kStatusGemv = 1u << 8;
 constexpr uint32_t kStatusGemvDrain = 1u << 9;
 
@@ -92,7 +91,8 @@ struct GemvParams {
     int kx;                                // row length of x: channel k reads x[k mod kx] (kx = K or K/2)
     const unsigned short* s[2];            // FP16 scales [N, lds] (KQ: super-block records, 8 halves each)
     const uint32_t* z[2];                  // zeros [N, ldz] (KQ: unused, ldz = 0)
-    __nv_bfloat16* y[2];                   // [M, N]
+    void* y[2];                            // [M, N], BF16 (or FP32 when yf32)
+    int yf32;                              // 1: FP32 outputs (no BF16 rounding)
     int M, N, K, G;
     int P, R, cols, xcols;                 // segments, weight rows per tile, B columns used (P*H*M),
                                            // staged x columns (P*M)
@@ -104,6 +104,8 @@ struct GemvParams {
     int warps;                             // warps that take units (<= nw)
     int nst;                               // unit slots per warp ring (power of two)
     int rows_cap;                          // weight rows per CTA the partial buffer holds
+    long long spin_limit;                  // cycles a bounded wait spins before it gives up
+    int withhold;                          // test hook: warp 0 of CTA 0 never issues its first unit
 };
 
 struct Layout {
@@ -184,26 +186,13 @@ __device__ __forceinline__ float4 lds_f4(uint32_t addr) {
     return v;
 }
 
-// Zero point in nibble j of a (shifted) zero word, as a float (2^23 + z has ulp 1).
-__device__ __forceinline__ float meta_zero(uint32_t zshifted, int j) {
-    return __uint_as_float(0x4B000000u | ((zshifted >> (4 * j)) & 0xFu)) - 8388608.0f;
-}
-
-// 6-bit code j of a super-block record as a float: low 4 bits at bit 4j of
-// `lo`, high 2 bits at bit 2j + hs of `hi` (hs = 0 for sc, 16 for m).
-__device__ __forceinline__ float kq_code(uint32_t lo, uint32_t hi, int j, int hs) {
-    const uint32_t v = ((lo >> (4 * j)) & 0xFu) | (((hi >> (2 * j + hs)) & 3u) << 4);
-    return __uint_as_float(0x4B000000u | v) - 8388608.0f;
-}
-__device__ __forceinline__ float half_lo(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu))); }
-__device__ __forceinline__ float half_hi(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w >> 16))); }
-
-// Bounded wait on a barrier phase; the thread sleeps between polls.
-__device__ __forceinline__ bool gemv_wait(uint32_t bar, uint32_t parity) {
+// Bounded wait on a barrier phase (gives up after `limit` cycles); the thread
+// sleeps between polls.
+__device__ __forceinline__ bool gemv_wait(uint32_t bar, uint32_t parity, long long limit) {
     if (tc::mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (!tc::mbar_try_wait_sleep(bar, parity, 100000u)) {
-        if (clock64() - t0 > kSpinCycles) {
+        if (clock64() - t0 > limit) {
             atomicOr(&g_gemv_status, kStatusGemv);
             return false;
         }
@@ -257,6 +246,8 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
         it_tl = ch0 / p.C;
         it_c = ch0 - it_tl * p.C;
     }
+    // test hook: warp 0 of CTA 0 never issues its first unit, so its wait on it runs out
+    const bool withhold = p.withhold && blockIdx.x == 0 && warp == 0;
     auto issue_next = [&]() {
         const int tau = tile0 + it_tl;
         const int mat = tau >= p.tiles_per_mat;
@@ -264,10 +255,13 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
         const uint32_t slot = (uint32_t)(it_n & (nsl - 1));
         const uint32_t bar = bar0 + 8u * slot;
         const bool two = it_c + 1 < p.C && it_ch + 1 < ch1;
-        tc::mbar_arrive_expect_tx(bar, (uint32_t)(two ? 2 * kBoxBytes : kBoxBytes));
-        const void* tm = mat ? (const void*)&tm1 : (const void*)&tm0;
-        tc::tma_load_2d(ring + slot * (uint32_t)kUnitBytes, tm, it_c * 32, tile * 16, bar);
-        if (two) tc::tma_load_2d(ring + slot * (uint32_t)kUnitBytes + kBoxBytes, tm, (it_c + 1) * 32, tile * 16, bar);
+        if (!(withhold && it_n == 0)) {
+            tc::mbar_arrive_expect_tx(bar, (uint32_t)(two ? 2 * kBoxBytes : kBoxBytes));
+            const void* tm = mat ? (const void*)&tm1 : (const void*)&tm0;
+            tc::tma_load_2d(ring + slot * (uint32_t)kUnitBytes, tm, it_c * 32, tile * 16, bar);
+            if (two)
+                tc::tma_load_2d(ring + slot * (uint32_t)kUnitBytes + kBoxBytes, tm, (it_c + 1) * 32, tile * 16, bar);
+        }
         const int n = two ? 2 : 1;
         ++it_n;
         it_ch += n;
@@ -445,7 +439,7 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
 
         // the scale/zero rows have landed: lane 0 of each warp starts its ring of units and keeps
         // it filled from here on
-        pro_ok = __all_sync(0xFFFFFFFFu, gemv_wait(pbar, 0));
+        pro_ok = __all_sync(0xFFFFFFFFu, gemv_wait(pbar, 0, p.spin_limit));
         if (pro_ok && active && lane == 0) {
             for (int i = 0; i < nsl && it_ch < ch1; ++i) issue_next();
         }
@@ -540,7 +534,7 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
         const int lg = 31 - __clz(nsl);
         for (int k = 0; ch < ch1 && ok; ++k) {
             const uint32_t slot = (uint32_t)(k & (nsl - 1));
-            ok = gemv_wait(bar0 + 8u * slot, (uint32_t)((k >> lg) & 1));
+            ok = gemv_wait(bar0 + 8u * slot, (uint32_t)((k >> lg) & 1), p.spin_limit);
             ok = __all_sync(0xFFFFFFFFu, ok);
             if (ok) {
                 const bool two = cu + 1 < p.C && ch + 1 < ch1;   // as in issue_next
@@ -616,15 +610,9 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
                           const int ws = bq * V + i;                   // word step in the chunk
                           const int jg = ws / WSG;                     // group in the chunk
                           const int hcur = jg % H;                     // its parity (c * GPC is a multiple of H)
-                          const uint32_t a8 = wa[i] >> 8, b8 = wb[i] >> 8;
-                          const uint32_t a0 = lop3_and_or(wa[i], 0x000F000Fu, 0x64006400u);
-                          const uint32_t a1 = lop3_and_or(wa[i], 0x00F000F0u, 0x54005400u);
-                          const uint32_t a2 = lop3_and_or(a8, 0x000F000Fu, 0x64006400u);
-                          const uint32_t a3 = lop3_and_or(a8, 0x00F000F0u, 0x54005400u);
-                          const uint32_t b0 = lop3_and_or(wb[i], 0x000F000Fu, 0x64006400u);
-                          const uint32_t b1 = lop3_and_or(wb[i], 0x00F000F0u, 0x54005400u);
-                          const uint32_t b2 = lop3_and_or(b8, 0x000F000Fu, 0x64006400u);
-                          const uint32_t b3 = lop3_and_or(b8, 0x00F000F0u, 0x54005400u);
+                          uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+                          expand_codes_f16(wa[i], a0, a1, a2, a3);
+                          expand_codes_f16(wb[i], b0, b1, b2, b3);
 #pragma unroll
                           for (int nb = 0; nb < NB; ++nb) {
                               const uint4 xv = lds128(xb[nb][hcur] + (uint32_t)ws * xsp[nb][hcur]);
@@ -777,11 +765,11 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
         }
         if (!ok && lane == 0) {   // wait for this warp's ring copies still in flight
             for (int kk = it_n - nsl; kk < it_n; ++kk) {
-                if (kk < 0) continue;
+                if (kk < 0 || (withhold && kk == 0)) continue;     // never issued
                 const uint32_t bar = bar0 + 8u * (uint32_t)(kk & (nsl - 1));
                 const long long t0 = clock64();
                 while (!tc::mbar_try_wait(bar, (uint32_t)((kk >> lg) & 1))) {
-                    if (clock64() - t0 > kSpinCycles) {
+                    if (clock64() - t0 > p.spin_limit) {
                         atomicOr(&g_gemv_status, kStatusGemvDrain);
                         break;
                     }
@@ -792,7 +780,7 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
     if (!pro_ok && tid == 0) {    // the prologue's copies timed out: wait for them once more
         const long long t0 = clock64();
         while (!tc::mbar_try_wait(pbar, 0)) {
-            if (clock64() - t0 > kSpinCycles) {
+            if (clock64() - t0 > p.spin_limit) {
                 atomicOr(&g_gemv_status, kStatusGemvDrain);
                 break;
             }
@@ -814,39 +802,20 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
             float sum = 0.0f;
 #pragma unroll
             for (int q = 0; q < kSlots; ++q) sum += part[i * kSlots + q];
-            (mat ? p.y[1] : p.y[0])[(int64_t)m * p.N + row] = __float2bfloat16_rn(sum);
+            if (p.yf32)
+                static_cast<float*>(mat ? p.y[1] : p.y[0])[(int64_t)m * p.N + row] = sum;
+            else
+                static_cast<__nv_bfloat16*>(mat ? p.y[1] : p.y[0])[(int64_t)m * p.N + row] = __float2bfloat16_rn(sum);
         }
     }
 }
 
 // ---- host side -------------------------------------------------------------------
 
-PFN_cuTensorMapEncodeTiled_v12000 encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    });
-    return fn;
-}
-
 // Packed codes viewed as [N*P virtual rows][K/(8P) words], boxes of 32 words x 16 rows.
-bool make_code_map(CUtensorMap* map, const uint32_t* q, int64_t N, int64_t K, int P) {
-    auto enc = encoder();
-    if (!enc) return false;
+bool make_code_map(CUtensorMap* map, const uint32_t* q, int64_t N, int64_t K, int P, int dev) {
     const uint64_t words = (uint64_t)(K / 8 / P);
-    cuuint64_t dims[2] = {words, (uint64_t)(N * P)};
-    cuuint64_t strides[1] = {words * 4};
-    cuuint32_t box[2] = {32, 16};
-    cuuint32_t es[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(q), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return encode_tmap_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, q, words, (uint64_t)(N * P), words * 4, 32, 16, dev);
 }
 
 // Segments P and group parities H per row for M activation rows: the B
@@ -936,17 +905,17 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int G, int nmat, int sms, size_t
 }
 
 template <int NB, int G, int H, bool M1, int PT, bool KQ>
-cudaError_t launch_m(const CUtensorMap& tm0, const CUtensorMap& tm1, const Plan& pl, cudaStream_t stream) {
-    static int cached[kMaxDevices] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    if ((int)pl.smem > cached[dev]) {
-        e = cudaFuncSetAttribute(gemv_kernel<NB, G, H, M1, PT, KQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)pl.smem);
+cudaError_t launch_m(const CUtensorMap& tm0, const CUtensorMap& tm1, const Plan& pl, int dev, cudaStream_t stream) {
+    // largest dynamic shared memory this instance is already allowed per device (a raise may
+    // race with another thread's: both set the attribute, the larger value stays)
+    static std::atomic<int> cached[kMaxDevices];
+    int have = cached[dev].load(std::memory_order_relaxed);
+    if ((int)pl.smem > have) {
+        const cudaError_t e = cudaFuncSetAttribute(gemv_kernel<NB, G, H, M1, PT, KQ>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
         if (e != cudaSuccess) return e;
-        cached[dev] = (int)pl.smem;
+        while (have < (int)pl.smem && !cached[dev].compare_exchange_weak(have, (int)pl.smem)) {
+        }
     }
     // programmatic stream serialisation: set-up overlaps the tail of the previous launch
     cudaLaunchAttribute attr[1];
@@ -963,32 +932,32 @@ cudaError_t launch_m(const CUtensorMap& tm0, const CUtensorMap& tm1, const Plan&
 }
 
 template <int NB, int G, int H, bool KQ>
-cudaError_t launch_t(const CUtensorMap& tm0, const CUtensorMap& tm1, const Plan& pl, cudaStream_t stream) {
+cudaError_t launch_t(const CUtensorMap& tm0, const CUtensorMap& tm1, const Plan& pl, int dev, cudaStream_t stream) {
     if constexpr (NB == 1) {
         if (m1_kernel(pl.p)) {                       // M = 1: the segment count is a template constant
             switch (pl.p.P) {
-                case 2: return launch_m<NB, G, H, true, 2, KQ>(tm0, tm1, pl, stream);
-                case 4: return launch_m<NB, G, H, true, 4, KQ>(tm0, tm1, pl, stream);
-                case 8: return launch_m<NB, G, H, true, 8, KQ>(tm0, tm1, pl, stream);
+                case 2: return launch_m<NB, G, H, true, 2, KQ>(tm0, tm1, pl, dev, stream);
+                case 4: return launch_m<NB, G, H, true, 4, KQ>(tm0, tm1, pl, dev, stream);
+                case 8: return launch_m<NB, G, H, true, 8, KQ>(tm0, tm1, pl, dev, stream);
             }
             return cudaErrorInvalidValue;
         }
     }
-    return launch_m<NB, G, H, false, 0, KQ>(tm0, tm1, pl, stream);
+    return launch_m<NB, G, H, false, 0, KQ>(tm0, tm1, pl, dev, stream);
 }
 
 template <int NB, int G, bool KQ = false>
-cudaError_t launch_h(const CUtensorMap& tm0, const CUtensorMap& tm1, const Plan& pl, cudaStream_t stream) {
+cudaError_t launch_h(const CUtensorMap& tm0, const CUtensorMap& tm1, const Plan& pl, int dev, cudaStream_t stream) {
     if constexpr (NB == 2) {
-        return launch_t<NB, G, 1, KQ>(tm0, tm1, pl, stream);
+        return launch_t<NB, G, 1, KQ>(tm0, tm1, pl, dev, stream);
     } else {
         switch (pl.H) {
-            case 1: return launch_t<NB, G, 1, KQ>(tm0, tm1, pl, stream);
+            case 1: return launch_t<NB, G, 1, KQ>(tm0, tm1, pl, dev, stream);
             case 2:
-                if constexpr (256 / G >= 2) return launch_t<NB, G, 2, KQ>(tm0, tm1, pl, stream);
+                if constexpr (256 / G >= 2) return launch_t<NB, G, 2, KQ>(tm0, tm1, pl, dev, stream);
                 break;
             case 4:
-                if constexpr (256 / G >= 4) return launch_t<NB, G, 4, KQ>(tm0, tm1, pl, stream);
+                if constexpr (256 / G >= 4) return launch_t<NB, G, 4, KQ>(tm0, tm1, pl, dev, stream);
                 break;
         }
         return cudaErrorInvalidValue;
@@ -996,31 +965,17 @@ cudaError_t launch_h(const CUtensorMap& tm0, const CUtensorMap& tm1, const Plan&
 }
 
 template <int NB>
-cudaError_t launch_nb(const CUtensorMap& tm0, const CUtensorMap& tm1, const Plan& pl, cudaStream_t stream) {
+cudaError_t launch_nb(const CUtensorMap& tm0, const CUtensorMap& tm1, const Plan& pl, int dev, cudaStream_t stream) {
     switch (pl.p.G) {
-        case 32: return launch_h<NB, 32>(tm0, tm1, pl, stream);
-        case 64: return launch_h<NB, 64>(tm0, tm1, pl, stream);
-        case 128: return launch_h<NB, 128>(tm0, tm1, pl, stream);
-        case 256: return launch_h<NB, 256>(tm0, tm1, pl, stream);
+        case 32: return launch_h<NB, 32>(tm0, tm1, pl, dev, stream);
+        case 64: return launch_h<NB, 64>(tm0, tm1, pl, dev, stream);
+        case 128: return launch_h<NB, 128>(tm0, tm1, pl, dev, stream);
+        case 256: return launch_h<NB, 256>(tm0, tm1, pl, dev, stream);
         default: return cudaErrorInvalidValue;
     }
 }
 
-int device_sms() {
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    return sms;
-}
-
 }  // namespace
-
-size_t device_smem_optin() {
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
-    return (size_t)v;
-}
 
 cudaError_t gemv_take_status(uint32_t* word) {
     cudaError_t e = cudaMemcpyFromSymbol(word, g_gemv_status, sizeof(uint32_t));
@@ -1031,37 +986,42 @@ cudaError_t gemv_take_status(uint32_t* word) {
 
 bool gemv_fits(int64_t M, int64_t N, int64_t K, int G, int nmat, bool kq) {
     Plan pl;
-    int sms = device_sms();
-    if (sms <= 0) sms = 148;
-    size_t cap = device_smem_optin();
-    if (cap == 0) cap = 227 * 1024;
-    return make_plan(M, N, K, G, nmat, sms, cap, pl, kq);
+    DeviceInfo di;
+    if (current_device(di) != cudaSuccess) {   // no device: the B300's figures
+        di.sms = 148;
+        di.smem_optin = 227 * 1024;
+    }
+    return make_plan(M, N, K, G, nmat, di.sms, di.smem_optin, pl, kq);
 }
 
 cudaError_t launch_gemv(const void* x, const GemvMat* mats, int nmat, int64_t M, int64_t N, int64_t K, int G,
-                        cudaStream_t stream, const float* xsc, int64_t kx, bool kq) {
+                        cudaStream_t stream, const float* xsc, int64_t kx, bool kq, bool yf32) {
     if (kx == 0) kx = K;
     if (kx != K && (kx * 2 != K || kx % 8 != 0)) return cudaErrorInvalidValue;
     if (kq && (G != 32 || xsc != nullptr || kx != K)) return cudaErrorInvalidValue;
-    const int sms = device_sms();
-    if (sms <= 0) return cudaErrorNoDevice;
-    const size_t cap = device_smem_optin();
+    DeviceInfo di;
+    const cudaError_t e = current_device(di);
+    if (e != cudaSuccess) return e;
     Plan pl;
-    if (!make_plan(M, N, K, G, nmat, sms, cap, pl, kq)) return cudaErrorNotSupported;
+    if (!make_plan(M, N, K, G, nmat, di.sms, di.smem_optin, pl, kq)) return cudaErrorNotSupported;
     GemvParams& p = pl.p;
     p.x = static_cast<const __nv_bfloat16*>(x);
     p.xsc = xsc;
     p.kx = (int)kx;
+    p.yf32 = yf32 ? 1 : 0;
+    p.spin_limit = wait_limit();
+    p.withhold = take_withhold(1) ? 1 : 0;
     CUtensorMap tm[2];
     for (int i = 0; i < 2; ++i) {
         const GemvMat& mt = mats[i < nmat ? i : 0];
         p.s[i] = static_cast<const unsigned short*>(mt.s);
         p.z[i] = mt.z;
-        p.y[i] = static_cast<__nv_bfloat16*>(mt.y);
-        if (!make_code_map(&tm[i], mt.q, N, K, p.P)) return cudaErrorInvalidValue;
+        p.y[i] = mt.y;
+        if (i < nmat && !make_code_map(&tm[i], mt.q, N, K, p.P, di.dev)) return cudaErrorInvalidValue;
     }
-    if (kq) return launch_h<1, 32, true>(tm[0], tm[1], pl, stream);      // make_plan: M <= 8, so one column block
-    return pl.nb == 1 ? launch_nb<1>(tm[0], tm[1], pl, stream) : launch_nb<2>(tm[0], tm[1], pl, stream);
+    if (nmat < 2) tm[1] = tm[0];
+    if (kq) return launch_h<1, 32, true>(tm[0], tm[1], pl, di.dev, stream);   // make_plan: M <= 8, one column block
+    return pl.nb == 1 ? launch_nb<1>(tm[0], tm[1], pl, di.dev, stream) : launch_nb<2>(tm[0], tm[1], pl, di.dev, stream);
 }
 
 }  // namespace w4a16

@@ -1,18 +1,51 @@
 // kernels.h -- internal launchers behind the C ABI (not part of the public header).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstdint>
 
 namespace w4a16 {
+
+constexpr int kMaxDevices = 64;
+
+// The current device and its attributes, read once per device (host.cu).
+struct DeviceInfo {
+    int dev;
+    int sms;
+    size_t smem_optin;   // largest dynamic shared memory a block may opt into
+};
+cudaError_t current_device(DeviceInfo& info);
+
+// 2-D row-major tensor [outer][inner] with 128-byte swizzled boxes; encoded maps
+// are cached by every argument (host.cu).  False if the driver's encoder is
+// unavailable or rejects the arguments.
+// Cycles a kernel's bounded wait spins before it gives up (host.cu; settable for tests).
+long long wait_limit();
+void set_wait_limit(long long cycles);   // <= 0 restores the default
+// Test hook: arm (kernel 1 = decode, 2 = tensor-core, 0 = off) one launch that withholds
+// one copy; take_withhold returns true once for the armed kernel and disarms it.
+void arm_withhold(int kernel);
+bool take_withhold(int kernel);
+
+bool tmap_encoder_available();
+bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                    uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, int dev);
 
 cudaError_t launch_pack(const void* w, int64_t N, int64_t K, int G, uint32_t* qw, void* sc, uint32_t* zr,
                         cudaStream_t stream);
 // The 8-bit packer: codes as two 4-bit planes of a 2K-channel 4-bit layer (see pack.cu).
 cudaError_t launch_pack8(const void* w, int64_t N, int64_t K, int G, uint32_t* qw, void* sc, uint32_t* zr,
                          cudaStream_t stream);
+// Checking aids through the layer kernels' expansion routines (see pack.cu):
+// FP32 W_hat via the decode kernel's, FP16 RN(W_hat) via the tensor-core
+// kernel's, FP32 W_hat of the super-block layout via the decode kernel's.
 cudaError_t launch_dequant(const uint32_t* qw, const void* sc, const uint32_t* zr, int64_t N, int64_t K, int G,
                            float* out, cudaStream_t stream);
+cudaError_t launch_dequant_f16(const uint32_t* qw, const void* sc, const uint32_t* zr, int64_t N, int64_t K, int G,
+                               void* out, cudaStream_t stream);
+cudaError_t launch_dequant_q4k(const uint32_t* qw, const uint32_t* meta, int64_t N, int64_t K, float* out,
+                               cudaStream_t stream);
 // The super-block (Q4_K-style) packer: codes in the 4-bit layout, one 16-byte record per 256 channels
 // (see pack.cu).  K a multiple of 256.
 cudaError_t launch_pack_q4k(const void* w, int64_t N, int64_t K, uint32_t* qw, uint32_t* meta, cudaStream_t stream);
@@ -29,8 +62,6 @@ struct GemvMat {
 // stream rings fit the device's shared memory).  Host only.
 // kq: the super-block layout (G = 32, M <= 8).
 bool gemv_fits(int64_t M, int64_t N, int64_t K, int G, int nmat, bool kq = false);
-// Largest dynamic shared memory a block may use on the current device.
-size_t device_smem_optin();
 
 // y_i = x * W_hat_i^T for one matrix (nmat = 1) or two matrices sharing x (nmat = 2).
 // xsc (optional, FP32 [K], 16-byte aligned): x_k is taken as x_k * xsc_k.
@@ -38,13 +69,15 @@ size_t device_smem_optin();
 // (the two-plane 8-bit layer is a 4-bit layer of K = 2 kx channels over x repeated).
 // kq: the matrices are in the super-block layout (GemvMat.s = records, .z unused; G = 32,
 // M <= 8, no xsc or kx).
+// yf32: the outputs are FP32 [M, N] (the sums without the BF16 rounding).
 cudaError_t launch_gemv(const void* x, const GemvMat* mats, int nmat, int64_t M, int64_t N, int64_t K, int G,
-                        cudaStream_t stream, const float* xsc = nullptr, int64_t kx = 0, bool kq = false);
+                        cudaStream_t stream, const float* xsc = nullptr, int64_t kx = 0, bool kq = false,
+                        bool yf32 = false);
 
 // Tensor-core path (any M): y_i = x * W_hat_i^T for nmat matrices sharing x
 // (x is converted to FP16 once, into stream-ordered scratch).
 cudaError_t launch_gemm(const void* x, const GemvMat* mats, int nmat, int64_t M, int64_t N, int64_t K, int G,
-                        cudaStream_t stream, const float* xsc = nullptr, int64_t kx = 0);
+                        cudaStream_t stream, const float* xsc = nullptr, int64_t kx = 0, bool yf32 = false);
 // The same tensor-core path for one matrix with the FP16 copy of x in a
 // fixed-size file-scope device array (no allocation; M * K bounded by the
 // header's W4A16_NOALLOC_MAX_X_ELEMS, else cudaErrorNotSupported).

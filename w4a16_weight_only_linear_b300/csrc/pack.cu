@@ -1,5 +1,6 @@
-// pack.cu -- FP16 weight -> packed 4-bit codes + FP16 scales + 4-bit zeros,
-// and the exact dequantisation used by the tests.
+// pack.cu -- FP16 weight -> packed 4-bit codes + FP16 scales + 4-bit zeros
+// (and the 8-bit and super-block variants), and the dequantising checking aids
+// that run the layer kernels' own expansion routines.
 //
 // Quantiser: group-wise asymmetric min-max over G consecutive input channels
 // of one output column (klaylearn.com glossary "Weight-Only Quantisation",
@@ -14,6 +15,7 @@
 // fast-math), so the codes are bit-identical to any IEEE implementation.
 #include "common.cuh"
 #include "kernels.h"
+#include "unpack.cuh"
 
 namespace w4a16 {
 
@@ -185,9 +187,14 @@ __global__ void __launch_bounds__(256) pack8_kernel(const __half* __restrict__ w
     for (int64_t i = 2 * ngroups + lane; i < lds; i += 32) srow[i] = __ushort_as_half((unsigned short)0);
 }
 
-// W_hat = (q - z) * s through the same in-register nibble expansion the
-// linear kernels use (BF16 128 + q), then exact FP32 arithmetic.
+// ---- dequantising checking aids ------------------------------------------------------
+// Each runs one layer kernel's own expansion routine (unpack.cuh) over every
+// packed word, so their bit-exact checks against the oracle pin that routine.
 // One thread per packed word (8 outputs).
+
+// W_hat = (q - z) * s in FP32 through the decode kernel's expansion: the
+// word's codes as the FP16 values 1024 + q / 64 + q it multiplies, the zero
+// point and the scale as it extracts them; q - z and the product are exact.
 __global__ void __launch_bounds__(256) dequant_kernel(const uint32_t* __restrict__ qw, const __half* __restrict__ sc,
                                                       const uint32_t* __restrict__ zr, int64_t N, int64_t K, int G,
                                                       float* __restrict__ out) {
@@ -198,14 +205,64 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint32_t* __restrict
     const int64_t g = (w8 * 8) / G;
     const uint32_t word = qw[n * qweight_ld(K) + w8];
     const float s = __half2float(sc[n * scales_ld(K, G) + g]);
-    const float off = 128.0f + (float)nibble(zr[n * zeros_ld(K, G) + g / 8], (int)(g & 7));
-    uint32_t p[4];
-    codes_to_bf16x2(word, p);
+    const float z = meta_zero(zr[n * zeros_ld(K, G) + g / 8] >> (4 * (g & 7)), 0);
+    uint32_t e[4];
+    expand_codes_f16(word, e[0], e[1], e[2], e[3]);
     float o[8];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        o[j] = __fmul_rn(__fsub_rn(bf16lo_to_f32(p[j]), off), s);
-        o[j + 4] = __fmul_rn(__fsub_rn(bf16hi_to_f32(p[j]), off), s);
+    for (int i = 0; i < 4; ++i) {          // pair i holds codes i (low half) and i + 4 (high half)
+        o[i] = __fmul_rn(__fsub_rn(__fsub_rn(half_lo(e[i]), expand_offset(i)), z), s);
+        o[i + 4] = __fmul_rn(__fsub_rn(__fsub_rn(half_hi(e[i]), expand_offset(i)), z), s);
+    }
+    float4* dst = reinterpret_cast<float4*>(out + n * K + w8 * 8);
+    dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+}
+
+// RN_fp16((q - z) * s) through the tensor-core kernel's expansion: the same
+// 128-bit scale chunk and zero word, group constants and packed FP16
+// subtract/multiply it writes into tensor memory as the MMA's A operand.
+__global__ void __launch_bounds__(256) dequant_f16_kernel(const uint32_t* __restrict__ qw,
+                                                          const unsigned short* __restrict__ sc,
+                                                          const uint32_t* __restrict__ zr, int64_t N, int64_t K,
+                                                          int G, uint32_t* __restrict__ out) {
+    const int64_t words = K / 8;
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= N * words) return;
+    const int64_t n = idx / words, w8 = idx % words;
+    const int64_t g = (w8 * 8) / G;
+    const uint4 sv = *reinterpret_cast<const uint4*>(sc + n * scales_ld(K, G) + (g >> 3) * 8);
+    const uint32_t zw = zr[n * zeros_ld(K, G) + (g >> 3)];
+    uint32_t s2, zz;
+    group_consts(sv, zw, (int)(g & 7), true, s2, zz);
+    uint32_t o[4];
+    dequant_word(qw[n * qweight_ld(K) + w8], s2, zz, o);
+    *reinterpret_cast<uint4*>(out + (n * K + w8 * 8) / 2) = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Super-block layout: W_hat = d*sc_j*q - dmin*m_j in FP32 through the decode
+// kernel's super-block mode: codes from its expansion, the record's FP16
+// factors and 6-bit codes as it decodes them, s = d*sc_j and mn = dmin*m_j
+// (both exact), then s*q (exact) minus mn, rounded once.
+__global__ void __launch_bounds__(256) dequant_q4k_kernel(const uint32_t* __restrict__ qw,
+                                                          const uint32_t* __restrict__ meta, int64_t N, int64_t K,
+                                                          float* __restrict__ out) {
+    const int64_t words = K / 8;
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= N * words) return;
+    const int64_t n = idx / words, w8 = idx % words;
+    const int64_t sb = w8 / 32;
+    const int j = (int)((w8 % 32) / 4);                 // sub-block of 32 channels
+    const uint4 rec = *reinterpret_cast<const uint4*>(meta + n * (K / 256 * 4) + sb * 4);
+    const float s = half_lo(rec.x) * kq_code(rec.y, rec.w, j, 0);
+    const float mn = half_hi(rec.x) * kq_code(rec.z, rec.w, j, 16);
+    uint32_t e[4];
+    expand_codes_f16(qw[n * qweight_ld(K) + w8], e[0], e[1], e[2], e[3]);
+    float o[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        o[i] = __fsub_rn(__fmul_rn(s, __fsub_rn(half_lo(e[i]), expand_offset(i))), mn);
+        o[i + 4] = __fsub_rn(__fmul_rn(s, __fsub_rn(half_hi(e[i]), expand_offset(i))), mn);
     }
     float4* dst = reinterpret_cast<float4*>(out + n * K + w8 * 8);
     dst[0] = make_float4(o[0], o[1], o[2], o[3]);
@@ -332,12 +389,36 @@ cudaError_t launch_pack8(const void* w, int64_t N, int64_t K, int G, uint32_t* q
     return cudaGetLastError();
 }
 
+// Grid for one thread per packed word of N x K codes (false when it does not fit one launch).
+static bool word_grid(int64_t N, int64_t K, dim3& grid) {
+    const int64_t blocks = (N * (K / 8) + 255) / 256;
+    if (blocks > 0x7FFFFFFF) return false;
+    grid = dim3((unsigned)blocks);
+    return true;
+}
+
 cudaError_t launch_dequant(const uint32_t* qw, const void* sc, const uint32_t* zr, int64_t N, int64_t K, int G,
                            float* out, cudaStream_t stream) {
-    const int64_t total = N * (K / 8);
-    const dim3 block(256);
-    const dim3 grid((unsigned)((total + 255) / 256));
-    dequant_kernel<<<grid, block, 0, stream>>>(qw, static_cast<const __half*>(sc), zr, N, K, G, out);
+    dim3 grid;
+    if (!word_grid(N, K, grid)) return cudaErrorInvalidValue;
+    dequant_kernel<<<grid, 256, 0, stream>>>(qw, static_cast<const __half*>(sc), zr, N, K, G, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_f16(const uint32_t* qw, const void* sc, const uint32_t* zr, int64_t N, int64_t K, int G,
+                               void* out, cudaStream_t stream) {
+    dim3 grid;
+    if (!word_grid(N, K, grid)) return cudaErrorInvalidValue;
+    dequant_f16_kernel<<<grid, 256, 0, stream>>>(qw, static_cast<const unsigned short*>(sc), zr, N, K, G,
+                                                 static_cast<uint32_t*>(out));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_q4k(const uint32_t* qw, const uint32_t* meta, int64_t N, int64_t K, float* out,
+                               cudaStream_t stream) {
+    dim3 grid;
+    if (!word_grid(N, K, grid)) return cudaErrorInvalidValue;
+    dequant_q4k_kernel<<<grid, 256, 0, stream>>>(qw, meta, N, K, out);
     return cudaGetLastError();
 }
 

@@ -128,3 +128,26 @@ def act_seed(workload: Workload, j: int) -> int:
 def bits_u16(t: torch.Tensor):
     """FP16/BF16 tensor -> numpy uint16 bit patterns (for the oracle)."""
     return t.contiguous().view(torch.int16).numpy().view("uint16")
+
+
+def random_u32(shape, seed: int):
+    """numpy uint32 array of uniformly random words (every nibble and byte value
+    occurs): raw packed codes, zero-point words or record fields for the checks
+    that feed arbitrary bit patterns through the unpacking routines."""
+    import numpy as np
+    g = torch.Generator().manual_seed(seed)
+    lo = torch.randint(0, 1 << 16, tuple(shape), generator=g, dtype=torch.int64)
+    hi = torch.randint(0, 1 << 16, tuple(shape), generator=g, dtype=torch.int64)
+    return ((hi << 16) | lo).numpy().astype(np.uint32)
+
+
+def random_f16_bits(shape, seed: int, exp_lo: int = 1, exp_hi: int = 30, sign: bool = False):
+    """numpy uint16 array of FP16 bit patterns with a uniformly random biased
+    exponent in [exp_lo, exp_hi] (0 = subnormal, 30 = largest finite) and
+    mantissa, positive unless `sign`: arbitrary finite scale values."""
+    import numpy as np
+    g = torch.Generator().manual_seed(seed)
+    e = torch.randint(exp_lo, exp_hi + 1, tuple(shape), generator=g, dtype=torch.int64)
+    m = torch.randint(0, 1 << 10, tuple(shape), generator=g, dtype=torch.int64)
+    s = torch.randint(0, 2, tuple(shape), generator=g, dtype=torch.int64) if sign else torch.zeros_like(e)
+    return ((s << 15) | (e << 10) | m).numpy().astype(np.uint16)
