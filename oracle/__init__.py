@@ -51,6 +51,15 @@ def _load():
         lib.oracle_dequant8.restype = None
         lib.oracle_linear8.argtypes = [p, p, p, p, i64, i64, i64, i64, p, i32]
         lib.oracle_linear8.restype = None
+        lib.oracle_zeros8w_ld.argtypes, lib.oracle_zeros8w_ld.restype = [i64, i64], i64
+        lib.oracle_pack8w.argtypes = [p, i64, i64, i64, p, p, p, i32]
+        lib.oracle_pack8w.restype = i32
+        lib.oracle_dequant8w.argtypes = [p, p, p, i64, i64, i64, p, i32]
+        lib.oracle_dequant8w.restype = None
+        lib.oracle_linear8w.argtypes = [p, p, p, p, i64, i64, i64, i64, p, i32]
+        lib.oracle_linear8w.restype = None
+        lib.oracle_linear8w_sampled.argtypes = [p, p, p, p, i64, i64, p, p, i64, p, i32]
+        lib.oracle_linear8w_sampled.restype = None
         lib.oracle_linear_xs.argtypes = [p, p, p, p, p, i64, i64, i64, i64, p, i32]
         lib.oracle_linear_xs.restype = None
         lib.oracle_q4k_meta_ld.argtypes, lib.oracle_q4k_meta_ld.restype = [i64], i64
@@ -270,6 +279,65 @@ def linear8(x_bf16: np.ndarray, q, s, z, N: int, K: int, G: int, nthreads: int =
     z = np.ascontiguousarray(z, dtype=np.uint32)
     y = np.zeros((M, N), np.float64)
     _load().oracle_linear8(_ptr(x), _ptr(q), _ptr(s), _ptr(z), M, N, K, G, _ptr(y), nthreads)
+    return y
+
+
+# ---- the 8-bit variant in the word layout (four codes per 32-bit word) -----------
+
+def zeros8w_ld(K: int, G: int) -> int:
+    """uint32 words per zeros row of the word layout (four 8-bit zero points per word)."""
+    return _load().oracle_zeros8w_ld(K, G)
+
+
+def pack8w(w_f16: np.ndarray, G: int, nthreads: int = 0):
+    """FP16 [N,K] -> (qweight u32 [N, K/4], scales u16 [N, scales_ld(K, G)],
+    zeros u32 [N, zeros8w_ld(K, G)]): 8-bit codes four per word, low byte
+    first; one FP16 scale and one 8-bit zero point per group."""
+    w = _u16(w_f16)
+    N, K = w.shape
+    q = np.zeros((N, K // 4), np.uint32)
+    s = np.zeros((N, scales_ld(K, G)), np.uint16)
+    z = np.zeros((N, zeros8w_ld(K, G)), np.uint32)
+    rc = _load().oracle_pack8w(_ptr(w), N, K, G, _ptr(q), _ptr(s), _ptr(z), nthreads)
+    if rc != 0:
+        raise ValueError("oracle_pack8w: bad shape")
+    return q, s, z
+
+
+def dequant8w(q, s, z, N: int, K: int, G: int, nthreads: int = 0) -> np.ndarray:
+    """W_hat [N,K] FP32 = (q - z) * s of the word layout."""
+    q = np.ascontiguousarray(q, dtype=np.uint32)
+    s = _u16(s)
+    z = np.ascontiguousarray(z, dtype=np.uint32)
+    out = np.zeros((N, K), np.float32)
+    _load().oracle_dequant8w(_ptr(q), _ptr(s), _ptr(z), N, K, G, _ptr(out), nthreads)
+    return out
+
+
+def linear8w(x_bf16: np.ndarray, q, s, z, N: int, K: int, G: int, nthreads: int = 0) -> np.ndarray:
+    """y_ref [M,N] FP64 = x * W_hat^T of the word layout, unrounded."""
+    x = _u16(x_bf16)
+    M = x.shape[0]
+    assert x.shape[1] == K
+    q = np.ascontiguousarray(q, dtype=np.uint32)
+    s = _u16(s)
+    z = np.ascontiguousarray(z, dtype=np.uint32)
+    y = np.zeros((M, N), np.float64)
+    _load().oracle_linear8w(_ptr(x), _ptr(q), _ptr(s), _ptr(z), M, N, K, G, _ptr(y), nthreads)
+    return y
+
+
+def linear8w_sampled(x_bf16: np.ndarray, q, s, z, K: int, G: int, ms, ns, nthreads: int = 0) -> np.ndarray:
+    """y_ref of the word layout at the listed (m, n) positions only, FP64."""
+    x = _u16(x_bf16)
+    q = np.ascontiguousarray(q, dtype=np.uint32)
+    s = _u16(s)
+    z = np.ascontiguousarray(z, dtype=np.uint32)
+    ms = np.ascontiguousarray(ms, dtype=np.int64)
+    ns = np.ascontiguousarray(ns, dtype=np.int64)
+    y = np.zeros(ms.shape[0], np.float64)
+    _load().oracle_linear8w_sampled(_ptr(x), _ptr(q), _ptr(s), _ptr(z), K, G, _ptr(ms), _ptr(ns), ms.shape[0],
+                                    _ptr(y), nthreads)
     return y
 
 

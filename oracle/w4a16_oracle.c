@@ -514,6 +514,128 @@ void oracle_linear8(const uint16_t* x_bf16, const uint32_t* qweight, const uint1
 }
 
 /* ------------------------------------------------------------------------ */
+/* The 8-bit variant in the word layout: four codes per 32-bit word.           */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * The pages name INT8 beside INT4 as the weight width of weight-only
+ * quantisation with 16-bit activations (klaylearn.com glossary "Weight-Only
+ * Quantisation", first FAQ answer) and give no 8-bit layout.  Reading: the
+ * same groups and the same 255-step quantiser as oracle_quantize_group8, with
+ * the metadata of the 4-bit layout widened to 8 bits:
+ *   qweight [N, K/4]          code of (n, k) in bits 8*(k%4) .. 8*(k%4)+7 of
+ *                             word k/4 (low byte first)
+ *   scales  [N, ldS(K, G)]    FP16 scale of group g, as the 4-bit layout
+ *   zeros   [N, ldZ8(K, G)]   8-bit zero point of group g in bits 8*(g%4) ..
+ *                             of word g/4; ldZ8 = ceil(K/G / 4) rounded up to
+ *                             a multiple of 4 words (16-byte rows)
+ *   W_hat = (q - z) * s, exact in FP32.
+ * Padding words and halves are zero.
+ */
+int64_t oracle_zeros8w_ld(int64_t K, int64_t G) { return round_up((K / G + 3) / 4, 4); }
+
+int oracle_pack8w(const uint16_t* w_f16, int64_t N, int64_t K, int64_t G,
+                  uint32_t* qweight, uint16_t* scales, uint32_t* zeros, int nthreads)
+{
+    if (N <= 0 || K <= 0 || G <= 0 || G > 256 || K % G != 0 || G % 8 != 0) return -1;
+    const int64_t ldq = K / 4;
+    const int64_t lds = oracle_scales_ld(K, G);
+    const int64_t ldz = oracle_zeros8w_ld(K, G);
+    const int64_t ngroups = K / G;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(static)
+#endif
+    for (int64_t n = 0; n < N; ++n) {
+        float wf[256];
+        int codes[256];
+        uint32_t* qrow = qweight + n * ldq;
+        uint16_t* srow = scales + n * lds;
+        uint32_t* zrow = zeros + n * ldz;
+        for (int64_t i = 0; i < ldq; ++i) qrow[i] = 0;
+        for (int64_t i = 0; i < lds; ++i) srow[i] = 0;
+        for (int64_t i = 0; i < ldz; ++i) zrow[i] = 0;
+        for (int64_t g = 0; g < ngroups; ++g) {
+            for (int64_t i = 0; i < G; ++i) wf[i] = oracle_f16_to_f32(w_f16[n * K + g * G + i]);
+            uint16_t sb;
+            int z;
+            oracle_quantize_group8(wf, G, &sb, &z, codes);
+            srow[g] = sb;
+            zrow[g / 4] |= (uint32_t)z << (8 * (g % 4));
+            for (int64_t i = 0; i < G; ++i) {
+                const int64_t k = g * G + i;
+                qrow[k / 4] |= (uint32_t)codes[i] << (8 * (k % 4));
+            }
+        }
+    }
+    (void)nthreads;
+    return 0;
+}
+
+/* W_hat = (q - z) * s of weight (n, k) in the word layout, exact in FP32. */
+float oracle_dequant8w_one(const uint32_t* qweight, const uint16_t* scales, const uint32_t* zeros,
+                           int64_t K, int64_t G, int64_t n, int64_t k)
+{
+    const int64_t g = k / G;
+    const int q = (int)((qweight[n * (K / 4) + k / 4] >> (8 * (k % 4))) & 0xFFu);
+    const int z = (int)((zeros[n * oracle_zeros8w_ld(K, G) + g / 4] >> (8 * (g % 4))) & 0xFFu);
+    const float s = oracle_f16_to_f32(scales[n * oracle_scales_ld(K, G) + g]);
+    return (float)(q - z) * s;
+}
+
+void oracle_dequant8w(const uint32_t* qweight, const uint16_t* scales, const uint32_t* zeros,
+                      int64_t N, int64_t K, int64_t G, float* w_out, int nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(static)
+#endif
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k)
+            w_out[n * K + k] = oracle_dequant8w_one(qweight, scales, zeros, K, G, n, k);
+    (void)nthreads;
+}
+
+/* y_ref[m][n] = sum_k (double)x[m][k] * (double)W_hat[n][k], FP64 in increasing k, unrounded. */
+double oracle_linear8w_one(const uint16_t* x_bf16, const uint32_t* qweight, const uint16_t* scales,
+                           const uint32_t* zeros, int64_t K, int64_t G, int64_t m, int64_t n)
+{
+    double acc = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        double xv = (double)oracle_bf16_to_f32(x_bf16[m * K + k]);
+        double wv = (double)oracle_dequant8w_one(qweight, scales, zeros, K, G, n, k);
+        acc += xv * wv;
+    }
+    return acc;
+}
+
+void oracle_linear8w(const uint16_t* x_bf16, const uint32_t* qweight, const uint16_t* scales,
+                     const uint32_t* zeros, int64_t M, int64_t N, int64_t K, int64_t G, double* y_out,
+                     int nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t m = 0; m < M; ++m) y_out[m * N + n] = oracle_linear8w_one(x_bf16, qweight, scales, zeros, K, G, m, n);
+    (void)nthreads;
+}
+
+void oracle_linear8w_sampled(const uint16_t* x_bf16, const uint32_t* qweight, const uint16_t* scales,
+                             const uint32_t* zeros, int64_t K, int64_t G, const int64_t* ms, const int64_t* ns,
+                             int64_t count, double* y_out, int nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int64_t i = 0; i < count; ++i)
+        y_out[i] = oracle_linear8w_one(x_bf16, qweight, scales, zeros, K, G, ms[i], ns[i]);
+    (void)nthreads;
+}
+
+/* ------------------------------------------------------------------------ */
 /* The super-block variant (Q4_K-style K-quant).                              */
 /* ------------------------------------------------------------------------ */
 

@@ -464,6 +464,77 @@ def test_linear8_brute_force_rational(M, N, Kg, G):
             assert abs(y[m, n] - ref) <= 1e-12 * max(1.0, abs(ref)), (m, n, y[m, n], ref)
 
 
+# ---- the 8-bit variant in the word layout (four codes per 32-bit word) ----------
+
+def _bytes_of(words, count):
+    """Bytes of little-endian 32-bit words, row by row (numpy's own view, not a shift)."""
+    return np.ascontiguousarray(words, dtype="<u4").view(np.uint8)[:, :count]
+
+
+@pytest.mark.parametrize("G", [32, 64, 128, 256])
+def test_pack8w_equals_the_two_plane_quantiser(G):
+    # the same 255-step quantiser: W_hat is bit-identical to the (separately pinned) two-plane
+    # storage, on random, outlier and special rows
+    rng = np.random.default_rng(300 + G)
+    N, K = 10, 4 * G
+    w16 = (rng.standard_normal((N, K)) * 0.02).astype(np.float16)
+    w16[1, ::7] *= np.float16(20.0)
+    w16[2] = 0.0
+    w16[3] = np.abs(w16[3])
+    w16[4] = -np.abs(w16[4])
+    w16[5, :G] = np.float16(2.0 ** -24)
+    q, s, z = oracle.pack8w(w16, G)
+    q2, s2, z2 = oracle.pack8(w16, G)
+    a = oracle.dequant8w(q, s, z, N, K, G)
+    b = oracle.dequant8(q2, s2, z2, N, K, G)
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    # the codes, zeros and scales themselves, read through numpy's byte view of the words
+    q8, z8, s8, _ = _planes(q2, s2, z2, K, G)
+    assert np.array_equal(_bytes_of(q, K).astype(np.int64), q8)
+    assert np.array_equal(_bytes_of(z, K // G).astype(np.int64), z8)
+    assert np.array_equal(s[:, : K // G].view(np.float16).astype(np.float64), s8)
+    assert np.all(s[:, K // G:] == 0) and np.all(_bytes_of(z, z.shape[1] * 4)[:, K // G:] == 0)    # padding
+
+
+@pytest.mark.parametrize("G", [32, 128])
+def test_pack8w_on_grid_round_trip(G):
+    rng = np.random.default_rng(400 + G)
+    N, K = 6, 2 * G
+    q8 = rng.integers(0, 256, (N, K))
+    z8 = rng.integers(0, 256, (N, K // G))
+    s8 = (rng.integers(4, 8, (N, K // G)) * 2.0 ** rng.integers(-14, -6, (N, K // G))).astype(np.float64)
+    q8[:, ::G] = 0
+    q8[:, 1::G] = 255
+    w = (q8 - np.repeat(z8, G, axis=1)) * np.repeat(s8, G, axis=1)
+    w16 = w.astype(np.float16)
+    assert np.array_equal(w16.astype(np.float64), w)
+    q, s, z = oracle.pack8w(w16, G)
+    assert np.array_equal(_bytes_of(q, K).astype(np.int64), q8)
+    assert np.array_equal(_bytes_of(z, K // G).astype(np.int64), z8)
+    assert np.array_equal(s[:, : K // G].view(np.float16).astype(np.float64), s8)
+
+
+@pytest.mark.parametrize("M,N,Kg,G", [(1, 8, 1, 32), (2, 8, 2, 32), (1, 8, 1, 64)])
+def test_linear8w_brute_force_rational(M, N, Kg, G):
+    K = Kg * G
+    rng = np.random.default_rng(M * 13 + N + Kg)
+    w16 = (rng.standard_normal((N, K)) * 0.05).astype(np.float16)
+    x = _bits(torch.from_numpy(rng.standard_normal((M, K)).astype(np.float32)).to(torch.bfloat16))
+    q, s, z = oracle.pack8w(w16, G)
+    y = oracle.linear8w(x, q, s, z, N, K, G)
+    qb, zb = _bytes_of(q, K), _bytes_of(z, K // G)
+    for m in range(M):
+        for n in range(N):
+            acc = Fraction(0)
+            for k in range(K):
+                g = k // G
+                acc += _frac_bf16(x[m, k]) * (int(qb[n, k]) - int(zb[n, g])) * _frac_f16(s[n, g])
+            ref = float(acc)
+            assert abs(y[m, n] - ref) <= 1e-12 * max(1.0, abs(ref)), (m, n, y[m, n], ref)
+    ms, ns = np.repeat(np.arange(M), N), np.tile(np.arange(N), M)
+    assert np.array_equal(oracle.linear8w_sampled(x, q, s, z, K, G, ms, ns), y.reshape(-1))
+
+
 def test_sampled_equals_full():
     N, K, G = 24, 512, 128
     q, s, z = _random_packed(N, K, G, 10)

@@ -33,6 +33,13 @@ MUTANTS = {
                                  0, "act_scale"),
     "8-bit high-plane scale 8 s8": ("srow[g] = oracle_f32_to_f16(16.0f * oracle_f16_to_f32(sb));",
                                     "srow[g] = oracle_f32_to_f16(8.0f * oracle_f16_to_f32(sb));", 0, "pack8 or linear8"),
+    # the 8-bit word layout
+    "8-bit word: codes high byte first": ("qrow[k / 4] |= (uint32_t)codes[i] << (8 * (k % 4));",
+                                          "qrow[k / 4] |= (uint32_t)codes[i] << (8 * (3 - k % 4));", 0, "pack8w"),
+    "8-bit word: zero in the next byte": ("zrow[g / 4] |= (uint32_t)z << (8 * (g % 4));",
+                                          "zrow[g / 4] |= (uint32_t)z << (8 * ((g + 1) % 4));", 0, "pack8w"),
+    "8-bit word: zero point added": ("    return (float)(q - z) * s;\n}\n\nvoid oracle_dequant8w(",
+                                     "    return (float)(q + z) * s;\n}\n\nvoid oracle_dequant8w(", 0, "8w"),
     # the super-block layer
     "q4k: m high bits at 2j + 1": ("rec[3] |= (uint32_t)(m[j] >> 4) << (16 + 2 * j);",
                                    "rec[3] |= (uint32_t)(m[j] >> 4) << (2 * j + 1);", 0, "q4k"),
