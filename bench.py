@@ -343,31 +343,54 @@ def run_ours(args):
 
 def e2e_ours(w4, mats, dev, args, gemm_ok):
     """Same metric through the C entry points, host buffers: every step copies
-    x from pinned host memory, runs the layer and reads y back to the host."""
+    x from pinned host memory, runs the layer and reads y back to the host.
+
+    As a serving loop does, the copies run on a copy stream and overlap the
+    neighbouring steps' layers: step i's inputs go in (into one of two device
+    buffers) while step i-1 computes, and its outputs come back while step i+1
+    computes; events order each copy against the layer calls that use its
+    buffer."""
     wk = wl.WORKLOADS[WORKLOAD]
     # the step's inputs (x of every matrix) travel in one host->device copy and its
     # outputs in one device->host copy; the layer calls take views of those buffers
     xs = [wl.activations_bf16(M_DECODE, lin.K, wl.act_seed(wk, j)) for j, (lin, _) in enumerate(mats)]
     hx_all = torch.cat([x.reshape(-1) for x in xs]).pin_memory()
-    hy_all = torch.empty(sum(M_DECODE * lin.N for lin, _ in mats), dtype=torch.bfloat16).pin_memory()
-    dx_all = torch.empty_like(hx_all, device=dev)
-    dy_all = torch.empty_like(hy_all, device=dev)
-    dx, dy, ox, oy = [], [], 0, 0
-    for lin, _ in mats:             # every view starts on a 16-byte boundary (K, N multiples of 8)
-        dx.append(dx_all[ox:ox + M_DECODE * lin.K].view(M_DECODE, lin.K))
-        dy.append(dy_all[oy:oy + M_DECODE * lin.N].view(M_DECODE, lin.N))
-        ox += M_DECODE * lin.K
-        oy += M_DECODE * lin.N
-    stream = torch.cuda.current_stream()
+    ny = sum(M_DECODE * lin.N for lin, _ in mats)
+    hy = [torch.empty(ny, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    dx_all = [torch.empty_like(hx_all, device=dev) for _ in range(2)]
+    dy_all = [torch.empty(ny, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    views = []
+    for b in range(2):                   # every view starts on a 16-byte boundary (K, N multiples of 8)
+        dx, dy, ox, oy = [], [], 0, 0
+        for lin, _ in mats:
+            dx.append(dx_all[b][ox:ox + M_DECODE * lin.K].view(M_DECODE, lin.K))
+            dy.append(dy_all[b][oy:oy + M_DECODE * lin.N].view(M_DECODE, lin.N))
+            ox += M_DECODE * lin.K
+            oy += M_DECODE * lin.N
+        views.append((dx, dy))
+    comp = torch.cuda.current_stream()
+    copy = torch.cuda.Stream()
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("h2d", "comp", "d2h")}
     steps = max(args.steps, 200)            # ~15 ms of steps: a few host hiccups do not dominate
     ncopy = len(mats[0][1])
 
     def run(n):
         for i in range(n):
-            dx_all.copy_(hx_all, non_blocking=True)
+            b = i % 2
+            dx, dy = views[b]
+            with torch.cuda.stream(copy):
+                copy.wait_event(ev["comp"][b])          # buffer b's previous layer calls are done
+                dx_all[b].copy_(hx_all, non_blocking=True)
+                ev["h2d"][b].record(copy)
+            comp.wait_event(ev["h2d"][b])
+            comp.wait_event(ev["d2h"][b])               # buffer b's previous outputs are read back
             for j, (lin, packed) in enumerate(mats):
-                w4.w4a16_linear(dx[j], *packed[i % ncopy], G, out=dy[j], stream=stream)
-            hy_all.copy_(dy_all, non_blocking=True)
+                w4.w4a16_linear(dx[j], *packed[i % ncopy], G, out=dy[j], stream=comp)
+            ev["comp"][b].record(comp)
+            with torch.cuda.stream(copy):
+                copy.wait_event(ev["comp"][b])
+                hy[b].copy_(dy_all[b], non_blocking=True)
+                ev["d2h"][b].record(copy)
         torch.cuda.synchronize()
 
     run(50)                                 # the host path (binding, caches, launch) warmed up
@@ -378,9 +401,10 @@ def e2e_ours(w4, mats, dev, args, gemm_ok):
     byts = sum(gemv_bytes(M_DECODE, lin.N, lin.K, G) for lin, _ in mats)
     return {"value": round(job_gbs(byts, steps, dt_ms, world), 1), "unit": "GB/s",
             "h2d_bytes_per_step": hx_all.numel() * 2,
-            "d2h_bytes_per_step": hy_all.numel() * 2,
-            "scope": "decode GEMVs (M=1) of the step, host wall clock, pinned buffers: one copy of the "
-                     "step's inputs in, eager layer calls, one copy of its outputs back"}
+            "d2h_bytes_per_step": ny * 2,
+            "scope": "decode GEMVs (M=1) of the step, host wall clock, pinned buffers: each step copies its "
+                     "inputs in and its outputs back on a copy stream, overlapping the neighbouring steps' "
+                     "layer calls (two device buffers, event-ordered)"}
 
 
 # ---------------------------------------------------------------------------
@@ -536,8 +560,8 @@ def run_sweep(args):
     a crossover summary per G for the batch sweep.  Each figure is the median
     of 5 replays of a CUDA graph of `steps` back-to-back launches over enough
     rotating weight copies that more than 2x L2 streams between two reads of a
-    copy.  The tensor-core path runs through its allocation-free entry point so
-    that it can be captured in a graph like the GEMV."""
+    copy.  The tensor-core path is timed as back-to-back eager calls (it takes
+    its scratch from the stream-ordered pool on every call)."""
     import w4a16_weight_only_linear_b300 as w4
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
@@ -560,7 +584,8 @@ def run_sweep(args):
     def record(wk, lin, M, Gv, path, us, nmat=1, extra_bytes=0):
         byts = nmat * gemv_bytes(M, lin.N, lin.K, Gv) - (nmat - 1) * M * lin.K * 2 + extra_bytes   # x read once
         fl = nmat * gemm_flops(M, lin.N, lin.K)
-        return emit({"sweep": wk.name, "matrix": lin.name if nmat == 1 else "gate+up", "M": M, "N": lin.N,
+        return emit({"sweep": wk.name, "matrix": lin.name if nmat == 1 else ("gate+up" if nmat == 2 else "q+k+v"),
+                     "M": M, "N": lin.N,
                      "K": lin.K, "G": Gv, "path": path, "us": round(us, 2),
                      "gbs": round(byts / (us * 1e-6) / 1e9, 1), "frac_hbm": round(byts / (us * 1e-6) / 1e9 / pk["hbm_gbs"], 4),
                      "tflops": round(fl / (us * 1e-6) / 1e12, 2),
@@ -578,7 +603,8 @@ def run_sweep(args):
             # same weights, and the gate projection paired with a second matrix of its shape
             def q4k_rec(lin, M, path, us, nmat=1):
                 byts = nmat * q4k_bytes(M, lin.N, lin.K) - (nmat - 1) * M * lin.K * 2
-                return emit({"sweep": wk.name, "matrix": lin.name if nmat == 1 else "gate+up", "M": M, "N": lin.N,
+                return emit({"sweep": wk.name, "matrix": lin.name if nmat == 1 else ("gate+up" if nmat == 2 else "q+k+v"),
+                     "M": M, "N": lin.N,
                              "K": lin.K, "G": 32, "path": path, "us": round(us, 2),
                              "gbs": round(byts / (us * 1e-6) / 1e9, 1),
                              "frac_hbm": round(byts / (us * 1e-6) / 1e9 / pk["hbm_gbs"], 4)})
@@ -614,29 +640,38 @@ def run_sweep(args):
                 del cps
             continue
         if wk.bits == 8:
-            # the 8-bit variant: codes as two 4-bit planes of a 2K-channel layer; the bytes read
-            # are those of that layer (both planes' scales and zeros) with x counted once
+            # the 8-bit variant in both storages: the word layout (four codes per word, one scale
+            # and one 8-bit zero per group; bytes = codes + scales + 8-bit zeros + x + y) and the
+            # two planes of a 2K-channel 4-bit layer (bytes = what the kernels read: both planes'
+            # scales and 4-bit zeros, x once, y)
             for j, lin in enumerate(wk.linears):
                 for Gv in wk.Gs:
                     w = wl.weight_f16(lin.N, lin.K, wk.sigma, wl.matrix_seed(wk, j), wk.outlier_frac).to(dev)
-                    one = gemv_bytes(1, lin.N, 2 * lin.K, Gv)
-                    cps = [w4.w8a16_pack(w, Gv) for _ in range(max(2, -(-2 * l2_bytes // one) + 1))]
+                    word_bytes = (lin.N * lin.K + lin.N * (lin.K // Gv) * 3)          # codes, scales, zeros
+                    ncp = max(2, -(-2 * l2_bytes // word_bytes) + 1)
+                    cps_w = [w4.w8a16_pack(w, Gv) for _ in range(ncp)]
+                    cps_p = [w4.w8a16_planes_pack(w, Gv) for _ in range(ncp)]
                     del w
                     for M in wk.Ms:
                         x = wl.activations_bf16(M, lin.K, wl.act_seed(wk, j)).to(dev)
                         y = torch.empty(M, lin.N, dtype=torch.bfloat16, device=dev)
-                        fn = lambda i, s: w4.w8a16_linear(x, *cps[i % len(cps)], Gv, out=y, stream=s)
-                        graph = w4.w4a16_linear_path(M, lin.N, 2 * lin.K, Gv) == 1
-                        us = _graph_us(fn, n) if graph else _eager_us(fn, n)
-                        byts = gemv_bytes(M, lin.N, 2 * lin.K, Gv) - M * lin.K * 2
-                        results.append(emit({"sweep": wk.name, "matrix": lin.name, "M": M, "N": lin.N, "K": lin.K,
-                                             "G": Gv, "path": "w8 gemv" if graph else "w8 gemm (eager)",
-                                             "us": round(us, 2), "gbs": round(byts / (us * 1e-6) / 1e9, 1),
-                                             "frac_hbm": round(byts / (us * 1e-6) / 1e9 / pk["hbm_gbs"], 4),
-                                             "tflops": round(gemm_flops(M, lin.N, lin.K) / (us * 1e-6) / 1e12, 2),
-                                             "frac_tensor": round(gemm_flops(M, lin.N, lin.K) / (us * 1e-6) / 1e12
-                                                                  / pk["bf16_tflops"], 4)}))
-                    del cps
+                        for store, cps, fn, byts, graph in (
+                                ("word", cps_w, w4.w8a16_linear, word_bytes + M * lin.K * 2 + M * lin.N * 2,
+                                 M <= 8 and Gv <= 128),
+                                ("planes", cps_p, w4.w8a16_planes_linear,
+                                 gemv_bytes(M, lin.N, 2 * lin.K, Gv) - M * lin.K * 2,
+                                 w4.w4a16_linear_path(M, lin.N, 2 * lin.K, Gv) == 1)):
+                            f = (lambda cps, fn: lambda i, s: fn(x, *cps[i % len(cps)], Gv, out=y, stream=s))(cps, fn)
+                            us = _graph_us(f, n) if graph else _eager_us(f, n)
+                            results.append(emit({"sweep": wk.name, "matrix": lin.name, "M": M, "N": lin.N,
+                                                 "K": lin.K, "G": Gv,
+                                                 "path": f"w8 {store} " + ("gemv" if graph else "gemm (eager)"),
+                                                 "us": round(us, 2), "gbs": round(byts / (us * 1e-6) / 1e9, 1),
+                                                 "frac_hbm": round(byts / (us * 1e-6) / 1e9 / pk["hbm_gbs"], 4),
+                                                 "tflops": round(gemm_flops(M, lin.N, lin.K) / (us * 1e-6) / 1e12, 2),
+                                                 "frac_tensor": round(gemm_flops(M, lin.N, lin.K) / (us * 1e-6) / 1e12
+                                                                      / pk["bf16_tflops"], 4)}))
+                    del cps_w, cps_p
             continue
         if wk.act_scaled:
             # activation scale fused into x staging (the x_scale vector counts as bytes read);
@@ -684,15 +719,32 @@ def run_sweep(args):
                     paths = []
                     if w4.w4a16_linear_path(M, lin.N, lin.K, Gv) == 1 or M <= 16:
                         paths.append(("gemv", w4.w4a16_linear_gemv))
-                    if name == "up13b_sweep" and M * lin.K <= w4.NOALLOC_MAX_X_ELEMS:
-                        paths.append(("gemm", w4.w4a16_linear_gemm_noalloc))
+                    if name == "up13b_sweep":
+                        paths.append(("gemm", w4.w4a16_linear_gemm))
                     for pname, fn in paths:
+                        # the tensor-core call allocates its x copy and split workspace stream-ordered,
+                        # so it is timed as back-to-back eager calls
+                        timer = _eager_us if pname == "gemm" else _graph_us
                         try:
-                            us = _graph_us(lambda i, s: fn(x, *cps[i % len(cps)], Gv, out=y, stream=s), n)
+                            us = timer(lambda i, s: fn(x, *cps[i % len(cps)], Gv, out=y, stream=s), n)
                         except w4.W4A16Error:
                             continue
                         results.append(record(wk, lin, M, Gv, pname, us))
                 del cps
+        if name == "layer13b_decode":
+            # the attention projections q, k and v share x: one launch over the three matrices
+            lins = wk.linears[:3]
+            Gv = wk.Gs[0]
+            cps3 = [packed_copies(wk, j, lin, Gv) for j, lin in enumerate(lins)]
+            nc = min(len(c) for c in cps3)
+            for M in wk.Ms:
+                x = wl.activations_bf16(M, lins[0].K, wl.act_seed(wk, 0)).to(dev)
+                ys = [torch.empty(M, lin.N, dtype=torch.bfloat16, device=dev) for lin in lins]
+                us = _graph_us(lambda i, s: w4.w4a16_linear_multi(x, [c[i % nc] for c in cps3], Gv, out=ys,
+                                                                  stream=s), n)
+                rec = record(wk, lins[0], M, Gv, "multi (q,k,v)", us, nmat=3)
+                results.append(rec)
+            del cps3
     assert w4.w4a16_device_status() == 0
 
     # crossover on the batch sweep, per G: the smallest M at which the tensor-core path is
@@ -724,6 +776,56 @@ def run_sweep(args):
     emit({"crossover": cross, "note": "pages: 16 to 32"})
 
 
+def run_oracle_table(args):
+    """The CPU oracle timed on this machine's host cores for every configuration
+    (a reported baseline, never a target): for each (workload, matrix, M) one
+    seeded problem, timed at 1 thread and at all threads on a bounded sample of
+    output rows (and, for M = 2048, a 64-row activation subset), each figure
+    extrapolated to the full launch by the work it covers.  One JSON line per
+    point: GB/s for decode rows (the GEMV's algorithmic bytes), GFLOP/s for the
+    prefill rows."""
+    import oracle
+    threads_all = oracle.max_threads()
+    points = [("single_4096", 0, 1, 128), ("layer13b_decode", 0, 1, 128), ("layer13b_decode", 4, 1, 128),
+              ("layer13b_decode", 6, 1, 128)]
+    points += [("up13b_sweep", 0, M, 128) for M in (1, 2, 4, 8, 16, 32)]
+    points += [("gateup13b_dual", 0, M, 128) for M in (1, 4)]
+    points += [("ffn70b", j, M, 128) for j in (0, 1) for M in (1, 2048)]
+    for name, j, M, Gv in points:
+        wk = wl.WORKLOADS[name]
+        lin = wk.linears[j]
+        w = wl.weight_f16(lin.N, lin.K, wk.sigma, wl.matrix_seed(wk, j), wk.outlier_frac)
+        q, s_, z = oracle.pack(wl.bits_u16(w), Gv)
+        del w
+        Ms = min(M, 64)                                   # activation rows actually computed
+        x = wl.bits_u16(wl.activations_bf16(Ms, lin.K, wl.act_seed(wk, j)))
+        nmat = 2 if wk.dual else 1
+        rec = {"oracle_table": name, "matrix": lin.name if nmat == 1 else "gate+up (2 GEMVs)", "M": M,
+               "N": lin.N, "K": lin.K, "G": Gv}
+        for label, nthreads, target in (("1_thread", 1, 1.0e8), ("all_threads", threads_all, 4.0e8)):
+            stride = max(1, int(Ms * lin.N * lin.K / target))
+            ns = np.arange(0, lin.N, stride, dtype=np.int64)
+            ms = np.repeat(np.arange(Ms, dtype=np.int64), ns.size)
+            nn = np.tile(ns, Ms)
+            oracle.linear_sampled(x, q, s_, z, lin.K, Gv, ms[:64], nn[:64], nthreads)      # warm
+            t0 = time.perf_counter()
+            oracle.linear_sampled(x, q, s_, z, lin.K, Gv, ms, nn, nthreads)
+            dt = time.perf_counter() - t0
+            frac = (ms.size / (M * lin.N))                # share of the launch's outputs computed
+            full_s = nmat * dt / frac
+            if M > 16:
+                rec[label] = {"gflops": round(nmat * gemm_flops(M, lin.N, lin.K) / full_s / 1e9, 3),
+                              "s_per_launch": round(full_s, 3), "threads": nthreads,
+                              "sample": f"{ms.size} outputs ({Ms} rows x every {_ordinal(stride)} column)"}
+            else:
+                byts = nmat * gemv_bytes(M, lin.N, lin.K, Gv) - (nmat - 1) * M * lin.K * 2
+                rec[label] = {"gbs": round(byts / full_s / 1e9, 4), "s_per_launch": round(full_s, 4),
+                              "threads": nthreads, "sample": f"{ms.size} outputs (every {_ordinal(stride)} column)"}
+        oracle.linear_sampled(x, q, s_, z, lin.K, Gv, ms[:1], nn[:1], threads_all)       # back to all threads
+        rec["extrapolated"] = True
+        print(json.dumps(rec), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--profile", choices=["decode", "prefill"], default=None,
@@ -738,10 +840,14 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="time the other workloads (decode layers, batch x group sweep, dual) instead")
     ap.add_argument("--only", default="", help="with --sweep: comma-separated workload names to time")
+    ap.add_argument("--oracle-table", action="store_true",
+                    help="time the CPU oracle at 1 thread and all threads for every configuration")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.profile:
+    if args.oracle_table:
+        run_oracle_table(args)
+    elif args.profile:
         run_profile(args)
     elif args.sweep:
         run_sweep(args)

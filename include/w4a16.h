@@ -169,6 +169,32 @@ W4A16_API w4a16_status w4a16_linear_dual(const void* x_bf16,
                                void* y_gate_bf16, void* y_up_bf16, w4a16_stream_t stream);
 
 /*
+ * w4a16_linear_multi: up to four projections of the same x in one pass, each
+ * with its own output size (e.g. the q, k and v projections of an attention
+ * layer, grouped-query k/v included):  y_i = x * W_hat_i^T,  i < nmat.
+ * At decode a layer's fixed per-launch cost (staging x, the first weights'
+ * latency, the tail) is paid once for all the matrices instead of once each,
+ * the multi-matrix generalisation of the paired gate/up traversal (zhuai.tech
+ * "Quantization Is Not a Zip File", section 2 "Moving fewer bytes can make
+ * decode faster").
+ *   nmat        1..4
+ *   qweight[i], scales_f16[i], zeros[i], y_bf16[i]
+ *               HOST arrays of nmat DEVICE pointers: matrix i packed as
+ *               above for [N[i], K] (same K and G for all), output y_i BF16
+ *               [M, N[i]]
+ *   N           HOST array of nmat output sizes (multiples of 8; 0 = skip)
+ * M <= 8 runs one decode launch over all the matrices (when their rows fit
+ * the kernel's shared memory); larger M runs the tensor-core kernel once per
+ * matrix on one FP16 copy of x.  The arrays are read during the call only.
+ * Errors: W4A16_ERR_INVALID_ARG for nmat outside 1..4 or a null array, else
+ * as w4a16_linear for each matrix.
+ */
+W4A16_API w4a16_status w4a16_linear_multi(const void* x_bf16, int nmat, const uint32_t* const* qweight,
+                                          const void* const* scales_f16, const uint32_t* const* zeros,
+                                          const int64_t* N, int64_t M, int64_t K, int G, void* const* y_bf16,
+                                          w4a16_stream_t stream);
+
+/*
  * Explicit-path variants of w4a16_linear, same arguments and result, for
  * measuring both kernels on the same shape (e.g. the batch at which the
  * decode kernel stops being bandwidth bound).
@@ -264,10 +290,29 @@ W4A16_API w4a16_status w4a16_linear_dual_act_scaled(const void* x_bf16, const fl
  *   s8 = RNE_fp16( fp32(hi - lo) / 255 ); s8 == 0 -> s8 = 1, z8 = 0
  *   z8 = clamp(rne(-lo / s8), 0, 255),  q8 = clamp(rne(w / s8) + z8, 0, 255)
  * (weights stored as INT8 or INT4 with 16-bit activations: klaylearn.com
- * glossary "Weight-Only Quantisation", first FAQ answer).  Storage: each 8-bit
- * code is kept as two 4-bit planes of a 4-bit layer with 2K input channels,
- * so the 4-bit kernels compute the 8-bit layer exactly
- * (16 s8 (q8>>4 - z8>>4) + s8 (q8&15 - z8&15) = s8 (q8 - z8)):
+ * glossary "Weight-Only Quantisation", first FAQ answer).  Two storages:
+ *
+ * The word layout (w8a16_*): four codes per 32-bit word, one FP16 scale and
+ * one 8-bit zero point per group:
+ *   qweight  uint32 [N, K/4]   code of (n, k) in bits 8*(k%4) .. 8*(k%4)+7 of
+ *                              word k/4 (low byte first)
+ *   scales   FP16 [N, ldS]     as the 4-bit layout (ldS = w8a16_scales_ld)
+ *   zeros    uint32 [N, ldZ8]  zero point of group g in bits 8*(g%4) .. of word
+ *                              g/4; ldZ8 = ceil(K/G / 4) rounded up to a
+ *                              multiple of 4 (w8a16_zeros_ld)
+ *   W_hat = (q8 - z8) * s8, 8.125 bits per weight at G = 128.
+ * w8a16_linear runs the decode kernel for M <= 8 and G <= 128 (where its rows
+ * fit), which expands each code as its two nibbles against one FP16 exponent,
+ * else the tensor-core kernel, which expands four codes per word with two byte
+ * permutes.  w8a16_linear_gemv / _gemm force one kernel (the decode kernel
+ * takes M <= 8 and G <= 128; W4A16_ERR_UNSUPPORTED otherwise).
+ * w8a16_dequant (FP32) and w8a16_dequant_f16 (the tensor-core kernel's FP16
+ * operand) are checking aids through the kernels' own 8-bit expansions, as
+ * w4a16_dequant and w4a16_dequant_f16 are for the 4-bit layout.
+ *
+ * The two-plane storage (w8a16_planes_*): each 8-bit code as two 4-bit planes
+ * of a 4-bit layer with 2K input channels, so the 4-bit kernels compute the
+ * 8-bit layer exactly (16 s8 (q8>>4 - z8>>4) + s8 (q8&15 - z8&15) = s8 (q8 - z8)):
  *   qweight  uint32 [N, K/4]   row n: the K codes' high nibbles (channels
  *                              0..K-1) then their low nibbles (K..2K-1), in the
  *                              4-bit layout (8 bits per weight)
@@ -275,8 +320,9 @@ W4A16_API w4a16_status w4a16_linear_dual_act_scaled(const void* x_bf16, const fl
  *                              lo-plane scales s8 (ldS8 = w4a16_scales_ld(2K, G))
  *   zeros    uint32 [N, ldZ8]  z8 >> 4 per group, then z8 & 15 per group, packed
  *                              as 4-bit zeros of 2K/G groups (ldZ8 = w4a16_zeros_ld(2K, G))
- * The layout helpers below return K/4, ldS8 and ldZ8.  Preconditions and
- * errors as for the 4-bit calls; the dispatch is w4a16_linear_path(M, N, 2K, G).
+ * (8.25 bits per weight at G = 128: each scale is stored twice.)  Its dispatch
+ * is w4a16_linear_path(M, N, 2K, G).
+ * Preconditions and errors as for the 4-bit calls.
  */
 W4A16_API int64_t w8a16_qweight_ld(int64_t K);
 W4A16_API int64_t w8a16_scales_ld(int64_t K, int G);
@@ -287,6 +333,25 @@ W4A16_API w4a16_status w8a16_pack(const void* w_f16, int64_t N, int64_t K, int G
 W4A16_API w4a16_status w8a16_linear(const void* x_bf16, const uint32_t* qweight, const void* scales_f16,
                                     const uint32_t* zeros, int64_t M, int64_t N, int64_t K, int G,
                                     void* y_bf16, w4a16_stream_t stream);
+W4A16_API w4a16_status w8a16_linear_gemv(const void* x_bf16, const uint32_t* qweight, const void* scales_f16,
+                                         const uint32_t* zeros, int64_t M, int64_t N, int64_t K, int G,
+                                         void* y_bf16, w4a16_stream_t stream);
+W4A16_API w4a16_status w8a16_linear_gemm(const void* x_bf16, const uint32_t* qweight, const void* scales_f16,
+                                         const uint32_t* zeros, int64_t M, int64_t N, int64_t K, int G,
+                                         void* y_bf16, w4a16_stream_t stream);
+W4A16_API w4a16_status w8a16_dequant(const uint32_t* qweight, const void* scales_f16, const uint32_t* zeros,
+                                     int64_t N, int64_t K, int G, float* w_out, w4a16_stream_t stream);
+W4A16_API w4a16_status w8a16_dequant_f16(const uint32_t* qweight, const void* scales_f16, const uint32_t* zeros,
+                                         int64_t N, int64_t K, int G, void* w_out_f16, w4a16_stream_t stream);
+
+W4A16_API int64_t w8a16_planes_qweight_ld(int64_t K);
+W4A16_API int64_t w8a16_planes_scales_ld(int64_t K, int G);
+W4A16_API int64_t w8a16_planes_zeros_ld(int64_t K, int G);
+W4A16_API w4a16_status w8a16_planes_pack(const void* w_f16, int64_t N, int64_t K, int G, uint32_t* qweight,
+                                         void* scales_f16, uint32_t* zeros, w4a16_stream_t stream);
+W4A16_API w4a16_status w8a16_planes_linear(const void* x_bf16, const uint32_t* qweight, const void* scales_f16,
+                                           const uint32_t* zeros, int64_t M, int64_t N, int64_t K, int G,
+                                           void* y_bf16, w4a16_stream_t stream);
 
 /* ---- the super-block variant (Q4_K-style) ------------------------------------
  * K-quants keep 4-bit codes in 256-weight super-blocks whose sub-blocks carry

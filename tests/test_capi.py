@@ -145,22 +145,49 @@ def test_dual_argument_errors():
     assert f(a, a, a, a, a, a, a, 0, 64, 256, 128, a, a, v(0)) == 0
 
 
-def test_w8a16_layout_and_argument_errors():
-    for K, G in ((4096, 128), (5120, 32), (13824, 128), (64, 32)):
+def test_w8a16_word_layout_and_argument_errors():
+    for K, G in ((4096, 128), (5120, 32), (13824, 128), (64, 32), (96, 32), (768, 256)):
+        ng = K // G
         assert w4._lib.w8a16_qweight_ld(K) == K // 4
-        assert w4._lib.w8a16_scales_ld(K, G) == w4.w4a16_scales_ld(2 * K, G)
-        assert w4._lib.w8a16_zeros_ld(K, G) == w4.w4a16_zeros_ld(2 * K, G)
+        assert w4._lib.w8a16_scales_ld(K, G) == w4.w4a16_scales_ld(K, G)
+        ldz = w4._lib.w8a16_zeros_ld(K, G)
+        assert ldz >= (ng + 3) // 4 and ldz % 4 == 0 and ldz - (ng + 3) // 4 < 4        # 16-byte rows
     v = ctypes.c_void_p
     a = v(1 << 12)
     assert w4._lib.w8a16_pack(a, 64, 256, 100, a, a, a, v(0)) == 2
     assert w4._lib.w8a16_pack(a, 60, 256, 128, a, a, a, v(0)) == 1
     assert w4._lib.w8a16_pack(v((1 << 12) + 4), 64, 256, 128, a, a, a, v(0)) == 3
     assert w4._lib.w8a16_pack(a, 0, 256, 128, a, a, a, v(0)) == 0
-    assert _call_linear("w8a16_linear", G=48) == 2
-    assert _call_linear("w8a16_linear", K=200) == 1
-    assert _call_linear("w8a16_linear", x=0) == 1
-    assert _call_linear("w8a16_linear", s=(1 << 12) + 2) == 3
-    assert _call_linear("w8a16_linear", M=0) == 0
+    for fn in ("w8a16_linear", "w8a16_linear_gemv", "w8a16_linear_gemm"):
+        assert _call_linear(fn, G=48) == 2
+        assert _call_linear(fn, K=200) == 1
+        assert _call_linear(fn, x=0) == 1
+        assert _call_linear(fn, s=(1 << 12) + 2) == 3
+        assert _call_linear(fn, M=0) == 0
+    for fn in ("w8a16_dequant", "w8a16_dequant_f16"):
+        f = getattr(w4._lib, fn)
+        assert f(a, a, a, 64, 256, 100, a, v(0)) == 2
+        assert f(a, a, a, 60, 256, 128, a, v(0)) == 1
+        assert f(a, a, a, 64, 256, 128, v((1 << 12) + 4), v(0)) == 3
+        assert f(a, a, a, 0, 256, 128, a, v(0)) == 0
+
+
+def test_w8a16_planes_layout_and_argument_errors():
+    for K, G in ((4096, 128), (5120, 32), (13824, 128), (64, 32)):
+        assert w4._lib.w8a16_planes_qweight_ld(K) == K // 4
+        assert w4._lib.w8a16_planes_scales_ld(K, G) == w4.w4a16_scales_ld(2 * K, G)
+        assert w4._lib.w8a16_planes_zeros_ld(K, G) == w4.w4a16_zeros_ld(2 * K, G)
+    v = ctypes.c_void_p
+    a = v(1 << 12)
+    assert w4._lib.w8a16_planes_pack(a, 64, 256, 100, a, a, a, v(0)) == 2
+    assert w4._lib.w8a16_planes_pack(a, 60, 256, 128, a, a, a, v(0)) == 1
+    assert w4._lib.w8a16_planes_pack(v((1 << 12) + 4), 64, 256, 128, a, a, a, v(0)) == 3
+    assert w4._lib.w8a16_planes_pack(a, 0, 256, 128, a, a, a, v(0)) == 0
+    assert _call_linear("w8a16_planes_linear", G=48) == 2
+    assert _call_linear("w8a16_planes_linear", K=200) == 1
+    assert _call_linear("w8a16_planes_linear", x=0) == 1
+    assert _call_linear("w8a16_planes_linear", s=(1 << 12) + 2) == 3
+    assert _call_linear("w8a16_planes_linear", M=0) == 0
 
 
 def test_q4k_layout_and_argument_errors():
@@ -277,3 +304,24 @@ def test_entry_points_from_several_threads():
     for t in threads:
         t.join()
     assert not errors, errors[:5]
+
+
+def test_multi_argument_errors():
+    v = ctypes.c_void_p
+    a = 1 << 12
+    arr = lambda *p: (ctypes.c_void_p * len(p))(*p)
+    ns = lambda *n: (ctypes.c_int64 * len(n))(*n)
+    f = w4._lib.w4a16_linear_multi
+    q3, s3, z3, y3 = arr(a, a, a), arr(a, a, a), arr(a, a, a), arr(a, a, a)
+    assert f(v(a), 0, q3, s3, z3, ns(64, 64, 64), 1, 256, 128, y3, v(0)) == 1      # nmat outside 1..4
+    assert f(v(a), 5, q3, s3, z3, ns(64, 64, 64), 1, 256, 128, y3, v(0)) == 1
+    assert f(v(a), 3, None, s3, z3, ns(64, 64, 64), 1, 256, 128, y3, v(0)) == 1    # null array
+    assert f(v(a), 3, q3, s3, z3, None, 1, 256, 128, y3, v(0)) == 1
+    assert f(v(a), 3, q3, s3, z3, ns(64, 60, 64), 1, 256, 128, y3, v(0)) == 1     # N % 8
+    assert f(v(a), 3, q3, s3, z3, ns(64, 64, 64), 1, 256, 96, y3, v(0)) == 2       # group size
+    assert f(v(a), 3, q3, s3, z3, ns(64, 64, 64), 1, 250, 128, y3, v(0)) == 1      # K % G
+    assert f(v(a), 3, arr(a, 0, a), s3, z3, ns(64, 64, 64), 1, 256, 128, y3, v(0)) == 1
+    assert f(v(a), 3, q3, s3, z3, ns(64, 64, 64), 1, 256, 128, arr(a, a + 2, a), v(0)) == 3
+    assert f(v(a + 8), 3, q3, s3, z3, ns(64, 64, 64), 1, 256, 128, y3, v(0)) == 3
+    assert f(v(a), 3, q3, s3, z3, ns(64, 64, 64), 0, 256, 128, y3, v(0)) == 0      # empty problem
+    assert f(v(a), 3, q3, s3, z3, ns(0, 0, 0), 1, 256, 128, y3, v(0)) == 0

@@ -39,6 +39,7 @@ EXPORTS = {
     "q4k_dequant": ([_vp, _vp, _i64, _i64, _vp, _vp], _i32),
     "w4a16_linear": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp], _i32),
     "w4a16_linear_dual": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp, _vp], _i32),
+    "w4a16_linear_multi": ([_vp, _i32, _vp, _vp, _vp, _vp, _i64, _i64, _i32, _vp, _vp], _i32),
     "w4a16_linear_gemv": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp], _i32),
     "w4a16_linear_gemm": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp], _i32),
     "w4a16_linear_gemm_noalloc": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp], _i32),
@@ -48,6 +49,15 @@ EXPORTS = {
     "w8a16_zeros_ld": ([_i64, _i32], _i64),
     "w8a16_pack": ([_vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp], _i32),
     "w8a16_linear": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp], _i32),
+    "w8a16_linear_gemv": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp], _i32),
+    "w8a16_linear_gemm": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp], _i32),
+    "w8a16_dequant": ([_vp, _vp, _vp, _i64, _i64, _i32, _vp, _vp], _i32),
+    "w8a16_dequant_f16": ([_vp, _vp, _vp, _i64, _i64, _i32, _vp, _vp], _i32),
+    "w8a16_planes_qweight_ld": ([_i64], _i64),
+    "w8a16_planes_scales_ld": ([_i64, _i32], _i64),
+    "w8a16_planes_zeros_ld": ([_i64, _i32], _i64),
+    "w8a16_planes_pack": ([_vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp], _i32),
+    "w8a16_planes_linear": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp], _i32),
     "w4a16_linear_dual_act_scaled": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _vp,
                                       _vp], _i32),
     "q4k_meta_ld": ([_i64], _i64),
@@ -237,6 +247,27 @@ def w4a16_linear_dual(x, gate, up, G, out=None, stream=None):
     return yg, yu
 
 
+def w4a16_linear_multi(x, mats, G, out=None, stream=None):
+    """[x * W_hat_i^T for each (qweight, scales, zeros) in mats] (1..4 matrices
+    sharing x, each with its own output size), in one decode launch at M <= 8."""
+    M, K = x.shape
+    n = len(mats)
+    if not 1 <= n <= 4:
+        raise ValueError("w4a16_linear_multi takes 1 to 4 matrices")
+    Ns = [m[0].shape[0] for m in mats]
+    if out is None:
+        out = [torch.empty((M, Ni), dtype=torch.bfloat16, device=x.device) for Ni in Ns]
+    arr = ctypes.c_void_p * n
+    qs = arr(*[_dev(m[0], torch.int32, "qweight") for m in mats])
+    ss = arr(*[_dev(m[1], torch.float16, "scales") for m in mats])
+    zs = arr(*[_dev(m[2], torch.int32, "zeros") for m in mats])
+    ys = arr(*[_dev(o, torch.bfloat16, "y") for o in out])
+    ns = (ctypes.c_int64 * n)(*Ns)
+    _check("w4a16_linear_multi", _lib.w4a16_linear_multi(_dev(x, torch.bfloat16, "x"), n, qs, ss, zs, ns, M, K, G,
+                                                         ys, _stream(stream)))
+    return out
+
+
 def w4a16_linear_act_scaled(x, x_scale, q, s, z, G, out=None, stream=None):
     """y BF16 [M,N] = (x * x_scale) * W_hat^T: x_scale FP32 [K] multiplies each
     input channel of x before it is rounded to FP16 (the deployed form of
@@ -277,13 +308,13 @@ def w4a16_linear_dual_act_scaled(x, x_scale, gate, up, G, out=None, stream=None)
 # ---- the 8-bit variant ---------------------------------------------------------
 
 def w8a16_packed_shapes(N, K, G):
-    """Shapes of (qweight int32, scales FP16, zeros int32) of an 8-bit layer."""
+    """Shapes of (qweight int32, scales FP16, zeros int32) of the 8-bit word layout."""
     return (N, _lib.w8a16_qweight_ld(K)), (N, _lib.w8a16_scales_ld(K, G)), (N, _lib.w8a16_zeros_ld(K, G))
 
 
 def w8a16_pack(w, G, out=None, stream=None):
-    """FP16 W [N,K] -> (qweight, scales, zeros) of the 8-bit layer (codes as two
-    4-bit planes; see the header)."""
+    """FP16 W [N,K] -> (qweight, scales, zeros) of the 8-bit word layout (four codes
+    per word, one FP16 scale and one 8-bit zero point per group)."""
     N, K = w.shape
     if out is None:
         sq, ss, sz = w8a16_packed_shapes(N, K, G)
@@ -297,8 +328,65 @@ def w8a16_pack(w, G, out=None, stream=None):
 
 
 def w8a16_linear(x, q, s, z, G, out=None, stream=None):
-    """y BF16 [M,N] = x BF16 [M,K] * W_hat8^T."""
+    """y BF16 [M,N] = x BF16 [M,K] * W_hat8^T, 8-bit word layout."""
     return _linear("w8a16_linear", x, q, s, z, q.shape[0], G, out, stream)
+
+
+def w8a16_linear_gemv(x, q, s, z, G, out=None, stream=None):
+    """8-bit word layout, decode kernel only (M <= 8, G <= 128)."""
+    return _linear("w8a16_linear_gemv", x, q, s, z, q.shape[0], G, out, stream)
+
+
+def w8a16_linear_gemm(x, q, s, z, G, out=None, stream=None):
+    """8-bit word layout, tensor-core kernel only (any M)."""
+    return _linear("w8a16_linear_gemm", x, q, s, z, q.shape[0], G, out, stream)
+
+
+def w8a16_dequant(q, s, z, N, K, G, out=None, stream=None):
+    """W_hat FP32 [N,K] of the 8-bit word layout through the decode kernel's own
+    8-bit expansion (checking aid)."""
+    if out is None:
+        out = torch.empty((N, K), dtype=torch.float32, device=q.device)
+    _check("w8a16_dequant", _lib.w8a16_dequant(_dev(q, torch.int32, "qweight"), _dev(s, torch.float16, "scales"),
+                                               _dev(z, torch.int32, "zeros"), N, K, G, _dev(out, torch.float32, "out"),
+                                               _stream(stream)))
+    return out
+
+
+def w8a16_dequant_f16(q, s, z, N, K, G, out=None, stream=None):
+    """RN_fp16(W_hat) FP16 [N,K] of the 8-bit word layout through the tensor-core
+    kernel's own 8-bit expansion (checking aid)."""
+    if out is None:
+        out = torch.empty((N, K), dtype=torch.float16, device=q.device)
+    _check("w8a16_dequant_f16", _lib.w8a16_dequant_f16(
+        _dev(q, torch.int32, "qweight"), _dev(s, torch.float16, "scales"), _dev(z, torch.int32, "zeros"), N, K, G,
+        _dev(out, torch.float16, "out"), _stream(stream)))
+    return out
+
+
+def w8a16_planes_packed_shapes(N, K, G):
+    """Shapes of (qweight int32, scales FP16, zeros int32) of an 8-bit layer."""
+    return (N, _lib.w8a16_planes_qweight_ld(K)), (N, _lib.w8a16_planes_scales_ld(K, G)), (N, _lib.w8a16_planes_zeros_ld(K, G))
+
+
+def w8a16_planes_pack(w, G, out=None, stream=None):
+    """FP16 W [N,K] -> (qweight, scales, zeros) of the 8-bit layer (codes as two
+    4-bit planes; see the header)."""
+    N, K = w.shape
+    if out is None:
+        sq, ss, sz = w8a16_planes_packed_shapes(N, K, G)
+        out = (torch.empty(sq, dtype=torch.int32, device=w.device), torch.empty(ss, dtype=torch.float16, device=w.device),
+               torch.empty(sz, dtype=torch.int32, device=w.device))
+    q, s, z = out
+    _check("w8a16_planes_pack", _lib.w8a16_planes_pack(_dev(w, torch.float16, "w"), N, K, G, _dev(q, torch.int32, "qweight"),
+                                         _dev(s, torch.float16, "scales"), _dev(z, torch.int32, "zeros"),
+                                         _stream(stream)))
+    return q, s, z
+
+
+def w8a16_planes_linear(x, q, s, z, G, out=None, stream=None):
+    """y BF16 [M,N] = x BF16 [M,K] * W_hat8^T."""
+    return _linear("w8a16_planes_linear", x, q, s, z, q.shape[0], G, out, stream)
 
 
 def q4k_packed_shapes(N, K):

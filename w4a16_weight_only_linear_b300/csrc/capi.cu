@@ -93,6 +93,35 @@ w4a16_status dual_common(const void* x_bf16, const uint32_t* qweight_gate, const
     return from_cuda(w4a16::launch_gemm(x_bf16, mats, 2, M, N, K, G, cs, xsc));
 }
 
+// Up to four matrices of their own output sizes sharing x (w4a16_linear_multi).
+w4a16_status multi_common(const void* x, int nmat, const uint32_t* const* q, const void* const* s,
+                          const uint32_t* const* z, const int64_t* Ns, int64_t M, int64_t K, int G, void* const* y,
+                          w4a16_stream_t stream) {
+    if (nmat < 1 || nmat > w4a16::kMaxMat || !q || !s || !z || !Ns || !y) return W4A16_ERR_INVALID_ARG;
+    w4a16_status st;
+    for (int i = 0; i < nmat; ++i)
+        if ((st = check_weight_shape(Ns[i], K, G)) != W4A16_OK) return st;
+    if (M < 0 || M > kMaxDim) return W4A16_ERR_INVALID_ARG;
+    GemvMat mats[w4a16::kMaxMat];
+    int64_t Nl[w4a16::kMaxMat];
+    int n = 0;
+    for (int i = 0; i < nmat; ++i) {
+        if (Ns[i] == 0) continue;                     // an empty matrix: nothing to compute
+        if ((st = check_weights(q[i], s[i], z[i])) != W4A16_OK) return st;
+        if (!y[i]) return W4A16_ERR_INVALID_ARG;
+        if (!aligned16(y[i])) return W4A16_ERR_MISALIGNED;
+        mats[n] = GemvMat{q[i], s[i], z[i], y[i], Ns[i]};
+        Nl[n++] = Ns[i];
+    }
+    if (M == 0 || n == 0) return W4A16_OK;
+    if (!x) return W4A16_ERR_INVALID_ARG;
+    if (!aligned16(x)) return W4A16_ERR_MISALIGNED;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if (M <= kGemvDispatchMaxM && w4a16::gemv_fits(M, Nl, n, K, G))
+        return from_cuda(w4a16::launch_gemv(x, mats, n, M, 0, K, G, cs));
+    return from_cuda(w4a16::launch_gemm(x, mats, n, M, 0, K, G, cs));
+}
+
 // The activation-scale vector of the *_act_scaled entry points: present and 16-byte aligned.
 w4a16_status check_act_scale(const float* x_scale) {
     if (!x_scale) return W4A16_ERR_INVALID_ARG;
@@ -186,11 +215,91 @@ int64_t w4a16_qweight_ld(int64_t K) { return w4a16::qweight_ld(K); }
 int64_t w4a16_scales_ld(int64_t K, int G) { return G > 0 ? w4a16::scales_ld(K, G) : 0; }
 int64_t w4a16_zeros_ld(int64_t K, int G) { return G > 0 ? w4a16::zeros_ld(K, G) : 0; }
 
-int64_t w8a16_qweight_ld(int64_t K) { return w4a16::qweight_ld(2 * K); }
-int64_t w8a16_scales_ld(int64_t K, int G) { return G > 0 ? w4a16::scales_ld(2 * K, G) : 0; }
-int64_t w8a16_zeros_ld(int64_t K, int G) { return G > 0 ? w4a16::zeros_ld(2 * K, G) : 0; }
+int64_t w8a16_qweight_ld(int64_t K) { return K / 4; }
+int64_t w8a16_scales_ld(int64_t K, int G) { return G > 0 ? w4a16::scales_ld(K, G) : 0; }
+int64_t w8a16_zeros_ld(int64_t K, int G) { return G > 0 ? w4a16::zeros8_ld(K, G) : 0; }
 
 w4a16_status w8a16_pack(const void* w_f16, int64_t N, int64_t K, int G, uint32_t* qweight, void* scales_f16,
+                        uint32_t* zeros, w4a16_stream_t stream) {
+    w4a16_status st = check_weight_shape(N, K, G);
+    if (st != W4A16_OK) return st;
+    if (N == 0) return W4A16_OK;
+    if ((st = check_weights(qweight, scales_f16, zeros)) != W4A16_OK) return st;
+    if (!w_f16) return W4A16_ERR_INVALID_ARG;
+    if (!aligned16(w_f16)) return W4A16_ERR_MISALIGNED;
+    return from_cuda(w4a16::launch_pack8w(w_f16, N, K, G, qweight, scales_f16, zeros,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w8a16_dequant(const uint32_t* qweight, const void* scales_f16, const uint32_t* zeros, int64_t N,
+                           int64_t K, int G, float* w_out, w4a16_stream_t stream) {
+    w4a16_status st = check_weight_shape(N, K, G);
+    if (st != W4A16_OK) return st;
+    if (N == 0) return W4A16_OK;
+    if ((st = check_weights(qweight, scales_f16, zeros)) != W4A16_OK) return st;
+    if (!w_out) return W4A16_ERR_INVALID_ARG;
+    if (!aligned16(w_out)) return W4A16_ERR_MISALIGNED;
+    return from_cuda(w4a16::launch_dequant8w(qweight, scales_f16, zeros, N, K, G, w_out,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w8a16_dequant_f16(const uint32_t* qweight, const void* scales_f16, const uint32_t* zeros, int64_t N,
+                               int64_t K, int G, void* w_out_f16, w4a16_stream_t stream) {
+    w4a16_status st = check_weight_shape(N, K, G);
+    if (st != W4A16_OK) return st;
+    if (N == 0) return W4A16_OK;
+    if ((st = check_weights(qweight, scales_f16, zeros)) != W4A16_OK) return st;
+    if (!w_out_f16) return W4A16_ERR_INVALID_ARG;
+    if (!aligned16(w_out_f16)) return W4A16_ERR_MISALIGNED;
+    return from_cuda(w4a16::launch_dequant8w_f16(qweight, scales_f16, zeros, N, K, G, w_out_f16,
+                                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+// path: 0 = automatic (the decode kernel for M <= 8 and G <= 128 where it fits, else the
+// tensor-core kernel), 1 = decode kernel, 2 = tensor-core kernel.
+static w4a16_status w8_common(const void* x, const uint32_t* q, const void* s, const uint32_t* z, int64_t M,
+                              int64_t N, int64_t K, int G, void* y, w4a16_stream_t stream, int path) {
+    w4a16_status st = check_weight_shape(N, K, G);
+    if (st != W4A16_OK) return st;
+    if (M < 0 || M > kMaxDim) return W4A16_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return W4A16_OK;
+    if ((st = check_weights(q, s, z)) != W4A16_OK) return st;
+    if (!x || !y) return W4A16_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(y)) return W4A16_ERR_MISALIGNED;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    GemvMat mat{q, s, z, y};
+    const int64_t Ns[1] = {N};
+    const bool gemv_ok = M <= 8 && G <= 128 && w4a16::gemv_fits(M, Ns, 1, K, G, false, true);
+    if (path == 0) path = M <= kGemvDispatchMaxM && gemv_ok ? 1 : 2;
+    if (path == 1) {
+        if (!gemv_ok) return W4A16_ERR_UNSUPPORTED;
+        return from_cuda(w4a16::launch_gemv(x, &mat, 1, M, N, K, G, cs, nullptr, 0, false, false, true));
+    }
+    return from_cuda(w4a16::launch_gemm(x, &mat, 1, M, N, K, G, cs, nullptr, 0, false, true));
+}
+
+w4a16_status w8a16_linear(const void* x_bf16, const uint32_t* qweight, const void* scales_f16, const uint32_t* zeros,
+                          int64_t M, int64_t N, int64_t K, int G, void* y_bf16, w4a16_stream_t stream) {
+    return w8_common(x_bf16, qweight, scales_f16, zeros, M, N, K, G, y_bf16, stream, 0);
+}
+
+w4a16_status w8a16_linear_gemv(const void* x_bf16, const uint32_t* qweight, const void* scales_f16,
+                               const uint32_t* zeros, int64_t M, int64_t N, int64_t K, int G, void* y_bf16,
+                               w4a16_stream_t stream) {
+    return w8_common(x_bf16, qweight, scales_f16, zeros, M, N, K, G, y_bf16, stream, 1);
+}
+
+w4a16_status w8a16_linear_gemm(const void* x_bf16, const uint32_t* qweight, const void* scales_f16,
+                               const uint32_t* zeros, int64_t M, int64_t N, int64_t K, int G, void* y_bf16,
+                               w4a16_stream_t stream) {
+    return w8_common(x_bf16, qweight, scales_f16, zeros, M, N, K, G, y_bf16, stream, 2);
+}
+
+int64_t w8a16_planes_qweight_ld(int64_t K) { return w4a16::qweight_ld(2 * K); }
+int64_t w8a16_planes_scales_ld(int64_t K, int G) { return G > 0 ? w4a16::scales_ld(2 * K, G) : 0; }
+int64_t w8a16_planes_zeros_ld(int64_t K, int G) { return G > 0 ? w4a16::zeros_ld(2 * K, G) : 0; }
+
+w4a16_status w8a16_planes_pack(const void* w_f16, int64_t N, int64_t K, int G, uint32_t* qweight, void* scales_f16,
                         uint32_t* zeros, w4a16_stream_t stream) {
     w4a16_status st = check_weight_shape(N, K, G);
     if (st != W4A16_OK) return st;
@@ -203,7 +312,7 @@ w4a16_status w8a16_pack(const void* w_f16, int64_t N, int64_t K, int G, uint32_t
                                          reinterpret_cast<cudaStream_t>(stream)));
 }
 
-w4a16_status w8a16_linear(const void* x_bf16, const uint32_t* qweight, const void* scales_f16,
+w4a16_status w8a16_planes_linear(const void* x_bf16, const uint32_t* qweight, const void* scales_f16,
                           const uint32_t* zeros, int64_t M, int64_t N, int64_t K, int G, void* y_bf16,
                           w4a16_stream_t stream) {
     w4a16_status st = check_weight_shape(N, K, G);
@@ -299,6 +408,12 @@ w4a16_status w4a16_linear_dual(const void* x_bf16, const uint32_t* qweight_gate,
                                void* y_gate_bf16, void* y_up_bf16, w4a16_stream_t stream) {
     return dual_common(x_bf16, qweight_gate, scales_gate, zeros_gate, qweight_up, scales_up, zeros_up, M, N, K, G,
                        y_gate_bf16, y_up_bf16, stream, nullptr);
+}
+
+w4a16_status w4a16_linear_multi(const void* x_bf16, int nmat, const uint32_t* const* qweight,
+                                const void* const* scales_f16, const uint32_t* const* zeros, const int64_t* N,
+                                int64_t M, int64_t K, int G, void* const* y_bf16, w4a16_stream_t stream) {
+    return multi_common(x_bf16, nmat, qweight, scales_f16, zeros, N, M, K, G, y_bf16, stream);
 }
 
 w4a16_status w4a16_linear_act_scaled(const void* x_bf16, const float* x_scale, const uint32_t* qweight,

@@ -17,6 +17,9 @@ namespace w4a16 {
 __host__ __device__ inline int64_t qweight_ld(int64_t K) { return K / 8; }
 __host__ __device__ inline int64_t scales_ld(int64_t K, int G) { return ((K / G) + 7) / 8 * 8; }
 __host__ __device__ inline int64_t zeros_ld(int64_t K, int G) { return (((K / G) + 7) / 8 + 3) / 4 * 4; }
+// 8-bit word layout: uint32 words per zeros row, four 8-bit zero points per word,
+// rounded up to 16 bytes.
+__host__ __device__ inline int64_t zeros8_ld(int64_t K, int G) { return (((K / G) + 3) / 4 + 3) / 4 * 4; }
 
 // (a & b) | c in one LOP3.
 __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {

@@ -76,7 +76,14 @@ __host__ __device__ constexpr int cta_warps(int NB, int G) { return NB == 1 && G
 constexpr int kBoxBytes = 2048;           // one TMA box: 16 virtual rows x 128 bytes (256 codes)
 constexpr int kUnitBytes = 2 * kBoxBytes;  // a ring slot: a unit of up to two consecutive chunks of a tile
 constexpr int kSlots = 4;                 // partial-sum slots per output (warps sharing a tile)
+// Weight formats the decode kernel reads.  kFmt8: 8-bit codes four per word
+// with 8-bit zero points; the kernel runs them as a 4-bit layer of 2K virtual
+// channels and groups of 2G (each 8-bit code is two nibbles), expanding both
+// nibbles against the exponent of 1024 and staging every x value twice (see
+// expand_codes8_f16), so the MMA sums x (2048 + b) exactly.
+constexpr int kFmt4 = 0, kFmtQ4K = 1, kFmt8 = 2;
 constexpr uint32_t kStatusGemv = 1u << 8;
+constexpr int64_t kPrefetchBytesPerCta = 512 * 1024;   // L2 prefetch at entry up to this many weight bytes per CTA
 constexpr uint32_t kStatusGemvDrain = 1u << 9;
 
 // MMA row i (< 8) of a warp reads virtual row sigma(i) = i/2 + 4*(i%2) of the
@@ -89,17 +96,23 @@ struct GemvParams {
     const __nv_bfloat16* x;                // [M, K]
     const float* xsc;                      // per-input-channel multiplier of x [K], or null
     int kx;                                // row length of x: channel k reads x[k mod kx] (kx = K or K/2)
-    const unsigned short* s[2];            // FP16 scales [N, lds] (KQ: super-block records, 8 halves each)
-    const uint32_t* z[2];                  // zeros [N, ldz] (KQ: unused, ldz = 0)
-    void* y[2];                            // [M, N], BF16 (or FP32 when yf32)
+    // per matrix (up to kMaxMat sharing x): FP16 scales [n, lds] (KQ: super-block records, 8
+    // halves each), zeros [n, ldz] (KQ: unused, ldz = 0), output [M, n] BF16 (or FP32 when yf32)
+    const uint32_t* q[kMaxMat];            // packed codes (read through the tensor maps; used for L2 prefetch)
+    const unsigned short* s[kMaxMat];
+    const uint32_t* z[kMaxMat];
+    void* y[kMaxMat];
+    int prefetch;                          // 1: ask L2 for this CTA's weights before the grid dependency wait
+    int n[kMaxMat];                        // rows (outputs) of each matrix
+    int tstart[kMaxMat + 1];               // first tile of each matrix; total_tiles from nmat on
     int yf32;                              // 1: FP32 outputs (no BF16 rounding)
-    int M, N, K, G;
+    int M, K, G;
     int P, R, cols, xcols;                 // segments, weight rows per tile, B columns used (P*H*M),
                                            // staged x columns (P*M)
     int Ks, C, ngs, ng;                    // codes per segment padded to whole chunks (C of 256), groups
                                            // per padded segment, groups per row
     int lds, ldz;
-    int tiles_per_mat, total_tiles;
+    int total_tiles;
     int nw;                                // warps in the CTA
     int warps;                             // warps that take units (<= nw)
     int nst;                               // unit slots per warp ring (power of two)
@@ -186,6 +199,14 @@ __device__ __forceinline__ float4 lds_f4(uint32_t addr) {
     return v;
 }
 
+// Matrix that tile tau belongs to (tiles are numbered matrix after matrix).
+__device__ __forceinline__ int mat_of(const GemvParams& p, int tau) {
+    int m = 0;
+#pragma unroll
+    for (int i = 1; i < kMaxMat; ++i) m += tau >= p.tstart[i];
+    return m;
+}
+
 // Bounded wait on a barrier phase (gives up after `limit` cycles); the thread
 // sleeps between polls.
 __device__ __forceinline__ bool gemv_wait(uint32_t bar, uint32_t parity, long long limit) {
@@ -203,9 +224,10 @@ __device__ __forceinline__ bool gemv_wait(uint32_t bar, uint32_t parity, long lo
 // M1: one activation row with P >= 2 segments.  The B columns are then
 // (parity, segment) pairs and each lane holds at most one useful D value per
 // row, so the block-end correction is done once per row on that value only.
-template <int NB, int G, int H, bool M1, int PT, bool KQ>
+template <int NB, int G, int H, bool M1, int PT, int FMT>
 __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
     gemv_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
+                const __grid_constant__ CUtensorMap tm2, const __grid_constant__ CUtensorMap tm3,
                 const GemvParams p) {
     constexpr int V = G >= 128 ? 4 : G / 32;      // words per lane per code load
     constexpr int GPC = 256 / G;                  // groups per chunk (H divides it)
@@ -215,6 +237,8 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
     const int R = 16 / P;                         // weight rows per tile
     const int kThreads = kWarps * 32;
     static_assert(GPC % H == 0, "a block of H groups lies inside one chunk");
+    constexpr bool KQ = FMT == kFmtQ4K;          // super-block records in place of scales and zeros
+    constexpr bool W8 = FMT == kFmt8;            // 8-bit codes, four per word (a virtual 4-bit layer of 2K)
     static_assert(!KQ || G == 32, "a super-block is one chunk of 8 sub-blocks of 32");
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base; derived by pointer arithmetic on the shared array so
@@ -250,14 +274,15 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
     const bool withhold = p.withhold && blockIdx.x == 0 && warp == 0;
     auto issue_next = [&]() {
         const int tau = tile0 + it_tl;
-        const int mat = tau >= p.tiles_per_mat;
-        const int tile = mat ? tau - p.tiles_per_mat : tau;
+        const int mat = mat_of(p, tau);
+        const int tile = tau - p.tstart[mat];
         const uint32_t slot = (uint32_t)(it_n & (nsl - 1));
         const uint32_t bar = bar0 + 8u * slot;
         const bool two = it_c + 1 < p.C && it_ch + 1 < ch1;
         if (!(withhold && it_n == 0)) {
             tc::mbar_arrive_expect_tx(bar, (uint32_t)(two ? 2 * kBoxBytes : kBoxBytes));
-            const void* tm = mat ? (const void*)&tm1 : (const void*)&tm0;
+            const void* tm = mat == 0 ? (const void*)&tm0 : mat == 1 ? (const void*)&tm1
+                           : mat == 2 ? (const void*)&tm2 : (const void*)&tm3;
             tc::tma_load_2d(ring + slot * (uint32_t)kUnitBytes, tm, it_c * 32, tile * 16, bar);
             if (two)
                 tc::tma_load_2d(ring + slot * (uint32_t)kUnitBytes + kBoxBytes, tm, (it_c + 1) * 32, tile * 16, bar);
@@ -282,6 +307,25 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
     // scheduled at once (its CTAs take SMs as this grid's CTAs exit), and this grid reads no
     // global memory before the previous grid on the stream has completed.
     tc::griddep_launch_dependents();
+    if (p.prefetch && tid == 0) {
+        // A layer this small is dominated by latency: ask L2 for the CTA's codes and metadata
+        // rows now, while the previous grid may still be running.  A prefetch returns nothing to
+        // the program and L2 is the point of coherence, so this reads nothing before the grid
+        // dependency wait below; the copies after it find the data in L2.
+#pragma unroll 1
+        for (int i = 0; i < kMaxMat; ++i) {
+            const int a = max(tile0, p.tstart[i]), b = min(tile1, p.tstart[i + 1]);
+            if (b <= a) continue;
+            const int64_t r0 = (int64_t)(a - p.tstart[i]) * R;
+            const int64_t rows = min((int64_t)(b - a) * R, (int64_t)p.n[i] - r0);
+            if (rows <= 0) continue;
+            const uint8_t* cq = reinterpret_cast<const uint8_t*>(p.q[i]) + r0 * (p.K / 2);
+            for (int64_t off = 0, tot = rows * (p.K / 2); off < tot; off += 1 << 16)
+                tc::prefetch_l2(cq + off, (uint32_t)(tot - off < (1 << 16) ? tot - off : (1 << 16)));
+            tc::prefetch_l2(p.s[i] + r0 * p.lds, (uint32_t)(rows * p.lds * 2));
+            if (!KQ) tc::prefetch_l2(p.z[i] + r0 * p.ldz, (uint32_t)(rows * p.ldz * 4));
+        }
+    }
     const uint32_t pbar = sbase + L.bars + 8u * (uint32_t)(kWarps * nsl);
     bool pro_ok = true;                           // the prologue's copies landed (warp-uniform)
     if (tid == 0) {
@@ -292,28 +336,35 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
     tc::griddep_wait();
     __syncthreads();
     {
-        // local rows: matrix 0 part at [0, n0), matrix 1 part at [l1, l1 + n1); rows at or past N
-        // and the gap between the parts are not copied but zero-filled
-        const int tpm = p.tiles_per_mat;
-        const bool has0 = tile0 < tpm;
-        const int r0 = has0 ? tile0 * R : 0;                                  // first row, matrix 0 part
-        const int n0 = !has0 ? 0 : tile1 <= tpm ? tc_ * R : (tpm - tile0) * R;
-        const int l1 = has0 ? (tpm - tile0) * R : 0;                        // local row of matrix 1
-        const int t1a = has0 ? tpm : tile0;
-        const int r1 = (t1a - tpm) * R;                                      // first row, matrix 1 part
-        const int n1 = tile1 > tpm ? (tile1 - t1a) * R : 0;
-        const int c0 = max(0, min(n0, p.N - r0)), c1 = max(0, min(n1, p.N - r1));   // rows copied
+        // local rows follow the CTA's tiles: the part of matrix i is the tiles [a_i, b_i) of the
+        // CTA's range, local rows [(a_i - tile0) R, (b_i - tile0) R); its rows below the matrix's
+        // n are bulk-copied (they are contiguous in the matrix), the rest zero-filled below
         const uint32_t sbytes = (uint32_t)p.lds * 2u, zbytes = (uint32_t)p.ldz * 4u;   // per row
         const uint32_t ms = sbase + L.ms, mz = sbase + L.mz;
+        int cl[kMaxMat], cc[kMaxMat];                  // local first row and rows copied, per matrix
+        int gs[kMaxMat + 1], gn[kMaxMat + 1];          // rows left to zero-fill: first, count
+        int copied = 0, gaps = 0;
+#pragma unroll
+        for (int i = 0; i < kMaxMat; ++i) {
+            const int a = max(tile0, p.tstart[i]), b = min(tile1, p.tstart[i + 1]);
+            cl[i] = (a - tile0) * R;
+            cc[i] = b > a ? max(0, min((b - a) * R, p.n[i] - (a - p.tstart[i]) * R)) : 0;
+            gs[i] = cl[i] + cc[i];
+            gn[i] = b > a ? (b - a) * R - cc[i] : 0;      // rows of the part past the matrix's n
+            copied += cc[i];
+            gaps += gn[i];
+        }
+        gs[kMaxMat] = tc_ * R;                           // rows past the CTA's tiles
+        gn[kMaxMat] = p.rows_cap - tc_ * R;
+        gaps += gn[kMaxMat];
         if (tid == 0) {
-            tc::mbar_arrive_expect_tx(pbar, (uint32_t)(c0 + c1) * (sbytes + zbytes));
-            if (c0 > 0) {
-                tc::bulk_load(ms, p.s[0] + (int64_t)r0 * p.lds, (uint32_t)c0 * sbytes, pbar);
-                if (!KQ) tc::bulk_load(mz, p.z[0] + (int64_t)r0 * p.ldz, (uint32_t)c0 * zbytes, pbar);
-            }
-            if (c1 > 0) {
-                tc::bulk_load(ms + (uint32_t)l1 * sbytes, p.s[1] + (int64_t)r1 * p.lds, (uint32_t)c1 * sbytes, pbar);
-                if (!KQ) tc::bulk_load(mz + (uint32_t)l1 * zbytes, p.z[1] + (int64_t)r1 * p.ldz, (uint32_t)c1 * zbytes, pbar);
+            tc::mbar_arrive_expect_tx(pbar, (uint32_t)copied * (sbytes + zbytes));
+#pragma unroll
+            for (int i = 0; i < kMaxMat; ++i) {
+                if (cc[i] <= 0) continue;
+                const int64_t r0 = (int64_t)(max(tile0, p.tstart[i]) - p.tstart[i]) * R;    // first row
+                tc::bulk_load(ms + (uint32_t)cl[i] * sbytes, p.s[i] + r0 * p.lds, (uint32_t)cc[i] * sbytes, pbar);
+                if (!KQ) tc::bulk_load(mz + (uint32_t)cl[i] * zbytes, p.z[i] + r0 * p.ldz, (uint32_t)cc[i] * zbytes, pbar);
             }
         }
 
@@ -352,8 +403,13 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
                 const int wseg = bc[j] * 32 + lane;
                 if (bxc[j] < xcols && wseg * 8 < kseg) {
                     int kk = pseg * kseg + wseg * 8;       // channel of the layer (< 2 kx)
-                    kk -= kk >= p.kx ? p.kx : 0;
-                    vv[j] = *reinterpret_cast<const uint4*>(p.x + (int64_t)m * p.kx + kk);
+                    if constexpr (W8) {                    // the word's four real channels
+                        const uint2 h = *reinterpret_cast<const uint2*>(p.x + (int64_t)m * p.kx + kk / 2);
+                        vv[j] = make_uint4(h.x, h.y, 0u, 0u);
+                    } else {
+                        kk -= kk >= p.kx ? p.kx : 0;
+                        vv[j] = *reinterpret_cast<const uint4*>(p.x + (int64_t)m * p.kx + kk);
+                    }
                 }
             }
         };
@@ -370,10 +426,18 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
                 // FP16-rounded values as floats for the sums
                 const uint32_t in[4] = {vv[j].x, vv[j].y, vv[j].z, vv[j].w};
                 float f[8];
+                if constexpr (W8) {
+                    // pairs (x0, x2), (x0, x2), (x1, x3), (x1, x3): both nibbles of a code meet its x
+                    f[0] = f[1] = bf16lo_to_f32(in[0]);
+                    f[2] = f[3] = bf16hi_to_f32(in[0]);
+                    f[4] = f[5] = bf16lo_to_f32(in[1]);
+                    f[6] = f[7] = bf16hi_to_f32(in[1]);
+                } else {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    f[2 * q] = bf16lo_to_f32(in[q]);
-                    f[2 * q + 1] = bf16hi_to_f32(in[q]);
+                    for (int q = 0; q < 4; ++q) {
+                        f[2 * q] = bf16lo_to_f32(in[q]);
+                        f[2 * q + 1] = bf16hi_to_f32(in[q]);
+                    }
                 }
                 if (p.xsc != nullptr && wseg * 8 < kseg) {  // activation scale: x_k * xsc_k in FP32
                     int kk = pseg * kseg + wseg * 8;
@@ -390,10 +454,11 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
                     f[q] = __low2float(hp[q]);
                     f[q + 4] = __high2float(hp[q]);
                 }
-                // 1024 * (x0 + x2 + x4 + x6) + 64 * (x1 + x3 + x5 + x7), and sum x
+                // 1024 * (x0 + x2 + x4 + x6) + 64 * (x1 + x3 + x5 + x7), and sum x (8-bit: both
+                // halves carry 1024 and every x appears twice, so 2048 * sum x and sum x)
                 const float se = (f[0] + f[2]) + (f[4] + f[6]), so = (f[1] + f[3]) + (f[5] + f[7]);
-                float e = fmaf(1024.0f, se, 64.0f * so);
-                float xsum = se + so;
+                float e = W8 ? 2048.0f * se : fmaf(1024.0f, se, 64.0f * so);
+                float xsum = W8 ? se : se + so;
 #pragma unroll
                 for (int off = 1; off < GW; off <<= 1) {
                     e += __shfl_xor_sync(0xFFFFFFFFu, e, off);
@@ -415,12 +480,15 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
         // zero fills: table rows not copied, E/X columns no (segment, parity, row) uses, the
         // zero block, the partial sums
         {
-            const int zr0 = c0, zr1 = min(has0 ? l1 : 0, p.rows_cap), zr2 = (has0 ? l1 : 0) + c1;
             const int sv = p.lds / 8, per = sv + p.ldz / 4;                       // uint4 per row
-            const int nz = (zr1 > zr0 ? zr1 - zr0 : 0) + (p.rows_cap > zr2 ? p.rows_cap - zr2 : 0);
-            for (int i = tid; i < nz * per; i += kThreads) {
-                const int k = i / per, col = i - k * per;
-                const int lr = zr0 + k < zr1 ? zr0 + k : zr2 + (k - (zr1 > zr0 ? zr1 - zr0 : 0));
+            for (int i = tid; i < gaps * per; i += kThreads) {
+                int k = i / per, lr = 0;
+                const int col = i - k * per;
+#pragma unroll
+                for (int j = 0; j <= kMaxMat; ++j) {       // the k-th row of the gap ranges
+                    if (k >= 0 && k < gn[j]) lr = gs[j] + k;
+                    k -= gn[j];
+                }
                 const uint32_t dst = col < sv ? ms + (uint32_t)lr * sbytes + (uint32_t)col * 16u
                                               : mz + (uint32_t)lr * zbytes + (uint32_t)(col - sv) * 16u;
                 asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(0u), "r"(0u), "r"(0u), "r"(0u)
@@ -552,7 +620,10 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
                   const unsigned short* sra1 = sra + h_use;
                   const unsigned short* srb1 = srb + h_use;
                   uint32_t zwa1 = 0u, zwb1 = 0u;
-                  if constexpr (M1 && !KQ) {
+                  if constexpr (M1 && W8) {                   // 8-bit zero points, four per word
+                      zwa1 = zra[gia >> 2] >> (8 * ((gia & 3) + h_use));
+                      zwb1 = zrb[gib >> 2] >> (8 * ((gib & 3) + h_use));
+                  } else if constexpr (M1 && !KQ) {
                       zwa1 = zra[gia >> 3] >> (4 * ((gia & 7) + h_use));
                       zwb1 = zrb[gib >> 3] >> (4 * ((gib & 7) + h_use));
                   }
@@ -611,8 +682,13 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
                           const int jg = ws / WSG;                     // group in the chunk
                           const int hcur = jg % H;                     // its parity (c * GPC is a multiple of H)
                           uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-                          expand_codes_f16(wa[i], a0, a1, a2, a3);
-                          expand_codes_f16(wb[i], b0, b1, b2, b3);
+                          if constexpr (W8) {
+                              expand_codes8_f16(wa[i], a0, a1, a2, a3);
+                              expand_codes8_f16(wb[i], b0, b1, b2, b3);
+                          } else {
+                              expand_codes_f16(wa[i], a0, a1, a2, a3);
+                              expand_codes_f16(wb[i], b0, b1, b2, b3);
+                          }
 #pragma unroll
                           for (int nb = 0; nb < NB; ++nb) {
                               const uint4 xv = lds128(xb[nb][hcur] + (uint32_t)ws * xsp[nb][hcur]);
@@ -644,7 +720,8 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
                                   } else {
                                       const float s_a = __half2float(__ushort_as_half(sra1[jg0]));
                                       const float s_b = __half2float(__ushort_as_half(srb1[jg0]));
-                                      const float z_a = meta_zero(zwa1, jg0), z_b = meta_zero(zwb1, jg0);
+                                      const float z_a = W8 ? meta_zero8(zwa1, jg0) : meta_zero(zwa1, jg0);
+                                      const float z_b = W8 ? meta_zero8(zwb1, jg0) : meta_zero(zwb1, jg0);
                                       acc_a = fmaf(s_a, va_ - fmaf(z_a, ex.y, ex.x), acc_a);
                                       acc_b = fmaf(s_b, vb_ - fmaf(z_b, ex.y, ex.x), acc_b);
                                   }
@@ -664,15 +741,17 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
                                           zb[hh] = kmb * kq_code(krb.z, krb.w, jg0 + hh, 16);
                                       }
                                   } else {
-                                      const uint32_t zwa = zra[(gia + jg0) >> 3] >> (4 * ((gia + jg0) & 7));
-                                      const uint32_t zwb = zrb[(gib + jg0) >> 3] >> (4 * ((gib + jg0) & 7));
+                                      const uint32_t zwa = W8 ? zra[(gia + jg0) >> 2] >> (8 * ((gia + jg0) & 3))
+                                                              : zra[(gia + jg0) >> 3] >> (4 * ((gia + jg0) & 7));
+                                      const uint32_t zwb = W8 ? zrb[(gib + jg0) >> 2] >> (8 * ((gib + jg0) & 3))
+                                                              : zrb[(gib + jg0) >> 3] >> (4 * ((gib + jg0) & 7));
 #pragma unroll
                                       for (int hh = 0; hh < H; ++hh) {
                                           const bool va_ = gia + jg0 + hh < p.ng, vb_ = gib + jg0 + hh < p.ng;
                                           sa[hh] = va_ ? __half2float(__ushort_as_half(sra[jg0 + hh])) : 0.0f;
                                           sb[hh] = vb_ ? __half2float(__ushort_as_half(srb[jg0 + hh])) : 0.0f;
-                                          za[hh] = meta_zero(zwa, hh);
-                                          zb[hh] = meta_zero(zwb, hh);
+                                          za[hh] = W8 ? meta_zero8(zwa, hh) : meta_zero(zwa, hh);
+                                          zb[hh] = W8 ? meta_zero8(zwb, hh) : meta_zero(zwb, hh);
                                       }
                                   }
 #pragma unroll
@@ -796,16 +875,16 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
             const int rl = i / p.M, m = i - rl * p.M;
             const int tl2 = rl / R, rho = rl - tl2 * R;
             const int tau = tile0 + tl2;
-            const int mat = tau >= p.tiles_per_mat;
-            const int row = (mat ? tau - p.tiles_per_mat : tau) * R + rho;
-            if (row >= p.N) continue;
+            const int mat = mat_of(p, tau);
+            const int row = (tau - p.tstart[mat]) * R + rho;
+            if (row >= p.n[mat]) continue;
             float sum = 0.0f;
 #pragma unroll
             for (int q = 0; q < kSlots; ++q) sum += part[i * kSlots + q];
             if (p.yf32)
-                static_cast<float*>(mat ? p.y[1] : p.y[0])[(int64_t)m * p.N + row] = sum;
+                static_cast<float*>(p.y[mat])[(int64_t)m * p.n[mat] + row] = sum;
             else
-                static_cast<__nv_bfloat16*>(mat ? p.y[1] : p.y[0])[(int64_t)m * p.N + row] = __float2bfloat16_rn(sum);
+                static_cast<__nv_bfloat16*>(p.y[mat])[(int64_t)m * p.n[mat] + row] = __float2bfloat16_rn(sum);
         }
     }
 }
@@ -849,16 +928,21 @@ struct Plan {
     size_t smem;
 };
 
+// nmat matrices of Ns[i] rows sharing x (tiles numbered matrix after matrix).
 // kq: the super-block layout (G = 32, K a multiple of 256, M <= 8): one 16-byte
 // record per 256 codes in place of the scale row, no zero row.
-bool make_plan(int64_t M, int64_t N, int64_t K, int G, int nmat, int sms, size_t smem_cap, Plan& pl,
-               bool kq = false) {
-    if (M < 1 || M > 16 || N < 1 || K < 32 || K % 32 || K % G) return false;
+// w8: the 8-bit word layout, planned as the 4-bit layer of K' = 2K channels and
+// groups of G' = 2G it is run as (so K and G here are K' and G'; M <= 8, G' <= 256).
+bool make_plan(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G, int sms, size_t smem_cap, Plan& pl,
+               bool kq = false, bool w8 = false) {
+    if (M < 1 || M > 16 || nmat < 1 || nmat > kMaxMat || K < 32 || K % 32 || K % G) return false;
     if (kq && (G != 32 || K % 256 || M > 8)) return false;
-    if (N > (int64_t)1 << 24 || K > (int64_t)1 << 20) return false;   // keeps tile/unit indices small
+    if (w8 && (kq || M > 8 || G < 64 || G > 256 || K % 64)) return false;
+    if (K > (int64_t)1 << 20) return false;                          // keeps tile/unit indices small
+    for (int i = 0; i < nmat; ++i)
+        if (Ns[i] < 1 || Ns[i] > (int64_t)1 << 24) return false;
     GemvParams& p = pl.p;
     p.M = (int)M;
-    p.N = (int)N;
     p.K = (int)K;
     p.G = G;
     choose_segments(M, K, G, p.P, pl.H);
@@ -871,9 +955,17 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int G, int nmat, int sms, size_t
     p.ng = (int)(K / G);
     p.ngs = p.Ks / G;
     p.lds = kq ? (int)(K / 256 * 8) : (int)scales_ld(K, G);
-    p.ldz = kq ? 0 : (int)zeros_ld(K, G);
-    p.tiles_per_mat = (int)((N + p.R - 1) / p.R);
-    p.total_tiles = p.tiles_per_mat * nmat;
+    p.ldz = kq ? 0 : w8 ? (int)zeros8_ld(K / 2, G / 2) : (int)zeros_ld(K, G);
+    int64_t t = 0;
+    for (int i = 0; i < kMaxMat; ++i) {
+        p.tstart[i] = (int)t;
+        p.n[i] = i < nmat ? (int)Ns[i] : 0;
+        if (i < nmat) t += (Ns[i] + p.R - 1) / p.R;
+    }
+    if (t > (int64_t)1 << 26) return false;
+    p.tstart[kMaxMat] = (int)t;
+    for (int i = nmat; i < kMaxMat; ++i) p.tstart[i] = (int)t;
+    p.total_tiles = (int)t;
     pl.grid = p.total_tiles < sms ? p.total_tiles : sms;
     const int tmin = p.total_tiles / pl.grid, tmax = (p.total_tiles + pl.grid - 1) / pl.grid;
     if ((long long)tmax * p.C >= (1ll << 26)) return false;
@@ -904,14 +996,14 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int G, int nmat, int sms, size_t
     return false;
 }
 
-template <int NB, int G, int H, bool M1, int PT, bool KQ>
-cudaError_t launch_m(const CUtensorMap& tm0, const CUtensorMap& tm1, const Plan& pl, int dev, cudaStream_t stream) {
+template <int NB, int G, int H, bool M1, int PT, int FMT>
+cudaError_t launch_m(const CUtensorMap* tm, const Plan& pl, int dev, cudaStream_t stream) {
     // largest dynamic shared memory this instance is already allowed per device (a raise may
     // race with another thread's: both set the attribute, the larger value stays)
     static std::atomic<int> cached[kMaxDevices];
     int have = cached[dev].load(std::memory_order_relaxed);
     if ((int)pl.smem > have) {
-        const cudaError_t e = cudaFuncSetAttribute(gemv_kernel<NB, G, H, M1, PT, KQ>,
+        const cudaError_t e = cudaFuncSetAttribute(gemv_kernel<NB, G, H, M1, PT, FMT>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
         if (e != cudaSuccess) return e;
         while (have < (int)pl.smem && !cached[dev].compare_exchange_weak(have, (int)pl.smem)) {
@@ -928,36 +1020,36 @@ cudaError_t launch_m(const CUtensorMap& tm0, const CUtensorMap& tm1, const Plan&
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<NB, G, H, M1, PT, KQ>, tm0, tm1, pl.p);
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<NB, G, H, M1, PT, FMT>, tm[0], tm[1], tm[2], tm[3], pl.p);
 }
 
-template <int NB, int G, int H, bool KQ>
-cudaError_t launch_t(const CUtensorMap& tm0, const CUtensorMap& tm1, const Plan& pl, int dev, cudaStream_t stream) {
+template <int NB, int G, int H, int FMT>
+cudaError_t launch_t(const CUtensorMap* tm, const Plan& pl, int dev, cudaStream_t stream) {
     if constexpr (NB == 1) {
         if (m1_kernel(pl.p)) {                       // M = 1: the segment count is a template constant
             switch (pl.p.P) {
-                case 2: return launch_m<NB, G, H, true, 2, KQ>(tm0, tm1, pl, dev, stream);
-                case 4: return launch_m<NB, G, H, true, 4, KQ>(tm0, tm1, pl, dev, stream);
-                case 8: return launch_m<NB, G, H, true, 8, KQ>(tm0, tm1, pl, dev, stream);
+                case 2: return launch_m<NB, G, H, true, 2, FMT>(tm, pl, dev, stream);
+                case 4: return launch_m<NB, G, H, true, 4, FMT>(tm, pl, dev, stream);
+                case 8: return launch_m<NB, G, H, true, 8, FMT>(tm, pl, dev, stream);
             }
             return cudaErrorInvalidValue;
         }
     }
-    return launch_m<NB, G, H, false, 0, KQ>(tm0, tm1, pl, dev, stream);
+    return launch_m<NB, G, H, false, 0, FMT>(tm, pl, dev, stream);
 }
 
-template <int NB, int G, bool KQ = false>
-cudaError_t launch_h(const CUtensorMap& tm0, const CUtensorMap& tm1, const Plan& pl, int dev, cudaStream_t stream) {
+template <int NB, int G, int FMT = kFmt4>
+cudaError_t launch_h(const CUtensorMap* tm, const Plan& pl, int dev, cudaStream_t stream) {
     if constexpr (NB == 2) {
-        return launch_t<NB, G, 1, KQ>(tm0, tm1, pl, dev, stream);
+        return launch_t<NB, G, 1, FMT>(tm, pl, dev, stream);
     } else {
         switch (pl.H) {
-            case 1: return launch_t<NB, G, 1, KQ>(tm0, tm1, pl, dev, stream);
+            case 1: return launch_t<NB, G, 1, FMT>(tm, pl, dev, stream);
             case 2:
-                if constexpr (256 / G >= 2) return launch_t<NB, G, 2, KQ>(tm0, tm1, pl, dev, stream);
+                if constexpr (256 / G >= 2) return launch_t<NB, G, 2, FMT>(tm, pl, dev, stream);
                 break;
             case 4:
-                if constexpr (256 / G >= 4) return launch_t<NB, G, 4, KQ>(tm0, tm1, pl, dev, stream);
+                if constexpr (256 / G >= 4) return launch_t<NB, G, 4, FMT>(tm, pl, dev, stream);
                 break;
         }
         return cudaErrorInvalidValue;
@@ -965,12 +1057,22 @@ cudaError_t launch_h(const CUtensorMap& tm0, const CUtensorMap& tm1, const Plan&
 }
 
 template <int NB>
-cudaError_t launch_nb(const CUtensorMap& tm0, const CUtensorMap& tm1, const Plan& pl, int dev, cudaStream_t stream) {
+cudaError_t launch_nb(const CUtensorMap* tm, const Plan& pl, int dev, cudaStream_t stream) {
     switch (pl.p.G) {
-        case 32: return launch_h<NB, 32>(tm0, tm1, pl, dev, stream);
-        case 64: return launch_h<NB, 64>(tm0, tm1, pl, dev, stream);
-        case 128: return launch_h<NB, 128>(tm0, tm1, pl, dev, stream);
-        case 256: return launch_h<NB, 256>(tm0, tm1, pl, dev, stream);
+        case 32: return launch_h<NB, 32>(tm, pl, dev, stream);
+        case 64: return launch_h<NB, 64>(tm, pl, dev, stream);
+        case 128: return launch_h<NB, 128>(tm, pl, dev, stream);
+        case 256: return launch_h<NB, 256>(tm, pl, dev, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+// The 8-bit word layout (one column block; G' = 2G in {64, 128, 256}).
+cudaError_t launch_w8(const CUtensorMap* tm, const Plan& pl, int dev, cudaStream_t stream) {
+    switch (pl.p.G) {
+        case 64: return launch_h<1, 64, kFmt8>(tm, pl, dev, stream);
+        case 128: return launch_h<1, 128, kFmt8>(tm, pl, dev, stream);
+        case 256: return launch_h<1, 256, kFmt8>(tm, pl, dev, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -984,26 +1086,40 @@ cudaError_t gemv_take_status(uint32_t* word) {
     return cudaMemcpyToSymbol(g_gemv_status, &zero, sizeof(uint32_t));
 }
 
-bool gemv_fits(int64_t M, int64_t N, int64_t K, int G, int nmat, bool kq) {
+bool gemv_fits(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G, bool kq, bool w8) {
     Plan pl;
     DeviceInfo di;
     if (current_device(di) != cudaSuccess) {   // no device: the B300's figures
         di.sms = 148;
         di.smem_optin = 227 * 1024;
     }
-    return make_plan(M, N, K, G, nmat, di.sms, di.smem_optin, pl, kq);
+    return w8 ? make_plan(M, Ns, nmat, 2 * K, 2 * G, di.sms, di.smem_optin, pl, false, true)
+              : make_plan(M, Ns, nmat, K, G, di.sms, di.smem_optin, pl, kq);
+}
+
+bool gemv_fits(int64_t M, int64_t N, int64_t K, int G, int nmat, bool kq) {
+    const int64_t Ns[kMaxMat] = {N, N, N, N};
+    return gemv_fits(M, Ns, nmat, K, G, kq);
 }
 
 cudaError_t launch_gemv(const void* x, const GemvMat* mats, int nmat, int64_t M, int64_t N, int64_t K, int G,
-                        cudaStream_t stream, const float* xsc, int64_t kx, bool kq, bool yf32) {
+                        cudaStream_t stream, const float* xsc, int64_t kx, bool kq, bool yf32, bool w8) {
     if (kx == 0) kx = K;
     if (kx != K && (kx * 2 != K || kx % 8 != 0)) return cudaErrorInvalidValue;
     if (kq && (G != 32 || xsc != nullptr || kx != K)) return cudaErrorInvalidValue;
+    if (w8 && (kq || xsc != nullptr || kx != K)) return cudaErrorInvalidValue;
+    if (nmat < 1 || nmat > kMaxMat) return cudaErrorInvalidValue;
     DeviceInfo di;
     const cudaError_t e = current_device(di);
     if (e != cudaSuccess) return e;
+    int64_t Ns[kMaxMat];
+    for (int i = 0; i < nmat; ++i) Ns[i] = mats[i].n > 0 ? mats[i].n : N;
+    // the 8-bit word layout runs as a 4-bit layer of 2K channels and groups of 2G over the
+    // same words; x keeps its K channels
+    const int64_t Kv = w8 ? 2 * K : K;
+    const int Gv = w8 ? 2 * G : G;
     Plan pl;
-    if (!make_plan(M, N, K, G, nmat, di.sms, di.smem_optin, pl, kq)) return cudaErrorNotSupported;
+    if (!make_plan(M, Ns, nmat, Kv, Gv, di.sms, di.smem_optin, pl, kq, w8)) return cudaErrorNotSupported;
     GemvParams& p = pl.p;
     p.x = static_cast<const __nv_bfloat16*>(x);
     p.xsc = xsc;
@@ -1011,17 +1127,27 @@ cudaError_t launch_gemv(const void* x, const GemvMat* mats, int nmat, int64_t M,
     p.yf32 = yf32 ? 1 : 0;
     p.spin_limit = wait_limit();
     p.withhold = take_withhold(1) ? 1 : 0;
-    CUtensorMap tm[2];
-    for (int i = 0; i < 2; ++i) {
+    CUtensorMap tm[kMaxMat];
+    // small layers: the CTA's weights are requested into L2 before the grid dependency wait
+    // (below this many bytes per CTA the launch is latency-bound rather than bandwidth-bound)
+    int64_t wbytes = 0;
+    for (int i = 0; i < nmat; ++i) wbytes += Ns[i] * (Kv / 2);
+    p.prefetch = wbytes / pl.grid <= kPrefetchBytesPerCta ? 1 : 0;
+    for (int i = 0; i < kMaxMat; ++i) {
         const GemvMat& mt = mats[i < nmat ? i : 0];
+        p.q[i] = mt.q;
         p.s[i] = static_cast<const unsigned short*>(mt.s);
         p.z[i] = mt.z;
         p.y[i] = mt.y;
-        if (i < nmat && !make_code_map(&tm[i], mt.q, N, K, p.P, di.dev)) return cudaErrorInvalidValue;
+        if (i < nmat) {
+            if (!make_code_map(&tm[i], mt.q, Ns[i], Kv, p.P, di.dev)) return cudaErrorInvalidValue;
+        } else {
+            tm[i] = tm[0];
+        }
     }
-    if (nmat < 2) tm[1] = tm[0];
-    if (kq) return launch_h<1, 32, true>(tm[0], tm[1], pl, di.dev, stream);   // make_plan: M <= 8, one column block
-    return pl.nb == 1 ? launch_nb<1>(tm[0], tm[1], pl, di.dev, stream) : launch_nb<2>(tm[0], tm[1], pl, di.dev, stream);
+    if (kq) return launch_h<1, 32, kFmtQ4K>(tm, pl, di.dev, stream);   // make_plan: M <= 8, one column block
+    if (w8) return launch_w8(tm, pl, di.dev, stream);
+    return pl.nb == 1 ? launch_nb<1>(tm, pl, di.dev, stream) : launch_nb<2>(tm, pl, di.dev, stream);
 }
 
 }  // namespace w4a16

@@ -49,9 +49,11 @@ struct MapKey {
     uint32_t box_inner, box_outer;
     int dtype;
     int dev;
+    int swizzle;
     bool operator==(const MapKey& o) const {
         return base == o.base && inner == o.inner && outer == o.outer && row_bytes == o.row_bytes &&
-               box_inner == o.box_inner && box_outer == o.box_outer && dtype == o.dtype && dev == o.dev;
+               box_inner == o.box_inner && box_outer == o.box_outer && dtype == o.dtype && dev == o.dev &&
+               swizzle == o.swizzle;
     }
 };
 
@@ -67,7 +69,8 @@ std::mutex g_maps_mu;
 uint32_t key_hash(const MapKey& k) {
     uint64_t h = reinterpret_cast<uintptr_t>(k.base) * 0x9E3779B97F4A7C15ull;
     h ^= (k.inner * 0xC2B2AE3D27D4EB4Full) ^ (k.outer * 0x165667B19E3779F9ull) ^ (k.row_bytes << 7);
-    h ^= ((uint64_t)k.box_inner << 32) ^ ((uint64_t)k.box_outer << 16) ^ (uint64_t)(k.dtype * 131 + k.dev);
+    h ^= ((uint64_t)k.box_inner << 32) ^ ((uint64_t)k.box_outer << 16) ^
+         (uint64_t)(k.dtype * 131 + k.dev * 7 + k.swizzle * 1031);
     h ^= h >> 29;
     return (uint32_t)(h % kMapSlots);
 }
@@ -116,10 +119,10 @@ cudaError_t current_device(DeviceInfo& info) {
 bool tmap_encoder_available() { return encoder() != nullptr; }
 
 bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
-                    uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, int dev) {
+                    uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, int dev, bool swizzle128) {
     auto enc = encoder();
     if (!enc) return false;
-    const MapKey key{base, inner, outer, row_bytes, box_inner, box_outer, (int)dt, dev};
+    const MapKey key{base, inner, outer, row_bytes, box_inner, box_outer, (int)dt, dev, swizzle128 ? 1 : 0};
     const uint32_t h = key_hash(key);
     {
         std::lock_guard<std::mutex> lock(g_maps_mu);
@@ -133,7 +136,7 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, 
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t es[2] = {1, 1};
     if (enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return false;
     std::lock_guard<std::mutex> lock(g_maps_mu);

@@ -187,6 +187,69 @@ __global__ void __launch_bounds__(256) pack8_kernel(const __half* __restrict__ w
     for (int64_t i = 2 * ngroups + lane; i < lds; i += 32) srow[i] = __ushort_as_half((unsigned short)0);
 }
 
+// The 8-bit quantiser of pack8_kernel in the word layout: four codes per 32-bit
+// word (code of k in byte k % 4 of word k / 4), one FP16 scale per group as the
+// 4-bit layout, one 8-bit zero point per group four to a word (byte g % 4 of
+// word g / 4, ldZ8 = zeros8_ld).  One warp per weight row walks its groups.
+template <int G>
+__global__ void __launch_bounds__(256) pack8w_kernel(const __half* __restrict__ w, int64_t N, int64_t K,
+                                                     uint32_t* __restrict__ qw, __half* __restrict__ sc,
+                                                     uint32_t* __restrict__ zr) {
+    constexpr int PER = G / 32;
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    if (row >= N) return;                    // uniform per warp
+    const int64_t ngroups = K / G;
+    const int64_t ldq = K / 4, lds = scales_ld(K, G), ldz = zeros8_ld(K, G);
+    const __half* wrow = w + row * K;
+    uint32_t* qrow = qw + row * ldq;
+    __half* srow = sc + row * lds;
+    uint32_t* zrow = zr + row * ldz;
+    uint32_t zacc = 0;                       // lane 0: the zero word being filled
+    for (int64_t g = 0; g < ngroups; ++g) {
+        float v[PER];
+        load_weights<PER>(wrow + g * G + lane * PER, v);
+        float lo, hi;
+        group_range<PER>(v, lo, hi);
+        const float range = __fsub_rn(hi, lo);
+        __half sh = __float2half_rn(__fdiv_rn(range, 255.0f));
+        float s = __half2float(sh);
+        int zp = 0;
+        if (s == 0.0f) {
+            sh = __float2half_rn(1.0f);
+            s = 1.0f;
+        } else {
+            zp = min(max(__float2int_rn(__fdiv_rn(-lo, s)), 0), 255);
+        }
+        // this lane's codes at their byte positions, words shared by 4 / PER lanes merged
+        uint32_t wv[PER >= 4 ? PER / 4 : 1] = {};
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int c = min(max(__float2int_rn(__fdiv_rn(v[i], s)) + zp, 0), 255);
+            wv[i / 4] |= (uint32_t)c << (8 * ((lane * PER + i) & 3));
+        }
+        const int64_t k0 = g * G + lane * PER;
+        if constexpr (PER >= 4) {
+#pragma unroll
+            for (int j = 0; j < PER / 4; ++j) qrow[k0 / 4 + j] = wv[j];
+        } else {
+#pragma unroll
+            for (int off = 1; off < 4 / PER; off <<= 1) wv[0] |= __shfl_xor_sync(0xFFFFFFFFu, wv[0], off);
+            if ((k0 & 3) == 0) qrow[k0 / 4] = wv[0];
+        }
+        if (lane == 0) {
+            srow[g] = sh;
+            zacc |= (uint32_t)zp << (8 * (g & 3));
+            if ((g & 3) == 3 || g == ngroups - 1) {
+                zrow[g / 4] = zacc;
+                zacc = 0;
+            }
+        }
+    }
+    for (int64_t i = ngroups + lane; i < lds; i += 32) srow[i] = __ushort_as_half((unsigned short)0);
+    for (int64_t i = (ngroups + 3) / 4 + lane; i < ldz; i += 32) zrow[i] = 0u;
+}
+
 // ---- dequantising checking aids ------------------------------------------------------
 // Each runs one layer kernel's own expansion routine (unpack.cuh) over every
 // packed word, so their bit-exact checks against the oracle pin that routine.
@@ -238,6 +301,50 @@ __global__ void __launch_bounds__(256) dequant_f16_kernel(const uint32_t* __rest
     uint32_t o[4];
     dequant_word(qw[n * qweight_ld(K) + w8], s2, zz, o);
     *reinterpret_cast<uint4*>(out + (n * K + w8 * 8) / 2) = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// 8-bit word layout, W_hat = (q - z) * s in FP32 through the decode kernel's
+// 8-bit expansion (each code as its two nibble halves 1024 + l and 1024 + 16 h,
+// added back) and its 8-bit zero extraction.  One thread per word (4 outputs).
+__global__ void __launch_bounds__(256) dequant8w_kernel(const uint32_t* __restrict__ qw, const __half* __restrict__ sc,
+                                                        const uint32_t* __restrict__ zr, int64_t N, int64_t K, int G,
+                                                        float* __restrict__ out) {
+    const int64_t words = K / 4;
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= N * words) return;
+    const int64_t n = idx / words, w4 = idx % words;
+    const int64_t g = (w4 * 4) / G;
+    const float s = __half2float(sc[n * scales_ld(K, G) + g]);
+    const float z = meta_zero8(zr[n * zeros8_ld(K, G) + g / 4] >> (8 * (g & 3)), 0);
+    uint32_t e0, e1, e2, e3;
+    expand_codes8_f16(qw[n * (K / 4) + w4], e0, e1, e2, e3);
+    // codes 0 and 2 from e0 (low nibbles) and e1 (high nibbles), codes 1 and 3 from e2 and e3
+    const float c0 = __fadd_rn(__fsub_rn(half_lo(e0), 1024.0f), __fsub_rn(half_lo(e1), 1024.0f));
+    const float c2 = __fadd_rn(__fsub_rn(half_hi(e0), 1024.0f), __fsub_rn(half_hi(e1), 1024.0f));
+    const float c1 = __fadd_rn(__fsub_rn(half_lo(e2), 1024.0f), __fsub_rn(half_lo(e3), 1024.0f));
+    const float c3 = __fadd_rn(__fsub_rn(half_hi(e2), 1024.0f), __fsub_rn(half_hi(e3), 1024.0f));
+    *reinterpret_cast<float4*>(out + n * K + w4 * 4) =
+        make_float4(__fmul_rn(__fsub_rn(c0, z), s), __fmul_rn(__fsub_rn(c1, z), s), __fmul_rn(__fsub_rn(c2, z), s),
+                    __fmul_rn(__fsub_rn(c3, z), s));
+}
+
+// 8-bit word layout, RN_fp16((q - z) * s) through the tensor-core kernel's
+// 8-bit expansion and group constants (its FP16 A operand).
+__global__ void __launch_bounds__(256) dequant8w_f16_kernel(const uint32_t* __restrict__ qw,
+                                                            const unsigned short* __restrict__ sc,
+                                                            const uint32_t* __restrict__ zr, int64_t N, int64_t K,
+                                                            int G, uint32_t* __restrict__ out) {
+    const int64_t words = K / 4;
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= N * words) return;
+    const int64_t n = idx / words, w4 = idx % words;
+    const int64_t g = (w4 * 4) / G;
+    const uint4 sv = *reinterpret_cast<const uint4*>(sc + n * scales_ld(K, G) + (g >> 3) * 8);
+    const uint32_t zw = zr[n * zeros8_ld(K, G) + g / 4];
+    uint32_t s2, zz, o[2];
+    group_consts8(sv, zw, (int)(g & 7), (int)(g & 3), true, s2, zz);
+    dequant_word8(qw[n * (K / 4) + w4], s2, zz, o);
+    *reinterpret_cast<uint2*>(out + (n * K + w4 * 4) / 2) = make_uint2(o[0], o[1]);
 }
 
 // Super-block layout: W_hat = d*sc_j*q - dmin*m_j in FP32 through the decode
@@ -389,6 +496,23 @@ cudaError_t launch_pack8(const void* w, int64_t N, int64_t K, int G, uint32_t* q
     return cudaGetLastError();
 }
 
+cudaError_t launch_pack8w(const void* w, int64_t N, int64_t K, int G, uint32_t* qw, void* sc, uint32_t* zr,
+                          cudaStream_t stream) {
+    const int warps = 8;
+    const dim3 block(32 * warps);
+    const dim3 grid((unsigned)((N + warps - 1) / warps));
+    const __half* wp = static_cast<const __half*>(w);
+    __half* sp = static_cast<__half*>(sc);
+    switch (G) {
+        case 32: pack8w_kernel<32><<<grid, block, 0, stream>>>(wp, N, K, qw, sp, zr); break;
+        case 64: pack8w_kernel<64><<<grid, block, 0, stream>>>(wp, N, K, qw, sp, zr); break;
+        case 128: pack8w_kernel<128><<<grid, block, 0, stream>>>(wp, N, K, qw, sp, zr); break;
+        case 256: pack8w_kernel<256><<<grid, block, 0, stream>>>(wp, N, K, qw, sp, zr); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
 // Grid for one thread per packed word of N x K codes (false when it does not fit one launch).
 static bool word_grid(int64_t N, int64_t K, dim3& grid) {
     const int64_t blocks = (N * (K / 8) + 255) / 256;
@@ -411,6 +535,23 @@ cudaError_t launch_dequant_f16(const uint32_t* qw, const void* sc, const uint32_
     if (!word_grid(N, K, grid)) return cudaErrorInvalidValue;
     dequant_f16_kernel<<<grid, 256, 0, stream>>>(qw, static_cast<const unsigned short*>(sc), zr, N, K, G,
                                                  static_cast<uint32_t*>(out));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dequant8w(const uint32_t* qw, const void* sc, const uint32_t* zr, int64_t N, int64_t K, int G,
+                             float* out, cudaStream_t stream) {
+    const int64_t blocks = (N * (K / 4) + 255) / 256;
+    if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    dequant8w_kernel<<<(unsigned)blocks, 256, 0, stream>>>(qw, static_cast<const __half*>(sc), zr, N, K, G, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dequant8w_f16(const uint32_t* qw, const void* sc, const uint32_t* zr, int64_t N, int64_t K, int G,
+                                 void* out, cudaStream_t stream) {
+    const int64_t blocks = (N * (K / 4) + 255) / 256;
+    if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    dequant8w_f16_kernel<<<(unsigned)blocks, 256, 0, stream>>>(qw, static_cast<const unsigned short*>(sc), zr, N, K,
+                                                               G, static_cast<uint32_t*>(out));
     return cudaGetLastError();
 }
 
