@@ -1,5 +1,5 @@
 // gemm_tc.cu -- prefill path of the W4A16 linear layer on the tcgen05 tensor
-// cores (any M; the library routes M > 8 here).
+// cores (any M; the library routes M > 16 here, and 8-bit codes at M > 8).
 //
 // At prefill many activation rows share each weight, so the layer is a dense
 // contraction bound by tensor-core throughput; the dequantisation is extra
@@ -17,13 +17,15 @@
 // Precision.  Operands are FP16: A = RN_fp16((q - z) * s) (the code difference
 // is exact in FP16, one rounding for the product), B = x converted from BF16
 // to FP16 once per call (exact for normal-range values), FP32 accumulation in
-// TMEM, one BF16 rounding per output.  A BF16 A operand would round W_hat to
-// 8 significant bits, which alone costs more relative error than the output
-// tolerance leaves after the BF16 output rounding; FP16 keeps 11.
+// TMEM, one BF16 rounding per output (or none: FP32 outputs).  A BF16 A
+// operand would round W_hat to 8 significant bits, which alone costs more
+// relative error than the output tolerance leaves after the BF16 output
+// rounding; FP16 keeps 11.
 //
 // Structure: a persistent kernel, one 320-thread CTA per SM, warp-specialised.
 //   warp 0      TMA producer: 64-k slices of x (BN rows, 128-byte swizzle) and
-//               256-k slices of packed codes (128 rows x 128 bytes, swizzled)
+//               code stages of 128 rows x 128 bytes (256 4-bit or 128 8-bit
+//               codes per row, swizzled)
 //   warp 1      tensor-memory owner and MMA issuer (one thread): per 64-k
 //               slice, four 128 x BN x 16 MMAs, A from TMEM, B from smem
 //   warps 2..5  dequantisers: thread = weight row = TMEM lane; codes from
@@ -33,7 +35,9 @@
 //   warps 6..9  epilogue: tcgen05.ld of the FP32 accumulator, BF16 rounding,
 //               stores to y
 // Tiles are 128 weight rows x BN activation rows (BN <= 256), ordered with the
-// activation tile fastest so consecutive CTAs share a weight tile in L2.
+// activation tile fastest so consecutive CTAs share a weight tile in L2.  When
+// narrow tiles (BN <= 64) fill at most half the SMs, each is cut along K and
+// the pieces' FP32 partials are added in a fixed order (see GemmParams).
 // Every wait is bounded: on expiry the kernel records a code in the status
 // word, waits (bounded) for its own copies and MMAs in flight, frees its
 // tensor memory and returns.
@@ -59,16 +63,13 @@ namespace {
 
 constexpr int kThreads = 320;              // 10 warps
 constexpr int kBM = 128;                   // weight rows per tile (MMA M)
-constexpr int kMaxXS = 8;                  // x ring: at most 8 slices of 64 k
-constexpr int kMaxCS = 6;                  // code ring: at most 6 slices of 256 k
+constexpr int kXS = 5;                     // x ring: slices of 64 k
+constexpr int kCS = 3;                     // code ring: slices of 256 k
 constexpr int kAS = 8;                     // A ring in TMEM: slices of 64 k (32 columns)
-constexpr uint32_t kCodeBytes = 128u * 128u;           // 128 rows x 256 codes
-constexpr uint32_t kScaleBytes = 128u * 16u;           // 128 rows x one 8-group chunk of FP16 scales
-constexpr uint32_t kZeroBytes = 128u * 16u;            // 128 rows x 4 zero words (32 groups)
-constexpr uint32_t kCodeStageBytes = kCodeBytes + kScaleBytes + kZeroBytes;
+constexpr uint32_t kCodeStageBytes = 128u * 128u;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kACol0 = 256;           // D uses columns [0, BN), A slices [256, 512)
-constexpr int kNumBars = 2 * kMaxXS + 2 * kMaxCS + 2 * kAS + 2;
+constexpr int kNumBars = 2 * kXS + 2 * kCS + 2 * kAS + 2;
 
 // Status codes (bit fields) recorded when a wait gives up.
 constexpr uint32_t kStatusProducer = 1u << 0;
@@ -78,70 +79,61 @@ constexpr uint32_t kStatusEpilogue = 1u << 3;
 constexpr uint32_t kStatusDrain = 1u << 4;
 
 // Work units.  A tile is 128 weight rows x BN activation rows; units [0, full)
-// are whole tiles (tile = unit).  The last `split` tiles (those that would
-// leave the last wave part-empty, or all of them when there are fewer tiles
-// than SMs) are each cut into `parts` pieces, unit full + j * split + i being
-// piece j of tile full + i:
-//   ksplit = 1 (small BN): piece j is a range of 256-k code slices; its FP32
-//     partial goes to a workspace and the last of the tile's pieces to finish
-//     adds them in a fixed order (so results do not depend on arrival order);
-//   ksplit = 0: piece j is the activation rows [j bt, (j + 1) bt) of the tile
-//     over all of K (bt = BN / parts, a multiple of 32), written straight to y.
+// are whole tiles (tile = unit).  When there are few tiles for the SMs and a
+// tile is narrow (small M, where a tile's time is its weight streaming and
+// expansion), the last `split` tiles are each cut along K into `parts` ranges
+// of code stages, unit full + j * split + i being range j of tile
+// full + i.  A range's FP32 partial goes to a workspace, and the last of a
+// tile's ranges to finish adds them in a fixed order (so results do not
+// depend on arrival order) and writes y.
 struct GemmParams {
+    const unsigned short* s;   // FP16 scales [N, lds]
+    const uint32_t* z;         // packed zeros [N, ldz] (4-bit: 8 per word; 8-bit: 4 per word)
     void* y;                   // [M, N], BF16 (or FP32 when yf32)
     float* ws;                 // K-split partials [split * parts][BN][128]
     uint32_t* cnt;             // arrivals per K-split tile (zero at launch)
-    int M, N, K, BN, bt;
-    int ngroups;
-    int mtiles, tiles;
-    int nk64, nk256;
-    int xs, cs;                // ring depths
-    int full, split, parts, ksplit, units;
     int yf32;                  // 1: FP32 outputs (no BF16 rounding)
+    int M, N, K, BN;
+    int lds, ldz, ngroups;
+    int mtiles, tiles;
+    int nk64;
+    int subs, nstage;          // 64-k slices per code stage (4: 4-bit codes, 2: 8-bit), code stages
+    int full, split, parts, units;
     long long spin_limit;      // cycles a bounded wait spins before it gives up
     int withhold;              // test hook: CTA 0 never issues its first code copy
 };
 
 struct Unit {
     int tile;                  // tile index (n-tile * mtiles + m-tile)
-    int kb0, kb1;              // its 64-k slices [kb0, kb1) (kb0 a multiple of 4)
-    int m0, bn;                // its first activation row and its activation rows (MMA N)
-    int part;                  // K-split piece: its partial's slot in the workspace; else -1
-    int stile;                 // K-split tile index (counter slot), or -1
+    int kb0, kb1;              // its 64-k slices [kb0, kb1) (kb0 on a code-stage boundary)
+    int part;                  // K range of a split tile: its partial's slot; else -1
+    int stile;                 // split tile index (counter slot), or -1
 };
 
 __device__ __forceinline__ Unit unit_of(const GemmParams& p, int u) {
     Unit U;
-    U.part = -1;
-    U.stile = -1;
-    U.kb0 = 0;
-    U.kb1 = p.nk64;
-    U.bn = p.BN;
     if (u < p.full) {
         U.tile = u;
-        U.m0 = (u % p.mtiles) * p.BN;
+        U.kb0 = 0;
+        U.kb1 = p.nk64;
+        U.part = -1;
+        U.stile = -1;
         return U;
     }
     const int v = u - p.full;
     const int j = v / p.split, i = v - j * p.split;
     U.tile = p.full + i;
-    U.m0 = (U.tile % p.mtiles) * p.BN;
-    if (p.ksplit) {
-        U.kb0 = 4 * ((j * p.nk256) / p.parts);
-        U.kb1 = min(4 * (((j + 1) * p.nk256) / p.parts), p.nk64);
-        U.part = i * p.parts + j;
-        U.stile = i;
-    } else {
-        U.m0 += j * p.bt;
-        U.bn = p.bt;
-    }
+    U.kb0 = p.subs * ((j * p.nstage) / p.parts);
+    U.kb1 = min(p.subs * (((j + 1) * p.nstage) / p.parts), p.nk64);
+    U.part = i * p.parts + j;
+    U.stile = i;
     return U;
 }
 
 // Dynamic shared memory per CTA.  Never less than 120 KB, so at most one CTA
 // is resident per SM and the 512 tensor-memory columns it allocates are free.
-size_t gemm_smem_bytes(int BN, int xs, int cs) {
-    const size_t need = 1024 + (size_t)xs * BN * 128 + (size_t)cs * kCodeStageBytes + kNumBars * 8 + 16;
+size_t gemm_smem_bytes(int BN) {
+    const size_t need = 1024 + (size_t)kXS * BN * 128 + (size_t)kCS * kCodeStageBytes + kNumBars * 8 + 16;
     return need < 120 * 1024 ? 120 * 1024 : need;
 }
 
@@ -150,27 +142,32 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
     return v;
 }
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+__device__ __forceinline__ uint4 ldg128_nc(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint32_t ldg32_nc(const void* p) {
     uint32_t v;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
     return v;
 }
 
 struct Smem {
-    uint8_t* x;       // xs slices of BN * 128 bytes
-    uint8_t* c;       // cs stages: codes (16 KB, swizzled), scales (2 KB), zeros (2 KB)
+    uint8_t* x;       // kXS slices of BN * 128 bytes
+    uint8_t* c;       // kCS slices of 16 KB
     uint64_t* bar;
     uint32_t* tmem_slot;
     volatile int* abort_flag;
-    volatile int* last_flag;   // epilogue: this CTA completes the K-split tile
+    volatile int* last_flag;   // epilogue: this CTA completes the split tile
     __device__ uint32_t x_full(int i) const { return tc::smem_u32(bar + i); }
-    __device__ uint32_t x_empty(int i) const { return tc::smem_u32(bar + kMaxXS + i); }
-    __device__ uint32_t c_full(int i) const { return tc::smem_u32(bar + 2 * kMaxXS + i); }
-    __device__ uint32_t c_empty(int i) const { return tc::smem_u32(bar + 2 * kMaxXS + kMaxCS + i); }
-    __device__ uint32_t a_full(int i) const { return tc::smem_u32(bar + 2 * kMaxXS + 2 * kMaxCS + i); }
-    __device__ uint32_t a_empty(int i) const { return tc::smem_u32(bar + 2 * kMaxXS + 2 * kMaxCS + kAS + i); }
-    __device__ uint32_t d_full() const { return tc::smem_u32(bar + 2 * kMaxXS + 2 * kMaxCS + 2 * kAS); }
-    __device__ uint32_t d_empty() const { return tc::smem_u32(bar + 2 * kMaxXS + 2 * kMaxCS + 2 * kAS + 1); }
+    __device__ uint32_t x_empty(int i) const { return tc::smem_u32(bar + kXS + i); }
+    __device__ uint32_t c_full(int i) const { return tc::smem_u32(bar + 2 * kXS + i); }
+    __device__ uint32_t c_empty(int i) const { return tc::smem_u32(bar + 2 * kXS + kCS + i); }
+    __device__ uint32_t a_full(int i) const { return tc::smem_u32(bar + 2 * kXS + 2 * kCS + i); }
+    __device__ uint32_t a_empty(int i) const { return tc::smem_u32(bar + 2 * kXS + 2 * kCS + kAS + i); }
+    __device__ uint32_t d_full() const { return tc::smem_u32(bar + 2 * kXS + 2 * kCS + 2 * kAS); }
+    __device__ uint32_t d_empty() const { return tc::smem_u32(bar + 2 * kXS + 2 * kCS + 2 * kAS + 1); }
 };
 
 // Bounded wait for a barrier phase; gives up (recording `site`) after `limit`
@@ -217,27 +214,24 @@ __device__ __forceinline__ bool epilogue_all(bool v) {
     return r != 0;
 }
 
-// Epilogue of one K-range piece of a K-split tile (BN <= 64; the four epilogue
-// warps, thread r = weight row r of the tile): the accumulator is loaded into
-// registers and released, the FP32 partial goes to the workspace (row r of
-// column m at [part][m][r], so a warp writes 128 contiguous bytes per column),
-// and the last of the tile's pieces to arrive adds the partials in a fixed
-// order (loads of every column of one piece in flight together) and writes y.
-__device__ __forceinline__ void epilogue_partial(const GemmParams& p, const Smem& sm, const Unit& U, int n,
+// Epilogue of one K range of a split tile (BN <= 64; the four epilogue warps,
+// thread r = weight row r of the tile): the accumulator goes 16 columns at a
+// time to the FP32 workspace (row r of column m at [part][m][r], so a warp
+// writes 128 contiguous bytes per column) and is released, and the last of the
+// tile's ranges to arrive adds the partials in a fixed order and writes y.
+__device__ __forceinline__ void epilogue_partial(const GemmParams& p, const Smem& sm, const Unit& U, int n, int m0,
                                                  uint32_t d_lane, int lane, int r) {
     float* wp = p.ws + (size_t)U.part * p.BN * kBM + r;
-    uint32_t v0[32], v1[32];
-    tc::tmem_ld32_wait(d_lane, v0);
-    if (p.BN > 32) tc::tmem_ld32_wait(d_lane + 32u, v1);
+#pragma unroll 1
+    for (int c = 0; c < p.BN; c += 16) {
+        uint32_t v[16];
+        tc::tmem_ld16_wait(d_lane + (uint32_t)c, v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) __stcg(wp + (size_t)(c + j) * kBM, __uint_as_float(v[j]));
+    }
     tc::tc_fence_before();
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(sm.d_empty());
-#pragma unroll
-    for (int j = 0; j < 32; ++j) __stcg(wp + (size_t)j * kBM, __uint_as_float(v0[j]));
-    if (p.BN > 32) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) __stcg(wp + (size_t)(32 + j) * kBM, __uint_as_float(v1[j]));
-    }
     __threadfence();
     epilogue_sync();
     if (threadIdx.x == 6 * 32) *sm.last_flag = atomicAdd(p.cnt + U.stile, 1u) == (uint32_t)(p.parts - 1);
@@ -246,25 +240,25 @@ __device__ __forceinline__ void epilogue_partial(const GemmParams& p, const Smem
     epilogue_sync();                                  // every thread has read the flag
     if (!last) return;
     __threadfence();
-    const int lim = min(p.BN, p.M - U.m0);            // activation rows of the tile
+    const int lim = min(p.BN, p.M - m0);              // activation rows of the tile
     const float* wt = p.ws + (size_t)U.stile * p.parts * p.BN * kBM + r;
 #pragma unroll 1
-    for (int h = 0; h < lim; h += 32) {               // 32 columns at a time, all their loads in flight
-        float acc[32];
+    for (int h = 0; h < lim; h += 16) {
+        float acc[16];
 #pragma unroll
-        for (int ml = 0; ml < 32; ++ml) acc[ml] = 0.0f;
+        for (int ml = 0; ml < 16; ++ml) acc[ml] = 0.0f;
 #pragma unroll 1
-        for (int j = 0; j < p.parts; ++j) {
+        for (int j = 0; j < p.parts; ++j) {          // the 16 loads of one partial in flight together
             const float* wj = wt + ((size_t)j * p.BN + h) * kBM;
 #pragma unroll
-            for (int ml = 0; ml < 32; ++ml)
+            for (int ml = 0; ml < 16; ++ml)
                 if (h + ml < lim) acc[ml] += __ldcg(wj + (size_t)ml * kBM);
         }
         if (n < p.N) {
 #pragma unroll
-            for (int ml = 0; ml < 32; ++ml) {
+            for (int ml = 0; ml < 16; ++ml) {
                 if (h + ml < lim) {
-                    const int64_t o = (int64_t)(U.m0 + h + ml) * p.N + n;
+                    const int64_t o = (int64_t)(m0 + h + ml) * p.N + n;
                     if (p.yf32)
                         static_cast<float*>(p.y)[o] = acc[ml];
                     else
@@ -275,61 +269,10 @@ __device__ __forceinline__ void epilogue_partial(const GemmParams& p, const Smem
     }
 }
 
-// Epilogue of a whole tile or an activation-row piece with FP32 outputs (no
-// BF16 rounding): each 32-column chunk is stored as loaded, and the
-// accumulator is released after the last one.
-__device__ __forceinline__ void epilogue_f32(const GemmParams& p, const Smem& sm, const Unit& U, int n,
-                                             uint32_t d_lane, int lane) {
-#pragma unroll 1
-    for (int ch = 0; ch < 8; ++ch) {
-        if (ch * 32 < U.bn) {
-            uint32_t v[32];
-            tc::tmem_ld32_wait(d_lane + (uint32_t)ch * 32u, v);
-            if (n < p.N) {
-                float* yc = static_cast<float*>(p.y) + n;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int m = U.m0 + ch * 32 + j;
-                    if (m < p.M) yc[(int64_t)m * p.N] = __uint_as_float(v[j]);
-                }
-            }
-        }
-    }
-    tc::tc_fence_before();
-    __syncwarp();
-    if (lane == 0) tc::mbar_arrive(sm.d_empty());
-}
-
-// One 64-k slice of A for this thread's weight row: the 64 codes of the slice
-// (two 16-byte words of the swizzled code stage) expanded with the tile's group
-// constants into 32 FP16 pairs.
-template <int G>
-__device__ __forceinline__ void dequant_slice(uint32_t rowp, int r, int sub, int ks, const uint4& sv, uint32_t zw,
-                                              int ngroups, uint32_t (&a)[32]) {
-    const uint4 w0 = lds128(rowp + ((uint32_t)((2 * sub) ^ (r & 7)) << 4));
-    const uint4 w1 = lds128(rowp + ((uint32_t)((2 * sub + 1) ^ (r & 7)) << 4));
-    const int ga = (ks * 256 + sub * 64) / G;        // group of the slice's first code
-    uint32_t s2a, zza, s2b, zzb;
-    group_consts(sv, zw, ga & 7, ga < ngroups, s2a, zza);
-    if constexpr (G == 32) {
-        group_consts(sv, zw, (ga + 1) & 7, ga + 1 < ngroups, s2b, zzb);
-    } else {
-        s2b = s2a;
-        zzb = zza;
-    }
-    dequant_word(w0.x, s2a, zza, a + 0);
-    dequant_word(w0.y, s2a, zza, a + 4);
-    dequant_word(w0.z, s2a, zza, a + 8);
-    dequant_word(w0.w, s2a, zza, a + 12);
-    dequant_word(w1.x, s2b, zzb, a + 16);
-    dequant_word(w1.y, s2b, zzb, a + 20);
-    dequant_word(w1.z, s2b, zzb, a + 24);
-    dequant_word(w1.w, s2b, zzb, a + 28);
-}
-
-// The same for 8-bit codes (the word layout): the slice's 64 codes are four
-// 16-byte words of the swizzled stage (a stage holds 128 codes per row), and
-// the zero points are bytes of the stage's zero words.
+// One 64-k slice of A from 8-bit codes (the word layout): the slice's 64 codes
+// are four 16-byte words of the swizzled stage (a stage holds 128 codes per
+// row); sv holds the 8-group scale chunk and zv the four zero words (16
+// groups) of the stage's groups.
 template <int G>
 __device__ __forceinline__ void dequant_slice8(uint32_t rowp, int r, int sub, int ks, const uint4& sv,
                                                const uint4& zv, int ngroups, uint32_t (&a)[32]) {
@@ -339,8 +282,8 @@ __device__ __forceinline__ void dequant_slice8(uint32_t rowp, int r, int sub, in
     const int ga = (ks * 128 + sub * 64) / G;        // group of the slice's first code
     const int gc = (ks * 128 / G) & ~7;              // first group of the scale chunk
     const int gz = (ks * 128 / G) & ~15;             // first group of the zero words
-    uint32_t s2a, zza, s2b, zzb;
     const uint32_t zs[4] = {zv.x, zv.y, zv.z, zv.w};
+    uint32_t s2a, zza, s2b, zzb;
     group_consts8(sv, zs[((ga - gz) >> 2) & 3], ga - gc, ga & 3, ga < ngroups, s2a, zza);
     if constexpr (G == 32) {
         group_consts8(sv, zs[((ga + 1 - gz) >> 2) & 3], ga + 1 - gc, (ga + 1) & 3, ga + 1 < ngroups, s2b, zzb);
@@ -360,29 +303,29 @@ __device__ __forceinline__ void dequant_slice8(uint32_t rowp, int r, int sub, in
 
 template <int G, bool W8>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_xt,
-                const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_s,
-                const __grid_constant__ CUtensorMap tm_z, const GemmParams p) {
-    constexpr int kSubs = W8 ? 2 : 4;            // 64-k slices per code stage (128 bytes per row)
+    gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_q,
+                const GemmParams p) {
+    // 64-k slices per code stage (a stage is 128 bytes of codes per row: 256 4-bit codes, or
+    // 128 8-bit codes)
+    constexpr int kSubs = W8 ? 2 : 4;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t xbytes = (uint32_t)p.BN * 128u;
-    const int XS = p.xs, CS = p.cs;
     Smem sm;
     sm.x = base;
-    sm.c = base + XS * xbytes;
-    sm.bar = reinterpret_cast<uint64_t*>(sm.c + CS * kCodeStageBytes);
+    sm.c = base + kXS * xbytes;
+    sm.bar = reinterpret_cast<uint64_t*>(sm.c + kCS * kCodeStageBytes);
     sm.tmem_slot = reinterpret_cast<uint32_t*>(sm.bar + kNumBars);
     sm.abort_flag = reinterpret_cast<volatile int*>(sm.tmem_slot + 1);
     sm.last_flag = reinterpret_cast<volatile int*>(sm.tmem_slot + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int i = 0; i < XS; ++i) {
+        for (int i = 0; i < kXS; ++i) {
             tc::mbar_init(sm.x_full(i), 1);
             tc::mbar_init(sm.x_empty(i), 1);
         }
-        for (int i = 0; i < CS; ++i) {
+        for (int i = 0; i < kCS; ++i) {
             tc::mbar_init(sm.c_full(i), 1);
             tc::mbar_init(sm.c_empty(i), 4);
         }
@@ -396,10 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *sm.last_flag = 0;
         tc::fence_barrier_init();
         tc::tma_prefetch_desc(&tm_x);
-        tc::tma_prefetch_desc(&tm_xt);
         tc::tma_prefetch_desc(&tm_q);
-        tc::tma_prefetch_desc(&tm_s);
-        tc::tma_prefetch_desc(&tm_z);
     }
     if (warp == 1) {
         tc::tmem_alloc(tc::smem_u32(sm.tmem_slot), kTmemCols);
@@ -422,53 +362,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool withhold = p.withhold && blockIdx.x == 0;
             for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
                 const Unit U = unit_of(p, u);
-                const int n0 = (U.tile / p.mtiles) * kBM;
-                const void* tmx = U.bn == p.BN ? (const void*)&tm_x : (const void*)&tm_xt;
+                const int n0 = (U.tile / p.mtiles) * kBM, m0 = (U.tile % p.mtiles) * p.BN;
                 for (int kb = U.kb0; kb < U.kb1; ++kb) {
                     if ((kb & (kSubs - 1)) == 0) {
-                        // one stage: 128 bytes of codes per row (256 k, or 128 k of 8-bit codes),
-                        // the 8-group chunk of scales holding its groups, and the 4-word block of
-                        // zero words holding them
-                        if (!(ok = wait_phase(sm.c_empty(ci), cph ^ 1u, sm.abort_flag, kStatusProducer, p.spin_limit)))
-                            break;
+                        if (!(ok = wait_phase(sm.c_empty(ci), cph ^ 1u, sm.abort_flag, kStatusProducer, p.spin_limit))) break;
                         if (!(withhold && c_issued == 0)) {
-                            const uint32_t st = tc::smem_u32(sm.c + ci * kCodeStageBytes);
-                            const int g0 = kb * 64 / G;                      // the stage's first group
-                            const int zword = W8 ? (g0 >> 2) & ~3 : (g0 >> 3) & ~3;
                             tc::mbar_arrive_expect_tx(sm.c_full(ci), kCodeStageBytes);
-                            tc::tma_load_2d(st, &tm_q, (kb / kSubs) * 32, n0, sm.c_full(ci));
-                            tc::tma_load_2d(st + kCodeBytes, &tm_s, g0 & ~7, n0, sm.c_full(ci));
-                            tc::tma_load_2d(st + kCodeBytes + kScaleBytes, &tm_z, zword, n0, sm.c_full(ci));
+                            tc::tma_load_2d(tc::smem_u32(sm.c + ci * kCodeStageBytes), &tm_q, (kb / kSubs) * 32, n0,
+                                            sm.c_full(ci));
                         }
                         ++c_issued;
-                        if (++ci == CS) { ci = 0; cph ^= 1u; }
+                        if (++ci == kCS) { ci = 0; cph ^= 1u; }
                     }
-                    if (!(ok = wait_phase(sm.x_empty(xi), xph ^ 1u, sm.abort_flag, kStatusProducer, p.spin_limit)))
-                        break;
-                    tc::mbar_arrive_expect_tx(sm.x_full(xi), (uint32_t)U.bn * 128u);
-                    tc::tma_load_2d(tc::smem_u32(sm.x + xi * xbytes), tmx, kb * 64, U.m0, sm.x_full(xi));
+                    if (!(ok = wait_phase(sm.x_empty(xi), xph ^ 1u, sm.abort_flag, kStatusProducer, p.spin_limit))) break;
+                    tc::mbar_arrive_expect_tx(sm.x_full(xi), xbytes);
+                    tc::tma_load_2d(tc::smem_u32(sm.x + xi * xbytes), &tm_x, kb * 64, m0, sm.x_full(xi));
                     ++x_issued;
-                    if (++xi == XS) { xi = 0; xph ^= 1u; }
+                    if (++xi == kXS) { xi = 0; xph ^= 1u; }
                 }
             }
             if (!ok) {   // wait for the copies this thread started
-                for (int s = 0; s < XS; ++s)
+                for (int s = 0; s < kXS; ++s)
                     if (x_issued > s) drain_phase(sm.x_full(s), s < xi ? xph : (xph ^ 1u), p.spin_limit);
-                for (int s = 0; s < CS; ++s)
-                    if (c_issued > s && !(withhold && s == 0 && c_issued <= CS))
-                        drain_phase(sm.c_full(s), s < ci ? cph : (cph ^ 1u), p.spin_limit);
+                for (int s = 0; s < kCS; ++s)
+                    if (c_issued > s && !(withhold && s == 0 && c_issued <= kCS)) drain_phase(sm.c_full(s), s < ci ? cph : (cph ^ 1u), p.spin_limit);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
+            const uint32_t idesc = tc::idesc_f16_f32(kBM, p.BN);
             int xi = 0, ai = 0;
             uint32_t xph = 0, aph = 0, dph = 0, d_commits = 0;
             bool ok = true;
             bool issued = false;
             for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
                 const Unit U = unit_of(p, u);
-                const uint32_t idesc = tc::idesc_f16_f32(kBM, U.bn);
                 if (!(ok = wait_phase(sm.d_empty(), dph ^ 1u, sm.abort_flag, kStatusMma, p.spin_limit))) break;
                 dph ^= 1u;
                 tc::tc_fence_after();
@@ -485,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     issued = true;
                     tc::mma_commit(sm.x_empty(xi));
                     tc::mma_commit(sm.a_empty(ai));
-                    if (++xi == XS) { xi = 0; xph ^= 1u; }
+                    if (++xi == kXS) { xi = 0; xph ^= 1u; }
                     if (++ai == kAS) { ai = 0; aph ^= 1u; }
                 }
                 if (!ok) break;
@@ -499,66 +428,72 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp < 6) {
         // ------------------------------------------------------------ dequantisers
-        // Each slice's tensor-memory store completes while the next slice is
-        // expanded: a slice is announced (a_full) only once its store has
-        // completed, one slice behind, and the two register buffers alternate.
         const int qd = warp & 3;
         const int r = qd * 32 + lane;                       // weight row in the tile = TMEM lane
         const uint32_t a_lane = tmem + ((uint32_t)(qd * 32) << 16) + kACol0;
-        int ci = 0, ai = 0, pend = -1;                      // pend: A slot whose store is in flight
-        uint32_t cph = 0, aph = 0, buf = 0;
-        uint32_t a0[32], a1[32];
+        int ci = 0, ai = 0;
+        uint32_t cph = 0, aph = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
             const Unit U = unit_of(p, u);
+            const int n = (U.tile / p.mtiles) * kBM + r;
+            const bool rv = n < p.N;
+            const unsigned short* srow = p.s + (int64_t)(rv ? n : 0) * p.lds;
+            const uint32_t* zrow = p.z + (int64_t)(rv ? n : 0) * p.ldz;
             for (int ks = U.kb0 / kSubs; kSubs * ks < U.kb1 && ok; ++ks) {
+                // this stage's groups: the 8-group chunk of scales holding them, and their zero
+                // points (4-bit: the chunk's zero word; 8-bit: the 4-word block holding 16 groups)
+                const int g0 = ks * (kSubs * 64) / G;
+                uint4 sv = make_uint4(0u, 0u, 0u, 0u), zv = make_uint4(0u, 0u, 0u, 0u);
+                uint32_t zw = 0u;
+                if (rv) {
+                    sv = ldg128_nc(srow + (g0 & ~7));
+                    if constexpr (W8) zv = ldg128_nc(zrow + ((g0 >> 2) & ~3));
+                    else zw = ldg32_nc(zrow + (g0 >> 3));
+                }
                 ok = wait_phase(sm.c_full(ci), cph, sm.abort_flag, kStatusDequant, p.spin_limit);
                 if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
-                const uint32_t st = tc::smem_u32(sm.c + ci * kCodeStageBytes);
-                const uint32_t rowp = st + (uint32_t)r * 128u;
-                const uint4 sv = lds128(st + kCodeBytes + (uint32_t)r * 16u);
-                // 4-bit: the zero word of the stage's 8-group chunk; 8-bit: the stage's 4 zero words
-                const int chunk = (ks * (256 / G)) >> 3;
-                const uint32_t zrow = st + kCodeBytes + kScaleBytes + (uint32_t)r * 16u;
-                uint32_t zw = 0u;
-                uint4 zv = make_uint4(0u, 0u, 0u, 0u);
-                if constexpr (W8) zv = lds128(zrow);
-                else zw = lds32(zrow + (uint32_t)(chunk & 3) * 4u);
+                const uint32_t rowp = tc::smem_u32(sm.c + ci * kCodeStageBytes) + (uint32_t)r * 128u;
                 const int nsub = min(kSubs, p.nk64 - ks * kSubs);
                 for (int sub = 0; sub < nsub; ++sub) {
                     ok = wait_phase(sm.a_empty(ai), aph ^ 1u, sm.abort_flag, kStatusDequant, p.spin_limit);
                     if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
                     tc::tc_fence_after();
+                    uint32_t a[32];
                     if constexpr (W8) {
-                        if (buf) dequant_slice8<G>(rowp, r, sub, ks, sv, zv, p.ngroups, a1);
-                        else dequant_slice8<G>(rowp, r, sub, ks, sv, zv, p.ngroups, a0);
+                        dequant_slice8<G>(rowp, r, sub, ks, sv, zv, p.ngroups, a);
                     } else {
-                        if (buf) dequant_slice<G>(rowp, r, sub, ks, sv, zw, p.ngroups, a1);
-                        else dequant_slice<G>(rowp, r, sub, ks, sv, zw, p.ngroups, a0);
+                        const uint4 w0 = lds128(rowp + ((uint32_t)((2 * sub) ^ (r & 7)) << 4));
+                        const uint4 w1 = lds128(rowp + ((uint32_t)((2 * sub + 1) ^ (r & 7)) << 4));
+                        const int ga = (ks * 256 + sub * 64) / G;        // group of the slice's first code
+                        uint32_t s2a, zza, s2b, zzb;
+                        group_consts(sv, zw, ga & 7, ga < p.ngroups, s2a, zza);
+                        if constexpr (G == 32) {
+                            group_consts(sv, zw, (ga + 1) & 7, ga + 1 < p.ngroups, s2b, zzb);
+                        } else {
+                            s2b = s2a;
+                            zzb = zza;
+                        }
+                        dequant_word(w0.x, s2a, zza, a + 0);
+                        dequant_word(w0.y, s2a, zza, a + 4);
+                        dequant_word(w0.z, s2a, zza, a + 8);
+                        dequant_word(w0.w, s2a, zza, a + 12);
+                        dequant_word(w1.x, s2b, zzb, a + 16);
+                        dequant_word(w1.y, s2b, zzb, a + 20);
+                        dequant_word(w1.z, s2b, zzb, a + 24);
+                        dequant_word(w1.w, s2b, zzb, a + 28);
                     }
-                    if (pend >= 0) {                                // the previous slice's store is done
-                        tc::tmem_wait_st();
-                        tc::tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) tc::mbar_arrive(sm.a_full(pend));
-                    }
-                    if (buf) tc::tmem_st32(a_lane + (uint32_t)ai * 32u, a1);
-                    else tc::tmem_st32(a_lane + (uint32_t)ai * 32u, a0);
-                    pend = ai;
-                    buf ^= 1u;
+                    tc::tmem_st32_wait(a_lane + (uint32_t)ai * 32u, a);
+                    tc::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(sm.a_full(ai));
                     if (++ai == kAS) { ai = 0; aph ^= 1u; }
                 }
                 if (!ok) break;
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(sm.c_empty(ci));    // the stage's codes are read
-                if (++ci == CS) { ci = 0; cph ^= 1u; }
+                if (lane == 0) tc::mbar_arrive(sm.c_empty(ci));
+                if (++ci == kCS) { ci = 0; cph ^= 1u; }
             }
-        }
-        tc::tmem_wait_st();                                      // no store left in flight
-        if (ok && pend >= 0) {
-            tc::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(sm.a_full(pend));
         }
     } else {
         // ------------------------------------------------------------ epilogue
@@ -569,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
             const Unit U = unit_of(p, u);
-            const int n = (U.tile / p.mtiles) * kBM + r;
+            const int n = (U.tile / p.mtiles) * kBM + r, m0 = (U.tile % p.mtiles) * p.BN;
             ok = wait_phase(sm.d_full(), dph, sm.abort_flag, kStatusEpilogue, p.spin_limit);
             if (!epilogue_all(ok)) {
                 ok = false;
@@ -578,27 +513,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             dph ^= 1u;
             tc::tc_fence_after();
             if (U.part >= 0) {
-                epilogue_partial(p, sm, U, n, d_lane, lane, r);
+                epilogue_partial(p, sm, U, n, m0, d_lane, lane, r);
                 continue;
             }
             if (p.yf32) {
-                epilogue_f32(p, sm, U, n, d_lane, lane);
+                // FP32 output (no BF16 rounding): each 32-column chunk is stored as loaded, and the
+                // accumulator is released after the last one
+#pragma unroll 1
+                for (int ch = 0; ch < 8; ++ch) {
+                    if (ch * 32 < p.BN) {
+                        uint32_t v[32];
+                        tc::tmem_ld32_wait(d_lane + (uint32_t)ch * 32u, v);
+                        if (n < p.N) {
+                            float* yc = static_cast<float*>(p.y) + n;
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {
+                                const int m = m0 + ch * 32 + j;
+                                if (m < p.M) yc[(int64_t)m * p.N] = __uint_as_float(v[j]);
+                            }
+                        }
+                    }
+                }
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(sm.d_empty());
                 continue;
             }
-            // BF16 output: the accumulator is read 16 columns at a time and rounded into
-            // registers, released, and only then stored (a warp writes 64 contiguous bytes per
-            // column), so the next unit's MMAs overlap the stores
             uint32_t packed[128];
 #pragma unroll
-            for (int ch = 0; ch < 16; ++ch) {
-                if (ch * 16 < U.bn) {
-                    uint32_t v[16];
-                    tc::tmem_ld16_wait(d_lane + (uint32_t)ch * 16u, v);
+            for (int ch = 0; ch < 8; ++ch) {
+                if (ch * 32 < p.BN) {
+                    uint32_t v[32];
+                    tc::tmem_ld32_wait(d_lane + (uint32_t)ch * 32u, v);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
+                    for (int j = 0; j < 16; ++j) {
                         const __nv_bfloat162 b =
                             __floats2bfloat162_rn(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-                        packed[ch * 8 + j] = *reinterpret_cast<const uint32_t*>(&b);
+                        packed[ch * 16 + j] = *reinterpret_cast<const uint32_t*>(&b);
                     }
                 }
             }
@@ -606,15 +557,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(sm.d_empty());
             if (n < p.N) {
-                unsigned short* yc = static_cast<unsigned short*>(p.y) + n;
+                unsigned short* yc = reinterpret_cast<unsigned short*>(p.y) + n;
 #pragma unroll
-                for (int ch = 0; ch < 16; ++ch) {
-                    if (ch * 16 < U.bn) {
+                for (int ch = 0; ch < 8; ++ch) {
+                    if (ch * 32 < p.BN) {
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int m = U.m0 + ch * 16 + j;
+                        for (int j = 0; j < 32; ++j) {
+                            const int m = m0 + ch * 32 + j;
                             if (m < p.M) {
-                                const uint32_t pr = packed[ch * 8 + (j >> 1)];
+                                const uint32_t pr = packed[ch * 16 + (j >> 1)];
                                 yc[(int64_t)m * p.N] = (unsigned short)((j & 1) ? (pr >> 16) : (pr & 0xFFFFu));
                             }
                         }
@@ -634,11 +585,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 // per-input-channel multiplier xsc [K] (null: none), x_k * xsc_k is formed in
 // FP32 and rounded to FP16 once.  The output has kvec = K / 8 vectors per row;
 // the input rows have kxvec = kx / 8, and output channel k reads input channel
-// k mod kx (kx = K, or K / 2 for a layer over x repeated twice).
+// k mod kx (kx = K, or K / 2 for a layer over x repeated twice).  Block 0 also
+// clears ncnt arrival counters (the launch is stream-ordered before the
+// layer kernels that count on them).
 __global__ void __launch_bounds__(256) bf16_to_f16_kernel(const uint4* __restrict__ x, uint4* __restrict__ out,
                                                           int64_t nvec, const float4* __restrict__ xsc,
-                                                          int64_t kvec, int64_t kxvec) {
+                                                          int64_t kvec, int64_t kxvec, uint32_t* __restrict__ cnt,
+                                                          int ncnt) {
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    if (blockIdx.x == 0)   // the K-split arrival counters of the call's layer launches start at zero
+        for (int i = threadIdx.x; i < ncnt; i += blockDim.x) cnt[i] = 0u;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
         int64_t src = i, kv = 0;                 // input vector; its channel vector (when needed)
         if (kxvec != kvec || xsc != nullptr) {
@@ -673,7 +629,8 @@ __global__ void __launch_bounds__(256) bf16_to_f16_kernel(const uint4* __restric
 // ---- host side -----------------------------------------------------------------
 
 template <int G, bool W8>
-cudaError_t launch_g(const CUtensorMap* tm, const GemmParams& p, int grid, size_t smem, int dev, cudaStream_t stream) {
+cudaError_t launch_g(const CUtensorMap& tmx, const CUtensorMap& tmq, const GemmParams& p, int grid, size_t smem,
+                     int dev, cudaStream_t stream) {
     // largest dynamic shared memory this instance is already allowed per device (a raise may
     // race with another thread's: both set the attribute, the larger value stays)
     static std::atomic<int> cached[kMaxDevices];
@@ -685,75 +642,40 @@ cudaError_t launch_g(const CUtensorMap* tm, const GemmParams& p, int grid, size_
         while (have < (int)smem && !cached[dev].compare_exchange_weak(have, (int)smem)) {
         }
     }
-    gemm_kernel<G, W8><<<grid, kThreads, smem, stream>>>(tm[0], tm[1], tm[2], tm[3], tm[4], p);
+    gemm_kernel<G, W8><<<grid, kThreads, smem, stream>>>(tmx, tmq, p);
     return cudaGetLastError();
 }
 
-// Converts x (BF16 [M, kx]) into the FP16 B operand x16 [M, K] (see bf16_to_f16_kernel).
+// Converts x (BF16 [M, kx]) into the FP16 B operand x16 [M, K] and clears the
+// call's ncnt arrival counters (see bf16_to_f16_kernel).
 cudaError_t convert_x(const void* x, void* x16, int64_t M, int64_t K, int64_t kx, const float* xsc, int sms,
-                      cudaStream_t stream) {
+                      uint32_t* cnt, int ncnt, cudaStream_t stream) {
     const int64_t nvec = M * K / 8;
     int64_t blocks = (nvec + 255) / 256;
     if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
     bf16_to_f16_kernel<<<(unsigned)blocks, 256, 0, stream>>>(static_cast<const uint4*>(x), static_cast<uint4*>(x16),
                                                              nvec, reinterpret_cast<const float4*>(xsc), K / 8,
-                                                             kx / 8);
+                                                             kx / 8, cnt, ncnt);
     return cudaGetLastError();
 }
 
-// Ring depths for BN activation rows: the x ring up to 160 KB (4..8 slices), the
-// code ring (2..6 stages) in what shared memory has left.
-void choose_rings(int BN, size_t cap, int& xs, int& cs) {
-    const long long xslot = (long long)BN * 128;
-    xs = (int)std::min<long long>(kMaxXS, std::max<long long>(4, (160 * 1024) / xslot));
-    const long long fixed = 1024 + kNumBars * 8 + 16;
-    long long rem = (long long)cap - fixed - xs * xslot;
-    cs = (int)std::min<long long>(kMaxCS, rem / kCodeStageBytes);
-    while (cs < 2 && xs > 2) {
-        --xs;
-        rem += xslot;
-        cs = (int)std::min<long long>(kMaxCS, rem / kCodeStageBytes);
-    }
-}
-
-// Work split.  With T tiles on `sms` SMs the whole waves run whole tiles; the
-// R tiles that would leave the last wave part-empty are cut into pieces.
-//   BN > 64 (large M): along the activation rows, s = 2 or 4 pieces of BN / s
-//     rows over all of K, as many as one wave holds (R s <= sms).  No partial
-//     sums; each piece expands its tile's weights again, which the tensor pipe
-//     has time for at this width.
-//   BN <= 64 (small M, where a tile's time is its weight streaming and
-//     expansion): along K, into s ranges of the nk 256-k slices, s chosen to
-//     minimise an estimate in slice times: the waves of pieces times their
-//     length plus about 0.1 slice per piece for its partial and the final
-//     reduction.  Among estimates within 1 % of the best the smallest s wins.
-void choose_split(int T, int nk, int BN, int sms, GemmParams& p) {
+// K split.  Narrow tiles (BN <= 64: small M, where a tile's time is its
+// weight streaming and expansion) that fill at most half the SMs are each cut
+// along K into s ranges of the nst code stages, s chosen to minimise an
+// estimate in stage times: the waves of pieces times their length, plus about
+// 0.1 stage per piece for its partial and the final reduction.  Among
+// estimates within 1 % of the best the smallest s wins.  Wider tiles, or
+// enough of them to fill the SMs, run whole.
+void choose_split(int T, int nst, int BN, int sms, GemmParams& p) {
     p.full = T;
     p.split = 0;
     p.parts = 1;
-    p.ksplit = 0;
-    p.bt = BN;
-    const int F = T / sms, R = T - F * sms;
-    if (R == 0) return;
-    if (BN > 64) {
-        int s = 1;
-        for (int c : {2, 4})
-            if (R * c <= sms && BN % (32 * c) == 0) s = c;
-        if (s > 1) {
-            p.full = T - R;
-            p.split = R;
-            p.parts = s;
-            p.bt = BN / s;
-        }
-        return;
-    }
-    if (nk < 2) return;
+    if (BN > 64 || 2 * T > sms || nst < 2) return;
     auto cost = [&](int c) {
-        if (c == 1) return (double)(F + 1) * nk;
-        const int waves = (R * c + sms - 1) / sms;
-        return (double)F * nk + waves * ((double)((nk + c - 1) / c) + 0.1) + 0.1 * c;
+        const int waves = (T * c + sms - 1) / sms;
+        return waves * ((double)((nst + c - 1) / c) + 0.1) + (c > 1 ? 0.1 * c : 0.0);
     };
-    const int smax = std::min(nk, 16);
+    const int smax = std::min(nst, 16);
     double best = cost(1);
     for (int c = 2; c <= smax; ++c) best = std::min(best, cost(c));
     int s = 1;
@@ -763,108 +685,96 @@ void choose_split(int T, int nk, int BN, int sms, GemmParams& p) {
             break;
         }
     if (s > 1) {
-        p.full = T - R;
-        p.split = R;
+        p.full = 0;
+        p.split = T;
         p.parts = s;
-        p.ksplit = 1;
     }
 }
 
-// Everything about one call but its pointers: tiles, rings, schedule, grid, shared memory.
+// Everything about one matrix's launch but its pointers.
 struct GemmPlan {
     GemmParams p;
     int grid;
     size_t smem;
-    size_t ws_bytes;    // split partials + arrival counters (0: no split)
+    size_t ws_bytes;    // K-split partials (0: no split)
 };
 
-bool plan_gemm(int64_t M, int64_t N, int64_t K, int G, const DeviceInfo& di, bool allow_split, GemmPlan& pl) {
+bool plan_gemm(int64_t M, int64_t N, int64_t K, int G, bool w8, const DeviceInfo& di, bool allow_split,
+               GemmPlan& pl) {
     GemmParams& p = pl.p;
     p = GemmParams{};
     p.M = (int)M;
     p.N = (int)N;
     p.K = (int)K;
     p.BN = gemm_tile_n(M);
+    p.lds = (int)scales_ld(K, G);
+    p.ldz = (int)(w8 ? zeros8_ld(K, G) : zeros_ld(K, G));
     p.ngroups = (int)(K / G);
     p.mtiles = (int)((M + p.BN - 1) / p.BN);
     const int64_t tiles = ((N + kBM - 1) / kBM) * p.mtiles;
     if (tiles > (1 << 24)) return false;
     p.tiles = (int)tiles;
     p.nk64 = (int)((K + 63) / 64);
-    p.nk256 = (int)((K + 255) / 256);
-    choose_rings(p.BN, di.smem_optin, p.xs, p.cs);
-    if (p.cs < 2 || p.xs < 2) return false;
-    choose_split(p.tiles, p.nk256, p.BN, di.sms, p);
-    if (!allow_split && p.ksplit) {           // no workspace: whole tiles only
-        p.full = p.tiles;
-        p.split = 0;
-        p.parts = 1;
-        p.ksplit = 0;
-        p.bt = p.BN;
-    }
+    p.subs = w8 ? 2 : 4;
+    p.nstage = (p.nk64 + p.subs - 1) / p.subs;
+    if (allow_split) choose_split(p.tiles, p.nstage, p.BN, di.sms, p);
+    else choose_split(p.tiles, 1, p.BN, di.sms, p);           // whole tiles only
     p.units = p.full + p.split * p.parts;
     pl.grid = p.units < di.sms ? p.units : di.sms;
-    pl.smem = gemm_smem_bytes(p.BN, p.xs, p.cs);
-    pl.ws_bytes = p.ksplit ? (size_t)p.split * p.parts * p.BN * kBM * 4 + (size_t)p.split * 4 : 0;
+    pl.smem = gemm_smem_bytes(p.BN);
+    pl.ws_bytes = p.split ? (size_t)p.split * p.parts * p.BN * kBM * 4 : 0;
     p.spin_limit = wait_limit();
     return pl.smem <= di.smem_optin;
 }
 
-// Launches one matrix: maps of x16, codes, scales and zeros, then the kernel.
-// ws: the call's workspace (pl.ws_bytes), its counters cleared on the stream first.
-cudaError_t launch_one(const void* x16, const GemvMat& mat, const GemmPlan& pl, int G, bool w8, void* ws, int dev,
-                       cudaStream_t stream) {
-    const GemmParams& p0 = pl.p;
-    const uint64_t K = (uint64_t)p0.K, N = (uint64_t)p0.N;
-    const uint64_t ldq = w8 ? K / 4 : K / 8;
-    const uint64_t lds = (uint64_t)scales_ld(K, G), ldz = (uint64_t)(w8 ? zeros8_ld(K, G) : zeros_ld(K, G));
-    // x with boxes of BN rows (whole tiles, K ranges) and of bt rows (activation-row pieces),
-    // codes, scales and zeros
-    CUtensorMap tm[5];
-    if (!encode_tmap_2d(&tm[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x16, K, (uint64_t)p0.M, K * 2, 64,
-                        (uint32_t)p0.BN, dev) ||
-        !encode_tmap_2d(&tm[1], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x16, K, (uint64_t)p0.M, K * 2, 64,
-                        (uint32_t)p0.bt, dev) ||
-        !encode_tmap_2d(&tm[2], CU_TENSOR_MAP_DATA_TYPE_UINT32, mat.q, ldq, N, ldq * 4, 32, kBM, dev) ||
-        !encode_tmap_2d(&tm[3], CU_TENSOR_MAP_DATA_TYPE_UINT16, mat.s, lds, N, lds * 2, 8, kBM, dev, false) ||
-        !encode_tmap_2d(&tm[4], CU_TENSOR_MAP_DATA_TYPE_UINT32, mat.z, ldz, N, ldz * 4, 4, kBM, dev, false))
+// Launches one matrix: the map of its codes, then the kernel.  ws: the call's
+// K-split partials; cnt: this matrix's arrival counters (cleared by the conversion).
+cudaError_t launch_one(const CUtensorMap& tmx, const GemvMat& mat, const GemmPlan& pl, int G, bool w8, void* ws,
+                       uint32_t* cnt, int dev, cudaStream_t stream) {
+    const uint64_t ldq = (uint64_t)(w8 ? pl.p.K / 4 : pl.p.K / 8);
+    CUtensorMap tmq;
+    if (!encode_tmap_2d(&tmq, CU_TENSOR_MAP_DATA_TYPE_UINT32, mat.q, ldq, (uint64_t)pl.p.N, ldq * 4, 32, kBM, dev))
         return cudaErrorInvalidValue;
-    GemmParams p = p0;
+    GemmParams p = pl.p;
     p.withhold = take_withhold(2) ? 1 : 0;
+    p.s = static_cast<const unsigned short*>(mat.s);
+    p.z = mat.z;
     p.y = mat.y;
-    if (p.ksplit) {
-        p.ws = static_cast<float*>(ws);
-        p.cnt = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + (size_t)p.split * p.parts * p.BN * kBM * 4);
-        const cudaError_t e = cudaMemsetAsync(p.cnt, 0, (size_t)p.split * 4, stream);
-        if (e != cudaSuccess) return e;
-    }
+    p.ws = static_cast<float*>(ws);
+    p.cnt = cnt;
     if (w8) {
         switch (G) {
-            case 32: return launch_g<32, true>(tm, p, pl.grid, pl.smem, dev, stream);
-            case 64: return launch_g<64, true>(tm, p, pl.grid, pl.smem, dev, stream);
-            case 128: return launch_g<128, true>(tm, p, pl.grid, pl.smem, dev, stream);
-            case 256: return launch_g<256, true>(tm, p, pl.grid, pl.smem, dev, stream);
+            case 32: return launch_g<32, true>(tmx, tmq, p, pl.grid, pl.smem, dev, stream);
+            case 64: return launch_g<64, true>(tmx, tmq, p, pl.grid, pl.smem, dev, stream);
+            case 128: return launch_g<128, true>(tmx, tmq, p, pl.grid, pl.smem, dev, stream);
+            case 256: return launch_g<256, true>(tmx, tmq, p, pl.grid, pl.smem, dev, stream);
             default: return cudaErrorInvalidValue;
         }
     }
     switch (G) {
-        case 32: return launch_g<32, false>(tm, p, pl.grid, pl.smem, dev, stream);
-        case 64: return launch_g<64, false>(tm, p, pl.grid, pl.smem, dev, stream);
-        case 128: return launch_g<128, false>(tm, p, pl.grid, pl.smem, dev, stream);
-        case 256: return launch_g<256, false>(tm, p, pl.grid, pl.smem, dev, stream);
+        case 32: return launch_g<32, false>(tmx, tmq, p, pl.grid, pl.smem, dev, stream);
+        case 64: return launch_g<64, false>(tmx, tmq, p, pl.grid, pl.smem, dev, stream);
+        case 128: return launch_g<128, false>(tmx, tmq, p, pl.grid, pl.smem, dev, stream);
+        case 256: return launch_g<256, false>(tmx, tmq, p, pl.grid, pl.smem, dev, stream);
         default: return cudaErrorInvalidValue;
     }
+}
+
+bool encode_x_map(CUtensorMap* tmx, const void* x16, int64_t M, int64_t K, int BN, int dev) {
+    return encode_tmap_2d(tmx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x16, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, 64,
+                          (uint32_t)BN, dev);
 }
 
 }  // namespace
 
 int gemm_tile_n(int64_t M) { return M >= 256 ? 256 : (int)((M + 31) / 32 * 32); }
 
-// The FP16 copy of x and the split workspace are taken from the device's
-// current memory pool with one stream-ordered allocation and freed on the
-// stream after the call's kernels.  The library keeps no pool or cache of its
-// own: what stays reserved between calls is that pool's policy (its release
-// threshold), which belongs to the application.
+// The FP16 copy of x, the K-split partials and the arrival counters are taken
+// from the device's current memory pool with one stream-ordered allocation and
+// freed on the stream after the call's kernels.  The library keeps no pool or
+// cache of device memory of its own: what stays reserved between calls is
+// that pool's policy (its release threshold), which belongs to the
+// application.
 cudaError_t launch_gemm(const void* x, const GemvMat* mats, int nmat, int64_t M, int64_t N, int64_t K, int G,
                         cudaStream_t stream, const float* xsc, int64_t kx, bool yf32, bool w8) {
     if (kx == 0) kx = K;
@@ -878,18 +788,26 @@ cudaError_t launch_gemm(const void* x, const GemvMat* mats, int nmat, int64_t M,
     if (e != cudaSuccess) return e;
     GemmPlan pl[kMaxMat];
     size_t ws_bytes = 0;
+    int ncnt = 0, cnt0[kMaxMat];
     for (int i = 0; i < nmat; ++i) {
         const int64_t Ni = mats[i].n > 0 ? mats[i].n : N;     // every matrix's rows: its own n, else N
-        if (Ni < 1 || Ni > INT32_MAX || !plan_gemm(M, Ni, K, G, di, true, pl[i])) return cudaErrorInvalidValue;
+        if (Ni < 1 || Ni > INT32_MAX || !plan_gemm(M, Ni, K, G, w8, di, true, pl[i])) return cudaErrorInvalidValue;
         pl[i].p.yf32 = yf32 ? 1 : 0;
-        ws_bytes = std::max(ws_bytes, pl[i].ws_bytes);
+        ws_bytes = std::max(ws_bytes, pl[i].ws_bytes);        // the launches run one after another
+        cnt0[i] = ncnt;
+        ncnt += pl[i].p.split;
     }
     const size_t xbytes = ((size_t)M * (size_t)K * 2 + 255) / 256 * 256;
+    const size_t wbytes = (ws_bytes + 255) / 256 * 256;
     void* buf = nullptr;
-    if ((e = cudaMallocAsync(&buf, xbytes + ws_bytes, stream)) != cudaSuccess) return e;
-    e = convert_x(x, buf, M, K, kx, xsc, di.sms, stream);
+    if ((e = cudaMallocAsync(&buf, xbytes + wbytes + (size_t)ncnt * 4, stream)) != cudaSuccess) return e;
+    uint8_t* ws = static_cast<uint8_t*>(buf) + xbytes;
+    uint32_t* cnt = reinterpret_cast<uint32_t*>(ws + wbytes);
+    CUtensorMap tmx;
+    if (!encode_x_map(&tmx, buf, M, K, pl[0].p.BN, di.dev)) e = cudaErrorInvalidValue;
+    if (e == cudaSuccess) e = convert_x(x, buf, M, K, kx, xsc, di.sms, cnt, ncnt, stream);
     for (int i = 0; i < nmat && e == cudaSuccess; ++i)
-        e = launch_one(buf, mats[i], pl[i], G, w8, static_cast<uint8_t*>(buf) + xbytes, di.dev, stream);
+        e = launch_one(tmx, mats[i], pl[i], G, w8, ws, cnt + cnt0[i], di.dev, stream);
     const cudaError_t ef = cudaFreeAsync(buf, stream);
     return e != cudaSuccess ? e : ef;
 }
@@ -903,9 +821,9 @@ cudaError_t launch_gemm(const void* x, const GemvMat* mats, int nmat, int64_t M,
 // out-of-memory error.  For them the FP16 copy of x lives in one file-scope
 // device array of fixed size instead of a stream-ordered allocation, and the
 // work is never split along K (a split needs a workspace).  Every GPU that
-// loads the library holds this array until the process exits.  All calls
-// share it, so two calls whose kernels overlap on the GPU (different streams,
-// no ordering between them) race on its contents.
+// loads the library holds this array until the process exits.  All
+// calls share it, so two calls whose kernels overlap on the GPU (different
+// streams, no ordering between them) race on its contents.
 constexpr size_t kNoAllocScratchBytes = (size_t)W4A16_NOALLOC_MAX_X_ELEMS * 2;
 static __device__ __align__(256) uint8_t g_noalloc_x16[kNoAllocScratchBytes];
 
@@ -937,10 +855,12 @@ cudaError_t launch_gemm_noalloc(const void* x, const GemvMat& mat, int64_t M, in
     void* x16 = nullptr;
     if ((e = noalloc_scratch(di.dev, &x16)) != cudaSuccess) return e;
     GemmPlan pl;
-    if (!plan_gemm(M, N, K, G, di, false, pl)) return cudaErrorInvalidValue;
+    CUtensorMap tmx;
+    if (!plan_gemm(M, N, K, G, false, di, false, pl) || !encode_x_map(&tmx, x16, M, K, pl.p.BN, di.dev))
+        return cudaErrorInvalidValue;
     // every element of the array this call reads is written first by the conversion
-    if ((e = convert_x(x, x16, M, K, K, nullptr, di.sms, stream)) != cudaSuccess) return e;
-    return launch_one(x16, mat, pl, G, false, nullptr, di.dev, stream);
+    if ((e = convert_x(x, x16, M, K, K, nullptr, di.sms, nullptr, 0, stream)) != cudaSuccess) return e;
+    return launch_one(tmx, mat, pl, G, false, nullptr, nullptr, di.dev, stream);
 }
 
 cudaError_t read_and_clear_status(uint32_t* word) {

@@ -83,7 +83,6 @@ constexpr int kSlots = 4;                 // partial-sum slots per output (warps
 // expand_codes8_f16), so the MMA sums x (2048 + b) exactly.
 constexpr int kFmt4 = 0, kFmtQ4K = 1, kFmt8 = 2;
 constexpr uint32_t kStatusGemv = 1u << 8;
-constexpr int64_t kPrefetchBytesPerCta = 512 * 1024;   // L2 prefetch at entry up to this many weight bytes per CTA
 constexpr uint32_t kStatusGemvDrain = 1u << 9;
 
 // MMA row i (< 8) of a warp reads virtual row sigma(i) = i/2 + 4*(i%2) of the
@@ -98,11 +97,9 @@ struct GemvParams {
     int kx;                                // row length of x: channel k reads x[k mod kx] (kx = K or K/2)
     // per matrix (up to kMaxMat sharing x): FP16 scales [n, lds] (KQ: super-block records, 8
     // halves each), zeros [n, ldz] (KQ: unused, ldz = 0), output [M, n] BF16 (or FP32 when yf32)
-    const uint32_t* q[kMaxMat];            // packed codes (read through the tensor maps; used for L2 prefetch)
     const unsigned short* s[kMaxMat];
     const uint32_t* z[kMaxMat];
     void* y[kMaxMat];
-    int prefetch;                          // 1: ask L2 for this CTA's weights before the grid dependency wait
     int n[kMaxMat];                        // rows (outputs) of each matrix
     int tstart[kMaxMat + 1];               // first tile of each matrix; total_tiles from nmat on
     int yf32;                              // 1: FP32 outputs (no BF16 rounding)
@@ -199,13 +196,21 @@ __device__ __forceinline__ float4 lds_f4(uint32_t addr) {
     return v;
 }
 
-// Matrix that tile tau belongs to (tiles are numbered matrix after matrix).
+// Matrix that tile tau belongs to (tiles are numbered matrix after matrix; an
+// instance takes up to NM matrices).
+template <int NM>
 __device__ __forceinline__ int mat_of(const GemvParams& p, int tau) {
     int m = 0;
 #pragma unroll
-    for (int i = 1; i < kMaxMat; ++i) m += tau >= p.tstart[i];
+    for (int i = 1; i < NM; ++i) m += tau >= p.tstart[i];
     return m;
 }
+
+// The code maps of up to NM matrices, one kernel parameter.
+template <int NM>
+struct CodeMaps {
+    CUtensorMap m[NM];
+};
 
 // Bounded wait on a barrier phase (gives up after `limit` cycles); the thread
 // sleeps between polls.
@@ -224,11 +229,10 @@ __device__ __forceinline__ bool gemv_wait(uint32_t bar, uint32_t parity, long lo
 // M1: one activation row with P >= 2 segments.  The B columns are then
 // (parity, segment) pairs and each lane holds at most one useful D value per
 // row, so the block-end correction is done once per row on that value only.
-template <int NB, int G, int H, bool M1, int PT, int FMT>
+// NM: matrices the instance takes (2 for one or two, 4 for three or four).
+template <int NB, int G, int H, bool M1, int PT, int FMT, int NM>
 __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
-    gemv_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
-                const __grid_constant__ CUtensorMap tm2, const __grid_constant__ CUtensorMap tm3,
-                const GemvParams p) {
+    gemv_kernel(const __grid_constant__ CodeMaps<NM> tm, const GemvParams p) {
     constexpr int V = G >= 128 ? 4 : G / 32;      // words per lane per code load
     constexpr int GPC = 256 / G;                  // groups per chunk (H divides it)
     constexpr int WSG = G / 32;                   // word steps per group
@@ -272,20 +276,23 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
     }
     // test hook: warp 0 of CTA 0 never issues its first unit, so its wait on it runs out
     const bool withhold = p.withhold && blockIdx.x == 0 && warp == 0;
-    auto issue_next = [&]() {
+    // copy = false (the test hook only) advances past a unit without issuing its copies
+    auto issue_next = [&](bool copy) {
         const int tau = tile0 + it_tl;
-        const int mat = mat_of(p, tau);
+        const int mat = mat_of<NM>(p, tau);
         const int tile = tau - p.tstart[mat];
         const uint32_t slot = (uint32_t)(it_n & (nsl - 1));
         const uint32_t bar = bar0 + 8u * slot;
         const bool two = it_c + 1 < p.C && it_ch + 1 < ch1;
-        if (!(withhold && it_n == 0)) {
+        if (copy) {
             tc::mbar_arrive_expect_tx(bar, (uint32_t)(two ? 2 * kBoxBytes : kBoxBytes));
-            const void* tm = mat == 0 ? (const void*)&tm0 : mat == 1 ? (const void*)&tm1
-                           : mat == 2 ? (const void*)&tm2 : (const void*)&tm3;
-            tc::tma_load_2d(ring + slot * (uint32_t)kUnitBytes, tm, it_c * 32, tile * 16, bar);
+            const void* map = &tm.m[0];
+#pragma unroll
+            for (int i = 1; i < NM; ++i)
+                if (mat == i) map = &tm.m[i];
+            tc::tma_load_2d(ring + slot * (uint32_t)kUnitBytes, map, it_c * 32, tile * 16, bar);
             if (two)
-                tc::tma_load_2d(ring + slot * (uint32_t)kUnitBytes + kBoxBytes, tm, (it_c + 1) * 32, tile * 16, bar);
+                tc::tma_load_2d(ring + slot * (uint32_t)kUnitBytes + kBoxBytes, map, (it_c + 1) * 32, tile * 16, bar);
         }
         const int n = two ? 2 : 1;
         ++it_n;
@@ -307,25 +314,6 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
     // scheduled at once (its CTAs take SMs as this grid's CTAs exit), and this grid reads no
     // global memory before the previous grid on the stream has completed.
     tc::griddep_launch_dependents();
-    if (p.prefetch && tid == 0) {
-        // A layer this small is dominated by latency: ask L2 for the CTA's codes and metadata
-        // rows now, while the previous grid may still be running.  A prefetch returns nothing to
-        // the program and L2 is the point of coherence, so this reads nothing before the grid
-        // dependency wait below; the copies after it find the data in L2.
-#pragma unroll 1
-        for (int i = 0; i < kMaxMat; ++i) {
-            const int a = max(tile0, p.tstart[i]), b = min(tile1, p.tstart[i + 1]);
-            if (b <= a) continue;
-            const int64_t r0 = (int64_t)(a - p.tstart[i]) * R;
-            const int64_t rows = min((int64_t)(b - a) * R, (int64_t)p.n[i] - r0);
-            if (rows <= 0) continue;
-            const uint8_t* cq = reinterpret_cast<const uint8_t*>(p.q[i]) + r0 * (p.K / 2);
-            for (int64_t off = 0, tot = rows * (p.K / 2); off < tot; off += 1 << 16)
-                tc::prefetch_l2(cq + off, (uint32_t)(tot - off < (1 << 16) ? tot - off : (1 << 16)));
-            tc::prefetch_l2(p.s[i] + r0 * p.lds, (uint32_t)(rows * p.lds * 2));
-            if (!KQ) tc::prefetch_l2(p.z[i] + r0 * p.ldz, (uint32_t)(rows * p.ldz * 4));
-        }
-    }
     const uint32_t pbar = sbase + L.bars + 8u * (uint32_t)(kWarps * nsl);
     bool pro_ok = true;                           // the prologue's copies landed (warp-uniform)
     if (tid == 0) {
@@ -341,11 +329,11 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
         // n are bulk-copied (they are contiguous in the matrix), the rest zero-filled below
         const uint32_t sbytes = (uint32_t)p.lds * 2u, zbytes = (uint32_t)p.ldz * 4u;   // per row
         const uint32_t ms = sbase + L.ms, mz = sbase + L.mz;
-        int cl[kMaxMat], cc[kMaxMat];                  // local first row and rows copied, per matrix
-        int gs[kMaxMat + 1], gn[kMaxMat + 1];          // rows left to zero-fill: first, count
+        int cl[NM], cc[NM];                            // local first row and rows copied, per matrix
+        int gs[NM + 1], gn[NM + 1];                    // rows left to zero-fill: first, count
         int copied = 0, gaps = 0;
 #pragma unroll
-        for (int i = 0; i < kMaxMat; ++i) {
+        for (int i = 0; i < NM; ++i) {
             const int a = max(tile0, p.tstart[i]), b = min(tile1, p.tstart[i + 1]);
             cl[i] = (a - tile0) * R;
             cc[i] = b > a ? max(0, min((b - a) * R, p.n[i] - (a - p.tstart[i]) * R)) : 0;
@@ -354,13 +342,13 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
             copied += cc[i];
             gaps += gn[i];
         }
-        gs[kMaxMat] = tc_ * R;                           // rows past the CTA's tiles
-        gn[kMaxMat] = p.rows_cap - tc_ * R;
-        gaps += gn[kMaxMat];
+        gs[NM] = tc_ * R;                                // rows past the CTA's tiles
+        gn[NM] = p.rows_cap - tc_ * R;
+        gaps += gn[NM];
         if (tid == 0) {
             tc::mbar_arrive_expect_tx(pbar, (uint32_t)copied * (sbytes + zbytes));
 #pragma unroll
-            for (int i = 0; i < kMaxMat; ++i) {
+            for (int i = 0; i < NM; ++i) {
                 if (cc[i] <= 0) continue;
                 const int64_t r0 = (int64_t)(max(tile0, p.tstart[i]) - p.tstart[i]) * R;    // first row
                 tc::bulk_load(ms + (uint32_t)cl[i] * sbytes, p.s[i] + r0 * p.lds, (uint32_t)cc[i] * sbytes, pbar);
@@ -485,7 +473,7 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
                 int k = i / per, lr = 0;
                 const int col = i - k * per;
 #pragma unroll
-                for (int j = 0; j <= kMaxMat; ++j) {       // the k-th row of the gap ranges
+                for (int j = 0; j <= NM; ++j) {            // the k-th row of the gap ranges
                     if (k >= 0 && k < gn[j]) lr = gs[j] + k;
                     k -= gn[j];
                 }
@@ -509,7 +497,7 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
         // it filled from here on
         pro_ok = __all_sync(0xFFFFFFFFu, gemv_wait(pbar, 0, p.spin_limit));
         if (pro_ok && active && lane == 0) {
-            for (int i = 0; i < nsl && it_ch < ch1; ++i) issue_next();
+            for (int i = 0; i < nsl && it_ch < ch1; ++i) issue_next(!(withhold && i == 0));
         }
         for (;;) {
             x_stage();
@@ -832,7 +820,7 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
                 __syncwarp();
                 if (lane == 0 && it_ch < ch1) {
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    issue_next();
+                    issue_next(true);
                 }
                 ch += n;
                 cu += n;
@@ -875,7 +863,7 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
             const int rl = i / p.M, m = i - rl * p.M;
             const int tl2 = rl / R, rho = rl - tl2 * R;
             const int tau = tile0 + tl2;
-            const int mat = mat_of(p, tau);
+            const int mat = mat_of<NM>(p, tau);
             const int row = (tau - p.tstart[mat]) * R + rho;
             if (row >= p.n[mat]) continue;
             float sum = 0.0f;
@@ -996,14 +984,14 @@ bool make_plan(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G, int sms
     return false;
 }
 
-template <int NB, int G, int H, bool M1, int PT, int FMT>
+template <int NB, int G, int H, bool M1, int PT, int FMT, int NM>
 cudaError_t launch_m(const CUtensorMap* tm, const Plan& pl, int dev, cudaStream_t stream) {
     // largest dynamic shared memory this instance is already allowed per device (a raise may
     // race with another thread's: both set the attribute, the larger value stays)
     static std::atomic<int> cached[kMaxDevices];
     int have = cached[dev].load(std::memory_order_relaxed);
     if ((int)pl.smem > have) {
-        const cudaError_t e = cudaFuncSetAttribute(gemv_kernel<NB, G, H, M1, PT, FMT>,
+        const cudaError_t e = cudaFuncSetAttribute(gemv_kernel<NB, G, H, M1, PT, FMT, NM>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
         if (e != cudaSuccess) return e;
         while (have < (int)pl.smem && !cached[dev].compare_exchange_weak(have, (int)pl.smem)) {
@@ -1020,49 +1008,51 @@ cudaError_t launch_m(const CUtensorMap* tm, const Plan& pl, int dev, cudaStream_
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<NB, G, H, M1, PT, FMT>, tm[0], tm[1], tm[2], tm[3], pl.p);
+    CodeMaps<NM> maps;
+    for (int i = 0; i < NM; ++i) maps.m[i] = tm[i];
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<NB, G, H, M1, PT, FMT, NM>, maps, pl.p);
 }
 
-template <int NB, int G, int H, int FMT>
+template <int NB, int G, int H, int FMT, int NM>
 cudaError_t launch_t(const CUtensorMap* tm, const Plan& pl, int dev, cudaStream_t stream) {
     if constexpr (NB == 1) {
         if (m1_kernel(pl.p)) {                       // M = 1: the segment count is a template constant
             switch (pl.p.P) {
-                case 2: return launch_m<NB, G, H, true, 2, FMT>(tm, pl, dev, stream);
-                case 4: return launch_m<NB, G, H, true, 4, FMT>(tm, pl, dev, stream);
-                case 8: return launch_m<NB, G, H, true, 8, FMT>(tm, pl, dev, stream);
+                case 2: return launch_m<NB, G, H, true, 2, FMT, NM>(tm, pl, dev, stream);
+                case 4: return launch_m<NB, G, H, true, 4, FMT, NM>(tm, pl, dev, stream);
+                case 8: return launch_m<NB, G, H, true, 8, FMT, NM>(tm, pl, dev, stream);
             }
             return cudaErrorInvalidValue;
         }
     }
-    return launch_m<NB, G, H, false, 0, FMT>(tm, pl, dev, stream);
+    return launch_m<NB, G, H, false, 0, FMT, NM>(tm, pl, dev, stream);
 }
 
-template <int NB, int G, int FMT = kFmt4>
+template <int NB, int G, int FMT = kFmt4, int NM = 2>
 cudaError_t launch_h(const CUtensorMap* tm, const Plan& pl, int dev, cudaStream_t stream) {
     if constexpr (NB == 2) {
-        return launch_t<NB, G, 1, FMT>(tm, pl, dev, stream);
+        return launch_t<NB, G, 1, FMT, NM>(tm, pl, dev, stream);
     } else {
         switch (pl.H) {
-            case 1: return launch_t<NB, G, 1, FMT>(tm, pl, dev, stream);
+            case 1: return launch_t<NB, G, 1, FMT, NM>(tm, pl, dev, stream);
             case 2:
-                if constexpr (256 / G >= 2) return launch_t<NB, G, 2, FMT>(tm, pl, dev, stream);
+                if constexpr (256 / G >= 2) return launch_t<NB, G, 2, FMT, NM>(tm, pl, dev, stream);
                 break;
             case 4:
-                if constexpr (256 / G >= 4) return launch_t<NB, G, 4, FMT>(tm, pl, dev, stream);
+                if constexpr (256 / G >= 4) return launch_t<NB, G, 4, FMT, NM>(tm, pl, dev, stream);
                 break;
         }
         return cudaErrorInvalidValue;
     }
 }
 
-template <int NB>
+template <int NB, int NM>
 cudaError_t launch_nb(const CUtensorMap* tm, const Plan& pl, int dev, cudaStream_t stream) {
     switch (pl.p.G) {
-        case 32: return launch_h<NB, 32>(tm, pl, dev, stream);
-        case 64: return launch_h<NB, 64>(tm, pl, dev, stream);
-        case 128: return launch_h<NB, 128>(tm, pl, dev, stream);
-        case 256: return launch_h<NB, 256>(tm, pl, dev, stream);
+        case 32: return launch_h<NB, 32, kFmt4, NM>(tm, pl, dev, stream);
+        case 64: return launch_h<NB, 64, kFmt4, NM>(tm, pl, dev, stream);
+        case 128: return launch_h<NB, 128, kFmt4, NM>(tm, pl, dev, stream);
+        case 256: return launch_h<NB, 256, kFmt4, NM>(tm, pl, dev, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -1098,7 +1088,8 @@ bool gemv_fits(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G, bool kq
 }
 
 bool gemv_fits(int64_t M, int64_t N, int64_t K, int G, int nmat, bool kq) {
-    const int64_t Ns[kMaxMat] = {N, N, N, N};
+    int64_t Ns[kMaxMat];
+    for (int i = 0; i < kMaxMat; ++i) Ns[i] = N;
     return gemv_fits(M, Ns, nmat, K, G, kq);
 }
 
@@ -1128,14 +1119,8 @@ cudaError_t launch_gemv(const void* x, const GemvMat* mats, int nmat, int64_t M,
     p.spin_limit = wait_limit();
     p.withhold = take_withhold(1) ? 1 : 0;
     CUtensorMap tm[kMaxMat];
-    // small layers: the CTA's weights are requested into L2 before the grid dependency wait
-    // (below this many bytes per CTA the launch is latency-bound rather than bandwidth-bound)
-    int64_t wbytes = 0;
-    for (int i = 0; i < nmat; ++i) wbytes += Ns[i] * (Kv / 2);
-    p.prefetch = wbytes / pl.grid <= kPrefetchBytesPerCta ? 1 : 0;
     for (int i = 0; i < kMaxMat; ++i) {
         const GemvMat& mt = mats[i < nmat ? i : 0];
-        p.q[i] = mt.q;
         p.s[i] = static_cast<const unsigned short*>(mt.s);
         p.z[i] = mt.z;
         p.y[i] = mt.y;
@@ -1145,9 +1130,13 @@ cudaError_t launch_gemv(const void* x, const GemvMat* mats, int nmat, int64_t M,
             tm[i] = tm[0];
         }
     }
+    // one or two matrices (kq, w8: always) run the two-map instances; three or four the four-map ones
+    if ((kq || w8) && nmat > 2) return cudaErrorInvalidValue;
     if (kq) return launch_h<1, 32, kFmtQ4K>(tm, pl, di.dev, stream);   // make_plan: M <= 8, one column block
     if (w8) return launch_w8(tm, pl, di.dev, stream);
-    return pl.nb == 1 ? launch_nb<1>(tm, pl, di.dev, stream) : launch_nb<2>(tm, pl, di.dev, stream);
+    if (nmat > 2)
+        return pl.nb == 1 ? launch_nb<1, 4>(tm, pl, di.dev, stream) : launch_nb<2, 4>(tm, pl, di.dev, stream);
+    return pl.nb == 1 ? launch_nb<1, 2>(tm, pl, di.dev, stream) : launch_nb<2, 2>(tm, pl, di.dev, stream);
 }
 
 }  // namespace w4a16
