@@ -63,13 +63,12 @@ namespace {
 
 constexpr int kThreads = 320;              // 10 warps
 constexpr int kBM = 128;                   // weight rows per tile (MMA M)
-constexpr int kXS = 5;                     // x ring: slices of 64 k
-constexpr int kCS = 3;                     // code ring: slices of 256 k
-constexpr int kAS = 8;                     // A ring in TMEM: slices of 64 k (32 columns)
+constexpr int kMaxS = 4;                   // slice ring: x (smem) and A (TMEM) slices of 128 k
+constexpr int kMaxCS = 3;                  // code ring: stages of 128 bytes of codes per row
 constexpr uint32_t kCodeStageBytes = 128u * 128u;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kACol0 = 256;           // D uses columns [0, BN), A slices [256, 512)
-constexpr int kNumBars = 2 * kXS + 2 * kCS + 2 * kAS + 2;
+constexpr uint32_t kACol0 = 256;           // D uses columns [0, BN), A slices (64 columns each) [256, 512)
+constexpr int kNumBars = 3 * kMaxS + 2 * kMaxCS + 2;
 
 // Status codes (bit fields) recorded when a wait gives up.
 constexpr uint32_t kStatusProducer = 1u << 0;
@@ -130,10 +129,20 @@ __device__ __forceinline__ Unit unit_of(const GemmParams& p, int u) {
     return U;
 }
 
+// Ring depths for BN activation rows.  A slice is 128 k: two 64-k x boxes (BN
+// rows of 128 bytes each) and 64 tensor-memory columns of A.  Four slices up
+// to BN = 128 (x slots of at most 32 KB, three code stages); at BN = 256 three
+// (192 KB of x, the most that leaves room for two code stages).  x slices come
+// from L2 with a latency of several slice times, so the x ring is as deep as
+// shared memory allows.
+__host__ __device__ constexpr int slice_slots(int BN) { return BN <= 128 ? 4 : 3; }
+__host__ __device__ constexpr int code_stages(int BN) { return BN <= 128 ? 3 : 2; }
+
 // Dynamic shared memory per CTA.  Never less than 120 KB, so at most one CTA
 // is resident per SM and the 512 tensor-memory columns it allocates are free.
 size_t gemm_smem_bytes(int BN) {
-    const size_t need = 1024 + (size_t)kXS * BN * 128 + (size_t)kCS * kCodeStageBytes + kNumBars * 8 + 16;
+    const size_t need = 1024 + (size_t)slice_slots(BN) * BN * 256 + (size_t)code_stages(BN) * kCodeStageBytes +
+                        kNumBars * 8 + 16;
     return need < 120 * 1024 ? 120 * 1024 : need;
 }
 
@@ -154,26 +163,28 @@ __device__ __forceinline__ uint32_t ldg32_nc(const void* p) {
 }
 
 struct Smem {
-    uint8_t* x;       // kXS slices of BN * 128 bytes
-    uint8_t* c;       // kCS slices of 16 KB
+    uint8_t* x;       // slice_slots(BN) slices of 2 x BN * 128 bytes
+    uint8_t* c;       // code_stages(BN) stages of 16 KB
     uint64_t* bar;
     uint32_t* tmem_slot;
     volatile int* abort_flag;
     volatile int* last_flag;   // epilogue: this CTA completes the split tile
+    // slice slot i: x_full (its x copy landed), a_full (its A slice written), s_empty (the MMAs
+    // that read both completed: one commit frees the x slot and the A slot)
     __device__ uint32_t x_full(int i) const { return tc::smem_u32(bar + i); }
-    __device__ uint32_t x_empty(int i) const { return tc::smem_u32(bar + kXS + i); }
-    __device__ uint32_t c_full(int i) const { return tc::smem_u32(bar + 2 * kXS + i); }
-    __device__ uint32_t c_empty(int i) const { return tc::smem_u32(bar + 2 * kXS + kCS + i); }
-    __device__ uint32_t a_full(int i) const { return tc::smem_u32(bar + 2 * kXS + 2 * kCS + i); }
-    __device__ uint32_t a_empty(int i) const { return tc::smem_u32(bar + 2 * kXS + 2 * kCS + kAS + i); }
-    __device__ uint32_t d_full() const { return tc::smem_u32(bar + 2 * kXS + 2 * kCS + 2 * kAS); }
-    __device__ uint32_t d_empty() const { return tc::smem_u32(bar + 2 * kXS + 2 * kCS + 2 * kAS + 1); }
+    __device__ uint32_t a_full(int i) const { return tc::smem_u32(bar + kMaxS + i); }
+    __device__ uint32_t s_empty(int i) const { return tc::smem_u32(bar + 2 * kMaxS + i); }
+    __device__ uint32_t c_full(int i) const { return tc::smem_u32(bar + 3 * kMaxS + i); }
+    __device__ uint32_t c_empty(int i) const { return tc::smem_u32(bar + 3 * kMaxS + kMaxCS + i); }
+    __device__ uint32_t d_full() const { return tc::smem_u32(bar + 3 * kMaxS + 2 * kMaxCS); }
+    __device__ uint32_t d_empty() const { return tc::smem_u32(bar + 3 * kMaxS + 2 * kMaxCS + 1); }
 };
 
 // Bounded wait for a barrier phase; gives up (recording `site`) after `limit`
-// cycles, or at once when another role has given up.
-__device__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint32_t site, long long limit) {
-    if (tc::mbar_try_wait(bar, parity)) return true;
+// cycles, or at once when another role has given up.  The first poll is
+// inline; the spin loop is a call, taken only when the phase is not complete.
+__device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint32_t site,
+                                             long long limit) {
     const long long t0 = clock64();
     while (true) {
         if (tc::mbar_try_wait(bar, parity)) return true;
@@ -184,6 +195,11 @@ __device__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_fl
             return false;
         }
     }
+}
+
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint32_t site,
+                                           long long limit) {
+    return tc::mbar_try_wait(bar, parity) || wait_phase_slow(bar, parity, abort_flag, site, limit);
 }
 
 // Bounded wait used while shutting down after a give-up: ignores the abort flag.
@@ -310,28 +326,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kSubs = W8 ? 2 : 4;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const uint32_t xbytes = (uint32_t)p.BN * 128u;
+    const uint32_t xhalf = (uint32_t)p.BN * 128u;      // one 64-k box of x
+    const uint32_t xbytes = 2u * xhalf;                 // a slice slot
     Smem sm;
     sm.x = base;
-    sm.c = base + kXS * xbytes;
-    sm.bar = reinterpret_cast<uint64_t*>(sm.c + kCS * kCodeStageBytes);
+    const int NS = slice_slots(p.BN), NC = code_stages(p.BN);
+    sm.c = base + NS * xbytes;
+    sm.bar = reinterpret_cast<uint64_t*>(sm.c + NC * kCodeStageBytes);
     sm.tmem_slot = reinterpret_cast<uint32_t*>(sm.bar + kNumBars);
     sm.abort_flag = reinterpret_cast<volatile int*>(sm.tmem_slot + 1);
     sm.last_flag = reinterpret_cast<volatile int*>(sm.tmem_slot + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kXS; ++i) {
+        for (int i = 0; i < NS; ++i) {
             tc::mbar_init(sm.x_full(i), 1);
-            tc::mbar_init(sm.x_empty(i), 1);
+            tc::mbar_init(sm.a_full(i), 4);
+            tc::mbar_init(sm.s_empty(i), 1);
         }
-        for (int i = 0; i < kCS; ++i) {
+        for (int i = 0; i < NC; ++i) {
             tc::mbar_init(sm.c_full(i), 1);
             tc::mbar_init(sm.c_empty(i), 4);
-        }
-        for (int i = 0; i < kAS; ++i) {
-            tc::mbar_init(sm.a_full(i), 4);
-            tc::mbar_init(sm.a_empty(i), 1);
         }
         tc::mbar_init(sm.d_full(), 1);
         tc::mbar_init(sm.d_empty(), 4);
@@ -363,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
                 const Unit U = unit_of(p, u);
                 const int n0 = (U.tile / p.mtiles) * kBM, m0 = (U.tile % p.mtiles) * p.BN;
-                for (int kb = U.kb0; kb < U.kb1; ++kb) {
+                for (int kb = U.kb0; kb < U.kb1; kb += 2) {      // slices of 128 k: 64-k boxes kb, kb+1
                     if ((kb & (kSubs - 1)) == 0) {
                         if (!(ok = wait_phase(sm.c_empty(ci), cph ^ 1u, sm.abort_flag, kStatusProducer, p.spin_limit))) break;
                         if (!(withhold && c_issued == 0)) {
@@ -372,28 +387,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             sm.c_full(ci));
                         }
                         ++c_issued;
-                        if (++ci == kCS) { ci = 0; cph ^= 1u; }
+                        if (++ci == NC) { ci = 0; cph ^= 1u; }
                     }
-                    if (!(ok = wait_phase(sm.x_empty(xi), xph ^ 1u, sm.abort_flag, kStatusProducer, p.spin_limit))) break;
-                    tc::mbar_arrive_expect_tx(sm.x_full(xi), xbytes);
+                    if (!(ok = wait_phase(sm.s_empty(xi), xph ^ 1u, sm.abort_flag, kStatusProducer, p.spin_limit))) break;
+                    const bool two = kb + 1 < U.kb1;
+                    tc::mbar_arrive_expect_tx(sm.x_full(xi), two ? xbytes : xhalf);
                     tc::tma_load_2d(tc::smem_u32(sm.x + xi * xbytes), &tm_x, kb * 64, m0, sm.x_full(xi));
+                    if (two)
+                        tc::tma_load_2d(tc::smem_u32(sm.x + xi * xbytes + xhalf), &tm_x, kb * 64 + 64, m0, sm.x_full(xi));
                     ++x_issued;
-                    if (++xi == kXS) { xi = 0; xph ^= 1u; }
+                    if (++xi == NS) { xi = 0; xph ^= 1u; }
                 }
             }
             if (!ok) {   // wait for the copies this thread started
-                for (int s = 0; s < kXS; ++s)
+                for (int s = 0; s < NS; ++s)
                     if (x_issued > s) drain_phase(sm.x_full(s), s < xi ? xph : (xph ^ 1u), p.spin_limit);
-                for (int s = 0; s < kCS; ++s)
-                    if (c_issued > s && !(withhold && s == 0 && c_issued <= kCS)) drain_phase(sm.c_full(s), s < ci ? cph : (cph ^ 1u), p.spin_limit);
+                for (int s = 0; s < NC; ++s)
+                    if (c_issued > s && !(withhold && s == 0 && c_issued <= NC)) drain_phase(sm.c_full(s), s < ci ? cph : (cph ^ 1u), p.spin_limit);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc = tc::idesc_f16_f32(kBM, p.BN);
-            int xi = 0, ai = 0;
-            uint32_t xph = 0, aph = 0, dph = 0, d_commits = 0;
+            int si = 0;
+            uint32_t sph = 0, dph = 0, d_commits = 0;
             bool ok = true;
             bool issued = false;
             for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
@@ -401,21 +419,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!(ok = wait_phase(sm.d_empty(), dph ^ 1u, sm.abort_flag, kStatusMma, p.spin_limit))) break;
                 dph ^= 1u;
                 tc::tc_fence_after();
-                for (int kb = U.kb0; kb < U.kb1; ++kb) {
-                    if (!(ok = wait_phase(sm.x_full(xi), xph, sm.abort_flag, kStatusMma, p.spin_limit))) break;
-                    if (!(ok = wait_phase(sm.a_full(ai), aph, sm.abort_flag, kStatusMma, p.spin_limit))) break;
+                for (int kb = U.kb0; kb < U.kb1; kb += 2) {
+                    if (!(ok = wait_phase(sm.x_full(si), sph, sm.abort_flag, kStatusMma, p.spin_limit))) break;
+                    if (!(ok = wait_phase(sm.a_full(si), sph, sm.abort_flag, kStatusMma, p.spin_limit))) break;
                     tc::tc_fence_after();
-                    const uint64_t bdesc = tc::smem_desc_k_sw128(tc::smem_u32(sm.x + xi * xbytes));
-                    const uint32_t a_t = tmem + kACol0 + (uint32_t)ai * 32u;
+                    const uint64_t bdesc0 = tc::smem_desc_k_sw128(tc::smem_u32(sm.x + si * xbytes));
+                    const uint64_t bdesc1 = tc::smem_desc_k_sw128(tc::smem_u32(sm.x + si * xbytes + xhalf));
+                    const uint32_t a_t = tmem + kACol0 + (uint32_t)si * 64u;
+                    const int nkk = kb + 1 < U.kb1 ? 8 : 4;       // K = 16 per MMA
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        tc::mma_f16_ts(tmem, a_t + 8u * kk, bdesc + (uint64_t)(2 * kk), idesc,
-                                       (kb != U.kb0 || kk != 0) ? 1u : 0u);
+                    for (int kk = 0; kk < 8; ++kk)
+                        if (kk < nkk)
+                            tc::mma_f16_ts(tmem, a_t + 8u * kk,
+                                           (kk < 4 ? bdesc0 : bdesc1) + (uint64_t)(2 * (kk & 3)), idesc,
+                                           (kb != U.kb0 || kk != 0) ? 1u : 0u);
                     issued = true;
-                    tc::mma_commit(sm.x_empty(xi));
-                    tc::mma_commit(sm.a_empty(ai));
-                    if (++xi == kXS) { xi = 0; xph ^= 1u; }
-                    if (++ai == kAS) { ai = 0; aph ^= 1u; }
+                    tc::mma_commit(sm.s_empty(si));
+                    if (++si == NS) { si = 0; sph ^= 1u; }
                 }
                 if (!ok) break;
                 tc::mma_commit(sm.d_full());
@@ -431,41 +451,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qd = warp & 3;
         const int r = qd * 32 + lane;                       // weight row in the tile = TMEM lane
         const uint32_t a_lane = tmem + ((uint32_t)(qd * 32) << 16) + kACol0;
-        int ci = 0, ai = 0;
+        int ci = 0, ai = 0;                                   // ai: slice slot
         uint32_t cph = 0, aph = 0;
         bool ok = true;
+        // this row's scale chunk (8 groups) and zero points of code stage ks of unit uu (4-bit:
+        // the chunk's zero word; 8-bit: the 4-word block of 16 groups holding them); zeros for a
+        // row past N
+        auto load_meta = [&](int uu, int ks, uint4& sv, uint4& zv, uint32_t& zw) {
+            const int nn = (unit_of(p, uu).tile / p.mtiles) * kBM + r;
+            sv = make_uint4(0u, 0u, 0u, 0u);
+            zv = make_uint4(0u, 0u, 0u, 0u);
+            zw = 0u;
+            if (nn < p.N) {
+                const int g0 = ks * (kSubs * 64) / G;
+                sv = ldg128_nc(p.s + (int64_t)nn * p.lds + (g0 & ~7));
+                if constexpr (W8) zv = ldg128_nc(p.z + (int64_t)nn * p.ldz + ((g0 >> 2) & ~3));
+                else zw = ldg32_nc(p.z + (int64_t)nn * p.ldz + (g0 >> 3));
+            }
+        };
+        // the metadata is requested one code stage ahead of its use (the next unit's first
+        // stage during a unit's last), so its latency hides behind a stage of expansion
+        uint4 sv, zv;
+        uint32_t zw;
+        if (blockIdx.x < p.units) load_meta(blockIdx.x, unit_of(p, blockIdx.x).kb0 / kSubs, sv, zv, zw);
         for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
             const Unit U = unit_of(p, u);
-            const int n = (U.tile / p.mtiles) * kBM + r;
-            const bool rv = n < p.N;
-            const unsigned short* srow = p.s + (int64_t)(rv ? n : 0) * p.lds;
-            const uint32_t* zrow = p.z + (int64_t)(rv ? n : 0) * p.ldz;
-            for (int ks = U.kb0 / kSubs; kSubs * ks < U.kb1 && ok; ++ks) {
-                // this stage's groups: the 8-group chunk of scales holding them, and their zero
-                // points (4-bit: the chunk's zero word; 8-bit: the 4-word block holding 16 groups)
-                const int g0 = ks * (kSubs * 64) / G;
-                uint4 sv = make_uint4(0u, 0u, 0u, 0u), zv = make_uint4(0u, 0u, 0u, 0u);
-                uint32_t zw = 0u;
-                if (rv) {
-                    sv = ldg128_nc(srow + (g0 & ~7));
-                    if constexpr (W8) zv = ldg128_nc(zrow + ((g0 >> 2) & ~3));
-                    else zw = ldg32_nc(zrow + (g0 >> 3));
-                }
+            const int ks_end = (U.kb1 + kSubs - 1) / kSubs;
+            for (int ks = U.kb0 / kSubs; ks < ks_end && ok; ++ks) {
+                uint4 svn = sv, zvn = zv;
+                uint32_t zwn = zw;
+                if (ks + 1 < ks_end) load_meta(u, ks + 1, svn, zvn, zwn);
+                else if (u + (int)gridDim.x < p.units)
+                    load_meta(u + gridDim.x, unit_of(p, u + gridDim.x).kb0 / kSubs, svn, zvn, zwn);
                 ok = wait_phase(sm.c_full(ci), cph, sm.abort_flag, kStatusDequant, p.spin_limit);
                 if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
                 const uint32_t rowp = tc::smem_u32(sm.c + ci * kCodeStageBytes) + (uint32_t)r * 128u;
                 const int nsub = min(kSubs, p.nk64 - ks * kSubs);
-                for (int sub = 0; sub < nsub; ++sub) {
-                    ok = wait_phase(sm.a_empty(ai), aph ^ 1u, sm.abort_flag, kStatusDequant, p.spin_limit);
-                    if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
-                    tc::tc_fence_after();
-                    uint32_t a[32];
+                // 64-k sub-slice `sub` of the stage -> 32 FP16 pairs
+                auto expand = [&](int sub, uint32_t (&a)[32]) {
                     if constexpr (W8) {
                         dequant_slice8<G>(rowp, r, sub, ks, sv, zv, p.ngroups, a);
                     } else {
                         const uint4 w0 = lds128(rowp + ((uint32_t)((2 * sub) ^ (r & 7)) << 4));
                         const uint4 w1 = lds128(rowp + ((uint32_t)((2 * sub + 1) ^ (r & 7)) << 4));
-                        const int ga = (ks * 256 + sub * 64) / G;        // group of the slice's first code
+                        const int ga = (ks * 256 + sub * 64) / G;        // group of the sub-slice's first code
                         uint32_t s2a, zza, s2b, zzb;
                         group_consts(sv, zw, ga & 7, ga < p.ngroups, s2a, zza);
                         if constexpr (G == 32) {
@@ -483,16 +512,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                         dequant_word(w1.z, s2b, zzb, a + 24);
                         dequant_word(w1.w, s2b, zzb, a + 28);
                     }
-                    tc::tmem_st32_wait(a_lane + (uint32_t)ai * 32u, a);
+                };
+                for (int sub = 0; sub < nsub; sub += 2) {          // one 128-k slice: sub, sub + 1
+                    ok = wait_phase(sm.s_empty(ai), aph ^ 1u, sm.abort_flag, kStatusDequant, p.spin_limit);
+                    if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
+                    tc::tc_fence_after();
+                    uint32_t a0[32], a1[32];
+                    expand(sub, a0);
+                    tc::tmem_st32(a_lane + (uint32_t)ai * 64u, a0);
+                    if (sub + 1 < nsub) {
+                        expand(sub + 1, a1);
+                        tc::tmem_st32(a_lane + (uint32_t)ai * 64u + 32u, a1);
+                    }
+                    tc::tmem_wait_st();
                     tc::tc_fence_before();
                     __syncwarp();
                     if (lane == 0) tc::mbar_arrive(sm.a_full(ai));
-                    if (++ai == kAS) { ai = 0; aph ^= 1u; }
+                    if (++ai == NS) { ai = 0; aph ^= 1u; }
                 }
                 if (!ok) break;
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(sm.c_empty(ci));
-                if (++ci == kCS) { ci = 0; cph ^= 1u; }
+                if (++ci == NC) { ci = 0; cph ^= 1u; }
+                sv = svn;
+                zv = zvn;
+                zw = zwn;
             }
         }
     } else {
