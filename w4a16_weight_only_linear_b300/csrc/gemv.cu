@@ -113,6 +113,7 @@ struct GemvParams {
     int nw;                                // warps in the CTA
     int warps;                             // warps that take units (<= nw)
     int nst;                               // unit slots per warp ring (power of two)
+    int pf;                                // chunks ahead of the ring each warp asks L2 for (0: none)
     int rows_cap;                          // weight rows per CTA the partial buffer holds
     long long spin_limit;                  // cycles a bounded wait spins before it gives up
     int withhold;                          // test hook: warp 0 of CTA 0 never issues its first unit
@@ -229,7 +230,7 @@ __device__ __forceinline__ bool gemv_wait(uint32_t bar, uint32_t parity, long lo
 // M1: one activation row with P >= 2 segments.  The B columns are then
 // (parity, segment) pairs and each lane holds at most one useful D value per
 // row, so the block-end correction is done once per row on that value only.
-// NM: matrices the instance takes (2 for one or two, 4 for three or four).
+// NM: matrices the instance takes (1, 2, or 4 for three or four).
 template <int NB, int G, int H, bool M1, int PT, int FMT, int NM>
 __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
     gemv_kernel(const __grid_constant__ CodeMaps<NM> tm, const GemvParams p) {
@@ -277,6 +278,31 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
     // test hook: warp 0 of CTA 0 never issues its first unit, so its wait on it runs out
     const bool withhold = p.withhold && blockIdx.x == 0 && warp == 0;
     // copy = false (the test hook only) advances past a unit without issuing its copies
+    // With a ring of one unit per warp (shared memory taken by long metadata rows) the copies in
+    // flight do not cover the memory latency; each warp then also asks L2 for its next p.pf chunks
+    // (boxes not yet in the ring, inside the warp's run) so that the ring's copies hit L2.  Only
+    // groups of 32 (and super-blocks) have rows that long; the other instances leave the code
+    // out, as its mere presence in the refill path costs them 1-2 %.
+    constexpr bool kPf = G == 32;
+    int pf_ch = it_ch, pf_tl = it_tl, pf_c = it_c;     // next chunk to prefetch
+    auto prefetch_upto = [&](int lim) {
+        lim = min(lim, ch1);
+        for (; pf_ch < lim; ++pf_ch) {
+            if (pf_ch >= it_ch) {
+                const int tau = tile0 + pf_tl;
+                const int mat = mat_of<NM>(p, tau);
+                const void* map = &tm.m[0];
+#pragma unroll
+                for (int i = 1; i < NM; ++i)
+                    if (mat == i) map = &tm.m[i];
+                tc::tma_prefetch_2d(map, pf_c * 32, (tau - p.tstart[mat]) * 16);
+            }
+            if (++pf_c == p.C) {
+                pf_c = 0;
+                ++pf_tl;
+            }
+        }
+    };
     auto issue_next = [&](bool copy) {
         const int tau = tile0 + it_tl;
         const int mat = mat_of<NM>(p, tau);
@@ -301,6 +327,9 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
         if (it_c == p.C) {
             it_c = 0;
             ++it_tl;
+        }
+        if constexpr (kPf) {
+            if (p.pf && copy) prefetch_upto(it_ch + p.pf);
         }
     };
 
@@ -977,6 +1006,7 @@ bool make_plan(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G, int sms
         }
         for (int nst = 4; nst >= 1; nst >>= 1) {
             p.nst = nst;
+            p.pf = nst == 1 && G == 32 ? 4 : 0;   // measured: 4 chunks ahead helps a one-unit ring at G = 32
             pl.smem = make_layout(p, pl.nb, pl.H).total + 1024;
             if (pl.smem <= smem_cap) return true;
         }
@@ -1028,7 +1058,7 @@ cudaError_t launch_t(const CUtensorMap* tm, const Plan& pl, int dev, cudaStream_
     return launch_m<NB, G, H, false, 0, FMT, NM>(tm, pl, dev, stream);
 }
 
-template <int NB, int G, int FMT = kFmt4, int NM = 2>
+template <int NB, int G, int FMT, int NM>
 cudaError_t launch_h(const CUtensorMap* tm, const Plan& pl, int dev, cudaStream_t stream) {
     if constexpr (NB == 2) {
         return launch_t<NB, G, 1, FMT, NM>(tm, pl, dev, stream);
@@ -1060,9 +1090,9 @@ cudaError_t launch_nb(const CUtensorMap* tm, const Plan& pl, int dev, cudaStream
 // The 8-bit word layout (one column block; G' = 2G in {64, 128, 256}).
 cudaError_t launch_w8(const CUtensorMap* tm, const Plan& pl, int dev, cudaStream_t stream) {
     switch (pl.p.G) {
-        case 64: return launch_h<1, 64, kFmt8>(tm, pl, dev, stream);
-        case 128: return launch_h<1, 128, kFmt8>(tm, pl, dev, stream);
-        case 256: return launch_h<1, 256, kFmt8>(tm, pl, dev, stream);
+        case 64: return launch_h<1, 64, kFmt8, 1>(tm, pl, dev, stream);
+        case 128: return launch_h<1, 128, kFmt8, 1>(tm, pl, dev, stream);
+        case 256: return launch_h<1, 256, kFmt8, 1>(tm, pl, dev, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -1130,13 +1160,19 @@ cudaError_t launch_gemv(const void* x, const GemvMat* mats, int nmat, int64_t M,
             tm[i] = tm[0];
         }
     }
-    // one or two matrices (kq, w8: always) run the two-map instances; three or four the four-map ones
-    if ((kq || w8) && nmat > 2) return cudaErrorInvalidValue;
-    if (kq) return launch_h<1, 32, kFmtQ4K>(tm, pl, di.dev, stream);   // make_plan: M <= 8, one column block
+    // instances by matrix count: one map for one matrix (no per-tile matrix lookup), two for a
+    // pair, four for three or four (4-bit only); the super-block layout takes one or two, the
+    // 8-bit word layout one
+    if ((kq && nmat > 2) || (w8 && nmat > 1)) return cudaErrorInvalidValue;
+    if (kq)                                                   // make_plan: M <= 8, one column block
+        return nmat == 1 ? launch_h<1, 32, kFmtQ4K, 1>(tm, pl, di.dev, stream)
+                         : launch_h<1, 32, kFmtQ4K, 2>(tm, pl, di.dev, stream);
     if (w8) return launch_w8(tm, pl, di.dev, stream);
     if (nmat > 2)
         return pl.nb == 1 ? launch_nb<1, 4>(tm, pl, di.dev, stream) : launch_nb<2, 4>(tm, pl, di.dev, stream);
-    return pl.nb == 1 ? launch_nb<1, 2>(tm, pl, di.dev, stream) : launch_nb<2, 2>(tm, pl, di.dev, stream);
+    if (nmat == 2)
+        return pl.nb == 1 ? launch_nb<1, 2>(tm, pl, di.dev, stream) : launch_nb<2, 2>(tm, pl, di.dev, stream);
+    return pl.nb == 1 ? launch_nb<1, 1>(tm, pl, di.dev, stream) : launch_nb<2, 1>(tm, pl, di.dev, stream);
 }
 
 }  // namespace w4a16

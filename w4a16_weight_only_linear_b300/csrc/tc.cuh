@@ -71,6 +71,13 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
         : "memory");
 }
 
+// Asks L2 to fetch one box of a 2-D tensor map at (c0, c1) (nothing is
+// written to shared memory and no barrier is signalled).
+__device__ __forceinline__ void tma_prefetch_2d(const void* tmap, int32_t c0, int32_t c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                 ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1) : "memory");
+}
+
 // Contiguous (non-tensor) bulk copy global -> this CTA's shared memory; both
 // addresses 16-byte aligned, `bytes` a multiple of 16.  Completion is reported
 // to `bar` as transaction bytes.
