@@ -76,6 +76,7 @@ __host__ __device__ constexpr int cta_warps(int NB, int G) { return NB == 1 && G
 constexpr int kBoxBytes = 2048;           // one TMA box: 16 virtual rows x 128 bytes (256 codes)
 constexpr int kUnitBytes = 2 * kBoxBytes;  // a ring slot: a unit of up to two consecutive chunks of a tile
 constexpr int kSlots = 4;                 // partial-sum slots per output (warps sharing a tile)
+constexpr int kMetaBytes = 512;           // streamed metadata of a unit: 16 virtual rows x 16 halves
 // Weight formats the decode kernel reads.  kFmt8: 8-bit codes four per word
 // with 8-bit zero points; the kernel runs them as a 4-bit layer of 2K virtual
 // channels and groups of 2G (each 8-bit code is two nibbles), expanding both
@@ -114,13 +115,14 @@ struct GemvParams {
     int warps;                             // warps that take units (<= nw)
     int nst;                               // unit slots per warp ring (power of two)
     int pf;                                // chunks ahead of the ring each warp asks L2 for (0: none)
+    int mstream;                           // 1: scales (super-block records) stream with the units
     int rows_cap;                          // weight rows per CTA the partial buffer holds
     long long spin_limit;                  // cycles a bounded wait spins before it gives up
     int withhold;                          // test hook: warp 0 of CTA 0 never issues its first unit
 };
 
 struct Layout {
-    uint32_t ring, xs, zero, exs, ms, mz, part, red, bars;
+    uint32_t ring, mring, xs, zero, exs, ms, mz, part, red, bars;
     uint32_t total;
 };
 
@@ -136,14 +138,16 @@ __host__ __device__ inline Layout make_layout(const GemvParams& p, int nb, int H
     uint32_t off = 0;
     L.ring = off;
     off += (uint32_t)(p.nw * p.nst * kUnitBytes);
+    L.mring = off;                                        // streamed metadata, one area per ring slot
+    off += p.mstream ? (uint32_t)(p.nw * p.nst * kMetaBytes) : 0u;
     L.xs = off;
     off += align_up((uint32_t)p.xcols * (uint32_t)p.Ks * 2u, 16);        // xcols x Ks FP16 (whole chunks)
     L.zero = off;                                         // zeros read by idle B columns: one 16-byte
     off += m1 ? 8u * (uint32_t)p.xcols * 64u : 16u;        // block, or (M = 1) a chunk's 8 word steps of x
     L.exs = off;
     off += align_up((uint32_t)(p.ngs / H) * 8u * (uint32_t)nb * 8u, 16);
-    L.ms = off;
-    off += align_up((uint32_t)p.rows_cap * (uint32_t)p.lds * 2u, 16);
+    L.ms = off;                                           // resident scale rows (or records) unless streamed
+    off += p.mstream ? 0u : align_up((uint32_t)p.rows_cap * (uint32_t)p.lds * 2u, 16);
     L.mz = off;
     off += align_up((uint32_t)p.rows_cap * (uint32_t)p.ldz * 4u, 16);
     L.part = off;
@@ -207,11 +211,22 @@ __device__ __forceinline__ int mat_of(const GemvParams& p, int tau) {
     return m;
 }
 
-// The code maps of up to NM matrices, one kernel parameter.
-template <int NM>
+// The code maps of up to NM matrices, one kernel parameter; with MS also the
+// maps of their scale rows (or super-block records) viewed per virtual row.
+template <int NM, bool MS>
 struct CodeMaps {
     CUtensorMap m[NM];
+    CUtensorMap s[NM];
 };
+template <int NM>
+struct CodeMaps<NM, false> {
+    CUtensorMap m[NM];
+};
+
+// Instances whose scale rows (or super-block records) stream with the weight units instead of
+// staying resident: groups of 32, where a row's metadata is long (0.0625-0.078 bytes per code,
+// 100 KB per CTA at K = 28672) and would crowd the weight ring out of shared memory.
+__host__ __device__ constexpr bool meta_streamed(int G) { return G == 32; }
 
 // Bounded wait on a barrier phase (gives up after `limit` cycles); the thread
 // sleeps between polls.
@@ -233,7 +248,7 @@ __device__ __forceinline__ bool gemv_wait(uint32_t bar, uint32_t parity, long lo
 // NM: matrices the instance takes (1, 2, or 4 for three or four).
 template <int NB, int G, int H, bool M1, int PT, int FMT, int NM>
 __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
-    gemv_kernel(const __grid_constant__ CodeMaps<NM> tm, const GemvParams p) {
+    gemv_kernel(const __grid_constant__ CodeMaps<NM, meta_streamed(G)> tm, const GemvParams p) {
     constexpr int V = G >= 128 ? 4 : G / 32;      // words per lane per code load
     constexpr int GPC = 256 / G;                  // groups per chunk (H divides it)
     constexpr int WSG = G / 32;                   // word steps per group
@@ -245,6 +260,10 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
     constexpr bool KQ = FMT == kFmtQ4K;          // super-block records in place of scales and zeros
     constexpr bool W8 = FMT == kFmt8;            // 8-bit codes, four per word (a virtual 4-bit layer of 2K)
     static_assert(!KQ || G == 32, "a super-block is one chunk of 8 sub-blocks of 32");
+    // MS: each unit also brings the scales (super-block records) of its two chunks for the tile's
+    // 16 virtual rows, 32 bytes per row (kMetaBytes), into a per-slot area; only the zero rows
+    // (4-bit) stay resident
+    constexpr bool MS = meta_streamed(G);
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base; derived by pointer arithmetic on the shared array so
     // the compiler keeps every access below in the shared address space
@@ -265,6 +284,7 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
     const int ch1 = active ? ((warp + 1) * chunks) / p.warps : 0;
     const int nsl = p.nst;                        // unit slots in this warp's ring (power of two)
     const uint32_t ring = sbase + L.ring + (uint32_t)(warp * nsl * kUnitBytes);
+    const uint32_t mring = sbase + L.mring + (uint32_t)(warp * nsl * kMetaBytes);   // MS only
     const uint32_t bar0 = sbase + L.bars + (uint32_t)(warp * nsl * 8);
 
     // ---- stream: lane 0 of each warp keeps its ring of units filled -----------
@@ -311,7 +331,7 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
         const uint32_t bar = bar0 + 8u * slot;
         const bool two = it_c + 1 < p.C && it_ch + 1 < ch1;
         if (copy) {
-            tc::mbar_arrive_expect_tx(bar, (uint32_t)(two ? 2 * kBoxBytes : kBoxBytes));
+            tc::mbar_arrive_expect_tx(bar, (uint32_t)(two ? 2 * kBoxBytes : kBoxBytes) + (MS ? kMetaBytes : 0u));
             const void* map = &tm.m[0];
 #pragma unroll
             for (int i = 1; i < NM; ++i)
@@ -319,6 +339,13 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
             tc::tma_load_2d(ring + slot * (uint32_t)kUnitBytes, map, it_c * 32, tile * 16, bar);
             if (two)
                 tc::tma_load_2d(ring + slot * (uint32_t)kUnitBytes + kBoxBytes, map, (it_c + 1) * 32, tile * 16, bar);
+            if constexpr (MS) {   // the scales of chunks it_c, it_c + 1 (a box of 16 halves per virtual row)
+                const void* smap = &tm.s[0];
+#pragma unroll
+                for (int i = 1; i < NM; ++i)
+                    if (mat == i) smap = &tm.s[i];
+                tc::tma_load_2d(mring + slot * (uint32_t)kMetaBytes, smap, it_c * 8, tile * 16, bar);
+            }
         }
         const int n = two ? 2 : 1;
         ++it_n;
@@ -356,7 +383,7 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
         // local rows follow the CTA's tiles: the part of matrix i is the tiles [a_i, b_i) of the
         // CTA's range, local rows [(a_i - tile0) R, (b_i - tile0) R); its rows below the matrix's
         // n are bulk-copied (they are contiguous in the matrix), the rest zero-filled below
-        const uint32_t sbytes = (uint32_t)p.lds * 2u, zbytes = (uint32_t)p.ldz * 4u;   // per row
+        const uint32_t sbytes = MS ? 0u : (uint32_t)p.lds * 2u, zbytes = (uint32_t)p.ldz * 4u;   // per row
         const uint32_t ms = sbase + L.ms, mz = sbase + L.mz;
         int cl[NM], cc[NM];                            // local first row and rows copied, per matrix
         int gs[NM + 1], gn[NM + 1];                    // rows left to zero-fill: first, count
@@ -380,7 +407,7 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
             for (int i = 0; i < NM; ++i) {
                 if (cc[i] <= 0) continue;
                 const int64_t r0 = (int64_t)(max(tile0, p.tstart[i]) - p.tstart[i]) * R;    // first row
-                tc::bulk_load(ms + (uint32_t)cl[i] * sbytes, p.s[i] + r0 * p.lds, (uint32_t)cc[i] * sbytes, pbar);
+                if (!MS) tc::bulk_load(ms + (uint32_t)cl[i] * sbytes, p.s[i] + r0 * p.lds, (uint32_t)cc[i] * sbytes, pbar);
                 if (!KQ) tc::bulk_load(mz + (uint32_t)cl[i] * zbytes, p.z[i] + r0 * p.ldz, (uint32_t)cc[i] * zbytes, pbar);
             }
         }
@@ -497,7 +524,7 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
         // zero fills: table rows not copied, E/X columns no (segment, parity, row) uses, the
         // zero block, the partial sums
         {
-            const int sv = p.lds / 8, per = sv + p.ldz / 4;                       // uint4 per row
+            const int sv = MS ? 0 : p.lds / 8, per = sv + p.ldz / 4;              // uint4 per row
             for (int i = tid; i < gaps * per; i += kThreads) {
                 int k = i / per, lr = 0;
                 const int col = i - k * per;
@@ -628,8 +655,12 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
                   if (cc == 1 && !two) break;                 // one-chunk unit (uniform)
                   const int c = cu + cc;                      // chunk in the tile
                   const int rla = tl * R + rho_a, rlb = tl * R + rho_b;   // local rows
-                  const unsigned short* sra = smtab + rla * p.lds + pa * p.ngs + c * GPC;
-                  const unsigned short* srb = smtab + rlb * p.lds + pb * p.ngs + c * GPC;
+                  // scales of the chunk's groups: the resident row, or (MS) the unit's streamed box,
+                  // 16 halves per virtual row, chunk cc at half 8 cc
+                  const unsigned short* msu = reinterpret_cast<const unsigned short*>(
+                      base + (mring - sbase) + slot * (uint32_t)kMetaBytes);
+                  const unsigned short* sra = MS ? msu + va * 16 + cc * 8 : smtab + rla * p.lds + pa * p.ngs + c * GPC;
+                  const unsigned short* srb = MS ? msu + vb * 16 + cc * 8 : smtab + rlb * p.lds + pb * p.ngs + c * GPC;
                   const uint32_t* zra = zmtab + rla * p.ldz;
                   const uint32_t* zrb = zmtab + rlb * p.ldz;
                   const int gia = pa * p.ngs + c * GPC, gib = pb * p.ngs + c * GPC;   // first group of the chunk
@@ -649,8 +680,8 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
                   uint4 kra = make_uint4(0u, 0u, 0u, 0u), krb = kra;
                   float kda = 0.0f, kma = 0.0f, kdb = 0.0f, kmb = 0.0f;
                   if constexpr (KQ) {
-                      kra = *reinterpret_cast<const uint4*>(smtab + rla * p.lds + (pa * p.C + c) * 8);
-                      krb = *reinterpret_cast<const uint4*>(smtab + rlb * p.lds + (pb * p.C + c) * 8);
+                      kra = *reinterpret_cast<const uint4*>(sra);       // the record is 8 halves at the
+                      krb = *reinterpret_cast<const uint4*>(srb);       // chunk's first group
                       kda = half_lo(kra.x);
                       kma = half_hi(kra.x);
                       kdb = half_lo(krb.x);
@@ -914,6 +945,16 @@ bool make_code_map(CUtensorMap* map, const uint32_t* q, int64_t N, int64_t K, in
     return encode_tmap_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, q, words, (uint64_t)(N * P), words * 4, 32, 16, dev);
 }
 
+// Scale rows (or super-block records) [N][lds halves] viewed per virtual row as [N*P][lds/P],
+// unswizzled boxes of 16 halves (two chunks' groups of 32, or two records) x 16 rows.  A row's
+// segments are consecutive (lds = P * the groups of a segment when a row's groups fill whole
+// chunks, which make_plan checks), so virtual row n*P + seg is segment seg of row n.
+bool make_meta_map(CUtensorMap* map, const void* s, int64_t N, int lds, int P, int dev) {
+    const uint64_t halves = (uint64_t)(lds / P);
+    return encode_tmap_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, s, halves, (uint64_t)(N * P), halves * 2, 16, 16, dev,
+                          false);
+}
+
 // Segments P and group parities H per row for M activation rows: the B
 // operand's columns are (segment, parity, row) triples, P*H*M <= 8 (one
 // column block; M > 8 uses two blocks with P = H = 1).  Preferred: few weight
@@ -972,6 +1013,9 @@ bool make_plan(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G, int sms
     p.ng = (int)(K / G);
     p.ngs = p.Ks / G;
     p.lds = kq ? (int)(K / 256 * 8) : (int)scales_ld(K, G);
+    p.mstream = meta_streamed(G) ? 1 : 0;
+    // streamed metadata needs each segment's groups (records) to be whole chunks laid out back to back
+    if (p.mstream && (p.lds % p.P != 0 || p.lds / p.P != p.C * (256 / G) || (p.lds / p.P) % 8 != 0)) return false;
     p.ldz = kq ? 0 : w8 ? (int)zeros8_ld(K / 2, G / 2) : (int)zeros_ld(K, G);
     int64_t t = 0;
     for (int i = 0; i < kMaxMat; ++i) {
@@ -1038,8 +1082,11 @@ cudaError_t launch_m(const CUtensorMap* tm, const Plan& pl, int dev, cudaStream_
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    CodeMaps<NM> maps;
+    // tm[0, kMaxMat): code maps; tm[kMaxMat, 2 kMaxMat): streamed-metadata maps (MS instances)
+    CodeMaps<NM, meta_streamed(G)> maps;
     for (int i = 0; i < NM; ++i) maps.m[i] = tm[i];
+    if constexpr (meta_streamed(G))
+        for (int i = 0; i < NM; ++i) maps.s[i] = tm[kMaxMat + i];
     return cudaLaunchKernelEx(&cfg, gemv_kernel<NB, G, H, M1, PT, FMT, NM>, maps, pl.p);
 }
 
@@ -1148,7 +1195,7 @@ cudaError_t launch_gemv(const void* x, const GemvMat* mats, int nmat, int64_t M,
     p.yf32 = yf32 ? 1 : 0;
     p.spin_limit = wait_limit();
     p.withhold = take_withhold(1) ? 1 : 0;
-    CUtensorMap tm[kMaxMat];
+    CUtensorMap tm[2 * kMaxMat];
     for (int i = 0; i < kMaxMat; ++i) {
         const GemvMat& mt = mats[i < nmat ? i : 0];
         p.s[i] = static_cast<const unsigned short*>(mt.s);
@@ -1156,8 +1203,11 @@ cudaError_t launch_gemv(const void* x, const GemvMat* mats, int nmat, int64_t M,
         p.y[i] = mt.y;
         if (i < nmat) {
             if (!make_code_map(&tm[i], mt.q, Ns[i], Kv, p.P, di.dev)) return cudaErrorInvalidValue;
+            if (p.mstream && !make_meta_map(&tm[kMaxMat + i], mt.s, Ns[i], p.lds, p.P, di.dev))
+                return cudaErrorInvalidValue;
         } else {
             tm[i] = tm[0];
+            tm[kMaxMat + i] = tm[kMaxMat];
         }
     }
     // instances by matrix count: one map for one matrix (no per-tile matrix lookup), two for a
