@@ -259,9 +259,14 @@ def test_dispatch_rule(N, K, G):
 
 
 def test_dispatch_falls_back_when_the_gemv_does_not_fit():
-    # x staged as M*K FP16 plus G = 32 tables: at K = 65536 not even one row fits the decode kernel
-    assert w4.w4a16_linear_path(1, 8192, 65536, 32) == 2
+    # x is staged as M*K FP16 beside the resident metadata rows: at K = 65536 one row still fits at
+    # G = 32 (whose scales stream with the weights; only the zero rows stay resident) and G = 128,
+    # not at G = 64 (resident scales and zeros); at K = 98304 the staged x alone leaves no room
+    assert w4.w4a16_linear_path(1, 8192, 65536, 32) == 1
+    assert w4.w4a16_linear_path(1, 8192, 65536, 64) == 2
     assert w4.w4a16_linear_path(1, 8192, 65536, 128) == 1
+    for G in (32, 64, 128, 256):
+        assert w4.w4a16_linear_path(1, 8192, 98304, G) == 2
 
 
 def test_withhold_hook_rejects_unknown_kernels():
