@@ -88,6 +88,18 @@ def test_gemv_parity(M, N, K, G):
     assert_close(y, y_ref, f"gemv M={M} N={N} K={K} G={G}")
 
 
+@pytest.mark.parametrize("M,N,K", [(1, 264, 28672), (3, 264, 28672), (1, 520, 65536)])
+def test_gemv_long_rows_with_streamed_scales(M, N, K):
+    """Groups of 32 on long rows: the scales stream with the weight units (only the zero rows stay
+    resident), so K = 65536 runs as a GEMV; several CTAs, ragged N, up to 2048 groups per row."""
+    G = 32
+    assert w4.w4a16_linear_path(M, N, K, G) == 1
+    w, x, (q, s, z), y_ref = _case(M, N, K, G, seed=M * 17 + N + K, outliers=0.002)
+    y = w4.w4a16_linear_gemv(x.cuda(), *dev_packed(q, s, z), G)
+    torch.cuda.synchronize()
+    assert_close(y, y_ref, f"gemv long rows M={M} N={N} K={K} G={G}")
+
+
 @pytest.mark.parametrize("M", [1, 4, 8])
 def test_linear_dispatches_to_gemv(M):
     N, K, G = 264, 1024, 128
