@@ -77,6 +77,13 @@ constexpr int kBoxBytes = 2048;           // one TMA box: 16 virtual rows x 128 
 constexpr int kUnitBytes = 2 * kBoxBytes;  // a ring slot: a unit of up to two consecutive chunks of a tile
 constexpr int kSlots = 4;                 // partial-sum slots per output (warps sharing a tile)
 constexpr int kMetaBytes = 512;           // streamed metadata of a unit: 16 virtual rows x 16 halves
+// Small layers (a few tens of KB of weights per SM) are latency bound: a launch spends about
+// 4 us in its prologue and on its first units' latency against 1-2 us of streaming.  Their
+// instance runs 8 warps with at most half the shared memory, so two CTAs fit on an SM: the
+// next launch's CTAs can become resident while this one runs (programmatic stream
+// serialisation) and ask L2 for their weights before their grid-dependency wait.
+constexpr int kDuoWarps = 8;
+constexpr size_t kDuoSmem = 110 * 1024;
 // Weight formats the decode kernel reads.  kFmt8: 8-bit codes four per word
 // with 8-bit zero points; the kernel runs them as a 4-bit layer of 2K virtual
 // channels and groups of 2G (each 8-bit code is two nibbles), expanding both
@@ -98,6 +105,8 @@ struct GemvParams {
     int kx;                                // row length of x: channel k reads x[k mod kx] (kx = K or K/2)
     // per matrix (up to kMaxMat sharing x): FP16 scales [n, lds] (KQ: super-block records, 8
     // halves each), zeros [n, ldz] (KQ: unused, ldz = 0), output [M, n] BF16 (or FP32 when yf32)
+    const uint32_t* q[kMaxMat];            // packed codes (read through the tensor maps; the small-layer
+                                           // instance also asks L2 for them ahead of time)
     const unsigned short* s[kMaxMat];
     const uint32_t* z[kMaxMat];
     void* y[kMaxMat];
@@ -116,6 +125,7 @@ struct GemvParams {
     int nst;                               // unit slots per warp ring (power of two)
     int pf;                                // chunks ahead of the ring each warp asks L2 for (0: none)
     int mstream;                           // 1: scales (super-block records) stream with the units
+    int duo;                               // 1: the small-layer instance (two CTAs per SM, see kDuoWarps)
     int rows_cap;                          // weight rows per CTA the partial buffer holds
     long long spin_limit;                  // cycles a bounded wait spins before it gives up
     int withhold;                          // test hook: warp 0 of CTA 0 never issues its first unit
@@ -246,8 +256,8 @@ __device__ __forceinline__ bool gemv_wait(uint32_t bar, uint32_t parity, long lo
 // (parity, segment) pairs and each lane holds at most one useful D value per
 // row, so the block-end correction is done once per row on that value only.
 // NM: matrices the instance takes (1, 2, or 4 for three or four).
-template <int NB, int G, int H, bool M1, int PT, int FMT, int NM>
-__global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
+template <int NB, int G, int H, bool M1, int PT, int FMT, int NM, bool DUO = false>
+__global__ void __launch_bounds__(DUO ? kDuoWarps * 32 : cta_warps(NB, G) * 32, DUO ? 2 : 1)
     gemv_kernel(const __grid_constant__ CodeMaps<NM, meta_streamed(G)> tm, const GemvParams p) {
     constexpr int V = G >= 128 ? 4 : G / 32;      // words per lane per code load
     constexpr int GPC = 256 / G;                  // groups per chunk (H divides it)
@@ -370,6 +380,26 @@ __global__ void __launch_bounds__(cta_warps(NB, G) * 32, 1)
     // scheduled at once (its CTAs take SMs as this grid's CTAs exit), and this grid reads no
     // global memory before the previous grid on the stream has completed.
     tc::griddep_launch_dependents();
+    if constexpr (DUO) {
+        if (tid == 0) {
+            // the CTA's code, scale and zero rows into L2 now, while the previous grid may still be
+            // running: a prefetch returns nothing to the program and L2 is the point of coherence, so
+            // this reads nothing before the grid-dependency wait below
+#pragma unroll 1
+            for (int i = 0; i < NM; ++i) {
+                const int a = max(tile0, p.tstart[i]), b = min(tile1, p.tstart[i + 1]);
+                if (b <= a) continue;
+                const int64_t r0 = (int64_t)(a - p.tstart[i]) * R;
+                const int64_t rows = min((int64_t)(b - a) * R, (int64_t)p.n[i] - r0);
+                if (rows <= 0) continue;
+                const uint8_t* cq = reinterpret_cast<const uint8_t*>(p.q[i]) + r0 * (p.K / 2);
+                for (int64_t off = 0, tot = rows * (p.K / 2); off < tot; off += 1 << 16)
+                    tc::prefetch_l2(cq + off, (uint32_t)(tot - off < (1 << 16) ? tot - off : (1 << 16)));
+                tc::prefetch_l2(p.s[i] + r0 * p.lds, (uint32_t)(rows * p.lds * 2));
+                tc::prefetch_l2(p.z[i] + r0 * p.ldz, (uint32_t)(rows * p.ldz * 4));
+            }
+        }
+    }
     const uint32_t pbar = sbase + L.bars + 8u * (uint32_t)(kWarps * nsl);
     bool pro_ok = true;                           // the prologue's copies landed (warp-uniform)
     if (tid == 0) {
@@ -1034,9 +1064,9 @@ bool make_plan(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G, int sms
     p.rows_cap = tmax * p.R;
     // CTA warps (the instance's launch bound, or fewer when shared memory is short), then the
     // deepest per-warp ring of units that fits
-    for (int nw = cta_warps(pl.nb, G); nw >= 4; nw -= 4) {
+    // warps taking units: as many as keep every tile within kSlots consecutive warps
+    auto set_warps = [&](int nw) {
         p.nw = nw;
-        // warps taking units: as many as keep every tile within kSlots consecutive warps
         p.warps = 1;
         for (int w = nw; w >= 1; --w) {
             const long long chunks = (long long)tmin * p.C;
@@ -1048,6 +1078,31 @@ bool make_plan(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G, int sms
                 break;
             }
         }
+    };
+    // the small-layer instance: M = 1 at G = 128 with the 70B/13B geometry (P = 4, H = 2), one or
+    // three-four matrices, at most kDuoMaxBytes of weights per CTA, and a layout that leaves room
+    // for a second CTA on the SM.  Measured against the 16-warp instance: 4096^2 5.45 -> 5.26 us,
+    // 5120^2 6.85 -> 6.51 us; at 240 KB per CTA (5120 -> 13824) 11.6 -> 13.7 us, where 8 warps
+    // no longer keep up with the stream, hence the bound.
+    constexpr int64_t kDuoMaxBytes = 128 * 1024;
+    int64_t wbytes = 0;
+    for (int i = 0; i < nmat; ++i) wbytes += Ns[i] * (K / 2);
+    p.duo = 0;
+    if (M == 1 && G == 128 && !kq && !w8 && p.P == 4 && pl.H == 2 && nmat != 2 &&
+        wbytes / pl.grid <= kDuoMaxBytes) {
+        set_warps(kDuoWarps);
+        for (int nst = 4; nst >= 1; nst >>= 1) {
+            p.nst = nst;
+            p.pf = 0;
+            pl.smem = make_layout(p, pl.nb, pl.H).total + 1024;
+            if (pl.smem <= kDuoSmem) {
+                p.duo = 1;
+                return true;
+            }
+        }
+    }
+    for (int nw = cta_warps(pl.nb, G); nw >= 4; nw -= 4) {
+        set_warps(nw);
         for (int nst = 4; nst >= 1; nst >>= 1) {
             p.nst = nst;
             p.pf = nst == 1 && G == 32 ? 4 : 0;   // measured: 4 chunks ahead helps a one-unit ring at G = 32
@@ -1058,15 +1113,18 @@ bool make_plan(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G, int sms
     return false;
 }
 
-template <int NB, int G, int H, bool M1, int PT, int FMT, int NM>
+template <int NB, int G, int H, bool M1, int PT, int FMT, int NM, bool DUO = false>
 cudaError_t launch_m(const CUtensorMap* tm, const Plan& pl, int dev, cudaStream_t stream) {
     // largest dynamic shared memory this instance is already allowed per device (a raise may
     // race with another thread's: both set the attribute, the larger value stays)
     static std::atomic<int> cached[kMaxDevices];
     int have = cached[dev].load(std::memory_order_relaxed);
     if ((int)pl.smem > have) {
-        const cudaError_t e = cudaFuncSetAttribute(gemv_kernel<NB, G, H, M1, PT, FMT, NM>,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+        cudaError_t e = cudaFuncSetAttribute(gemv_kernel<NB, G, H, M1, PT, FMT, NM, DUO>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+        if (e == cudaSuccess && DUO)   // the shared-memory carveout that lets two CTAs share an SM
+            e = cudaFuncSetAttribute(gemv_kernel<NB, G, H, M1, PT, FMT, NM, DUO>,
+                                     cudaFuncAttributePreferredSharedMemoryCarveout, 100);
         if (e != cudaSuccess) return e;
         while (have < (int)pl.smem && !cached[dev].compare_exchange_weak(have, (int)pl.smem)) {
         }
@@ -1087,7 +1145,7 @@ cudaError_t launch_m(const CUtensorMap* tm, const Plan& pl, int dev, cudaStream_
     for (int i = 0; i < NM; ++i) maps.m[i] = tm[i];
     if constexpr (meta_streamed(G))
         for (int i = 0; i < NM; ++i) maps.s[i] = tm[kMaxMat + i];
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<NB, G, H, M1, PT, FMT, NM>, maps, pl.p);
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<NB, G, H, M1, PT, FMT, NM, DUO>, maps, pl.p);
 }
 
 template <int NB, int G, int H, int FMT, int NM>
@@ -1198,6 +1256,7 @@ cudaError_t launch_gemv(const void* x, const GemvMat* mats, int nmat, int64_t M,
     CUtensorMap tm[2 * kMaxMat];
     for (int i = 0; i < kMaxMat; ++i) {
         const GemvMat& mt = mats[i < nmat ? i : 0];
+        p.q[i] = mt.q;
         p.s[i] = static_cast<const unsigned short*>(mt.s);
         p.z[i] = mt.z;
         p.y[i] = mt.y;
@@ -1214,6 +1273,9 @@ cudaError_t launch_gemv(const void* x, const GemvMat* mats, int nmat, int64_t M,
     // pair, four for three or four (4-bit only); the super-block layout takes one or two, the
     // 8-bit word layout one
     if ((kq && nmat > 2) || (w8 && nmat > 1)) return cudaErrorInvalidValue;
+    if (p.duo)                                                // make_plan: M = 1, G = 128, P = 4, H = 2
+        return nmat == 1 ? launch_m<1, 128, 2, true, 4, kFmt4, 1, true>(tm, pl, di.dev, stream)
+                         : launch_m<1, 128, 2, true, 4, kFmt4, 4, true>(tm, pl, di.dev, stream);
     if (kq)                                                   // make_plan: M <= 8, one column block
         return nmat == 1 ? launch_h<1, 32, kFmtQ4K, 1>(tm, pl, di.dev, stream)
                          : launch_h<1, 32, kFmtQ4K, 2>(tm, pl, di.dev, stream);

@@ -71,6 +71,13 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
         : "memory");
 }
 
+// Asks L2 to fetch `bytes` (a multiple of 16) from global memory at a 16-byte
+// aligned address; nothing is returned to the thread.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+                 : "memory");
+}
+
 // Asks L2 to fetch one box of a 2-D tensor map at (c0, c1) (nothing is
 // written to shared memory and no barrier is signalled).
 __device__ __forceinline__ void tma_prefetch_2d(const void* tmap, int32_t c0, int32_t c1) {
