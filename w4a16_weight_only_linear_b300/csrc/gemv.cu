@@ -21,7 +21,8 @@
 // and each lane corrects only the one value per row it holds.
 //
 // Data path.  One CTA per SM (16 warps, or 12 when registers or shared memory
-// are short) takes a balanced contiguous range of tiles; its warps take
+// are short; two CTAs of 8 warps for small layers) takes a balanced contiguous
+// range of tiles; its warps take
 // contiguous runs of 256-code chunks, balanced to the chunk.  Each warp
 // streams its run with TMA (16 virtual rows x 128 bytes per chunk, 128-byte
 // swizzle) into a private ring of shared-memory slots; a slot holds a unit of
@@ -46,12 +47,27 @@
 // scale and zero rows.  The block-end correction becomes
 // acc += s*(D - E) - mn*X with s = d*sc_j and mn = dmin*m_j, both exact in FP32.
 //
+// 8-bit mode (W8).  Codes four per word with 8-bit zero points run as a 4-bit
+// layer of 2K virtual channels and groups of 2G: both nibbles of a code are
+// expanded against the exponent of 1024 and x is staged twice (see
+// expand_codes8_f16), so the MMA sums x (2048 + b) exactly.
+//
+// Metadata.  At G >= 64 the CTA's scale and zero rows stay in shared memory for
+// the whole launch.  At G = 32 (and for super-blocks) each ring unit also
+// brings the scales (records) of its two chunks for the tile's 16 virtual rows
+// by one more TMA box, and only the zero rows stay resident: long rows of fine
+// groups would otherwise leave room for one unit per warp.
+//
 // Prologue.  The launch uses programmatic stream serialisation: a CTA lets the
 // next launch be scheduled on entry and waits for the previous grid before it
-// reads global memory.  One thread then bulk-copies the CTA's scale and zero
-// rows while every warp loads its first x items; the weight ring starts once
-// the rows have landed (copies issued together complete in no particular
-// order), and x is staged while the first units are in flight.
+// reads global memory.  One thread then bulk-copies the CTA's resident
+// metadata rows while every warp loads its first x items; the weight ring
+// starts once the rows have landed (copies issued together complete in no
+// particular order), and x is staged while the first units are in flight.
+// Small layers run an 8-warp instance that leaves room for a second CTA per
+// SM; its CTAs ask L2 for their rows before the grid-dependency wait.
+//
+// Instances cover one matrix, a pair (the dual call) or up to four sharing x.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
