@@ -1010,13 +1010,18 @@ bool make_meta_map(CUtensorMap* map, const void* s, int64_t N, int lds, int P, i
 // before (4, 2): at M = 1 every lane then holds a useful D value and the
 // block-end corrections per chunk halve, which makes groups of 32 (and
 // super-blocks) 3-14 % faster; groups of 128 or more cannot take H = 4.
-void choose_segments(int64_t M, int64_t K, int G, int& P, int& H) {
+void choose_segments(int64_t M, int64_t K, int G, bool kq, int& P, int& H) {
     P = 1;
     H = 1;
     if (M > 8) return;
     const int gpc = 256 / G;
     static const int pref[][2] = {{2, 4}, {4, 2}, {8, 1}, {4, 1}, {2, 2}, {1, 4}, {2, 1}, {1, 2}, {1, 1}};
-    for (const auto& c : pref) {
+    // 4-bit groups of 32 at M >= 2: group parities before segments, since a correction every group
+    // (every word step) costs more than the extra rows per tile (5120 -> 13824: M = 2 17.9 -> 16.3 us,
+    // M = 4 17.4 -> 17.0 us; the same order was 1-3 % slower at G = 128, and 4-11 % slower for
+    // super-blocks at M = 3, whose correction is per record rather than per group)
+    static const int pref_fine[][2] = {{2, 2}, {1, 4}, {1, 2}, {4, 1}, {2, 1}, {1, 1}, {1, 1}, {1, 1}, {1, 1}};
+    for (const auto& c : (M >= 2 && G == 32 && !kq ? pref_fine : pref)) {
         const int p = c[0], h = c[1];
         if (p * h * M > 8 || h > gpc || gpc % h) continue;
         if (p > 1 && K % (256 * p)) continue;
@@ -1049,7 +1054,7 @@ bool make_plan(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G, int sms
     p.M = (int)M;
     p.K = (int)K;
     p.G = G;
-    choose_segments(M, K, G, p.P, pl.H);
+    choose_segments(M, K, G, kq, p.P, pl.H);
     p.R = 16 / p.P;
     p.cols = p.P * pl.H * p.M;
     p.xcols = p.P * p.M;
