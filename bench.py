@@ -483,30 +483,55 @@ def run_reference(args):
 
 
 def run_profile(args):
-    """Small case for ncu captures: one packed 70B gate matrix (8192 -> 28672,
-    ~122 MB of packed weights, above L2), `warmup` + 2 calls of one phase, no
-    timing and no CPU leg."""
+    """Small case for ncu captures: by default one packed 70B gate matrix
+    (8192 -> 28672, ~122 MB of packed weights, above L2), `warmup` + 2 calls of
+    one phase, no timing and no CPU leg.  `--workload W` profiles matrix
+    `--matrix` of another workload at `--m` activation rows (default: 1 for
+    decode, the workload's largest M for prefill) and group size `--g` (default:
+    the workload's first); the dual workload runs its paired call.  Weights are
+    packed into enough rotating copies that more than 2x L2 streams between two
+    uses of a copy, so the captured call reads cold weights."""
     import w4a16_weight_only_linear_b300 as w4
     q4k = args.format == "q4k"
     if q4k and args.profile != "decode":
         raise SystemExit("--format q4k profiles the decode kernel only")
-    wk = wl.WORKLOADS["ffn70b_q4k" if q4k else WORKLOAD]
-    lin = wk.linears[int(args.matrix)]
-    w = wl.weight_f16(lin.N, lin.K, wk.sigma, wl.matrix_seed(wk, int(args.matrix)), wk.outlier_frac).cuda()
-    packed = w4.q4k_pack(w) if q4k else w4.w4a16_pack(w, G)
-    del w
-    M = M_DECODE if args.profile == "decode" else M_PREFILL
-    x = wl.activations_bf16(M, lin.K, wl.act_seed(wk, int(args.matrix))).cuda()
-    y = torch.empty(M, lin.N, dtype=torch.bfloat16, device="cuda")
-    for _ in range(args.warmup + 2):
+    name = "ffn70b_q4k" if q4k else (args.workload or WORKLOAD)
+    wk = wl.WORKLOADS[name]
+    j = int(args.matrix)
+    lin = wk.linears[j]
+    Gv = 32 if q4k else (args.g or (G if name == WORKLOAD else wk.Gs[0]))
+    if args.m:
+        M = args.m
+    elif name == WORKLOAD or q4k:
+        M = M_DECODE if args.profile == "decode" else M_PREFILL
+    else:
+        M = 1 if args.profile == "decode" else max(wk.Ms)
+    mats = [j, 1 - j] if wk.dual else [j]
+    one = sum(q4k_bytes(1, wk.linears[i].N, wk.linears[i].K) if q4k else
+              gemv_bytes(1, wk.linears[i].N, wk.linears[i].K, Gv) for i in mats)
+    copies = max(1, -(-2 * 126 * 2 ** 20 // one) + 1)
+    packs = []
+    for i in mats:
+        li = wk.linears[i]
+        w = wl.weight_f16(li.N, li.K, wk.sigma, wl.matrix_seed(wk, i), wk.outlier_frac).cuda()
+        packs.append([w4.q4k_pack(w) if q4k else w4.w4a16_pack(w, Gv) for _ in range(copies)])
+        del w
+    x = wl.activations_bf16(M, lin.K, wl.act_seed(wk, j)).cuda()
+    ys = [torch.empty(M, wk.linears[i].N, dtype=torch.bfloat16, device="cuda") for i in mats]
+    calls = args.warmup + 2
+    for c in range(calls):
+        pk = [p[c % copies] for p in packs]
         if q4k:
-            w4.q4k_linear(x, *packed, out=y)
+            w4.q4k_linear(x, *pk[0], out=ys[0])
+        elif wk.dual:
+            w4.w4a16_linear_dual(x, pk[0], pk[1], Gv, out=(ys[0], ys[1]))
         else:
-            w4.w4a16_linear(x, *packed, G, out=y)
+            w4.w4a16_linear(x, *pk[0], Gv, out=ys[0])
     torch.cuda.synchronize()
     assert w4.w4a16_device_status() == 0
-    print(json.dumps({"profile": args.profile, "format": args.format, "matrix": lin.name, "M": M, "N": lin.N,
-                      "K": lin.K, "G": 32 if q4k else G, "calls": args.warmup + 2}))
+    print(json.dumps({"profile": args.profile, "workload": name, "format": args.format,
+                      "matrix": "+".join(wk.linears[i].name for i in mats), "M": M, "N": lin.N, "K": lin.K,
+                      "G": Gv, "calls": calls, "weight_copies": copies}))
 
 
 # ---------------------------------------------------------------------------
@@ -837,7 +862,10 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--profile", choices=["decode", "prefill"], default=None,
                     help="small case for ncu: one matrix, warmup + 2 calls of one phase")
-    ap.add_argument("--matrix", choices=["0", "1"], default="0", help="with --profile: 0 = gate, 1 = down")
+    ap.add_argument("--matrix", default="0", help="with --profile: the workload's matrix index (70B: 0 = gate, 1 = down)")
+    ap.add_argument("--workload", default="", help="with --profile: a workloads.py workload other than the bench's")
+    ap.add_argument("--m", type=int, default=0, help="with --profile: activation rows")
+    ap.add_argument("--g", type=int, default=0, help="with --profile: group size")
     ap.add_argument("--format", choices=["w4", "q4k"], default="w4",
                     help="with --profile decode: the 4-bit group layout or the super-block layout")
     ap.add_argument("--gpus", type=int, default=1)
