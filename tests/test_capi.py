@@ -330,3 +330,18 @@ def test_multi_argument_errors():
     assert f(v(a + 8), 3, q3, s3, z3, ns(64, 64, 64), 1, 256, 128, y3, v(0)) == 3
     assert f(v(a), 3, q3, s3, z3, ns(64, 64, 64), 0, 256, 128, y3, v(0)) == 0      # empty problem
     assert f(v(a), 3, q3, s3, z3, ns(0, 0, 0), 1, 256, 128, y3, v(0)) == 0
+
+
+def test_host_planning_cost_of_a_call():
+    """The host side of a call is planning, two cached tensor-map lookups and the launch.  The
+    planning part runs here without a GPU (the path query plans both kernels for the shape): it
+    must stay far below a decode launch's 25 us, or the host falls behind the GPU in a decode loop."""
+    import time
+    for _ in range(200):
+        w4.w4a16_linear_path(1, 28672, 8192, 128)
+    n = 5000
+    t = time.perf_counter()
+    for _ in range(n):
+        w4.w4a16_linear_path(1, 28672, 8192, 128)
+    us = (time.perf_counter() - t) / n * 1e6
+    assert us < 20.0, f"{us:.1f} us per path query"

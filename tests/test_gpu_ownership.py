@@ -75,3 +75,27 @@ def test_calls_from_several_threads_on_their_own_streams():
         th.join()
     assert not errors, errors[:5]
     assert w4.w4a16_device_status() == 0
+
+
+def test_host_time_per_decode_call_through_the_binding():
+    """A decode call's host cost (binding, planning, cached tensor maps, launch), measured without
+    synchronising: it must stay below the GPU time of the call it launches (about 25 us on the 70B
+    shapes), or an eager decode loop becomes host-bound."""
+    import time
+    N, K, G = 28672, 8192, 128
+    w = wl.weight_f16(N, K, 0.015, 5)
+    q, s, z = w4.w4a16_pack(w.cuda(), G)
+    x = wl.activations_bf16(1, K, 6).cuda()
+    y = torch.empty(1, N, dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(50):
+        w4.w4a16_linear(x, q, s, z, G, out=y, stream=stream)
+    torch.cuda.synchronize()
+    n = 400
+    t = time.perf_counter()
+    for _ in range(n):
+        w4.w4a16_linear(x, q, s, z, G, out=y, stream=stream)
+    host_us = (time.perf_counter() - t) / n * 1e6
+    torch.cuda.synchronize()
+    assert host_us < 20.0, f"{host_us:.1f} us of host time per call"
+    assert w4.w4a16_device_status() == 0
