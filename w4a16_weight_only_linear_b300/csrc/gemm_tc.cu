@@ -69,6 +69,7 @@ constexpr int kMaxCS = 3;                  // code ring: stages of 128 bytes of 
 constexpr uint32_t kCodeStageBytes = 128u * 128u;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kACol0 = 256;           // D uses columns [0, BN), A slices (64 columns each) [256, 512)
+constexpr uint32_t kParkCol = 448;         // BN = 256 (three A slices): the epilogue parks BF16 pairs here
 constexpr int kNumBars = 3 * kMaxS + 2 * kMaxCS + 2;
 
 // Status codes (bit fields) recorded when a wait gives up.
@@ -584,9 +585,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) tc::mbar_arrive(sm.d_empty());
                 continue;
             }
-            uint32_t packed[128];
+            // BF16 output: the row's columns are rounded into packed pairs and the accumulator is
+            // released before the stores, so the next unit's MMAs overlap them.  At BN = 256 the
+            // first 128 columns' pairs are parked in the 64 tensor-memory columns past the A ring
+            // (the ring then holds three slices, columns 256..447), so at most 64 packed registers
+            // are live and the epilogue does not spill.
+            const bool wide = p.BN > 128;
+            uint32_t packed[64];
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
+            for (int ch = 0; ch < 4; ++ch) {
                 if (ch * 32 < p.BN) {
                     uint32_t v[32];
                     tc::tmem_ld32_wait(d_lane + (uint32_t)ch * 32u, v);
@@ -598,23 +605,54 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            if (wide) {
+                uint32_t h0[32], h1[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    h0[j] = packed[j];
+                    h1[j] = packed[32 + j];
+                }
+                tc::tmem_st32(d_lane + kParkCol, h0);
+                tc::tmem_st32(d_lane + kParkCol + 32u, h1);
+                tc::tmem_wait_st();
+#pragma unroll
+                for (int ch = 4; ch < 8; ++ch) {
+                    uint32_t v[32];
+                    tc::tmem_ld32_wait(d_lane + (uint32_t)ch * 32u, v);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const __nv_bfloat162 b =
+                            __floats2bfloat162_rn(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+                        packed[(ch - 4) * 16 + j] = *reinterpret_cast<const uint32_t*>(&b);
+                    }
+                }
+            }
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(sm.d_empty());
-            if (n < p.N) {
-                unsigned short* yc = reinterpret_cast<unsigned short*>(p.y) + n;
+            // packed holds columns [c0, c0 + 128): the second half when wide, else the only one
+            unsigned short* yc = reinterpret_cast<unsigned short*>(p.y) + n;
+            auto store_pairs = [&](const uint32_t* pr, int c0, int npairs) {
+                if (n >= p.N) return;
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    if (ch * 32 < p.BN) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const int m = m0 + ch * 32 + j;
-                            if (m < p.M) {
-                                const uint32_t pr = packed[ch * 16 + (j >> 1)];
-                                yc[(int64_t)m * p.N] = (unsigned short)((j & 1) ? (pr >> 16) : (pr & 0xFFFFu));
-                            }
-                        }
+                for (int q = 0; q < 32; ++q) {
+                    if (q < npairs) {
+                        const int m = m0 + c0 + 2 * q;
+                        if (m < p.M) yc[(int64_t)m * p.N] = (unsigned short)(pr[q] & 0xFFFFu);
+                        if (m + 1 < p.M) yc[(int64_t)(m + 1) * p.N] = (unsigned short)(pr[q] >> 16);
                     }
+                }
+            };
+            const int c0 = wide ? 128 : 0;
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                if (c0 + h * 64 < p.BN) store_pairs(packed + 32 * h, c0 + h * 64, 32);
+            if (wide) {   // the parked first half (every lane loads: the tensor-memory load is warp-wide)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t v[32];
+                    tc::tmem_ld32_wait(d_lane + kParkCol + 32u * (uint32_t)h, v);
+                    store_pairs(v, h * 64, 32);
                 }
             }
         }
