@@ -40,6 +40,9 @@ GEMM_SHAPES = [
     (17, 136, 256, 32), (32, 264, 640, 64), (100, 520, 1024, 128), (256, 128, 2048, 256),
     (300, 264, 1280, 128), (513, 392, 768, 64), (40, 8, 96, 32), (64, 1032, 4096, 128),
     (777, 136, 512, 256), (1, 264, 1024, 128), (16, 136, 5120, 32),
+    # one activation tile wider than 128 rows (BN = 160, 256): the epilogue parks the first 128
+    # columns' BF16 pairs in tensor memory
+    (160, 264, 1024, 128), (230, 392, 768, 32),
 ]
 
 
@@ -75,17 +78,18 @@ def test_gemm_and_gemv_agree_on_small_batches():
     assert_close(yb, y_ref, "gemv")
 
 
+@pytest.mark.parametrize("M", [40, 200])
 @pytest.mark.parametrize("G", [32, 64, 128, 256])
-def test_gemm_one_hot_rows(G):
+def test_gemm_one_hot_rows(G, M):
     """x rows = e_k: y[i, n] = bf16_rn(fp16_rn(W_hat[n, k_i])).  The kernel's
     weight operand is W_hat rounded once to FP16, and a single product by 1.0
-    accumulates exactly in FP32."""
+    accumulates exactly in FP32.  M = 40 spans two 32-column chunks of the
+    epilogue; M = 200 (BN = 224) its parked first half."""
     N, K = 264, 4 * G
     w = wl.weight_f16(N, K, 0.02, 99 + G)
     q, s, z = oracle.pack(wl.bits_u16(w), G)
     what = oracle.dequant(q, s, z, N, K, G)
     ks = [0, 1, 7, 8, G - 1, G, K - 33, K - 1]
-    M = 40                                           # > 32: two activation-row chunks of the epilogue
     x = torch.zeros(M, K, dtype=torch.bfloat16)
     for i in range(M):
         x[i, ks[i % len(ks)]] = 1.0
