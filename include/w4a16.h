@@ -44,7 +44,8 @@
  *     stream finishes, but it reads and writes no global memory before that
  *     kernel has completed, so stream order keeps its usual meaning.
  *   - Scratch memory: the tensor-core path takes each call's scratch (the
- *     FP16 copy of x; FP32 partial sums when a narrow layer is split along K)
+ *     FP16 copy of x; FP32 partial sums when tiles are split along K: a
+ *     narrow layer's tiles, or the last, partial wave of wider tiles)
  *     from the current device's current memory pool with cudaMallocAsync and
  *     frees it on the stream after the call's kernels; the library keeps no
  *     device memory of its own between calls (the no-allocation entry point

@@ -43,6 +43,8 @@ GEMM_SHAPES = [
     # one activation tile wider than 128 rows (BN = 160, 256): the epilogue parks the first 128
     # columns' BF16 pairs in tensor memory
     (160, 264, 1024, 128), (230, 392, 768, 32),
+    # 100 narrow tiles (more than half the SMs of a B300): each cut in four along K, 400 pieces
+    (17, 12792, 2048, 64),
 ]
 
 
@@ -151,6 +153,47 @@ def test_gemm_repeated_calls_are_identical():
     y0 = w4.w4a16_linear_gemm(xd, *dq, G)
     for _ in range(3):
         assert torch.equal(w4.w4a16_linear_gemm(xd, *dq, G), y0)
+
+
+def _split_shape(case, sms):
+    """(M, N, K, G, R) of a K-split case; R = the tiles cut in two."""
+    if case == "tail":
+        # M = 3000: 256-row activation tiles, 12 per weight tile, the last one ragged; N ragged.
+        # Whole tiles fill the SMs once, then R tiles remain: those are split (K = 4096: 16 stages).
+        ntiles = -(-(sms + 20) // 12)
+        M, N, K, G = 3000, 128 * ntiles - 8, 4096, 128
+        T = 12 * ntiles
+        R = T % sms if T > sms else T
+    else:
+        # 160-row tiles (M = 150), 30 of them, the only wave: every tile is cut in three; K = 6208
+        # (97 slices of 64, a ragged last stage: 25 stages) puts the range boundaries at slices 32
+        # and 64
+        M, N, K, G = 150, 128 * 30 - 40, 6208, 64
+        R = 30
+    return M, N, K, G, R
+
+
+@pytest.mark.parametrize("case", ["tail", "all"])
+def test_gemm_wide_tiles_split_along_k(case):
+    """Wide tiles (BN > 64) of a last wave at most half full are cut along K (in
+    two, or up to three when they are the only wave); y adds the ranges' FP32
+    partials in a fixed order."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    M, N, K, G, R = _split_shape(case, sms)
+    assert 0 < 2 * R <= sms
+    x, (q, s, z), y_ref = _case(M, N, K, G, seed=M + N, outliers=0.002)
+    dq = dev_packed(q, s, z)
+    xd = x.cuda()
+    y = w4.w4a16_linear_gemm(xd, *dq, G)
+    torch.cuda.synchronize()
+    assert_close(y, y_ref, f"split gemm {case} M={M} N={N} K={K} G={G}")
+    for _ in range(2):                               # the partials are added in a fixed order
+        assert torch.equal(w4.w4a16_linear_gemm(xd, *dq, G), y)
+    # FP32 outputs of the same call: unrounded sums, against the oracle's
+    y32 = w4.w4a16_linear_f32(xd, *dq, G, path=2)
+    torch.cuda.synchronize()
+    assert torch.equal(y32.to(torch.bfloat16), y)
+    assert_close(y32, y_ref, f"split gemm fp32 {case}")
 
 
 def test_gemm_no_kernel_gave_up_waiting():

@@ -83,6 +83,10 @@ LAYER = [
     (2, 72, 640, 32, "w8a16_linear_gemv"),
     (9, 264, 1024, 128, "w8a16_linear_gemm"), (17, 136, 256, 32, "w8a16_linear_gemm"),
     (100, 520, 1024, 256, "w8a16_linear_gemm"), (300, 264, 1280, 64, "w8a16_linear_gemm"),
+    # 160-row tiles, 30 of them, K = 2048 (16 stages of 128 8-bit codes): each cut in two along K
+    (150, 3800, 2048, 128, "w8a16_linear_gemm"),
+    # 100 narrow tiles, each cut in four along K
+    (17, 12792, 2048, 128, "w8a16_linear_gemm"),
     (1, 264, 1024, 256, "w8a16_linear"), (4, 264, 2048, 128, "w8a16_linear"), (40, 392, 768, 32, "w8a16_linear"),
 ]
 

@@ -24,21 +24,24 @@
 // rounding; FP16 keeps 11.
 //
 // Structure: a persistent kernel, one 320-thread CTA per SM, warp-specialised.
-//   warp 0      TMA producer: 64-k slices of x (BN rows, 128-byte swizzle) and
-//               code stages of 128 rows x 128 bytes (256 4-bit or 128 8-bit
-//               codes per row, swizzled)
-//   warp 1      tensor-memory owner and MMA issuer (one thread): per 64-k
-//               slice, four 128 x BN x 16 MMAs, A from TMEM, B from smem
+//   warp 0      TMA producer: 128-k slices of x (two 64-k boxes of BN rows,
+//               128-byte swizzle) and code stages of 128 rows x 128 bytes
+//               (256 4-bit or 128 8-bit codes per row, swizzled)
+//   warp 1      tensor-memory owner and MMA issuer (one thread): per 128-k
+//               slice, eight 128 x BN x 16 MMAs and one commit, A from TMEM,
+//               B from smem
 //   warps 2..5  dequantisers: thread = weight row = TMEM lane; codes from
 //               smem -> FP16 pairs with PRMT/LOP3 (no conversion
 //               instruction), code difference and scale in packed FP16 ->
-//               tcgen05.st into a ring of 64-k A slices in TMEM
+//               tcgen05.st into a ring of 128-k A slices in TMEM
 //   warps 6..9  epilogue: tcgen05.ld of the FP32 accumulator, BF16 rounding,
 //               stores to y
 // Tiles are 128 weight rows x BN activation rows (BN <= 256), ordered with the
 // activation tile fastest so consecutive CTAs share a weight tile in L2.  When
-// narrow tiles (BN <= 64) fill at most half the SMs, each is cut along K and
-// the pieces' FP32 partials are added in a fixed order (see GemmParams).
+// narrow tiles (BN <= 64) fill at most half the SMs, each is cut along K; when
+// the last wave of wider tiles is at most half full, its tiles are cut in two
+// along K.  The pieces' FP32 partials are added in a fixed order (see
+// GemmParams).
 // Every wait is bounded: on expiry the kernel records a code in the status
 // word, waits (bounded) for its own copies and MMAs in flight, frees its
 // tensor memory and returns.
@@ -80,18 +83,17 @@ constexpr uint32_t kStatusEpilogue = 1u << 3;
 constexpr uint32_t kStatusDrain = 1u << 4;
 
 // Work units.  A tile is 128 weight rows x BN activation rows; units [0, full)
-// are whole tiles (tile = unit).  When there are few tiles for the SMs and a
-// tile is narrow (small M, where a tile's time is its weight streaming and
-// expansion), the last `split` tiles are each cut along K into `parts` ranges
-// of code stages, unit full + j * split + i being range j of tile
-// full + i.  A range's FP32 partial goes to a workspace, and the last of a
+// are whole tiles (tile = unit).  The last `split` tiles (all of them when
+// narrow tiles are few for the SMs; the last, partial wave of wider tiles) are
+// each cut along K into `parts` ranges of code stages, unit full + j * split
+// + i being range j of tile full + i.  A range's FP32 partial goes to a workspace, and the last of a
 // tile's ranges to finish adds them in a fixed order (so results do not
 // depend on arrival order) and writes y.
 struct GemmParams {
     const unsigned short* s;   // FP16 scales [N, lds]
     const uint32_t* z;         // packed zeros [N, ldz] (4-bit: 8 per word; 8-bit: 4 per word)
     void* y;                   // [M, N], BF16 (or FP32 when yf32)
-    float* ws;                 // K-split partials [split * parts][BN][128]
+    float* ws;                 // K-split partials [split * parts][BN / 4][128][4]
     uint32_t* cnt;             // arrivals per K-split tile (zero at launch)
     int yf32;                  // 1: FP32 outputs (no BF16 rounding)
     int M, N, K, BN;
@@ -232,59 +234,106 @@ __device__ __forceinline__ bool epilogue_all(bool v) {
     return r != 0;
 }
 
-// Epilogue of one K range of a split tile (BN <= 64; the four epilogue warps,
-// thread r = weight row r of the tile): the accumulator goes 16 columns at a
-// time to the FP32 workspace (row r of column m at [part][m][r], so a warp
-// writes 128 contiguous bytes per column) and is released, and the last of the
-// tile's ranges to arrive adds the partials in a fixed order and writes y.
-__device__ __forceinline__ void epilogue_partial(const GemmParams& p, const Smem& sm, const Unit& U, int n, int m0,
-                                                 uint32_t d_lane, int lane, int r) {
-    float* wp = p.ws + (size_t)U.part * p.BN * kBM + r;
-#pragma unroll 1
-    for (int c = 0; c < p.BN; c += 16) {
-        uint32_t v[16];
-        tc::tmem_ld16_wait(d_lane + (uint32_t)c, v);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) __stcg(wp + (size_t)(c + j) * kBM, __uint_as_float(v[j]));
-    }
+// Epilogue of one K range of a split tile (the four epilogue warps, thread r =
+// weight row r of the tile).  A range's FP32 partial goes to the workspace in
+// quads of activation rows, [part][m / 4][r][m % 4], so that thread r moves 16
+// bytes per access and a warp 512 contiguous bytes; the last of the tile's
+// ranges to finish adds every range's partial in range order and
+// writes y.  A range that finds the others all done before it writes skips
+// its own write, and a range that is its CTA's last unit (hold) keeps its
+// accumulator in tensor memory until its sum is done; when the summing range
+// still holds its accumulator it reads its own partial from there, the same
+// FP32 values, so the result does not depend on which range sums.
+__device__ __forceinline__ void release_accumulator(const Smem& sm, int lane) {
     tc::tc_fence_before();
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(sm.d_empty());
-    __threadfence();
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* a) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void epilogue_partial(const GemmParams& p, const Smem& sm, const Unit& U, int n, int m0,
+                                                 uint32_t d_lane, int lane, int r, bool hold) {
+    const uint32_t others = (uint32_t)(p.parts - 1);
+    if (threadIdx.x == 6 * 32) *sm.last_flag = ld_acquire_u32(p.cnt + U.stile) == others;
     epilogue_sync();
-    if (threadIdx.x == 6 * 32) *sm.last_flag = atomicAdd(p.cnt + U.stile, 1u) == (uint32_t)(p.parts - 1);
-    epilogue_sync();
-    const bool last = *sm.last_flag != 0;
+    bool last = *sm.last_flag != 0;
     epilogue_sync();                                  // every thread has read the flag
-    if (!last) return;
+    bool own_tmem = last;                             // this range's partial is still in tensor memory
+    if (!last) {
+        float4* wp = reinterpret_cast<float4*>(p.ws + (size_t)U.part * p.BN * kBM) + r;
+#pragma unroll 1
+        for (int c = 0; c < p.BN; c += 16) {
+            uint32_t v[16];
+            tc::tmem_ld16_wait(d_lane + (uint32_t)c, v);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                __stcg(wp + (size_t)(c / 4 + q) * kBM,
+                       make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                   __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3])));
+        }
+        if (!hold) release_accumulator(sm, lane);
+        __threadfence();
+        epilogue_sync();
+        if (threadIdx.x == 6 * 32) *sm.last_flag = atomicAdd(p.cnt + U.stile, 1u) == others;
+        epilogue_sync();
+        last = *sm.last_flag != 0;
+        epilogue_sync();
+        if (!last) {
+            if (hold) release_accumulator(sm, lane);
+            return;
+        }
+        own_tmem = hold;
+    }
     __threadfence();
     const int lim = min(p.BN, p.M - m0);              // activation rows of the tile
-    const float* wt = p.ws + (size_t)U.stile * p.parts * p.BN * kBM + r;
+    const int own = U.part - U.stile * p.parts;       // this unit's range
+    const float4* wt = reinterpret_cast<const float4*>(p.ws + (size_t)U.stile * p.parts * p.BN * kBM) + r;
 #pragma unroll 1
-    for (int h = 0; h < lim; h += 16) {
-        float acc[16];
+    for (int h = 0; h < lim; h += 32) {
+        float acc[32];
 #pragma unroll
-        for (int ml = 0; ml < 16; ++ml) acc[ml] = 0.0f;
+        for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
 #pragma unroll 1
-        for (int j = 0; j < p.parts; ++j) {          // the 16 loads of one partial in flight together
-            const float* wj = wt + ((size_t)j * p.BN + h) * kBM;
+        for (int j = 0; j < p.parts; ++j) {           // ranges in order; 32 values of one in flight
+            float v[32];
+            if (j == own && own_tmem) {
+                uint32_t b[32];
+                tc::tmem_ld32_wait(d_lane + (uint32_t)h, b);
 #pragma unroll
-            for (int ml = 0; ml < 16; ++ml)
-                if (h + ml < lim) acc[ml] += __ldcg(wj + (size_t)ml * kBM);
+                for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(b[i]);
+            } else {
+                const float4* wj = wt + ((size_t)j * p.BN + h) / 4 * kBM;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float4 f = __ldcg(wj + (size_t)q * kBM);
+                    v[4 * q] = f.x;
+                    v[4 * q + 1] = f.y;
+                    v[4 * q + 2] = f.z;
+                    v[4 * q + 3] = f.w;
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[i] += v[i];
         }
         if (n < p.N) {
 #pragma unroll
-            for (int ml = 0; ml < 16; ++ml) {
-                if (h + ml < lim) {
-                    const int64_t o = (int64_t)(m0 + h + ml) * p.N + n;
+            for (int i = 0; i < 32; ++i) {
+                if (h + i < lim) {
+                    const int64_t o = (int64_t)(m0 + h + i) * p.N + n;
                     if (p.yf32)
-                        static_cast<float*>(p.y)[o] = acc[ml];
+                        static_cast<float*>(p.y)[o] = acc[i];
                     else
-                        static_cast<__nv_bfloat16*>(p.y)[o] = __float2bfloat16_rn(acc[ml]);
+                        static_cast<__nv_bfloat16*>(p.y)[o] = __float2bfloat16_rn(acc[i]);
                 }
             }
         }
     }
+    if (own_tmem) release_accumulator(sm, lane);
 }
 
 // One 64-k slice of A from 8-bit codes (the word layout): the slice's 64 codes
@@ -559,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             dph ^= 1u;
             tc::tc_fence_after();
             if (U.part >= 0) {
-                epilogue_partial(p, sm, U, n, m0, d_lane, lane, r);
+                epilogue_partial(p, sm, U, n, m0, d_lane, lane, r, u + (int)gridDim.x >= p.units);
                 continue;
             }
             if (p.yf32) {
@@ -743,22 +792,37 @@ cudaError_t convert_x(const void* x, void* x16, int64_t M, int64_t K, int64_t kx
 }
 
 // K split.  Narrow tiles (BN <= 64: small M, where a tile's time is its
-// weight streaming and expansion) that fill at most half the SMs are each cut
-// along K into s ranges of the nst code stages, s chosen to minimise an
-// estimate in stage times: the waves of pieces times their length, plus about
-// 0.1 stage per piece for its partial and the final reduction.  Among
-// estimates within 1 % of the best the smallest s wins.  Wider tiles, or
-// enough of them to fill the SMs, run whole.
+// weight streaming and expansion) are each cut along K into s ranges of the
+// nst code stages, s chosen to minimise an estimate in stage times: the waves
+// of pieces times their length, plus about 0.1 stage per piece for its
+// partial and the final reduction.  Among estimates within 1 % of the best the
+// smallest s wins.  Tiles that fill at most half the SMs always split; up to
+// four waves of them split when the estimate gains at least 10 % (a partial
+// wave evened out: 108 tiles in 4 ranges fill 148 SMs about three times).
+// Wider tiles run whole, except the R tiles of a last wave that is at most
+// half full (2R <= SMs) when K spans at least 16 code stages: those are cut in
+// two, so that wave takes about half a tile plus the partials' write and
+// reduction (a 128 x BN FP32 partial per piece) instead of a whole tile; when
+// they are the only wave, in up to three (at least 8 stages each) as the SMs
+// allow.
 void choose_split(int T, int nst, int BN, int sms, GemmParams& p) {
     p.full = T;
     p.split = 0;
     p.parts = 1;
-    if (BN > 64 || 2 * T > sms || nst < 2) return;
+    if (BN > 64) {
+        const int R = T % sms;
+        if (R == 0 || 2 * R > sms || nst < 16) return;
+        p.full = T - R;
+        p.split = R;
+        p.parts = T < sms ? std::max(2, std::min(std::min(sms / T, 3), nst / 8)) : 2;
+        return;
+    }
+    if (T > 4 * sms || nst < 2) return;
     auto cost = [&](int c) {
         const int waves = (T * c + sms - 1) / sms;
         return waves * ((double)((nst + c - 1) / c) + 0.1) + (c > 1 ? 0.1 * c : 0.0);
     };
-    const int smax = std::min(nst, 16);
+    const int smax = std::min(std::min(nst, 16), std::max(1, 6 * sms / T));   // at most 6 pieces per SM
     double best = cost(1);
     for (int c = 2; c <= smax; ++c) best = std::min(best, cost(c));
     int s = 1;
@@ -767,7 +831,7 @@ void choose_split(int T, int nst, int BN, int sms, GemmParams& p) {
             s = c;
             break;
         }
-    if (s > 1) {
+    if (s > 1 && (2 * T <= sms || cost(s) <= 0.9 * cost(1))) {
         p.full = 0;
         p.split = T;
         p.parts = s;
