@@ -153,8 +153,10 @@ W4A16_API w4a16_status w4a16_dequant_f16(const uint32_t* qweight, const void* sc
  * w4a16_linear: y[M,N] (BF16) = x[M,K] (BF16) * W_hat^T, FP32 accumulation,
  * one round-to-nearest-even to BF16 per output.  Dispatch: M <= 8 runs the
  * bandwidth-bound decode GEMV (when x of M rows fits the kernel's shared
- * memory), anything else runs the tcgen05 tensor-core GEMM (measured: on a
- * 5120 -> 13824 layer the GEMM is already the faster kernel at M = 16).  Decode is
+ * memory), and so does M = 9..16 where the GEMV runs with all its warps and
+ * also takes M = 8 (long rows then split K over a two-CTA cluster; measured
+ * on a 5120 -> 13824 layer at M = 16: 27.4 us against 33.7 us for the GEMM);
+ * anything else runs the tcgen05 tensor-core GEMM.  Decode is
  * weight-bandwidth bound and prefill compute bound (klaylearn glossary, FAQ
  * "Why is it especially useful for decode?"; multigrid.ai, section "Where it
  * stops being the right answer").
@@ -170,7 +172,8 @@ W4A16_API w4a16_status w4a16_linear(const void* x_bf16, const uint32_t* qweight,
  *   y_gate = x * W_hat_gate^T,  y_up = x * W_hat_up^T.
  * Both weights share K, N and G.  Paired gate/up traversal is the zhuai.tech
  * page's section 2 ("Moving fewer bytes can make decode faster") workload.
- * M <= 8 runs the dual GEMV; larger M runs the GEMM once per projection.
+ * The dual GEMV runs where one matrix of twice the rows would (M <= 8, or
+ * 9..16 with all its warps); otherwise the GEMM runs once per projection.
  */
 W4A16_API w4a16_status w4a16_linear_dual(const void* x_bf16,
                                const uint32_t* qweight_gate, const void* scales_gate,
@@ -196,8 +199,9 @@ W4A16_API w4a16_status w4a16_linear_dual(const void* x_bf16,
  *               [M, N[i]]
  *   N           HOST array of nmat output sizes (multiples of 8; 0 = skip)
  * M <= 8 runs one decode launch over all the matrices (when their rows fit
- * the kernel's shared memory); larger M runs the tensor-core kernel once per
- * matrix on one FP16 copy of x.  The arrays are read during the call only.
+ * the kernel's shared memory), and so does M = 9..16 where that launch runs
+ * with all its warps; otherwise the tensor-core kernel runs once per matrix on
+ * one FP16 copy of x.  The arrays are read during the call only.
  * Errors: W4A16_ERR_INVALID_ARG for nmat outside 1..4 or a null array, else
  * as w4a16_linear for each matrix.
  */

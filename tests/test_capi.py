@@ -246,13 +246,13 @@ def test_path_query_rejects_bad_shapes():
                                  (8192, 28672)])
 @pytest.mark.parametrize("G", [32, 64, 128, 256])
 def test_dispatch_rule(N, K, G):
-    """Host-only dispatch: the decode GEMV up to M = 8 where its x staging and tables fit, the tensor-core
-    GEMM above; M = 1 fits at every workload shape, and once a batch size leaves the GEMV every larger
-    one does too."""
+    """Host-only dispatch: the decode GEMV up to M = 8 where its x staging and tables fit, and up to
+    M = 16 where it runs with all its warps; the tensor-core GEMM above.  M = 1 fits at every workload
+    shape, and once a batch size leaves the GEMV every larger one does too."""
     paths = [w4.w4a16_linear_path(M, N, K, G) for M in range(1, 20)]
     assert set(paths) <= {1, 2}
     assert paths[0] == 1
-    assert all(p == 2 for p in paths[8:])                      # M >= 9
+    assert all(p == 2 for p in paths[16:])                     # M >= 17
     first_gemm = paths.index(2)
     assert all(p == 2 for p in paths[first_gemm:])
     assert w4.w4a16_linear_path(2048, N, K, G) == 2

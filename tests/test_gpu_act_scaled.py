@@ -124,11 +124,22 @@ def test_act_scaled_workload(j, M):
     assert_close(y, y_ref, f"ffn13b_awq/{lin.name} M={M}")
 
 
+def test_scale_with_the_k_split():
+    """M = 16 on 8192-long rows: the decode kernel splits K over a two-CTA cluster, each CTA
+    staging (and scaling) its half of x."""
+    N, K, G, M = 520, 8192, 128, 16
+    x, xs, (q, s, z) = _problem(M, N, K, G, seed=77, scale="arbitrary")
+    assert w4.w4a16_linear_path(M, N, K, G) == 1
+    y = w4.w4a16_linear_act_scaled(x.cuda(), xs.cuda(), *dev_packed(q, s, z), G)
+    torch.cuda.synchronize()
+    assert_close(y, oracle.linear_xs(wl.bits_u16(x), xs.numpy(), q, s, z, N, K, G), "k-split scaled")
+
+
 def test_both_kernels_take_the_scale():
     """The explicit-path entries are not scaled; run both kernels through the
     act-scaled entry at an M each one serves and compare with the oracle."""
     N, K, G = 264, 1024, 128
-    for M in (8, 9):
+    for M in (8, 17):
         x, xs, (q, s, z) = _problem(M, N, K, G, seed=21 + M, scale="arbitrary")
         assert w4.w4a16_linear_path(M, N, K, G) == (1 if M <= 8 else 2)
         y = w4.w4a16_linear_act_scaled(x.cuda(), xs.cuda(), *dev_packed(q, s, z), G)

@@ -56,7 +56,7 @@ def test_gemm_parity(M, N, K, G):
     assert_close(y, y_ref, f"gemm M={M} N={N} K={K} G={G}")
 
 
-@pytest.mark.parametrize("M", [9, 16, 17, 48, 600])
+@pytest.mark.parametrize("M", [17, 48, 600])
 def test_linear_dispatches_to_gemm(M):
     N, K, G = 264, 1024, 128
     assert w4.w4a16_linear_path(M, N, K, G) == 2

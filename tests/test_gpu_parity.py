@@ -100,7 +100,30 @@ def test_gemv_long_rows_with_streamed_scales(M, N, K):
     assert_close(y, y_ref, f"gemv long rows M={M} N={N} K={K} G={G}")
 
 
-@pytest.mark.parametrize("M", [1, 4, 8])
+# M = 9..16 with long rows: x (M * K FP16) would leave the kernel a short weight ring or no room,
+# so two CTAs of a cluster each stage and stream half of every row's chunks and add their partial
+# sums through distributed shared memory.  Odd chunk counts (rank 1 streams one fewer), a last
+# chunk cut short (K % 256 != 0), several CTA pairs, ragged N.
+KSPLIT_SHAPES = [(16, 520, 8192, 128), (9, 136, 12288, 64), (12, 1032, 5120, 256), (11, 392, 6336, 64),
+                 (16, 264, 6400, 128)]
+
+
+@pytest.mark.parametrize("M,N,K,G", KSPLIT_SHAPES)
+def test_gemv_k_split_across_a_cluster(M, N, K, G):
+    w, x, (q, s, z), y_ref = _case(M, N, K, G, seed=M * 13 + N + K + G, outliers=0.002)
+    dq = dev_packed(q, s, z)
+    xd = x.cuda()
+    y = w4.w4a16_linear_gemv(xd, *dq, G)
+    torch.cuda.synchronize()
+    assert_close(y, y_ref, f"gemv k-split M={M} N={N} K={K} G={G}")
+    assert torch.equal(w4.w4a16_linear_gemv(xd, *dq, G), y)          # the two ranks add in a fixed order
+    y32 = w4.w4a16_linear_f32(xd, *dq, G, path=1)
+    torch.cuda.synchronize()
+    assert torch.equal(y32.to(torch.bfloat16), y)
+    assert w4.w4a16_device_status() == 0
+
+
+@pytest.mark.parametrize("M", [1, 4, 8, 9, 16])
 def test_linear_dispatches_to_gemv(M):
     N, K, G = 264, 1024, 128
     assert w4.w4a16_linear_path(M, N, K, G) == 1
@@ -172,16 +195,21 @@ def test_dual_parity(M, N, K, G):
     torch.cuda.synchronize()
     assert_close(yg, yg_ref, "dual gate")
     assert_close(yu, yu_ref, "dual up")
-    # Against the single-matrix call that dispatches the same way (the decode
-    # GEMV up to M = 8, the tensor-core GEMM above): the dual GEMV splits the
-    # concatenated tiles of both matrices over the SMs, so a tile's partial
-    # sums may be added in a different order than in a single-matrix call, and
-    # the two agree to within one BF16 ulp.
-    assert w4.w4a16_linear_path(M, N, K, G) == (1 if M <= 8 else 2)
-    for y2, y1 in ((yg, w4.w4a16_linear(xd, *dg, G)), (yu, w4.w4a16_linear(xd, *du, G))):
+    # Against a single-matrix call of the kernel the dual call ran (the decode GEMV
+    # up to M = 8; at M = 9..16 the GEMV where two matrices' x leaves it all its
+    # warps, else the tensor-core GEMM): the dual GEMV splits the concatenated
+    # tiles of both matrices over the SMs, so a tile's partial sums may be added
+    # in a different order than in a single-matrix call, and the two agree to
+    # within one BF16 ulp.
+    def within_ulp(y2, y1):
         a, b = y2.double().cpu().numpy(), y1.double().cpu().numpy()
-        ulp = bf16_ulp(np.maximum(np.abs(a), np.abs(b)))
-        assert np.all(np.abs(a - b) <= ulp)
+        return bool(np.all(np.abs(a - b) <= bf16_ulp(np.maximum(np.abs(a), np.abs(b)))))
+
+    for y2, d in ((yg, dg), (yu, du)):
+        if M <= 8:
+            assert within_ulp(y2, w4.w4a16_linear_gemv(xd, *d, G))
+        else:
+            assert within_ulp(y2, w4.w4a16_linear_gemv(xd, *d, G)) or within_ulp(y2, w4.w4a16_linear_gemm(xd, *d, G))
 
 
 # --------------------------------------------------------------------------

@@ -249,7 +249,8 @@ def w4a16_linear_dual(x, gate, up, G, out=None, stream=None):
 
 def w4a16_linear_multi(x, mats, G, out=None, stream=None):
     """[x * W_hat_i^T for each (qweight, scales, zeros) in mats] (1..4 matrices
-    sharing x, each with its own output size), in one decode launch at M <= 8."""
+    sharing x, each with its own output size), in one decode launch at M <= 8
+    (and M <= 16 where that launch runs with all its warps)."""
     M, K = x.shape
     n = len(mats)
     if not 1 <= n <= 4:

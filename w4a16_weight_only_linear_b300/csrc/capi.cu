@@ -43,14 +43,26 @@ w4a16_status from_cuda(cudaError_t e) {
 }
 
 // Path for a shape whose arguments are valid: 1 = GEMV, 2 = GEMM.
-// Automatic dispatch: the decode GEMV up to 8 activation rows.  Above that the GEMV needs
-// two MMA column blocks per tile, and on the 13B up-projection sweep (5120 -> 13824, every
-// G in {32, 64, 128, 256}) the tensor-core GEMM is already faster at M = 16.
-constexpr int64_t kGemvDispatchMaxM = 8;
+// Automatic dispatch: the decode GEMV up to 8 activation rows wherever it fits, and up to 16
+// where it runs with all its warps (two MMA column blocks per tile; x of long rows split
+// along K over a two-CTA cluster) and also takes M = 8, so that a shape leaves the GEMV at
+// one batch size for good.  Measured on one B300 at M = 9-16: 5120 -> 13824 (G = 128)
+// 20.1-27.4 us against the tensor-core call's 36.2 us, 5120 -> 5120 at M = 16 17.5 against
+// 26.0 us.  Where x crowds out the GEMV's weight rings it loses (43.8 against 35 us at
+// M = 16 before the K split), hence the full-warp condition.
+constexpr int64_t kGemvDispatchMaxM = 16;
+constexpr int64_t kGemvAnyFitMaxM = 8;
+
+bool gemv_dispatch(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G) {
+    if (M <= kGemvAnyFitMaxM) return w4a16::gemv_fits(M, Ns, nmat, K, G);
+    return M <= kGemvDispatchMaxM && w4a16::gemv_fits(kGemvAnyFitMaxM, Ns, nmat, K, G) &&
+           w4a16::gemv_runs_full(M, Ns, nmat, K, G);
+}
 
 int choose_path(int64_t M, int64_t N, int64_t K, int G, int nmat) {
-    if (M <= kGemvDispatchMaxM && w4a16::gemv_fits(M, N, K, G, nmat)) return 1;
-    return 2;
+    int64_t Ns[w4a16::kMaxMat];
+    for (int i = 0; i < w4a16::kMaxMat; ++i) Ns[i] = N;
+    return gemv_dispatch(M, Ns, nmat, K, G) ? 1 : 2;
 }
 
 w4a16_status linear_common(const void* x, const uint32_t* q, const void* s, const uint32_t* z, int64_t M,
@@ -117,8 +129,7 @@ w4a16_status multi_common(const void* x, int nmat, const uint32_t* const* q, con
     if (!x) return W4A16_ERR_INVALID_ARG;
     if (!aligned16(x)) return W4A16_ERR_MISALIGNED;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    if (M <= kGemvDispatchMaxM && w4a16::gemv_fits(M, Nl, n, K, G))
-        return from_cuda(w4a16::launch_gemv(x, mats, n, M, 0, K, G, cs));
+    if (gemv_dispatch(M, Nl, n, K, G)) return from_cuda(w4a16::launch_gemv(x, mats, n, M, 0, K, G, cs));
     return from_cuda(w4a16::launch_gemm(x, mats, n, M, 0, K, G, cs));
 }
 

@@ -1,5 +1,6 @@
 // gemm_tc.cu -- prefill path of the W4A16 linear layer on the tcgen05 tensor
-// cores (any M; the library routes M > 8 here, and decode shapes whose x the
+// cores (any M; the library routes M > 16 here, M = 9..16 where the decode
+// kernel would not run with all its warps, and decode shapes whose x the
 // decode kernel cannot stage).
 //
 // At prefill many activation rows share each weight, so the layer is a dense

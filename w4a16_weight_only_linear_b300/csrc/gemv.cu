@@ -1,5 +1,6 @@
 // gemv.cu -- decode path of the W4A16 linear layer (up to 16 activation rows;
-// the library dispatches M <= 8 here).
+// the library dispatches M <= 8 here, and M <= 16 where the kernel runs with
+// all its warps).
 //
 // Decode rereads every weight for each generated token with little work per
 // weight, so this kernel is bound by HBM bandwidth on the packed weights
@@ -66,6 +67,12 @@
 // particular order), and x is staged while the first units are in flight.
 // Small layers run an 8-warp instance that leaves room for a second CTA per
 // SM; its CTAs ask L2 for their rows before the grid-dependency wait.
+//
+// K split.  At M > 8 on long rows the staged x (M * K FP16) would leave the
+// weight rings too little shared memory; a cluster of two CTAs on two SMs
+// then takes each tile range, each CTA streaming and staging half of every
+// row's chunks, and the two add their partial sums through distributed shared
+// memory (see gemv_kernel's KS).
 //
 // Instances cover one matrix, a pair (the dual call) or up to four sharing x.
 #include <cuda.h>
@@ -145,6 +152,9 @@ struct GemvParams {
     int rows_cap;                          // weight rows per CTA the partial buffer holds
     long long spin_limit;                  // cycles a bounded wait spins before it gives up
     int withhold;                          // test hook: warp 0 of CTA 0 never issues its first unit
+    int ks;                                // 1: K split across the two CTAs of a cluster (see gemv_kernel)
+    int Ct, kc1;                           // KS: chunks per row; rank 0 streams chunks [0, kc1) of each
+                                           // tile, rank 1 [kc1, Ct); C = kc1 sizes the staged x
 };
 
 struct Layout {
@@ -254,6 +264,29 @@ struct CodeMaps<NM, false> {
 // 100 KB per CTA at K = 28672) and would crowd the weight ring out of shared memory.
 __host__ __device__ constexpr bool meta_streamed(int G) { return G == 32; }
 
+// Thread-block cluster helpers (the K split): this CTA's rank in its cluster,
+// a barrier of all threads of the cluster (release / acquire, so shared-memory
+// writes before it are visible to the peer after it), the peer's address of a
+// shared-memory location, and a load from there.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_map(uint32_t smem_addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 // Bounded wait on a barrier phase (gives up after `limit` cycles); the thread
 // sleeps between polls.
 __device__ __forceinline__ bool gemv_wait(uint32_t bar, uint32_t parity, long long limit) {
@@ -272,7 +305,12 @@ __device__ __forceinline__ bool gemv_wait(uint32_t bar, uint32_t parity, long lo
 // (parity, segment) pairs and each lane holds at most one useful D value per
 // row, so the block-end correction is done once per row on that value only.
 // NM: matrices the instance takes (1, 2, or 4 for three or four).
-template <int NB, int G, int H, bool M1, int PT, int FMT, int NM, bool DUO = false>
+// KS: the K split.  Where M * K of x would crowd out the weight ring (two
+// column blocks, long rows), each tile range is taken by a cluster of two
+// CTAs on two SMs: rank r streams and stages only its half of the chunks of
+// every row, and at the end the two CTAs add both ranks' partial sums, read
+// through distributed shared memory, in a fixed order.
+template <int NB, int G, int H, bool M1, int PT, int FMT, int NM, bool DUO = false, bool KS = false>
 __global__ void __launch_bounds__(DUO ? kDuoWarps * 32 : cta_warps(NB, G) * 32, DUO ? 2 : 1)
     gemv_kernel(const __grid_constant__ CodeMaps<NM, meta_streamed(G)> tm, const GemvParams p) {
     constexpr int V = G >= 128 ? 4 : G / 32;      // words per lane per code load
@@ -301,10 +339,18 @@ __global__ void __launch_bounds__(DUO ? kDuoWarps * 32 : cta_warps(NB, G) * 32, 
 
     // ---- this CTA's tiles and this warp's run of chunks -------------------------
     const int T = p.total_tiles;
-    const int tile0 = (int)((blockIdx.x * (uint32_t)T) / gridDim.x);        // T * grid < 2^32 (host check)
-    const int tile1 = (int)(((blockIdx.x + 1) * (uint32_t)T) / gridDim.x);
+    uint32_t crank = 0, cid = blockIdx.x, ncl = gridDim.x;    // KS: rank in the cluster, cluster, clusters
+    if constexpr (KS) {
+        crank = cluster_ctarank();
+        cid = blockIdx.x >> 1;
+        ncl = gridDim.x >> 1;
+    }
+    const int Cw = KS ? (crank == 0 ? p.kc1 : p.Ct - p.kc1) : p.C;   // chunks per tile this CTA streams
+    const int kc0 = KS ? (int)crank * p.kc1 : 0;                      // the first of them in the row
+    const int tile0 = (int)((cid * (uint32_t)T) / ncl);        // T * grid < 2^32 (host check)
+    const int tile1 = (int)(((cid + 1) * (uint32_t)T) / ncl);
     const int tc_ = tile1 - tile0;
-    const int chunks = tc_ * p.C;                 // < 2^26 (host check), so products below fit 32 bits
+    const int chunks = tc_ * Cw;                  // < 2^26 (host check), so products below fit 32 bits
     const bool active = warp < p.warps;
     const int ch0 = active ? (warp * chunks) / p.warps : 0;        // this warp's chunks [ch0, ch1)
     const int ch1 = active ? ((warp + 1) * chunks) / p.warps : 0;
@@ -318,8 +364,8 @@ __global__ void __launch_bounds__(DUO ? kDuoWarps * 32 : cta_warps(NB, G) * 32, 
     // tile or the run ends; producer and consumer walk the same sequence.
     int it_n = 0, it_ch = ch0, it_tl = 0, it_c = 0;   // units issued; next chunk, its tile and chunk in it
     if (active) {
-        it_tl = ch0 / p.C;
-        it_c = ch0 - it_tl * p.C;
+        it_tl = ch0 / Cw;
+        it_c = ch0 - it_tl * Cw;
     }
     // test hook: warp 0 of CTA 0 never issues its first unit, so its wait on it runs out
     const bool withhold = p.withhold && blockIdx.x == 0 && warp == 0;
@@ -341,9 +387,9 @@ __global__ void __launch_bounds__(DUO ? kDuoWarps * 32 : cta_warps(NB, G) * 32, 
 #pragma unroll
                 for (int i = 1; i < NM; ++i)
                     if (mat == i) map = &tm.m[i];
-                tc::tma_prefetch_2d(map, pf_c * 32, (tau - p.tstart[mat]) * 16);
+                tc::tma_prefetch_2d(map, (kc0 + pf_c) * 32, (tau - p.tstart[mat]) * 16);
             }
-            if (++pf_c == p.C) {
+            if (++pf_c == Cw) {
                 pf_c = 0;
                 ++pf_tl;
             }
@@ -355,29 +401,30 @@ __global__ void __launch_bounds__(DUO ? kDuoWarps * 32 : cta_warps(NB, G) * 32, 
         const int tile = tau - p.tstart[mat];
         const uint32_t slot = (uint32_t)(it_n & (nsl - 1));
         const uint32_t bar = bar0 + 8u * slot;
-        const bool two = it_c + 1 < p.C && it_ch + 1 < ch1;
+        const bool two = it_c + 1 < Cw && it_ch + 1 < ch1;
         if (copy) {
             tc::mbar_arrive_expect_tx(bar, (uint32_t)(two ? 2 * kBoxBytes : kBoxBytes) + (MS ? kMetaBytes : 0u));
             const void* map = &tm.m[0];
 #pragma unroll
             for (int i = 1; i < NM; ++i)
                 if (mat == i) map = &tm.m[i];
-            tc::tma_load_2d(ring + slot * (uint32_t)kUnitBytes, map, it_c * 32, tile * 16, bar);
+            tc::tma_load_2d(ring + slot * (uint32_t)kUnitBytes, map, (kc0 + it_c) * 32, tile * 16, bar);
             if (two)
-                tc::tma_load_2d(ring + slot * (uint32_t)kUnitBytes + kBoxBytes, map, (it_c + 1) * 32, tile * 16, bar);
+                tc::tma_load_2d(ring + slot * (uint32_t)kUnitBytes + kBoxBytes, map, (kc0 + it_c + 1) * 32, tile * 16,
+                                bar);
             if constexpr (MS) {   // the scales of chunks it_c, it_c + 1 (a box of 16 halves per virtual row)
                 const void* smap = &tm.s[0];
 #pragma unroll
                 for (int i = 1; i < NM; ++i)
                     if (mat == i) smap = &tm.s[i];
-                tc::tma_load_2d(mring + slot * (uint32_t)kMetaBytes, smap, it_c * 8, tile * 16, bar);
+                tc::tma_load_2d(mring + slot * (uint32_t)kMetaBytes, smap, (kc0 + it_c) * 8, tile * 16, bar);
             }
         }
         const int n = two ? 2 : 1;
         ++it_n;
         it_ch += n;
         it_c += n;
-        if (it_c == p.C) {
+        if (it_c == Cw) {
             it_c = 0;
             ++it_tl;
         }
@@ -467,6 +514,7 @@ __global__ void __launch_bounds__(DUO ? kDuoWarps * 32 : cta_warps(NB, G) * 32, 
         uint4* xs = reinterpret_cast<uint4*>(base + L.xs);
         float2* exs = reinterpret_cast<float2*>(base + L.exs);
         const int kseg = p.K / P;                        // real codes per segment
+        const int kbase = kc0 * 256;                    // KS: first channel of this CTA's window
         constexpr int GW = G / 8;                          // words per group
         constexpr int XB = 8;                              // items per batch
         const int dxc = kWarps / C, dc = kWarps - dxc * C;                 // item step as (column, block)
@@ -491,8 +539,8 @@ __global__ void __launch_bounds__(DUO ? kDuoWarps * 32 : cta_warps(NB, G) * 32, 
                 vv[j] = make_uint4(0u, 0u, 0u, 0u);
                 const int pseg = (int)(((uint32_t)bxc[j] * minv) >> 16), m = bxc[j] - pseg * M;
                 const int wseg = bc[j] * 32 + lane;
-                if (bxc[j] < xcols && wseg * 8 < kseg) {
-                    int kk = pseg * kseg + wseg * 8;       // channel of the layer (< 2 kx)
+                if (bxc[j] < xcols && kbase + wseg * 8 < kseg) {
+                    int kk = pseg * kseg + kbase + wseg * 8;       // channel of the layer (< 2 kx)
                     if constexpr (W8) {                    // the word's four real channels
                         const uint2 h = *reinterpret_cast<const uint2*>(p.x + (int64_t)m * p.kx + kk / 2);
                         vv[j] = make_uint4(h.x, h.y, 0u, 0u);
@@ -529,8 +577,8 @@ __global__ void __launch_bounds__(DUO ? kDuoWarps * 32 : cta_warps(NB, G) * 32, 
                         f[2 * q + 1] = bf16hi_to_f32(in[q]);
                     }
                 }
-                if (p.xsc != nullptr && wseg * 8 < kseg) {  // activation scale: x_k * xsc_k in FP32
-                    int kk = pseg * kseg + wseg * 8;
+                if (p.xsc != nullptr && kbase + wseg * 8 < kseg) {  // activation scale: x_k * xsc_k in FP32
+                    int kk = pseg * kseg + kbase + wseg * 8;
                     kk -= kk >= p.kx ? p.kx : 0;
                     const float4* sp = reinterpret_cast<const float4*>(p.xsc + kk);
                     const float4 s0 = sp[0], s1 = sp[1];
@@ -670,7 +718,7 @@ __global__ void __launch_bounds__(DUO ? kDuoWarps * 32 : cta_warps(NB, G) * 32, 
         // slot of the first tile of the run: warps before this one that hold chunks of it
         int first_slot = 0;
         {
-            const int fch = (ch0 / p.C) * p.C;              // the tile's first chunk
+            const int fch = (ch0 / Cw) * Cw;                // the tile's first chunk
             if (fch < ch0) {
                 int fw = warp;
                 while (fw > 0 && (fw * chunks) / p.warps > fch) --fw;
@@ -688,14 +736,14 @@ __global__ void __launch_bounds__(DUO ? kDuoWarps * 32 : cta_warps(NB, G) * 32, 
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[nb][e] = 0.0f;
         float acc_a = 0.0f, acc_b = 0.0f;                  // M1: this lane's useful sums
-        int tl = ch0 / p.C, cu = ch0 - (ch0 / p.C) * p.C, ch = ch0;   // unit's tile, chunk in it, chunk in run
+        int tl = ch0 / Cw, cu = ch0 - (ch0 / Cw) * Cw, ch = ch0;   // unit's tile, chunk in it, chunk in run
         const int lg = 31 - __clz(nsl);
         for (int k = 0; ch < ch1 && ok; ++k) {
             const uint32_t slot = (uint32_t)(k & (nsl - 1));
             ok = gemv_wait(bar0 + 8u * slot, (uint32_t)((k >> lg) & 1), p.spin_limit);
             ok = __all_sync(0xFFFFFFFFu, ok);
             if (ok) {
-                const bool two = cu + 1 < p.C && ch + 1 < ch1;   // as in issue_next
+                const bool two = cu + 1 < Cw && ch + 1 < ch1;    // as in issue_next
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
                   if (cc == 1 && !two) break;                 // one-chunk unit (uniform)
@@ -705,11 +753,13 @@ __global__ void __launch_bounds__(DUO ? kDuoWarps * 32 : cta_warps(NB, G) * 32, 
                   // 16 halves per virtual row, chunk cc at half 8 cc
                   const unsigned short* msu = reinterpret_cast<const unsigned short*>(
                       base + (mring - sbase) + slot * (uint32_t)kMetaBytes);
-                  const unsigned short* sra = MS ? msu + va * 16 + cc * 8 : smtab + rla * p.lds + pa * p.ngs + c * GPC;
-                  const unsigned short* srb = MS ? msu + vb * 16 + cc * 8 : smtab + rlb * p.lds + pb * p.ngs + c * GPC;
+                  const unsigned short* sra =
+                      MS ? msu + va * 16 + cc * 8 : smtab + rla * p.lds + pa * p.ngs + (kc0 + c) * GPC;
+                  const unsigned short* srb =
+                      MS ? msu + vb * 16 + cc * 8 : smtab + rlb * p.lds + pb * p.ngs + (kc0 + c) * GPC;
                   const uint32_t* zra = zmtab + rla * p.ldz;
                   const uint32_t* zrb = zmtab + rlb * p.ldz;
-                  const int gia = pa * p.ngs + c * GPC, gib = pb * p.ngs + c * GPC;   // first group of the chunk
+                  const int gia = pa * p.ngs + (kc0 + c) * GPC, gib = pb * p.ngs + (kc0 + c) * GPC;   // its first group
                   // M1: scales of the lane's parity; zero words shifted to the lane's first group
                   const unsigned short* sra1 = sra + h_use;
                   const unsigned short* srb1 = srb + h_use;
@@ -880,7 +930,7 @@ __global__ void __launch_bounds__(DUO ? kDuoWarps * 32 : cta_warps(NB, G) * 32, 
                 }
                 // tile finished in this warp's run: reduce the diagonal over segments and parities
                 const int n = two ? 2 : 1;
-                if (cu + n == p.C || ch + n == ch1) {
+                if (cu + n == Cw || ch + n == ch1) {
                     if constexpr (M1) {
                         // red[vrow][parity]: written by the one lane holding each useful sum
                         if (useful) {
@@ -889,7 +939,7 @@ __global__ void __launch_bounds__(DUO ? kDuoWarps * 32 : cta_warps(NB, G) * 32, 
                         }
                         acc_a = acc_b = 0.0f;
                         __syncwarp();
-                        const int slotp = (tl * p.C < ch0) ? first_slot : 0;
+                        const int slotp = (tl * Cw < ch0) ? first_slot : 0;
                         if (lane < R) {
                             float sum = 0.0f;
                             for (int q = 0; q < P; ++q)
@@ -909,7 +959,7 @@ __global__ void __launch_bounds__(DUO ? kDuoWarps * 32 : cta_warps(NB, G) * 32, 
                             for (int e = 0; e < 4; ++e) acc[nb][e] = 0.0f;
                         }
                         __syncwarp();
-                        const int slotp = (tl * p.C < ch0) ? first_slot : 0;
+                        const int slotp = (tl * Cw < ch0) ? first_slot : 0;
                         for (int o = lane; o < R * p.M; o += 32) {   // R*M reaches 256
                             const int rho = o / p.M, m = o - rho * p.M;
                             float sum = 0.0f;
@@ -930,7 +980,7 @@ __global__ void __launch_bounds__(DUO ? kDuoWarps * 32 : cta_warps(NB, G) * 32, 
                 }
                 ch += n;
                 cu += n;
-                if (cu == p.C) {
+                if (cu == Cw) {
                     cu = 0;
                     ++tl;
                 }
@@ -962,10 +1012,16 @@ __global__ void __launch_bounds__(DUO ? kDuoWarps * 32 : cta_warps(NB, G) * 32, 
     __syncthreads();
 
     // ---- combine the slots in a fixed order and store ------------------------------
+    // KS: both CTAs' partial sums are complete once the cluster barrier is passed; each CTA
+    // then stores every other output, adding rank 0's slots and then rank 1's, read through
+    // distributed shared memory, and the second barrier keeps both alive until the peer has
+    // read.
+    if constexpr (KS) cluster_sync();
     {
         const float* part = reinterpret_cast<const float*>(base + L.part);
         const int nout = tc_ * R * p.M;
-        for (int i = tid; i < nout; i += kThreads) {
+        const int i0 = KS ? 2 * tid + (int)crank : tid, di = KS ? 2 * kThreads : kThreads;
+        for (int i = i0; i < nout; i += di) {
             const int rl = i / p.M, m = i - rl * p.M;
             const int tl2 = rl / R, rho = rl - tl2 * R;
             const int tau = tile0 + tl2;
@@ -973,14 +1029,25 @@ __global__ void __launch_bounds__(DUO ? kDuoWarps * 32 : cta_warps(NB, G) * 32, 
             const int row = (tau - p.tstart[mat]) * R + rho;
             if (row >= p.n[mat]) continue;
             float sum = 0.0f;
+            if constexpr (KS) {
+                const uint32_t a = tc::smem_u32(part + i * kSlots);
 #pragma unroll
-            for (int q = 0; q < kSlots; ++q) sum += part[i * kSlots + q];
+                for (uint32_t rk = 0; rk < 2; ++rk) {
+                    const uint32_t ra = cluster_map(a, rk);
+#pragma unroll
+                    for (int q = 0; q < kSlots; ++q) sum += ld_cluster_f32(ra + 4u * (uint32_t)q);
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < kSlots; ++q) sum += part[i * kSlots + q];
+            }
             if (p.yf32)
                 static_cast<float*>(p.y[mat])[(int64_t)m * p.n[mat] + row] = sum;
             else
                 static_cast<__nv_bfloat16*>(p.y[mat])[(int64_t)m * p.n[mat] + row] = __float2bfloat16_rn(sum);
         }
     }
+    if constexpr (KS) cluster_sync();
 }
 
 // ---- host side -------------------------------------------------------------------
@@ -1042,8 +1109,9 @@ struct Plan {
 // record per 256 codes in place of the scale row, no zero row.
 // w8: the 8-bit word layout, planned as the 4-bit layer of K' = 2K channels and
 // groups of G' = 2G it is run as (so K and G here are K' and G'; M <= 8, G' <= 256).
+// ks_clusters: two-CTA clusters the device runs at once (0: the K split is not used).
 bool make_plan(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G, int sms, size_t smem_cap, Plan& pl,
-               bool kq = false, bool w8 = false) {
+               bool kq = false, bool w8 = false, int ks_clusters = 0) {
     if (M < 1 || M > 16 || nmat < 1 || nmat > kMaxMat || K < 32 || K % 32 || K % G) return false;
     if (kq && (G != 32 || K % 256 || M > 8)) return false;
     if (w8 && (kq || M > 8 || G < 64 || G > 256 || K % 64)) return false;
@@ -1061,6 +1129,9 @@ bool make_plan(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G, int sms
     pl.nb = M > 8 ? 2 : 1;
     p.C = (int)((K / p.P + 255) / 256);
     p.Ks = p.C * 256;                           // equals K / P whenever P > 1
+    p.ks = 0;
+    p.Ct = p.C;
+    p.kc1 = p.C;
     p.ng = (int)(K / G);
     p.ngs = p.Ks / G;
     p.lds = kq ? (int)(K / 256 * 8) : (int)scales_ld(K, G);
@@ -1086,11 +1157,12 @@ bool make_plan(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G, int sms
     // CTA warps (the instance's launch bound, or fewer when shared memory is short), then the
     // deepest per-warp ring of units that fits
     // warps taking units: as many as keep every tile within kSlots consecutive warps
-    auto set_warps = [&](int nw) {
+    // (tiles per CTA at least tn, each of cn chunks: the K split's rank 1 streams the fewer)
+    auto set_warps = [&](int nw, int tn, int cn) {
         p.nw = nw;
         p.warps = 1;
         for (int w = nw; w >= 1; --w) {
-            const long long chunks = (long long)tmin * p.C;
+            const long long chunks = (long long)tn * cn;
             const long long per = chunks / w;
             if (per < 1) continue;
             const long long span = (p.C + per - 1) / per + 1;
@@ -1111,7 +1183,7 @@ bool make_plan(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G, int sms
     p.duo = 0;
     if (M == 1 && G == 128 && !kq && !w8 && p.P == 4 && pl.H == 2 && nmat != 2 &&
         wbytes / pl.grid <= kDuoMaxBytes) {
-        set_warps(kDuoWarps);
+        set_warps(kDuoWarps, tmin, p.C);
         for (int nst = 4; nst >= 1; nst >>= 1) {
             p.nst = nst;
             p.pf = 0;
@@ -1122,51 +1194,82 @@ bool make_plan(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G, int sms
             }
         }
     }
-    for (int nw = cta_warps(pl.nb, G); nw >= 4; nw -= 4) {
-        set_warps(nw);
-        for (int nst = 4; nst >= 1; nst >>= 1) {
-            p.nst = nst;
-            p.pf = nst == 1 && G == 32 ? 4 : 0;   // measured: 4 chunks ahead helps a one-unit ring at G = 32
-            pl.smem = make_layout(p, pl.nb, pl.H).total + 1024;
-            if (pl.smem <= smem_cap) return true;
+    // the CTA's warps (the instance's launch bound, or fewer when shared memory is short), then
+    // the deepest ring that fits
+    auto fit = [&](int tn, int cn) {
+        for (int nw = cta_warps(pl.nb, G); nw >= 4; nw -= 4) {
+            set_warps(nw, tn, cn);
+            for (int nst = 4; nst >= 1; nst >>= 1) {
+                p.nst = nst;
+                p.pf = nst == 1 && G == 32 ? 4 : 0;   // measured: 4 chunks ahead helps a one-unit ring at G = 32
+                pl.smem = make_layout(p, pl.nb, pl.H).total + 1024;
+                if (pl.smem <= smem_cap) return true;
+            }
         }
+        return false;
+    };
+    const bool plain_ok = fit(tmin, p.C);
+    // The K split (two column blocks, one matrix, 4-bit codes with resident metadata): taken
+    // when x leaves the plain kernel fewer warps than its launch bound, or no room at all.
+    const bool ks_able = pl.nb == 2 && nmat == 1 && !kq && !w8 && !p.mstream && p.P == 1 && p.C >= 2 && ks_clusters >= 1;
+    if (!ks_able || (plain_ok && p.nw >= cta_warps(pl.nb, G))) return plain_ok;
+    const Plan plain = pl;
+    p.ks = 1;
+    p.Ct = p.C;
+    p.kc1 = (p.C + 1) / 2;
+    p.C = p.kc1;                                // sizes the staged x and its group sums
+    p.Ks = p.C * 256;
+    p.ngs = p.Ks / G;
+    const int ncl = p.total_tiles < ks_clusters ? p.total_tiles : ks_clusters;
+    pl.grid = 2 * ncl;
+    const int ktmin = p.total_tiles / ncl, ktmax = (p.total_tiles + ncl - 1) / ncl;
+    if ((long long)ktmax * p.Ct >= (1ll << 26) || (long long)p.total_tiles * ncl >= (1ll << 32)) {
+        pl = plain;
+        return plain_ok;
     }
-    return false;
+    p.rows_cap = ktmax * p.R;
+    if (fit(ktmin, p.Ct - p.kc1) && (!plain_ok || p.nw > plain.p.nw)) return true;
+    pl = plain;
+    return plain_ok;
 }
 
-template <int NB, int G, int H, bool M1, int PT, int FMT, int NM, bool DUO = false>
+template <int NB, int G, int H, bool M1, int PT, int FMT, int NM, bool DUO = false, bool KS = false>
 cudaError_t launch_m(const CUtensorMap* tm, const Plan& pl, int dev, cudaStream_t stream) {
     // largest dynamic shared memory this instance is already allowed per device (a raise may
     // race with another thread's: both set the attribute, the larger value stays)
     static std::atomic<int> cached[kMaxDevices];
     int have = cached[dev].load(std::memory_order_relaxed);
     if ((int)pl.smem > have) {
-        cudaError_t e = cudaFuncSetAttribute(gemv_kernel<NB, G, H, M1, PT, FMT, NM, DUO>,
+        cudaError_t e = cudaFuncSetAttribute(gemv_kernel<NB, G, H, M1, PT, FMT, NM, DUO, KS>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
         if (e == cudaSuccess && DUO)   // the shared-memory carveout that lets two CTAs share an SM
-            e = cudaFuncSetAttribute(gemv_kernel<NB, G, H, M1, PT, FMT, NM, DUO>,
+            e = cudaFuncSetAttribute(gemv_kernel<NB, G, H, M1, PT, FMT, NM, DUO, KS>,
                                      cudaFuncAttributePreferredSharedMemoryCarveout, 100);
         if (e != cudaSuccess) return e;
         while (have < (int)pl.smem && !cached[dev].compare_exchange_weak(have, (int)pl.smem)) {
         }
     }
     // programmatic stream serialisation: set-up overlaps the tail of the previous launch
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;     // KS: clusters of two CTAs
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)pl.grid);
     cfg.blockDim = dim3((unsigned)(pl.p.nw * 32));
     cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = KS ? 2 : 1;
     // tm[0, kMaxMat): code maps; tm[kMaxMat, 2 kMaxMat): streamed-metadata maps (MS instances)
     CodeMaps<NM, meta_streamed(G)> maps;
     for (int i = 0; i < NM; ++i) maps.m[i] = tm[i];
     if constexpr (meta_streamed(G))
         for (int i = 0; i < NM; ++i) maps.s[i] = tm[kMaxMat + i];
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<NB, G, H, M1, PT, FMT, NM, DUO>, maps, pl.p);
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<NB, G, H, M1, PT, FMT, NM, DUO, KS>, maps, pl.p);
 }
 
 template <int NB, int G, int H, int FMT, int NM>
@@ -1213,6 +1316,47 @@ cudaError_t launch_nb(const CUtensorMap* tm, const Plan& pl, int dev, cudaStream
     }
 }
 
+// The K split (two column blocks, one matrix, 4-bit codes, G >= 64).
+cudaError_t launch_ks(const CUtensorMap* tm, const Plan& pl, int dev, cudaStream_t stream) {
+    switch (pl.p.G) {
+        case 64: return launch_m<2, 64, 1, false, 0, kFmt4, 1, false, true>(tm, pl, dev, stream);
+        case 128: return launch_m<2, 128, 1, false, 0, kFmt4, 1, false, true>(tm, pl, dev, stream);
+        case 256: return launch_m<2, 256, 1, false, 0, kFmt4, 1, false, true>(tm, pl, dev, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+// Two-CTA clusters of the K-split kernel that the device runs at once, one CTA per SM (the
+// SMs pair up within their GPCs, so this can be below SMs / 2); asked once per device, 0
+// when the device cannot say.
+int ks_clusters(const DeviceInfo& di, int64_t M, int nmat, bool kq, bool w8, int G) {
+    if (M <= 8 || nmat != 1 || kq || w8 || G < 64) return 0;      // plans that never split
+    static std::atomic<int> cached[kMaxDevices];
+    const int v = cached[di.dev].load(std::memory_order_relaxed);
+    if (v != 0) return v > 0 ? v : 0;
+    auto kern = gemv_kernel<2, 128, 1, false, 0, kFmt4, 1, false, true>;
+    const int smem = 200 * 1024;
+    int n = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess) {
+        cudaLaunchAttribute a[1];
+        a[0].id = cudaLaunchAttributeClusterDimension;
+        a[0].val.clusterDim.x = 2;
+        a[0].val.clusterDim.y = 1;
+        a[0].val.clusterDim.z = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2u);
+        cfg.blockDim = dim3((unsigned)(cta_warps(2, 128) * 32));
+        cfg.dynamicSmemBytes = smem;
+        cfg.attrs = a;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+    }
+    (void)cudaGetLastError();
+    if (n > di.sms / 2) n = di.sms / 2;
+    cached[di.dev].store(n > 0 ? n : -1, std::memory_order_relaxed);
+    return n > 0 ? n : 0;
+}
+
 // The 8-bit word layout (one column block; G' = 2G in {64, 128, 256}).
 cudaError_t launch_w8(const CUtensorMap* tm, const Plan& pl, int dev, cudaStream_t stream) {
     switch (pl.p.G) {
@@ -1235,12 +1379,30 @@ cudaError_t gemv_take_status(uint32_t* word) {
 bool gemv_fits(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G, bool kq, bool w8) {
     Plan pl;
     DeviceInfo di;
+    int kcl;
     if (current_device(di) != cudaSuccess) {   // no device: the B300's figures
         di.sms = 148;
         di.smem_optin = 227 * 1024;
+        kcl = 74;
+    } else {
+        kcl = ks_clusters(di, M, nmat, kq, w8, G);
     }
     return w8 ? make_plan(M, Ns, nmat, 2 * K, 2 * G, di.sms, di.smem_optin, pl, false, true)
-              : make_plan(M, Ns, nmat, K, G, di.sms, di.smem_optin, pl, kq);
+              : make_plan(M, Ns, nmat, K, G, di.sms, di.smem_optin, pl, kq, false, kcl);
+}
+
+bool gemv_runs_full(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G) {
+    Plan pl;
+    DeviceInfo di;
+    int kcl = 74;
+    if (current_device(di) != cudaSuccess) {   // no device: the B300's figures
+        di.sms = 148;
+        di.smem_optin = 227 * 1024;
+    } else {
+        kcl = ks_clusters(di, M, nmat, false, false, G);
+    }
+    return make_plan(M, Ns, nmat, K, G, di.sms, di.smem_optin, pl, false, false, kcl) &&
+           pl.p.nw == cta_warps(pl.nb, G);
 }
 
 bool gemv_fits(int64_t M, int64_t N, int64_t K, int G, int nmat, bool kq) {
@@ -1266,7 +1428,8 @@ cudaError_t launch_gemv(const void* x, const GemvMat* mats, int nmat, int64_t M,
     const int64_t Kv = w8 ? 2 * K : K;
     const int Gv = w8 ? 2 * G : G;
     Plan pl;
-    if (!make_plan(M, Ns, nmat, Kv, Gv, di.sms, di.smem_optin, pl, kq, w8)) return cudaErrorNotSupported;
+    if (!make_plan(M, Ns, nmat, Kv, Gv, di.sms, di.smem_optin, pl, kq, w8, ks_clusters(di, M, nmat, kq, w8, G)))
+        return cudaErrorNotSupported;
     GemvParams& p = pl.p;
     p.x = static_cast<const __nv_bfloat16*>(x);
     p.xsc = xsc;
@@ -1301,6 +1464,7 @@ cudaError_t launch_gemv(const void* x, const GemvMat* mats, int nmat, int64_t M,
         return nmat == 1 ? launch_h<1, 32, kFmtQ4K, 1>(tm, pl, di.dev, stream)
                          : launch_h<1, 32, kFmtQ4K, 2>(tm, pl, di.dev, stream);
     if (w8) return launch_w8(tm, pl, di.dev, stream);
+    if (p.ks) return launch_ks(tm, pl, di.dev, stream);      // make_plan: one matrix, M > 8, G >= 64
     if (nmat > 2)
         return pl.nb == 1 ? launch_nb<1, 4>(tm, pl, di.dev, stream) : launch_nb<2, 4>(tm, pl, di.dev, stream);
     if (nmat == 2)

@@ -77,6 +77,9 @@ bool gemv_fits(int64_t M, int64_t N, int64_t K, int G, int nmat, bool kq = false
 // The same for nmat matrices of Ns[i] rows each.
 // w8: the 8-bit word layout (K, G its real channels and group size; G <= 128, M <= 8).
 bool gemv_fits(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G, bool kq = false, bool w8 = false);
+// Whether the 4-bit decode GEMV takes these matrices with all the warps of its instance (its
+// launch bound; fewer when x leaves too little shared memory for the weight rings).  Host only.
+bool gemv_runs_full(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G);
 
 // y_i = x * W_hat_i^T for nmat (1..kMaxMat) matrices sharing x; matrix i has mats[i].n rows
 // (0: N).
