@@ -152,11 +152,11 @@ W4A16_API w4a16_status w4a16_dequant_f16(const uint32_t* qweight, const void* sc
 /* ---- the layer ---------------------------------------------------------------
  * w4a16_linear: y[M,N] (BF16) = x[M,K] (BF16) * W_hat^T, FP32 accumulation,
  * one round-to-nearest-even to BF16 per output.  Dispatch: M <= 8 runs the
- * bandwidth-bound decode GEMV (when x of M rows fits the kernel's shared
- * memory), and so does M = 9..16 where the GEMV runs with all its warps and
- * also takes M = 8 (long rows then split K over a two-CTA cluster; measured
- * on a 5120 -> 13824 layer at M = 16: 27.4 us against 33.7 us for the GEMM);
- * anything else runs the tcgen05 tensor-core GEMM.  Decode is
+ * bandwidth-bound decode GEMV (when x of M rows, or half of it on each SM of
+ * a two-CTA cluster splitting K, fits the kernel's shared memory), and so
+ * does M = 9..16 where the GEMV runs with all its warps and also takes M = 8
+ * (measured on a 5120 -> 13824 layer at M = 16: 27.4 us against 33.7 us for
+ * the GEMM); anything else runs the tcgen05 tensor-core GEMM.  Decode is
  * weight-bandwidth bound and prefill compute bound (klaylearn glossary, FAQ
  * "Why is it especially useful for decode?"; multigrid.ai, section "Where it
  * stops being the right answer").
@@ -458,6 +458,18 @@ W4A16_API w4a16_status w4a16_device_status(uint32_t* detail);
  */
 W4A16_API void w4a16_debug_set_wait_limit(int64_t cycles);
 W4A16_API w4a16_status w4a16_debug_withhold_copy(int kernel);
+
+/*
+ * w4a16_debug_gemv_plan: how the decode kernel would run one 4-bit matrix
+ * [N, K] at M activation rows on the current device (host only, launches
+ * nothing): plan[0] = segments per row P, plan[1] = group parities H,
+ * plan[2] = warps per CTA, plan[3] = 1 when K is split across two-CTA
+ * clusters, plan[4] = CTAs.  plan is a HOST array of 5 int32.  Returns
+ * W4A16_OK, W4A16_ERR_UNSUPPORTED when the decode kernel cannot take the
+ * shape, W4A16_ERR_INVALID_ARG for a null plan or a bad shape.  For tests of
+ * the planner; the layer calls plan by themselves.
+ */
+W4A16_API w4a16_status w4a16_debug_gemv_plan(int64_t M, int64_t N, int64_t K, int G, int32_t* plan);
 
 #ifdef __cplusplus
 }

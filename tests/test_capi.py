@@ -258,6 +258,29 @@ def test_dispatch_rule(N, K, G):
     assert w4.w4a16_linear_path(2048, N, K, G) == 2
 
 
+def test_gemv_plan_query():
+    """The planner's choices on a B300 (148 SMs, 227 KB of shared memory; on a GPU the device's own
+    figures): the 70B decode geometry, the K split where x would crowd out the rings, and errors."""
+    plan = (ctypes.c_int32 * 5)()
+
+    def q(M, N, K, G):
+        st = w4._lib.w4a16_debug_gemv_plan(M, N, K, G, plan)
+        return st, list(plan)
+
+    st, p = q(1, 28672, 8192, 128)
+    assert st == 0 and p[:4] == [4, 2, 16, 0] and p[4] == 148
+    st, p = q(16, 13824, 5120, 128)                     # x = 160 KB: split over clusters of two
+    assert st == 0 and p[0] == 1 and p[3] == 1 and p[4] % 2 == 0 and p[2] == 12
+    st, p = q(12, 13824, 5120, 128)                     # x = 120 KB: the plain kernel keeps all its warps
+    assert st == 0 and p[3] == 0 and p[2] == 12
+    st, p = q(8, 264, 13824, 128)                       # x = 221 KB: only the split fits
+    assert st == 0 and p[:2] == [1, 1] and p[3] == 1
+    assert q(16, 28672, 8192, 128)[0] == 2              # unsupported: even half of x leaves no room
+    assert q(17, 264, 1024, 128)[0] == 1                # M outside 1..16
+    assert q(1, 60, 1024, 128)[0] == 1                  # N not a multiple of 8
+    assert w4._lib.w4a16_debug_gemv_plan(1, 264, 1024, 128, None) == 1
+
+
 def test_dispatch_falls_back_when_the_gemv_does_not_fit():
     # x is staged as M*K FP16 beside the resident metadata rows: at K = 65536 one row still fits at
     # G = 32 (whose scales stream with the weights; only the zero rows stay resident) and G = 128,

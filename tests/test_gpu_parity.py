@@ -100,16 +100,26 @@ def test_gemv_long_rows_with_streamed_scales(M, N, K):
     assert_close(y, y_ref, f"gemv long rows M={M} N={N} K={K} G={G}")
 
 
-# M = 9..16 with long rows: x (M * K FP16) would leave the kernel a short weight ring or no room,
-# so two CTAs of a cluster each stage and stream half of every row's chunks and add their partial
-# sums through distributed shared memory.  Odd chunk counts (rank 1 streams one fewer), a last
-# chunk cut short (K % 256 != 0), several CTA pairs, ragged N.
-KSPLIT_SHAPES = [(16, 520, 8192, 128), (9, 136, 12288, 64), (12, 1032, 5120, 256), (11, 392, 6336, 64),
-                 (16, 264, 6400, 128)]
+# Long rows: x (M * K FP16) would leave the kernel a short weight ring or no room, so two CTAs of
+# a cluster each stage and stream half of every row's chunks and add their partial sums through
+# distributed shared memory.  Two column blocks (M = 9..16) and one with 1, 2 or 4 group parities
+# (M <= 8); odd chunk counts (rank 1 streams one fewer), a last chunk cut short (K % 256 != 0),
+# several CTA pairs, ragged N.
+KSPLIT_SHAPES = [(16, 520, 8192, 128), (9, 136, 12288, 64), (12, 1032, 8192, 256), (11, 392, 10560, 64),
+                 (16, 264, 6400, 128), (8, 264, 13824, 128), (3, 136, 28672, 128), (2, 72, 49152, 64),
+                 (4, 392, 20480, 128), (6, 264, 13824, 256), (5, 520, 16384, 64), (7, 136, 16384, 64)]
+
+
+def _gemv_plan(M, N, K, G):
+    import ctypes
+    plan = (ctypes.c_int32 * 5)()
+    assert w4._lib.w4a16_debug_gemv_plan(M, N, K, G, plan) == 0
+    return list(plan)
 
 
 @pytest.mark.parametrize("M,N,K,G", KSPLIT_SHAPES)
 def test_gemv_k_split_across_a_cluster(M, N, K, G):
+    assert _gemv_plan(M, N, K, G)[3] == 1                          # the planner takes the split
     w, x, (q, s, z), y_ref = _case(M, N, K, G, seed=M * 13 + N + K + G, outliers=0.002)
     dq = dev_packed(q, s, z)
     xd = x.cuda()

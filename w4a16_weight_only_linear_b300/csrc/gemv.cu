@@ -68,8 +68,8 @@
 // Small layers run an 8-warp instance that leaves room for a second CTA per
 // SM; its CTAs ask L2 for their rows before the grid-dependency wait.
 //
-// K split.  At M > 8 on long rows the staged x (M * K FP16) would leave the
-// weight rings too little shared memory; a cluster of two CTAs on two SMs
+// K split.  On long rows the staged x (M * K FP16) would leave the weight
+// rings too little shared memory (M >= 2); a cluster of two CTAs on two SMs
 // then takes each tile range, each CTA streaming and staging half of every
 // row's chunks, and the two add their partial sums through distributed shared
 // memory (see gemv_kernel's KS).
@@ -305,8 +305,8 @@ __device__ __forceinline__ bool gemv_wait(uint32_t bar, uint32_t parity, long lo
 // (parity, segment) pairs and each lane holds at most one useful D value per
 // row, so the block-end correction is done once per row on that value only.
 // NM: matrices the instance takes (1, 2, or 4 for three or four).
-// KS: the K split.  Where M * K of x would crowd out the weight ring (two
-// column blocks, long rows), each tile range is taken by a cluster of two
+// KS: the K split.  Where M * K of x would crowd out the weight ring (long
+// rows, M >= 2), each tile range is taken by a cluster of two
 // CTAs on two SMs: rank r streams and stages only its half of the chunks of
 // every row, and at the end the two CTAs add both ranks' partial sums, read
 // through distributed shared memory, in a fixed order.
@@ -1109,9 +1109,11 @@ struct Plan {
 // record per 256 codes in place of the scale row, no zero row.
 // w8: the 8-bit word layout, planned as the 4-bit layer of K' = 2K channels and
 // groups of G' = 2G it is run as (so K and G here are K' and G'; M <= 8, G' <= 256).
-// ks_clusters: two-CTA clusters the device runs at once (0: the K split is not used).
-bool make_plan(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G, int sms, size_t smem_cap, Plan& pl,
-               bool kq = false, bool w8 = false, int ks_clusters = 0) {
+// One plan: the plain kernel (ks_ncl = 0) or the K split over ks_ncl two-CTA clusters, whose
+// geometry is one segment per row (P = 1) with as many group parities as one column block of
+// M <= 8 rows holds.
+bool plan_one(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G, int sms, size_t smem_cap, Plan& pl,
+              bool kq, bool w8, int ks_ncl) {
     if (M < 1 || M > 16 || nmat < 1 || nmat > kMaxMat || K < 32 || K % 32 || K % G) return false;
     if (kq && (G != 32 || K % 256 || M > 8)) return false;
     if (w8 && (kq || M > 8 || G < 64 || G > 256 || K % 64)) return false;
@@ -1122,16 +1124,28 @@ bool make_plan(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G, int sms
     p.M = (int)M;
     p.K = (int)K;
     p.G = G;
-    choose_segments(M, K, G, kq, p.P, pl.H);
+    if (ks_ncl > 0) {
+        p.P = 1;
+        pl.H = 1;
+        for (int h = 4; h >= 2; h >>= 1)
+            if (M <= 8 && h * M <= 8 && (256 / G) % h == 0) {
+                pl.H = h;
+                break;
+            }
+    } else {
+        choose_segments(M, K, G, kq, p.P, pl.H);
+    }
     p.R = 16 / p.P;
     p.cols = p.P * pl.H * p.M;
     p.xcols = p.P * p.M;
     pl.nb = M > 8 ? 2 : 1;
     p.C = (int)((K / p.P + 255) / 256);
-    p.Ks = p.C * 256;                           // equals K / P whenever P > 1
-    p.ks = 0;
+    p.ks = ks_ncl > 0 ? 1 : 0;
     p.Ct = p.C;
-    p.kc1 = p.C;
+    p.kc1 = p.ks ? (p.C + 1) / 2 : p.C;         // K split: rank 0 streams chunks [0, kc1), rank 1 the rest
+    if (p.ks && (p.C < 2 || nmat != 1 || kq || w8 || meta_streamed(G))) return false;
+    p.C = p.kc1;                                // chunks this CTA stages x for (the K split: rank 0's)
+    p.Ks = p.C * 256;                           // equals K / P whenever P > 1 (and no K split)
     p.ng = (int)(K / G);
     p.ngs = p.Ks / G;
     p.lds = kq ? (int)(K / 256 * 8) : (int)scales_ld(K, G);
@@ -1149,8 +1163,11 @@ bool make_plan(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G, int sms
     p.tstart[kMaxMat] = (int)t;
     for (int i = nmat; i < kMaxMat; ++i) p.tstart[i] = (int)t;
     p.total_tiles = (int)t;
-    pl.grid = p.total_tiles < sms ? p.total_tiles : sms;
-    const int tmin = p.total_tiles / pl.grid, tmax = (p.total_tiles + pl.grid - 1) / pl.grid;
+    // CTAs (the K split: clusters of two) and the tiles each takes
+    const int units = p.ks ? (p.total_tiles < ks_ncl ? p.total_tiles : ks_ncl)
+                           : (p.total_tiles < sms ? p.total_tiles : sms);
+    pl.grid = p.ks ? 2 * units : units;
+    const int tmin = p.total_tiles / units, tmax = (p.total_tiles + units - 1) / units;
     if ((long long)tmax * p.C >= (1ll << 26)) return false;
     if ((long long)p.total_tiles * pl.grid >= (1ll << 32)) return false;
     p.rows_cap = tmax * p.R;
@@ -1208,28 +1225,22 @@ bool make_plan(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G, int sms
         }
         return false;
     };
-    const bool plain_ok = fit(tmin, p.C);
-    // The K split (two column blocks, one matrix, 4-bit codes with resident metadata): taken
-    // when x leaves the plain kernel fewer warps than its launch bound, or no room at all.
-    const bool ks_able = pl.nb == 2 && nmat == 1 && !kq && !w8 && !p.mstream && p.P == 1 && p.C >= 2 && ks_clusters >= 1;
-    if (!ks_able || (plain_ok && p.nw >= cta_warps(pl.nb, G))) return plain_ok;
-    const Plan plain = pl;
-    p.ks = 1;
-    p.Ct = p.C;
-    p.kc1 = (p.C + 1) / 2;
-    p.C = p.kc1;                                // sizes the staged x and its group sums
-    p.Ks = p.C * 256;
-    p.ngs = p.Ks / G;
-    const int ncl = p.total_tiles < ks_clusters ? p.total_tiles : ks_clusters;
-    pl.grid = 2 * ncl;
-    const int ktmin = p.total_tiles / ncl, ktmax = (p.total_tiles + ncl - 1) / ncl;
-    if ((long long)ktmax * p.Ct >= (1ll << 26) || (long long)p.total_tiles * ncl >= (1ll << 32)) {
-        pl = plain;
-        return plain_ok;
+    return fit(tmin, p.ks ? p.Ct - p.kc1 : p.C);
+}
+
+// The plan of a launch.  The K split (one matrix of 4-bit codes with resident metadata, M >= 2;
+// ks_clusters: two-CTA clusters the device runs at once, 0 = never) is taken when x leaves the
+// plain kernel fewer warps than its launch bound, or no room at all, and the split has more.
+bool make_plan(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G, int sms, size_t smem_cap, Plan& pl,
+               bool kq = false, bool w8 = false, int ks_clusters = 0) {
+    const bool plain_ok = plan_one(M, Ns, nmat, K, G, sms, smem_cap, pl, kq, w8, 0);
+    const bool ks_able = ks_clusters >= 1 && M >= 2 && nmat == 1 && !kq && !w8 && !meta_streamed(G);
+    if (!ks_able || (plain_ok && pl.p.nw >= cta_warps(pl.nb, G))) return plain_ok;
+    Plan kp;
+    if (plan_one(M, Ns, nmat, K, G, sms, smem_cap, kp, kq, w8, ks_clusters) && (!plain_ok || kp.p.nw > pl.p.nw)) {
+        pl = kp;
+        return true;
     }
-    p.rows_cap = ktmax * p.R;
-    if (fit(ktmin, p.Ct - p.kc1) && (!plain_ok || p.nw > plain.p.nw)) return true;
-    pl = plain;
     return plain_ok;
 }
 
@@ -1316,12 +1327,23 @@ cudaError_t launch_nb(const CUtensorMap* tm, const Plan& pl, int dev, cudaStream
     }
 }
 
-// The K split (two column blocks, one matrix, 4-bit codes, G >= 64).
+// The K split (one matrix, 4-bit codes, G >= 64; one segment per row, H group parities).
 cudaError_t launch_ks(const CUtensorMap* tm, const Plan& pl, int dev, cudaStream_t stream) {
-    switch (pl.p.G) {
-        case 64: return launch_m<2, 64, 1, false, 0, kFmt4, 1, false, true>(tm, pl, dev, stream);
-        case 128: return launch_m<2, 128, 1, false, 0, kFmt4, 1, false, true>(tm, pl, dev, stream);
-        case 256: return launch_m<2, 256, 1, false, 0, kFmt4, 1, false, true>(tm, pl, dev, stream);
+    if (pl.nb == 2) {
+        switch (pl.p.G) {
+            case 64: return launch_m<2, 64, 1, false, 0, kFmt4, 1, false, true>(tm, pl, dev, stream);
+            case 128: return launch_m<2, 128, 1, false, 0, kFmt4, 1, false, true>(tm, pl, dev, stream);
+            case 256: return launch_m<2, 256, 1, false, 0, kFmt4, 1, false, true>(tm, pl, dev, stream);
+            default: return cudaErrorInvalidValue;
+        }
+    }
+    switch (pl.p.G * 8 + pl.H) {
+        case 64 * 8 + 1: return launch_m<1, 64, 1, false, 0, kFmt4, 1, false, true>(tm, pl, dev, stream);
+        case 64 * 8 + 2: return launch_m<1, 64, 2, false, 0, kFmt4, 1, false, true>(tm, pl, dev, stream);
+        case 64 * 8 + 4: return launch_m<1, 64, 4, false, 0, kFmt4, 1, false, true>(tm, pl, dev, stream);
+        case 128 * 8 + 1: return launch_m<1, 128, 1, false, 0, kFmt4, 1, false, true>(tm, pl, dev, stream);
+        case 128 * 8 + 2: return launch_m<1, 128, 2, false, 0, kFmt4, 1, false, true>(tm, pl, dev, stream);
+        case 256 * 8 + 1: return launch_m<1, 256, 1, false, 0, kFmt4, 1, false, true>(tm, pl, dev, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -1330,7 +1352,7 @@ cudaError_t launch_ks(const CUtensorMap* tm, const Plan& pl, int dev, cudaStream
 // SMs pair up within their GPCs, so this can be below SMs / 2); asked once per device, 0
 // when the device cannot say.
 int ks_clusters(const DeviceInfo& di, int64_t M, int nmat, bool kq, bool w8, int G) {
-    if (M <= 8 || nmat != 1 || kq || w8 || G < 64) return 0;      // plans that never split
+    if (M < 2 || nmat != 1 || kq || w8 || G < 64) return 0;       // plans that never split
     static std::atomic<int> cached[kMaxDevices];
     const int v = cached[di.dev].load(std::memory_order_relaxed);
     if (v != 0) return v > 0 ? v : 0;
@@ -1405,6 +1427,26 @@ bool gemv_runs_full(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G) {
            pl.p.nw == cta_warps(pl.nb, G);
 }
 
+bool gemv_describe(int64_t M, int64_t N, int64_t K, int G, int32_t* plan) {
+    Plan pl;
+    DeviceInfo di;
+    int kcl = 74;
+    if (current_device(di) != cudaSuccess) {   // no device: the B300's figures
+        di.sms = 148;
+        di.smem_optin = 227 * 1024;
+    } else {
+        kcl = ks_clusters(di, M, 1, false, false, G);
+    }
+    const int64_t Ns[1] = {N};
+    if (!make_plan(M, Ns, 1, K, G, di.sms, di.smem_optin, pl, false, false, kcl)) return false;
+    plan[0] = pl.p.P;
+    plan[1] = pl.H;
+    plan[2] = pl.p.nw;
+    plan[3] = pl.p.ks;
+    plan[4] = pl.grid;
+    return true;
+}
+
 bool gemv_fits(int64_t M, int64_t N, int64_t K, int G, int nmat, bool kq) {
     int64_t Ns[kMaxMat];
     for (int i = 0; i < kMaxMat; ++i) Ns[i] = N;
@@ -1464,7 +1506,7 @@ cudaError_t launch_gemv(const void* x, const GemvMat* mats, int nmat, int64_t M,
         return nmat == 1 ? launch_h<1, 32, kFmtQ4K, 1>(tm, pl, di.dev, stream)
                          : launch_h<1, 32, kFmtQ4K, 2>(tm, pl, di.dev, stream);
     if (w8) return launch_w8(tm, pl, di.dev, stream);
-    if (p.ks) return launch_ks(tm, pl, di.dev, stream);      // make_plan: one matrix, M > 8, G >= 64
+    if (p.ks) return launch_ks(tm, pl, di.dev, stream);      // make_plan: one matrix, M >= 2, G >= 64
     if (nmat > 2)
         return pl.nb == 1 ? launch_nb<1, 4>(tm, pl, di.dev, stream) : launch_nb<2, 4>(tm, pl, di.dev, stream);
     if (nmat == 2)
