@@ -464,12 +464,14 @@ W4A16_API w4a16_status w4a16_debug_withhold_copy(int kernel);
  * [N, K] at M activation rows on the current device (host only, launches
  * nothing): plan[0] = segments per row P, plan[1] = group parities H,
  * plan[2] = warps per CTA, plan[3] = 1 when K is split across two-CTA
- * clusters, plan[4] = CTAs.  plan is a HOST array of 5 int32.  Returns
- * W4A16_OK, W4A16_ERR_UNSUPPORTED when the decode kernel cannot take the
- * shape, W4A16_ERR_INVALID_ARG for a null plan or a bad shape.  For tests of
- * the planner; the layer calls plan by themselves.
+ * clusters, plan[4] = CTAs, plan[5] = ring units per warp.  mode 0: the plan
+ * the layer takes; 1: the plain kernel's; 2: the K split's.  plan is a HOST
+ * array of 6 int32.  Returns W4A16_OK, W4A16_ERR_UNSUPPORTED when that plan
+ * cannot take the shape, W4A16_ERR_INVALID_ARG for a null plan, a mode
+ * outside 0..2 or a bad shape.  For tests of the planner; the layer calls
+ * plan by themselves.
  */
-W4A16_API w4a16_status w4a16_debug_gemv_plan(int64_t M, int64_t N, int64_t K, int G, int32_t* plan);
+W4A16_API w4a16_status w4a16_debug_gemv_plan(int64_t M, int64_t N, int64_t K, int G, int mode, int32_t* plan);
 
 #ifdef __cplusplus
 }

@@ -261,10 +261,10 @@ def test_dispatch_rule(N, K, G):
 def test_gemv_plan_query():
     """The planner's choices on a B300 (148 SMs, 227 KB of shared memory; on a GPU the device's own
     figures): the 70B decode geometry, the K split where x would crowd out the rings, and errors."""
-    plan = (ctypes.c_int32 * 5)()
+    plan = (ctypes.c_int32 * 6)()
 
-    def q(M, N, K, G):
-        st = w4._lib.w4a16_debug_gemv_plan(M, N, K, G, plan)
+    def q(M, N, K, G, mode=0):
+        st = w4._lib.w4a16_debug_gemv_plan(M, N, K, G, mode, plan)
         return st, list(plan)
 
     st, p = q(1, 28672, 8192, 128)
@@ -278,7 +278,10 @@ def test_gemv_plan_query():
     assert q(16, 28672, 8192, 128)[0] == 2              # unsupported: even half of x leaves no room
     assert q(17, 264, 1024, 128)[0] == 1                # M outside 1..16
     assert q(1, 60, 1024, 128)[0] == 1                  # N not a multiple of 8
-    assert w4._lib.w4a16_debug_gemv_plan(1, 264, 1024, 128, None) == 1
+    assert q(16, 13824, 5120, 128, 1)[1][2] == 4       # the plain kernel there: 4 warps
+    assert q(8, 264, 13824, 128, 1)[0] == 2             # ... and no plain plan at all
+    assert q(1, 264, 1024, 128, 3)[0] == 1              # mode outside 0..2
+    assert w4._lib.w4a16_debug_gemv_plan(1, 264, 1024, 128, 0, None) == 1
 
 
 def test_dispatch_falls_back_when_the_gemv_does_not_fit():

@@ -112,8 +112,8 @@ KSPLIT_SHAPES = [(16, 520, 8192, 128), (9, 136, 12288, 64), (12, 1032, 8192, 256
 
 def _gemv_plan(M, N, K, G):
     import ctypes
-    plan = (ctypes.c_int32 * 5)()
-    assert w4._lib.w4a16_debug_gemv_plan(M, N, K, G, plan) == 0
+    plan = (ctypes.c_int32 * 6)()
+    assert w4._lib.w4a16_debug_gemv_plan(M, N, K, G, 0, plan) == 0
     return list(plan)
 
 

@@ -68,7 +68,7 @@ EXPORTS = {
     "w4a16_device_status": ([_vp], _i32),
     "w4a16_debug_set_wait_limit": ([_i64], None),
     "w4a16_debug_withhold_copy": ([_i32], _i32),
-    "w4a16_debug_gemv_plan": ([_i64, _i64, _i64, _i32, _vp], _i32),
+    "w4a16_debug_gemv_plan": ([_i64, _i64, _i64, _i32, _i32, _vp], _i32),
 }
 
 

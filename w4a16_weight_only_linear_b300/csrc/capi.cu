@@ -508,9 +508,10 @@ int w4a16_linear_path(int64_t M, int64_t N, int64_t K, int G) {
 
 void w4a16_debug_set_wait_limit(int64_t cycles) { w4a16::set_wait_limit(cycles); }
 
-w4a16_status w4a16_debug_gemv_plan(int64_t M, int64_t N, int64_t K, int G, int32_t* plan) {
-    if (!plan || M < 1 || M > 16 || check_weight_shape(N, K, G) != W4A16_OK) return W4A16_ERR_INVALID_ARG;
-    return w4a16::gemv_describe(M, N, K, G, plan) ? W4A16_OK : W4A16_ERR_UNSUPPORTED;
+w4a16_status w4a16_debug_gemv_plan(int64_t M, int64_t N, int64_t K, int G, int mode, int32_t* plan) {
+    if (!plan || mode < 0 || mode > 2 || M < 1 || M > 16 || check_weight_shape(N, K, G) != W4A16_OK)
+        return W4A16_ERR_INVALID_ARG;
+    return w4a16::gemv_describe(M, N, K, G, mode, plan) ? W4A16_OK : W4A16_ERR_UNSUPPORTED;
 }
 
 w4a16_status w4a16_debug_withhold_copy(int kernel) {

@@ -1229,19 +1229,38 @@ bool plan_one(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G, int sms,
 }
 
 // The plan of a launch.  The K split (one matrix of 4-bit codes with resident metadata, M >= 2;
-// ks_clusters: two-CTA clusters the device runs at once, 0 = never) is taken when x leaves the
-// plain kernel fewer warps than its launch bound, or no room at all, and the split has more.
+// ks_clusters: two-CTA clusters the device runs at once, 0 = never) is taken
+//   * when x leaves the plain kernel fewer warps than its launch bound, or no room at all,
+//     and the split has more;
+//   * with all warps either way, when it evens out the work: the busiest CTA's weight rows
+//     times the share of K it streams at least 10 % below the plain kernel's (5120 -> 5120 at
+//     M = 8: 320 tiles on 148 CTAs, 3 against 2.5 tiles' work, 15.6 -> 12.6 us), or on rows of
+//     8192 or more codes when the plain kernel has one ring unit per warp and the split two
+//     (13824 -> 5120 at M = 4: 20.2 -> 17.6 us).  Measured where neither holds (5120 -> 13824
+//     at M = 2..12, 8192 -> 28672 at M = 2 and 4, 5120 -> 5120 at M = 4), the split was 2-25 %
+//     slower.
 bool make_plan(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G, int sms, size_t smem_cap, Plan& pl,
                bool kq = false, bool w8 = false, int ks_clusters = 0) {
     const bool plain_ok = plan_one(M, Ns, nmat, K, G, sms, smem_cap, pl, kq, w8, 0);
     const bool ks_able = ks_clusters >= 1 && M >= 2 && nmat == 1 && !kq && !w8 && !meta_streamed(G);
-    if (!ks_able || (plain_ok && pl.p.nw >= cta_warps(pl.nb, G))) return plain_ok;
+    if (!ks_able) return plain_ok;
     Plan kp;
-    if (plan_one(M, Ns, nmat, K, G, sms, smem_cap, kp, kq, w8, ks_clusters) && (!plain_ok || kp.p.nw > pl.p.nw)) {
-        pl = kp;
-        return true;
+    if (!plan_one(M, Ns, nmat, K, G, sms, smem_cap, kp, kq, w8, ks_clusters)) return plain_ok;
+    bool take;
+    if (!plain_ok) {
+        take = true;
+    } else if (pl.p.nw < cta_warps(pl.nb, G)) {
+        take = kp.p.nw > pl.p.nw;
+    } else {
+        // the busiest CTA's work in weight rows x half rows of K: plain ceil(T / grid) tiles of R rows
+        // over all of K, split ceil(T' / clusters) tiles of 16 rows over half of it
+        const long long wp = (long long)((pl.p.total_tiles + pl.grid - 1) / pl.grid) * pl.p.R * 2;
+        const int ncl = kp.grid / 2;
+        const long long wk = (long long)((kp.p.total_tiles + ncl - 1) / ncl) * kp.p.R;
+        take = kp.p.nw >= pl.p.nw && (10 * wk <= 9 * wp || (K >= 8192 && pl.p.nst == 1 && kp.p.nst >= 2));
     }
-    return plain_ok;
+    if (take) pl = kp;
+    return plain_ok || take;
 }
 
 template <int NB, int G, int H, bool M1, int PT, int FMT, int NM, bool DUO = false, bool KS = false>
@@ -1427,7 +1446,7 @@ bool gemv_runs_full(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G) {
            pl.p.nw == cta_warps(pl.nb, G);
 }
 
-bool gemv_describe(int64_t M, int64_t N, int64_t K, int G, int32_t* plan) {
+bool gemv_describe(int64_t M, int64_t N, int64_t K, int G, int mode, int32_t* plan) {
     Plan pl;
     DeviceInfo di;
     int kcl = 74;
@@ -1438,12 +1457,15 @@ bool gemv_describe(int64_t M, int64_t N, int64_t K, int G, int32_t* plan) {
         kcl = ks_clusters(di, M, 1, false, false, G);
     }
     const int64_t Ns[1] = {N};
-    if (!make_plan(M, Ns, 1, K, G, di.sms, di.smem_optin, pl, false, false, kcl)) return false;
+    const bool ok = mode == 0 ? make_plan(M, Ns, 1, K, G, di.sms, di.smem_optin, pl, false, false, kcl)
+                              : plan_one(M, Ns, 1, K, G, di.sms, di.smem_optin, pl, false, false, mode == 2 ? kcl : 0);
+    if (!ok) return false;
     plan[0] = pl.p.P;
     plan[1] = pl.H;
     plan[2] = pl.p.nw;
     plan[3] = pl.p.ks;
     plan[4] = pl.grid;
+    plan[5] = pl.p.nst;
     return true;
 }
 

@@ -80,8 +80,9 @@ bool gemv_fits(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G, bool kq
 // Whether the 4-bit decode GEMV takes these matrices with all the warps of its instance (its
 // launch bound; fewer when x leaves too little shared memory for the weight rings).  Host only.
 bool gemv_runs_full(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G);
-// The plan of one 4-bit matrix: {P, H, warps, K split, CTAs}; false when the GEMV cannot take it.
-bool gemv_describe(int64_t M, int64_t N, int64_t K, int G, int32_t* plan);
+// The plan of one 4-bit matrix: {P, H, warps, K split, CTAs, ring units per warp}; mode 0 the
+// chosen plan, 1 the plain kernel's, 2 the K split's; false when that plan cannot take it.
+bool gemv_describe(int64_t M, int64_t N, int64_t K, int G, int mode, int32_t* plan);
 
 // y_i = x * W_hat_i^T for nmat (1..kMaxMat) matrices sharing x; matrix i has mats[i].n rows
 // (0: N).
