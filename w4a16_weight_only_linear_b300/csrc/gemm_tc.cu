@@ -390,6 +390,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     sm.last_flag = reinterpret_cast<volatile int*>(sm.tmem_slot + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // launched with programmatic stream serialisation: this grid touches no global memory
+    // before the previous grid on the stream has completed (the wait below), so the barriers,
+    // tensor memory and descriptor prefetches of the prologue overlap that grid's tail.  It
+    // does not let the next launch in early: blocks of a next grid resident beside this one,
+    // waiting, cost the contraction 2 % at M = 2048.
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
             tc::mbar_init(sm.x_full(i), 1);
@@ -416,6 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = *sm.tmem_slot;
+    tc::griddep_wait();
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -725,6 +731,11 @@ __global__ void __launch_bounds__(256) bf16_to_f16_kernel(const uint4* __restric
                                                           int64_t nvec, const float4* __restrict__ xsc,
                                                           int64_t kvec, int64_t kxvec, uint32_t* __restrict__ cnt,
                                                           int ncnt) {
+    // programmatic stream serialisation: the layer kernel may be scheduled at once (its prologue
+    // touches no global memory); this grid reads and writes nothing before the previous grid on
+    // the stream has completed
+    tc::griddep_launch_dependents();
+    tc::griddep_wait();
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     if (blockIdx.x == 0)   // the K-split arrival counters of the call's layer launches start at zero
         for (int i = threadIdx.x; i < ncnt; i += blockDim.x) cnt[i] = 0u;
@@ -775,8 +786,17 @@ cudaError_t launch_g(const CUtensorMap& tmx, const CUtensorMap& tmq, const GemmP
         while (have < (int)smem && !cached[dev].compare_exchange_weak(have, (int)smem)) {
         }
     }
-    gemm_kernel<G, W8><<<grid, kThreads, smem, stream>>>(tmx, tmq, p);
-    return cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<G, W8>, tmx, tmq, p);
 }
 
 // Converts x (BF16 [M, kx]) into the FP16 B operand x16 [M, K] and clears the
@@ -786,10 +806,18 @@ cudaError_t convert_x(const void* x, void* x16, int64_t M, int64_t K, int64_t kx
     const int64_t nvec = M * K / 8;
     int64_t blocks = (nvec + 255) / 256;
     if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
-    bf16_to_f16_kernel<<<(unsigned)blocks, 256, 0, stream>>>(static_cast<const uint4*>(x), static_cast<uint4*>(x16),
-                                                             nvec, reinterpret_cast<const float4*>(xsc), K / 8,
-                                                             kx / 8, cnt, ncnt);
-    return cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(256u);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, bf16_to_f16_kernel, static_cast<const uint4*>(x), static_cast<uint4*>(x16), nvec,
+                              reinterpret_cast<const float4*>(xsc), (int64_t)(K / 8), (int64_t)(kx / 8), cnt, ncnt);
 }
 
 // K split.  Narrow tiles (BN <= 64: small M, where a tile's time is its
