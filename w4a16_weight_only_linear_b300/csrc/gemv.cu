@@ -1375,8 +1375,11 @@ int ks_clusters(const DeviceInfo& di, int64_t M, int nmat, bool kq, bool w8, int
     static std::atomic<int> cached[kMaxDevices];
     const int v = cached[di.dev].load(std::memory_order_relaxed);
     if (v != 0) return v > 0 ? v : 0;
+    // one CTA per SM, as in every K-split plan; the attribute is set to the device's opt-in
+    // maximum, which is never below what a launch of this instance has set (launch_m only raises
+    // it to a plan's size), so a launch on another thread cannot be left short
     auto kern = gemv_kernel<2, 128, 1, false, 0, kFmt4, 1, false, true>;
-    const int smem = 200 * 1024;
+    const int smem = (int)di.smem_optin;
     int n = 0;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess) {
         cudaLaunchAttribute a[1];
