@@ -155,7 +155,7 @@ W4A16_API w4a16_status w4a16_dequant_f16(const uint32_t* qweight, const void* sc
  * bandwidth-bound decode GEMV (when x of M rows, or half of it on each SM of
  * a two-CTA cluster splitting K, fits the kernel's shared memory), and so
  * does M = 9..16 where the GEMV runs with all its warps and also takes M = 8
- * (measured on a 5120 -> 13824 layer at M = 16: 27.4 us against 29.2 us for
+ * (measured on a 5120 -> 13824 layer at M = 16: 24.9 us against 29.1 us for
  * the GEMM); anything else runs the tcgen05 tensor-core GEMM.  Decode is
  * weight-bandwidth bound and prefill compute bound (klaylearn glossary, FAQ
  * "Why is it especially useful for decode?"; multigrid.ai, section "Where it

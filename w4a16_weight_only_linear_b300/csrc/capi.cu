@@ -47,7 +47,7 @@ w4a16_status from_cuda(cudaError_t e) {
 // where it runs with all its warps (two MMA column blocks per tile; x of long rows split
 // along K over a two-CTA cluster) and also takes M = 8, so that a shape leaves the GEMV at
 // one batch size for good.  Measured on one B300 at M = 9-16: 5120 -> 13824 (G = 128)
-// 20.1-27.4 us against the tensor-core call's 29.2-32 us, 5120 -> 5120 at M = 16 17.5
+// 20.1-24.9 us against the tensor-core call's 29.1-32 us, 5120 -> 5120 at M = 16 17.5
 // against 21-26 us.  Where x crowds out the GEMV's weight rings it loses (43.8 against 35 us at
 // M = 16 before the K split), hence the full-warp condition.
 constexpr int64_t kGemvDispatchMaxM = 16;

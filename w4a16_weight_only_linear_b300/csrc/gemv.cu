@@ -155,6 +155,8 @@ struct GemvParams {
     int ks;                                // 1: K split across the two CTAs of a cluster (see gemv_kernel)
     int Ct, kc1;                           // KS: chunks per row; rank 0 streams chunks [0, kc1) of each
                                            // tile, rank 1 [kc1, Ct); C = kc1 sizes the staged x
+    int nslot;                             // KS: partial-sum slots per output (<= kSlots; the most warps
+                                           // sharing a tile), which sizes the partial buffer
 };
 
 struct Layout {
@@ -187,7 +189,7 @@ __host__ __device__ inline Layout make_layout(const GemvParams& p, int nb, int H
     L.mz = off;
     off += align_up((uint32_t)p.rows_cap * (uint32_t)p.ldz * 4u, 16);
     L.part = off;
-    off += align_up((uint32_t)p.rows_cap * (uint32_t)p.M * kSlots * 4u, 16);
+    off += align_up((uint32_t)p.rows_cap * (uint32_t)p.M * (uint32_t)(p.ks ? p.nslot : kSlots) * 4u, 16);
     L.red = off;
     off += (uint32_t)p.nw * 16u * (m1 ? (uint32_t)H : 8u * (uint32_t)nb) * 4u;
     L.bars = off;
@@ -347,6 +349,7 @@ __global__ void __launch_bounds__(DUO ? kDuoWarps * 32 : cta_warps(NB, G) * 32, 
     }
     const int Cw = KS ? (crank == 0 ? p.kc1 : p.Ct - p.kc1) : p.C;   // chunks per tile this CTA streams
     const int kc0 = KS ? (int)crank * p.kc1 : 0;                      // the first of them in the row
+    const int NSL = KS ? p.nslot : kSlots;                            // partial-sum slots per output
     const int tile0 = (int)((cid * (uint32_t)T) / ncl);        // T * grid < 2^32 (host check)
     const int tile1 = (int)(((cid + 1) * (uint32_t)T) / ncl);
     const int tc_ = tile1 - tile0;
@@ -641,7 +644,7 @@ __global__ void __launch_bounds__(DUO ? kDuoWarps * 32 : cta_warps(NB, G) * 32, 
         for (uint32_t i = tid; i < (M1 ? 8u * (uint32_t)P * 64u : 16u) / 16u; i += kThreads)
             reinterpret_cast<uint4*>(base + L.zero)[i] = make_uint4(0u, 0u, 0u, 0u);
         float* part = reinterpret_cast<float*>(base + L.part);
-        for (int i = tid; i < p.rows_cap * p.M * kSlots; i += kThreads) part[i] = 0.0f;
+        for (int i = tid; i < p.rows_cap * p.M * NSL; i += kThreads) part[i] = 0.0f;
 
         // the scale/zero rows have landed: lane 0 of each warp starts its ring of units and keeps
         // it filled from here on
@@ -945,7 +948,7 @@ __global__ void __launch_bounds__(DUO ? kDuoWarps * 32 : cta_warps(NB, G) * 32, 
                             for (int q = 0; q < P; ++q)
 #pragma unroll
                                 for (int hh = 0; hh < H; ++hh) sum += red[(lane * P + q) * H + hh];
-                            part[(tl * R + lane) * kSlots + slotp] = sum;
+                            part[(tl * R + lane) * NSL + slotp] = sum;
                         }
                         __syncwarp();
                     } else {
@@ -967,7 +970,7 @@ __global__ void __launch_bounds__(DUO ? kDuoWarps * 32 : cta_warps(NB, G) * 32, 
 #pragma unroll
                                 for (int hh = 0; hh < H; ++hh)
                                     sum += red[(rho * P + q) * 8 * NB + (q * H + hh) * p.M + m];
-                            part[((tl * R + rho) * p.M + m) * kSlots + slotp] = sum;
+                            part[((tl * R + rho) * p.M + m) * NSL + slotp] = sum;
                         }
                         __syncwarp();
                     }
@@ -1030,12 +1033,16 @@ __global__ void __launch_bounds__(DUO ? kDuoWarps * 32 : cta_warps(NB, G) * 32, 
             if (row >= p.n[mat]) continue;
             float sum = 0.0f;
             if constexpr (KS) {
-                const uint32_t a = tc::smem_u32(part + i * kSlots);
+                const uint32_t a = tc::smem_u32(part + i * NSL);
 #pragma unroll
                 for (uint32_t rk = 0; rk < 2; ++rk) {
                     const uint32_t ra = cluster_map(a, rk);
+                    float v[kSlots];                     // the slots' loads in flight together
 #pragma unroll
-                    for (int q = 0; q < kSlots; ++q) sum += ld_cluster_f32(ra + 4u * (uint32_t)q);
+                    for (int q = 0; q < kSlots; ++q) v[q] = q < NSL ? ld_cluster_f32(ra + 4u * (uint32_t)q) : 0.0f;
+#pragma unroll
+                    for (int q = 0; q < kSlots; ++q)
+                        if (q < NSL) sum += v[q];
                 }
             } else {
 #pragma unroll
@@ -1178,6 +1185,7 @@ bool plan_one(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G, int sms,
     auto set_warps = [&](int nw, int tn, int cn) {
         p.nw = nw;
         p.warps = 1;
+        p.nslot = kSlots;
         for (int w = nw; w >= 1; --w) {
             const long long chunks = (long long)tn * cn;
             const long long per = chunks / w;
@@ -1185,6 +1193,7 @@ bool plan_one(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G, int sms,
             const long long span = (p.C + per - 1) / per + 1;
             if (span <= kSlots) {
                 p.warps = w;
+                p.nslot = (int)span;       // the most warps whose runs meet one tile
                 break;
             }
         }
