@@ -107,7 +107,9 @@ def test_gemv_long_rows_with_streamed_scales(M, N, K):
 # several CTA pairs, ragged N.
 KSPLIT_SHAPES = [(16, 520, 8192, 128), (9, 136, 12288, 64), (12, 1032, 8192, 256), (11, 392, 10560, 64),
                  (16, 264, 6400, 128), (8, 264, 13824, 128), (3, 136, 28672, 128), (2, 72, 49152, 64),
-                 (4, 392, 20480, 128), (6, 264, 13824, 256), (5, 520, 16384, 64), (7, 136, 16384, 64)]
+                 (4, 392, 20480, 128), (6, 264, 13824, 256), (5, 520, 16384, 64), (7, 136, 16384, 64),
+                 # groups of 32: the scales stream with the units, each CTA's from its own first chunk
+                 (12, 264, 8192, 32), (4, 136, 28672, 32)]
 
 
 def _gemv_plan(M, N, K, G):

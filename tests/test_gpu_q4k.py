@@ -84,6 +84,18 @@ def test_q4k_empty_and_status():
     assert w4.w4a16_device_status() == 0
 
 
+@pytest.mark.parametrize("M,N,K", [(3, 264, 28672), (5, 136, 16384), (2, 72, 49152)])
+def test_q4k_linear_k_split(M, N, K):
+    """Long rows: x of M rows leaves the kernel too little room, so two CTAs of a cluster each
+    stream half of every row's super-blocks (records included) and add their partial sums."""
+    w = _weights(N, K, 7 * N + K)
+    q, meta = oracle.q4k_pack(wl.bits_u16(w))
+    x = wl.activations_bf16(M, K, N + M + K)
+    y = w4.q4k_linear(x.cuda(), *_dev(q, meta))
+    torch.cuda.synchronize()
+    assert_close(y, oracle.q4k_linear(wl.bits_u16(x), q, meta, N, K), f"q4k k-split M={M} N={N} K={K}")
+
+
 @pytest.mark.parametrize("j", [0, 1])
 @pytest.mark.parametrize("M", [1, 3])
 def test_q4k_workload(j, M):

@@ -1150,7 +1150,7 @@ bool plan_one(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G, int sms,
     p.ks = ks_ncl > 0 ? 1 : 0;
     p.Ct = p.C;
     p.kc1 = p.ks ? (p.C + 1) / 2 : p.C;         // K split: rank 0 streams chunks [0, kc1), rank 1 the rest
-    if (p.ks && (p.C < 2 || nmat != 1 || kq || w8 || meta_streamed(G))) return false;
+    if (p.ks && (p.C < 2 || nmat != 1 || w8)) return false;
     p.C = p.kc1;                                // chunks this CTA stages x for (the K split: rank 0's)
     p.Ks = p.C * 256;                           // equals K / P whenever P > 1 (and no K split)
     p.ng = (int)(K / G);
@@ -1158,7 +1158,7 @@ bool plan_one(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G, int sms,
     p.lds = kq ? (int)(K / 256 * 8) : (int)scales_ld(K, G);
     p.mstream = meta_streamed(G) ? 1 : 0;
     // streamed metadata needs each segment's groups (records) to be whole chunks laid out back to back
-    if (p.mstream && (p.lds % p.P != 0 || p.lds / p.P != p.C * (256 / G) || (p.lds / p.P) % 8 != 0)) return false;
+    if (p.mstream && (p.lds % p.P != 0 || p.lds / p.P != p.Ct * (256 / G) || (p.lds / p.P) % 8 != 0)) return false;
     p.ldz = kq ? 0 : w8 ? (int)zeros8_ld(K / 2, G / 2) : (int)zeros_ld(K, G);
     int64_t t = 0;
     for (int i = 0; i < kMaxMat; ++i) {
@@ -1251,7 +1251,7 @@ bool plan_one(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G, int sms,
 bool make_plan(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G, int sms, size_t smem_cap, Plan& pl,
                bool kq = false, bool w8 = false, int ks_clusters = 0) {
     const bool plain_ok = plan_one(M, Ns, nmat, K, G, sms, smem_cap, pl, kq, w8, 0);
-    const bool ks_able = ks_clusters >= 1 && M >= 2 && nmat == 1 && !kq && !w8 && !meta_streamed(G);
+    const bool ks_able = ks_clusters >= 1 && M >= 2 && nmat == 1 && !w8;
     if (!ks_able) return plain_ok;
     Plan kp;
     if (!plan_one(M, Ns, nmat, K, G, sms, smem_cap, kp, kq, w8, ks_clusters)) return plain_ok;
@@ -1355,10 +1355,19 @@ cudaError_t launch_nb(const CUtensorMap* tm, const Plan& pl, int dev, cudaStream
     }
 }
 
-// The K split (one matrix, 4-bit codes, G >= 64; one segment per row, H group parities).
-cudaError_t launch_ks(const CUtensorMap* tm, const Plan& pl, int dev, cudaStream_t stream) {
+// The K split (one matrix; 4-bit codes or super-blocks; one segment per row, H group parities).
+cudaError_t launch_ks(const CUtensorMap* tm, const Plan& pl, int dev, cudaStream_t stream, bool kq) {
+    if (kq) {                                  // make_plan: M <= 8, one column block, G = 32
+        switch (pl.H) {
+            case 1: return launch_m<1, 32, 1, false, 0, kFmtQ4K, 1, false, true>(tm, pl, dev, stream);
+            case 2: return launch_m<1, 32, 2, false, 0, kFmtQ4K, 1, false, true>(tm, pl, dev, stream);
+            case 4: return launch_m<1, 32, 4, false, 0, kFmtQ4K, 1, false, true>(tm, pl, dev, stream);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     if (pl.nb == 2) {
         switch (pl.p.G) {
+            case 32: return launch_m<2, 32, 1, false, 0, kFmt4, 1, false, true>(tm, pl, dev, stream);
             case 64: return launch_m<2, 64, 1, false, 0, kFmt4, 1, false, true>(tm, pl, dev, stream);
             case 128: return launch_m<2, 128, 1, false, 0, kFmt4, 1, false, true>(tm, pl, dev, stream);
             case 256: return launch_m<2, 256, 1, false, 0, kFmt4, 1, false, true>(tm, pl, dev, stream);
@@ -1366,6 +1375,9 @@ cudaError_t launch_ks(const CUtensorMap* tm, const Plan& pl, int dev, cudaStream
         }
     }
     switch (pl.p.G * 8 + pl.H) {
+        case 32 * 8 + 1: return launch_m<1, 32, 1, false, 0, kFmt4, 1, false, true>(tm, pl, dev, stream);
+        case 32 * 8 + 2: return launch_m<1, 32, 2, false, 0, kFmt4, 1, false, true>(tm, pl, dev, stream);
+        case 32 * 8 + 4: return launch_m<1, 32, 4, false, 0, kFmt4, 1, false, true>(tm, pl, dev, stream);
         case 64 * 8 + 1: return launch_m<1, 64, 1, false, 0, kFmt4, 1, false, true>(tm, pl, dev, stream);
         case 64 * 8 + 2: return launch_m<1, 64, 2, false, 0, kFmt4, 1, false, true>(tm, pl, dev, stream);
         case 64 * 8 + 4: return launch_m<1, 64, 4, false, 0, kFmt4, 1, false, true>(tm, pl, dev, stream);
@@ -1380,7 +1392,7 @@ cudaError_t launch_ks(const CUtensorMap* tm, const Plan& pl, int dev, cudaStream
 // SMs pair up within their GPCs, so this can be below SMs / 2); asked once per device, 0
 // when the device cannot say.
 int ks_clusters(const DeviceInfo& di, int64_t M, int nmat, bool kq, bool w8, int G) {
-    if (M < 2 || nmat != 1 || kq || w8 || G < 64) return 0;       // plans that never split
+    if (M < 2 || nmat != 1 || w8) return 0;                      // plans that never split
     static std::atomic<int> cached[kMaxDevices];
     const int v = cached[di.dev].load(std::memory_order_relaxed);
     if (v != 0) return v > 0 ? v : 0;
@@ -1454,8 +1466,10 @@ bool gemv_runs_full(int64_t M, const int64_t* Ns, int nmat, int64_t K, int G) {
     } else {
         kcl = ks_clusters(di, M, nmat, false, false, G);
     }
+    // groups of 32 split along K run behind the tensor cores at M = 16 (5120 -> 13824: 30.5
+    // against 29.1 us), so only their plain plans count there
     return make_plan(M, Ns, nmat, K, G, di.sms, di.smem_optin, pl, false, false, kcl) &&
-           pl.p.nw == cta_warps(pl.nb, G);
+           pl.p.nw == cta_warps(pl.nb, G) && !(pl.p.ks && G == 32 && M > 8);
 }
 
 bool gemv_describe(int64_t M, int64_t N, int64_t K, int G, int mode, int32_t* plan) {
@@ -1536,11 +1550,11 @@ cudaError_t launch_gemv(const void* x, const GemvMat* mats, int nmat, int64_t M,
     if (p.duo)                                                // make_plan: M = 1, G = 128, P = 4, H = 2
         return nmat == 1 ? launch_m<1, 128, 2, true, 4, kFmt4, 1, true>(tm, pl, di.dev, stream)
                          : launch_m<1, 128, 2, true, 4, kFmt4, 4, true>(tm, pl, di.dev, stream);
+    if (p.ks) return launch_ks(tm, pl, di.dev, stream, kq);  // make_plan: one matrix, M >= 2
     if (kq)                                                   // make_plan: M <= 8, one column block
         return nmat == 1 ? launch_h<1, 32, kFmtQ4K, 1>(tm, pl, di.dev, stream)
                          : launch_h<1, 32, kFmtQ4K, 2>(tm, pl, di.dev, stream);
     if (w8) return launch_w8(tm, pl, di.dev, stream);
-    if (p.ks) return launch_ks(tm, pl, di.dev, stream);      // make_plan: one matrix, M >= 2, G >= 64
     if (nmat > 2)
         return pl.nb == 1 ? launch_nb<1, 4>(tm, pl, di.dev, stream) : launch_nb<2, 4>(tm, pl, di.dev, stream);
     if (nmat == 2)
