@@ -39,10 +39,12 @@
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is
  *     enqueued asynchronously; results are valid once the stream reaches the
  *     point of the call.  Calls on distinct streams may run concurrently.
- *   - The decode kernel is launched with programmatic stream serialisation:
- *     it may begin (initialise its barriers) while the previous kernel on the
- *     stream finishes, but it reads and writes no global memory before that
- *     kernel has completed, so stream order keeps its usual meaning.
+ *   - The decode kernel, the tensor-core kernel and its x conversion are
+ *     launched with programmatic stream serialisation: each may begin
+ *     (initialise its barriers, allocate tensor memory) while the previous
+ *     kernel on the stream finishes, but it reads and writes no global memory
+ *     before that kernel has completed, so stream order keeps its usual
+ *     meaning.  For long rows the decode kernel runs as clusters of two CTAs.
  *   - Scratch memory: the tensor-core path takes each call's scratch (the
  *     FP16 copy of x; FP32 partial sums when tiles are split along K: a
  *     narrow layer's tiles, or the last, partial wave of wider tiles)
